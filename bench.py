@@ -1,0 +1,435 @@
+"""Benchmark of the sequence-parallel DiT attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input
+already resident in HBM: Ulysses pack -> simulated all-to-all -> unpack ->
+attention partials -> merge (when R > 1) -> inverse pack / all-to-all /
+unpack -> CFG combine.  The default workload is the FLUX-1024-like one
+(B=1, S=4608, H=24, D=128, U=4, R=1; CFG on [2,4608,3072] bf16, g=3.5).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--U U]
+    python bench.py --impl reference ...     # the fp64 CPU oracle, timed
+
+Prints one JSON line (rank 0).  `value` is attention TFLOP/s over the whole
+step (algorithmic 4*B*H*S^2*D flops / step time, summed over ranks);
+`e2e` is the same through the public API with pinned host buffers and the
+host<->device copies inside the timed region.  L2 is flushed (a 256 MiB
+write) before every timed step; only the step itself is inside the events.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "DiT attn TFLOP/s & % bf16 TC peak (S=4608,H=24,D=128); pack/CFG GB/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+ATTN_SRC = os.path.join(ROOT, "sequence_attention_gb300", "csrc", "attn_tc.cu")
+TRAFFIC_NOTE = os.path.join(ROOT, "profiles", "attn_tc_flux1024.md")
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def init_dist(backend: str):
+    import torch.distributed as dist
+    rank, _, ws = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return dist
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- peaks, clocks
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_per_launch(kernel_src: str, note: str):
+    """dram bytes per launch recorded by an ncu capture, if the kernel source
+    has not changed since (the note stores the source's sha256)."""
+    try:
+        text = open(note).read()
+        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram_bytes_per_launch_full:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_b) or m_sha.group(1) != sha:
+        return None
+    return float(m_b.group(1))
+
+
+# ---------------------------------------------------------------- workload
+def workload_config(name: str, U: int):
+    import synth
+    w = synth.WORKLOADS[name]
+    if U is None:
+        U = max(w.U)
+    return w, U
+
+
+def cpu_oracle_rate(w, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle's attention on a bounded sample of query rows
+    (all heads, full key sequence); returns (TFLOP/s, seconds, rows, cores)."""
+    import numpy as np
+    import torch
+    from oracle import attention as oatt
+    q, k, v = w.qkv()
+    rng = np.random.default_rng(seed)
+    rows = rng.permutation(w.S)
+    chunk = max(16, min(256, w.S))
+    done = 0
+    flops = 0.0
+    t0 = time.perf_counter()
+    kf = [k[b].to(torch.float64).numpy() for b in range(w.B)]
+    vf = [v[b].to(torch.float64).numpy() for b in range(w.B)]
+    while done < w.S and (time.perf_counter() - t0) < budget_s:
+        sel = np.sort(rows[done:done + chunk])
+        for b in range(w.B):
+            qb = q[b, torch.from_numpy(sel)].to(torch.float64).numpy()
+            oatt.attention(qb[None], kf[b][None], vf[b][None])
+        flops += 4.0 * w.B * w.H * len(sel) * w.S * w.D
+        done += len(sel)
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, done, blas_threads()
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    rank, local_rank, ws = dist_env()
+    torch.cuda.set_device(local_rank)
+    if ws > 1:
+        init_dist("nccl")
+    dev = torch.device("cuda", local_rank)
+    import synth
+    import sequence_attention_gb300 as sa
+    from sequence_attention_gb300.usp import UspPlan
+
+    w, U = workload_config(args.workload, args.U)
+    q, k, v = (t.to(dev) for t in w.qkv())
+    pred = w.cfg_pair().to(dev)
+    out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev)
+    cfg_out = torch.empty(w.cfg_shape[1:], dtype=synth.torch_dtype(w.cfg_out), device=dev)
+    plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev))
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    names = plan.steps() + ["cfg"]
+    n_cfg_kernels = 1 if (pred.numel() // 2) % 8 == 0 else 2
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        plan.layout_in(q, k, v)
+        mark(1)
+        plan.attend()
+        mark(2)
+        plan.layout_out(out)
+        mark(3)
+        sa.dit_cfg_combine(pred, cfg_out, w.g)
+        mark(4)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] or 0) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank
+
+    def timed():
+        barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(gpu_index) as cs:
+            for i in range(K):
+                flush.zero_()
+                step(evs[i])
+            torch.cuda.synchronize(dev)
+        barrier()
+        return cs.summary()
+
+    clocks = timed()
+    if any(r in clocks["reasons"] for r in BAD_REASONS):
+        clocks = timed()        # rejected once: measure again
+        clocks["remeasured"] = True
+
+    seg = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(4)]   # ms per segment
+    step_ms = [sum(x) for x in zip(*seg)]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, dev)
+    attn_ms = statistics.mean(seg[1])
+    flops = w.attn_flops
+    value = ws * flops / (ms_max * 1e-3) / 1e12
+
+    # bytes of the bandwidth steps (real elements read + written)
+    L = plan.L
+    eb = 2 if w.dtype != "f32" else 4
+    qkv_bytes = 3 * w.B * w.S * w.H * w.D * eb
+    wire3 = 3 * w.B * w.S * L.Hp * w.D * eb
+    layout_in_bytes = (qkv_bytes + wire3) + 2 * wire3 + (wire3 + wire3)
+    o_bytes = w.B * w.S * w.H * w.D * 2
+    wire1 = w.B * w.S * L.Hp * w.D * 2
+    layout_out_bytes = (o_bytes + wire1) + 2 * wire1 + (wire1 + o_bytes)
+    cfg_n = pred.numel() // 2
+    cfg_bytes = cfg_n * (2 * pred.element_size() + cfg_out.element_size())
+
+    peaks, peak_src = load_peaks()
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    traffic = traffic_per_launch(ATTN_SRC, TRAFFIC_NOTE)
+
+    # end to end through the public API: pinned host inputs in, results out
+    e2e = run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args)
+
+    res = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V, N(0,1) CFG branches)",
+        "config": {"workload": f"{w.name}-like: B={w.B} S={w.S} H={w.H} D={w.D}, Ulysses U={U}, "
+                               f"ring R={w.R}; CFG [2,{','.join(map(str, w.cfg_shape[1:]))}] "
+                               f"{w.cfg_in}->{w.cfg_out} g={w.g}",
+                   "B": w.B, "S": w.S, "H": w.H, "D": w.D, "U": U, "R": w.R,
+                   "parallelism": f"virtual ranks U{U}xR{w.R} on one GPU; replicas across GPUs",
+                   "l2": "flushed before every timed step (256 MiB write, outside the events)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": traffic, "kernel": "attn_tc_kernel<128,false> (dit_attn_partial)",
+                     "peak_source": f"{peak_src} bf16 burst",
+                     "frac_of_sustained": round(achieved / peaks.get("bf16_tflops_sustained",
+                                                                      peaks["bf16_tflops"]), 4)},
+        "kernels": {
+            "layout_in_ms": round(statistics.mean(seg[0]), 4),
+            "layout_in_GBs": round(layout_in_bytes / (statistics.mean(seg[0]) * 1e-3) / 1e9, 1),
+            "attention_ms": round(attn_ms, 4), "attention_TFLOPs": round(achieved, 1),
+            "layout_out_ms": round(statistics.mean(seg[2]), 4),
+            "layout_out_GBs": round(layout_out_bytes / (statistics.mean(seg[2]) * 1e-3) / 1e9, 1),
+            "cfg_ms": round(statistics.mean(seg[3]), 4),
+            "cfg_GBs": round(cfg_bytes / (statistics.mean(seg[3]) * 1e-3) / 1e9, 1),
+            "hbm_peak_GBs": peaks.get("hbm_gbs"),
+        },
+        "e2e": e2e,
+        "gpu_launches": K * (len(names) - 1 + n_cfg_kernels),
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, secs, rows, cores = cpu_oracle_rate(w, args.cpu_budget)
+        res["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": cores,
+                               "kind": "oracle",
+                               "sample": f"fp64 numpy oracle attention of {rows} random query rows x "
+                                         f"{w.H} heads x B={w.B} against all {w.S} keys "
+                                         f"({secs:.1f} s on host cores)"}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args):
+    import torch
+    import sequence_attention_gb300 as sa
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    hp = pred.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hc = torch.empty(cfg_out.shape, dtype=cfg_out.dtype).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        pred.copy_(hp, non_blocking=True)
+        plan.run(q, k, v, out)
+        sa.dit_cfg_combine(pred, cfg_out, w.g)
+        ho.copy_(out, non_blocking=True)
+        hc.copy_(cfg_out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    n = max(3, min(args.steps, 20))
+    barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(n):
+        e2e_step()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(s.elapsed_time(e) / n, dev)
+    _, _, ws = dist_env()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hp))
+    d2h = ho.numel() * ho.element_size() + hc.numel() * hc.element_size()
+    return {"value": round(ws * w.attn_flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, _, ws = dist_env()
+    if rank != 0:
+        return
+    w, U = workload_config(args.workload, args.U)
+    per_step = max(1.0, args.cpu_budget / max(args.steps + args.warmup, 1))
+    for _ in range(max(args.warmup, 3) if args.warmup else 0):
+        cpu_oracle_rate(w, per_step / 4, seed=1)
+    rates, secs, rows_tot, cores = [], 0.0, 0, 1
+    for i in range(args.steps):
+        r, s, rows, cores = cpu_oracle_rate(w, per_step, seed=100 + i)
+        rates.append(r)
+        secs += s
+        rows_tot += rows
+    value = statistics.mean(rates)
+    ms = 4.0 * w.B * w.H * w.S * w.S * w.D / (value * 1e12) * 1e3
+    sample = (f"each step: fp64 numpy oracle attention of ~{rows_tot // max(args.steps, 1)} random "
+              f"query rows x {w.H} heads x B={w.B} against all {w.S} keys, about {per_step:.1f} s")
+    res = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
+           "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": f"{w.name}-like: B={w.B} S={w.S} H={w.H} D={w.D}, Ulysses U={U}, "
+                                  f"ring R={w.R}", "B": w.B, "S": w.S, "H": w.H, "D": w.D,
+                      "U": U, "R": w.R},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="flux1024")
+    ap.add_argument("--U", type=int, default=None)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, dest="cpu_budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,277 @@
+/*
+ * ditsp.h -- C ABI of the GB300 sequence-parallel DiT attention hot path.
+ *
+ * One shared library, libditsp.so, exposes the steps of sequence-parallel
+ * attention for diffusion transformers as plain C calls on device pointers:
+ *
+ *   dit_sp_layout_init / dit_sp_a2a_counts   rank partition bookkeeping
+ *   dit_ulysses_pack / dit_a2a_sim / dit_ulysses_unpack
+ *                                            the Ulysses all-to-all, both ways
+ *   dit_attn_partial                         attention of query blocks against
+ *                                            key/value chunks, with log-sum-exp
+ *   dit_attn_merge_lse                       exact merge of the partials
+ *   dit_attention                            single-shot attention
+ *   dit_cfg_combine                          classifier-free guidance combine
+ *
+ * The "ranks" of Ulysses (degree U) and ring (degree R) parallelism are
+ * partitions of buffers in one GPU's memory.  Virtual rank id = r*U + u:
+ * ring blocks outer, Ulysses ranks inner, so ranks in id order cover the
+ * sequence in order (SGLang Diffusion "Parallelism Overview": Ulysses groups
+ * on contiguous ranks, ring groups strided).
+ *
+ * Conventions shared by every call
+ *  - Ownership: the caller allocates and owns every buffer.  The library
+ *    allocates no device or host memory in any call.
+ *  - Asynchrony: every call that takes `stream` (a cudaStream_t passed as
+ *    void*, NULL = legacy default stream) validates its arguments on the
+ *    host, enqueues its kernels on that stream and returns without waiting.
+ *  - Errors: argument problems are reported synchronously as
+ *    DIT_ERR_INVALID_ARG / DIT_ERR_UNSUPPORTED before anything is launched;
+ *    a failed launch returns DIT_ERR_CUDA.  dit_last_error() then holds a
+ *    one-line description (per calling thread).  Conditions found on the
+ *    device (a bounded wait that ran out, a value out of a target type's
+ *    range) are written to a caller-supplied device int `d_status`, or to
+ *    the library's own device word when d_status is NULL; read the latter
+ *    with dit_device_status().  Nothing traps and nothing crosses the ABI
+ *    as an exception.
+ *  - Threads: calls hold no global mutable host state except the
+ *    thread-local error string and a once-initialised driver entry point.
+ *  - Element types: DIT_F32, DIT_BF16, DIT_F16.  Narrowing conversions round
+ *    to nearest even; widening is exact.
+ *  - Pointers passed to kernels must be 16-byte aligned and every tensor's
+ *    innermost (head-dim) extent in bytes a multiple of 16.
+ */
+#ifndef DITSP_H
+#define DITSP_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DIT_API __attribute__((visibility("default")))
+#else
+#define DIT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DIT_OK = 0,
+    DIT_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment */
+    DIT_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head dim) */
+    DIT_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    DIT_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out */
+    DIT_ERR_RANGE = 5          /* a value overflowed the target type */
+} dit_status;
+
+typedef enum { DIT_F32 = 0, DIT_BF16 = 1, DIT_F16 = 2 } dit_dtype;
+
+/* Direction of a Ulysses exchange (edge-dit.cpp "Parallel execution",
+ * SPAllToAll4DLayout: kSeqToHead / kHeadToSeq). */
+typedef enum { DIT_SEQ_TO_HEAD = 0, DIT_HEAD_TO_SEQ = 1 } dit_a2a_dir;
+
+#define DIT_MAX_U 64
+#define DIT_MAX_R 8
+#define DIT_MAX_RANKS 64
+
+/*
+ * Rank partition of one sequence-parallel attention (edge-dit.cpp
+ * "Parallel execution", SPSequenceSplit and SPAllToAll4DLayout; cache-dit
+ * "Context Parallelism", UAA and Any Head Num).
+ *
+ * The sequence of S rows is split over R ring blocks and each ring block
+ * over U Ulysses ranks with the balanced rule: of n parts the first S mod n
+ * get one extra row (lengths differ by at most one; no sequence padding).
+ * Heads are padded from H to Hp = ceil(H/U)*U; Ulysses rank v owns global
+ * heads [v*Hl, (v+1)*Hl), Hl = Hp/U, and heads >= H are zero.
+ */
+typedef struct {
+    int B, S, H, D, U, R;
+    int Hp, Hl;
+    int S_cap;                        /* max ring-block length */
+    int ring_len[DIT_MAX_R];          /* rows of ring block r */
+    int ring_off[DIT_MAX_R];          /* first global row of ring block r */
+    int rank_len[DIT_MAX_RANKS];      /* rows of virtual rank r*U+u */
+    int rank_off[DIT_MAX_RANKS];      /* first global row of that rank */
+} dit_sp_layout;
+
+/*
+ * A strided view of a [blocks][B][rows][heads][D] tensor; d is contiguous.
+ * Strides are in elements.  stride_q steps between query (ring) blocks,
+ * stride_kv between key/value blocks (for partial outputs: the partial of
+ * query block r against key/value block j is at r*stride_q + j*stride_kv).
+ * A stride that a call does not use is ignored.
+ */
+typedef struct {
+    void* ptr;
+    int64_t stride_q, stride_kv, stride_b, stride_s, stride_h;
+} dit_view;
+
+/* A strided view of float32 log-sum-exp rows [blocks][B][heads][rows];
+ * rows are contiguous. */
+typedef struct {
+    float* ptr;
+    int64_t stride_q, stride_kv, stride_b, stride_h;
+} dit_lse_view;
+
+DIT_API const char* dit_status_string(dit_status s);
+
+/* One-line description of the last error returned on this thread. */
+DIT_API const char* dit_last_error(void);
+
+/* Reads (and if reset != 0 clears) the library's own device status word,
+ * used by calls whose d_status is NULL.  Synchronises the device. */
+DIT_API dit_status dit_device_status(int* out_code, int reset);
+
+/*
+ * dit_sp_layout_init: fill *out for a [B, S, H, D] attention split over
+ * U Ulysses ranks inside R ring blocks.  Host only, no device work.
+ * Requires B,H,D >= 1, S >= 0, 1 <= U <= DIT_MAX_U, 1 <= R <= DIT_MAX_R,
+ * U*R <= DIT_MAX_RANKS, and every size product within int64.
+ */
+DIT_API dit_status dit_sp_layout_init(int B, int S, int H, int D, int U, int R,
+                              dit_sp_layout* out);
+
+/*
+ * dit_sp_a2a_counts: the alltoallv argument set of virtual rank `rank` for
+ * one exchange carrying `nplanes` planes (3 = packed Q,K,V; 1 = O), in
+ * elements, indexed by the peer's Ulysses index within the rank's ring
+ * group.  Send blocks are peer-major; the block rank u sends rank v is
+ * [nplanes][B][rows][Hl][D] with rows = rank_len of u (seq-to-head) or of
+ * v (head-to-seq).  Each output array has room for U entries.  Host only.
+ */
+DIT_API dit_status dit_sp_a2a_counts(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
+                             int rank, int64_t* send_counts, int64_t* send_displs,
+                             int64_t* recv_counts, int64_t* recv_displs);
+
+/*
+ * Buffer shapes used by the Ulysses calls (all dense, row-major):
+ *   seq layout   [B][S][H][D]              rank (r,u) owns rows
+ *                                          [rank_off, rank_off + rank_len)
+ *   head layout  [R][B][S_cap][Hp][D]      rank (r,v) owns ring block r,
+ *                                          rows [0, ring_len[r]), heads
+ *                                          [v*Hl, (v+1)*Hl); rows past
+ *                                          ring_len[r] are never touched
+ *   wire         all ranks' send (or receive) buffers end to end in rank-id
+ *                order; total nplanes*B*S*Hp*D elements
+ *
+ * dit_ulysses_pack (edge-dit.cpp "Parallel execution": packed QKV send path
+ * and head-to-sequence path).
+ *   DIT_SEQ_TO_HEAD: src[p] (p < nplanes) are seq-layout planes; every rank
+ *     writes, for each destination v in order, its rows of heads
+ *     [v*Hl, (v+1)*Hl) of every plane; heads >= H are written as zero.
+ *   DIT_HEAD_TO_SEQ: src[0] is a head-layout tensor (nplanes must be 1);
+ *     rank (r,v) writes, for each destination u, u's rows of its heads;
+ *     heads >= H are written as zero.
+ *   Values are converted src_dt -> wire_dt.
+ *
+ * dit_a2a_sim: the exchange itself: every rank's receive buffer is the
+ *   concatenation, over source ranks in order, of the blocks they addressed
+ *   to it.  A permutation copy in one memory; no arithmetic.
+ *
+ * dit_ulysses_unpack:
+ *   DIT_SEQ_TO_HEAD: dst[p] are head-layout planes, converted wire_dt ->
+ *     dst_dt[p] (e.g. Q,K bf16 and V f16).  If d_range_flag is not NULL,
+ *     a value that overflows dst_dt[p] sets *d_range_flag = DIT_ERR_RANGE
+ *     (the converted value is the rounded infinity).
+ *   DIT_HEAD_TO_SEQ: dst[0] is a seq-layout tensor [B][S][H][D] in dst_dt[0];
+ *     padded heads are dropped.
+ *
+ * The three calls require D*sizeof(type) to be a multiple of 16 bytes for
+ * every type involved and 16-byte aligned pointers.  send/recv must not
+ * overlap any other buffer of the same call.
+ */
+DIT_API dit_status dit_ulysses_pack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
+                            const void* const* src, dit_dtype src_dt,
+                            void* send, dit_dtype wire_dt, void* stream);
+
+DIT_API dit_status dit_a2a_sim(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
+                       const void* send, void* recv, dit_dtype wire_dt, void* stream);
+
+DIT_API dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
+                              const void* recv, dit_dtype wire_dt,
+                              void* const* dst, const dit_dtype* dst_dt,
+                              int* d_range_flag, void* stream);
+
+/*
+ * dit_attn_partial: for every query block r < n_q and key/value block
+ * j < n_kv, the attention of Q_r against the first kv_len[j] keys of
+ * (K_j, V_j) (SGLang Diffusion "Parallelism Overview", Constraints: the
+ * ring's per-hop merge needs each call's softmax log-sum-exp; diffusers
+ * "Distributed inference", Ring Anything: padded K/V trimmed to the real
+ * length).  For each batch b, head h < H and row i < q_len[r]:
+ *   s_t   = scale * <q_i, k_t>              for keys t < kv_len[j]
+ *   lse_i = ln sum_t exp(s_t)
+ *   o_i   = sum_t exp(s_t - lse_i) * v_t    (normalised by this chunk only)
+ * Keys at or past kv_len[j] are excluded from the softmax, whatever their
+ * contents.  A chunk with kv_len[j] == 0 gives o = 0 and lse = -inf.
+ *
+ *   q        rows of block r at q.ptr + r*q.stride_q, [B][q_len[r]][H][D]
+ *   k, v     rows of block j at ptr + j*stride_kv,    [B][kv_len[j]][H][D]
+ *   o        partial (r, j) at o.ptr + r*o.stride_q + j*o.stride_kv
+ *   lse      partial (r, j) row i of (b, h) at
+ *            r*stride_q + j*stride_kv + b*stride_b + h*stride_h + i;
+ *            lse.ptr may be NULL (not written)
+ *   q_len, kv_len: host arrays; n_q, n_kv <= DIT_MAX_R.
+ *
+ * Supported: (qk_dt, v_dt) = (F32, F32) with o_dt F32 and D a multiple of 4
+ * up to 128 (fp32 CUDA-core path); or qk_dt in {BF16, F16}, v_dt in {BF16,
+ * F16}, D in {64, 128}, o_dt in {F32, BF16, F16} (tensor-core path: Q K^T
+ * in qk_dt with fp32 accumulation; P rounded to v_dt for P V with fp32
+ * accumulation).  Strides and pointers must be 16-byte aligned.
+ * Head dims other than these return DIT_ERR_UNSUPPORTED.
+ */
+DIT_API dit_status dit_attn_partial(int B, int H, int D, float scale,
+                            int n_q, const int* q_len, int n_kv, const int* kv_len,
+                            dit_view q, dit_dtype qk_dt, dit_view k, dit_view v,
+                            dit_dtype v_dt, dit_view o, dit_dtype o_dt,
+                            dit_lse_view lse, int* d_status, void* stream);
+
+/*
+ * dit_attn_merge_lse: fold n_parts partials of each query block into the
+ * exact result (SGLang Diffusion "Parallelism Overview", What happens to the
+ * shapes and Constraints: online-softmax merge over ranks holding the same
+ * heads over different rows).  For each (r, b, h, i):
+ *   M   = max_j lse_j,   lse = M + ln sum_j exp(lse_j - M)
+ *   out = sum_j exp(lse_j - lse) * O_j          (j ascending, fp32)
+ * Rows whose every partial is empty (lse_j = -inf) give out = 0, lse = -inf.
+ *   parts:  partial j of block r at parts.ptr + r*stride_q + j*stride_kv
+ *   lse_parts: same indexing as dit_attn_partial's lse
+ *   out:    block r at out.ptr + r*out.stride_q; lse_out may have ptr NULL
+ * parts_dt in {F32, BF16, F16}; out_dt in {F32, BF16, F16}; D % 8 == 0.
+ */
+DIT_API dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int* q_len,
+                              int n_parts, dit_view parts, dit_dtype parts_dt,
+                              dit_lse_view lse_parts, dit_view out, dit_dtype out_dt,
+                              dit_lse_view lse_out, void* stream);
+
+/*
+ * dit_attention: single-shot attention O = softmax(scale * Q K^T) V over
+ * all Sk keys (edge-dit.cpp "Parallel execution", Ulysses sequence
+ * parallelism: exact full-sequence attention per head), with the row
+ * log-sum-exp if lse.ptr is not NULL.  Same types and layout rules as
+ * dit_attn_partial with one query block and one key/value block.
+ */
+DIT_API dit_status dit_attention(int B, int H, int D, float scale, int Sq, int Sk,
+                         dit_view q, dit_dtype qk_dt, dit_view k, dit_view v,
+                         dit_dtype v_dt, dit_view o, dit_dtype o_dt,
+                         dit_lse_view lse, int* d_status, void* stream);
+
+/*
+ * dit_cfg_combine: p = p_uncond + g * (p_cond - p_uncond), elementwise
+ * (edge-dit.cpp "Parallel execution", classifier-free guidance; under CFG
+ * parallelism rank 0 holds the unconditional branch).  pred is a dense
+ * [2][N] tensor: pred[0] unconditional, pred[1] conditional.  Arithmetic in
+ * fp32 as fma(g, p_cond - p_uncond, p_uncond), rounded once to out_dt;
+ * g = 0 returns p_uncond and g = 1 returns p_cond exactly.  N >= 0; pointers
+ * 16-byte aligned; out must not overlap pred.
+ */
+DIT_API dit_status dit_cfg_combine(const void* pred, dit_dtype in_dt, int64_t N, float g,
+                           void* out, dit_dtype out_dt, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DITSP_H */

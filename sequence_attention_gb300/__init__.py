@@ -1,0 +1,221 @@
+"""GB300 sequence-parallel DiT attention hot path: Python binding of libditsp.
+
+Each function here has the name of the C entry point it calls and only
+marshals arguments: tensor pointers, strides and element types go in, the
+CUDA kernels of libditsp.so do all of the work on the caller's current CUDA
+stream.  PyTorch is used for device memory and streams only.  There is no
+CPU or PyTorch fallback: if the library is missing, importing raises.
+
+Tensor conventions (element strides are read from the tensors, the head dim
+must be contiguous):
+  Q of the query blocks         [n_q,  B, S, H, D]
+  K, V of the key/value blocks  [n_kv, B, S, H, D]
+  partial outputs               [n_q, n_kv, B, S, H, D]
+  partial log-sum-exp           [n_q, n_kv, B, H, S]   (float32)
+"""
+from __future__ import annotations
+
+import math
+from ctypes import byref, c_int, c_int64, c_void_p
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import (DIT_BF16, DIT_F16, DIT_F32, DIT_HEAD_TO_SEQ, DIT_SEQ_TO_HEAD, DitError,
+                   DitLseView, DitSpLayout, DitView, check, lib)
+
+__all__ = [
+    "DitError", "Layout", "DIT_SEQ_TO_HEAD", "DIT_HEAD_TO_SEQ",
+    "dit_sp_layout_init", "dit_sp_a2a_counts", "dit_ulysses_pack", "dit_a2a_sim",
+    "dit_ulysses_unpack", "dit_attn_partial", "dit_attn_merge_lse", "dit_attention",
+    "dit_cfg_combine", "dit_device_status", "library_path",
+]
+
+lib()   # load now: fail at import time, not at first call
+
+_DT = {torch.float32: DIT_F32, torch.bfloat16: DIT_BF16, torch.float16: DIT_F16}
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _dt(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _stream(stream) -> c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+class Layout:
+    """A filled dit_sp_layout plus the buffer shapes it implies."""
+
+    def __init__(self, raw: DitSpLayout):
+        self.raw = raw
+
+    def __getattr__(self, name):
+        raw = self.__dict__["raw"]
+        v = getattr(raw, name)
+        if name in ("ring_len", "ring_off"):
+            return list(v)[: raw.R]
+        if name in ("rank_len", "rank_off"):
+            return list(v)[: raw.R * raw.U]
+        return v
+
+    def head_shape(self):
+        """Head-layout plane [R, B, S_cap, Hp, D]."""
+        r = self.raw
+        return (r.R, r.B, r.S_cap, r.Hp, r.D)
+
+    def seq_shape(self):
+        r = self.raw
+        return (r.B, r.S, r.H, r.D)
+
+    def wire_elems(self, nplanes: int) -> int:
+        r = self.raw
+        return nplanes * r.B * r.S * r.Hp * r.D
+
+
+def dit_sp_layout_init(B: int, S: int, H: int, D: int, U: int, R: int) -> Layout:
+    raw = DitSpLayout()
+    check(lib().dit_sp_layout_init(B, S, H, D, U, R, byref(raw)))
+    return Layout(raw)
+
+
+def dit_sp_a2a_counts(L: Layout, direction: int, nplanes: int, rank: int):
+    U = L.raw.U
+    arrs = [(c_int64 * U)() for _ in range(4)]
+    check(lib().dit_sp_a2a_counts(byref(L.raw), direction, nplanes, rank, *arrs))
+    return tuple(list(a) for a in arrs)
+
+
+def dit_ulysses_pack(L: Layout, direction: int, srcs: Sequence[torch.Tensor], send: torch.Tensor,
+                     stream=None) -> None:
+    arr = (c_void_p * 3)(*[s.data_ptr() for s in srcs])
+    check(lib().dit_ulysses_pack(byref(L.raw), direction, len(srcs), arr, _dt(srcs[0]),
+                                 _ptr(send), _dt(send), _stream(stream)))
+
+
+def dit_a2a_sim(L: Layout, direction: int, nplanes: int, send: torch.Tensor, recv: torch.Tensor,
+                stream=None) -> None:
+    check(lib().dit_a2a_sim(byref(L.raw), direction, nplanes, _ptr(send), _ptr(recv), _dt(send),
+                            _stream(stream)))
+
+
+def dit_ulysses_unpack(L: Layout, direction: int, recv: torch.Tensor, dsts: Sequence[torch.Tensor],
+                       range_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    ptrs = (c_void_p * 3)(*[d.data_ptr() for d in dsts])
+    dts = (c_int * 3)(*[_dt(d) for d in dsts])
+    check(lib().dit_ulysses_unpack(byref(L.raw), direction, len(dsts), _ptr(recv), _dt(recv), ptrs,
+                                   dts, _ptr(range_flag), _stream(stream)))
+
+
+def _view(t: torch.Tensor, kind: str) -> DitView:
+    """kind: 'q' [n_q,B,S,H,D], 'kv' [n_kv,B,S,H,D], 'o' [n_q,n_kv,B,S,H,D],
+    'out' [n_q,B,S,H,D], 'single' [B,S,H,D]."""
+    st = t.stride()
+    if st[-1] != 1:
+        raise ValueError("the head dim must be contiguous")
+    v = DitView()
+    v.ptr = t.data_ptr()
+    if kind in ("q", "out"):
+        v.stride_q, v.stride_b, v.stride_s, v.stride_h = st[0], st[1], st[2], st[3]
+    elif kind == "kv":
+        v.stride_kv, v.stride_b, v.stride_s, v.stride_h = st[0], st[1], st[2], st[3]
+    elif kind == "o":
+        v.stride_q, v.stride_kv, v.stride_b, v.stride_s, v.stride_h = st[0], st[1], st[2], st[3], st[4]
+    elif kind == "single":
+        v.stride_b, v.stride_s, v.stride_h = st[0], st[1], st[2]
+    else:
+        raise ValueError(kind)
+    return v
+
+
+def _lse_view(t: Optional[torch.Tensor], kind: str) -> DitLseView:
+    v = DitLseView()
+    if t is None:
+        return v
+    if t.dtype != torch.float32 or t.stride(-1) != 1:
+        raise ValueError("lse must be float32 with contiguous rows")
+    st = t.stride()
+    v.ptr = t.data_ptr()
+    if kind == "o":        # [n_q, n_kv, B, H, S]
+        v.stride_q, v.stride_kv, v.stride_b, v.stride_h = st[0], st[1], st[2], st[3]
+    elif kind == "out":    # [n_q, B, H, S]
+        v.stride_q, v.stride_b, v.stride_h = st[0], st[1], st[2]
+    elif kind == "single":  # [B, H, S]
+        v.stride_b, v.stride_h = st[0], st[1]
+    else:
+        raise ValueError(kind)
+    return v
+
+
+def _lens(vals: Optional[Sequence[int]], n: int, default: int):
+    vals = [default] * n if vals is None else list(vals)
+    if len(vals) != n:
+        raise ValueError("length list does not match the block count")
+    return (c_int * max(n, 1))(*vals)
+
+
+def dit_attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                     lse: Optional[torch.Tensor] = None, q_len: Optional[Sequence[int]] = None,
+                     kv_len: Optional[Sequence[int]] = None, scale: Optional[float] = None,
+                     status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """All (query block, key/value block) partials in one launch."""
+    n_q, B, Sq, H, D = q.shape
+    n_kv = k.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    check(lib().dit_attn_partial(B, H, D, float(scale), n_q, _lens(q_len, n_q, Sq), n_kv,
+                                 _lens(kv_len, n_kv, k.shape[2]), _view(q, "q"), _dt(q),
+                                 _view(k, "kv"), _view(v, "kv"), _dt(v), _view(o, "o"), _dt(o),
+                                 _lse_view(lse, "o"), _ptr(status), _stream(stream)))
+
+
+def dit_attn_merge_lse(parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor,
+                       lse_out: Optional[torch.Tensor] = None,
+                       q_len: Optional[Sequence[int]] = None, stream=None) -> None:
+    n_q, n_parts, B, S, H, D = parts.shape
+    check(lib().dit_attn_merge_lse(B, H, D, n_q, _lens(q_len, n_q, S), n_parts, _view(parts, "o"),
+                                   _dt(parts), _lse_view(lse_parts, "o"), _view(out, "out"), _dt(out),
+                                   _lse_view(lse_out, "out"), _stream(stream)))
+
+
+def dit_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                  lse: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                  status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Single-shot attention: q [B,Sq,H,D], k/v [B,Sk,H,D], o [B,Sq,H,D]."""
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    check(lib().dit_attention(B, H, D, float(scale), Sq, Sk, _view(q, "single"), _dt(q),
+                              _view(k, "single"), _view(v, "single"), _dt(v), _view(o, "single"),
+                              _dt(o), _lse_view(lse, "single"), _ptr(status), _stream(stream)))
+
+
+def dit_cfg_combine(pred: torch.Tensor, out: torch.Tensor, g: float, stream=None) -> None:
+    """pred [2, ...] (0 = unconditional, 1 = conditional) -> out [...]."""
+    if not (pred.is_contiguous() and out.is_contiguous()):
+        raise ValueError("cfg combine needs contiguous tensors")
+    N = out.numel()
+    if pred.numel() != 2 * N:
+        raise ValueError("pred must hold two branches of out's size")
+    check(lib().dit_cfg_combine(_ptr(pred), _dt(pred), N, float(g), _ptr(out), _dt(out),
+                                _stream(stream)))
+
+
+def dit_device_status(reset: bool = True) -> int:
+    code = c_int(0)
+    check(lib().dit_device_status(byref(code), 1 if reset else 0))
+    return code.value

@@ -1,0 +1,89 @@
+// ABI entry points of the attention step: argument validation and dispatch
+// to the fp32 CUDA-core kernel or the tcgen05 tensor-core kernel.
+#include <string.h>
+
+#include "attn_common.cuh"
+
+namespace ditsp {
+namespace {
+
+bool stride_ok(int64_t s, int elem_bytes) { return s >= 0 && ((s * elem_bytes) % 16) == 0; }
+
+dit_status validate_and_launch(AttnArgs& a, const char* who, cudaStream_t st) {
+    if (a.B < 1 || a.H < 1 || a.D < 1) return fail(DIT_ERR_INVALID_ARG, "%s: need B, H, D >= 1", who);
+    if (a.n_q < 1 || a.n_q > DIT_MAX_R || a.n_kv < 1 || a.n_kv > DIT_MAX_R)
+        return fail(DIT_ERR_INVALID_ARG, "%s: need 1 <= n_q, n_kv <= %d", who, DIT_MAX_R);
+    for (int r = 0; r < a.n_q; ++r)
+        if (a.q_len[r] < 0) return fail(DIT_ERR_INVALID_ARG, "%s: negative query length", who);
+    for (int r = 0; r < a.n_kv; ++r)
+        if (a.kv_len[r] < 0) return fail(DIT_ERR_INVALID_ARG, "%s: negative key length", who);
+    if (!dtype_ok(a.qk_dt) || !dtype_ok(a.v_dt) || !dtype_ok(a.o_dt))
+        return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (!a.q.ptr || !a.k.ptr || !a.v.ptr || !a.o.ptr)
+        return fail(DIT_ERR_INVALID_ARG, "%s: NULL tensor pointer", who);
+    if (!aligned16(a.q.ptr) || !aligned16(a.k.ptr) || !aligned16(a.v.ptr) || !aligned16(a.o.ptr))
+        return fail(DIT_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", who);
+    if (a.lse.ptr && (reinterpret_cast<uintptr_t>(a.lse.ptr) & 3))
+        return fail(DIT_ERR_INVALID_ARG, "%s: lse pointer misaligned", who);
+    const bool f32 = a.qk_dt == DIT_F32;
+    if (f32) {
+        if (a.v_dt != DIT_F32 || a.o_dt != DIT_F32)
+            return fail(DIT_ERR_UNSUPPORTED, "%s: fp32 Q/K need fp32 V and fp32 O", who);
+        if (a.D != 16 && a.D != 32 && a.D != 64 && a.D != 128)
+            return fail(DIT_ERR_UNSUPPORTED, "%s: fp32 path supports D in {16,32,64,128}", who);
+    } else {
+        if (a.v_dt == DIT_F32) return fail(DIT_ERR_UNSUPPORTED, "%s: 16-bit Q/K need 16-bit V", who);
+        if (a.D != 64 && a.D != 128)
+            return fail(DIT_ERR_UNSUPPORTED, "%s: tensor-core path supports D in {64,128}", who);
+    }
+    const int qb = dtype_bytes(a.qk_dt), vb = dtype_bytes(a.v_dt), ob = dtype_bytes(a.o_dt);
+    const bool ok = stride_ok(a.q.stride_q, qb) && stride_ok(a.q.stride_b, qb) && stride_ok(a.q.stride_s, qb) &&
+                    stride_ok(a.q.stride_h, qb) && stride_ok(a.k.stride_kv, qb) && stride_ok(a.k.stride_b, qb) &&
+                    stride_ok(a.k.stride_s, qb) && stride_ok(a.k.stride_h, qb) && stride_ok(a.v.stride_kv, vb) &&
+                    stride_ok(a.v.stride_b, vb) && stride_ok(a.v.stride_s, vb) && stride_ok(a.v.stride_h, vb) &&
+                    stride_ok(a.o.stride_q, ob) && stride_ok(a.o.stride_kv, ob) && stride_ok(a.o.stride_b, ob) &&
+                    stride_ok(a.o.stride_s, ob) && stride_ok(a.o.stride_h, ob);
+    if (!ok) return fail(DIT_ERR_INVALID_ARG, "%s: strides must be non-negative 16-byte multiples", who);
+    if (!a.status) a.status = default_status_word();
+    if (!a.status) return fail(DIT_ERR_CUDA, "%s: no device status word", who);
+    return f32 ? launch_attn_f32(a, st) : launch_attn_tc(a, st);
+}
+
+}  // namespace
+}  // namespace ditsp
+
+using namespace ditsp;
+
+extern "C" dit_status dit_attn_partial(int B, int H, int D, float scale, int n_q, const int* q_len, int n_kv,
+                                       const int* kv_len, dit_view q, dit_dtype qk_dt, dit_view k, dit_view v,
+                                       dit_dtype v_dt, dit_view o, dit_dtype o_dt, dit_lse_view lse,
+                                       int* d_status, void* stream) {
+    if (!q_len || !kv_len) return fail(DIT_ERR_INVALID_ARG, "dit_attn_partial: NULL length array");
+    if (n_q < 1 || n_q > DIT_MAX_R || n_kv < 1 || n_kv > DIT_MAX_R)
+        return fail(DIT_ERR_INVALID_ARG, "dit_attn_partial: need 1 <= n_q, n_kv <= %d", DIT_MAX_R);
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.B = B; a.H = H; a.D = D; a.n_q = n_q; a.n_kv = n_kv; a.scale = scale;
+    for (int r = 0; r < n_q; ++r) a.q_len[r] = q_len[r];
+    for (int r = 0; r < n_kv; ++r) a.kv_len[r] = kv_len[r];
+    a.q = q; a.k = k; a.v = v; a.o = o;
+    a.qk_dt = qk_dt; a.v_dt = v_dt; a.o_dt = o_dt; a.lse = lse; a.status = d_status;
+    return validate_and_launch(a, "dit_attn_partial", (cudaStream_t)stream);
+}
+
+extern "C" dit_status dit_attention(int B, int H, int D, float scale, int Sq, int Sk, dit_view q, dit_dtype qk_dt,
+                                    dit_view k, dit_view v, dit_dtype v_dt, dit_view o, dit_dtype o_dt,
+                                    dit_lse_view lse, int* d_status, void* stream) {
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.B = B; a.H = H; a.D = D; a.n_q = 1; a.n_kv = 1; a.scale = scale;
+    a.q_len[0] = Sq; a.kv_len[0] = Sk;
+    q.stride_q = q.stride_kv = 0;
+    k.stride_q = k.stride_kv = 0;
+    v.stride_q = v.stride_kv = 0;
+    o.stride_q = o.stride_kv = 0;
+    lse.stride_q = lse.stride_kv = 0;
+    a.q = q; a.k = k; a.v = v; a.o = o;
+    a.qk_dt = qk_dt; a.v_dt = v_dt; a.o_dt = o_dt; a.lse = lse; a.status = d_status;
+    return validate_and_launch(a, "dit_attention", (cudaStream_t)stream);
+}

@@ -1,0 +1,23 @@
+// Argument block shared by the two attention implementations (fp32 CUDA
+// cores, bf16/f16 tensor cores) and the ABI entry points that dispatch to them.
+#pragma once
+
+#include "common.cuh"
+
+namespace ditsp {
+
+struct AttnArgs {
+    int B, H, D, n_q, n_kv;
+    int q_len[DIT_MAX_R];
+    int kv_len[DIT_MAX_R];
+    float scale;
+    dit_view q, k, v, o;
+    dit_dtype qk_dt, v_dt, o_dt;
+    dit_lse_view lse;
+    int* status;
+};
+
+dit_status launch_attn_f32(const AttnArgs& a, cudaStream_t st);
+dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st);
+
+}  // namespace ditsp

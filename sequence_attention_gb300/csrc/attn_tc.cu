@@ -1,0 +1,599 @@
+// Attention partial on the Blackwell tensor cores (tcgen05 + TMEM + TMA).
+//
+// Computes, per (query block r, key/value block j, batch b, head h), the
+// attention of Q_r against the valid keys of (K_j, V_j) with the row
+// log-sum-exp (SGLang Diffusion "Parallelism Overview", Constraints: the
+// ring merge needs each call's softmax LSE; edge-dit.cpp "Parallel
+// execution": exact full-sequence attention per head).
+//
+// CTA = 256 query rows as two 128-row tiles, one (r, j, b, h).  Warp roles:
+//   warps 0-3  softmax for Q tile 0 (TMEM lanes 0-127, one row per thread)
+//   warps 4-7  softmax for Q tile 1
+//   warp  8    TMA producer: Q once, then K and V tiles into a 2-stage ring
+//   warp  9    MMA issuer (one thread): S = Q K^T and O += P V
+//   warps 10-11 idle
+// TMEM (512 columns x 128 lanes, fp32): S0 [0,128) S1 [128,256)
+// O0 [256,256+D) O1 [256+D,256+2D).  P (16-bit) overwrites the first half
+// of its tile's S columns and feeds the P V MMA straight from TMEM.
+//
+// Per key tile the MMA thread issues, for the two Q tiles in turn:
+// P V for tile t of key tile n, then Q K^T for tile t of key tile n+1, so
+// the tensor core computes one tile's products while the other tile's
+// softmax runs.  Softmax keeps the row max in the log2 domain and only
+// rescales the O accumulator when a row's max grows by more than 2^8
+// (values of P stay <= 256, exact in f16/bf16 and fp32); the final 1/l
+// normalisation uses the same reference max, so the result is exact up to
+// rounding.  Keys at or past the block's valid length are masked to -inf;
+// TMA zero-fills rows past each block's extent, so padding bytes in the
+// buffers are never read.
+//
+// Every mbarrier wait is bounded (a few seconds of %globaltimer); on expiry
+// the CTA records DIT_ERR_TIMEOUT in the status word, stops issuing work,
+// waits (bounded) for the copies and MMAs it already issued, frees TMEM and
+// exits.
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "attn_common.cuh"
+
+namespace ditsp {
+namespace {
+
+constexpr int BM = 128;          // query rows per tile (MMA M)
+constexpr int BN = 128;          // keys per tile (MMA N of Q K^T, K of P V)
+constexpr int NQT = 2;           // query tiles per CTA
+constexpr int NST = 2;           // K and V pipeline stages
+constexpr int NTHREADS = 384;
+constexpr int CHUNK = BM * 128;  // bytes of one 64-column (128-byte) swizzle chunk
+constexpr unsigned long long kWaitNs = 4000000000ull;
+
+enum { B_Q = 0, B_KF = 1, B_KE = 3, B_VF = 5, B_VE = 7, B_SF = 9, B_PF = 11, B_OD = 13, NBAR = 14 };
+
+struct TcParams {
+    CUtensorMap qmap[DIT_MAX_R];
+    CUtensorMap kmap[DIT_MAX_R];
+    CUtensorMap vmap[DIT_MAX_R];
+    int q_len[DIT_MAX_R];
+    int kv_len[DIT_MAX_R];
+    int B, n_q, n_kv;
+    float c;                      // scale * log2(e)
+    uint32_t idesc_qk, idesc_pv;
+    dit_view o;
+    dit_dtype o_dt;
+    dit_lse_view lse;
+    int* status;
+};
+
+template <int D>
+constexpr int smem_bytes() {
+    return (NQT + 2 * NST) * BM * D * 2 + NBAR * 8 + 16 + 1024;
+}
+
+// ---- PTX wrappers -----------------------------------------------------------
+__device__ __forceinline__ uint32_t su32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+struct Ctl {
+    volatile int* abort;
+    int* status;
+};
+
+// Wait for the phase of `parity` to complete.  Returns false if the CTA has
+// aborted or this wait ran out of time (then the CTA is marked aborted).
+__device__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl& ctl) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = gtimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 0) {
+            if (*ctl.abort) return false;
+            if (gtimer() - t0 > kWaitNs) {
+                *ctl.abort = 1;
+                atomicExch(ctl.status, (int)DIT_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: used to drain work already
+// issued before the CTA frees its resources.
+__device__ void drain_phase(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = gtimer();
+    while (!mbar_try_wait(bar, parity))
+        if (gtimer() - t0 > kWaitNs) return;
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            int c3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem)
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem)
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
+// address, leading/stride byte offsets in 16-byte units, version 1).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+#define R32(x) "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), \
+    "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]),       \
+    "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]),    \
+    "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]),    \
+    "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
+#define W16(x) "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]), \
+    "r"(x[8]), "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15])
+#define W32(x) W16(x), "r"(x[16]), "r"(x[17]), "r"(x[18]), "r"(x[19]), "r"(x[20]), "r"(x[21]),     \
+    "r"(x[22]), "r"(x[23]), "r"(x[24]), "r"(x[25]), "r"(x[26]), "r"(x[27]), "r"(x[28]), "r"(x[29]), \
+    "r"(x[30]), "r"(x[31])
+
+// 32 consecutive fp32 columns of this thread's TMEM lane, with the wait in
+// the same asm block so no use of the registers can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&x)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : R32(x)
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&x)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16};\n" ::"r"(taddr),
+        W16(x)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&x)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+        W32(x)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+    if (BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---- the kernel -------------------------------------------------------------
+template <int D, bool P_BF16>
+__global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
+    constexpr int NCH = D / 64;          // 128-byte chunks per row
+    constexpr int TILE = BM * D * 2;     // bytes of one Q, K or V tile
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sK = sQ + NQT * TILE;
+    uint8_t* sV = sK + NST * TILE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NST * TILE);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int z = blockIdx.z;
+    const int b = z % p.B;
+    const int j = (z / p.B) % p.n_kv;
+    const int r = z / (p.B * p.n_kv);
+    const int h = blockIdx.y;
+    const int qlen = p.q_len[r], kvlen = p.kv_len[j];
+    const int row_base = blockIdx.x * (NQT * BM);
+    if (row_base >= qlen) return;
+    const int ntiles = (kvlen + BN - 1) / BN;
+
+    const int eb = dtype_bytes(p.o_dt);
+    char* obase = static_cast<char*>(p.o.ptr) +
+                  (r * p.o.stride_q + j * p.o.stride_kv + b * p.o.stride_b + h * p.o.stride_h) * eb;
+    float* lbase = p.lse.ptr ? p.lse.ptr + r * p.lse.stride_q + j * p.lse.stride_kv + b * p.lse.stride_b +
+                                   h * p.lse.stride_h
+                             : nullptr;
+
+    if (ntiles == 0) {   // empty key chunk: O = 0, lse = -inf
+        if (threadIdx.x < NQT * BM) {
+            const int row = row_base + threadIdx.x;
+            if (row < qlen) {
+                char* orow = obase + (long long)row * p.o.stride_s * eb;
+                for (int d = 0; d < D; d += 8) store8_zero(orow + d * eb, p.o_dt);
+                if (lbase) lbase[row] = -INFINITY;
+            }
+        }
+        return;
+    }
+
+    const Ctl ctl{abort_flag, p.status};
+    auto bar = [&](int i) { return su32(bars + i); };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B_Q), 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(bar(B_KF + s), 1);
+            mbar_init(bar(B_KE + s), 1);
+            mbar_init(bar(B_VF + s), 1);
+            mbar_init(bar(B_VE + s), 1);
+        }
+        for (int t = 0; t < NQT; ++t) {
+            mbar_init(bar(B_SF + t), 1);
+            mbar_init(bar(B_PF + t), 128);
+        }
+        mbar_init(bar(B_OD), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const CUtensorMap* qm = &p.qmap[r];
+            const CUtensorMap* km = &p.kmap[j];
+            const CUtensorMap* vm = &p.vmap[j];
+            mbar_expect_tx(bar(B_Q), NQT * TILE);
+            for (int t = 0; t < NQT; ++t)
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_4d(su32(sQ + t * TILE + c * CHUNK), qm, c * 64, h, row_base + t * BM, b, bar(B_Q));
+            int issued = 0;
+            bool ok = true;
+            for (int n = 0; n < ntiles && ok; ++n) {
+                const int s = n % NST;
+                const uint32_t ph = (n / NST) & 1;
+                if (n >= NST && !(ok = wait_phase(bar(B_KE + s), ph ^ 1, ctl))) break;
+                mbar_expect_tx(bar(B_KF + s), TILE);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_4d(su32(sK + s * TILE + c * CHUNK), km, c * 64, h, n * BN, b, bar(B_KF + s));
+                if (n >= NST && !(ok = wait_phase(bar(B_VE + s), ph ^ 1, ctl))) {
+                    // K of tile n is in flight but V is not: drain K only
+                    drain_phase(bar(B_KF + s), ph);
+                    break;
+                }
+                mbar_expect_tx(bar(B_VF + s), TILE);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_4d(su32(sV + s * TILE + c * CHUNK), vm, c * 64, h, n * BN, b, bar(B_VF + s));
+                issued = n + 1;
+            }
+            if (!ok || *abort_flag) {
+                // let every copy this thread issued land before smem is released
+                drain_phase(bar(B_Q), 0);
+                for (int n = issued > NST ? issued - NST : 0; n < issued; ++n) {
+                    drain_phase(bar(B_KF + n % NST), (n / NST) & 1);
+                    drain_phase(bar(B_VF + n % NST), (n / NST) & 1);
+                }
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t S[NQT] = {tmem, tmem + 128};
+            const uint32_t O[NQT] = {tmem + 256, tmem + 256 + D};
+            auto issue_qk = [&](int t, int s) {
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks & 3) * 32 + (ks >> 2) * CHUNK;
+                    const uint64_t a = sdesc(su32(sQ + t * TILE) + off, 16, 1024);
+                    const uint64_t bd = sdesc(su32(sK + s * TILE) + off, 16, 1024);
+                    mma_ss(S[t], a, bd, p.idesc_qk, ks > 0);
+                }
+            };
+            auto issue_pv = [&](int t, int s, bool acc) {
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks) {
+                    // V tile rows are keys (K dim), 64-wide d chunks CHUNK apart (N dim)
+                    const uint64_t bd = sdesc(su32(sV + s * TILE) + ks * 16 * 128, CHUNK, 1024);
+                    mma_ts(O[t], S[t] + ks * 8, bd, p.idesc_pv, (acc || ks > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = wait_phase(bar(B_Q), 0, ctl) && wait_phase(bar(B_KF), 0, ctl);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(0, 0);
+                tc_commit(bar(B_SF + 0));
+                issue_qk(1, 0);
+                tc_commit(bar(B_SF + 1));
+                tc_commit(bar(B_KE + 0));
+            }
+            for (int n = 0; n < ntiles && ok; ++n) {
+                const int s = n % NST;
+                const bool nxt = n + 1 < ntiles;
+                const int s1 = (n + 1) % NST;
+                const uint32_t ph1 = ((n + 1) / NST) & 1;
+                if (!(ok = wait_phase(bar(B_VF + s), (n / NST) & 1, ctl))) break;
+                if (!(ok = wait_phase(bar(B_PF + 0), n & 1, ctl))) break;
+                tc_fence_after();
+                issue_pv(0, s, n > 0);
+                if (nxt) {
+                    if (!(ok = wait_phase(bar(B_KF + s1), ph1, ctl))) break;
+                    tc_fence_after();
+                    issue_qk(0, s1);
+                    tc_commit(bar(B_SF + 0));
+                }
+                if (!(ok = wait_phase(bar(B_PF + 1), n & 1, ctl))) break;
+                tc_fence_after();
+                issue_pv(1, s, n > 0);
+                tc_commit(bar(B_VE + s));
+                if (nxt) {
+                    issue_qk(1, s1);
+                    tc_commit(bar(B_SF + 1));
+                    tc_commit(bar(B_KE + s1));
+                }
+            }
+            tc_commit(bar(B_OD));
+            if (!ok) drain_phase(bar(B_OD), 0);   // every issued MMA has finished
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ softmax
+        const int t = warp >> 2, q4 = warp & 3;
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const uint32_t St = tmem + t * 128 + lane_off;
+        const uint32_t Ot = tmem + 256 + t * D + lane_off;
+        const int row = row_base + t * BM + q4 * 32 + lane;
+        const float c = p.c;
+        float m_used = 0.f, l = 0.f;
+        bool ok = true;
+        uint32_t x[32];
+        for (int n = 0; n < ntiles; ++n) {
+            ok = __all_sync(0xffffffffu, wait_phase(bar(B_SF + t), n & 1, ctl));
+            if (!ok) break;
+            tc_fence_after();
+            const int valid = min(BN, kvlen - n * BN);
+            // pass 1: row max of the tile's valid keys
+            float mx = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                tmem_ld32(St + cc * 32, x);
+                if (valid == BN) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(x[e]));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (cc * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(x[e]));
+                }
+            }
+            const float mxs = mx * c;
+            if (n == 0) {
+                m_used = mxs;
+            } else if (__any_sync(0xffffffffu, mxs > m_used + 8.f)) {
+                // Raise the reference max and rescale O (the previous P V of
+                // this tile finished before this tile's S became ready).
+                const float mnew = fmaxf(m_used, mxs);
+                const float alpha = ex2(m_used - mnew);
+                l *= alpha;
+                m_used = mnew;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    tmem_ld32(Ot + cc * 32, x);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha);
+                    tmem_st32(Ot + cc * 32, x);
+                }
+            }
+            // pass 2: P = 2^(s*c - m), row sum, P written over S as 16-bit pairs
+#pragma unroll
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                tmem_ld32(St + cc * 32, x);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float a0 = fmaf(__uint_as_float(x[2 * e]), c, -m_used);
+                    float a1 = fmaf(__uint_as_float(x[2 * e + 1]), c, -m_used);
+                    if (valid != BN) {
+                        if (cc * 32 + 2 * e >= valid) a0 = -INFINITY;
+                        if (cc * 32 + 2 * e + 1 >= valid) a1 = -INFINITY;
+                    }
+                    const float p0 = ex2(a0), p1 = ex2(a1);
+                    l += p0 + p1;
+                    pk[e] = pack_p<P_BF16>(p0, p1);
+                }
+                tmem_st16(St + cc * 16, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(B_PF + t));
+        }
+        // epilogue: O / l and lse = ln(2) * (m + log2 l)
+        if (ok) ok = __all_sync(0xffffffffu, wait_phase(bar(B_OD), 0, ctl));
+        if (ok) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            const bool live = row < qlen;
+            char* orow = obase + (long long)(live ? row : 0) * p.o.stride_s * eb;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                tmem_ld32(Ot + cc * 32, x);
+                if (live) {
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        Vec8 v;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v.f[e] = __uint_as_float(x[q8 * 8 + e]) * inv;
+                        store8(orow + (cc * 32 + q8 * 8) * eb, p.o_dt, v);
+                    }
+                }
+            }
+            if (live && lbase) lbase[row] = (m_used + log2f(l)) * 0.69314718055994531f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+    }
+}
+
+// ---- host side --------------------------------------------------------------
+std::atomic<void*> g_encode{nullptr};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    void* f = g_encode.load(std::memory_order_acquire);
+    if (!f) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !f)
+            return nullptr;
+        g_encode.store(f, std::memory_order_release);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// 4-D map over [B][rows][H][D] (innermost first: d, h, row, b) with a
+// 64 x 1 x 128 x 1 box and 128-byte swizzle; rows past `rows` read as 0.
+dit_status make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base, dit_dtype dt,
+                    int D, int H, int rows, int B, int64_t sh, int64_t ss, int64_t sb) {
+    if (rows < 1) rows = 1;     // never read: the kernel skips empty blocks
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)B};
+    const int64_t sbb = B > 1 ? sb : (int64_t)rows * ss;   // unused when B == 1
+    const cuuint64_t strides[3] = {(cuuint64_t)(sh * 2), (cuuint64_t)(ss * 2), (cuuint64_t)(sbb * 2)};
+    const cuuint32_t box[4] = {64, 1, BM, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult res = enc(m, dt == DIT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                       const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS) return fail(DIT_ERR_INVALID_ARG, "attention: tensor map rejected (CUresult %d)", (int)res);
+    return DIT_OK;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 accumulation.
+uint32_t make_idesc(bool bf16, bool b_mn_major, int N, int M) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <int D, bool PB>
+dit_status launch_kernel(const TcParams& prm, dim3 grid, cudaStream_t st) {
+    int smem = smem_bytes<D>();
+    if (smem < 116 * 1024) smem = 116 * 1024;   // one CTA per SM: it owns all 512 TMEM columns
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "attention: %s", cudaGetErrorString(e));
+    attn_tc_kernel<D, PB><<<grid, NTHREADS, smem, st>>>(prm);
+    return check_launch("dit_attn_partial(tcgen05)");
+}
+
+}  // namespace
+
+dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return fail(DIT_ERR_CUDA, "attention: cuTensorMapEncodeTiled unavailable");
+    TcParams params;                // kernel parameter block (~3.3 KB, on the stack)
+    memset(&params, 0, sizeof(params));
+    TcParams* prm = &params;
+    dit_status s = DIT_OK;
+    int maxq = 0;
+    for (int r = 0; r < a.n_q && s == DIT_OK; ++r) {
+        prm->q_len[r] = a.q_len[r];
+        if (a.q_len[r] > maxq) maxq = a.q_len[r];
+        const char* base = static_cast<const char*>(a.q.ptr) + r * a.q.stride_q * 2;
+        s = make_map(enc, &prm->qmap[r], base, a.qk_dt, a.D, a.H, a.q_len[r], a.B, a.q.stride_h, a.q.stride_s,
+                     a.q.stride_b);
+    }
+    for (int j = 0; j < a.n_kv && s == DIT_OK; ++j) {
+        prm->kv_len[j] = a.kv_len[j];
+        const char* kb = static_cast<const char*>(a.k.ptr) + j * a.k.stride_kv * 2;
+        const char* vb = static_cast<const char*>(a.v.ptr) + j * a.v.stride_kv * 2;
+        s = make_map(enc, &prm->kmap[j], kb, a.qk_dt, a.D, a.H, a.kv_len[j], a.B, a.k.stride_h, a.k.stride_s,
+                     a.k.stride_b);
+        if (s == DIT_OK)
+            s = make_map(enc, &prm->vmap[j], vb, a.v_dt, a.D, a.H, a.kv_len[j], a.B, a.v.stride_h, a.v.stride_s,
+                         a.v.stride_b);
+    }
+    if (s == DIT_OK && maxq > 0) {
+        prm->B = a.B; prm->n_q = a.n_q; prm->n_kv = a.n_kv;
+        prm->c = a.scale * 1.4426950408889634f;
+        prm->idesc_qk = make_idesc(a.qk_dt == DIT_BF16, false, BN, BM);
+        prm->idesc_pv = make_idesc(a.v_dt == DIT_BF16, true, a.D, BM);
+        prm->o = a.o; prm->o_dt = a.o_dt; prm->lse = a.lse; prm->status = a.status;
+        dim3 grid((maxq + NQT * BM - 1) / (NQT * BM), a.H, a.n_q * a.n_kv * a.B);
+        if (grid.y > 65535 || grid.z > 65535) s = fail(DIT_ERR_UNSUPPORTED, "attention: grid too large");
+        else if (a.D == 128) s = a.v_dt == DIT_BF16 ? launch_kernel<128, true>(*prm, grid, st) : launch_kernel<128, false>(*prm, grid, st);
+        else s = a.v_dt == DIT_BF16 ? launch_kernel<64, true>(*prm, grid, st) : launch_kernel<64, false>(*prm, grid, st);
+    }
+    return s;
+}
+
+}  // namespace ditsp

@@ -1,0 +1,219 @@
+// Bandwidth-bound elementwise steps: the classifier-free guidance combine and
+// the log-sum-exp merge of ring partials.
+//
+// CFG (edge-dit.cpp "Parallel execution", classifier-free guidance):
+//   p = p_uncond + g * (p_cond - p_uncond), evaluated literally in fp32 as
+//   fma(g, p_cond - p_uncond, p_uncond) and fused with the cast to the output
+//   type.  g = 0 gives p_uncond exactly; for g = 1 the formula reduces to
+//   p_cond, which is returned as is (fp32 rounding of p_cond - p_uncond could
+//   otherwise move it when the two differ by many binades).
+// Merge (SGLang Diffusion "Parallelism Overview", What happens to the shapes /
+// Constraints: the ring's online-softmax merge over same-head, different-row
+// partials):  lse = M + ln sum_j exp(lse_j - M),  O = sum_j exp(lse_j - lse) O_j.
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace ditsp {
+namespace {
+
+// ---------------------------------------------------------------------------
+// CFG: each thread moves 8 elements per step; 4 steps are issued before any
+// store so that enough loads are in flight to cover HBM latency.
+__global__ void __launch_bounds__(256) cfg_vec_kernel(const char* __restrict__ pred, dit_dtype in_dt,
+                                                      long long nvec, long long N, float g,
+                                                      char* __restrict__ out, dit_dtype out_dt) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const int ib = 8 * dtype_bytes(in_dt), ob = 8 * dtype_bytes(out_dt);
+    const char* cond = pred + N * dtype_bytes(in_dt);
+    const bool g_one = (g == 1.0f);
+    for (long long v0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; v0 < nvec; v0 += 4 * stride) {
+        Vec8 u[4], c[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const long long v = v0 + k * stride;
+            if (v < nvec) {
+                load8(pred + v * ib, in_dt, u[k]);
+                load8(cond + v * ib, in_dt, c[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const long long v = v0 + k * stride;
+            if (v < nvec) {
+                Vec8 p;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    p.f[e] = g_one ? c[k].f[e] : fmaf(g, c[k].f[e] - u[k].f[e], u[k].f[e]);
+                store8(out + v * ob, out_dt, p);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float load1(const char* p, dit_dtype t, long long i) {
+    if (t == DIT_F32) return reinterpret_cast<const float*>(p)[i];
+    if (t == DIT_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+    return __half2float(reinterpret_cast<const __half*>(p)[i]);
+}
+
+__device__ __forceinline__ void store1(char* p, dit_dtype t, long long i, float x) {
+    if (t == DIT_F32) reinterpret_cast<float*>(p)[i] = x;
+    else if (t == DIT_BF16) reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
+    else reinterpret_cast<__half*>(p)[i] = __float2half_rn(x);
+}
+
+// Scalar tail / unaligned-length path.
+__global__ void cfg_scalar_kernel(const char* __restrict__ pred, dit_dtype in_dt, long long begin,
+                                  long long N, float g, char* __restrict__ out, dit_dtype out_dt) {
+    for (long long i = begin + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < N;
+         i += (long long)gridDim.x * blockDim.x) {
+        const float u = load1(pred, in_dt, i), c = load1(pred, in_dt, N + i);
+        store1(out, out_dt, i, g == 1.0f ? c : fmaf(g, c - u, u));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Merge: one thread per 8 consecutive d of one (r, b, i, h) row.  Grid y is
+// (r, b); x covers rows * heads * D/8 of the longest block.
+struct MergeArgs {
+    int B, H, D, n_parts;
+    int q_len[DIT_MAX_R];
+    dit_view parts;
+    dit_dtype parts_dt;
+    dit_lse_view lse_parts;
+    dit_view out;
+    dit_dtype out_dt;
+    dit_lse_view lse_out;
+};
+
+__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ MergeArgs a) {
+    const int r = blockIdx.y / a.B, b = blockIdx.y % a.B;
+    const int chunks = a.D >> 3;
+    const long long per_row = (long long)a.H * chunks;
+    const long long total = (long long)a.q_len[r] * per_row;
+    for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+         t += (long long)gridDim.x * blockDim.x) {
+        const int i = (int)(t / per_row);
+        const int rem = (int)(t - (long long)i * per_row);
+        const int h = rem / chunks, c = rem - h * chunks;
+        const float* lp = a.lse_parts.ptr + r * a.lse_parts.stride_q + b * a.lse_parts.stride_b +
+                          h * a.lse_parts.stride_h + i;
+        float lj[DIT_MAX_R];
+        float M = -INFINITY;
+        for (int j = 0; j < a.n_parts; ++j) {
+            lj[j] = lp[j * a.lse_parts.stride_kv];
+            M = fmaxf(M, lj[j]);
+        }
+        Vec8 acc;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc.f[e] = 0.f;
+        float lse = -INFINITY;
+        if (M != -INFINITY) {
+            float s = 0.f;
+            for (int j = 0; j < a.n_parts; ++j) s += expf(lj[j] - M);
+            lse = M + logf(s);
+            const long long base = r * a.parts.stride_q + b * a.parts.stride_b + i * a.parts.stride_s +
+                                   h * a.parts.stride_h + c * 8;
+            const char* pp = static_cast<const char*>(a.parts.ptr);
+            const int eb = dtype_bytes(a.parts_dt);
+            for (int j = 0; j < a.n_parts; ++j) {
+                const float w = expf(lj[j] - lse);
+                Vec8 o;
+                load8(pp + (base + j * a.parts.stride_kv) * eb, a.parts_dt, o);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc.f[e] = fmaf(w, o.f[e], acc.f[e]);
+            }
+        }
+        const long long ob = r * a.out.stride_q + b * a.out.stride_b + i * a.out.stride_s +
+                             h * a.out.stride_h + c * 8;
+        store8(static_cast<char*>(a.out.ptr) + ob * dtype_bytes(a.out_dt), a.out_dt, acc);
+        if (a.lse_out.ptr && c == 0)
+            a.lse_out.ptr[r * a.lse_out.stride_q + b * a.lse_out.stride_b + h * a.lse_out.stride_h + i] = lse;
+    }
+}
+
+}  // namespace
+}  // namespace ditsp
+
+using namespace ditsp;
+
+extern "C" dit_status dit_cfg_combine(const void* pred, dit_dtype in_dt, int64_t N, float g, void* out,
+                                      dit_dtype out_dt, void* stream) {
+    const char* who = "dit_cfg_combine";
+    if (!dtype_ok(in_dt) || !dtype_ok(out_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (N < 0) return fail(DIT_ERR_INVALID_ARG, "%s: N < 0", who);
+    if (N == 0) return DIT_OK;
+    if (!pred || !out || !aligned16(pred) || !aligned16(out))
+        return fail(DIT_ERR_INVALID_ARG, "%s: pred/out NULL or not 16-byte aligned", who);
+    const char* pb = static_cast<const char*>(pred);
+    const char* pe = pb + 2 * N * dtype_bytes(in_dt);
+    const char* ob = static_cast<const char*>(out);
+    const char* oe = ob + N * dtype_bytes(out_dt);
+    if (ob < pe && pb < oe) return fail(DIT_ERR_INVALID_ARG, "%s: out overlaps pred", who);
+    cudaStream_t st = (cudaStream_t)stream;
+    // The vector path needs the conditional half 16-byte aligned too.
+    const bool vec_ok = ((N * dtype_bytes(in_dt)) % 16) == 0;
+    long long done = 0;
+    if (vec_ok) {
+        const long long nvec = N / 8;
+        if (nvec > 0) {
+            long long blocks = (nvec + 255) / 256;
+            const long long cap = (long long)num_sms() * 8;
+            if (blocks > cap) blocks = cap;
+            cfg_vec_kernel<<<(unsigned)blocks, 256, 0, st>>>(pb, in_dt, nvec, N, g, static_cast<char*>(out), out_dt);
+            dit_status s = check_launch(who);
+            if (s != DIT_OK) return s;
+        }
+        done = nvec * 8;
+    }
+    if (done < N) {
+        const long long rest = N - done;
+        long long blocks = (rest + 255) / 256;
+        if (blocks > 4096) blocks = 4096;
+        cfg_scalar_kernel<<<(unsigned)blocks, 256, 0, st>>>(pb, in_dt, done, N, g, static_cast<char*>(out), out_dt);
+        return check_launch(who);
+    }
+    return DIT_OK;
+}
+
+extern "C" dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int* q_len, int n_parts,
+                                         dit_view parts, dit_dtype parts_dt, dit_lse_view lse_parts,
+                                         dit_view out, dit_dtype out_dt, dit_lse_view lse_out,
+                                         void* stream) {
+    const char* who = "dit_attn_merge_lse";
+    if (B < 1 || H < 1 || D < 8 || D % 8 != 0)
+        return fail(DIT_ERR_INVALID_ARG, "%s: need B,H >= 1 and D a positive multiple of 8", who);
+    if (n_q < 1 || n_q > DIT_MAX_R || !q_len || n_parts < 1 || n_parts > DIT_MAX_R)
+        return fail(DIT_ERR_INVALID_ARG, "%s: need 1 <= n_q, n_parts <= %d", who, DIT_MAX_R);
+    if (!dtype_ok(parts_dt) || !dtype_ok(out_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (!parts.ptr || !out.ptr || !lse_parts.ptr || !aligned16(parts.ptr) || !aligned16(out.ptr))
+        return fail(DIT_ERR_INVALID_ARG, "%s: NULL or misaligned pointer", who);
+    const int64_t pstr[] = {parts.stride_q, parts.stride_kv, parts.stride_b, parts.stride_s, parts.stride_h};
+    const int64_t ostr[] = {out.stride_q, out.stride_b, out.stride_s, out.stride_h};
+    for (int64_t s : pstr)
+        if ((s * dtype_bytes(parts_dt)) % 16) return fail(DIT_ERR_INVALID_ARG, "%s: parts strides not 16-byte multiples", who);
+    for (int64_t s : ostr)
+        if ((s * dtype_bytes(out_dt)) % 16) return fail(DIT_ERR_INVALID_ARG, "%s: out strides not 16-byte multiples", who);
+    MergeArgs a;
+    memset(&a, 0, sizeof(a));
+    a.B = B; a.H = H; a.D = D; a.n_parts = n_parts;
+    int maxq = 0;
+    for (int r = 0; r < n_q; ++r) {
+        if (q_len[r] < 0) return fail(DIT_ERR_INVALID_ARG, "%s: negative q_len", who);
+        a.q_len[r] = q_len[r];
+        if (q_len[r] > maxq) maxq = q_len[r];
+    }
+    if (maxq == 0) return DIT_OK;
+    a.parts = parts; a.parts_dt = parts_dt; a.lse_parts = lse_parts;
+    a.out = out; a.out_dt = out_dt; a.lse_out = lse_out;
+    const long long work = (long long)maxq * H * (D / 8);
+    long long bx = (work + 255) / 256;
+    const long long cap = (long long)num_sms() * 8;
+    if (bx > cap) bx = cap;
+    dim3 grid((unsigned)bx, (unsigned)(n_q * B));
+    if (grid.y > 65535) return fail(DIT_ERR_UNSUPPORTED, "%s: n_q * B too large", who);
+    merge_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(a);
+    return check_launch(who);
+}

@@ -1,0 +1,112 @@
+"""Unified sequence parallelism (Ulysses inside, ring outside) on one GPU.
+
+The U*R virtual ranks are partitions of the buffers below, all in one GPU's
+memory; every step is one call into libditsp (cache-dit "Context
+Parallelism", USP: Ulysses all-to-all, then ring attention on the
+redistributed data, then the inverse all-to-all; SGLang Diffusion
+"Parallelism Overview", What happens to the shapes):
+
+  dit_ulysses_pack(S2H)   seq-sharded Q,K,V -> peer-major send buffer
+  dit_a2a_sim(S2H)        send -> receive buffers (the all-to-all)
+  dit_ulysses_unpack(S2H) receive -> head layout [R,B,S_cap,Hp,D] (V as f16)
+  dit_attn_partial        every (ring block r, ring block j) partial, one launch
+  dit_attn_merge_lse      R partials -> exact output (skipped when R = 1)
+  dit_ulysses_pack(H2S), dit_a2a_sim(H2S), dit_ulysses_unpack(H2S)
+                          head layout -> seq-sharded output [B,S,H,D]
+
+All buffers are allocated once, when the plan is built; run() allocates
+nothing and only enqueues kernels on the current (or given) stream.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+
+from . import (DIT_HEAD_TO_SEQ, DIT_SEQ_TO_HEAD, dit_a2a_sim, dit_attn_merge_lse, dit_attn_partial,
+               dit_sp_layout_init, dit_ulysses_pack, dit_ulysses_unpack)
+
+
+class UspPlan:
+    def __init__(self, B: int, S: int, H: int, D: int, U: int, R: int,
+                 in_dtype: torch.dtype = torch.bfloat16,
+                 out_dtype: Optional[torch.dtype] = None,
+                 v_dtype: Optional[torch.dtype] = None,
+                 device: str = "cuda", scale: Optional[float] = None):
+        self.L = dit_sp_layout_init(B, S, H, D, U, R)
+        self.B, self.S, self.H, self.D, self.U, self.R = B, S, H, D, U, R
+        self.in_dtype = in_dtype
+        self.wire_dtype = in_dtype
+        self.out_dtype = out_dtype or in_dtype
+        if v_dtype is None:
+            # P V runs with P in V's type: f16 keeps P to 11 bits (see DESIGN)
+            v_dtype = torch.float16 if in_dtype == torch.bfloat16 else in_dtype
+        self.v_dtype = v_dtype
+        self.scale = 1.0 / math.sqrt(D) if scale is None else scale
+        L = self.L
+        hs = L.head_shape()
+        dev = torch.device(device)
+        self.send = torch.empty(L.wire_elems(3), dtype=in_dtype, device=dev)
+        self.recv = torch.empty(L.wire_elems(3), dtype=in_dtype, device=dev)
+        self.q_h = torch.empty(hs, dtype=in_dtype, device=dev)
+        self.k_h = torch.empty(hs, dtype=in_dtype, device=dev)
+        self.v_h = torch.empty(hs, dtype=v_dtype, device=dev)
+        self.o_h = torch.empty(hs, dtype=self.out_dtype, device=dev)
+        if R > 1:
+            self.parts = torch.empty((R, R) + tuple(hs[1:]), dtype=torch.float32, device=dev)
+            self.lse_parts = torch.empty((R, R, B, L.Hp, L.S_cap), dtype=torch.float32, device=dev)
+        else:
+            self.parts = self.lse_parts = None
+        self.send_o = torch.empty(L.wire_elems(1), dtype=self.out_dtype, device=dev)
+        self.recv_o = torch.empty(L.wire_elems(1), dtype=self.out_dtype, device=dev)
+        self.range_flag = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    # ---- views of the real (unpadded) heads --------------------------------
+    def heads(self, t: torch.Tensor) -> torch.Tensor:
+        return t[..., : self.H, :]
+
+    @property
+    def ring_len(self):
+        return self.L.ring_len
+
+    def steps(self):
+        """Names of the kernels one run() launches, in order."""
+        s = ["pack_s2h", "a2a_s2h", "unpack_s2h", "attn_partial"]
+        if self.R > 1:
+            s.append("merge")
+        return s + ["pack_h2s", "a2a_h2s", "unpack_h2s"]
+
+    def layout_in(self, q, k, v, stream=None):
+        L = self.L
+        dit_ulysses_pack(L, DIT_SEQ_TO_HEAD, [q, k, v], self.send, stream)
+        dit_a2a_sim(L, DIT_SEQ_TO_HEAD, 3, self.send, self.recv, stream)
+        dit_ulysses_unpack(L, DIT_SEQ_TO_HEAD, self.recv, [self.q_h, self.k_h, self.v_h],
+                           self.range_flag, stream)
+
+    def attend(self, stream=None):
+        rl = self.ring_len
+        qv, kv, vv = self.heads(self.q_h), self.heads(self.k_h), self.heads(self.v_h)
+        if self.R == 1:
+            o = self.heads(self.o_h).unsqueeze(1)        # [1, 1, B, S, H, D]
+            dit_attn_partial(qv, kv, vv, o, None, rl, rl, self.scale, self.status, stream)
+        else:
+            dit_attn_partial(qv, kv, vv, self.heads(self.parts),
+                             self.lse_parts[:, :, :, : self.H, :], rl, rl, self.scale,
+                             self.status, stream)
+            dit_attn_merge_lse(self.heads(self.parts), self.lse_parts[:, :, :, : self.H, :],
+                               self.heads(self.o_h), None, rl, stream)
+
+    def layout_out(self, out, stream=None):
+        L = self.L
+        dit_ulysses_pack(L, DIT_HEAD_TO_SEQ, [self.o_h], self.send_o, stream)
+        dit_a2a_sim(L, DIT_HEAD_TO_SEQ, 1, self.send_o, self.recv_o, stream)
+        dit_ulysses_unpack(L, DIT_HEAD_TO_SEQ, self.recv_o, [out], None, stream)
+
+    def run(self, q, k, v, out, stream=None):
+        """q, k, v: [B, S, H, D] seq-sharded inputs; out: [B, S, H, D]."""
+        self.layout_in(q, k, v, stream)
+        self.attend(stream)
+        self.layout_out(out, stream)
+        return out

@@ -1,0 +1,153 @@
+"""The C ABI on the host: the library loads, exports every symbol the header
+declares, its layout bookkeeping equals the oracle's, and bad arguments are
+rejected before anything is launched (these calls never reach a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import layout as olayout
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ditsp.h")
+
+
+@pytest.fixture(scope="module")
+def dl():
+    if not os.path.exists(os.path.join(ROOT, "sequence_attention_gb300", "libditsp.so")):
+        import __graft_entry__
+        __graft_entry__.build()
+    from sequence_attention_gb300 import _lib
+    return _lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"DIT_API\s+[\w\s\*]*?\b(dit_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for n in ("dit_attn_partial", "dit_attn_merge_lse", "dit_ulysses_pack", "dit_ulysses_unpack",
+              "dit_a2a_sim", "dit_cfg_combine", "dit_attention", "dit_sp_layout_init"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(dl):
+    raw = ctypes.CDLL(dl.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+    assert set(declared_functions()) == set(dl.EXPORTS)
+
+
+def test_binding_imports(dl):
+    import sequence_attention_gb300 as sa
+    assert os.path.samefile(sa.library_path(), dl.LIB_PATH)
+
+
+@pytest.mark.parametrize("dims", [(1, 256, 4, 64, 2, 2), (1, 4608, 24, 128, 4, 1), (1, 4481, 24, 128, 4, 2),
+                                  (2, 7145, 24, 128, 5, 2), (1, 75600, 40, 128, 8, 4), (1, 3, 2, 8, 2, 2),
+                                  (1, 0, 1, 8, 3, 2), (3, 17, 5, 8, 64, 1)])
+def test_layout_init_matches_oracle(dl, dims):
+    import sequence_attention_gb300 as sa
+    L = sa.dit_sp_layout_init(*dims)
+    ref = olayout.make_layout(*dims)
+    assert (L.Hp, L.Hl, L.S_cap) == (ref.Hp, ref.Hl, ref.S_cap)
+    assert L.ring_len == list(ref.ring_len) and L.ring_off == list(ref.ring_off)
+    assert L.rank_len == list(ref.rank_len) and L.rank_off == list(ref.rank_off)
+
+
+@pytest.mark.parametrize("direction,np_", [(0, 3), (1, 1), (0, 1)])
+def test_a2a_counts_match_oracle(dl, direction, np_):
+    import sequence_attention_gb300 as sa
+    dims = (2, 7145, 24, 128, 5, 2)
+    L = sa.dit_sp_layout_init(*dims)
+    ref = olayout.make_layout(*dims)
+    for rank in range(10):
+        got = sa.dit_sp_a2a_counts(L, direction, np_, rank)
+        exp = olayout.a2a_counts(ref, "s2h" if direction == 0 else "h2s", np_, rank)
+        assert [list(x) for x in got] == [list(x) for x in exp]
+
+
+@pytest.mark.parametrize("args", [(0, 8, 1, 8, 1, 1), (1, -1, 1, 8, 1, 1), (1, 8, 1, 8, 65, 1),
+                                  (1, 8, 1, 8, 1, 9), (1, 8, 1, 8, 16, 8)])
+def test_layout_init_rejects_bad_sizes(dl, args):
+    import sequence_attention_gb300 as sa
+    with pytest.raises(sa.DitError) as e:
+        sa.dit_sp_layout_init(*args)
+    assert e.value.status == dl.DIT_ERR_INVALID_ARG
+
+
+def test_validation_happens_before_any_launch(dl):
+    """Each call below fails validation; none of them touches the CUDA runtime,
+    so they behave the same with or without a GPU."""
+    L = dl.lib()
+    lay = dl.DitSpLayout()
+    assert L.dit_sp_layout_init(1, 64, 4, 64, 2, 2, ctypes.byref(lay)) == 0
+    bad = dl.DitSpLayout.from_buffer_copy(lay)
+    bad.rank_len[0] += 1                      # corrupted table
+    ptrs = (ctypes.c_void_p * 3)(16, 32, 48)
+    st = L.dit_ulysses_pack(ctypes.byref(bad), 0, 3, ptrs, dl.DIT_BF16, ctypes.c_void_p(64), dl.DIT_BF16, None)
+    assert st == dl.DIT_ERR_INVALID_ARG and b"inconsistent" in L.dit_last_error()
+    # misaligned send buffer
+    st = L.dit_ulysses_pack(ctypes.byref(lay), 0, 3, ptrs, dl.DIT_BF16, ctypes.c_void_p(8), dl.DIT_BF16, None)
+    assert st == dl.DIT_ERR_INVALID_ARG
+    # head-to-seq with 3 planes
+    st = L.dit_ulysses_pack(ctypes.byref(lay), 1, 3, ptrs, dl.DIT_BF16, ctypes.c_void_p(64), dl.DIT_BF16, None)
+    assert st == dl.DIT_ERR_INVALID_ARG
+    # a2a with identical send/recv
+    st = L.dit_a2a_sim(ctypes.byref(lay), 0, 3, ctypes.c_void_p(64), ctypes.c_void_p(64), dl.DIT_BF16, None)
+    assert st == dl.DIT_ERR_INVALID_ARG
+    # cfg: N < 0, NULL, overlap
+    assert L.dit_cfg_combine(ctypes.c_void_p(64), dl.DIT_BF16, -1, 1.0, ctypes.c_void_p(128), dl.DIT_BF16, None) \
+        == dl.DIT_ERR_INVALID_ARG
+    assert L.dit_cfg_combine(None, dl.DIT_BF16, 8, 1.0, ctypes.c_void_p(128), dl.DIT_BF16, None) \
+        == dl.DIT_ERR_INVALID_ARG
+    assert L.dit_cfg_combine(ctypes.c_void_p(64), dl.DIT_BF16, 64, 1.0, ctypes.c_void_p(96), dl.DIT_BF16, None) \
+        == dl.DIT_ERR_INVALID_ARG
+    assert L.dit_cfg_combine(ctypes.c_void_p(64), 7, 8, 1.0, ctypes.c_void_p(4096), dl.DIT_BF16, None) \
+        == dl.DIT_ERR_INVALID_ARG
+    assert L.dit_cfg_combine(ctypes.c_void_p(64), dl.DIT_BF16, 0, 1.0, ctypes.c_void_p(4096), dl.DIT_BF16, None) \
+        == dl.DIT_OK                           # empty: nothing to do
+
+
+def _view(ptr, sb=0, ss=0, sh=0):
+    from sequence_attention_gb300._lib import DitView
+    v = DitView()
+    v.ptr, v.stride_b, v.stride_s, v.stride_h = ptr, sb, ss, sh
+    return v
+
+
+def test_attention_argument_checks(dl):
+    from sequence_attention_gb300._lib import DitLseView
+    L = dl.lib()
+    q = _view(1 << 20, 64 * 4 * 128, 4 * 128, 128)
+    lse = DitLseView()
+    ok = dict(B=1, H=4, D=128, Sq=64, Sk=64)
+
+    def call(**kw):
+        a = dict(ok, qk=dl.DIT_BF16, v=dl.DIT_F16, o=dl.DIT_BF16, q=q)
+        a.update(kw)
+        return L.dit_attention(a["B"], a["H"], a["D"], 0.1, a["Sq"], a["Sk"], a["q"], a["qk"], q, q,
+                               a["v"], q, a["o"], lse, None, None)
+
+    assert call(D=96) == dl.DIT_ERR_UNSUPPORTED          # tensor-core path: D in {64, 128}
+    assert call(qk=dl.DIT_F32) == dl.DIT_ERR_UNSUPPORTED  # fp32 Q/K need fp32 V and O
+    assert call(v=dl.DIT_F32) == dl.DIT_ERR_UNSUPPORTED
+    assert call(B=0) == dl.DIT_ERR_INVALID_ARG
+    assert call(Sq=-1) == dl.DIT_ERR_INVALID_ARG
+    assert call(q=_view(1 << 20, 64 * 4 * 128, 4 * 128 + 1, 128)) == dl.DIT_ERR_INVALID_ARG  # odd stride
+    assert call(q=_view((1 << 20) + 8, 64 * 4 * 128, 4 * 128, 128)) == dl.DIT_ERR_INVALID_ARG  # misaligned
+    assert call(q=_view(0)) == dl.DIT_ERR_INVALID_ARG    # NULL
+    lens = (ctypes.c_int * 9)(*([8] * 9))
+    st = L.dit_attn_partial(1, 4, 128, 0.1, 9, lens, 1, lens, q, dl.DIT_BF16, q, q, dl.DIT_F16, q,
+                            dl.DIT_BF16, lse, None, None)
+    assert st == dl.DIT_ERR_INVALID_ARG                  # more than 8 query blocks
+
+
+def test_status_strings(dl):
+    L = dl.lib()
+    assert L.dit_status_string(0) == b"DIT_OK"
+    assert L.dit_status_string(4) == b"DIT_ERR_TIMEOUT"
+    assert L.dit_status_string(99) == b"DIT_ERR_UNKNOWN"

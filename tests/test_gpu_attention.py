@@ -1,0 +1,168 @@
+"""GPU parity of the attention partial, the merge and single-shot attention.
+
+Tensor-core path (bf16 Q/K, f16 or bf16 V): O within max-abs 2e-2 and
+relative RMS 5e-3 of the fp64 oracle, log-sum-exp within 1e-4.  fp32 path:
+within 1e-5.  Shapes span several 128-row tiles with ragged tails, several
+heads and batches, and the degenerate cases (one key, empty chunk).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import attention as oatt
+from tests.helpers import (F32_MAX_ABS, LSE_ABS, MERGE_REL_RMS, assert_bf16_close, f64, max_abs,
+                           rel_rms)
+
+pytestmark = pytest.mark.gpu
+
+
+def _qkv(B, Sq, Sk, H, D, dt="bf16", scale=0.5, seed=0):
+    q = synth.normal((B, Sq, H, D), seed, scale, dt)
+    k = synth.normal((B, Sk, H, D), seed + 1, scale, dt)
+    v = synth.normal((B, Sk, H, D), seed + 2, scale, dt)
+    return q, k, v
+
+
+def _single(q, k, v, v_dtype, o_dtype, with_lse=True):
+    import sequence_attention_gb300 as sa
+    B, Sq, H, D = q.shape
+    qd, kd, vd = q.cuda(), k.cuda(), v.to(v_dtype).cuda()
+    o = torch.empty((B, Sq, H, D), dtype=o_dtype, device="cuda")
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device="cuda") if with_lse else None
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sa.dit_attention(qd, kd, vd, o, lse, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return o, lse
+
+
+@pytest.mark.parametrize("B,Sq,Sk,H,D", [
+    (1, 128, 128, 1, 128),     # one tile
+    (1, 256, 256, 2, 128),     # two query tiles, two key tiles
+    (2, 300, 333, 3, 128),     # ragged query and key tails, batch 2
+    (1, 5, 7, 1, 128),         # fewer rows than a tile
+    (1, 1, 1, 1, 128),         # a single key
+    (1, 640, 1000, 2, 64),     # D = 64
+    (1, 513, 4097, 1, 128),    # long key sequence, 33 key tiles
+])
+@pytest.mark.parametrize("v_dtype", [torch.float16, torch.bfloat16])
+def test_tensor_core_attention_matches_oracle(B, Sq, Sk, H, D, v_dtype):
+    q, k, v = _qkv(B, Sq, Sk, H, D)
+    for o_dtype in (torch.float32, torch.bfloat16):
+        o, lse = _single(q, k, v, v_dtype, o_dtype)
+        o_ref, lse_ref = oatt.attention(f64(q), f64(k), f64(v))
+        assert_bf16_close(f64(o), o_ref, f"O ({o_dtype}, V {v_dtype})")
+        assert max_abs(f64(lse), lse_ref) <= LSE_ABS
+
+
+def test_tensor_core_large_logits():
+    """Unit-variance inputs at D = 128 give logits of std ~1 and row maxima
+    that grow across key tiles, exercising the O rescale path."""
+    B, Sq, Sk, H, D = 1, 256, 2048, 2, 128
+    q, k, v = _qkv(B, Sq, Sk, H, D, scale=2.0, seed=40)
+    # make late keys dominate: the running max must be raised several times
+    k[:, -300:] *= 1.5
+    o, lse = _single(q, k, v, torch.float16, torch.float32)
+    o_ref, lse_ref = oatt.attention(f64(q), f64(k), f64(v))
+    assert_bf16_close(f64(o), o_ref, "O")
+    assert max_abs(f64(lse), lse_ref) <= 10 * LSE_ABS
+
+
+@pytest.mark.parametrize("B,Sq,Sk,H,D", [(1, 256, 256, 4, 64), (1, 100, 77, 2, 32), (2, 70, 130, 3, 128)])
+def test_fp32_attention_matches_oracle(B, Sq, Sk, H, D):
+    q, k, v = _qkv(B, Sq, Sk, H, D, dt="f32", scale=1.0, seed=3)
+    o, lse = _single(q, k, v, torch.float32, torch.float32)
+    o_ref, lse_ref = oatt.attention(f64(q), f64(k), f64(v))
+    assert max_abs(f64(o), o_ref) <= F32_MAX_ABS
+    assert max_abs(f64(lse), lse_ref) <= F32_MAX_ABS
+
+
+def _partials(q, k, v, lens, v_dtype, seed_rows=None):
+    """Split the keys into chunks of a common stride (last chunk shorter) and
+    run every partial in one launch; returns (O parts, LSE parts)."""
+    import sequence_attention_gb300 as sa
+    B, Sq, H, D = q.shape
+    n = len(lens)
+    stride = max(lens)
+    Skp = stride * n
+    kp = torch.zeros((n, B, stride, H, D), dtype=k.dtype)
+    vp = torch.zeros((n, B, stride, H, D), dtype=v.dtype)
+    off = 0
+    for j, L in enumerate(lens):
+        kp[j, :, :L] = k[:, off:off + L]
+        vp[j, :, :L] = v[:, off:off + L]
+        kp[j, :, L:] = float("nan")         # padding rows must never be read
+        vp[j, :, L:] = float("nan")
+        off += L
+    o = torch.empty((1, n, B, Sq, H, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((1, n, B, H, Sq), dtype=torch.float32, device="cuda")
+    sa.dit_attn_partial(q.unsqueeze(0).cuda(), kp.cuda(), vp.to(v_dtype).cuda(), o, lse,
+                        [Sq], lens)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+@pytest.mark.parametrize("dt,lens", [("bf16", [200, 200, 133]), ("bf16", [128, 0, 77]),
+                                     ("f32", [100, 100, 56]), ("bf16", [1000] * 4 + [997])])
+def test_partials_and_merge(dt, lens):
+    import sequence_attention_gb300 as sa
+    B, Sq, H, D = 2, 190, 2, (128 if dt == "bf16" else 64)
+    Sk = sum(lens)
+    q, k, v = _qkv(B, Sq, Sk, H, D, dt=dt, scale=0.5 if dt == "bf16" else 1.0, seed=11)
+    vdt = torch.float16 if dt == "bf16" else torch.float32
+    o, lse = _partials(q, k, v, lens, vdt)
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    off = 0
+    for j, L in enumerate(lens):
+        o_ref, l_ref = oatt.partial(qf, kf[:, off:off + L], vf[:, off:off + L], L)
+        got_o, got_l = f64(o[0, j]), f64(lse[0, j])
+        if L == 0:
+            assert np.all(got_o == 0) and np.all(np.isneginf(got_l))
+        elif dt == "bf16":
+            assert_bf16_close(got_o, o_ref, f"partial {j}")
+            assert max_abs(got_l, l_ref) <= LSE_ABS
+        else:
+            assert max_abs(got_o, o_ref) <= F32_MAX_ABS and max_abs(got_l, l_ref) <= F32_MAX_ABS
+        off += L
+    # merge on the device vs the fp64 oracle of the whole sequence
+    out = torch.empty((1, B, Sq, H, D), dtype=torch.float32, device="cuda")
+    lse_out = torch.empty((1, B, H, Sq), dtype=torch.float32, device="cuda")
+    sa.dit_attn_merge_lse(o, lse, out, lse_out, [Sq])
+    torch.cuda.synchronize()
+    o_ref, l_ref = oatt.attention(qf, kf, vf)
+    if dt == "bf16":
+        assert_bf16_close(f64(out[0]), o_ref, "merged")
+        # the merge bar: R-way merge vs single-shot on the device
+        single, _ = _single(q, k, v, vdt, torch.float32)
+        assert rel_rms(f64(out[0]), f64(single)) <= MERGE_REL_RMS
+    else:
+        assert max_abs(f64(out[0]), o_ref) <= F32_MAX_ABS
+    assert max_abs(f64(lse_out[0]), l_ref) <= LSE_ABS
+
+
+def test_merge_kernel_against_oracle_merge():
+    """Merge alone on random partials (fp32 parts, bf16 out), with an all-empty row."""
+    import sequence_attention_gb300 as sa
+    n_q, n, B, S, H, D = 2, 4, 1, 77, 3, 64
+    rng = np.random.default_rng(5)
+    parts = torch.from_numpy(rng.standard_normal((n_q, n, B, S, H, D)).astype(np.float32))
+    lse = torch.from_numpy((rng.standard_normal((n_q, n, B, H, S)) * 3).astype(np.float32))
+    lse[:, :, :, :, 5] = -math.inf
+    parts[:, :, :, 5] = 0.0
+    lse[0, 1, :, :, 9] = -math.inf            # one empty chunk for row 9
+    out = torch.empty((n_q, B, S, H, D), dtype=torch.bfloat16, device="cuda")
+    lse_out = torch.empty((n_q, B, H, S), dtype=torch.float32, device="cuda")
+    sa.dit_attn_merge_lse(parts.cuda(), lse.cuda(), out, lse_out, [S, S - 10])
+    torch.cuda.synchronize()
+    for r in range(n_q):
+        rows = S if r == 0 else S - 10
+        o_ref, l_ref = oatt.merge([(f64(parts[r, j, :, :rows]), f64(lse[r, j, :, :, :rows]))
+                                   for j in range(n)])
+        assert_bf16_close(f64(out[r, :, :rows]), o_ref, "merge")
+        got_l = f64(lse_out[r, :, :, :rows])
+        fin = np.isfinite(l_ref)
+        assert np.array_equal(np.isneginf(got_l), np.isneginf(l_ref))
+        assert max_abs(got_l[fin], l_ref[fin]) <= 1e-5

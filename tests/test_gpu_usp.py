@@ -1,0 +1,139 @@
+"""The whole hot path on the five workloads, against the fp64 oracle.
+
+Each run goes seq-sharded Q/K/V -> Ulysses pack -> simulated all-to-all ->
+unpack (V to f16) -> all ring partials in one launch -> log-sum-exp merge ->
+inverse all-to-all -> seq-sharded output, through the C ABI.  Small cases are
+compared in full; full-size cases on the first and last rows of every virtual
+rank (the UAA and ring seams) plus seeded random rows, all heads, against the
+oracle's attention over the full key sequence.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import attention as oatt
+from oracle import layout as olayout
+from oracle import usp as ousp
+from tests.helpers import F32_MAX_ABS, assert_bf16_close, f64, max_abs, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _plan(w, U, R=None, **kw):
+    from sequence_attention_gb300.usp import UspPlan
+    return UspPlan(w.B, w.S, w.H, w.D, U, w.R if R is None else R,
+                   in_dtype=synth.torch_dtype(w.dtype), **kw)
+
+
+def _oracle_rows(q, k, v, rows):
+    """fp64 attention of the given query rows against all keys, head by head."""
+    B, S, H, D = q.shape
+    out = np.empty((B, len(rows), H, D))
+    sel = torch.from_numpy(rows)
+    for b in range(B):
+        for h in range(H):
+            qh = f64(q[b:b + 1, sel, h:h + 1])
+            kh = f64(k[b:b + 1, :, h:h + 1])
+            vh = f64(v[b:b + 1, :, h:h + 1])
+            o, _ = oatt.attention(qh, kh, vh)
+            out[b, :, h] = o[0, :, 0]
+    return out
+
+
+@pytest.mark.parametrize("U,R", [(2, 1), (1, 2), (2, 2)])
+def test_tiny_fp32_full(U, R):
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = w.qkv()
+    plan = _plan(w, U, R)
+    out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.float32, device="cuda")
+    plan.run(q.cuda(), k.cuda(), v.cuda(), out)
+    torch.cuda.synchronize()
+    ref, _ = oatt.attention(f64(q), f64(k), f64(v))
+    assert max_abs(f64(out), ref) <= F32_MAX_ABS
+    # and the oracle's own USP composition agrees with its single shot
+    o2, _ = ousp.usp_attention(olayout.make_layout(w.B, w.S, w.H, w.D, U, R), f64(q), f64(k), f64(v))
+    assert max_abs(o2, ref) <= 1e-12
+
+
+@pytest.mark.parametrize("B,S,H,U,R", [(1, 1000, 5, 3, 2), (2, 700, 4, 2, 3), (1, 333, 3, 4, 1)])
+def test_medium_bf16_full(B, S, H, U, R):
+    """Sizes the oracle finishes in seconds, spanning several tiles and ragged
+    tails, with padded heads and uneven ranks: compared in full."""
+    D = 128
+    q = synth.normal((B, S, H, D), 20, 0.5, "bf16")
+    k = synth.normal((B, S, H, D), 21, 0.5, "bf16")
+    v = synth.normal((B, S, H, D), 22, 0.5, "bf16")
+    from sequence_attention_gb300.usp import UspPlan
+    plan = UspPlan(B, S, H, D, U, R)
+    out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device="cuda")
+    plan.run(q.cuda(), k.cuda(), v.cuda(), out)
+    torch.cuda.synchronize()
+    ref, _ = oatt.attention(f64(q), f64(k), f64(v))
+    assert_bf16_close(f64(out), ref, "usp")
+    assert int(plan.status.item()) == 0 and int(plan.range_flag.item()) == 0
+
+
+FULL = [("flux1024", 2), ("flux1024", 4), ("flux1008", 4), ("flux1008_4480", 4),
+        ("qwen1328", 5), ("wan", 8)]
+
+
+@pytest.mark.parametrize("name,U", FULL)
+def test_full_size_sampled(name, U):
+    w = synth.WORKLOADS[name]
+    q, k, v = w.qkv()
+    plan = _plan(w, U)
+    out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device="cuda")
+    plan.run(q.cuda(), k.cuda(), v.cuda(), out)
+    torch.cuda.synchronize()
+    assert int(plan.status.item()) == 0 and int(plan.range_flag.item()) == 0
+    n_random = 64 if name == "wan" else 192
+    rows = sample_rows(plan.L, n_random, seed=1)
+    ref = _oracle_rows(q, k, v, rows)
+    got = f64(out[:, torch.from_numpy(rows)])
+    assert_bf16_close(got, ref, name)
+
+
+def test_padding_never_reaches_outputs():
+    """FLUX-1008 (uneven ring blocks 2241/2240): the head-layout buffers are
+    filled with NaN before the run, so the padding row of ring block 1 holds
+    NaN.  The output must be NaN-free and bit-identical to a clean run."""
+    w = synth.WORKLOADS["flux1008"]
+    q, k, v = (t.cuda() for t in w.qkv())
+    plan = _plan(w, 4)
+    clean = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device="cuda")
+    plan.run(q, k, v, clean)
+    for t in (plan.q_h, plan.k_h, plan.v_h, plan.o_h, plan.parts):
+        t.fill_(float("nan"))
+    dirty = torch.empty_like(clean)
+    plan.run(q, k, v, dirty)
+    torch.cuda.synchronize()
+    assert not torch.isnan(dirty).any()
+    assert torch.equal(dirty.view(torch.int16), clean.view(torch.int16))
+
+
+def test_merge_vs_single_shot_on_device():
+    """The R-way merge agrees with single-shot attention on the device to
+    1e-3 relative RMS (fp32 outputs), FLUX-1008 with R = 2."""
+    import sequence_attention_gb300 as sa
+    from tests.helpers import MERGE_REL_RMS, rel_rms
+    w = synth.WORKLOADS["flux1008"]
+    q, k, v = (t.cuda() for t in w.qkv())
+    v16 = v.to(torch.float16)
+    single = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    sa.dit_attention(q, k, v16, single)
+    # keys split in two chunks of one common stride (ring blocks 2241 / 2240)
+    L = sa.dit_sp_layout_init(w.B, w.S, w.H, w.D, 1, 2)
+    cap = L.S_cap
+    kp = torch.zeros((2, w.B, cap, w.H, w.D), dtype=k.dtype, device="cuda")
+    vp = torch.zeros((2, w.B, cap, w.H, w.D), dtype=torch.float16, device="cuda")
+    for j in range(2):
+        kp[j, :, : L.ring_len[j]] = k[:, L.ring_off[j]:L.ring_off[j] + L.ring_len[j]]
+        vp[j, :, : L.ring_len[j]] = v16[:, L.ring_off[j]:L.ring_off[j] + L.ring_len[j]]
+    parts = torch.empty((1, 2, w.B, w.S, w.H, w.D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((1, 2, w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    sa.dit_attn_partial(q.unsqueeze(0), kp, vp, parts, lse, [w.S], L.ring_len)
+    merged = torch.empty((1,) + tuple(q.shape), dtype=torch.float32, device="cuda")
+    sa.dit_attn_merge_lse(parts, lse, merged, None, [w.S])
+    torch.cuda.synchronize()
+    assert rel_rms(f64(merged[0]), f64(single)) <= MERGE_REL_RMS
