@@ -206,6 +206,7 @@ DIT_API dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir, i
  *   o_i   = sum_t exp(s_t - lse_i) * v_t    (normalised by this chunk only)
  * Keys at or past kv_len[j] are excluded from the softmax, whatever their
  * contents.  A chunk with kv_len[j] == 0 gives o = 0 and lse = -inf.
+ * scale must be positive and finite (1/sqrt(D) in the pages' attention).
  *
  *   q        rows of block r at q.ptr + r*q.stride_q, [B][q_len[r]][H][D]
  *   k, v     rows of block j at ptr + j*stride_kv,    [B][kv_len[j]][H][D]

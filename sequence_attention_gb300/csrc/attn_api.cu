@@ -1,5 +1,6 @@
 // ABI entry points of the attention step: argument validation and dispatch
 // to the fp32 CUDA-core kernel or the tcgen05 tensor-core kernel.
+#include <math.h>
 #include <string.h>
 
 #include "attn_common.cuh"
@@ -11,6 +12,8 @@ bool stride_ok(int64_t s, int elem_bytes) { return s >= 0 && ((s * elem_bytes) %
 
 dit_status validate_and_launch(AttnArgs& a, const char* who, cudaStream_t st) {
     if (a.B < 1 || a.H < 1 || a.D < 1) return fail(DIT_ERR_INVALID_ARG, "%s: need B, H, D >= 1", who);
+    if (!(a.scale > 0.f) || !isfinite(a.scale))
+        return fail(DIT_ERR_INVALID_ARG, "%s: scale must be positive and finite", who);
     if (a.n_q < 1 || a.n_q > DIT_MAX_R || a.n_kv < 1 || a.n_kv > DIT_MAX_R)
         return fail(DIT_ERR_INVALID_ARG, "%s: need 1 <= n_q, n_kv <= %d", who, DIT_MAX_R);
     for (int r = 0; r < a.n_q; ++r)

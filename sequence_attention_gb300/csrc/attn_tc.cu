@@ -11,7 +11,10 @@
 //   warps 4-7  softmax for Q tile 1
 //   warp  8    TMA producer: Q once, then K and V tiles into a 2-stage ring
 //   warp  9    MMA issuer (one thread): S = Q K^T and O += P V
-//   warps 10-11 idle
+//   warps 10-11 idle (they complete the third warpgroup)
+// Registers: launched at 168 per thread; the producer/MMA warpgroup gives
+// back down to 72 and the two softmax warpgroups take 216 each
+// (2*216 + 72 = 3*168), enough to hold a whole 128-column score row.
 // TMEM (512 columns x 128 lanes, fp32): S0 [0,128) S1 [128,256)
 // O0 [256,256+D) O1 [256+D,256+2D).  P (16-bit) overwrites the first half
 // of its tile's S columns and feeds the P V MMA straight from TMEM.
@@ -176,41 +179,38 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-#define R32(x) "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), \
-    "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]),       \
-    "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]),    \
-    "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]),    \
-    "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
-#define W16(x) "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]), \
-    "r"(x[8]), "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15])
-#define W32(x) W16(x), "r"(x[16]), "r"(x[17]), "r"(x[18]), "r"(x[19]), "r"(x[20]), "r"(x[21]),     \
-    "r"(x[22]), "r"(x[23]), "r"(x[24]), "r"(x[25]), "r"(x[26]), "r"(x[27]), "r"(x[28]), "r"(x[29]), \
-    "r"(x[30]), "r"(x[31])
-
-// 32 consecutive fp32 columns of this thread's TMEM lane, with the wait in
-// the same asm block so no use of the registers can be scheduled before it.
+// TMEM <-> register moves of 32-bit columns of this thread's lane.  Each load
+// carries its wait in the same asm block, so no use of the registers can be
+// scheduled before the data has arrived.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&x)[32]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
         "tcgen05.wait::ld.sync.aligned;\n"
-        : R32(x)
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31])
         : "r"(taddr)
         : "memory");
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&x)[16]) {
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&x)[64]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15,%16};\n" ::"r"(taddr),
-        W16(x)
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31]), "=r"(x[32]), "=r"(x[33]), "=r"(x[34]), "=r"(x[35]), "=r"(x[36]), "=r"(x[37]), "=r"(x[38]), "=r"(x[39]), "=r"(x[40]), "=r"(x[41]), "=r"(x[42]), "=r"(x[43]), "=r"(x[44]), "=r"(x[45]), "=r"(x[46]), "=r"(x[47]), "=r"(x[48]), "=r"(x[49]), "=r"(x[50]), "=r"(x[51]), "=r"(x[52]), "=r"(x[53]), "=r"(x[54]), "=r"(x[55]), "=r"(x[56]), "=r"(x[57]), "=r"(x[58]), "=r"(x[59]), "=r"(x[60]), "=r"(x[61]), "=r"(x[62]), "=r"(x[63])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&x)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31]), "=r"(x[32]), "=r"(x[33]), "=r"(x[34]), "=r"(x[35]), "=r"(x[36]), "=r"(x[37]), "=r"(x[38]), "=r"(x[39]), "=r"(x[40]), "=r"(x[41]), "=r"(x[42]), "=r"(x[43]), "=r"(x[44]), "=r"(x[45]), "=r"(x[46]), "=r"(x[47]), "=r"(x[48]), "=r"(x[49]), "=r"(x[50]), "=r"(x[51]), "=r"(x[52]), "=r"(x[53]), "=r"(x[54]), "=r"(x[55]), "=r"(x[56]), "=r"(x[57]), "=r"(x[58]), "=r"(x[59]), "=r"(x[60]), "=r"(x[61]), "=r"(x[62]), "=r"(x[63]), "=r"(x[64]), "=r"(x[65]), "=r"(x[66]), "=r"(x[67]), "=r"(x[68]), "=r"(x[69]), "=r"(x[70]), "=r"(x[71]), "=r"(x[72]), "=r"(x[73]), "=r"(x[74]), "=r"(x[75]), "=r"(x[76]), "=r"(x[77]), "=r"(x[78]), "=r"(x[79]), "=r"(x[80]), "=r"(x[81]), "=r"(x[82]), "=r"(x[83]), "=r"(x[84]), "=r"(x[85]), "=r"(x[86]), "=r"(x[87]), "=r"(x[88]), "=r"(x[89]), "=r"(x[90]), "=r"(x[91]), "=r"(x[92]), "=r"(x[93]), "=r"(x[94]), "=r"(x[95]), "=r"(x[96]), "=r"(x[97]), "=r"(x[98]), "=r"(x[99]), "=r"(x[100]), "=r"(x[101]), "=r"(x[102]), "=r"(x[103]), "=r"(x[104]), "=r"(x[105]), "=r"(x[106]), "=r"(x[107]), "=r"(x[108]), "=r"(x[109]), "=r"(x[110]), "=r"(x[111]), "=r"(x[112]), "=r"(x[113]), "=r"(x[114]), "=r"(x[115]), "=r"(x[116]), "=r"(x[117]), "=r"(x[118]), "=r"(x[119]), "=r"(x[120]), "=r"(x[121]), "=r"(x[122]), "=r"(x[123]), "=r"(x[124]), "=r"(x[125]), "=r"(x[126]), "=r"(x[127])
+        : "r"(taddr)
         : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&x)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
-        W32(x)
-        : "memory");
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr), "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]), "r"(x[8]), "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15]), "r"(x[16]), "r"(x[17]), "r"(x[18]), "r"(x[19]), "r"(x[20]), "r"(x[21]), "r"(x[22]), "r"(x[23]), "r"(x[24]), "r"(x[25]), "r"(x[26]), "r"(x[27]), "r"(x[28]), "r"(x[29]), "r"(x[30]), "r"(x[31]) : "memory");
+}
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&x)[64]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n" ::"r"(taddr), "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]), "r"(x[8]), "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15]), "r"(x[16]), "r"(x[17]), "r"(x[18]), "r"(x[19]), "r"(x[20]), "r"(x[21]), "r"(x[22]), "r"(x[23]), "r"(x[24]), "r"(x[25]), "r"(x[26]), "r"(x[27]), "r"(x[28]), "r"(x[29]), "r"(x[30]), "r"(x[31]), "r"(x[32]), "r"(x[33]), "r"(x[34]), "r"(x[35]), "r"(x[36]), "r"(x[37]), "r"(x[38]), "r"(x[39]), "r"(x[40]), "r"(x[41]), "r"(x[42]), "r"(x[43]), "r"(x[44]), "r"(x[45]), "r"(x[46]), "r"(x[47]), "r"(x[48]), "r"(x[49]), "r"(x[50]), "r"(x[51]), "r"(x[52]), "r"(x[53]), "r"(x[54]), "r"(x[55]), "r"(x[56]), "r"(x[57]), "r"(x[58]), "r"(x[59]), "r"(x[60]), "r"(x[61]), "r"(x[62]), "r"(x[63]) : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -305,7 +305,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
+    if (warp >= 8) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
+        if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const CUtensorMap* qm = &p.qmap[r];
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 }
             }
         }
-    } else if (warp == 9) {
+        } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t S[NQT] = {tmem, tmem + 128};
@@ -402,7 +404,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             tc_commit(bar(B_OD));
             if (!ok) drain_phase(bar(B_OD), 0);   // every issued MMA has finished
         }
-    } else if (warp < 8) {
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
         // ------------------------------------------------------------ softmax
         const int t = warp >> 2, q4 = warp & 3;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -412,62 +416,65 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         const float c = p.c;
         float m_used = 0.f, l = 0.f;
         bool ok = true;
-        uint32_t x[32];
         for (int n = 0; n < ntiles; ++n) {
             ok = __all_sync(0xffffffffu, wait_phase(bar(B_SF + t), n & 1, ctl));
             if (!ok) break;
             tc_fence_after();
-            const int valid = min(BN, kvlen - n * BN);
-            // pass 1: row max of the tile's valid keys
-            float mx = -INFINITY;
+            uint32_t x[BN];
+            tmem_ld128(St, x);                       // the whole score row, one round trip
+            const int valid = kvlen - n * BN;
+            if (valid < BN) {                        // keys past the block: -inf
 #pragma unroll
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                tmem_ld32(St + cc * 32, x);
-                if (valid == BN) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(x[e]));
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (cc * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(x[e]));
-                }
+                for (int e = 0; e < BN; ++e)
+                    if (e >= valid) x[e] = 0xff800000u;
             }
+            // row max with 8 independent chains
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(x[e]);
+#pragma unroll
+            for (int e = 8; e < BN; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(x[e]));
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             const float mxs = mx * c;
+            float alpha = 1.f;
+            bool rescale = false;
             if (n == 0) {
                 m_used = mxs;
             } else if (__any_sync(0xffffffffu, mxs > m_used + 8.f)) {
-                // Raise the reference max and rescale O (the previous P V of
-                // this tile finished before this tile's S became ready).
+                // Raise the reference max; O is rescaled below, after P is
+                // written (this tile's P V is not issued before we arrive).
                 const float mnew = fmaxf(m_used, mxs);
-                const float alpha = ex2(m_used - mnew);
-                l *= alpha;
+                alpha = ex2(m_used - mnew);
                 m_used = mnew;
+                rescale = true;
+            }
+            // P = 2^(s*c - m), row sum with 8 independent chains, P over S
+            const float negm = -m_used;
+            float l8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) l8[e] = 0.f;
+            uint32_t pk[BN / 2];
+#pragma unroll
+            for (int e = 0; e < BN / 2; ++e) {
+                const float p0 = ex2(fmaf(__uint_as_float(x[2 * e]), c, negm));
+                const float p1 = ex2(fmaf(__uint_as_float(x[2 * e + 1]), c, negm));
+                l8[(2 * e) & 7] += p0;
+                l8[(2 * e + 1) & 7] += p1;
+                pk[e] = pack_p<P_BF16>(p0, p1);
+            }
+            tmem_st64(St, pk);
+            l = fmaf(l, alpha, ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+            if (rescale) {
+                // the previous P V of this tile completed before S became ready
 #pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
-                    tmem_ld32(Ot + cc * 32, x);
+                    uint32_t y[32];
+                    tmem_ld32(Ot + cc * 32, y);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha);
-                    tmem_st32(Ot + cc * 32, x);
+                    for (int e = 0; e < 32; ++e) y[e] = __float_as_uint(__uint_as_float(y[e]) * alpha);
+                    tmem_st32(Ot + cc * 32, y);
                 }
-            }
-            // pass 2: P = 2^(s*c - m), row sum, P written over S as 16-bit pairs
-#pragma unroll
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                tmem_ld32(St + cc * 32, x);
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float a0 = fmaf(__uint_as_float(x[2 * e]), c, -m_used);
-                    float a1 = fmaf(__uint_as_float(x[2 * e + 1]), c, -m_used);
-                    if (valid != BN) {
-                        if (cc * 32 + 2 * e >= valid) a0 = -INFINITY;
-                        if (cc * 32 + 2 * e + 1 >= valid) a1 = -INFINITY;
-                    }
-                    const float p0 = ex2(a0), p1 = ex2(a1);
-                    l += p0 + p1;
-                    pk[e] = pack_p<P_BF16>(p0, p1);
-                }
-                tmem_st16(St + cc * 16, pk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -480,17 +487,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             const float inv = 1.f / l;
             const bool live = row < qlen;
             char* orow = obase + (long long)(live ? row : 0) * p.o.stride_s * eb;
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                tmem_ld32(Ot + cc * 32, x);
-                if (live) {
+            uint32_t x[D];
+            if constexpr (D == 128) tmem_ld128(Ot, x); else tmem_ld64(Ot, x);
+            if (live) {
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        Vec8 v;
+                for (int q8 = 0; q8 < D / 8; ++q8) {
+                    Vec8 v;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v.f[e] = __uint_as_float(x[q8 * 8 + e]) * inv;
-                        store8(orow + (cc * 32 + q8 * 8) * eb, p.o_dt, v);
-                    }
+                    for (int e = 0; e < 8; ++e) v.f[e] = __uint_as_float(x[q8 * 8 + e]) * inv;
+                    store8(orow + q8 * 8 * eb, p.o_dt, v);
                 }
             }
             if (live && lbase) lbase[row] = (m_used + log2f(l)) * 0.69314718055994531f;
