@@ -19,35 +19,44 @@ namespace ditsp {
 namespace {
 
 // ---------------------------------------------------------------------------
-// CFG: each thread moves 8 elements per step; 4 steps are issued before any
-// store so that enough loads are in flight to cover HBM latency.
-__global__ void __launch_bounds__(256) cfg_vec_kernel(const char* __restrict__ pred, dit_dtype in_dt,
-                                                      long long nvec, long long N, float g,
-                                                      char* __restrict__ out, dit_dtype out_dt) {
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    const int ib = 8 * dtype_bytes(in_dt), ob = 8 * dtype_bytes(out_dt);
-    const char* cond = pred + N * dtype_bytes(in_dt);
-    const bool g_one = (g == 1.0f);
-    for (long long v0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; v0 < nvec; v0 += 4 * stride) {
-        Vec8 u[4], c[4];
+// CFG: a one-shot grid (no grid-stride loop); each thread combines four
+// 8-element vectors spaced one block apart (coalesced), issuing all eight
+// 16-byte loads before any arithmetic.
+constexpr int kCfgThreads = 256;
+constexpr int kCfgVecs = 4;
+
+template <int IB>   // input element bytes
+__global__ void __launch_bounds__(kCfgThreads) cfg_vec_kernel(const char* __restrict__ pred, dit_dtype in_dt,
+                                                              long long nvec, long long N, float g,
+                                                              char* __restrict__ out, dit_dtype out_dt) {
+    const long long base = (long long)blockIdx.x * (kCfgThreads * kCfgVecs) + threadIdx.x;
+    const char* cond = pred + N * IB;
+    uint4 ru[kCfgVecs][IB / 2], rc[kCfgVecs][IB / 2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const long long v = v0 + k * stride;
-            if (v < nvec) {
-                load8(pred + v * ib, in_dt, u[k]);
-                load8(cond + v * ib, in_dt, c[k]);
+    for (int k = 0; k < kCfgVecs; ++k) {
+        const long long v = base + (long long)k * kCfgThreads;
+        if (v < nvec) {
+#pragma unroll
+            for (int h = 0; h < IB / 2; ++h) {
+                ru[k][h] = reinterpret_cast<const uint4*>(pred + v * 8 * IB)[h];
+                rc[k][h] = reinterpret_cast<const uint4*>(cond + v * 8 * IB)[h];
             }
         }
+    }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const long long v = v0 + k * stride;
-            if (v < nvec) {
-                Vec8 p;
+    for (int k = 0; k < kCfgVecs; ++k) {
+        const long long v = base + (long long)k * kCfgThreads;
+        if (v < nvec) {
+            Vec8 u, c, p;
+            load8(&ru[k][0], in_dt, u);
+            load8(&rc[k][0], in_dt, c);
+            if (g == 1.0f) {
+                p = c;
+            } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    p.f[e] = g_one ? c[k].f[e] : fmaf(g, c[k].f[e] - u[k].f[e], u[k].f[e]);
-                store8(out + v * ob, out_dt, p);
+                for (int e = 0; e < 8; ++e) p.f[e] = fmaf(g, c.f[e] - u.f[e], u.f[e]);
             }
+            store8(out + v * 8 * dtype_bytes(out_dt), out_dt, p);
         }
     }
 }
@@ -75,8 +84,9 @@ __global__ void cfg_scalar_kernel(const char* __restrict__ pred, dit_dtype in_dt
 }
 
 // ---------------------------------------------------------------------------
-// Merge: one thread per 8 consecutive d of one (r, b, i, h) row.  Grid y is
-// (r, b); x covers rows * heads * D/8 of the longest block.
+// Merge: one thread per 8 consecutive d of one (r, b, i, h) row, no
+// grid-stride loop.  Grid y is (r, b); x covers rows * heads * D/8 of the
+// longest block.
 struct MergeArgs {
     int B, H, D, n_parts;
     int q_len[DIT_MAX_R];
@@ -93,8 +103,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
     const int chunks = a.D >> 3;
     const long long per_row = (long long)a.H * chunks;
     const long long total = (long long)a.q_len[r] * per_row;
-    for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total;
-         t += (long long)gridDim.x * blockDim.x) {
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < total) {
         const int i = (int)(t / per_row);
         const int rem = (int)(t - (long long)i * per_row);
         const int h = rem / chunks, c = rem - h * chunks;
@@ -159,10 +169,13 @@ extern "C" dit_status dit_cfg_combine(const void* pred, dit_dtype in_dt, int64_t
     if (vec_ok) {
         const long long nvec = N / 8;
         if (nvec > 0) {
-            long long blocks = (nvec + 255) / 256;
-            const long long cap = (long long)num_sms() * 8;
-            if (blocks > cap) blocks = cap;
-            cfg_vec_kernel<<<(unsigned)blocks, 256, 0, st>>>(pb, in_dt, nvec, N, g, static_cast<char*>(out), out_dt);
+            const long long blocks = (nvec + kCfgThreads * kCfgVecs - 1) / (kCfgThreads * kCfgVecs);
+            if (in_dt == DIT_F32)
+                cfg_vec_kernel<4><<<(unsigned)blocks, kCfgThreads, 0, st>>>(pb, in_dt, nvec, N, g,
+                                                                            static_cast<char*>(out), out_dt);
+            else
+                cfg_vec_kernel<2><<<(unsigned)blocks, kCfgThreads, 0, st>>>(pb, in_dt, nvec, N, g,
+                                                                            static_cast<char*>(out), out_dt);
             dit_status s = check_launch(who);
             if (s != DIT_OK) return s;
         }
@@ -209,9 +222,7 @@ extern "C" dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int
     a.parts = parts; a.parts_dt = parts_dt; a.lse_parts = lse_parts;
     a.out = out; a.out_dt = out_dt; a.lse_out = lse_out;
     const long long work = (long long)maxq * H * (D / 8);
-    long long bx = (work + 255) / 256;
-    const long long cap = (long long)num_sms() * 8;
-    if (bx > cap) bx = cap;
+    const long long bx = (work + 255) / 256;     // one thread per 8 outputs
     dim3 grid((unsigned)bx, (unsigned)(n_q * B));
     if (grid.y > 65535) return fail(DIT_ERR_UNSUPPORTED, "%s: n_q * B too large", who);
     merge_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(a);

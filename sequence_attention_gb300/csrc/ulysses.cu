@@ -15,6 +15,8 @@
 //      index  np*B*U*off_r + v*np*B*S_r + np*B*(off_u-off_r) + (p*B+b)*L_u + i
 // Seq-to-head: pack writes A, the exchange copies A->B, unpack reads B.
 // Head-to-seq: pack writes B, the exchange copies B->A, unpack reads A.
+// Each kernel walks the runs in its destination's order (A, B, head-layout
+// or sequence order), so its writes are sequential and its reads gather.
 #include <string.h>
 
 #include "common.cuh"
@@ -55,45 +57,83 @@ __device__ __forceinline__ int ring_of_row(const dit_sp_layout& L, int t) {
     return r;
 }
 
-__device__ __forceinline__ Run decode_A(const dit_sp_layout& L, int np, long long a) {
-    const long long per_row = (long long)np * L.B * L.U;
-    const int rid = rank_of_row(L, (int)(a / per_row));
+// Run index -> (r, u, v, p, b, i).  All run counts fit in 32 bits (checked
+// on the host), so the divisions here are 32-bit.
+__device__ __forceinline__ Run decode_A(const dit_sp_layout& L, int np, int a) {
+    const int per_row = np * L.B * L.U;
+    const int rid = rank_of_row(L, a / per_row);
     Run x;
-    x.r = rid / L.U; x.u = rid % L.U;
-    const long long Lu = L.rank_len[rid];
-    long long local = a - per_row * L.rank_off[rid];
-    const long long blk = (long long)np * L.B * Lu;
-    x.v = (int)(local / blk);
-    long long rem = local - x.v * blk;
-    const int pb = (int)(rem / Lu);
-    x.i = (int)(rem - pb * Lu);
-    x.p = pb / L.B; x.b = pb % L.B;
+    x.r = rid / L.U; x.u = rid - x.r * L.U;
+    const int Lu = L.rank_len[rid];
+    const int local = a - per_row * L.rank_off[rid];
+    const int blk = np * L.B * Lu;
+    x.v = local / blk;
+    const int rem = local - x.v * blk;
+    const int pb = rem / Lu;
+    x.i = rem - pb * Lu;
+    x.p = pb / L.B; x.b = pb - x.p * L.B;
     return x;
 }
 
-__device__ __forceinline__ Run decode_B(const dit_sp_layout& L, int np, long long bi) {
-    const long long per_row = (long long)np * L.B * L.U;
+__device__ __forceinline__ Run decode_B(const dit_sp_layout& L, int np, int bi) {
+    const int per_row = np * L.B * L.U;
     Run x;
-    x.r = ring_of_row(L, (int)(bi / per_row));
+    x.r = ring_of_row(L, bi / per_row);
     const int offr = L.ring_off[x.r];
-    const long long Sr = L.ring_len[x.r];
-    long long local = bi - per_row * offr;
-    const long long grp = (long long)np * L.B * Sr;
-    x.v = (int)(local / grp);
-    long long rem = local - x.v * grp;
-    const int rid = rank_of_row(L, offr + (int)(rem / ((long long)np * L.B)));
+    const int grp = np * L.B * L.ring_len[x.r];
+    const int local = bi - per_row * offr;
+    x.v = local / grp;
+    int rem = local - x.v * grp;
+    const int rid = rank_of_row(L, offr + rem / (np * L.B));
     x.u = rid - x.r * L.U;
-    const long long Lu = L.rank_len[rid];
-    rem -= (long long)np * L.B * (L.rank_off[rid] - offr);
-    const int pb = (int)(rem / Lu);
-    x.i = (int)(rem - pb * Lu);
-    x.p = pb / L.B; x.b = pb % L.B;
+    const int Lu = L.rank_len[rid];
+    rem -= np * L.B * (L.rank_off[rid] - offr);
+    const int pb = rem / Lu;
+    x.i = rem - pb * Lu;
+    x.p = pb / L.B; x.b = pb - x.p * L.B;
+    return x;
+}
+
+// Head-layout order (destination order of the seq->head unpack): runs of
+// plane p enumerated as (r, b, row of ring block r, v), so consecutive runs
+// fill one head-layout row.
+__device__ __forceinline__ Run decode_H(const dit_sp_layout& L, int np, int h) {
+    const int per_plane = L.B * L.S * L.U;
+    Run x;
+    x.p = h / per_plane;
+    const int rem = h - x.p * per_plane;
+    x.r = ring_of_row(L, rem / (L.B * L.U));
+    const int offr = L.ring_off[x.r], Sr = L.ring_len[x.r];
+    const int local = rem - L.B * L.U * offr;
+    x.b = local / (Sr * L.U);
+    const int rem2 = local - x.b * Sr * L.U;
+    const int row = rem2 / L.U;
+    x.v = rem2 - row * L.U;
+    const int rid = rank_of_row(L, offr + row);
+    x.u = rid - x.r * L.U;
+    x.i = offr + row - L.rank_off[rid];
+    return x;
+}
+
+// Sequence order (destination order of the head->seq unpack, one plane):
+// runs enumerated as (b, token, v), so consecutive runs fill one token row.
+__device__ __forceinline__ Run decode_S(const dit_sp_layout& L, int s) {
+    Run x;
+    x.p = 0;
+    const int bt = s / L.U;
+    x.v = s - bt * L.U;
+    x.b = bt / L.S;
+    const int t = bt - x.b * L.S;
+    const int rid = rank_of_row(L, t);
+    x.r = rid / L.U;
+    x.u = rid - x.r * L.U;
+    x.i = t - L.rank_off[rid];
     return x;
 }
 
 __device__ __forceinline__ long long index_A(const dit_sp_layout& L, int np, const Run& x) {
     const int rid = x.r * L.U + x.u;
-    const long long Lu = L.rank_len[rid];
+    const int Lu = L.rank_len[rid];
     return (long long)np * L.B * L.U * L.rank_off[rid] + (long long)x.v * np * L.B * Lu +
            ((long long)x.p * L.B + x.b) * Lu + x.i;
 }
@@ -123,113 +163,157 @@ __device__ __forceinline__ bool narrowing(dit_dtype s, dit_dtype d) {
     return (s == DIT_F32 && d != DIT_F32) || (s == DIT_BF16 && d == DIT_F16);
 }
 
+// Where one run comes from and goes to (chunk = 8 elements).
+struct RunIO {
+    const char* src;
+    char* dst;
+    int src_lim;      // chunks of the source holding data; later chunks read as zero
+    int dst_lim;      // chunks of the destination written; later chunks skipped
+    int sdt, ddt;     // dit_dtype of source and destination
+};
+
 template <int MODE>
-__global__ void __launch_bounds__(256, 4) run_kernel(const __grid_constant__ RunArgs A) {
+__device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
     const dit_sp_layout& L = A.L;
-    const int lane = threadIdx.x & 31;
-    const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-    const int run_elems = L.Hl * L.D;
-    const int nch = run_elems >> 3;
-    bool overflow = false;
+    // Every kernel enumerates runs in the order of its destination, so that
+    // consecutive runs write consecutive memory.
+    Run x;
+    if (MODE == PACK_S2H || MODE == A2A_H2S) x = decode_A(L, A.np, ri);
+    else if (MODE == UNPACK_S2H) x = decode_H(L, A.np, ri);
+    else if (MODE == UNPACK_H2S) x = decode_S(L, ri);
+    else x = decode_B(L, A.np, ri);
+    const int p = x.p;
+    const long long run_elems = (long long)L.Hl * L.D;
+    // real heads of this head group; heads at or past nreal are padding
+    const int nreal = min(max(L.H - x.v * L.Hl, 0), L.Hl);
+    const int full = (L.Hl * L.D) >> 3, real = (nreal * L.D) >> 3;
+    RunIO io;
+    io.src_lim = io.dst_lim = full;
+    long long so = 0, doff = 0;
+    dit_dtype sdt, ddt;
+    if (MODE == PACK_S2H) {
+        sdt = A.src_dt[p]; ddt = A.dst_dt[0];
+        so = nreal > 0 ? seq_offset(L, x) : 0; doff = ri * run_elems;
+        io.src = (const char*)A.src[p]; io.dst = (char*)A.dst[0];
+        io.src_lim = real;
+    } else if (MODE == UNPACK_H2S) {
+        sdt = A.src_dt[0]; ddt = A.dst_dt[0];
+        so = index_A(L, A.np, x) * run_elems; doff = nreal > 0 ? seq_offset(L, x) : 0;
+        io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[0];
+        io.dst_lim = real;
+    } else if (MODE == PACK_H2S) {
+        sdt = A.src_dt[0]; ddt = A.dst_dt[0];
+        so = head_offset(L, x); doff = ri * run_elems;
+        io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[0];
+        io.src_lim = real;
+    } else if (MODE == UNPACK_S2H) {
+        sdt = A.src_dt[0]; ddt = A.dst_dt[p];
+        so = index_B(L, A.np, x) * run_elems; doff = head_offset(L, x);
+        io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[p];
+    } else if (MODE == A2A_S2H) {
+        sdt = ddt = A.src_dt[0];
+        so = index_A(L, A.np, x) * run_elems; doff = ri * run_elems;
+        io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[0];
+    } else {  // A2A_H2S
+        sdt = ddt = A.src_dt[0];
+        so = index_B(L, A.np, x) * run_elems; doff = ri * run_elems;
+        io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[0];
+    }
+    io.src += so * dtype_bytes(sdt);
+    io.dst += doff * dtype_bytes(ddt);
+    io.sdt = sdt;
+    io.ddt = ddt;
+    return io;
+}
 
-    for (long long ri = warp0; ri < A.nruns; ri += nwarps) {
-        Run x;
-        if (MODE == PACK_S2H || MODE == UNPACK_H2S || MODE == A2A_H2S) x = decode_A(L, A.np, ri);
-        else x = decode_B(L, A.np, ri);
-        const int p = x.p;
-        // real heads of this head group; heads at or past nreal are padding
-        const int nreal = min(max(L.H - x.v * L.Hl, 0), L.Hl);
-
-        const char* src;
-        char* dst;
-        dit_dtype sdt, ddt;
-        int src_heads = L.Hl;   // source heads that hold data (rest read as 0)
-        int dst_heads = L.Hl;   // destination heads that are written
-        long long so = 0, doff = 0;
-        if (MODE == PACK_S2H) {
-            sdt = A.src_dt[p]; ddt = A.dst_dt[0];
-            so = nreal > 0 ? seq_offset(L, x) : 0; doff = ri * run_elems;
-            src = (const char*)A.src[p]; dst = (char*)A.dst[0];
-            src_heads = nreal;
-        } else if (MODE == UNPACK_H2S) {
-            sdt = A.src_dt[0]; ddt = A.dst_dt[0];
-            so = ri * run_elems; doff = nreal > 0 ? seq_offset(L, x) : 0;
-            src = (const char*)A.src[0]; dst = (char*)A.dst[0];
-            dst_heads = nreal;
-        } else if (MODE == PACK_H2S) {
-            sdt = A.src_dt[0]; ddt = A.dst_dt[0];
-            so = head_offset(L, x); doff = ri * run_elems;
-            src = (const char*)A.src[0]; dst = (char*)A.dst[0];
-            src_heads = nreal;
-        } else if (MODE == UNPACK_S2H) {
-            sdt = A.src_dt[0]; ddt = A.dst_dt[p];
-            so = ri * run_elems; doff = head_offset(L, x);
-            src = (const char*)A.src[0]; dst = (char*)A.dst[p];
-        } else if (MODE == A2A_S2H) {
-            sdt = ddt = A.src_dt[0];
-            so = index_A(L, A.np, x) * run_elems; doff = ri * run_elems;
-            src = (const char*)A.src[0]; dst = (char*)A.dst[0];
-        } else {  // A2A_H2S
-            sdt = ddt = A.src_dt[0];
-            so = index_B(L, A.np, x) * run_elems; doff = ri * run_elems;
-            src = (const char*)A.src[0]; dst = (char*)A.dst[0];
+// Convert 8 elements held in registers (SB bytes each) to the destination
+// encoding (DB bytes each); narrowing rounds to nearest even.  With `check`,
+// a finite value that becomes infinite sets `overflow`.
+template <int SB, int DB>
+__device__ __forceinline__ void convert8(const uint4 (&in)[SB / 2], dit_dtype sdt, dit_dtype ddt, bool check,
+                                         uint4 (&out)[DB / 2], bool& overflow) {
+    if (sdt == ddt) {
+#pragma unroll
+        for (int h = 0; h < DB / 2; ++h) out[h] = in[h < SB / 2 ? h : 0];
+        return;
+    }
+    Vec8 v;
+    load8(&in[0], sdt, v);
+    if constexpr (DB == 4) {
+        out[0] = make_uint4(__float_as_uint(v.f[0]), __float_as_uint(v.f[1]), __float_as_uint(v.f[2]),
+                            __float_as_uint(v.f[3]));
+        out[1] = make_uint4(__float_as_uint(v.f[4]), __float_as_uint(v.f[5]), __float_as_uint(v.f[6]),
+                            __float_as_uint(v.f[7]));
+    } else {
+        out[0] = make_uint4(pack2(v.f[0], v.f[1], ddt), pack2(v.f[2], v.f[3], ddt),
+                            pack2(v.f[4], v.f[5], ddt), pack2(v.f[6], v.f[7], ddt));
+        if (check) {
+            Vec8 back;
+            load8(&out[0], ddt, back);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) overflow |= isinf(back.f[e]) && !isinf(v.f[e]);
         }
-        src += so * dtype_bytes(sdt);
-        dst += doff * dtype_bytes(ddt);
-        const int sb = 8 * dtype_bytes(sdt), db = 8 * dtype_bytes(ddt);
-        const bool same = (sdt == ddt);
-        const bool check_range = (MODE == UNPACK_S2H) && A.range_flag && narrowing(sdt, ddt);
+    }
+}
 
-        if (same) {
-            // bit-exact move: 16 (or 32) bytes per chunk, four chunks in flight
-            for (int c0 = lane; c0 < nch; c0 += 128) {
-                uint4 raw[4][2];
+constexpr int kThreads = 256;
+constexpr int kItems = 8;       // 8-element items per lane in flight
+
+// Each block takes 8 * rpw consecutive runs (rpw = runs per warp, 4, or 2
+// for small exchanges): threads decode
+// one run each into shared memory, then each warp streams its rpw runs,
+// lanes over their 8-element chunks.  Per group of kItems items a lane
+// issues every load first, converts in registers, then stores.
+template <int MODE, int SB, int DB>
+__global__ void __launch_bounds__(kThreads) run_kernel(const __grid_constant__ RunArgs A, int rpw) {
+    __shared__ RunIO ios[kThreads];
+    const int rpb = rpw * (kThreads / 32);
+    const long long r0 = (long long)blockIdx.x * rpb;
+    const int nrun = (int)min((long long)rpb, A.nruns - r0);
+    if ((int)threadIdx.x < nrun) ios[threadIdx.x] = run_io<MODE>(A, (int)(r0 + threadIdx.x));
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g0 = warp * rpw;
+    const int gn = min(rpw, nrun - g0);
+    if (gn <= 0) return;
+    const int nch = (A.L.Hl * A.L.D) >> 3;
+    const int items = gn * nch;
+    const bool want_check = (MODE == UNPACK_S2H) && A.range_flag != nullptr;
+    bool overflow = false;
+    int g = lane / nch, c = lane - (lane / nch) * nch;   // item k0 = lane
+    for (int k0 = lane; k0 < items; k0 += 32 * kItems) {
+        uint4 raw[kItems][SB / 2];
+        int gi[kItems], ci[kItems];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int c = c0 + 32 * k;
-                    raw[k][0] = raw[k][1] = make_uint4(0, 0, 0, 0);
-                    if (c < nch && (c * 8) / L.D < src_heads) {
-                        const uint4* q = reinterpret_cast<const uint4*>(src + (long long)c * sb);
-                        raw[k][0] = q[0];
-                        if (sb == 32) raw[k][1] = q[1];
-                    }
-                }
+        for (int t = 0; t < kItems; ++t) {
+            gi[t] = g; ci[t] = c;
+            c += 32;
+            while (c >= nch) { c -= nch; ++g; }
+        }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int c = c0 + 32 * k;
-                    if (c < nch && (c * 8) / L.D < dst_heads) {
-                        uint4* q = reinterpret_cast<uint4*>(dst + (long long)c * db);
-                        q[0] = raw[k][0];
-                        if (db == 32) q[1] = raw[k][1];
-                    }
+        for (int t = 0; t < kItems; ++t) {
+#pragma unroll
+            for (int h = 0; h < SB / 2; ++h) raw[t][h] = make_uint4(0, 0, 0, 0);
+            if (k0 + 32 * t < items) {
+                const RunIO& io = ios[g0 + gi[t]];
+                if (ci[t] < io.src_lim) {
+                    const uint4* q = reinterpret_cast<const uint4*>(io.src + (long long)ci[t] * 8 * SB);
+#pragma unroll
+                    for (int h = 0; h < SB / 2; ++h) raw[t][h] = q[h];
                 }
             }
-        } else {
-            // converting move: through fp32, rounded to nearest even
-            for (int c0 = lane; c0 < nch; c0 += 64) {
-                Vec8 val[2];
+        }
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int c = c0 + 32 * k;
+        for (int t = 0; t < kItems; ++t) {
+            if (k0 + 32 * t < items) {
+                const RunIO& io = ios[g0 + gi[t]];
+                if (ci[t] < io.dst_lim) {
+                    const dit_dtype sdt = (dit_dtype)io.sdt, ddt = (dit_dtype)io.ddt;
+                    uint4 o[DB / 2];
+                    convert8<SB, DB>(raw[t], sdt, ddt, want_check && narrowing(sdt, ddt), o, overflow);
+                    uint4* q = reinterpret_cast<uint4*>(io.dst + (long long)ci[t] * 8 * DB);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) val[k].f[e] = 0.f;
-                    if (c < nch && (c * 8) / L.D < src_heads) load8(src + (long long)c * sb, sdt, val[k]);
-                }
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int c = c0 + 32 * k;
-                    if (c < nch && (c * 8) / L.D < dst_heads) {
-                        char* d = dst + (long long)c * db;
-                        store8(d, ddt, val[k]);
-                        if (check_range) {
-                            Vec8 back;
-                            load8(d, ddt, back);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                overflow |= isinf(back.f[e]) && !isinf(val[k].f[e]);
-                        }
-                    }
+                    for (int h = 0; h < DB / 2; ++h) q[h] = o[h];
                 }
             }
         }
@@ -255,14 +339,38 @@ dit_status check_layout(const dit_sp_layout* L, const char* who) {
     return DIT_OK;
 }
 
+template <int MODE, int SB, int DB>
+dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
+    // 4 runs per warp keep each block's fixed decode latency small against
+    // its copy time; drop to 2 only when the grid would otherwise have fewer
+    // than two blocks per resident block slot
+    const long long slots = (long long)num_sms() * 3;
+    int rpw = 4;
+    if ((a.nruns + 31) / 32 < 2 * slots) rpw = 2;
+    const long long blocks = (a.nruns + 8LL * rpw - 1) / (8LL * rpw);
+    run_kernel<MODE, SB, DB><<<(unsigned)blocks, kThreads, 0, st>>>(a, rpw);
+    return check_launch(who);
+}
+
+// Element sizes are template parameters so that 16-bit paths hold 16-byte
+// items; every plane of one call must use source (and destination) types
+// of one size.
 template <int MODE>
 dit_status launch_runs(const RunArgs& a, cudaStream_t st, const char* who) {
     if (a.nruns == 0) return DIT_OK;
-    long long blocks = (a.nruns + 7) / 8;
-    const long long cap = (long long)num_sms() * 16;
-    if (blocks > cap) blocks = cap;
-    run_kernel<MODE><<<(unsigned)blocks, 256, 0, st>>>(a);
-    return check_launch(who);
+    if (a.nruns >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 2^31 runs", who);
+    const int sb = dtype_bytes(a.src_dt[0]);
+    const int db = dtype_bytes(a.dst_dt[0]);
+    for (int p = 1; p < 3; ++p) {
+        if (a.src[p] && dtype_bytes(a.src_dt[p]) != sb)
+            return fail(DIT_ERR_UNSUPPORTED, "%s: planes of one call need source types of one size", who);
+        if (a.dst[p] && dtype_bytes(a.dst_dt[p]) != db)
+            return fail(DIT_ERR_UNSUPPORTED, "%s: planes of one call need destination types of one size", who);
+    }
+    if (sb == 2 && db == 2) return launch_sized<MODE, 2, 2>(a, st, who);
+    if (sb == 4 && db == 4) return launch_sized<MODE, 4, 4>(a, st, who);
+    if (sb == 4 && db == 2) return launch_sized<MODE, 4, 2>(a, st, who);
+    return launch_sized<MODE, 2, 4>(a, st, who);
 }
 
 }  // namespace
