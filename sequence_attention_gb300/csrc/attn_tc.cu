@@ -9,12 +9,14 @@
 // CTA = 256 query rows as two 128-row tiles, one (r, j, b, h).  Warp roles:
 //   warps 0-3  softmax for Q tile 0 (TMEM lanes 0-127, one row per thread)
 //   warps 4-7  softmax for Q tile 1
-//   warp  8    TMA producer: Q once, then K and V tiles into a 2-stage ring
+//   warp  8    TMA producer of Q (once) and K tiles (2-stage ring)
 //   warp  9    MMA issuer (one thread): S = Q K^T and O += P V
-//   warps 10-11 idle (they complete the third warpgroup)
+//   warp  10   TMA producer of V tiles (3-stage ring); K and V loads wait on
+//              their own ring's releases, so neither holds up the other
+//   warp  11   idle (completes the third warpgroup)
 // Registers: launched at 168 per thread; the producer/MMA warpgroup gives
-// back down to 72 and the two softmax warpgroups take 216 each
-// (2*216 + 72 = 3*168), enough to hold a whole 128-column score row.
+// back down to 88 and the two softmax warpgroups take 208 each
+// (2*208 + 88 = 3*168), enough to hold a whole 128-column score row.
 // TMEM (512 columns x 128 lanes, fp32): S0 [0,128) S1 [128,256)
 // O0 [256,256+D) O1 [256+D,256+2D).  P (16-bit) overwrites the first half
 // of its tile's S columns and feeds the P V MMA straight from TMEM.
@@ -50,12 +52,13 @@ namespace {
 constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 128;          // keys per tile (MMA N of Q K^T, K of P V)
 constexpr int NQT = 2;           // query tiles per CTA
-constexpr int NST = 2;           // K and V pipeline stages
+constexpr int NSK = 2;           // K pipeline stages
+constexpr int NSV = 3;           // V pipeline stages
 constexpr int NTHREADS = 384;
 constexpr int CHUNK = BM * 128;  // bytes of one 64-column (128-byte) swizzle chunk
 constexpr unsigned long long kWaitNs = 4000000000ull;
 
-enum { B_Q = 0, B_KF = 1, B_KE = 3, B_VF = 5, B_VE = 7, B_SF = 9, B_PF = 11, B_OD = 13, NBAR = 14 };
+enum { B_Q = 0, B_KF = 1, B_KE = 3, B_VF = 5, B_VE = 8, B_SF = 11, B_PF = 13, B_OD = 15, NBAR = 16 };
 
 struct TcParams {
     CUtensorMap qmap[DIT_MAX_R];
@@ -74,7 +77,7 @@ struct TcParams {
 
 template <int D>
 constexpr int smem_bytes() {
-    return (NQT + 2 * NST) * BM * D * 2 + NBAR * 8 + 16 + 1024;
+    return (NQT + NSK + NSV) * BM * D * 2 + NBAR * 8 + 16 + 1024;
 }
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -214,6 +217,12 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&x)[64
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -239,8 +248,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
     uint8_t* sK = sQ + NQT * TILE;
-    uint8_t* sV = sK + NST * TILE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NST * TILE);
+    uint8_t* sV = sK + NSK * TILE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NSV * TILE);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -279,9 +288,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q), 1);
-        for (int s = 0; s < NST; ++s) {
+        for (int s = 0; s < NSK; ++s) {
             mbar_init(bar(B_KF + s), 1);
             mbar_init(bar(B_KE + s), 1);
+        }
+        for (int s = 0; s < NSV; ++s) {
             mbar_init(bar(B_VF + s), 1);
             mbar_init(bar(B_VE + s), 1);
         }
@@ -306,43 +317,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
 
     if (warp >= 8) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
-        if (warp == 8) {
-        // ------------------------------------------------------------ producer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+        if (warp == 8 || warp == 10) {
+        // ------------------------------------------------------------ producers
         if (lane == 0) {
-            const CUtensorMap* qm = &p.qmap[r];
-            const CUtensorMap* km = &p.kmap[j];
-            const CUtensorMap* vm = &p.vmap[j];
-            mbar_expect_tx(bar(B_Q), NQT * TILE);
-            for (int t = 0; t < NQT; ++t)
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_4d(su32(sQ + t * TILE + c * CHUNK), qm, c * 64, h, row_base + t * BM, b, bar(B_Q));
+            const bool is_k = (warp == 8);
+            const CUtensorMap* map = is_k ? &p.kmap[j] : &p.vmap[j];
+            const int nst = is_k ? NSK : NSV;
+            const int full = is_k ? B_KF : B_VF, empty = is_k ? B_KE : B_VE;
+            uint8_t* ring = is_k ? sK : sV;
+            if (is_k) {
+                const CUtensorMap* qm = &p.qmap[r];
+                mbar_expect_tx(bar(B_Q), NQT * TILE);
+                for (int t = 0; t < NQT; ++t)
+                    for (int c = 0; c < NCH; ++c)
+                        tma_load_4d(su32(sQ + t * TILE + c * CHUNK), qm, c * 64, h, row_base + t * BM, b, bar(B_Q));
+            }
             int issued = 0;
             bool ok = true;
-            for (int n = 0; n < ntiles && ok; ++n) {
-                const int s = n % NST;
-                const uint32_t ph = (n / NST) & 1;
-                if (n >= NST && !(ok = wait_phase(bar(B_KE + s), ph ^ 1, ctl))) break;
-                mbar_expect_tx(bar(B_KF + s), TILE);
+            for (int n = 0; n < ntiles; ++n) {
+                const int s = n % nst;
+                const uint32_t ph = (n / nst) & 1;
+                if (n >= nst && !(ok = wait_phase(bar(empty + s), ph ^ 1, ctl))) break;
+                mbar_expect_tx(bar(full + s), TILE);
                 for (int c = 0; c < NCH; ++c)
-                    tma_load_4d(su32(sK + s * TILE + c * CHUNK), km, c * 64, h, n * BN, b, bar(B_KF + s));
-                if (n >= NST && !(ok = wait_phase(bar(B_VE + s), ph ^ 1, ctl))) {
-                    // K of tile n is in flight but V is not: drain K only
-                    drain_phase(bar(B_KF + s), ph);
-                    break;
-                }
-                mbar_expect_tx(bar(B_VF + s), TILE);
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_4d(su32(sV + s * TILE + c * CHUNK), vm, c * 64, h, n * BN, b, bar(B_VF + s));
+                    tma_load_4d(su32(ring + s * TILE + c * CHUNK), map, c * 64, h, n * BN, b, bar(full + s));
                 issued = n + 1;
             }
             if (!ok || *abort_flag) {
                 // let every copy this thread issued land before smem is released
-                drain_phase(bar(B_Q), 0);
-                for (int n = issued > NST ? issued - NST : 0; n < issued; ++n) {
-                    drain_phase(bar(B_KF + n % NST), (n / NST) & 1);
-                    drain_phase(bar(B_VF + n % NST), (n / NST) & 1);
-                }
+                if (is_k) drain_phase(bar(B_Q), 0);
+                for (int n = issued > nst ? issued - nst : 0; n < issued; ++n)
+                    drain_phase(bar(full + n % nst), (n / nst) & 1);
             }
         }
         } else if (warp == 9) {
@@ -350,22 +356,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         if (lane == 0) {
             const uint32_t S[NQT] = {tmem, tmem + 128};
             const uint32_t O[NQT] = {tmem + 256, tmem + 256 + D};
+            // Descriptors are built once; a k-step only adds an offset (in
+            // 16-byte units) to the start-address field.  Stage buffers are
+            // selected with (s ? x1 : x0), never by indexing an array.
+            static_assert(NQT == 2 && NSK == 2 && NSV == 3, "descriptor selection assumes 2 tiles, 2+3 stages");
+            const uint64_t qd0 = sdesc(su32(sQ), 16, 1024), qd1 = sdesc(su32(sQ + TILE), 16, 1024);
+            const uint64_t kd0 = sdesc(su32(sK), 16, 1024), kd1 = sdesc(su32(sK + TILE), 16, 1024);
+            // V tile rows are keys (K dim), 64-wide d chunks CHUNK apart (N dim)
+            const uint64_t vd0 = sdesc(su32(sV), CHUNK, 1024), vd1 = sdesc(su32(sV + TILE), CHUNK, 1024),
+                           vd2 = sdesc(su32(sV + 2 * TILE), CHUNK, 1024);
+            const uint32_t idesc_qk = p.idesc_qk, idesc_pv = p.idesc_pv;
             auto issue_qk = [&](int t, int s) {
+                const uint64_t a0 = t ? qd1 : qd0, b0 = s ? kd1 : kd0;
+                const uint32_t d = t ? S[1] : S[0];
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks & 3) * 32 + (ks >> 2) * CHUNK;
-                    const uint64_t a = sdesc(su32(sQ + t * TILE) + off, 16, 1024);
-                    const uint64_t bd = sdesc(su32(sK + s * TILE) + off, 16, 1024);
-                    mma_ss(S[t], a, bd, p.idesc_qk, ks > 0);
+                    const uint64_t off = (uint64_t)(((ks & 3) * 32 + (ks >> 2) * CHUNK) >> 4);
+                    mma_ss(d, a0 + off, b0 + off, idesc_qk, ks > 0);
                 }
             };
             auto issue_pv = [&](int t, int s, bool acc) {
+                const uint64_t b0 = s == 0 ? vd0 : (s == 1 ? vd1 : vd2);
+                const uint32_t d = t ? O[1] : O[0], a = t ? S[1] : S[0];
 #pragma unroll
-                for (int ks = 0; ks < BN / 16; ++ks) {
-                    // V tile rows are keys (K dim), 64-wide d chunks CHUNK apart (N dim)
-                    const uint64_t bd = sdesc(su32(sV + s * TILE) + ks * 16 * 128, CHUNK, 1024);
-                    mma_ts(O[t], S[t] + ks * 8, bd, p.idesc_pv, (acc || ks > 0) ? 1u : 0u);
-                }
+                for (int ks = 0; ks < BN / 16; ++ks)
+                    mma_ts(d, a + ks * 8, b0 + (uint64_t)(ks * 16 * 128 / 16), idesc_pv, (acc || ks > 0) ? 1u : 0u);
             };
             bool ok = wait_phase(bar(B_Q), 0, ctl) && wait_phase(bar(B_KF), 0, ctl);
             if (ok) {
@@ -377,11 +392,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 tc_commit(bar(B_KE + 0));
             }
             for (int n = 0; n < ntiles && ok; ++n) {
-                const int s = n % NST;
+                const int s = n % NSV;
                 const bool nxt = n + 1 < ntiles;
-                const int s1 = (n + 1) % NST;
-                const uint32_t ph1 = ((n + 1) / NST) & 1;
-                if (!(ok = wait_phase(bar(B_VF + s), (n / NST) & 1, ctl))) break;
+                const int s1 = (n + 1) % NSK;
+                const uint32_t ph1 = ((n + 1) / NSK) & 1;
+                if (!(ok = wait_phase(bar(B_VF + s), (n / NSV) & 1, ctl))) break;
                 if (!(ok = wait_phase(bar(B_PF + 0), n & 1, ctl))) break;
                 tc_fence_after();
                 issue_pv(0, s, n > 0);
@@ -406,7 +421,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         }
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
         // ------------------------------------------------------------ softmax
         const int t = warp >> 2, q4 = warp & 3;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -428,14 +443,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 for (int e = 0; e < BN; ++e)
                     if (e >= valid) x[e] = 0xff800000u;
             }
-            // row max with 8 independent chains
+            // row max: 8 independent chains of three-input max
             float m8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(x[e]);
 #pragma unroll
-            for (int e = 8; e < BN; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(x[e]));
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int e = 8; e < BN; e += 16)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    m8[j] = max3(m8[j], __uint_as_float(x[e + j]), __uint_as_float(x[e + 8 + j]));
+            const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             const float mxs = mx * c;
             float alpha = 1.f;
             bool rescale = false;
@@ -449,22 +466,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 m_used = mnew;
                 rescale = true;
             }
-            // P = 2^(s*c - m), row sum with 8 independent chains, P over S
-            const float negm = -m_used;
-            float l8[8];
+            // P = 2^(s*c - m) (packed fp32 pairs), row sum in 4 packed
+            // chains, P written over S in two halves
+            const float2 c2 = make_float2(c, c), negm2 = make_float2(-m_used, -m_used);
+            float2 l2[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) l8[e] = 0.f;
-            uint32_t pk[BN / 2];
+            for (int e = 0; e < 4; ++e) l2[e] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < BN / 2; ++e) {
-                const float p0 = ex2(fmaf(__uint_as_float(x[2 * e]), c, negm));
-                const float p1 = ex2(fmaf(__uint_as_float(x[2 * e + 1]), c, negm));
-                l8[(2 * e) & 7] += p0;
-                l8[(2 * e + 1) & 7] += p1;
-                pk[e] = pack_p<P_BF16>(p0, p1);
+            for (int half = 0; half < 2; ++half) {
+                // each half's TMEM store runs while the next half is computed
+                uint32_t pk[BN / 4];
+#pragma unroll
+                for (int e = 0; e < BN / 4; ++e) {
+                    const int i0 = half * (BN / 2) + 2 * e;
+                    const float2 a = __ffma2_rn(make_float2(__uint_as_float(x[i0]), __uint_as_float(x[i0 + 1])),
+                                                c2, negm2);
+                    const float2 pp = make_float2(ex2(a.x), ex2(a.y));
+                    l2[e & 3] = __fadd2_rn(l2[e & 3], pp);
+                    pk[e] = pack_p<P_BF16>(pp.x, pp.y);
+                }
+                tmem_st32(St + half * (BN / 4), pk);
             }
-            tmem_st64(St, pk);
-            l = fmaf(l, alpha, ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+            l = fmaf(l, alpha, ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) + ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y)));
             if (rescale) {
                 // the previous P V of this tile completed before S became ready
 #pragma unroll 1
