@@ -344,41 +344,73 @@ def run_ours(args):
 
 
 def run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args):
+    """End to end through the public API: every step copies its inputs from
+    pinned host memory and reads both results back.  Copies run on their own
+    streams and overlap the neighbouring steps' kernels (inputs and outputs
+    are double-buffered); all of them are inside the timed region."""
     import torch
     import sequence_attention_gb300 as sa
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     hp = pred.cpu().pin_memory()
-    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    hc = torch.empty(cfg_out.shape, dtype=cfg_out.dtype).pin_memory()
-    stream = torch.cuda.current_stream(dev)
+    ho = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    hc = [torch.empty(cfg_out.shape, dtype=cfg_out.dtype).pin_memory() for _ in range(2)]
+    din = [(q, k, v, pred)] + [tuple(torch.empty_like(t) for t in (q, k, v, pred))]
+    dout = [(out, cfg_out), (torch.empty_like(out), torch.empty_like(cfg_out))]
+    comp = torch.cuda.current_stream(dev)
+    h2d = torch.cuda.Stream(dev)
+    d2h = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready, in_free = [ev(), ev()], [ev(), ev()]
+    out_ready, out_free = [ev(), ev()], [ev(), ev()]
+    for e in in_free + out_free:
+        e.record(comp)
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        pred.copy_(hp, non_blocking=True)
-        plan.run(q, k, v, out)
-        sa.dit_cfg_combine(pred, cfg_out, w.g)
-        ho.copy_(out, non_blocking=True)
-        hc.copy_(cfg_out, non_blocking=True)
+    def upload(i):
+        b = i % 2
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(in_free[b])
+            for dst, src in zip(din[b], (hq, hk, hv, hp)):
+                dst.copy_(src, non_blocking=True)
+            in_ready[b].record(h2d)
 
-    for _ in range(3):
-        e2e_step()
+    def run(n):
+        upload(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                upload(i + 1)
+            comp.wait_event(in_ready[b])
+            comp.wait_event(out_free[b])
+            dq, dk, dv, dp = din[b]
+            o, c = dout[b]
+            plan.run(dq, dk, dv, o)
+            sa.dit_cfg_combine(dp, c, w.g)
+            in_free[b].record(comp)
+            out_ready[b].record(comp)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(out_ready[b])
+                ho[b].copy_(o, non_blocking=True)
+                hc[b].copy_(c, non_blocking=True)
+                out_free[b].record(d2h)
+        comp.wait_stream(d2h)
+
+    run(3)
     torch.cuda.synchronize(dev)
-    n = max(3, min(args.steps, 20))
+    n = max(3, min(args.steps, 50))
     barrier()
+    torch.cuda.synchronize(dev)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(n):
-        e2e_step()
-    e.record(stream)
+    s.record(comp)
+    run(n)
+    e.record(comp)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(s.elapsed_time(e) / n, dev)
     _, _, ws = dist_env()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hp))
-    d2h = ho.numel() * ho.element_size() + hc.numel() * hc.element_size()
+    h2d_b = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hp))
+    d2h_b = ho[0].numel() * ho[0].element_size() + hc[0].numel() * hc[0].element_size()
     return {"value": round(ws * w.attn_flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+            "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b, "ms_per_step": round(ms, 4),
+            "note": "inputs H2D and results D2H every step on copy streams overlapping adjacent steps"}
 
 
 # ---------------------------------------------------------------- reference arm
