@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const __grid_constant__ A
     const int qlen = a.q_len[r], kvlen = a.kv_len[j];
     if (row0 >= qlen) return;
 
+    pdl_wait();
     const int tr = threadIdx.x / TPR, part = threadIdx.x % TPR;
     const int i = row0 + tr;
     const bool valid = i < qlen;
@@ -91,7 +92,10 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const __grid_constant__ A
         }
         m = mnew;
     }
-    if (!valid) return;
+    if (!valid) {
+        pdl_trigger();
+        return;
+    }
     const float inv = kvlen > 0 ? 1.f / l : 0.f;
     float* op = static_cast<float*>(a.o.ptr) + r * a.o.stride_q + j * a.o.stride_kv + b * a.o.stride_b +
                 (long long)i * a.o.stride_s + h * a.o.stride_h + part * DT;
@@ -101,6 +105,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const __grid_constant__ A
     if (a.lse.ptr && part == 0)
         a.lse.ptr[r * a.lse.stride_q + j * a.lse.stride_kv + b * a.lse.stride_b + h * a.lse.stride_h + i] =
             kvlen > 0 ? m + logf(l) : -INFINITY;
+    pdl_trigger();
 }
 
 }  // namespace
@@ -112,13 +117,15 @@ dit_status launch_attn_f32(const AttnArgs& a, cudaStream_t st) {
     const int rows = a.D == 128 ? 64 : 128;
     dim3 grid((maxq + rows - 1) / rows, a.H, a.n_q * a.n_kv * a.B);
     if (grid.y > 65535 || grid.z > 65535) return fail(DIT_ERR_UNSUPPORTED, "attention: grid too large");
+    cudaError_t e;
     switch (a.D) {
-        case 16: attn_f32_kernel<16><<<grid, 128, 0, st>>>(a); break;
-        case 32: attn_f32_kernel<32><<<grid, 128, 0, st>>>(a); break;
-        case 64: attn_f32_kernel<64><<<grid, 128, 0, st>>>(a); break;
-        case 128: attn_f32_kernel<128><<<grid, 128, 0, st>>>(a); break;
+        case 16: e = launch_pdl(attn_f32_kernel<16>, grid, dim3(128), 0, st, a); break;
+        case 32: e = launch_pdl(attn_f32_kernel<32>, grid, dim3(128), 0, st, a); break;
+        case 64: e = launch_pdl(attn_f32_kernel<64>, grid, dim3(128), 0, st, a); break;
+        case 128: e = launch_pdl(attn_f32_kernel<128>, grid, dim3(128), 0, st, a); break;
         default: return fail(DIT_ERR_UNSUPPORTED, "attention: fp32 path supports D in {16,32,64,128}");
     }
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "attention: launch failed: %s", cudaGetErrorString(e));
     return check_launch("dit_attn_partial(f32)");
 }
 

@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                              : nullptr;
 
     if (ntiles == 0) {   // empty key chunk: O = 0, lse = -inf
+        pdl_wait();
         if (threadIdx.x < NQT * BM) {
             const int row = row_base + threadIdx.x;
             if (row < qlen) {
@@ -315,6 +316,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();          // barriers and TMEM are set up; tensors from here on
 
     if (warp >= 8) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
@@ -525,6 +527,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         }
     }
 
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -579,7 +582,8 @@ dit_status launch_kernel(const TcParams& prm, dim3 grid, cudaStream_t st) {
     if (smem < 116 * 1024) smem = 116 * 1024;   // one CTA per SM: it owns all 512 TMEM columns
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "attention: %s", cudaGetErrorString(e));
-    attn_tc_kernel<D, PB><<<grid, NTHREADS, smem, st>>>(prm);
+    e = launch_pdl(attn_tc_kernel<D, PB>, grid, dim3(NTHREADS), (size_t)smem, st, prm);
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "attention: launch failed: %s", cudaGetErrorString(e));
     return check_launch("dit_attn_partial(tcgen05)");
 }
 

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kCfgThreads) cfg_vec_kernel(const char* __rest
                                                               char* __restrict__ out, dit_dtype out_dt) {
     const long long base = (long long)blockIdx.x * (kCfgThreads * kCfgVecs) + threadIdx.x;
     const char* cond = pred + N * IB;
+    pdl_wait();
     uint4 ru[kCfgVecs][IB / 2], rc[kCfgVecs][IB / 2];
 #pragma unroll
     for (int k = 0; k < kCfgVecs; ++k) {
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(kCfgThreads) cfg_vec_kernel(const char* __rest
             store8(out + v * 8 * dtype_bytes(out_dt), out_dt, p);
         }
     }
+    pdl_trigger();
 }
 
 __device__ __forceinline__ float load1(const char* p, dit_dtype t, long long i) {
@@ -76,11 +78,13 @@ __device__ __forceinline__ void store1(char* p, dit_dtype t, long long i, float 
 // Scalar tail / unaligned-length path.
 __global__ void cfg_scalar_kernel(const char* __restrict__ pred, dit_dtype in_dt, long long begin,
                                   long long N, float g, char* __restrict__ out, dit_dtype out_dt) {
+    pdl_wait();
     for (long long i = begin + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < N;
          i += (long long)gridDim.x * blockDim.x) {
         const float u = load1(pred, in_dt, i), c = load1(pred, in_dt, N + i);
         store1(out, out_dt, i, g == 1.0f ? c : fmaf(g, c - u, u));
     }
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -104,6 +108,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
     const long long per_row = (long long)a.H * chunks;
     const long long total = (long long)a.q_len[r] * per_row;
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    pdl_wait();
     if (t < total) {
         const int i = (int)(t / per_row);
         const int rem = (int)(t - (long long)i * per_row);
@@ -142,6 +147,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
         if (a.lse_out.ptr && c == 0)
             a.lse_out.ptr[r * a.lse_out.stride_q + b * a.lse_out.stride_b + h * a.lse_out.stride_h + i] = lse;
     }
+    pdl_trigger();
 }
 
 }  // namespace
@@ -170,12 +176,10 @@ extern "C" dit_status dit_cfg_combine(const void* pred, dit_dtype in_dt, int64_t
         const long long nvec = N / 8;
         if (nvec > 0) {
             const long long blocks = (nvec + kCfgThreads * kCfgVecs - 1) / (kCfgThreads * kCfgVecs);
-            if (in_dt == DIT_F32)
-                cfg_vec_kernel<4><<<(unsigned)blocks, kCfgThreads, 0, st>>>(pb, in_dt, nvec, N, g,
-                                                                            static_cast<char*>(out), out_dt);
-            else
-                cfg_vec_kernel<2><<<(unsigned)blocks, kCfgThreads, 0, st>>>(pb, in_dt, nvec, N, g,
-                                                                            static_cast<char*>(out), out_dt);
+            cudaError_t e = launch_pdl(in_dt == DIT_F32 ? cfg_vec_kernel<4> : cfg_vec_kernel<2>, dim3((unsigned)blocks),
+                                       dim3(kCfgThreads), 0, st, pb, in_dt, nvec, N, g, static_cast<char*>(out),
+                                       out_dt);
+            if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
             dit_status s = check_launch(who);
             if (s != DIT_OK) return s;
         }
@@ -185,7 +189,9 @@ extern "C" dit_status dit_cfg_combine(const void* pred, dit_dtype in_dt, int64_t
         const long long rest = N - done;
         long long blocks = (rest + 255) / 256;
         if (blocks > 4096) blocks = 4096;
-        cfg_scalar_kernel<<<(unsigned)blocks, 256, 0, st>>>(pb, in_dt, done, N, g, static_cast<char*>(out), out_dt);
+        cudaError_t e = launch_pdl(cfg_scalar_kernel, dim3((unsigned)blocks), dim3(256), 0, st, pb, in_dt, done, N, g,
+                                   static_cast<char*>(out), out_dt);
+        if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
         return check_launch(who);
     }
     return DIT_OK;
@@ -225,6 +231,7 @@ extern "C" dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int
     const long long bx = (work + 255) / 256;     // one thread per 8 outputs
     dim3 grid((unsigned)bx, (unsigned)(n_q * B));
     if (grid.y > 65535) return fail(DIT_ERR_UNSUPPORTED, "%s: n_q * B too large", who);
-    merge_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(a);
+    cudaError_t e = launch_pdl(merge_kernel, grid, dim3(256), 0, (cudaStream_t)stream, a);
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     return check_launch(who);
 }

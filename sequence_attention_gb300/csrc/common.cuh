@@ -7,6 +7,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "ditsp.h"
 
 namespace ditsp {
@@ -20,6 +22,32 @@ int num_sms();                   // SM count of the current device (cached)
 inline bool dtype_ok(dit_dtype t) { return t == DIT_F32 || t == DIT_BF16 || t == DIT_F16; }
 __host__ __device__ inline int dtype_bytes(dit_dtype t) { return t == DIT_F32 ? 4 : 2; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- programmatic dependent launch -------------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialization allowed: it may begin while the previous kernel in the
+// stream drains.  A kernel runs its input-independent prologue, then
+// pdl_wait() (which returns once every earlier kernel has completed and its
+// writes are visible) before it reads or writes any tensor, and calls
+// pdl_trigger() when its CTA has finished its work.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- device-side element access --------------------------------------------
 // Eight consecutive elements of one type, moved as 16-byte (16-bit types) or

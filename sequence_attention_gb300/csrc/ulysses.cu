@@ -272,10 +272,14 @@ __global__ void __launch_bounds__(kThreads) run_kernel(const __grid_constant__ R
     const int nrun = (int)min((long long)rpb, A.nruns - r0);
     if ((int)threadIdx.x < nrun) ios[threadIdx.x] = run_io<MODE>(A, (int)(r0 + threadIdx.x));
     __syncthreads();
+    pdl_wait();          // the decode above used only the layout; data from here on
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g0 = warp * rpw;
     const int gn = min(rpw, nrun - g0);
-    if (gn <= 0) return;
+    if (gn <= 0) {
+        pdl_trigger();
+        return;
+    }
     const int nch = (A.L.Hl * A.L.D) >> 3;
     const int items = gn * nch;
     const bool want_check = (MODE == UNPACK_S2H) && A.range_flag != nullptr;
@@ -319,6 +323,7 @@ __global__ void __launch_bounds__(kThreads) run_kernel(const __grid_constant__ R
         }
     }
     if (overflow) *A.range_flag = (int)DIT_ERR_RANGE;
+    pdl_trigger();
 }
 
 // Host-side check of a caller-supplied layout: every field must be what
@@ -348,7 +353,8 @@ dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
     int rpw = 4;
     if ((a.nruns + 31) / 32 < 2 * slots) rpw = 2;
     const long long blocks = (a.nruns + 8LL * rpw - 1) / (8LL * rpw);
-    run_kernel<MODE, SB, DB><<<(unsigned)blocks, kThreads, 0, st>>>(a, rpw);
+    cudaError_t e = launch_pdl(run_kernel<MODE, SB, DB>, dim3((unsigned)blocks), dim3(kThreads), 0, st, a, rpw);
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     return check_launch(who);
 }
 
