@@ -7,6 +7,8 @@
  *   dit_sp_layout_init / dit_sp_a2a_counts   rank partition bookkeeping
  *   dit_ulysses_pack / dit_a2a_sim / dit_ulysses_unpack
  *                                            the Ulysses all-to-all, both ways
+ *   dit_sp_signal / dit_a2a_sim_checked      the exchange with arrival counters
+ *                                            and a bounded wait
  *   dit_attn_partial                         attention of query blocks against
  *                                            key/value chunks, with log-sum-exp
  *   dit_attn_merge_lse                       exact merge of the partials
@@ -188,6 +190,32 @@ DIT_API dit_status dit_ulysses_pack(const dit_sp_layout* L, dit_a2a_dir dir, int
 
 DIT_API dit_status dit_a2a_sim(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
                        const void* send, void* recv, dit_dtype wire_dt, void* stream);
+
+/*
+ * Checked exchange (SGLang Diffusion "Parallelism Overview", The Ulysses
+ * transport: senders publish GPU-side sequence counters instead of a
+ * rendezvous, and a timeout backstop makes the request fail rather than
+ * return incomplete data).
+ *
+ * dit_sp_signal: every virtual rank i with rank_mask[i] != 0 (all ranks if
+ *   rank_mask is NULL; host array of U*R bytes) publishes `epoch` on its
+ *   arrival counter d_arrival[i] (device, U*R unsigned ints, caller-owned).
+ *   Stream-ordered: issue it after the pack that fills the send buffers.
+ * dit_a2a_sim_checked: as dit_a2a_sim, but each run is copied only once its
+ *   sender's counter has reached `epoch` (unsigned sequence comparison).  A
+ *   counter that does not get there within timeout_ns (0 < t <= 10 s) sets
+ *   *d_status = DIT_ERR_TIMEOUT (the library's word if d_status is NULL) and
+ *   the rest of the exchange is abandoned: runs whose senders timed out are
+ *   not written, and the receive buffer must be treated as invalid.  The
+ *   kernel always returns; the device stays usable.
+ */
+DIT_API dit_status dit_sp_signal(const dit_sp_layout* L, unsigned* d_arrival, const unsigned char* rank_mask,
+                                 unsigned epoch, void* stream);
+
+DIT_API dit_status dit_a2a_sim_checked(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
+                                       const void* send, void* recv, dit_dtype wire_dt,
+                                       const unsigned* d_arrival, unsigned epoch, int64_t timeout_ns,
+                                       int* d_status, void* stream);
 
 DIT_API dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
                               const void* recv, dit_dtype wire_dt,

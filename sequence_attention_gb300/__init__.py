@@ -15,6 +15,7 @@ must be contiguous):
 """
 from __future__ import annotations
 
+import ctypes
 import math
 from ctypes import byref, c_int, c_int64, c_void_p
 from typing import List, Optional, Sequence
@@ -29,7 +30,7 @@ __all__ = [
     "DitError", "Layout", "DIT_SEQ_TO_HEAD", "DIT_HEAD_TO_SEQ",
     "dit_sp_layout_init", "dit_sp_a2a_counts", "dit_ulysses_pack", "dit_a2a_sim",
     "dit_ulysses_unpack", "dit_attn_partial", "dit_attn_merge_lse", "dit_attention",
-    "dit_cfg_combine", "dit_device_status", "library_path",
+    "dit_cfg_combine", "dit_device_status", "library_path", "dit_sp_signal", "dit_a2a_sim_checked",
 ]
 
 lib()   # load now: fail at import time, not at first call
@@ -110,6 +111,23 @@ def dit_a2a_sim(L: Layout, direction: int, nplanes: int, send: torch.Tensor, rec
                 stream=None) -> None:
     check(lib().dit_a2a_sim(byref(L.raw), direction, nplanes, _ptr(send), _ptr(recv), _dt(send),
                             _stream(stream)))
+
+
+def dit_sp_signal(L: Layout, arrival: torch.Tensor, epoch: int, ranks=None, stream=None) -> None:
+    """Publish `epoch` on the arrival counters of `ranks` (all if None)."""
+    mask = None
+    if ranks is not None:
+        n = L.raw.U * L.raw.R
+        mask = (ctypes.c_ubyte * n)(*[1 if i in set(ranks) else 0 for i in range(n)])
+    check(lib().dit_sp_signal(byref(L.raw), _ptr(arrival), mask, epoch & 0xFFFFFFFF, _stream(stream)))
+
+
+def dit_a2a_sim_checked(L: Layout, direction: int, nplanes: int, send: torch.Tensor, recv: torch.Tensor,
+                        arrival: torch.Tensor, epoch: int, timeout_ns: int,
+                        status: Optional[torch.Tensor] = None, stream=None) -> None:
+    check(lib().dit_a2a_sim_checked(byref(L.raw), direction, nplanes, _ptr(send), _ptr(recv), _dt(send),
+                                    _ptr(arrival), epoch & 0xFFFFFFFF, int(timeout_ns), _ptr(status),
+                                    _stream(stream)))
 
 
 def dit_ulysses_unpack(L: Layout, direction: int, recv: torch.Tensor, dsts: Sequence[torch.Tensor],

@@ -8,7 +8,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, Structure, c_char_p, c_float, c_int, c_int64, c_void_p
+from ctypes import POINTER, Structure, c_char_p, c_float, c_int, c_int64, c_uint, c_void_p
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libditsp.so")
 
@@ -25,6 +25,7 @@ EXPORTS = (
     "dit_status_string", "dit_last_error", "dit_device_status", "dit_sp_layout_init",
     "dit_sp_a2a_counts", "dit_ulysses_pack", "dit_a2a_sim", "dit_ulysses_unpack",
     "dit_attn_partial", "dit_attn_merge_lse", "dit_attention", "dit_cfg_combine",
+    "dit_sp_signal", "dit_a2a_sim_checked",
 )
 
 
@@ -79,6 +80,11 @@ def lib() -> ctypes.CDLL:
                                    c_void_p, c_int, c_void_p]
     L.dit_a2a_sim.restype = c_int
     L.dit_a2a_sim.argtypes = [POINTER(DitSpLayout), c_int, c_int, c_void_p, c_void_p, c_int, c_void_p]
+    L.dit_sp_signal.restype = c_int
+    L.dit_sp_signal.argtypes = [POINTER(DitSpLayout), c_void_p, c_void_p, c_uint, c_void_p]
+    L.dit_a2a_sim_checked.restype = c_int
+    L.dit_a2a_sim_checked.argtypes = [POINTER(DitSpLayout), c_int, c_int, c_void_p, c_void_p, c_int, c_void_p,
+                                      c_uint, c_int64, c_void_p, c_void_p]
     L.dit_ulysses_unpack.restype = c_int
     L.dit_ulysses_unpack.argtypes = [POINTER(DitSpLayout), c_int, c_int, c_void_p, c_int,
                                      POINTER(c_void_p), POINTER(c_int), c_void_p, c_void_p]

@@ -35,6 +35,11 @@ struct RunArgs {
     dit_dtype dst_dt[3];
     int* range_flag;
     long long nruns;
+    // checked exchange: copy a run only once its sender's counter reached epoch
+    const unsigned* arrival;
+    unsigned epoch;
+    long long timeout_ns;
+    int* status;
 };
 
 struct Run {
@@ -159,6 +164,23 @@ __device__ __forceinline__ long long head_offset(const dit_sp_layout& L, const R
     return ((((long long)x.r * L.B + x.b) * L.S_cap + row) * L.Hp + (long long)x.v * L.Hl) * L.D;
 }
 
+__device__ __forceinline__ unsigned long long gtimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Publish `epoch` on the arrival counter of every rank whose bit is set.
+__global__ void signal_kernel(unsigned* arrival, int nranks, unsigned long long mask, unsigned epoch) {
+    pdl_wait();
+    const int i = threadIdx.x;
+    if (i < nranks && ((mask >> i) & 1ull)) {
+        __threadfence();
+        arrival[i] = epoch;
+    }
+    pdl_trigger();
+}
+
 __device__ __forceinline__ bool narrowing(dit_dtype s, dit_dtype d) {
     return (s == DIT_F32 && d != DIT_F32) || (s == DIT_BF16 && d == DIT_F16);
 }
@@ -170,6 +192,7 @@ struct RunIO {
     int src_lim;      // chunks of the source holding data; later chunks read as zero
     int dst_lim;      // chunks of the destination written; later chunks skipped
     int sdt, ddt;     // dit_dtype of source and destination
+    int sender;       // virtual rank that sent this run (exchange kernels)
 };
 
 template <int MODE>
@@ -223,6 +246,8 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
     io.dst += doff * dtype_bytes(ddt);
     io.sdt = sdt;
     io.ddt = ddt;
+    // seq->head: rank (r,u) sends to (r,v); head->seq: rank (r,v) sends to (r,u)
+    io.sender = x.r * L.U + (MODE == A2A_H2S || MODE == PACK_H2S || MODE == UNPACK_H2S ? x.v : x.u);
     return io;
 }
 
@@ -273,6 +298,28 @@ __global__ void __launch_bounds__(kThreads) run_kernel(const __grid_constant__ R
     if ((int)threadIdx.x < nrun) ios[threadIdx.x] = run_io<MODE>(A, (int)(r0 + threadIdx.x));
     __syncthreads();
     pdl_wait();          // the decode above used only the layout; data from here on
+    if (A.arrival != nullptr && (int)threadIdx.x < nrun) {
+        // Bounded wait for the sender's arrival counter (a transport whose
+        // peer never publishes must fail, not hang).  Once any wait of the
+        // call has run out, every other run is abandoned at once.
+        RunIO& io = ios[threadIdx.x];
+        const volatile unsigned* cnt = A.arrival + io.sender;
+        volatile int* st = A.status;
+        bool arrived = (int)(*cnt - A.epoch) >= 0;
+        if (!arrived) {
+            const unsigned long long t0 = gtimer_ns();
+            while (!arrived && *st != (int)DIT_ERR_TIMEOUT) {
+                __nanosleep(256);
+                arrived = (int)(*cnt - A.epoch) >= 0;
+                if (!arrived && gtimer_ns() - t0 > (unsigned long long)A.timeout_ns) {
+                    atomicExch(A.status, (int)DIT_ERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        if (!arrived) io.src_lim = io.dst_lim = 0;
+    }
+    __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g0 = warp * rpw;
     const int gn = min(rpw, nrun - g0);
@@ -459,4 +506,51 @@ extern "C" dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir
     a.nruns = (long long)nplanes * L->B * L->U * L->S;
     cudaStream_t st = (cudaStream_t)stream;
     return dir == DIT_SEQ_TO_HEAD ? launch_runs<UNPACK_S2H>(a, st, who) : launch_runs<UNPACK_H2S>(a, st, who);
+}
+
+extern "C" dit_status dit_sp_signal(const dit_sp_layout* L, unsigned* d_arrival, const unsigned char* rank_mask,
+                                    unsigned epoch, void* stream) {
+    const char* who = "dit_sp_signal";
+    dit_status s = check_layout(L, who);
+    if (s != DIT_OK) return s;
+    if (!d_arrival || (reinterpret_cast<uintptr_t>(d_arrival) & 3))
+        return fail(DIT_ERR_INVALID_ARG, "%s: arrival counters NULL or misaligned", who);
+    const int n = L->U * L->R;
+    unsigned long long mask = 0;
+    for (int i = 0; i < n; ++i)
+        if (!rank_mask || rank_mask[i]) mask |= 1ull << i;
+    cudaError_t e = launch_pdl(signal_kernel, dim3(1), dim3(64), 0, (cudaStream_t)stream, d_arrival, n, mask, epoch);
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
+    return check_launch(who);
+}
+
+extern "C" dit_status dit_a2a_sim_checked(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, const void* send,
+                                          void* recv, dit_dtype wire_dt, const unsigned* d_arrival, unsigned epoch,
+                                          int64_t timeout_ns, int* d_status, void* stream) {
+    const char* who = "dit_a2a_sim_checked";
+    dit_status s = check_layout(L, who);
+    if (s != DIT_OK) return s;
+    if (!dtype_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (dir != DIT_SEQ_TO_HEAD && dir != DIT_HEAD_TO_SEQ) return fail(DIT_ERR_INVALID_ARG, "%s: bad direction", who);
+    if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
+    if (!send || !recv || !aligned16(send) || !aligned16(recv) || send == recv)
+        return fail(DIT_ERR_INVALID_ARG, "%s: send/recv NULL, misaligned or identical", who);
+    if (!d_arrival || (reinterpret_cast<uintptr_t>(d_arrival) & 3))
+        return fail(DIT_ERR_INVALID_ARG, "%s: arrival counters NULL or misaligned", who);
+    if (timeout_ns <= 0 || timeout_ns > 10000000000LL)
+        return fail(DIT_ERR_INVALID_ARG, "%s: timeout must be in (0, 10 s]", who);
+    RunArgs a;
+    memset(&a, 0, sizeof(a));
+    a.L = *L;
+    a.np = nplanes;
+    a.src[0] = send; a.src_dt[0] = wire_dt;
+    a.dst[0] = recv; a.dst_dt[0] = wire_dt;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    a.arrival = d_arrival;
+    a.epoch = epoch;
+    a.timeout_ns = timeout_ns;
+    a.status = d_status ? d_status : default_status_word();
+    if (!a.status) return fail(DIT_ERR_CUDA, "%s: no device status word", who);
+    cudaStream_t st = (cudaStream_t)stream;
+    return dir == DIT_SEQ_TO_HEAD ? launch_runs<A2A_S2H>(a, st, who) : launch_runs<A2A_H2S>(a, st, who);
 }

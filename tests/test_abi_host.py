@@ -112,6 +112,20 @@ def test_validation_happens_before_any_launch(dl):
         == dl.DIT_OK                           # empty: nothing to do
 
 
+def test_checked_exchange_argument_checks(dl):
+    L = dl.lib()
+    lay = dl.DitSpLayout()
+    assert L.dit_sp_layout_init(1, 64, 4, 64, 2, 2, ctypes.byref(lay)) == 0
+    send, recv, arr = ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20)
+    assert L.dit_a2a_sim_checked(ctypes.byref(lay), 0, 3, send, recv, dl.DIT_BF16, arr, 1, 0, None, None) \
+        == dl.DIT_ERR_INVALID_ARG                            # timeout must be positive
+    assert L.dit_a2a_sim_checked(ctypes.byref(lay), 0, 3, send, recv, dl.DIT_BF16, arr, 1, 20_000_000_000, None,
+                                 None) == dl.DIT_ERR_INVALID_ARG   # and at most 10 s
+    assert L.dit_a2a_sim_checked(ctypes.byref(lay), 0, 3, send, recv, dl.DIT_BF16, None, 1, 1000, None, None) \
+        == dl.DIT_ERR_INVALID_ARG                            # counters required
+    assert L.dit_sp_signal(ctypes.byref(lay), ctypes.c_void_p(2), None, 1, None) == dl.DIT_ERR_INVALID_ARG
+
+
 def _view(ptr, sb=0, ss=0, sh=0):
     from sequence_attention_gb300._lib import DitView
     v = DitView()
