@@ -296,6 +296,7 @@ def run_ours(args):
 
     # end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args)
+    extra = {} if args.no_extra else bandwidth_at_scale(dev, flush, peaks)
 
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
@@ -324,6 +325,7 @@ def run_ours(args):
             "cfg_ms": round(statistics.mean(seg[3]), 4),
             "cfg_GBs": round(cfg_bytes / (statistics.mean(seg[3]) * 1e-3) / 1e9, 1),
             "hbm_peak_GBs": peaks.get("hbm_gbs"),
+            **extra,
         },
         "e2e": e2e,
         "gpu_launches": K * (len(names) - 1 + n_cfg_kernels),
@@ -341,6 +343,106 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def bandwidth_at_scale(dev, flush, peaks):
+    """The merge (not in the R = 1 step) and CFG on the Wan-like shapes,
+    each launch timed alone with L2 flushed before it (median of 10)."""
+    import torch
+    import sequence_attention_gb300 as sa
+    import synth
+    w = synth.WORKLOADS["wan"]
+    R, H, D = w.R, w.H, w.D
+    L = sa.dit_sp_layout_init(w.B, w.S, H, D, max(w.U), R)
+    cap = L.S_cap
+    parts = torch.randn((R, R, w.B, cap, H, D), dtype=torch.float32, device=dev)
+    lse = torch.randn((R, R, w.B, H, cap), dtype=torch.float32, device=dev)
+    out = torch.empty((R, w.B, cap, H, D), dtype=torch.bfloat16, device=dev)
+    rl = L.ring_len
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(13):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 3:
+                ts.append(s.elapsed_time(e))
+        return statistics.median(ts)
+
+    res = {}
+    ms = timed(lambda: sa.dit_attn_merge_lse(parts, lse, out, None, rl))
+    rows = sum(rl) * w.B
+    nbytes = rows * H * (R * D * 4 + R * 4 + D * 2)
+    res["merge_wan_ms"] = round(ms, 4)
+    res["merge_wan_GBs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+    del parts, lse, out
+    pred = torch.randn(w.cfg_shape, dtype=torch.bfloat16, device=dev)
+    cfg = torch.empty(w.cfg_shape[1:], dtype=torch.bfloat16, device=dev)
+    ms = timed(lambda: sa.dit_cfg_combine(pred, cfg, w.g))
+    res["cfg_wan_ms"] = round(ms, 4)
+    res["cfg_wan_GBs"] = round(3 * cfg.numel() * 2 / (ms * 1e-3) / 1e9, 1)
+    del pred, cfg
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_sweep(args):
+    """One JSON line per workload: the full step (layout, attention partials,
+    merge, layout back, CFG) with per-segment times, on one GPU."""
+    import torch
+    import synth
+    import sequence_attention_gb300 as sa
+    from sequence_attention_gb300.usp import UspPlan
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cases = [("tiny", 2), ("flux1024", 2), ("flux1024", 4), ("flux1008", 4), ("flux1008_4480", 4),
+             ("qwen1328", 5), ("wan", 8)]
+    for name, U in cases:
+        w = synth.WORKLOADS[name]
+        q, k, v = (t.to(dev) for t in w.qkv())
+        pred = w.cfg_pair().to(dev)
+        out = torch.empty((w.B, w.S, w.H, w.D), dtype=q.dtype, device=dev)
+        cfg_out = torch.empty(w.cfg_shape[1:], dtype=synth.torch_dtype(w.cfg_out), device=dev)
+        plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev))
+        stream = torch.cuda.current_stream(dev)
+        reps = 3 if name == "wan" else 10
+        seg = [[] for _ in range(4)]
+        for i in range(reps + 3):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev[0].record(stream)
+            plan.layout_in(q, k, v)
+            ev[1].record(stream)
+            plan.attend()
+            ev[2].record(stream)
+            plan.layout_out(out)
+            ev[3].record(stream)
+            sa.dit_cfg_combine(pred, cfg_out, w.g)
+            ev[4].record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 3:
+                for j in range(4):
+                    seg[j].append(ev[j].elapsed_time(ev[j + 1]))
+        med = [statistics.median(x) for x in seg]
+        fl = w.attn_flops
+        tf = fl / (med[1] * 1e-3) / 1e12
+        res = {"workload": name, "U": U, "R": w.R, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "dtype": w.dtype,
+               "step_ms": round(sum(med), 4), "layout_in_ms": round(med[0], 4),
+               "attention_ms": round(med[1], 4), "attention_TFLOPs": round(tf, 1),
+               "attention_frac_of_measured_peak": round(tf / peaks["bf16_tflops"], 4) if w.dtype != "f32" else None,
+               "layout_out_ms": round(med[2], 4), "cfg_ms": round(med[3], 4),
+               "attention_includes_merge": w.R > 1, "status": int(plan.status.item()),
+               "range_flag": int(plan.range_flag.item())}
+        print(json.dumps(res), flush=True)
+        del q, k, v, pred, out, cfg_out, plan
+        torch.cuda.empty_cache()
 
 
 def run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args):
@@ -456,8 +558,12 @@ def main(argv=None):
     ap.add_argument("--U", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=12.0, dest="cpu_budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the Wan-size merge/CFG timings")
+    ap.add_argument("--sweep", action="store_true", help="one line per workload instead of the bench line")
     args = ap.parse_args(argv)
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
