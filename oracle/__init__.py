@@ -26,9 +26,12 @@ all floating-point arithmetic, with numpy as the only numerical library:
 * ``usp``         -- Ulysses inside, ring outside, composed end to end
                      (cache-dit "USP: Unified Sequence Parallelism").
 * ``numeric``     -- round-to-nearest-even conversions to bfloat16/float16.
+* ``rope``        -- rotary embedding of the receive preparation and the
+                     joint text+image sequence (edge-dit.cpp, receive
+                     preparation and paired text/image streams).
 
 Every function is pinned in ``tests/test_oracle_*.py`` to closed forms,
 invariants, library routines or brute force; none is "parity unpinned".
 """
 
-from . import attention, cfg, layout, numeric, ulysses, usp  # noqa: F401
+from . import attention, cfg, layout, numeric, rope, ulysses, usp  # noqa: F401
