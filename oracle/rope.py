@@ -36,3 +36,27 @@ def joint(txt: np.ndarray, img: np.ndarray) -> np.ndarray:
     """The joint attention sequence of a double-stream block: text tokens
     first, then image tokens, along the sequence axis of [B, S, H, D]."""
     return np.concatenate([np.asarray(txt), np.asarray(img)], axis=1)
+
+
+def receive_prep(L, recv: np.ndarray, wire_dt: str, dst_dts, cos: np.ndarray, sin: np.ndarray,
+                 rope_planes: int):
+    """Head-sharded planes of every rank from the received buffers, with the
+    rotary embedding applied to the planes whose bit is set in rope_planes.
+
+    Returns {(r, v): [plane_0, ...]} with planes of shape [B, S_r, Hl, D]:
+    a rotated plane as float64 (the exact rotation of the received values,
+    before the rounding to its destination type); any other plane as the
+    storage bits of dst_dts[p], as ``ulysses.s2h_unpack`` gives them.  Row s
+    of ring block r is the token at joint position ring_off[r] + s.
+    """
+    from . import numeric, ulysses
+
+    kinds = [wire_dt if (rope_planes >> p) & 1 else dt for p, dt in enumerate(dst_dts)]
+    ranks = ulysses.s2h_unpack(L, recv, wire_dt, kinds)
+    for (r, _v), planes in ranks.items():
+        rows = slice(L.ring_off[r], L.ring_off[r] + L.ring_len[r])
+        for p in range(len(planes)):
+            if (rope_planes >> p) & 1:
+                x = numeric.to_f64(planes[p], wire_dt)
+                planes[p] = rope(x, np.asarray(cos)[rows], np.asarray(sin)[rows])
+    return ranks

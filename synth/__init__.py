@@ -68,6 +68,47 @@ def as_bits(t: torch.Tensor) -> np.ndarray:
     raise ValueError("unsupported element size")
 
 
+def _tables(angles: np.ndarray):
+    """float32 cos/sin tables of float64 angles [S, D/2] (RNE to float32)."""
+    return (torch.from_numpy(np.cos(angles).astype(np.float32)),
+            torch.from_numpy(np.sin(angles).astype(np.float32)))
+
+
+def rope_tables_linear(S: int, D: int, base: float = 10000.0):
+    """Rotary angle tables of a 1-D position index: token t, pair i has the
+    angle t * base**(-2i/D).  Every token has distinct angles, which makes it
+    the stronger test input."""
+    i = np.arange(D // 2, dtype=np.float64)
+    t = np.arange(S, dtype=np.float64)[:, None]
+    return _tables(t * base ** (-2.0 * i / D))
+
+
+def rope_axes(D: int) -> Tuple[int, int, int]:
+    """Head-dim split of the three-axis position ids (16, 56, 56 for D=128)."""
+    a0 = 2 * max(1, D // 16)
+    a1 = 2 * ((D - a0) // 4)
+    return a0, a1, D - a0 - a1
+
+
+def rope_tables_joint(S_txt: int, S: int, D: int, base: float = 10000.0):
+    """Rotary angle tables of a joint text+image sequence with three-axis
+    position ids, the stand-in for the FLUX-family models' positions: text
+    tokens have ids (0, 0, 0), image token k of a w-wide grid (0, k // w,
+    k % w), w = ceil(sqrt(S - S_txt)).  Axis a owns rope_axes(D)[a] of the
+    head dims; its pair j turns by id_a * base**(-2j/d_a)."""
+    n = S - S_txt
+    w = max(1, int(np.ceil(np.sqrt(n)))) if n > 0 else 1
+    k = np.arange(n)
+    ids = np.zeros((S, 3), dtype=np.float64)
+    ids[S_txt:, 1] = k // w
+    ids[S_txt:, 2] = k % w
+    cols = []
+    for a, da in enumerate(rope_axes(D)):
+        j = np.arange(da // 2, dtype=np.float64)
+        cols.append(ids[:, a:a + 1] * base ** (-2.0 * j / da))
+    return _tables(np.concatenate(cols, axis=1))
+
+
 @dataclass(frozen=True)
 class Workload:
     """One attention workload: shapes, parallel degrees and value recipe."""
@@ -87,6 +128,7 @@ class Workload:
     g: float
     seed: int = 0
     note: str = ""
+    S_txt: int = 0                  # text tokens at the head of the joint sequence
 
     def qkv(self, device: Optional[str] = None):
         shp = (self.B, self.S, self.H, self.D)
@@ -115,17 +157,17 @@ WORKLOADS = {
                      note="fp32 path, U=2 and R=2, also USP 2x2"),
     "flux1024": Workload("flux1024", 1, 4608, 24, 128, "bf16", 0.5, (2, 4), 1,
                          (2, 4608, 3072), "bf16", "bf16", 3.5,
-                         note="4096 image + 512 text tokens"),
+                         note="4096 image + 512 text tokens", S_txt=512),
     "flux1008": Workload("flux1008", 1, 4481, 24, 128, "bf16", 0.5, (4,), 2,
                          (2, 4481, 3072), "bf16", "bf16", 3.5,
-                         note="63x63=3969 image + 512 text tokens; uneven"),
+                         note="63x63=3969 image + 512 text tokens; uneven", S_txt=512),
     "flux1008_4480": Workload("flux1008_4480", 1, 4480, 24, 128, "bf16", 0.5,
                               (4,), 2, (2, 4480, 3072), "bf16", "bf16", 3.5,
-                              note="the literal 3969 + 511 token count"),
+                              note="the literal 3969 + 511 token count", S_txt=511),
     "qwen1328": Workload("qwen1328", 2, 7145, 24, 128, "bf16", 0.5, (5,), 2,
                          (2, 7145, 3072), "f32", "bf16", 4.0,
                          note="83x83=6889 image + 256 text tokens; 24 heads "
-                              "padded to 25 for U=5"),
+                              "padded to 25 for U=5", S_txt=256),
     "wan": Workload("wan", 1, 75600, 40, 128, "bf16", 0.5, (8,), 4,
                     (2, 75600, 5120), "bf16", "bf16", 5.0,
                     note="21 latent frames x 45x80 tokens; U=8 x R=4"),

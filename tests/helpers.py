@@ -57,3 +57,30 @@ def sample_rows(L, n_random: int, seed: int = 0):
     rng = np.random.default_rng(seed)
     rows.update(int(x) for x in rng.integers(0, L.S, n_random))
     return np.array(sorted(rows))
+
+
+_PRECISION = {"bf16": (8, -133), "f16": (11, -24), "f32": (24, -149)}
+
+
+def half_ulp(y, dt: str) -> np.ndarray:
+    """Half a unit in the last place of |y|'s binade in type dt (subnormal
+    spacing at the bottom): the largest error of a round-to-nearest."""
+    p, sub = _PRECISION[dt]
+    a = np.abs(np.asarray(y, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return 0.5 * np.exp2(np.maximum(e - (p - 1), sub))
+
+
+def assert_rotation_close(gpu, exact, x, dt: str, what=""):
+    """A pair rotation done in fp32 (one rounded product, one fused
+    multiply-add) then rounded to dt: the error is at most 2^-23 (|x0| + |x1|)
+    before the final rounding plus half an ulp of dt.  x are the rotated
+    inputs, [..., D]."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    exact = np.asarray(exact, dtype=np.float64)
+    m = np.abs(x[..., 0::2]) + np.abs(x[..., 1::2])
+    m = np.repeat(m, 2, axis=-1)
+    bound = 2.0 ** -23 * m + half_ulp(np.maximum(np.abs(gpu), np.abs(exact)), dt)
+    err = np.abs(gpu - exact)
+    bad = err > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} beyond the bound, worst {err[bad].max():.3e}"

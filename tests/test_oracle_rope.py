@@ -64,3 +64,48 @@ def test_joint_sequence_puts_text_first():
     t = np.full((1, 2, 1, 1), 1.0)
     i = np.full((1, 3, 1, 1), 2.0)
     np.testing.assert_array_equal(orope.joint(t, i)[0, :, 0, 0], [1, 1, 2, 2, 2])
+
+
+def _global_planes(B, S, H, D, n, dt, seed):
+    import synth
+    from tests.helpers import bits
+    ts = [synth.normal((B, S, H, D), seed + p, 1.0, dt) for p in range(n)]
+    return [bits(t) for t in ts]
+
+
+def test_receive_prep_matches_direct_indexing():
+    # brute force: every head-layout element of every rank, read straight
+    # from the rotated global planes (no send/receive bookkeeping)
+    import synth
+    from oracle import layout as olayout, numeric, ulysses
+    B, S, H, D, U, R = 2, 23, 5, 8, 3, 2
+    L = olayout.make_layout(B, S, H, D, U, R)
+    planes = _global_planes(B, S, H, D, 3, "bf16", 40)
+    cos, sin = (t.numpy().astype(np.float64) for t in synth.rope_tables_linear(S, D))
+    recv = ulysses.a2a(L, "s2h", 3, ulysses.s2h_pack(L, planes, "bf16", "bf16"))
+    got = orope.receive_prep(L, recv, "bf16", ["bf16", "bf16", "f16"], cos, sin, 0b011)
+    rotated = [orope.rope(numeric.to_f64(planes[p], "bf16"), cos, sin) for p in range(2)]
+    for (r, v), pl in got.items():
+        for s in range(L.ring_len[r]):
+            t = L.ring_off[r] + s
+            for hl in range(L.Hl):
+                h = v * L.Hl + hl
+                for p in range(2):
+                    want = rotated[p][:, t, h] if h < H else np.zeros((B, D))
+                    np.testing.assert_array_equal(pl[p][:, s, hl], want)
+                want_v = (numeric.convert_bits(planes[2][:, t, h], "bf16", "f16") if h < H
+                          else np.zeros((B, D), np.uint16))
+                np.testing.assert_array_equal(pl[2][:, s, hl], want_v)
+
+
+def test_receive_prep_with_zero_angles_is_the_plain_unpack():
+    from oracle import layout as olayout, numeric, ulysses
+    B, S, H, D, U, R = 1, 11, 4, 8, 2, 1
+    L = olayout.make_layout(B, S, H, D, U, R)
+    planes = _global_planes(B, S, H, D, 2, "f32", 50)
+    recv = ulysses.a2a(L, "s2h", 2, ulysses.s2h_pack(L, planes, "f32", "f32"))
+    got = orope.receive_prep(L, recv, "f32", ["f32", "f32"], np.ones((S, 4)), np.zeros((S, 4)), 0b11)
+    plain = ulysses.s2h_unpack(L, recv, "f32", ["f32", "f32"])
+    for key, pl in got.items():
+        for p in range(2):
+            np.testing.assert_array_equal(pl[p], numeric.to_f64(plain[key][p], "f32"))
