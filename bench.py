@@ -296,7 +296,8 @@ def run_ours(args):
 
     # end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args)
-    extra = {} if args.no_extra else bandwidth_at_scale(dev, flush, peaks)
+    extra = {} if args.no_extra else {**bandwidth_at_scale(dev, flush, peaks),
+                                      **receive_prep_at_scale(dev, flush)}
 
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
@@ -388,6 +389,66 @@ def bandwidth_at_scale(dev, flush, peaks):
     res["cfg_wan_GBs"] = round(3 * cfg.numel() * 2 / (ms * 1e-3) / 1e9, 1)
     del pred, cfg
     torch.cuda.empty_cache()
+    return res
+
+
+def receive_prep_at_scale(dev, flush):
+    """The receive preparation with RoPE on Q and K against the plain
+    seq->head unpack, on the FLUX-like (U=4) and Wan-like (U=8, R=4) shapes,
+    and the paired text/image pack against the plain pack on the FLUX-like
+    shape; each launch timed alone with L2 flushed before it (median of 10).
+    Bytes: the wire read, the head-layout planes written and, with RoPE, the
+    two float32 angle tables read once."""
+    import torch
+    import sequence_attention_gb300 as sa
+    import synth
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(13):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 3:
+                ts.append(s.elapsed_time(e))
+        return statistics.median(ts)
+
+    res = {}
+    for name, U in (("flux1024", 4), ("wan", 8)):
+        w = synth.WORKLOADS[name]
+        L = sa.dit_sp_layout_init(w.B, w.S, w.H, w.D, U, w.R)
+        recv = torch.randn(L.wire_elems(3), dtype=torch.bfloat16, device=dev)
+        heads = [torch.empty(L.head_shape(), dtype=t, device=dev)
+                 for t in (torch.bfloat16, torch.bfloat16, torch.float16)]
+        cos, sin = (t.to(dev) for t in synth.rope_tables_joint(w.S_txt, w.S, w.D))
+        moved = 2 * 3 * w.B * w.S * L.Hp * w.D * 2
+        tables = 2 * w.S * (w.D // 2) * 4
+        tag = "flux" if name == "flux1024" else name
+        ms = timed(lambda: sa.dit_ulysses_unpack(L, sa.DIT_SEQ_TO_HEAD, recv, heads))
+        res[f"unpack_{tag}_ms"] = round(ms, 4)
+        res[f"unpack_{tag}_GBs"] = round(moved / (ms * 1e-3) / 1e9, 1)
+        ms = timed(lambda: sa.dit_ulysses_unpack_rope(L, recv, heads, cos, sin, 0b011))
+        res[f"unpack_rope_{tag}_ms"] = round(ms, 4)
+        res[f"unpack_rope_{tag}_GBs"] = round((moved + tables) / (ms * 1e-3) / 1e9, 1)
+        if w.S_txt > 0:
+            joint = [torch.randn((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+            txt = [j[:, :w.S_txt].contiguous() for j in joint]
+            img = [j[:, w.S_txt:].contiguous() for j in joint]
+            send = torch.empty(L.wire_elems(3), dtype=torch.bfloat16, device=dev)
+            pmoved = 3 * w.B * w.S * (w.H + L.Hp) * w.D * 2
+            ms = timed(lambda: sa.dit_ulysses_pack(L, sa.DIT_SEQ_TO_HEAD, joint, send))
+            res[f"pack_{tag}_ms"] = round(ms, 4)
+            res[f"pack_{tag}_GBs"] = round(pmoved / (ms * 1e-3) / 1e9, 1)
+            ms = timed(lambda: sa.dit_ulysses_pack_joint(L, txt, img, send))
+            res[f"pack_joint_{tag}_ms"] = round(ms, 4)
+            res[f"pack_joint_{tag}_GBs"] = round(pmoved / (ms * 1e-3) / 1e9, 1)
+            del joint, txt, img, send
+        del recv, heads
+        torch.cuda.empty_cache()
     return res
 
 

@@ -7,6 +7,10 @@
  *   dit_sp_layout_init / dit_sp_a2a_counts   rank partition bookkeeping
  *   dit_ulysses_pack / dit_a2a_sim / dit_ulysses_unpack
  *                                            the Ulysses all-to-all, both ways
+ *   dit_ulysses_pack_joint / dit_ulysses_unpack_joint
+ *                                            the same for paired text/image
+ *                                            streams (joint sequence)
+ *   dit_ulysses_unpack_rope                  receive preparation with RoPE
  *   dit_sp_signal / dit_a2a_sim_checked      the exchange with arrival counters
  *                                            and a bounded wait
  *   dit_attn_partial                         attention of query blocks against
@@ -221,6 +225,56 @@ DIT_API dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir, i
                               const void* recv, dit_dtype wire_dt,
                               void* const* dst, const dit_dtype* dst_dt,
                               int* d_range_flag, void* stream);
+
+/*
+ * Paired text and image streams (edge-dit.cpp "Parallel execution": the
+ * packed QKV path has a variant for the paired streams of FLUX double-stream
+ * blocks, decoded and assembled into the joint attention sequence).  The
+ * joint sequence is the S_txt text tokens followed by the S - S_txt image
+ * tokens; the layout L splits the joint sequence as usual, so a rank's rows
+ * may come from either stream or both.
+ *
+ * dit_ulysses_pack_joint: as dit_ulysses_pack(DIT_SEQ_TO_HEAD), with plane p
+ *   read from txt[p] ([B][S_txt][H][D]) for joint rows t < S_txt and from
+ *   img[p] ([B][S - S_txt][H][D]) at row t - S_txt for the others.  0 <= S_txt
+ *   <= S; txt (img) may be NULL when S_txt == 0 (S_txt == S).  The send
+ *   buffer is bit-identical to dit_ulysses_pack of the concatenated planes.
+ * dit_ulysses_unpack_joint: as dit_ulysses_unpack(DIT_HEAD_TO_SEQ), writing
+ *   joint rows t < S_txt to out_txt [B][S_txt][H][D] and the others to
+ *   out_img [B][S - S_txt][H][D] at row t - S_txt, in out_dt.
+ * Errors and alignment as for dit_ulysses_pack / dit_ulysses_unpack.
+ */
+DIT_API dit_status dit_ulysses_pack_joint(const dit_sp_layout* L, int nplanes, const void* const* txt,
+                                          const void* const* img, int S_txt, dit_dtype src_dt, void* send,
+                                          dit_dtype wire_dt, void* stream);
+
+DIT_API dit_status dit_ulysses_unpack_joint(const dit_sp_layout* L, const void* recv, dit_dtype wire_dt,
+                                            void* out_txt, void* out_img, int S_txt, dit_dtype out_dt,
+                                            void* stream);
+
+/*
+ * dit_ulysses_unpack_rope: the receive preparation (edge-dit.cpp "Parallel
+ * execution": one pass decodes the rank-major receive buffer, extracts the
+ * Q/K/V planes, writes the head-sharded layout and applies RoPE to Q and K,
+ * with V in its attention layout).  As dit_ulysses_unpack(DIT_SEQ_TO_HEAD),
+ * except that every plane p with bit p of rope_planes set is rotated while
+ * it is written: for the token at joint-sequence position t and each pair
+ * i < D/2 of every head,
+ *   y[2i]   = x[2i] * cos_tab[t*D/2 + i] - x[2i+1] * sin_tab[t*D/2 + i]
+ *   y[2i+1] = x[2i] * sin_tab[t*D/2 + i] + x[2i+1] * cos_tab[t*D/2 + i]
+ * with x the received value in fp32, computed in fp32 (one rounded product
+ * and one fused multiply-add per output) and rounded to dst_dt[p].
+ *   cos_tab, sin_tab  device, float32 [S][D/2] row-major, 16-byte aligned,
+ *                     caller-owned (the model's angles: the pages give none).
+ *   rope_planes       bit mask over the nplanes planes (0x3 = Q and K);
+ *                     0 gives dit_ulysses_unpack exactly.
+ * Padded heads stay zero.  d_range_flag as for dit_ulysses_unpack (a 16-bit
+ * destination value that becomes infinite sets it).
+ */
+DIT_API dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplanes, const void* recv,
+                                           dit_dtype wire_dt, void* const* dst, const dit_dtype* dst_dt,
+                                           const float* cos_tab, const float* sin_tab, unsigned rope_planes,
+                                           int* d_range_flag, void* stream);
 
 /*
  * dit_attn_partial: for every query block r < n_q and key/value block

@@ -31,6 +31,7 @@ __all__ = [
     "dit_sp_layout_init", "dit_sp_a2a_counts", "dit_ulysses_pack", "dit_a2a_sim",
     "dit_ulysses_unpack", "dit_attn_partial", "dit_attn_merge_lse", "dit_attention",
     "dit_cfg_combine", "dit_device_status", "library_path", "dit_sp_signal", "dit_a2a_sim_checked",
+    "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint", "dit_ulysses_unpack_rope",
 ]
 
 lib()   # load now: fail at import time, not at first call
@@ -136,6 +137,44 @@ def dit_ulysses_unpack(L: Layout, direction: int, recv: torch.Tensor, dsts: Sequ
     dts = (c_int * 3)(*[_dt(d) for d in dsts])
     check(lib().dit_ulysses_unpack(byref(L.raw), direction, len(dsts), _ptr(recv), _dt(recv), ptrs,
                                    dts, _ptr(range_flag), _stream(stream)))
+
+
+def _ptrs(ts: Optional[Sequence[torch.Tensor]], n: int):
+    return None if ts is None else (c_void_p * n)(*[t.data_ptr() for t in ts])
+
+
+def dit_ulysses_pack_joint(L: Layout, txt: Optional[Sequence[torch.Tensor]], img: Optional[Sequence[torch.Tensor]],
+                           send: torch.Tensor, stream=None) -> None:
+    """Seq->head pack of the joint sequence [text; image]: txt[p] [B,S_txt,H,D],
+    img[p] [B,S-S_txt,H,D] (either may be None when it has no rows)."""
+    planes = txt if txt is not None else img
+    n = len(planes)
+    S_txt = txt[0].shape[1] if txt is not None else 0
+    check(lib().dit_ulysses_pack_joint(byref(L.raw), n, _ptrs(txt, n), _ptrs(img, n), S_txt, _dt(planes[0]),
+                                       _ptr(send), _dt(send), _stream(stream)))
+
+
+def dit_ulysses_unpack_joint(L: Layout, recv: torch.Tensor, out_txt: Optional[torch.Tensor],
+                             out_img: Optional[torch.Tensor], stream=None) -> None:
+    """Head->seq unpack into the text rows (out_txt) and image rows (out_img)."""
+    S_txt = out_txt.shape[1] if out_txt is not None else 0
+    out = out_txt if out_txt is not None else out_img
+    check(lib().dit_ulysses_unpack_joint(byref(L.raw), _ptr(recv), _dt(recv), _ptr(out_txt), _ptr(out_img),
+                                         S_txt, _dt(out), _stream(stream)))
+
+
+def dit_ulysses_unpack_rope(L: Layout, recv: torch.Tensor, dsts: Sequence[torch.Tensor], cos: torch.Tensor,
+                            sin: torch.Tensor, rope_planes: int = 0x3,
+                            range_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Seq->head unpack that rotates the planes in rope_planes; cos/sin are
+    float32 [S, D/2] tables of the joint sequence's positions."""
+    for t in (cos, sin):
+        if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (L.raw.S, L.raw.D // 2):
+            raise ValueError("rotary tables must be contiguous float32 [S, D/2]")
+    ptrs = (c_void_p * 3)(*[d.data_ptr() for d in dsts])
+    dts = (c_int * 3)(*[_dt(d) for d in dsts])
+    check(lib().dit_ulysses_unpack_rope(byref(L.raw), len(dsts), _ptr(recv), _dt(recv), ptrs, dts, _ptr(cos),
+                                        _ptr(sin), rope_planes, _ptr(range_flag), _stream(stream)))
 
 
 def _view(t: torch.Tensor, kind: str) -> DitView:

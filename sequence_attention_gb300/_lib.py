@@ -25,7 +25,8 @@ EXPORTS = (
     "dit_status_string", "dit_last_error", "dit_device_status", "dit_sp_layout_init",
     "dit_sp_a2a_counts", "dit_ulysses_pack", "dit_a2a_sim", "dit_ulysses_unpack",
     "dit_attn_partial", "dit_attn_merge_lse", "dit_attention", "dit_cfg_combine",
-    "dit_sp_signal", "dit_a2a_sim_checked",
+    "dit_sp_signal", "dit_a2a_sim_checked", "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint",
+    "dit_ulysses_unpack_rope",
 )
 
 
@@ -88,6 +89,15 @@ def lib() -> ctypes.CDLL:
     L.dit_ulysses_unpack.restype = c_int
     L.dit_ulysses_unpack.argtypes = [POINTER(DitSpLayout), c_int, c_int, c_void_p, c_int,
                                      POINTER(c_void_p), POINTER(c_int), c_void_p, c_void_p]
+    L.dit_ulysses_pack_joint.restype = c_int
+    L.dit_ulysses_pack_joint.argtypes = [POINTER(DitSpLayout), c_int, POINTER(c_void_p), POINTER(c_void_p),
+                                         c_int, c_int, c_void_p, c_int, c_void_p]
+    L.dit_ulysses_unpack_joint.restype = c_int
+    L.dit_ulysses_unpack_joint.argtypes = [POINTER(DitSpLayout), c_void_p, c_int, c_void_p, c_void_p, c_int,
+                                           c_int, c_void_p]
+    L.dit_ulysses_unpack_rope.restype = c_int
+    L.dit_ulysses_unpack_rope.argtypes = [POINTER(DitSpLayout), c_int, c_void_p, c_int, POINTER(c_void_p),
+                                          POINTER(c_int), c_void_p, c_void_p, c_uint, c_void_p, c_void_p]
     L.dit_attn_partial.restype = c_int
     L.dit_attn_partial.argtypes = [c_int, c_int, c_int, c_float, c_int, POINTER(c_int), c_int,
                                    POINTER(c_int), DitView, c_int, DitView, DitView, c_int, DitView,

@@ -17,6 +17,17 @@
 // Head-to-seq: pack writes B, the exchange copies B->A, unpack reads A.
 // Each kernel walks the runs in its destination's order (A, B, head-layout
 // or sequence order), so its writes are sequential and its reads gather.
+//
+// Two additions of the receive preparation and of the FLUX double-stream
+// blocks (edge-dit.cpp "Parallel execution"):
+//  - paired streams: the sequence side of a call may live in two tensors,
+//    text rows [0, split) and image rows [split, S) of the joint sequence,
+//    so that the pack assembles the joint sequence and the head-to-seq
+//    unpack splits it again without a concatenation or a slice copy;
+//  - rotary embedding: the seq-to-head unpack may rotate chosen planes
+//    (Q, K) while it writes the head layout, each interleaved pair (2i, 2i+1)
+//    of a token at joint position t by the angle whose cosine and sine are
+//    cos[t][i], sin[t][i]:  (x0, x1) -> (x0 c - x1 s, x0 s + x1 c), in fp32.
 #include <string.h>
 
 #include "common.cuh"
@@ -40,6 +51,16 @@ struct RunArgs {
     unsigned epoch;
     long long timeout_ns;
     int* status;
+    // paired streams (split > 0): sequence-side rows t >= split live in
+    // src2/dst2 at row t - split; split == 0 means a single stream
+    const void* src2[3];
+    void* dst2[3];
+    int split;
+    // rotary embedding of the seq->head unpack: tables [S][D/2] (fp32),
+    // applied to plane p when bit p of rope_planes is set
+    const float* rope_cos;
+    const float* rope_sin;
+    unsigned rope_planes;
 };
 
 struct Run {
@@ -152,10 +173,18 @@ __device__ __forceinline__ long long index_B(const dit_sp_layout& L, int np, con
 }
 
 // element offset of the run's first head in a seq-layout plane [B][S][H][D]
-// (only meaningful when the group has a real head)
-__device__ __forceinline__ long long seq_offset(const dit_sp_layout& L, const Run& x) {
-    const int row = L.rank_off[x.r * L.U + x.u] + x.i;
-    return (((long long)x.b * L.S + row) * L.H + (long long)x.v * L.Hl) * L.D;
+// (only meaningful when the group has a real head).  With paired streams,
+// rows at or past `split` are in the second tensor, [B][S - split][H][D];
+// `second` says which.
+__device__ __forceinline__ long long seq_offset(const dit_sp_layout& L, const Run& x, int split, bool& second) {
+    int row = L.rank_off[x.r * L.U + x.u] + x.i;
+    int rows = L.S;
+    second = split > 0 && row >= split;
+    if (split > 0) {
+        rows = second ? L.S - split : split;
+        if (second) row -= split;
+    }
+    return (((long long)x.b * rows + row) * L.H + (long long)x.v * L.Hl) * L.D;
 }
 
 // element offset in a head-layout plane [R][B][S_cap][Hp][D]
@@ -193,6 +222,7 @@ struct RunIO {
     int dst_lim;      // chunks of the destination written; later chunks skipped
     int sdt, ddt;     // dit_dtype of source and destination
     int sender;       // virtual rank that sent this run (exchange kernels)
+    int rope_pos;     // joint-sequence position whose angles rotate the run; -1: none
 };
 
 template <int MODE>
@@ -212,17 +242,19 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
     const int full = (L.Hl * L.D) >> 3, real = (nreal * L.D) >> 3;
     RunIO io;
     io.src_lim = io.dst_lim = full;
+    io.rope_pos = -1;
     long long so = 0, doff = 0;
     dit_dtype sdt, ddt;
+    bool second = false;
     if (MODE == PACK_S2H) {
         sdt = A.src_dt[p]; ddt = A.dst_dt[0];
-        so = nreal > 0 ? seq_offset(L, x) : 0; doff = ri * run_elems;
-        io.src = (const char*)A.src[p]; io.dst = (char*)A.dst[0];
+        so = nreal > 0 ? seq_offset(L, x, A.split, second) : 0; doff = ri * run_elems;
+        io.src = (const char*)(second ? A.src2[p] : A.src[p]); io.dst = (char*)A.dst[0];
         io.src_lim = real;
     } else if (MODE == UNPACK_H2S) {
         sdt = A.src_dt[0]; ddt = A.dst_dt[0];
-        so = index_A(L, A.np, x) * run_elems; doff = nreal > 0 ? seq_offset(L, x) : 0;
-        io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[0];
+        so = index_A(L, A.np, x) * run_elems; doff = nreal > 0 ? seq_offset(L, x, A.split, second) : 0;
+        io.src = (const char*)A.src[0]; io.dst = (char*)(second ? A.dst2[0] : A.dst[0]);
         io.dst_lim = real;
     } else if (MODE == PACK_H2S) {
         sdt = A.src_dt[0]; ddt = A.dst_dt[0];
@@ -233,6 +265,7 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
         sdt = A.src_dt[0]; ddt = A.dst_dt[p];
         so = index_B(L, A.np, x) * run_elems; doff = head_offset(L, x);
         io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[p];
+        if ((A.rope_planes >> p) & 1u) io.rope_pos = L.rank_off[x.r * L.U + x.u] + x.i;
     } else if (MODE == A2A_S2H) {
         sdt = ddt = A.src_dt[0];
         so = index_A(L, A.np, x) * run_elems; doff = ri * run_elems;
@@ -281,7 +314,42 @@ __device__ __forceinline__ void convert8(const uint4 (&in)[SB / 2], dit_dtype sd
     }
 }
 
+// Rotate the four interleaved pairs held in 8 elements by the angles with
+// cosines c and sines s, in fp32, then convert to the destination type.
+template <int SB, int DB>
+__device__ __forceinline__ void rope8(const uint4 (&in)[SB / 2], dit_dtype sdt, dit_dtype ddt, float4 c, float4 s,
+                                      bool check, uint4 (&out)[DB / 2], bool& overflow) {
+    Vec8 v;
+    load8(&in[0], sdt, v);
+    const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {s.x, s.y, s.z, s.w};
+    Vec8 y;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float x0 = v.f[2 * k], x1 = v.f[2 * k + 1];
+        y.f[2 * k] = fmaf(x0, cc[k], -(x1 * ss[k]));
+        y.f[2 * k + 1] = fmaf(x0, ss[k], x1 * cc[k]);
+    }
+    if constexpr (DB == 4) {
+        out[0] = make_uint4(__float_as_uint(y.f[0]), __float_as_uint(y.f[1]), __float_as_uint(y.f[2]),
+                            __float_as_uint(y.f[3]));
+        out[1] = make_uint4(__float_as_uint(y.f[4]), __float_as_uint(y.f[5]), __float_as_uint(y.f[6]),
+                            __float_as_uint(y.f[7]));
+    } else {
+        out[0] = make_uint4(pack2(y.f[0], y.f[1], ddt), pack2(y.f[2], y.f[3], ddt),
+                            pack2(y.f[4], y.f[5], ddt), pack2(y.f[6], y.f[7], ddt));
+        if (check) {
+            Vec8 back;
+            load8(&out[0], ddt, back);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) overflow |= isinf(back.f[e]) && !isinf(y.f[e]);
+        }
+    }
+}
+
 constexpr int kThreads = 256;
+// the rotary path stages 32 runs x 2 x D/2 floats in shared memory: D <= 384
+// keeps that within the 48 KB a block gets without opting in
+constexpr int kRopeMaxD = 384;
 constexpr int kItems = 8;       // 8-element items per lane in flight
 
 // Each block takes 8 * rpw consecutive runs (rpw = runs per warp, 4, or 2
@@ -289,9 +357,17 @@ constexpr int kItems = 8;       // 8-element items per lane in flight
 // one run each into shared memory, then each warp streams its rpw runs,
 // lanes over their 8-element chunks.  Per group of kItems items a lane
 // issues every load first, converts in registers, then stores.
-template <int MODE, int SB, int DB>
-__global__ void __launch_bounds__(kThreads) run_kernel(const __grid_constant__ RunArgs A, int rpw) {
+// The rotary variant is held to three blocks per SM (80 registers): measured
+// on the Wan-like shape it moves 3.8 TB/s that way against 2.9 TB/s at two
+// blocks per SM with no spill.
+template <int MODE, int SB, int DB, bool ROPE>
+__global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __grid_constant__ RunArgs A, int rpw) {
     __shared__ RunIO ios[kThreads];
+    // rotary path: each run's table rows (cos, then sin; D/8 float4 each),
+    // loaded once per distinct token of the block; slot[] = the run whose
+    // rows a run uses
+    extern __shared__ float4 rope_sm[];
+    __shared__ short slot[ROPE ? kThreads : 1];
     const int rpb = rpw * (kThreads / 32);
     const long long r0 = (long long)blockIdx.x * rpb;
     const int nrun = (int)min((long long)rpb, A.nruns - r0);
@@ -320,6 +396,27 @@ __global__ void __launch_bounds__(kThreads) run_kernel(const __grid_constant__ R
         if (!arrived) io.src_lim = io.dst_lim = 0;
     }
     __syncthreads();
+    const int dch = A.L.D >> 3;          // chunks per head = float4s per table row
+    if constexpr (ROPE) {
+        if ((int)threadIdx.x < nrun) {
+            // runs of one token are adjacent (head groups innermost)
+            const int pos = ios[threadIdx.x].rope_pos;
+            int l = threadIdx.x;
+            while (l > 0 && ios[l - 1].rope_pos == pos) --l;
+            slot[threadIdx.x] = (short)l;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < nrun * dch; e += kThreads) {
+            const int run = e / dch, c = e - run * dch;
+            const int pos = ios[run].rope_pos;
+            if (pos >= 0 && slot[run] == run) {
+                const long long off = (long long)pos * (A.L.D >> 1) + 4 * c;
+                rope_sm[(2 * run) * dch + c] = *reinterpret_cast<const float4*>(A.rope_cos + off);
+                rope_sm[(2 * run + 1) * dch + c] = *reinterpret_cast<const float4*>(A.rope_sin + off);
+            }
+        }
+        __syncthreads();
+    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g0 = warp * rpw;
     const int gn = min(rpw, nrun - g0);
@@ -331,18 +428,19 @@ __global__ void __launch_bounds__(kThreads) run_kernel(const __grid_constant__ R
     const int items = gn * nch;
     const bool want_check = (MODE == UNPACK_S2H) && A.range_flag != nullptr;
     bool overflow = false;
+    constexpr int NI = kItems;
     int g = lane / nch, c = lane - (lane / nch) * nch;   // item k0 = lane
-    for (int k0 = lane; k0 < items; k0 += 32 * kItems) {
-        uint4 raw[kItems][SB / 2];
-        int gi[kItems], ci[kItems];
+    for (int k0 = lane; k0 < items; k0 += 32 * NI) {
+        uint4 raw[NI][SB / 2];
+        int gi[NI], ci[NI];
 #pragma unroll
-        for (int t = 0; t < kItems; ++t) {
+        for (int t = 0; t < NI; ++t) {
             gi[t] = g; ci[t] = c;
             c += 32;
             while (c >= nch) { c -= nch; ++g; }
         }
 #pragma unroll
-        for (int t = 0; t < kItems; ++t) {
+        for (int t = 0; t < NI; ++t) {
 #pragma unroll
             for (int h = 0; h < SB / 2; ++h) raw[t][h] = make_uint4(0, 0, 0, 0);
             if (k0 + 32 * t < items) {
@@ -355,13 +453,18 @@ __global__ void __launch_bounds__(kThreads) run_kernel(const __grid_constant__ R
             }
         }
 #pragma unroll
-        for (int t = 0; t < kItems; ++t) {
+        for (int t = 0; t < NI; ++t) {
             if (k0 + 32 * t < items) {
                 const RunIO& io = ios[g0 + gi[t]];
                 if (ci[t] < io.dst_lim) {
                     const dit_dtype sdt = (dit_dtype)io.sdt, ddt = (dit_dtype)io.ddt;
                     uint4 o[DB / 2];
-                    convert8<SB, DB>(raw[t], sdt, ddt, want_check && narrowing(sdt, ddt), o, overflow);
+                    if (ROPE && io.rope_pos >= 0) {
+                        const int sl = slot[ROPE ? g0 + gi[t] : 0], c = ci[t] % dch;
+                        rope8<SB, DB>(raw[t], sdt, ddt, rope_sm[(2 * sl) * dch + c], rope_sm[(2 * sl + 1) * dch + c],
+                                      want_check && ddt != DIT_F32, o, overflow);
+                    } else
+                        convert8<SB, DB>(raw[t], sdt, ddt, want_check && narrowing(sdt, ddt), o, overflow);
                     uint4* q = reinterpret_cast<uint4*>(io.dst + (long long)ci[t] * 8 * DB);
 #pragma unroll
                     for (int h = 0; h < DB / 2; ++h) q[h] = o[h];
@@ -391,7 +494,7 @@ dit_status check_layout(const dit_sp_layout* L, const char* who) {
     return DIT_OK;
 }
 
-template <int MODE, int SB, int DB>
+template <int MODE, int SB, int DB, bool ROPE>
 dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
     // 4 runs per warp keep each block's fixed decode latency small against
     // its copy time; drop to 2 only when the grid would otherwise have fewer
@@ -400,7 +503,9 @@ dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
     int rpw = 4;
     if ((a.nruns + 31) / 32 < 2 * slots) rpw = 2;
     const long long blocks = (a.nruns + 8LL * rpw - 1) / (8LL * rpw);
-    cudaError_t e = launch_pdl(run_kernel<MODE, SB, DB>, dim3((unsigned)blocks), dim3(kThreads), 0, st, a, rpw);
+    // rotary tables: two rows of D/2 floats for each of the block's runs
+    const size_t smem = ROPE ? (size_t)8 * rpw * a.L.D * sizeof(float) : 0;
+    cudaError_t e = launch_pdl(run_kernel<MODE, SB, DB, ROPE>, dim3((unsigned)blocks), dim3(kThreads), smem, st, a, rpw);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     return check_launch(who);
 }
@@ -408,7 +513,7 @@ dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
 // Element sizes are template parameters so that 16-bit paths hold 16-byte
 // items; every plane of one call must use source (and destination) types
 // of one size.
-template <int MODE>
+template <int MODE, bool ROPE = false>
 dit_status launch_runs(const RunArgs& a, cudaStream_t st, const char* who) {
     if (a.nruns == 0) return DIT_OK;
     if (a.nruns >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 2^31 runs", who);
@@ -420,10 +525,10 @@ dit_status launch_runs(const RunArgs& a, cudaStream_t st, const char* who) {
         if (a.dst[p] && dtype_bytes(a.dst_dt[p]) != db)
             return fail(DIT_ERR_UNSUPPORTED, "%s: planes of one call need destination types of one size", who);
     }
-    if (sb == 2 && db == 2) return launch_sized<MODE, 2, 2>(a, st, who);
-    if (sb == 4 && db == 4) return launch_sized<MODE, 4, 4>(a, st, who);
-    if (sb == 4 && db == 2) return launch_sized<MODE, 4, 2>(a, st, who);
-    return launch_sized<MODE, 2, 4>(a, st, who);
+    if (sb == 2 && db == 2) return launch_sized<MODE, 2, 2, ROPE>(a, st, who);
+    if (sb == 4 && db == 4) return launch_sized<MODE, 4, 4, ROPE>(a, st, who);
+    if (sb == 4 && db == 2) return launch_sized<MODE, 4, 2, ROPE>(a, st, who);
+    return launch_sized<MODE, 2, 4, ROPE>(a, st, who);
 }
 
 }  // namespace
@@ -553,4 +658,98 @@ extern "C" dit_status dit_a2a_sim_checked(const dit_sp_layout* L, dit_a2a_dir di
     if (!a.status) return fail(DIT_ERR_CUDA, "%s: no device status word", who);
     cudaStream_t st = (cudaStream_t)stream;
     return dir == DIT_SEQ_TO_HEAD ? launch_runs<A2A_S2H>(a, st, who) : launch_runs<A2A_H2S>(a, st, who);
+}
+
+extern "C" dit_status dit_ulysses_pack_joint(const dit_sp_layout* L, int nplanes, const void* const* txt,
+                                             const void* const* img, int S_txt, dit_dtype src_dt, void* send,
+                                             dit_dtype wire_dt, void* stream) {
+    const char* who = "dit_ulysses_pack_joint";
+    dit_status s = check_layout(L, who);
+    if (s != DIT_OK) return s;
+    if (!dtype_ok(src_dt) || !dtype_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
+    if (S_txt < 0 || S_txt > L->S) return fail(DIT_ERR_INVALID_ARG, "%s: S_txt out of [0, S]", who);
+    if (!send || !aligned16(send)) return fail(DIT_ERR_INVALID_ARG, "%s: send NULL or misaligned", who);
+    const bool has_txt = S_txt > 0, has_img = S_txt < L->S;
+    if ((has_txt && !txt) || (has_img && !img)) return fail(DIT_ERR_INVALID_ARG, "%s: stream array NULL", who);
+    RunArgs a;
+    memset(&a, 0, sizeof(a));
+    a.L = *L;
+    a.np = nplanes;
+    for (int p = 0; p < nplanes; ++p) {
+        if (has_txt && (!txt[p] || !aligned16(txt[p])))
+            return fail(DIT_ERR_INVALID_ARG, "%s: txt[%d] NULL or misaligned", who, p);
+        if (has_img && (!img[p] || !aligned16(img[p])))
+            return fail(DIT_ERR_INVALID_ARG, "%s: img[%d] NULL or misaligned", who, p);
+        // one stream only: it is the whole sequence
+        a.src[p] = has_txt ? txt[p] : img[p];
+        a.src2[p] = has_txt && has_img ? img[p] : nullptr;
+        a.src_dt[p] = src_dt;
+    }
+    a.split = has_txt && has_img ? S_txt : 0;
+    a.dst[0] = send;
+    a.dst_dt[0] = wire_dt;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    return launch_runs<PACK_S2H>(a, (cudaStream_t)stream, who);
+}
+
+extern "C" dit_status dit_ulysses_unpack_joint(const dit_sp_layout* L, const void* recv, dit_dtype wire_dt,
+                                               void* out_txt, void* out_img, int S_txt, dit_dtype out_dt,
+                                               void* stream) {
+    const char* who = "dit_ulysses_unpack_joint";
+    dit_status s = check_layout(L, who);
+    if (s != DIT_OK) return s;
+    if (!dtype_ok(wire_dt) || !dtype_ok(out_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (S_txt < 0 || S_txt > L->S) return fail(DIT_ERR_INVALID_ARG, "%s: S_txt out of [0, S]", who);
+    if (!recv || !aligned16(recv)) return fail(DIT_ERR_INVALID_ARG, "%s: recv NULL or misaligned", who);
+    const bool has_txt = S_txt > 0, has_img = S_txt < L->S;
+    if ((has_txt && (!out_txt || !aligned16(out_txt))) || (has_img && (!out_img || !aligned16(out_img))))
+        return fail(DIT_ERR_INVALID_ARG, "%s: output stream NULL or misaligned", who);
+    RunArgs a;
+    memset(&a, 0, sizeof(a));
+    a.L = *L;
+    a.np = 1;
+    a.src[0] = recv; a.src_dt[0] = wire_dt;
+    a.dst[0] = has_txt ? out_txt : out_img;
+    a.dst2[0] = has_txt && has_img ? out_img : nullptr;
+    a.dst_dt[0] = out_dt;
+    a.split = has_txt && has_img ? S_txt : 0;
+    a.nruns = (long long)L->B * L->U * L->S;
+    return launch_runs<UNPACK_H2S>(a, (cudaStream_t)stream, who);
+}
+
+extern "C" dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplanes, const void* recv,
+                                              dit_dtype wire_dt, void* const* dst, const dit_dtype* dst_dt,
+                                              const float* cos_tab, const float* sin_tab, unsigned rope_planes,
+                                              int* d_range_flag, void* stream) {
+    const char* who = "dit_ulysses_unpack_rope";
+    dit_status s = check_layout(L, who);
+    if (s != DIT_OK) return s;
+    if (!dtype_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad wire dtype", who);
+    if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
+    if (rope_planes >> nplanes) return fail(DIT_ERR_INVALID_ARG, "%s: rope_planes names a missing plane", who);
+    if (rope_planes && (!cos_tab || !sin_tab || !aligned16(cos_tab) || !aligned16(sin_tab)))
+        return fail(DIT_ERR_INVALID_ARG, "%s: rotary tables NULL or misaligned", who);
+    if (rope_planes && L->D > kRopeMaxD)
+        return fail(DIT_ERR_UNSUPPORTED, "%s: rotary path supports D <= %d", who, kRopeMaxD);
+    if (!recv || !aligned16(recv) || !dst || !dst_dt)
+        return fail(DIT_ERR_INVALID_ARG, "%s: recv/dst NULL or misaligned", who);
+    RunArgs a;
+    memset(&a, 0, sizeof(a));
+    a.L = *L;
+    a.np = nplanes;
+    a.src[0] = recv; a.src_dt[0] = wire_dt;
+    for (int p = 0; p < nplanes; ++p) {
+        if (!dst[p] || !aligned16(dst[p])) return fail(DIT_ERR_INVALID_ARG, "%s: dst[%d] NULL or misaligned", who, p);
+        if (!dtype_ok(dst_dt[p])) return fail(DIT_ERR_INVALID_ARG, "%s: bad dst dtype", who);
+        a.dst[p] = dst[p];
+        a.dst_dt[p] = dst_dt[p];
+    }
+    a.range_flag = d_range_flag;
+    a.rope_cos = cos_tab;
+    a.rope_sin = sin_tab;
+    a.rope_planes = rope_planes;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    cudaStream_t st = (cudaStream_t)stream;
+    return rope_planes ? launch_runs<UNPACK_S2H, true>(a, st, who) : launch_runs<UNPACK_S2H>(a, st, who);
 }

@@ -14,18 +14,25 @@ redistributed data, then the inverse all-to-all; SGLang Diffusion
   dit_ulysses_pack(H2S), dit_a2a_sim(H2S), dit_ulysses_unpack(H2S)
                           head layout -> seq-sharded output [B,S,H,D]
 
+With rotary tables, the seq-to-head unpack is the receive preparation that
+rotates Q and K as it writes them (dit_ulysses_unpack_rope); run_joint()
+takes the paired text and image streams of a double-stream block and
+returns the output in the same two streams (dit_ulysses_pack_joint,
+dit_ulysses_unpack_joint), so the joint sequence is never concatenated.
+
 All buffers are allocated once, when the plan is built; run() allocates
 nothing and only enqueues kernels on the current (or given) stream.
 """
 from __future__ import annotations
 
 import math
-from typing import Optional
+from typing import Optional, Sequence, Tuple
 
 import torch
 
 from . import (DIT_HEAD_TO_SEQ, DIT_SEQ_TO_HEAD, dit_a2a_sim, dit_attn_merge_lse, dit_attn_partial,
-               dit_sp_layout_init, dit_ulysses_pack, dit_ulysses_unpack)
+               dit_sp_layout_init, dit_ulysses_pack, dit_ulysses_pack_joint, dit_ulysses_unpack,
+               dit_ulysses_unpack_joint, dit_ulysses_unpack_rope)
 
 
 class UspPlan:
@@ -33,14 +40,18 @@ class UspPlan:
                  in_dtype: torch.dtype = torch.bfloat16,
                  out_dtype: Optional[torch.dtype] = None,
                  v_dtype: Optional[torch.dtype] = None,
-                 device: str = "cuda", scale: Optional[float] = None):
+                 device: str = "cuda", scale: Optional[float] = None,
+                 rope: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+        """rope: optional (cos, sin) float32 [S, D/2] device tables of the
+        joint sequence; Q and K are then rotated by the receive preparation."""
         self.L = dit_sp_layout_init(B, S, H, D, U, R)
         self.B, self.S, self.H, self.D, self.U, self.R = B, S, H, D, U, R
         self.in_dtype = in_dtype
         self.wire_dtype = in_dtype
         self.out_dtype = out_dtype or in_dtype
         if v_dtype is None:
-            # P V runs with P in V's type: f16 keeps P to 11 bits (see DESIGN)
+            # P V runs with P in V's type: f16 keeps P to 11 significant bits,
+            # which keeps the ring merge within 1e-3 of single-shot attention
             v_dtype = torch.float16 if in_dtype == torch.bfloat16 else in_dtype
         self.v_dtype = v_dtype
         self.scale = 1.0 / math.sqrt(D) if scale is None else scale
@@ -60,6 +71,7 @@ class UspPlan:
             self.parts = self.lse_parts = None
         self.send_o = torch.empty(L.wire_elems(1), dtype=self.out_dtype, device=dev)
         self.recv_o = torch.empty(L.wire_elems(1), dtype=self.out_dtype, device=dev)
+        self.rope = rope
         self.range_flag = torch.zeros(1, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -78,12 +90,26 @@ class UspPlan:
             s.append("merge")
         return s + ["pack_h2s", "a2a_h2s", "unpack_h2s"]
 
-    def layout_in(self, q, k, v, stream=None):
+    def _receive(self, stream):
         L = self.L
-        dit_ulysses_pack(L, DIT_SEQ_TO_HEAD, [q, k, v], self.send, stream)
         dit_a2a_sim(L, DIT_SEQ_TO_HEAD, 3, self.send, self.recv, stream)
-        dit_ulysses_unpack(L, DIT_SEQ_TO_HEAD, self.recv, [self.q_h, self.k_h, self.v_h],
-                           self.range_flag, stream)
+        heads = [self.q_h, self.k_h, self.v_h]
+        if self.rope is not None:
+            dit_ulysses_unpack_rope(L, self.recv, heads, self.rope[0], self.rope[1], 0b011,
+                                    self.range_flag, stream)
+        else:
+            dit_ulysses_unpack(L, DIT_SEQ_TO_HEAD, self.recv, heads, self.range_flag, stream)
+
+    def layout_in(self, q, k, v, stream=None):
+        dit_ulysses_pack(self.L, DIT_SEQ_TO_HEAD, [q, k, v], self.send, stream)
+        self._receive(stream)
+
+    def layout_in_joint(self, txt: Optional[Sequence[torch.Tensor]], img: Optional[Sequence[torch.Tensor]],
+                        stream=None):
+        """txt / img: (q, k, v) of the text [B,S_txt,H,D] and image
+        [B,S-S_txt,H,D] streams (None for a stream without rows)."""
+        dit_ulysses_pack_joint(self.L, txt, img, self.send, stream)
+        self._receive(stream)
 
     def attend(self, stream=None):
         rl = self.ring_len
@@ -103,6 +129,18 @@ class UspPlan:
         dit_ulysses_pack(L, DIT_HEAD_TO_SEQ, [self.o_h], self.send_o, stream)
         dit_a2a_sim(L, DIT_HEAD_TO_SEQ, 1, self.send_o, self.recv_o, stream)
         dit_ulysses_unpack(L, DIT_HEAD_TO_SEQ, self.recv_o, [out], None, stream)
+
+    def layout_out_joint(self, out_txt, out_img, stream=None):
+        L = self.L
+        dit_ulysses_pack(L, DIT_HEAD_TO_SEQ, [self.o_h], self.send_o, stream)
+        dit_a2a_sim(L, DIT_HEAD_TO_SEQ, 1, self.send_o, self.recv_o, stream)
+        dit_ulysses_unpack_joint(L, self.recv_o, out_txt, out_img, stream)
+
+    def run_joint(self, txt, img, out_txt, out_img, stream=None):
+        """The double-stream block's attention: paired streams in and out."""
+        self.layout_in_joint(txt, img, stream)
+        self.attend(stream)
+        self.layout_out_joint(out_txt, out_img, stream)
 
     def run(self, q, k, v, out, stream=None):
         """q, k, v: [B, S, H, D] seq-sharded inputs; out: [B, S, H, D]."""

@@ -137,3 +137,30 @@ def test_merge_vs_single_shot_on_device():
     sa.dit_attn_merge_lse(parts, lse, merged, None, [w.S])
     torch.cuda.synchronize()
     assert rel_rms(f64(merged[0]), f64(single)) <= MERGE_REL_RMS
+
+
+@pytest.mark.parametrize("B,S,H,U,R,S_txt", [(1, 700, 5, 2, 2, 77), (2, 517, 4, 3, 1, 64)])
+def test_double_stream_block_with_rope(B, S, H, U, R, S_txt):
+    """Paired text/image streams in, receive preparation with RoPE, ring
+    attention, paired streams out, against the oracle's attention over the
+    rotated joint sequence (edge-dit.cpp, receive preparation and FLUX
+    double-stream blocks)."""
+    from oracle import rope as orope
+    from sequence_attention_gb300.usp import UspPlan
+    D = 128
+    qkv = [synth.normal((B, S, H, D), 40 + p, 0.5, "bf16") for p in range(3)]
+    cos, sin = synth.rope_tables_joint(S_txt, S, D)
+    plan = UspPlan(B, S, H, D, U, R, rope=(cos.cuda(), sin.cuda()))
+    txt = [t[:, :S_txt].contiguous().cuda() for t in qkv]
+    img = [t[:, S_txt:].contiguous().cuda() for t in qkv]
+    out_t = torch.empty((B, S_txt, H, D), dtype=torch.bfloat16, device="cuda")
+    out_i = torch.empty((B, S - S_txt, H, D), dtype=torch.bfloat16, device="cuda")
+    plan.run_joint(txt, img, out_t, out_i)
+    torch.cuda.synchronize()
+    c, s = cos.double().numpy(), sin.double().numpy()
+    q = orope.rope(f64(qkv[0]), c, s)
+    k = orope.rope(f64(qkv[1]), c, s)
+    ref, _ = oatt.attention(q, k, f64(qkv[2]))
+    got = np.concatenate([f64(out_t), f64(out_i)], axis=1)
+    assert_bf16_close(got, ref, "double-stream attention")
+    assert int(plan.range_flag.item()) == 0
