@@ -314,6 +314,13 @@ __device__ __forceinline__ void convert8(const uint4 (&in)[SB / 2], dit_dtype sd
     }
 }
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Rotate the four interleaved pairs held in 8 elements by the angles with
 // cosines c and sines s, in fp32, then convert to the destination type.
 template <int SB, int DB>
@@ -357,9 +364,9 @@ constexpr int kItems = 8;       // 8-element items per lane in flight
 // one run each into shared memory, then each warp streams its rpw runs,
 // lanes over their 8-element chunks.  Per group of kItems items a lane
 // issues every load first, converts in registers, then stores.
-// The rotary variant is held to three blocks per SM (80 registers): measured
-// on the Wan-like shape it moves 3.8 TB/s that way against 2.9 TB/s at two
-// blocks per SM with no spill.
+// The rotary variant is held to three blocks per SM (80 registers, 8 bytes
+// of spill for 16-bit types): on the Wan-like shape it moves 4.2 TB/s that
+// way against 2.9 TB/s at two blocks per SM without the cap.
 template <int MODE, int SB, int DB, bool ROPE>
 __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __grid_constant__ RunArgs A, int rpw) {
     __shared__ RunIO ios[kThreads];
@@ -398,44 +405,48 @@ __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __gri
     __syncthreads();
     const int dch = A.L.D >> 3;          // chunks per head = float4s per table row
     if constexpr (ROPE) {
-        if ((int)threadIdx.x < nrun) {
-            // runs of one token are adjacent (head groups innermost)
-            const int pos = ios[threadIdx.x].rope_pos;
-            int l = threadIdx.x;
+        // Runs of one token are adjacent (head groups innermost): the first
+        // run of each token copies its table rows into shared memory with
+        // asynchronous copies, which land while the first data loads below
+        // are in flight.
+        const int t = threadIdx.x;
+        if (t < nrun) {
+            const int pos = ios[t].rope_pos;
+            int l = t;
             while (l > 0 && ios[l - 1].rope_pos == pos) --l;
-            slot[threadIdx.x] = (short)l;
-        }
-        __syncthreads();
-        for (int e = threadIdx.x; e < nrun * dch; e += kThreads) {
-            const int run = e / dch, c = e - run * dch;
-            const int pos = ios[run].rope_pos;
-            if (pos >= 0 && slot[run] == run) {
-                const long long off = (long long)pos * (A.L.D >> 1) + 4 * c;
-                rope_sm[(2 * run) * dch + c] = *reinterpret_cast<const float4*>(A.rope_cos + off);
-                rope_sm[(2 * run + 1) * dch + c] = *reinterpret_cast<const float4*>(A.rope_sin + off);
+            slot[t] = (short)l;
+            if (pos >= 0 && l == t) {
+                const float* cs = A.rope_cos + (long long)pos * (A.L.D >> 1);
+                const float* sn = A.rope_sin + (long long)pos * (A.L.D >> 1);
+                for (int c = 0; c < dch; ++c) {
+                    cp_async16(&rope_sm[(2 * t) * dch + c], cs + 4 * c);
+                    cp_async16(&rope_sm[(2 * t + 1) * dch + c], sn + 4 * c);
+                }
             }
         }
-        __syncthreads();
+        cp_async_commit();
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g0 = warp * rpw;
     const int gn = min(rpw, nrun - g0);
-    if (gn <= 0) {
+    if (!ROPE && gn <= 0) {   // the rotary variant's warps all reach its barrier
         pdl_trigger();
         return;
     }
     const int nch = (A.L.Hl * A.L.D) >> 3;
-    const int items = gn * nch;
+    const int items = gn > 0 ? gn * nch : 0;
     const bool want_check = (MODE == UNPACK_S2H) && A.range_flag != nullptr;
     bool overflow = false;
     constexpr int NI = kItems;
     int g = lane / nch, c = lane - (lane / nch) * nch;   // item k0 = lane
-    for (int k0 = lane; k0 < items; k0 += 32 * NI) {
-        uint4 raw[NI][SB / 2];
-        int gi[NI], ci[NI];
+    uint4 raw[NI][SB / 2];
+    // item t of a batch: run g0 + (it[t] >> 16), chunk it[t] & 0xffff
+    // (fewer than 2^16 chunks per run, checked on the host)
+    int it[NI];
+    auto load_batch = [&](int k0) {
 #pragma unroll
         for (int t = 0; t < NI; ++t) {
-            gi[t] = g; ci[t] = c;
+            it[t] = (g << 16) | c;
             c += 32;
             while (c >= nch) { c -= nch; ++g; }
         }
@@ -444,32 +455,56 @@ __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __gri
 #pragma unroll
             for (int h = 0; h < SB / 2; ++h) raw[t][h] = make_uint4(0, 0, 0, 0);
             if (k0 + 32 * t < items) {
-                const RunIO& io = ios[g0 + gi[t]];
-                if (ci[t] < io.src_lim) {
-                    const uint4* q = reinterpret_cast<const uint4*>(io.src + (long long)ci[t] * 8 * SB);
+                const int ci = it[t] & 0xffff;
+                const RunIO& io = ios[g0 + (it[t] >> 16)];
+                if (ci < io.src_lim) {
+                    const uint4* q = reinterpret_cast<const uint4*>(io.src + (long long)ci * 8 * SB);
 #pragma unroll
                     for (int h = 0; h < SB / 2; ++h) raw[t][h] = q[h];
                 }
             }
         }
+    };
+    auto store_batch = [&](int k0) {
 #pragma unroll
         for (int t = 0; t < NI; ++t) {
             if (k0 + 32 * t < items) {
-                const RunIO& io = ios[g0 + gi[t]];
-                if (ci[t] < io.dst_lim) {
+                const int gi = it[t] >> 16, ci = it[t] & 0xffff;
+                const RunIO& io = ios[g0 + gi];
+                if (ci < io.dst_lim) {
                     const dit_dtype sdt = (dit_dtype)io.sdt, ddt = (dit_dtype)io.ddt;
                     uint4 o[DB / 2];
                     if (ROPE && io.rope_pos >= 0) {
-                        const int sl = slot[ROPE ? g0 + gi[t] : 0], c = ci[t] % dch;
-                        rope8<SB, DB>(raw[t], sdt, ddt, rope_sm[(2 * sl) * dch + c], rope_sm[(2 * sl + 1) * dch + c],
-                                      want_check && ddt != DIT_F32, o, overflow);
-                    } else
+                        const int sl = slot[ROPE ? g0 + gi : 0], cc = ci % dch;
+                        rope8<SB, DB>(raw[t], sdt, ddt, rope_sm[(2 * sl) * dch + cc],
+                                      rope_sm[(2 * sl + 1) * dch + cc], want_check && ddt != DIT_F32, o,
+                                      overflow);
+                    } else {
                         convert8<SB, DB>(raw[t], sdt, ddt, want_check && narrowing(sdt, ddt), o, overflow);
-                    uint4* q = reinterpret_cast<uint4*>(io.dst + (long long)ci[t] * 8 * DB);
+                    }
+                    uint4* q = reinterpret_cast<uint4*>(io.dst + (long long)ci * 8 * DB);
 #pragma unroll
                     for (int h = 0; h < DB / 2; ++h) q[h] = o[h];
                 }
             }
+        }
+    };
+    if constexpr (ROPE) {
+        // the first batch of data loads is issued before the barrier that
+        // publishes the table rows
+        int k0 = lane;
+        load_batch(k0);
+        cp_async_wait_all();
+        __syncthreads();
+        while (k0 < items) {
+            store_batch(k0);
+            k0 += 32 * NI;
+            if (k0 < items) load_batch(k0);
+        }
+    } else {
+        for (int k0 = lane; k0 < items; k0 += 32 * NI) {
+            load_batch(k0);
+            store_batch(k0);
         }
     }
     if (overflow) *A.range_flag = (int)DIT_ERR_RANGE;
@@ -517,6 +552,8 @@ template <int MODE, bool ROPE = false>
 dit_status launch_runs(const RunArgs& a, cudaStream_t st, const char* who) {
     if (a.nruns == 0) return DIT_OK;
     if (a.nruns >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 2^31 runs", who);
+    if ((long long)a.L.Hl * a.L.D / 8 >= (1LL << 16))
+        return fail(DIT_ERR_UNSUPPORTED, "%s: a head group holds 2^19 or more elements", who);
     const int sb = dtype_bytes(a.src_dt[0]);
     const int db = dtype_bytes(a.dst_dt[0]);
     for (int p = 1; p < 3; ++p) {
