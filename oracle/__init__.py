@@ -26,6 +26,9 @@ all floating-point arithmetic, with numpy as the only numerical library:
 * ``usp``         -- Ulysses inside, ring outside, composed end to end
                      (cache-dit "USP: Unified Sequence Parallelism").
 * ``numeric``     -- round-to-nearest-even conversions to bfloat16/float16.
+* ``fp8``         -- the e4m3 wire of Q, V and O with one scale per
+                     (token, head) (cache-dit "Context Parallelism", Async
+                     FP8 Ulysses Attention).
 * ``rope``        -- rotary embedding of the receive preparation and the
                      joint text+image sequence (edge-dit.cpp, receive
                      preparation and paired text/image streams).
@@ -34,4 +37,4 @@ Every function is pinned in ``tests/test_oracle_*.py`` to closed forms,
 invariants, library routines or brute force; none is "parity unpinned".
 """
 
-from . import attention, cfg, layout, numeric, rope, ulysses, usp  # noqa: F401
+from . import attention, cfg, fp8, layout, numeric, rope, ulysses, usp  # noqa: F401
