@@ -297,7 +297,8 @@ def run_ours(args):
     # end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args)
     extra = {} if args.no_extra else {**bandwidth_at_scale(dev, flush, peaks),
-                                      **receive_prep_at_scale(dev, flush)}
+                                      **receive_prep_at_scale(dev, flush),
+                                      **fp8_wire_at_scale(dev, flush)}
 
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
@@ -448,6 +449,59 @@ def receive_prep_at_scale(dev, flush):
             res[f"pack_joint_{tag}_GBs"] = round(pmoved / (ms * 1e-3) / 1e9, 1)
             del joint, txt, img, send
         del recv, heads
+        torch.cuda.empty_cache()
+    return res
+
+
+def fp8_wire_at_scale(dev, flush):
+    """The e4m3 wire of Q and V (cache-dit's Async FP8 Ulysses Attention) on
+    the FLUX-like (U=4) and Wan-like (U=8, R=4) shapes: the quantizing pack,
+    the exchange of the records and the decoding unpack, each launch timed
+    alone with L2 flushed before it (median of 10), and the whole seq->head
+    layout step (K on its own 16-bit exchange) against the all-16-bit one.
+    Bytes: real elements read and records written (D + 16 bytes per token
+    and head) and the reverse for the unpack."""
+    import torch
+    import sequence_attention_gb300 as sa
+    import synth
+    from sequence_attention_gb300.usp import UspPlan
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(13):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 3:
+                ts.append(s.elapsed_time(e))
+        return statistics.median(ts)
+
+    res = {}
+    for name, U in (("flux1024", 4), ("wan", 8)):
+        w = synth.WORKLOADS[name]
+        tag = "flux" if name == "flux1024" else name
+        q, k, v = (torch.randn((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev) for _ in range(3))
+        plan16 = UspPlan(w.B, w.S, w.H, w.D, U, w.R, device=str(dev))
+        plan8 = UspPlan(w.B, w.S, w.H, w.D, U, w.R, device=str(dev), fp8_qv=True)
+        L = plan8.L
+        rec = 2 * w.B * w.S * L.Hp * (w.D + 16)
+        real = 2 * w.B * w.S * w.H * w.D * 2
+        heads = 2 * w.B * w.S * L.Hp * w.D * 2
+        ms = timed(lambda: sa.dit_ulysses_pack(L, sa.DIT_SEQ_TO_HEAD, [q, v], plan8.send_qv))
+        res[f"pack_e4m3_{tag}_GBs"] = round((real + rec) / (ms * 1e-3) / 1e9, 1)
+        ms = timed(lambda: sa.dit_a2a_sim(L, sa.DIT_SEQ_TO_HEAD, 2, plan8.send_qv, plan8.recv_qv))
+        res[f"a2a_e4m3_{tag}_GBs"] = round(2 * rec / (ms * 1e-3) / 1e9, 1)
+        ms = timed(lambda: sa.dit_ulysses_unpack(L, sa.DIT_SEQ_TO_HEAD, plan8.recv_qv, [plan8.q_h, plan8.v_h]))
+        res[f"unpack_e4m3_{tag}_GBs"] = round((rec + heads) / (ms * 1e-3) / 1e9, 1)
+        res[f"layout_in_bf16_{tag}_ms"] = round(timed(lambda: plan16.layout_in(q, k, v)), 4)
+        res[f"layout_in_e4m3_qv_{tag}_ms"] = round(timed(lambda: plan8.layout_in(q, k, v)), 4)
+        res[f"wire_bytes_ratio_{tag}"] = round((rec + w.B * w.S * L.Hp * w.D * 2) /
+                                               (3 * w.B * w.S * L.Hp * w.D * 2), 4)
+        del q, k, v, plan16, plan8
         torch.cuda.empty_cache()
     return res
 

@@ -71,7 +71,11 @@ typedef enum {
     DIT_ERR_RANGE = 5          /* a value overflowed the target type */
 } dit_status;
 
-typedef enum { DIT_F32 = 0, DIT_BF16 = 1, DIT_F16 = 2 } dit_dtype;
+/* DIT_E4M3 is a wire type only (dit_ulysses_pack / dit_a2a_sim /
+ * dit_ulysses_unpack and their variants): one record per (token, head) of D
+ * e4m3 codes, the head's float32 scale and 12 zero bytes (D + 16 bytes);
+ * see dit_ulysses_pack. */
+typedef enum { DIT_F32 = 0, DIT_BF16 = 1, DIT_F16 = 2, DIT_E4M3 = 3 } dit_dtype;
 
 /* Direction of a Ulysses exchange (edge-dit.cpp "Parallel execution",
  * SPAllToAll4DLayout: kSeqToHead / kHeadToSeq). */

@@ -12,6 +12,9 @@ must be contiguous):
   K, V of the key/value blocks  [n_kv, B, S, H, D]
   partial outputs               [n_q, n_kv, B, S, H, D]
   partial log-sum-exp           [n_q, n_kv, B, H, S]   (float32)
+
+Wire buffers are flat tensors; a uint8 wire buffer carries the e4m3 record
+format (DIT_E4M3, Layout.wire_bytes_e4m3 bytes), any other dtype its own.
 """
 from __future__ import annotations
 
@@ -23,11 +26,11 @@ from typing import List, Optional, Sequence
 import torch
 
 from . import _lib
-from ._lib import (DIT_BF16, DIT_F16, DIT_F32, DIT_HEAD_TO_SEQ, DIT_SEQ_TO_HEAD, DitError,
+from ._lib import (DIT_BF16, DIT_E4M3, DIT_F16, DIT_F32, DIT_HEAD_TO_SEQ, DIT_SEQ_TO_HEAD, DitError,
                    DitLseView, DitSpLayout, DitView, check, lib)
 
 __all__ = [
-    "DitError", "Layout", "DIT_SEQ_TO_HEAD", "DIT_HEAD_TO_SEQ",
+    "DitError", "Layout", "DIT_SEQ_TO_HEAD", "DIT_HEAD_TO_SEQ", "DIT_E4M3",
     "dit_sp_layout_init", "dit_sp_a2a_counts", "dit_ulysses_pack", "dit_a2a_sim",
     "dit_ulysses_unpack", "dit_attn_partial", "dit_attn_merge_lse", "dit_attention",
     "dit_cfg_combine", "dit_device_status", "library_path", "dit_sp_signal", "dit_a2a_sim_checked",
@@ -36,7 +39,7 @@ __all__ = [
 
 lib()   # load now: fail at import time, not at first call
 
-_DT = {torch.float32: DIT_F32, torch.bfloat16: DIT_BF16, torch.float16: DIT_F16}
+_DT = {torch.float32: DIT_F32, torch.bfloat16: DIT_BF16, torch.float16: DIT_F16, torch.uint8: DIT_E4M3}
 
 
 def library_path() -> str:
@@ -86,6 +89,11 @@ class Layout:
     def wire_elems(self, nplanes: int) -> int:
         r = self.raw
         return nplanes * r.B * r.S * r.Hp * r.D
+
+    def wire_bytes_e4m3(self, nplanes: int) -> int:
+        """Bytes of an e4m3 wire: one (D + 16)-byte record per (token, head)."""
+        r = self.raw
+        return nplanes * r.B * r.S * r.Hp * (r.D + 16)
 
 
 def dit_sp_layout_init(B: int, S: int, H: int, D: int, U: int, R: int) -> Layout:

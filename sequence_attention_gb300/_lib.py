@@ -17,7 +17,7 @@ DIT_MAX_R = 8
 DIT_MAX_RANKS = 64
 
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT, DIT_ERR_RANGE = range(6)
-DIT_F32, DIT_BF16, DIT_F16 = range(3)
+DIT_F32, DIT_BF16, DIT_F16, DIT_E4M3 = range(4)
 DIT_SEQ_TO_HEAD, DIT_HEAD_TO_SEQ = range(2)
 
 #: every function include/ditsp.h declares

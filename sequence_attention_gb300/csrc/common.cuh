@@ -20,6 +20,8 @@ int* default_status_word();      // device address of the library status word
 int num_sms();                   // SM count of the current device (cached)
 
 inline bool dtype_ok(dit_dtype t) { return t == DIT_F32 || t == DIT_BF16 || t == DIT_F16; }
+// element types plus the record-encoded e4m3 type, valid only on the wire
+inline bool wire_ok(dit_dtype t) { return dtype_ok(t) || t == DIT_E4M3; }
 __host__ __device__ inline int dtype_bytes(dit_dtype t) { return t == DIT_F32 ? 4 : 2; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

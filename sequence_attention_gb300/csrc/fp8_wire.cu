@@ -1,0 +1,359 @@
+// FP8 (e4m3) wire of the Ulysses exchange (cache-dit "Context Parallelism",
+// Async FP8 Ulysses Attention: Q, V and the attention output O cross the
+// all-to-all in float8, K stays 16-bit for the softmax's sake).
+//
+// Each (token, head) travels as one record of D + 16 bytes: the D e4m3 codes
+// of x * (1/s), then s = amax/448 as a float32, then 12 zero bytes.  Every
+// step that decides a code is an IEEE float32 operation with round to
+// nearest even (amax, s = amax / 448, r = 1 / s, y = x * r, then the e4m3
+// conversion with saturation), so a CPU float32 evaluation gives the same
+// codes.  Decoding is code * s in float32, then one rounding to the
+// destination type (and, in the receive preparation, the RoPE rotation of the
+// float32 values before that rounding).
+//
+// Kernels walk the same runs (Hl heads of one (plane, batch, row)) in the
+// same destination orders as the 16-bit permutation kernels; a block decodes
+// 32 runs into shared memory, each warp then covers its runs' heads with
+// D/8 lanes per head (8 elements per lane), so the head's amax is a shuffle
+// reduction inside an aligned group of lanes.  The exchange between the
+// pack and the unpack is the 16-bit permutation kernel on records seen as
+// (D + 16) / 2 words.
+#include <cuda_fp8.h>
+#include <string.h>
+
+#include "sp_index.cuh"
+
+namespace ditsp {
+namespace {
+
+enum Fp8Mode { Q_PACK_S2H = 0, Q_PACK_H2S, DQ_UNPACK_S2H, DQ_UNPACK_H2S };
+
+constexpr int kThreads = 256;
+constexpr int kUnits = 8;          // head units in flight per lane
+
+struct Fp8Args {
+    dit_sp_layout L;
+    int np;
+    int lg;                        // log2(D / 8): lanes per head = 1 << lg
+    const void* src[3];            // pack: planes (S2H) or head layout (H2S); unpack: wire
+    const void* src2[3];           // paired streams (rows >= split), pack S2H only
+    void* dst[3];                  // pack: wire; unpack: planes / output
+    void* dst2[3];                 // paired streams, unpack H2S only
+    int split;
+    dit_dtype sdt;                 // 16/32-bit type of the pack's source
+    dit_dtype ddt[3];              // 16/32-bit types of the unpack's destinations
+    int* range_flag;
+    const float* rope_cos;
+    const float* rope_sin;
+    unsigned rope_planes;
+    long long nruns;
+};
+
+struct Fp8IO {
+    const char* src;
+    char* dst;
+    int nreal;        // real heads of the run's group; later heads are padding
+    int dt;           // the 16/32-bit side's dit_dtype
+    int rope_pos;     // joint position whose angles rotate the run, -1 none
+};
+
+template <int MODE>
+__device__ __forceinline__ Fp8IO fp8_io(const Fp8Args& A, int ri) {
+    const dit_sp_layout& L = A.L;
+    Run x;
+    if (MODE == Q_PACK_S2H) x = decode_A(L, A.np, ri);
+    else if (MODE == Q_PACK_H2S) x = decode_B(L, 1, ri);
+    else if (MODE == DQ_UNPACK_S2H) x = decode_H(L, A.np, ri);
+    else x = decode_S(L, ri);
+    const long long rec_run = (long long)L.Hl * (L.D + 16);
+    Fp8IO io;
+    io.nreal = min(max(L.H - x.v * L.Hl, 0), L.Hl);
+    io.rope_pos = -1;
+    bool second = false;
+    if (MODE == Q_PACK_S2H) {
+        io.dt = A.sdt;
+        const long long so = io.nreal > 0 ? seq_offset(L, x, A.split, second) : 0;
+        io.src = (const char*)(second ? A.src2[x.p] : A.src[x.p]) + so * dtype_bytes(A.sdt);
+        io.dst = (char*)A.dst[0] + ri * rec_run;
+    } else if (MODE == Q_PACK_H2S) {
+        io.dt = A.sdt;
+        io.src = (const char*)A.src[0] + head_offset(L, x) * dtype_bytes(A.sdt);
+        io.dst = (char*)A.dst[0] + ri * rec_run;
+    } else if (MODE == DQ_UNPACK_S2H) {
+        io.dt = A.ddt[x.p];
+        io.src = (const char*)A.src[0] + index_B(L, A.np, x) * rec_run;
+        io.dst = (char*)A.dst[x.p] + head_offset(L, x) * dtype_bytes(A.ddt[x.p]);
+        if ((A.rope_planes >> x.p) & 1u) io.rope_pos = L.rank_off[x.r * L.U + x.u] + x.i;
+    } else {
+        io.dt = A.ddt[0];
+        io.src = (const char*)A.src[0] + index_A(L, 1, x) * rec_run;
+        const long long doff = io.nreal > 0 ? seq_offset(L, x, A.split, second) : 0;
+        io.dst = (char*)(second ? A.dst2[0] : A.dst[0]) + doff * dtype_bytes(A.ddt[0]);
+    }
+    return io;
+}
+
+__device__ __forceinline__ uint16_t to_e4m3x2(float lo, float hi) {
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float2 from_e4m3x2(uint16_t v) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+    return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+// Quantize 8 values (one lane's share of a head) with the head's scale.
+__device__ __forceinline__ uint2 quant8(const float (&x)[8], float r) {
+    uint16_t c[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] = to_e4m3x2(__fmul_rn(x[2 * k], r), __fmul_rn(x[2 * k + 1], r));
+    return make_uint2((uint32_t)c[0] | ((uint32_t)c[1] << 16), (uint32_t)c[2] | ((uint32_t)c[3] << 16));
+}
+
+template <int EB>
+__device__ __forceinline__ void load_vals(const char* p, dit_dtype t, float (&x)[8]) {
+    Vec8 v;
+    load8(p, t, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = v.f[k];
+}
+
+// Quantizing pack: source heads (16/32-bit) -> records.
+template <int MODE, int EB>
+__global__ void __launch_bounds__(kThreads) fp8_pack_kernel(const __grid_constant__ Fp8Args A, int rpw) {
+    __shared__ Fp8IO ios[kThreads];
+    const int rpb = rpw * (kThreads / 32);
+    const long long r0 = (long long)blockIdx.x * rpb;
+    const int nrun = (int)min((long long)rpb, A.nruns - r0);
+    if ((int)threadIdx.x < nrun) ios[threadIdx.x] = fp8_io<MODE>(A, (int)(r0 + threadIdx.x));
+    __syncthreads();
+    pdl_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g0 = warp * rpw;
+    const int gn = min(rpw, nrun - g0);
+    if (gn <= 0) {
+        pdl_trigger();
+        return;
+    }
+    const int Hl = A.L.Hl, D = A.L.D, G = 1 << A.lg;
+    const int units = gn * Hl;
+    const int upw = 32 >> A.lg;                 // head units per warp per step
+    const int c = lane & (G - 1);               // this lane's 8-element chunk of a head
+    const int mine = lane >> A.lg;
+    for (int base = 0; base < units; base += upw * kUnits) {   // warp-uniform trip count
+        uint4 raw[kUnits][EB / 2];
+#pragma unroll
+        for (int b = 0; b < kUnits; ++b) {
+#pragma unroll
+            for (int h = 0; h < EB / 2; ++h) raw[b][h] = make_uint4(0, 0, 0, 0);
+            const int u = base + b * upw + mine;
+            if (u < units) {
+                const int g = u / Hl, hl = u - (u / Hl) * Hl;
+                const Fp8IO& io = ios[g0 + g];
+                if (hl < io.nreal) {
+                    const uint4* q = reinterpret_cast<const uint4*>(io.src + ((long long)hl * D + c * 8) * EB);
+#pragma unroll
+                    for (int h = 0; h < EB / 2; ++h) raw[b][h] = q[h];
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kUnits; ++b) {
+            const int u = base + b * upw + mine;
+            float x[8];
+            // a 16-bit type for 2-byte sources: raw[b] holds 16 bytes then
+            dit_dtype t = EB == 4 ? DIT_F32 : DIT_BF16;
+            if (EB == 2 && u < units) t = (dit_dtype)ios[g0 + u / Hl].dt;
+            load_vals<EB>(reinterpret_cast<const char*>(&raw[b][0]), t, x);
+            float amax = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
+            for (int o = G >> 1; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (u < units) {
+                const int g = u / Hl, hl = u - (u / Hl) * Hl;
+                const float s = __fdiv_rn(amax, 448.f);
+                const float r = s > 0.f ? __frcp_rn(s) : 0.f;
+                char* rec = ios[g0 + g].dst + (long long)hl * (D + 16);
+                *reinterpret_cast<uint2*>(rec + c * 8) = quant8(x, r);
+                if (c == 0) *reinterpret_cast<uint4*>(rec + D) = make_uint4(__float_as_uint(s), 0u, 0u, 0u);
+            }
+        }
+    }
+    pdl_trigger();
+}
+
+// Dequantizing unpack: records -> destination heads (16/32-bit), with the
+// optional RoPE rotation of the receive preparation.
+template <int MODE, int EB, bool ROPE>
+__global__ void __launch_bounds__(kThreads) fp8_unpack_kernel(const __grid_constant__ Fp8Args A, int rpw) {
+    __shared__ Fp8IO ios[kThreads];
+    const int rpb = rpw * (kThreads / 32);
+    const long long r0 = (long long)blockIdx.x * rpb;
+    const int nrun = (int)min((long long)rpb, A.nruns - r0);
+    if ((int)threadIdx.x < nrun) ios[threadIdx.x] = fp8_io<MODE>(A, (int)(r0 + threadIdx.x));
+    __syncthreads();
+    pdl_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g0 = warp * rpw;
+    const int gn = min(rpw, nrun - g0);
+    if (gn <= 0) {
+        pdl_trigger();
+        return;
+    }
+    const int Hl = A.L.Hl, D = A.L.D, G = 1 << A.lg;
+    const int units = gn * Hl;
+    const int upw = 32 >> A.lg;
+    const int c = lane & (G - 1);
+    const int mine = lane >> A.lg;
+    const bool check = A.range_flag != nullptr;
+    bool overflow = false;
+    for (int base = mine; base < units; base += upw * kUnits) {
+        uint2 code[kUnits];
+        float scale[kUnits];
+#pragma unroll
+        for (int b = 0; b < kUnits; ++b) {
+            code[b] = make_uint2(0, 0);
+            scale[b] = 0.f;
+            const int u = base + b * upw;
+            if (u < units) {
+                const int g = u / Hl, hl = u - (u / Hl) * Hl;
+                const char* rec = ios[g0 + g].src + (long long)hl * (D + 16);
+                code[b] = *reinterpret_cast<const uint2*>(rec + c * 8);
+                scale[b] = *reinterpret_cast<const float*>(rec + D);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kUnits; ++b) {
+            const int u = base + b * upw;
+            if (u >= units) continue;
+            const int g = u / Hl, hl = u - (u / Hl) * Hl;
+            const Fp8IO& io = ios[g0 + g];
+            if (MODE == DQ_UNPACK_H2S && hl >= io.nreal) continue;
+            const uint32_t w[2] = {code[b].x, code[b].y};
+            Vec8 v;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = from_e4m3x2((uint16_t)(w[k >> 1] >> (16 * (k & 1))));
+                v.f[2 * k] = __fmul_rn(f.x, scale[b]);
+                v.f[2 * k + 1] = __fmul_rn(f.y, scale[b]);
+            }
+            if (ROPE && io.rope_pos >= 0) {
+                const long long e = (long long)io.rope_pos * (D >> 1) + c * 4;
+                const float4 cs = *reinterpret_cast<const float4*>(A.rope_cos + e);
+                const float4 sn = *reinterpret_cast<const float4*>(A.rope_sin + e);
+                const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float x0 = v.f[2 * k], x1 = v.f[2 * k + 1];
+                    v.f[2 * k] = fmaf(x0, cc[k], -(x1 * ss[k]));
+                    v.f[2 * k + 1] = fmaf(x0, ss[k], x1 * cc[k]);
+                }
+            }
+            const dit_dtype t = (dit_dtype)io.dt;
+            char* dst = io.dst + ((long long)hl * D + c * 8) * dtype_bytes(t);
+            if (EB == 4) {
+                store8(dst, DIT_F32, v);
+            } else {
+                uint4 o = make_uint4(pack2(v.f[0], v.f[1], t), pack2(v.f[2], v.f[3], t), pack2(v.f[4], v.f[5], t),
+                                     pack2(v.f[6], v.f[7], t));
+                if (check) {
+                    Vec8 back;
+                    load8(&o, t, back);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) overflow |= isinf(back.f[e]) && !isinf(v.f[e]);
+                }
+                *reinterpret_cast<uint4*>(dst) = o;
+            }
+        }
+    }
+    if (overflow) *A.range_flag = (int)DIT_ERR_RANGE;
+    pdl_trigger();
+}
+
+template <typename K>
+dit_status launch_fp8(K kernel, const Fp8Args& a, cudaStream_t st, const char* who) {
+    if (a.nruns == 0) return DIT_OK;
+    if (a.nruns >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 2^31 runs", who);
+    const long long slots = (long long)num_sms() * 3;
+    int rpw = 4;
+    if ((a.nruns + 31) / 32 < 2 * slots) rpw = 2;
+    const long long blocks = (a.nruns + 8LL * rpw - 1) / (8LL * rpw);
+    cudaError_t e = launch_pdl(kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, a, rpw);
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
+    return check_launch(who);
+}
+
+dit_status check_fp8_shape(const dit_sp_layout* L, const char* who, int* lg) {
+    const int D = L->D;
+    if (D < 16 || D > 256 || (D & (D - 1)))
+        return fail(DIT_ERR_UNSUPPORTED, "%s: the e4m3 wire needs D in {16, 32, 64, 128, 256}", who);
+    int g = 0;
+    while ((8 << g) < D) ++g;
+    *lg = g;
+    return DIT_OK;
+}
+
+}  // namespace
+
+dit_status fp8_pack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, const void* const* src,
+                    const void* const* src2, int split, dit_dtype src_dt, void* send, cudaStream_t st,
+                    const char* who) {
+    Fp8Args a;
+    memset(&a, 0, sizeof(a));
+    dit_status s = check_fp8_shape(L, who, &a.lg);
+    if (s != DIT_OK) return s;
+    a.L = *L;
+    a.np = nplanes;
+    for (int p = 0; p < nplanes; ++p) {
+        a.src[p] = src ? src[p] : nullptr;
+        a.src2[p] = src2 ? src2[p] : nullptr;
+    }
+    a.split = split;
+    a.sdt = src_dt;
+    a.dst[0] = send;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    const bool wide = dtype_bytes(src_dt) == 4;
+    if (dir == DIT_SEQ_TO_HEAD)
+        return wide ? launch_fp8(fp8_pack_kernel<Q_PACK_S2H, 4>, a, st, who)
+                    : launch_fp8(fp8_pack_kernel<Q_PACK_S2H, 2>, a, st, who);
+    return wide ? launch_fp8(fp8_pack_kernel<Q_PACK_H2S, 4>, a, st, who)
+                : launch_fp8(fp8_pack_kernel<Q_PACK_H2S, 2>, a, st, who);
+}
+
+dit_status fp8_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, const void* recv, void* const* dst,
+                      void* const* dst2, int split, const dit_dtype* dst_dt, const float* cos_tab,
+                      const float* sin_tab, unsigned rope_planes, int* range_flag, cudaStream_t st,
+                      const char* who) {
+    Fp8Args a;
+    memset(&a, 0, sizeof(a));
+    dit_status s = check_fp8_shape(L, who, &a.lg);
+    if (s != DIT_OK) return s;
+    a.L = *L;
+    a.np = nplanes;
+    a.src[0] = recv;
+    const int db = dtype_bytes(dst_dt[0]);
+    for (int p = 0; p < nplanes; ++p) {
+        a.dst[p] = dst[p];
+        a.dst2[p] = dst2 ? dst2[p] : nullptr;
+        a.ddt[p] = dst_dt[p];
+        if (dtype_bytes(dst_dt[p]) != db)
+            return fail(DIT_ERR_UNSUPPORTED, "%s: planes of one call need destination types of one size", who);
+    }
+    a.split = split;
+    a.range_flag = range_flag;
+    a.rope_cos = cos_tab;
+    a.rope_sin = sin_tab;
+    a.rope_planes = rope_planes;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    const bool wide = db == 4;
+    if (dir == DIT_HEAD_TO_SEQ)
+        return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_H2S, 4, false>, a, st, who)
+                    : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_H2S, 2, false>, a, st, who);
+    if (rope_planes)
+        return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 4, true>, a, st, who)
+                    : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 2, true>, a, st, who);
+    return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 4, false>, a, st, who)
+                : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 2, false>, a, st, who);
+}
+
+}  // namespace ditsp

@@ -30,7 +30,7 @@
 //    cos[t][i], sin[t][i]:  (x0, x1) -> (x0 c - x1 s, x0 s + x1 c), in fp32.
 #include <string.h>
 
-#include "common.cuh"
+#include "sp_index.cuh"
 
 namespace ditsp {
 namespace {
@@ -62,136 +62,6 @@ struct RunArgs {
     const float* rope_sin;
     unsigned rope_planes;
 };
-
-struct Run {
-    int r, u, v, p, b, i;
-};
-
-__device__ __forceinline__ int rank_of_row(const dit_sp_layout& L, int t) {
-    int lo = 0, hi = L.U * L.R - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (L.rank_off[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
-
-__device__ __forceinline__ int ring_of_row(const dit_sp_layout& L, int t) {
-    int r = 0;
-    for (int k = 1; k < L.R; ++k)
-        if (L.ring_off[k] <= t && L.ring_len[k] > 0) r = k;
-    return r;
-}
-
-// Run index -> (r, u, v, p, b, i).  All run counts fit in 32 bits (checked
-// on the host), so the divisions here are 32-bit.
-__device__ __forceinline__ Run decode_A(const dit_sp_layout& L, int np, int a) {
-    const int per_row = np * L.B * L.U;
-    const int rid = rank_of_row(L, a / per_row);
-    Run x;
-    x.r = rid / L.U; x.u = rid - x.r * L.U;
-    const int Lu = L.rank_len[rid];
-    const int local = a - per_row * L.rank_off[rid];
-    const int blk = np * L.B * Lu;
-    x.v = local / blk;
-    const int rem = local - x.v * blk;
-    const int pb = rem / Lu;
-    x.i = rem - pb * Lu;
-    x.p = pb / L.B; x.b = pb - x.p * L.B;
-    return x;
-}
-
-__device__ __forceinline__ Run decode_B(const dit_sp_layout& L, int np, int bi) {
-    const int per_row = np * L.B * L.U;
-    Run x;
-    x.r = ring_of_row(L, bi / per_row);
-    const int offr = L.ring_off[x.r];
-    const int grp = np * L.B * L.ring_len[x.r];
-    const int local = bi - per_row * offr;
-    x.v = local / grp;
-    int rem = local - x.v * grp;
-    const int rid = rank_of_row(L, offr + rem / (np * L.B));
-    x.u = rid - x.r * L.U;
-    const int Lu = L.rank_len[rid];
-    rem -= np * L.B * (L.rank_off[rid] - offr);
-    const int pb = rem / Lu;
-    x.i = rem - pb * Lu;
-    x.p = pb / L.B; x.b = pb - x.p * L.B;
-    return x;
-}
-
-// Head-layout order (destination order of the seq->head unpack): runs of
-// plane p enumerated as (r, b, row of ring block r, v), so consecutive runs
-// fill one head-layout row.
-__device__ __forceinline__ Run decode_H(const dit_sp_layout& L, int np, int h) {
-    const int per_plane = L.B * L.S * L.U;
-    Run x;
-    x.p = h / per_plane;
-    const int rem = h - x.p * per_plane;
-    x.r = ring_of_row(L, rem / (L.B * L.U));
-    const int offr = L.ring_off[x.r], Sr = L.ring_len[x.r];
-    const int local = rem - L.B * L.U * offr;
-    x.b = local / (Sr * L.U);
-    const int rem2 = local - x.b * Sr * L.U;
-    const int row = rem2 / L.U;
-    x.v = rem2 - row * L.U;
-    const int rid = rank_of_row(L, offr + row);
-    x.u = rid - x.r * L.U;
-    x.i = offr + row - L.rank_off[rid];
-    return x;
-}
-
-// Sequence order (destination order of the head->seq unpack, one plane):
-// runs enumerated as (b, token, v), so consecutive runs fill one token row.
-__device__ __forceinline__ Run decode_S(const dit_sp_layout& L, int s) {
-    Run x;
-    x.p = 0;
-    const int bt = s / L.U;
-    x.v = s - bt * L.U;
-    x.b = bt / L.S;
-    const int t = bt - x.b * L.S;
-    const int rid = rank_of_row(L, t);
-    x.r = rid / L.U;
-    x.u = rid - x.r * L.U;
-    x.i = t - L.rank_off[rid];
-    return x;
-}
-
-__device__ __forceinline__ long long index_A(const dit_sp_layout& L, int np, const Run& x) {
-    const int rid = x.r * L.U + x.u;
-    const int Lu = L.rank_len[rid];
-    return (long long)np * L.B * L.U * L.rank_off[rid] + (long long)x.v * np * L.B * Lu +
-           ((long long)x.p * L.B + x.b) * Lu + x.i;
-}
-
-__device__ __forceinline__ long long index_B(const dit_sp_layout& L, int np, const Run& x) {
-    const int rid = x.r * L.U + x.u;
-    const int offr = L.ring_off[x.r];
-    return (long long)np * L.B * L.U * offr + (long long)x.v * np * L.B * L.ring_len[x.r] +
-           (long long)np * L.B * (L.rank_off[rid] - offr) +
-           ((long long)x.p * L.B + x.b) * L.rank_len[rid] + x.i;
-}
-
-// element offset of the run's first head in a seq-layout plane [B][S][H][D]
-// (only meaningful when the group has a real head).  With paired streams,
-// rows at or past `split` are in the second tensor, [B][S - split][H][D];
-// `second` says which.
-__device__ __forceinline__ long long seq_offset(const dit_sp_layout& L, const Run& x, int split, bool& second) {
-    int row = L.rank_off[x.r * L.U + x.u] + x.i;
-    int rows = L.S;
-    second = split > 0 && row >= split;
-    if (split > 0) {
-        rows = second ? L.S - split : split;
-        if (second) row -= split;
-    }
-    return (((long long)x.b * rows + row) * L.H + (long long)x.v * L.Hl) * L.D;
-}
-
-// element offset in a head-layout plane [R][B][S_cap][Hp][D]
-__device__ __forceinline__ long long head_offset(const dit_sp_layout& L, const Run& x) {
-    const int row = L.rank_off[x.r * L.U + x.u] - L.ring_off[x.r] + x.i;
-    return ((((long long)x.r * L.B + x.b) * L.S_cap + row) * L.Hp + (long long)x.v * L.Hl) * L.D;
-}
 
 __device__ __forceinline__ unsigned long long gtimer_ns() {
     unsigned long long t;
@@ -511,24 +381,6 @@ __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __gri
     pdl_trigger();
 }
 
-// Host-side check of a caller-supplied layout: every field must be what
-// dit_sp_layout_init would have produced for its (B, S, H, D, U, R).
-dit_status check_layout(const dit_sp_layout* L, const char* who) {
-    if (!L) return fail(DIT_ERR_INVALID_ARG, "%s: layout is NULL", who);
-    dit_sp_layout ref;
-    if (dit_sp_layout_init(L->B, L->S, L->H, L->D, L->U, L->R, &ref) != DIT_OK)
-        return fail(DIT_ERR_INVALID_ARG, "%s: layout sizes invalid", who);
-    bool ok = ref.Hp == L->Hp && ref.Hl == L->Hl && ref.S_cap == L->S_cap;
-    for (int r = 0; ok && r < L->R; ++r)
-        ok = ref.ring_len[r] == L->ring_len[r] && ref.ring_off[r] == L->ring_off[r];
-    for (int i = 0; ok && i < L->R * L->U; ++i)
-        ok = ref.rank_len[i] == L->rank_len[i] && ref.rank_off[i] == L->rank_off[i];
-    if (!ok) return fail(DIT_ERR_INVALID_ARG, "%s: layout tables are inconsistent", who);
-    if (L->D % 8 != 0)
-        return fail(DIT_ERR_UNSUPPORTED, "%s: head dim %d is not a multiple of 8", who, L->D);
-    return DIT_OK;
-}
-
 template <int MODE, int SB, int DB, bool ROPE>
 dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
     // 4 runs per warp keep each block's fixed decode latency small against
@@ -569,6 +421,36 @@ dit_status launch_runs(const RunArgs& a, cudaStream_t st, const char* who) {
 }
 
 }  // namespace
+
+// The e4m3 wire's exchange: a record of D + 16 bytes is (D + 16) / 2 16-bit
+// words, so the exchange is the 16-bit permutation of runs of that width.
+dit_status record_words(RunArgs* a, const char* who) {
+    const int D = a->L.D;
+    if (D < 16 || D > 256 || (D & (D - 1)))
+        return fail(DIT_ERR_UNSUPPORTED, "%s: the e4m3 wire needs D in {16, 32, 64, 128, 256}", who);
+    a->L.D = (D + 16) / 2;
+    a->src_dt[0] = a->dst_dt[0] = DIT_BF16;
+    return DIT_OK;
+}
+
+// Host-side check of a caller-supplied layout: every field must be what
+// dit_sp_layout_init would have produced for its (B, S, H, D, U, R).
+dit_status check_layout(const dit_sp_layout* L, const char* who) {
+    if (!L) return fail(DIT_ERR_INVALID_ARG, "%s: layout is NULL", who);
+    dit_sp_layout ref;
+    if (dit_sp_layout_init(L->B, L->S, L->H, L->D, L->U, L->R, &ref) != DIT_OK)
+        return fail(DIT_ERR_INVALID_ARG, "%s: layout sizes invalid", who);
+    bool ok = ref.Hp == L->Hp && ref.Hl == L->Hl && ref.S_cap == L->S_cap;
+    for (int r = 0; ok && r < L->R; ++r)
+        ok = ref.ring_len[r] == L->ring_len[r] && ref.ring_off[r] == L->ring_off[r];
+    for (int i = 0; ok && i < L->R * L->U; ++i)
+        ok = ref.rank_len[i] == L->rank_len[i] && ref.rank_off[i] == L->rank_off[i];
+    if (!ok) return fail(DIT_ERR_INVALID_ARG, "%s: layout tables are inconsistent", who);
+    if (L->D % 8 != 0)
+        return fail(DIT_ERR_UNSUPPORTED, "%s: head dim %d is not a multiple of 8", who, L->D);
+    return DIT_OK;
+}
+
 }  // namespace ditsp
 
 using namespace ditsp;
@@ -579,7 +461,7 @@ extern "C" dit_status dit_ulysses_pack(const dit_sp_layout* L, dit_a2a_dir dir, 
     const char* who = "dit_ulysses_pack";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
-    if (!dtype_ok(src_dt) || !dtype_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (!dtype_ok(src_dt) || !wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
     if (dir != DIT_SEQ_TO_HEAD && dir != DIT_HEAD_TO_SEQ) return fail(DIT_ERR_INVALID_ARG, "%s: bad direction", who);
     if (nplanes < 1 || nplanes > 3 || (dir == DIT_HEAD_TO_SEQ && nplanes != 1))
         return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3 (1 for head-to-seq)", who);
@@ -597,6 +479,7 @@ extern "C" dit_status dit_ulysses_pack(const dit_sp_layout* L, dit_a2a_dir dir, 
     a.dst_dt[0] = wire_dt;
     a.nruns = (long long)nplanes * L->B * L->U * L->S;
     cudaStream_t st = (cudaStream_t)stream;
+    if (wire_dt == DIT_E4M3) return fp8_pack(L, dir, nplanes, src, nullptr, 0, src_dt, send, st, who);
     return dir == DIT_SEQ_TO_HEAD ? launch_runs<PACK_S2H>(a, st, who) : launch_runs<PACK_H2S>(a, st, who);
 }
 
@@ -605,7 +488,7 @@ extern "C" dit_status dit_a2a_sim(const dit_sp_layout* L, dit_a2a_dir dir, int n
     const char* who = "dit_a2a_sim";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
-    if (!dtype_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (!wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
     if (dir != DIT_SEQ_TO_HEAD && dir != DIT_HEAD_TO_SEQ) return fail(DIT_ERR_INVALID_ARG, "%s: bad direction", who);
     if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
     if (!send || !recv || !aligned16(send) || !aligned16(recv) || send == recv)
@@ -617,6 +500,7 @@ extern "C" dit_status dit_a2a_sim(const dit_sp_layout* L, dit_a2a_dir dir, int n
     a.src[0] = send; a.src_dt[0] = wire_dt;
     a.dst[0] = recv; a.dst_dt[0] = wire_dt;
     a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    if (wire_dt == DIT_E4M3 && (s = record_words(&a, who)) != DIT_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
     return dir == DIT_SEQ_TO_HEAD ? launch_runs<A2A_S2H>(a, st, who) : launch_runs<A2A_H2S>(a, st, who);
 }
@@ -627,7 +511,7 @@ extern "C" dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir
     const char* who = "dit_ulysses_unpack";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
-    if (!dtype_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad wire dtype", who);
+    if (!wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad wire dtype", who);
     if (dir != DIT_SEQ_TO_HEAD && dir != DIT_HEAD_TO_SEQ) return fail(DIT_ERR_INVALID_ARG, "%s: bad direction", who);
     if (nplanes < 1 || nplanes > 3 || (dir == DIT_HEAD_TO_SEQ && nplanes != 1))
         return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3 (1 for head-to-seq)", who);
@@ -647,6 +531,8 @@ extern "C" dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir
     a.range_flag = d_range_flag;
     a.nruns = (long long)nplanes * L->B * L->U * L->S;
     cudaStream_t st = (cudaStream_t)stream;
+    if (wire_dt == DIT_E4M3)
+        return fp8_unpack(L, dir, nplanes, recv, dst, nullptr, 0, dst_dt, nullptr, nullptr, 0, d_range_flag, st, who);
     return dir == DIT_SEQ_TO_HEAD ? launch_runs<UNPACK_S2H>(a, st, who) : launch_runs<UNPACK_H2S>(a, st, who);
 }
 
@@ -672,7 +558,7 @@ extern "C" dit_status dit_a2a_sim_checked(const dit_sp_layout* L, dit_a2a_dir di
     const char* who = "dit_a2a_sim_checked";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
-    if (!dtype_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (!wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
     if (dir != DIT_SEQ_TO_HEAD && dir != DIT_HEAD_TO_SEQ) return fail(DIT_ERR_INVALID_ARG, "%s: bad direction", who);
     if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
     if (!send || !recv || !aligned16(send) || !aligned16(recv) || send == recv)
@@ -693,6 +579,7 @@ extern "C" dit_status dit_a2a_sim_checked(const dit_sp_layout* L, dit_a2a_dir di
     a.timeout_ns = timeout_ns;
     a.status = d_status ? d_status : default_status_word();
     if (!a.status) return fail(DIT_ERR_CUDA, "%s: no device status word", who);
+    if (wire_dt == DIT_E4M3 && (s = record_words(&a, who)) != DIT_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
     return dir == DIT_SEQ_TO_HEAD ? launch_runs<A2A_S2H>(a, st, who) : launch_runs<A2A_H2S>(a, st, who);
 }
@@ -703,7 +590,7 @@ extern "C" dit_status dit_ulysses_pack_joint(const dit_sp_layout* L, int nplanes
     const char* who = "dit_ulysses_pack_joint";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
-    if (!dtype_ok(src_dt) || !dtype_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (!dtype_ok(src_dt) || !wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
     if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
     if (S_txt < 0 || S_txt > L->S) return fail(DIT_ERR_INVALID_ARG, "%s: S_txt out of [0, S]", who);
     if (!send || !aligned16(send)) return fail(DIT_ERR_INVALID_ARG, "%s: send NULL or misaligned", who);
@@ -727,6 +614,8 @@ extern "C" dit_status dit_ulysses_pack_joint(const dit_sp_layout* L, int nplanes
     a.dst[0] = send;
     a.dst_dt[0] = wire_dt;
     a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    if (wire_dt == DIT_E4M3)
+        return fp8_pack(L, DIT_SEQ_TO_HEAD, nplanes, a.src, a.src2, a.split, src_dt, send, (cudaStream_t)stream, who);
     return launch_runs<PACK_S2H>(a, (cudaStream_t)stream, who);
 }
 
@@ -736,7 +625,7 @@ extern "C" dit_status dit_ulysses_unpack_joint(const dit_sp_layout* L, const voi
     const char* who = "dit_ulysses_unpack_joint";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
-    if (!dtype_ok(wire_dt) || !dtype_ok(out_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
+    if (!wire_ok(wire_dt) || !dtype_ok(out_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
     if (S_txt < 0 || S_txt > L->S) return fail(DIT_ERR_INVALID_ARG, "%s: S_txt out of [0, S]", who);
     if (!recv || !aligned16(recv)) return fail(DIT_ERR_INVALID_ARG, "%s: recv NULL or misaligned", who);
     const bool has_txt = S_txt > 0, has_img = S_txt < L->S;
@@ -752,6 +641,9 @@ extern "C" dit_status dit_ulysses_unpack_joint(const dit_sp_layout* L, const voi
     a.dst_dt[0] = out_dt;
     a.split = has_txt && has_img ? S_txt : 0;
     a.nruns = (long long)L->B * L->U * L->S;
+    if (wire_dt == DIT_E4M3)
+        return fp8_unpack(L, DIT_HEAD_TO_SEQ, 1, recv, a.dst, a.dst2, a.split, a.dst_dt, nullptr, nullptr, 0, nullptr,
+                          (cudaStream_t)stream, who);
     return launch_runs<UNPACK_H2S>(a, (cudaStream_t)stream, who);
 }
 
@@ -762,12 +654,12 @@ extern "C" dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplane
     const char* who = "dit_ulysses_unpack_rope";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
-    if (!dtype_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad wire dtype", who);
+    if (!wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad wire dtype", who);
     if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
     if (rope_planes >> nplanes) return fail(DIT_ERR_INVALID_ARG, "%s: rope_planes names a missing plane", who);
     if (rope_planes && (!cos_tab || !sin_tab || !aligned16(cos_tab) || !aligned16(sin_tab)))
         return fail(DIT_ERR_INVALID_ARG, "%s: rotary tables NULL or misaligned", who);
-    if (rope_planes && L->D > kRopeMaxD)
+    if (rope_planes && L->D > kRopeMaxD && wire_dt != DIT_E4M3)
         return fail(DIT_ERR_UNSUPPORTED, "%s: rotary path supports D <= %d", who, kRopeMaxD);
     if (!recv || !aligned16(recv) || !dst || !dst_dt)
         return fail(DIT_ERR_INVALID_ARG, "%s: recv/dst NULL or misaligned", who);
@@ -788,5 +680,8 @@ extern "C" dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplane
     a.rope_planes = rope_planes;
     a.nruns = (long long)nplanes * L->B * L->U * L->S;
     cudaStream_t st = (cudaStream_t)stream;
+    if (wire_dt == DIT_E4M3)
+        return fp8_unpack(L, DIT_SEQ_TO_HEAD, nplanes, recv, dst, nullptr, 0, dst_dt, cos_tab, sin_tab, rope_planes,
+                          d_range_flag, st, who);
     return rope_planes ? launch_runs<UNPACK_S2H, true>(a, st, who) : launch_runs<UNPACK_S2H>(a, st, who);
 }

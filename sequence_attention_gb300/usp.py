@@ -41,9 +41,12 @@ class UspPlan:
                  out_dtype: Optional[torch.dtype] = None,
                  v_dtype: Optional[torch.dtype] = None,
                  device: str = "cuda", scale: Optional[float] = None,
-                 rope: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+                 rope: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
+                 fp8_qv: bool = False, fp8_o: bool = False):
         """rope: optional (cos, sin) float32 [S, D/2] device tables of the
-        joint sequence; Q and K are then rotated by the receive preparation."""
+        joint sequence; Q and K are then rotated by the receive preparation.
+        fp8_qv / fp8_o: Q and V (one exchange) / the output cross the
+        all-to-all as e4m3 records; K keeps its own 16-bit exchange."""
         self.L = dit_sp_layout_init(B, S, H, D, U, R)
         self.B, self.S, self.H, self.D, self.U, self.R = B, S, H, D, U, R
         self.in_dtype = in_dtype
@@ -58,8 +61,14 @@ class UspPlan:
         L = self.L
         hs = L.head_shape()
         dev = torch.device(device)
-        self.send = torch.empty(L.wire_elems(3), dtype=in_dtype, device=dev)
-        self.recv = torch.empty(L.wire_elems(3), dtype=in_dtype, device=dev)
+        self.fp8_qv, self.fp8_o = fp8_qv, fp8_o
+        if fp8_qv:
+            self.send_qv = torch.empty(L.wire_bytes_e4m3(2), dtype=torch.uint8, device=dev)
+            self.recv_qv = torch.empty_like(self.send_qv)
+            self.send = torch.empty(L.wire_elems(1), dtype=in_dtype, device=dev)     # K
+        else:
+            self.send = torch.empty(L.wire_elems(3), dtype=in_dtype, device=dev)
+        self.recv = torch.empty_like(self.send)
         self.q_h = torch.empty(hs, dtype=in_dtype, device=dev)
         self.k_h = torch.empty(hs, dtype=in_dtype, device=dev)
         self.v_h = torch.empty(hs, dtype=v_dtype, device=dev)
@@ -69,8 +78,11 @@ class UspPlan:
             self.lse_parts = torch.empty((R, R, B, L.Hp, L.S_cap), dtype=torch.float32, device=dev)
         else:
             self.parts = self.lse_parts = None
-        self.send_o = torch.empty(L.wire_elems(1), dtype=self.out_dtype, device=dev)
-        self.recv_o = torch.empty(L.wire_elems(1), dtype=self.out_dtype, device=dev)
+        if fp8_o:
+            self.send_o = torch.empty(L.wire_bytes_e4m3(1), dtype=torch.uint8, device=dev)
+        else:
+            self.send_o = torch.empty(L.wire_elems(1), dtype=self.out_dtype, device=dev)
+        self.recv_o = torch.empty_like(self.send_o)
         self.rope = rope
         self.range_flag = torch.zeros(1, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -85,30 +97,50 @@ class UspPlan:
 
     def steps(self):
         """Names of the kernels one run() launches, in order."""
-        s = ["pack_s2h", "a2a_s2h", "unpack_s2h", "attn_partial"]
+        s = ["pack_s2h", "a2a_s2h", "unpack_s2h"]
+        if self.fp8_qv:
+            s = ["pack_s2h_k", "pack_s2h_qv", "a2a_s2h_k", "a2a_s2h_qv", "unpack_s2h_k", "unpack_s2h_qv"]
+        s = s + ["attn_partial"]
         if self.R > 1:
             s.append("merge")
         return s + ["pack_h2s", "a2a_h2s", "unpack_h2s"]
 
-    def _receive(self, stream):
-        L = self.L
-        dit_a2a_sim(L, DIT_SEQ_TO_HEAD, 3, self.send, self.recv, stream)
-        heads = [self.q_h, self.k_h, self.v_h]
+    def _unpack(self, recv, heads, rope_mask, stream):
         if self.rope is not None:
-            dit_ulysses_unpack_rope(L, self.recv, heads, self.rope[0], self.rope[1], 0b011,
+            dit_ulysses_unpack_rope(self.L, recv, heads, self.rope[0], self.rope[1], rope_mask,
                                     self.range_flag, stream)
         else:
-            dit_ulysses_unpack(L, DIT_SEQ_TO_HEAD, self.recv, heads, self.range_flag, stream)
+            dit_ulysses_unpack(self.L, DIT_SEQ_TO_HEAD, recv, heads, self.range_flag, stream)
+
+    def _receive(self, stream):
+        L = self.L
+        if self.fp8_qv:
+            dit_a2a_sim(L, DIT_SEQ_TO_HEAD, 1, self.send, self.recv, stream)
+            dit_a2a_sim(L, DIT_SEQ_TO_HEAD, 2, self.send_qv, self.recv_qv, stream)
+            self._unpack(self.recv, [self.k_h], 0b1, stream)
+            self._unpack(self.recv_qv, [self.q_h, self.v_h], 0b01, stream)
+        else:
+            dit_a2a_sim(L, DIT_SEQ_TO_HEAD, 3, self.send, self.recv, stream)
+            self._unpack(self.recv, [self.q_h, self.k_h, self.v_h], 0b011, stream)
 
     def layout_in(self, q, k, v, stream=None):
-        dit_ulysses_pack(self.L, DIT_SEQ_TO_HEAD, [q, k, v], self.send, stream)
+        if self.fp8_qv:
+            dit_ulysses_pack(self.L, DIT_SEQ_TO_HEAD, [k], self.send, stream)
+            dit_ulysses_pack(self.L, DIT_SEQ_TO_HEAD, [q, v], self.send_qv, stream)
+        else:
+            dit_ulysses_pack(self.L, DIT_SEQ_TO_HEAD, [q, k, v], self.send, stream)
         self._receive(stream)
 
     def layout_in_joint(self, txt: Optional[Sequence[torch.Tensor]], img: Optional[Sequence[torch.Tensor]],
                         stream=None):
         """txt / img: (q, k, v) of the text [B,S_txt,H,D] and image
         [B,S-S_txt,H,D] streams (None for a stream without rows)."""
-        dit_ulysses_pack_joint(self.L, txt, img, self.send, stream)
+        if self.fp8_qv:
+            sel = lambda t, idx: None if t is None else [t[i] for i in idx]   # noqa: E731
+            dit_ulysses_pack_joint(self.L, sel(txt, [1]), sel(img, [1]), self.send, stream)
+            dit_ulysses_pack_joint(self.L, sel(txt, [0, 2]), sel(img, [0, 2]), self.send_qv, stream)
+        else:
+            dit_ulysses_pack_joint(self.L, txt, img, self.send, stream)
         self._receive(stream)
 
     def attend(self, stream=None):
