@@ -14,8 +14,9 @@
 // Kernels walk the same runs (Hl heads of one (plane, batch, row)) in the
 // same destination orders as the 16-bit permutation kernels; a block decodes
 // 32 runs into shared memory, each warp then covers its runs' heads with
-// D/8 lanes per head (8 elements per lane), so the head's amax is a shuffle
-// reduction inside an aligned group of lanes.  The exchange between the
+// D/32 lanes per head, so the head's amax is a shuffle
+// reduction inside an aligned group of lanes (32 values per lane; 16 when
+// D = 16).  The exchange between the
 // pack and the unpack is the 16-bit permutation kernel on records seen as
 // (D + 16) / 2 words.
 #include <cuda_fp8.h>
@@ -29,12 +30,11 @@ namespace {
 enum Fp8Mode { Q_PACK_S2H = 0, Q_PACK_H2S, DQ_UNPACK_S2H, DQ_UNPACK_H2S };
 
 constexpr int kThreads = 256;
-constexpr int kUnits = 8;          // head units in flight per lane
 
 struct Fp8Args {
     dit_sp_layout L;
     int np;
-    int lg;                        // log2(D / 8): lanes per head = 1 << lg
+    int lg;                        // log2 of the lanes that share one head
     const void* src[3];            // pack: planes (S2H) or head layout (H2S); unpack: wire
     const void* src2[3];           // paired streams (rows >= split), pack S2H only
     void* dst[3];                  // pack: wire; unpack: planes / output
@@ -102,25 +102,41 @@ __device__ __forceinline__ float2 from_e4m3x2(uint16_t v) {
     return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
-// Quantize 8 values (one lane's share of a head) with the head's scale.
-__device__ __forceinline__ uint2 quant8(const float (&x)[8], float r) {
-    uint16_t c[4];
+// Quantize one lane's EPL values of a head with the head's reciprocal scale.
+template <int EPL>
+__device__ __forceinline__ void quant(const float (&x)[EPL], float r, uint4 (&out)[EPL / 16]) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) c[k] = to_e4m3x2(__fmul_rn(x[2 * k], r), __fmul_rn(x[2 * k + 1], r));
-    return make_uint2((uint32_t)c[0] | ((uint32_t)c[1] << 16), (uint32_t)c[2] | ((uint32_t)c[3] << 16));
+    for (int q = 0; q < EPL / 16; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int e = 16 * q + 4 * k;
+            const uint32_t lo = to_e4m3x2(__fmul_rn(x[e], r), __fmul_rn(x[e + 1], r));
+            const uint32_t hi = to_e4m3x2(__fmul_rn(x[e + 2], r), __fmul_rn(x[e + 3], r));
+            w[k] = lo | (hi << 16);
+        }
+        out[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
 }
 
-template <int EB>
-__device__ __forceinline__ void load_vals(const char* p, dit_dtype t, float (&x)[8]) {
-    Vec8 v;
-    load8(p, t, v);
+// EPL values held as raw 16-byte vectors of element size EB -> float32.
+template <int EB, int EPL>
+__device__ __forceinline__ void widen(const uint4 (&raw)[EPL * EB / 16], dit_dtype t, float (&x)[EPL]) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) x[k] = v.f[k];
+    for (int v = 0; v < EPL / 8; ++v) {
+        Vec8 f;
+        load8(&raw[v * EB / 2], EB == 4 ? DIT_F32 : t, f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[8 * v + k] = f.f[k];
+    }
 }
 
-// Quantizing pack: source heads (16/32-bit) -> records.
-template <int MODE, int EB>
-__global__ void __launch_bounds__(kThreads) fp8_pack_kernel(const __grid_constant__ Fp8Args A, int rpw) {
+// Quantizing pack: source heads (16/32-bit) -> records.  A lane holds EPL
+// consecutive values of a head, so D / EPL lanes share one head.
+template <int MODE, int EB, int EPL>
+__global__ void __launch_bounds__(kThreads, 3) fp8_pack_kernel(const __grid_constant__ Fp8Args A, int rpw) {
+    constexpr int NV = EPL * EB / 16;        // 16-byte source vectors per lane and head
+    constexpr int NU = EB == 4 ? 1 : 2;      // heads in flight per lane
     __shared__ Fp8IO ios[kThreads];
     const int rpb = rpw * (kThreads / 32);
     const long long r0 = (long long)blockIdx.x * rpb;
@@ -137,44 +153,53 @@ __global__ void __launch_bounds__(kThreads) fp8_pack_kernel(const __grid_constan
     }
     const int Hl = A.L.Hl, D = A.L.D, G = 1 << A.lg;
     const int units = gn * Hl;
-    const int upw = 32 >> A.lg;                 // head units per warp per step
-    const int c = lane & (G - 1);               // this lane's 8-element chunk of a head
+    const int upw = 32 >> A.lg;                 // heads per warp per step
+    const int c = lane & (G - 1);               // this lane's EPL-element slice of a head
     const int mine = lane >> A.lg;
-    for (int base = 0; base < units; base += upw * kUnits) {   // warp-uniform trip count
-        uint4 raw[kUnits][EB / 2];
+    const dit_dtype sdt = A.sdt;
+    // (run, head) of this lane's next unit, advanced by upw per unit
+    int g = mine / Hl, hl = mine - (mine / Hl) * Hl;
+    for (int base = 0; base < units; base += upw * NU) {   // warp-uniform trip count
+        uint4 raw[NU][NV];
+        int gh[NU];
 #pragma unroll
-        for (int b = 0; b < kUnits; ++b) {
+        for (int b = 0; b < NU; ++b) {
+            gh[b] = (g << 16) | hl;
+            hl += upw;
+            while (hl >= Hl) { hl -= Hl; ++g; }
+        }
 #pragma unroll
-            for (int h = 0; h < EB / 2; ++h) raw[b][h] = make_uint4(0, 0, 0, 0);
+        for (int b = 0; b < NU; ++b) {
+#pragma unroll
+            for (int v = 0; v < NV; ++v) raw[b][v] = make_uint4(0, 0, 0, 0);
             const int u = base + b * upw + mine;
             if (u < units) {
-                const int g = u / Hl, hl = u - (u / Hl) * Hl;
-                const Fp8IO& io = ios[g0 + g];
-                if (hl < io.nreal) {
-                    const uint4* q = reinterpret_cast<const uint4*>(io.src + ((long long)hl * D + c * 8) * EB);
+                const int h = gh[b] & 0xffff;
+                const Fp8IO& io = ios[g0 + (gh[b] >> 16)];
+                if (h < io.nreal) {
+                    const uint4* q = reinterpret_cast<const uint4*>(io.src + ((long long)h * D + c * EPL) * EB);
 #pragma unroll
-                    for (int h = 0; h < EB / 2; ++h) raw[b][h] = q[h];
+                    for (int v = 0; v < NV; ++v) raw[b][v] = q[v];
                 }
             }
         }
 #pragma unroll
-        for (int b = 0; b < kUnits; ++b) {
+        for (int b = 0; b < NU; ++b) {
             const int u = base + b * upw + mine;
-            float x[8];
-            // a 16-bit type for 2-byte sources: raw[b] holds 16 bytes then
-            dit_dtype t = EB == 4 ? DIT_F32 : DIT_BF16;
-            if (EB == 2 && u < units) t = (dit_dtype)ios[g0 + u / Hl].dt;
-            load_vals<EB>(reinterpret_cast<const char*>(&raw[b][0]), t, x);
+            float x[EPL];
+            widen<EB, EPL>(raw[b], sdt, x);
             float amax = 0.f;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
+            for (int k = 0; k < EPL; ++k) amax = fmaxf(amax, fabsf(x[k]));
             for (int o = G >> 1; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             if (u < units) {
-                const int g = u / Hl, hl = u - (u / Hl) * Hl;
                 const float s = __fdiv_rn(amax, 448.f);
                 const float r = s > 0.f ? __frcp_rn(s) : 0.f;
-                char* rec = ios[g0 + g].dst + (long long)hl * (D + 16);
-                *reinterpret_cast<uint2*>(rec + c * 8) = quant8(x, r);
+                char* rec = ios[g0 + (gh[b] >> 16)].dst + (long long)(gh[b] & 0xffff) * (D + 16);
+                uint4 o[EPL / 16];
+                quant<EPL>(x, r, o);
+#pragma unroll
+                for (int q = 0; q < EPL / 16; ++q) reinterpret_cast<uint4*>(rec + c * EPL)[q] = o[q];
                 if (c == 0) *reinterpret_cast<uint4*>(rec + D) = make_uint4(__float_as_uint(s), 0u, 0u, 0u);
             }
         }
@@ -184,8 +209,10 @@ __global__ void __launch_bounds__(kThreads) fp8_pack_kernel(const __grid_constan
 
 // Dequantizing unpack: records -> destination heads (16/32-bit), with the
 // optional RoPE rotation of the receive preparation.
-template <int MODE, int EB, bool ROPE>
-__global__ void __launch_bounds__(kThreads) fp8_unpack_kernel(const __grid_constant__ Fp8Args A, int rpw) {
+template <int MODE, int EB, bool ROPE, int EPL>
+__global__ void __launch_bounds__(kThreads, 3) fp8_unpack_kernel(const __grid_constant__ Fp8Args A, int rpw) {
+    constexpr int NC = EPL / 16;             // 16-byte code vectors per lane and head
+    constexpr int NU = 4;                    // heads in flight per lane
     __shared__ Fp8IO ios[kThreads];
     const int rpb = rpw * (kThreads / 32);
     const long long r0 = (long long)blockIdx.x * rpb;
@@ -207,62 +234,79 @@ __global__ void __launch_bounds__(kThreads) fp8_unpack_kernel(const __grid_const
     const int mine = lane >> A.lg;
     const bool check = A.range_flag != nullptr;
     bool overflow = false;
-    for (int base = mine; base < units; base += upw * kUnits) {
-        uint2 code[kUnits];
-        float scale[kUnits];
+    int g = mine / Hl, hl = mine - (mine / Hl) * Hl;
+    for (int base = mine; base < units; base += upw * NU) {
+        uint4 code[NU][NC];
+        float scale[NU];
+        int gh[NU];
 #pragma unroll
-        for (int b = 0; b < kUnits; ++b) {
-            code[b] = make_uint2(0, 0);
+        for (int b = 0; b < NU; ++b) {
+            gh[b] = (g << 16) | hl;
+            hl += upw;
+            while (hl >= Hl) { hl -= Hl; ++g; }
+        }
+#pragma unroll
+        for (int b = 0; b < NU; ++b) {
+#pragma unroll
+            for (int q = 0; q < NC; ++q) code[b][q] = make_uint4(0, 0, 0, 0);
             scale[b] = 0.f;
-            const int u = base + b * upw;
-            if (u < units) {
-                const int g = u / Hl, hl = u - (u / Hl) * Hl;
-                const char* rec = ios[g0 + g].src + (long long)hl * (D + 16);
-                code[b] = *reinterpret_cast<const uint2*>(rec + c * 8);
+            if (base + b * upw < units) {
+                const char* rec = ios[g0 + (gh[b] >> 16)].src + (long long)(gh[b] & 0xffff) * (D + 16);
+#pragma unroll
+                for (int q = 0; q < NC; ++q) code[b][q] = reinterpret_cast<const uint4*>(rec + c * EPL)[q];
                 scale[b] = *reinterpret_cast<const float*>(rec + D);
             }
         }
 #pragma unroll
-        for (int b = 0; b < kUnits; ++b) {
-            const int u = base + b * upw;
-            if (u >= units) continue;
-            const int g = u / Hl, hl = u - (u / Hl) * Hl;
-            const Fp8IO& io = ios[g0 + g];
-            if (MODE == DQ_UNPACK_H2S && hl >= io.nreal) continue;
-            const uint32_t w[2] = {code[b].x, code[b].y};
-            Vec8 v;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 f = from_e4m3x2((uint16_t)(w[k >> 1] >> (16 * (k & 1))));
-                v.f[2 * k] = __fmul_rn(f.x, scale[b]);
-                v.f[2 * k + 1] = __fmul_rn(f.y, scale[b]);
-            }
+        for (int b = 0; b < NU; ++b) {
+            if (base + b * upw >= units) continue;
+            const int h = gh[b] & 0xffff;
+            const Fp8IO& io = ios[g0 + (gh[b] >> 16)];
+            if (MODE == DQ_UNPACK_H2S && h >= io.nreal) continue;
+            const dit_dtype t = (dit_dtype)io.dt;
+            char* dst = io.dst + ((long long)h * D + c * EPL) * dtype_bytes(t);
+            const float* cs = nullptr;
+            const float* sn = nullptr;
             if (ROPE && io.rope_pos >= 0) {
-                const long long e = (long long)io.rope_pos * (D >> 1) + c * 4;
-                const float4 cs = *reinterpret_cast<const float4*>(A.rope_cos + e);
-                const float4 sn = *reinterpret_cast<const float4*>(A.rope_sin + e);
-                const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
+                cs = A.rope_cos + (long long)io.rope_pos * (D >> 1) + c * (EPL / 2);
+                sn = A.rope_sin + (long long)io.rope_pos * (D >> 1) + c * (EPL / 2);
+            }
+#pragma unroll
+            for (int v = 0; v < EPL / 8; ++v) {          // 8 values at a time
+                const uint32_t w0 = (&code[b][v >> 1].x)[(v & 1) * 2];
+                const uint32_t w1 = (&code[b][v >> 1].x)[(v & 1) * 2 + 1];
+                const uint32_t w[2] = {w0, w1};
+                Vec8 y;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float x0 = v.f[2 * k], x1 = v.f[2 * k + 1];
-                    v.f[2 * k] = fmaf(x0, cc[k], -(x1 * ss[k]));
-                    v.f[2 * k + 1] = fmaf(x0, ss[k], x1 * cc[k]);
+                    const float2 f = from_e4m3x2((uint16_t)(w[k >> 1] >> (16 * (k & 1))));
+                    y.f[2 * k] = __fmul_rn(f.x, scale[b]);
+                    y.f[2 * k + 1] = __fmul_rn(f.y, scale[b]);
                 }
-            }
-            const dit_dtype t = (dit_dtype)io.dt;
-            char* dst = io.dst + ((long long)hl * D + c * 8) * dtype_bytes(t);
-            if (EB == 4) {
-                store8(dst, DIT_F32, v);
-            } else {
-                uint4 o = make_uint4(pack2(v.f[0], v.f[1], t), pack2(v.f[2], v.f[3], t), pack2(v.f[4], v.f[5], t),
-                                     pack2(v.f[6], v.f[7], t));
-                if (check) {
-                    Vec8 back;
-                    load8(&o, t, back);
+                if (ROPE && cs != nullptr) {
+                    const float4 cc = reinterpret_cast<const float4*>(cs)[v];
+                    const float4 ss = reinterpret_cast<const float4*>(sn)[v];
+                    const float ca[4] = {cc.x, cc.y, cc.z, cc.w}, sa[4] = {ss.x, ss.y, ss.z, ss.w};
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) overflow |= isinf(back.f[e]) && !isinf(v.f[e]);
+                    for (int k = 0; k < 4; ++k) {
+                        const float x0 = y.f[2 * k], x1 = y.f[2 * k + 1];
+                        y.f[2 * k] = fmaf(x0, ca[k], -(x1 * sa[k]));
+                        y.f[2 * k + 1] = fmaf(x0, sa[k], x1 * ca[k]);
+                    }
                 }
-                *reinterpret_cast<uint4*>(dst) = o;
+                if (EB == 4) {
+                    store8(dst + v * 32, DIT_F32, y);
+                } else {
+                    uint4 o = make_uint4(pack2(y.f[0], y.f[1], t), pack2(y.f[2], y.f[3], t),
+                                         pack2(y.f[4], y.f[5], t), pack2(y.f[6], y.f[7], t));
+                    if (check) {
+                        Vec8 back;
+                        load8(&o, t, back);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) overflow |= isinf(back.f[e]) && !isinf(y.f[e]);
+                    }
+                    reinterpret_cast<uint4*>(dst)[v] = o;
+                }
             }
         }
     }
@@ -283,14 +327,28 @@ dit_status launch_fp8(K kernel, const Fp8Args& a, cudaStream_t st, const char* w
     return check_launch(who);
 }
 
+// lg = log2 of the lanes per head: D / 32 (D / 16 for D = 16)
 dit_status check_fp8_shape(const dit_sp_layout* L, const char* who, int* lg) {
     const int D = L->D;
     if (D < 16 || D > 256 || (D & (D - 1)))
         return fail(DIT_ERR_UNSUPPORTED, "%s: the e4m3 wire needs D in {16, 32, 64, 128, 256}", who);
+    const int epl = D == 16 ? 16 : 32;
     int g = 0;
-    while ((8 << g) < D) ++g;
+    while ((epl << g) < D) ++g;
     *lg = g;
     return DIT_OK;
+}
+
+template <int EPL>
+dit_status launch_unpack(const Fp8Args& a, dit_a2a_dir dir, bool wide, bool rope, cudaStream_t st, const char* who) {
+    if (dir == DIT_HEAD_TO_SEQ)
+        return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_H2S, 4, false, EPL>, a, st, who)
+                    : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_H2S, 2, false, EPL>, a, st, who);
+    if (rope)
+        return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 4, true, EPL>, a, st, who)
+                    : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 2, true, EPL>, a, st, who);
+    return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 4, false, EPL>, a, st, who)
+                : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 2, false, EPL>, a, st, who);
 }
 
 }  // namespace
@@ -313,11 +371,18 @@ dit_status fp8_pack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, const 
     a.dst[0] = send;
     a.nruns = (long long)nplanes * L->B * L->U * L->S;
     const bool wide = dtype_bytes(src_dt) == 4;
+    if (L->D == 16) {
+        if (dir == DIT_SEQ_TO_HEAD)
+            return wide ? launch_fp8(fp8_pack_kernel<Q_PACK_S2H, 4, 16>, a, st, who)
+                        : launch_fp8(fp8_pack_kernel<Q_PACK_S2H, 2, 16>, a, st, who);
+        return wide ? launch_fp8(fp8_pack_kernel<Q_PACK_H2S, 4, 16>, a, st, who)
+                    : launch_fp8(fp8_pack_kernel<Q_PACK_H2S, 2, 16>, a, st, who);
+    }
     if (dir == DIT_SEQ_TO_HEAD)
-        return wide ? launch_fp8(fp8_pack_kernel<Q_PACK_S2H, 4>, a, st, who)
-                    : launch_fp8(fp8_pack_kernel<Q_PACK_S2H, 2>, a, st, who);
-    return wide ? launch_fp8(fp8_pack_kernel<Q_PACK_H2S, 4>, a, st, who)
-                : launch_fp8(fp8_pack_kernel<Q_PACK_H2S, 2>, a, st, who);
+        return wide ? launch_fp8(fp8_pack_kernel<Q_PACK_S2H, 4, 32>, a, st, who)
+                    : launch_fp8(fp8_pack_kernel<Q_PACK_S2H, 2, 32>, a, st, who);
+    return wide ? launch_fp8(fp8_pack_kernel<Q_PACK_H2S, 4, 32>, a, st, who)
+                : launch_fp8(fp8_pack_kernel<Q_PACK_H2S, 2, 32>, a, st, who);
 }
 
 dit_status fp8_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, const void* recv, void* const* dst,
@@ -345,15 +410,8 @@ dit_status fp8_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, cons
     a.rope_sin = sin_tab;
     a.rope_planes = rope_planes;
     a.nruns = (long long)nplanes * L->B * L->U * L->S;
-    const bool wide = db == 4;
-    if (dir == DIT_HEAD_TO_SEQ)
-        return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_H2S, 4, false>, a, st, who)
-                    : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_H2S, 2, false>, a, st, who);
-    if (rope_planes)
-        return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 4, true>, a, st, who)
-                    : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 2, true>, a, st, who);
-    return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 4, false>, a, st, who)
-                : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 2, false>, a, st, who);
+    if (L->D == 16) return launch_unpack<16>(a, dir, db == 4, rope_planes != 0, st, who);
+    return launch_unpack<32>(a, dir, db == 4, rope_planes != 0, st, who);
 }
 
 }  // namespace ditsp
