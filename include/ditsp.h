@@ -191,6 +191,19 @@ DIT_API dit_status dit_sp_a2a_counts(const dit_sp_layout* L, dit_a2a_dir dir, in
  * The three calls require D*sizeof(type) to be a multiple of 16 bytes for
  * every type involved and 16-byte aligned pointers.  send/recv must not
  * overlap any other buffer of the same call.
+ *
+ * wire_dt = DIT_E4M3 (cache-dit "Context Parallelism", Async FP8 Ulysses
+ * Attention: Q, V and O cross the all-to-all in float8, K stays 16-bit):
+ * every (token, head) travels as a record of D + 16 bytes, the send and
+ * receive buffers hold nplanes*B*S*Hp records in the wire order above.  The
+ * pack computes, in IEEE float32 with round to nearest even,
+ *   amax = max |x_d|,  s = amax / 448,  r = 1 / s (0 when s = 0),
+ *   code_d = e4m3(x_d * r) with saturation to +-448,
+ * and writes the D codes, s (float32) and 12 zero bytes; padded heads are
+ * zero records.  The unpack writes code_d * s (float32) rounded to dst_dt.
+ * dit_a2a_sim moves records unchanged.  D must be 16, 32, 64, 128 or 256
+ * (else DIT_ERR_UNSUPPORTED); inputs must be finite (a head holding an
+ * infinity or NaN gets an unspecified record).  Keep K on a 16-bit wire.
  */
 DIT_API dit_status dit_ulysses_pack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
                             const void* const* src, dit_dtype src_dt,
