@@ -102,7 +102,8 @@ def from_records(rec: np.ndarray):
 
 def _word_layout(L):
     from .layout import make_layout
-    return make_layout(L.B, L.S, L.H, record_bytes(L.D) // 2, L.U, L.R)
+    return make_layout(L.B, L.S, L.H, record_bytes(L.D) // 2, L.U, L.R, pad_heads=L.pad_heads,
+                       pad_lcm64=L.pad_lcm64)
 
 
 def _words(rec: np.ndarray) -> np.ndarray:

@@ -30,9 +30,14 @@ from .numeric import BITS_DTYPE, convert_bits
 
 def _heads_of(L: SPLayout, v: int) -> Tuple[int, int]:
     """Global heads [h0, h1) of head group v that are real (h < H)."""
-    h0 = v * L.Hl
-    h1 = min(h0 + L.Hl, L.H)
+    h0 = L.head_off[v]
+    h1 = min(h0 + L.head_len[v], L.H)
     return h0, max(h0, h1)
+
+
+def _real(L: SPLayout, off: int, n: int) -> int:
+    """How many of the rows [off, off + n) are real (not sequence padding)."""
+    return max(0, min(n, L.S - off))
 
 
 def s2h_pack(L: SPLayout, planes: Sequence[np.ndarray], src_dt: str,
@@ -40,9 +45,10 @@ def s2h_pack(L: SPLayout, planes: Sequence[np.ndarray], src_dt: str,
     """Build every virtual rank's sequence-to-head send buffer.
 
     planes[p] is the global [B, S, H, D] tensor of plane p (Q, K, V); rank
-    (r, u) owns rows [off, off + len).  Its send buffer is, for each
-    destination v in order, the block [planes][B][len][Hl][D] holding heads
-    v*Hl .. v*Hl+Hl-1 of its rows; heads >= H are zero.
+    (r, u) owns rows [off, off + len) of the S_pad rows.  Its send buffer is,
+    for each destination v in order, the block [planes][B][len][Hl_v][D]
+    holding head group v of its rows; heads >= H and rows >= S (sequence
+    padding) are zero.
     """
     nplanes = len(planes)
     send_base, _, total = buffer_bases(L, "s2h", nplanes)
@@ -52,13 +58,14 @@ def s2h_pack(L: SPLayout, planes: Sequence[np.ndarray], src_dt: str,
             rid = L.rank(r, u)
             n, off = L.rank_len[rid], L.rank_off[rid]
             sc, sd, _, _ = a2a_counts(L, "s2h", nplanes, rid)
+            m = _real(L, off, n)
             for v in range(L.U):
-                blk = np.zeros((nplanes, L.B, n, L.Hl, L.D),
+                blk = np.zeros((nplanes, L.B, n, L.head_len[v], L.D),
                                dtype=BITS_DTYPE[wire_dt])
                 h0, h1 = _heads_of(L, v)
                 for p in range(nplanes):
-                    src = planes[p][:, off:off + n, h0:h1, :]
-                    blk[p, :, :, 0:h1 - h0, :] = convert_bits(src, src_dt, wire_dt)
+                    src = planes[p][:, off:off + m, h0:h1, :]
+                    blk[p, :, 0:m, 0:h1 - h0, :] = convert_bits(src, src_dt, wire_dt)
                 assert blk.size == sc[v]
                 start = send_base[rid] + sd[v]
                 send[start:start + blk.size] = blk.reshape(-1)
@@ -87,9 +94,9 @@ def s2h_unpack(L: SPLayout, recv: np.ndarray, wire_dt: str,
                dst_dts: Sequence[str]) -> Dict[Tuple[int, int], List[np.ndarray]]:
     """Head-sharded per-rank planes from the received blocks.
 
-    Returns {(r, v): [plane_0, ...]} with plane_p of shape [B, S_r, Hl, D]
-    (ring block r's rows in global order, local heads of group v), each
-    converted to dst_dts[p].
+    Returns {(r, v): [plane_0, ...]} with plane_p of shape [B, S_r, Hl_v, D]
+    (ring block r's rows in global order, padding rows included, local heads
+    of group v), each converted to dst_dts[p].
     """
     nplanes = len(dst_dts)
     _, recv_base, _ = buffer_bases(L, "s2h", nplanes)
@@ -99,13 +106,13 @@ def s2h_unpack(L: SPLayout, recv: np.ndarray, wire_dt: str,
         for v in range(L.U):
             dst = L.rank(r, v)
             _, _, rc, rd = a2a_counts(L, "s2h", nplanes, dst)
-            planes = [np.zeros((L.B, Sr, L.Hl, L.D), dtype=BITS_DTYPE[dt])
+            planes = [np.zeros((L.B, Sr, L.head_len[v], L.D), dtype=BITS_DTYPE[dt])
                       for dt in dst_dts]
             for u in range(L.U):
                 n = L.rank_len[L.rank(r, u)]
                 row0 = L.rank_off[L.rank(r, u)] - L.ring_off[r]
                 a = recv_base[dst] + rd[u]
-                blk = recv[a:a + rc[u]].reshape(nplanes, L.B, n, L.Hl, L.D)
+                blk = recv[a:a + rc[u]].reshape(nplanes, L.B, n, L.head_len[v], L.D)
                 for p in range(nplanes):
                     planes[p][:, row0:row0 + n] = convert_bits(blk[p], wire_dt,
                                                                dst_dts[p])
@@ -115,10 +122,11 @@ def s2h_unpack(L: SPLayout, recv: np.ndarray, wire_dt: str,
 
 def h2s_pack(L: SPLayout, o_ranks: Dict[Tuple[int, int], np.ndarray], src_dt: str,
              wire_dt: str) -> np.ndarray:
-    """Head-to-sequence send buffers from each rank's [B, S_r, Hl, D] output.
+    """Head-to-sequence send buffers from each rank's [B, S_r, Hl_v, D] output.
 
-    Rank (r, v) sends peer u the rows of u's slice, all Hl local heads;
-    local heads whose global index is >= H are zero on the wire.
+    Rank (r, v) sends peer u the rows of u's slice, all Hl_v local heads;
+    local heads whose global index is >= H and sequence-padding rows are
+    zero on the wire.
     """
     send_base, _, total = buffer_bases(L, "h2s", 1)
     send = np.zeros(total, dtype=BITS_DTYPE[wire_dt])
@@ -130,10 +138,11 @@ def h2s_pack(L: SPLayout, o_ranks: Dict[Tuple[int, int], np.ndarray], src_dt: st
             h0, h1 = _heads_of(L, v)
             for u in range(L.U):
                 n = L.rank_len[L.rank(r, u)]
+                m = _real(L, L.rank_off[L.rank(r, u)], n)
                 row0 = L.rank_off[L.rank(r, u)] - L.ring_off[r]
-                blk = np.zeros((1, L.B, n, L.Hl, L.D), dtype=BITS_DTYPE[wire_dt])
-                blk[0, :, :, 0:h1 - h0, :] = convert_bits(
-                    o[:, row0:row0 + n, 0:h1 - h0, :], src_dt, wire_dt)
+                blk = np.zeros((1, L.B, n, L.head_len[v], L.D), dtype=BITS_DTYPE[wire_dt])
+                blk[0, :, 0:m, 0:h1 - h0, :] = convert_bits(
+                    o[:, row0:row0 + m, 0:h1 - h0, :], src_dt, wire_dt)
                 assert blk.size == sc[u]
                 start = send_base[src] + sd[u]
                 send[start:start + blk.size] = blk.reshape(-1)
@@ -141,19 +150,20 @@ def h2s_pack(L: SPLayout, o_ranks: Dict[Tuple[int, int], np.ndarray], src_dt: st
 
 
 def h2s_unpack(L: SPLayout, recv: np.ndarray, wire_dt: str, out_dt: str) -> np.ndarray:
-    """Sequence-sharded output [B, S, H, D]: rank (r, u) fills its rows from
-    every head group v, dropping the padded heads."""
+    """Sequence-sharded output [B, S, H, D]: rank (r, u) fills its real rows
+    from every head group v, dropping the padded heads and padding rows."""
     _, recv_base, _ = buffer_bases(L, "h2s", 1)
     out = np.zeros((L.B, L.S, L.H, L.D), dtype=BITS_DTYPE[out_dt])
     for r in range(L.R):
         for u in range(L.U):
             dst = L.rank(r, u)
             n, off = L.rank_len[dst], L.rank_off[dst]
+            m = _real(L, off, n)
             _, _, rc, rd = a2a_counts(L, "h2s", 1, dst)
             for v in range(L.U):
                 a = recv_base[dst] + rd[v]
-                blk = recv[a:a + rc[v]].reshape(1, L.B, n, L.Hl, L.D)
+                blk = recv[a:a + rc[v]].reshape(1, L.B, n, L.head_len[v], L.D)
                 h0, h1 = _heads_of(L, v)
-                out[:, off:off + n, h0:h1, :] = convert_bits(
-                    blk[0, :, :, 0:h1 - h0, :], wire_dt, out_dt)
+                out[:, off:off + m, h0:h1, :] = convert_bits(
+                    blk[0, :, 0:m, 0:h1 - h0, :], wire_dt, out_dt)
     return out

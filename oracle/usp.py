@@ -31,7 +31,7 @@ def usp_attention(L: SPLayout, q: np.ndarray, k: np.ndarray, v: np.ndarray,
                   scale: Optional[float] = None):
     """q, k, v: float64 [B, S, H, D].  Returns (O [B,S,H,D], per-rank lse).
 
-    The per-rank lse dict maps (r, v) to [B, Hl, S_r] (merged over the ring).
+    The per-rank lse dict maps (r, v) to [B, Hl_v, S_r] (merged over the ring).
     """
     planes = [from_f64(x, "f64") for x in (q, k, v)]
     send = ulysses.s2h_pack(L, planes, "f64", "f64")
@@ -46,7 +46,8 @@ def usp_attention(L: SPLayout, q: np.ndarray, k: np.ndarray, v: np.ndarray,
             for j in range(L.R):           # K/V chunks visiting rank (r, vv)
                 kj = to_f64(ranks[(j, vv)][1], "f64")
                 vj = to_f64(ranks[(j, vv)][2], "f64")
-                parts.append(att.partial(qr, kj, vj, kj.shape[1], scale))
+                # sequence-padding rows of the chunk are no keys
+                parts.append(att.partial(qr, kj, vj, L.real_rows(j), scale))
             o, lse = att.merge(parts)
             o_ranks[(r, vv)] = from_f64(o, "f64")
             lse_ranks[(r, vv)] = lse

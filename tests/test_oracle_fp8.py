@@ -102,3 +102,18 @@ def test_head_to_seq_exchange_drops_padding():
     got = numeric.to_f64(fp8.h2s_unpack(L, recv, "f32"), "f32")
     want = fp8.dequantize_heads(*fp8.quantize_heads(o[:, :, :H]))
     np.testing.assert_array_equal(got, want)
+
+
+def test_exchange_in_the_unpadded_and_lcm_padded_layouts():
+    B, S, H, D, U, R = 1, 70, 5, 16, 3, 2
+    for ph, pl in [(False, False), (True, True), (False, True)]:
+        L = olayout.make_layout(B, S, H, D, U, R, pad_heads=ph, pad_lcm64=pl)
+        x = bits(synth.normal((B, S, H, D), 80, 1.0, "bf16"))
+        recv = fp8.a2a(L, "s2h", 1, fp8.s2h_pack(L, [x], "bf16"))
+        want = fp8.dequantize_heads(*fp8.quantize_heads(numeric.to_f64(x, "bf16").astype(np.float32)))
+        for (r, v), planes in fp8.s2h_unpack(L, recv, ["f32"]).items():
+            got = numeric.to_f64(planes[0], "f32")
+            m = L.real_rows(r)
+            h0, h1 = L.head_off[v], min(L.head_off[v] + L.head_len[v], H)
+            np.testing.assert_array_equal(got[:, :m, :h1 - h0], want[:, L.ring_off[r]:L.ring_off[r] + m, h0:h1])
+            assert np.all(got[:, m:] == 0) and np.all(got[:, :, h1 - h0:] == 0)

@@ -91,3 +91,42 @@ def test_counts_are_consistent(direction, dims):
             assert sd == [sum(sc[:i]) for i in range(U)]
     send_base, recv_base, total = layout.buffer_bases(L, direction, nplanes)
     assert total == nplanes * B * S * L.Hp * D
+
+
+@pytest.mark.parametrize("S,sp,S_pad", [(4608, 4, 4608), (4481, 8, 4544), (7145, 10, 7360),
+                                        (75600, 32, 75648), (0, 4, 0), (1, 3, 192), (191, 3, 192)])
+def test_padded_length_is_the_next_multiple_of_lcm_sp_64(S, sp, S_pad):
+    # hand-worked: lcm(8, 64) = 64, lcm(10, 64) = 320, lcm(3, 64) = 192
+    assert layout.padded_length(S, sp) == S_pad
+
+
+@pytest.mark.parametrize("H,U,lens", [(24, 5, [5, 5, 5, 5, 4]), (30, 4, [8, 8, 7, 7]),
+                                      (40, 8, [5] * 8), (2, 3, [1, 1, 0])])
+def test_unpadded_heads_are_split_without_padding(H, U, lens):
+    L = layout.make_layout(1, 10, H, 8, U, 1, pad_heads=False)
+    assert list(L.head_len) == lens and L.Hp == H and L.Hl == max(lens)
+    assert list(L.head_off) == [sum(lens[:v]) for v in range(U)]
+
+
+def test_lcm_padding_splits_the_padded_length_evenly():
+    L = layout.make_layout(1, 4481, 24, 8, 4, 2, pad_lcm64=True)
+    assert L.S == 4481 and L.S_pad == 4544
+    assert set(L.rank_len) == {568} and L.ring_len == (2272, 2272)
+    assert [L.real_rows(r) for r in range(2)] == [2272, 2209]
+
+
+@pytest.mark.parametrize("direction", ["s2h", "h2s"])
+@pytest.mark.parametrize("flags", [(False, False), (False, True), (True, True)])
+@pytest.mark.parametrize("dims", [(2, 717, 24, 8, 5, 2), (1, 37, 5, 4, 3, 2)])
+def test_counts_are_consistent_in_every_layout(direction, flags, dims):
+    B, S, H, D, U, R = dims
+    L = layout.make_layout(B, S, H, D, U, R, pad_heads=flags[0], pad_lcm64=flags[1])
+    nplanes = 3 if direction == "s2h" else 1
+    for r in range(R):
+        for u in range(U):
+            sc, sd, _, _ = layout.a2a_counts(L, direction, nplanes, L.rank(r, u))
+            for v in range(U):
+                _, _, rc, rd = layout.a2a_counts(L, direction, nplanes, L.rank(r, v))
+                assert sc[v] == rc[u]
+    _, _, total = layout.buffer_bases(L, direction, nplanes)
+    assert total == nplanes * B * L.S_pad * L.Hp * D

@@ -40,26 +40,49 @@ def _slice_with_padded_heads(x, rows, h0, Hl, H):
     return out
 
 
+# (pad_heads, pad_lcm64): padded heads (the default), padding-free uneven
+# heads, and the lcm(SP, 64) sequence padding with either head layout
+MODES = [(True, False), (False, False), (True, True), (False, True)]
+
+
+def _slice_of(x, L, r, v):
+    """Rows of ring block r (zero past S) and heads of group v (zero past H)
+    of the global tensor x, as rank (r, v) must hold them."""
+    B, S, H, D = x.shape
+    out = np.zeros((B, L.ring_len[r], L.head_len[v], D), dtype=x.dtype)
+    m = L.real_rows(r)
+    h0, h1 = L.head_off[v], min(L.head_off[v] + L.head_len[v], H)
+    if h1 > h0 and m > 0:
+        out[:, :m, :h1 - h0] = x[:, L.ring_off[r]:L.ring_off[r] + m, h0:h1]
+    return out
+
+
 @pytest.mark.parametrize("case", CASES)
-def test_s2h_gives_each_rank_its_heads_over_its_ring_block(case):
+@pytest.mark.parametrize("mode", MODES)
+def test_s2h_gives_each_rank_its_heads_over_its_ring_block(case, mode):
     B, S, H, D, U, R = case
-    L = layout.make_layout(B, S, H, D, U, R)
+    L = layout.make_layout(B, S, H, D, U, R, pad_heads=mode[0], pad_lcm64=mode[1])
     planes = [_bits((B, S, H, D), 100 + p) for p in range(3)]
     send = ulysses.s2h_pack(L, planes, "bf16", "bf16")
     recv = ulysses.a2a(L, "s2h", 3, send)
     ranks = ulysses.s2h_unpack(L, recv, "bf16", ("bf16",) * 3)
     for r in range(R):
-        rows = (L.ring_off[r], L.ring_off[r] + L.ring_len[r])
         for v in range(U):
             for p in range(3):
-                expect = _slice_with_padded_heads(planes[p], rows, v * L.Hl, L.Hl, H)
-                np.testing.assert_array_equal(ranks[(r, v)][p], expect)
+                np.testing.assert_array_equal(ranks[(r, v)][p], _slice_of(planes[p], L, r, v))
+    if mode == (True, False):   # the original reading, written independently of the layout fields
+        for r in range(R):
+            rows = (L.ring_off[r], L.ring_off[r] + L.ring_len[r])
+            for v in range(U):
+                expect = _slice_with_padded_heads(planes[0], rows, v * L.Hl, L.Hl, H)
+                np.testing.assert_array_equal(ranks[(r, v)][0], expect)
 
 
 @pytest.mark.parametrize("case", CASES)
-def test_h2s_after_s2h_is_identity(case):
+@pytest.mark.parametrize("mode", MODES)
+def test_h2s_after_s2h_is_identity(case, mode):
     B, S, H, D, U, R = case
-    L = layout.make_layout(B, S, H, D, U, R)
+    L = layout.make_layout(B, S, H, D, U, R, pad_heads=mode[0], pad_lcm64=mode[1])
     x = _bits((B, S, H, D), 7)
     x[0, 0, 0, 0] = 0x7FC1            # a NaN payload must survive untouched
     send = ulysses.s2h_pack(L, [x], "bf16", "bf16")
@@ -72,25 +95,27 @@ def test_h2s_after_s2h_is_identity(case):
 
 
 @pytest.mark.parametrize("case", CASES)
-def test_padded_heads_never_reach_the_output(case):
+@pytest.mark.parametrize("mode", MODES)
+def test_padding_never_reaches_the_output(case, mode):
     B, S, H, D, U, R = case
-    L = layout.make_layout(B, S, H, D, U, R)
+    L = layout.make_layout(B, S, H, D, U, R, pad_heads=mode[0], pad_lcm64=mode[1])
     rng = np.random.default_rng(5)
     o_ranks = {}
     truth = np.zeros((B, S, H, D), dtype=np.uint16)
     for r in range(R):
+        m = L.real_rows(r)
         for v in range(U):
-            o = rng.integers(0, 0x7F80, size=(B, L.ring_len[r], L.Hl, D), dtype=np.uint16)
-            h0, h1 = v * L.Hl, min(v * L.Hl + L.Hl, H)
+            o = rng.integers(0, 0x7F80, size=(B, L.ring_len[r], L.head_len[v], D), dtype=np.uint16)
+            h0, h1 = L.head_off[v], min(L.head_off[v] + L.head_len[v], H)
             o[:, :, max(h1 - h0, 0):] = 0x7FC0           # NaN in the padded heads
+            o[:, m:] = 0x7FC0                             # and in the padding rows
             o_ranks[(r, v)] = o
             if h1 > h0:
-                truth[:, L.ring_off[r]:L.ring_off[r] + L.ring_len[r], h0:h1] = o[:, :, :h1 - h0]
+                truth[:, L.ring_off[r]:L.ring_off[r] + m, h0:h1] = o[:, :m, :h1 - h0]
     send = ulysses.h2s_pack(L, o_ranks, "bf16", "bf16")
     out = ulysses.h2s_unpack(L, ulysses.a2a(L, "h2s", 1, send), "bf16", "bf16")
     np.testing.assert_array_equal(out, truth)
-    if L.Hp > H:   # padded heads are zero on the wire, not NaN
-        assert not np.any(send == 0x7FC0)
+    assert not np.any(send == 0x7FC0)   # padding is zero on the wire, not NaN
 
 
 def test_send_buffer_matches_textbook_reshape_when_even():

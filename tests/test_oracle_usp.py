@@ -31,3 +31,17 @@ def test_usp_equals_single_shot(B, S, H, D, U, R):
         if h1 > h0:
             rows = slice(L.ring_off[r], L.ring_off[r] + L.ring_len[r])
             np.testing.assert_allclose(l[:, :h1 - h0], lse_ref[:, h0:h1, rows], atol=1e-13)
+
+
+@pytest.mark.parametrize("pad_heads,pad_lcm64", [(False, False), (True, True), (False, True)])
+@pytest.mark.parametrize("B,S,H,D,U,R", [(2, 37, 5, 4, 3, 2), (1, 23, 3, 8, 2, 4), (1, 130, 7, 4, 4, 1)])
+def test_usp_equals_single_shot_in_every_layout(pad_heads, pad_lcm64, B, S, H, D, U, R):
+    # no-pad uneven heads and lcm(SP, 64) sequence padding change only where
+    # rows and heads travel; padding rows are no keys, so the result is the
+    # same full attention
+    rng = np.random.default_rng(S * 17 + U + 5 * R)
+    q, k, v = (rng.standard_normal((B, S, H, D)) for _ in range(3))
+    L = layout.make_layout(B, S, H, D, U, R, pad_heads=pad_heads, pad_lcm64=pad_lcm64)
+    o, _ = usp.usp_attention(L, q, k, v)
+    o_ref, _ = att.attention(q, k, v)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-13)
