@@ -90,20 +90,41 @@ typedef enum { DIT_SEQ_TO_HEAD = 0, DIT_HEAD_TO_SEQ = 1 } dit_a2a_dir;
  * "Parallel execution", SPSequenceSplit and SPAllToAll4DLayout; cache-dit
  * "Context Parallelism", UAA and Any Head Num).
  *
- * The sequence of S rows is split over R ring blocks and each ring block
- * over U Ulysses ranks with the balanced rule: of n parts the first S mod n
- * get one extra row (lengths differ by at most one; no sequence padding).
- * Heads are padded from H to Hp = ceil(H/U)*U; Ulysses rank v owns global
- * heads [v*Hl, (v+1)*Hl), Hl = Hp/U, and heads >= H are zero.
+ * The S_pad rows of the sequence are split over R ring blocks and each ring
+ * block over U Ulysses ranks with the balanced rule: of n parts the first
+ * S_pad mod n get one extra row (lengths differ by at most one).  Rows at or
+ * past S are sequence padding (S_pad = S unless DIT_LAYOUT_PAD_LCM64).
+ * Ulysses rank v owns head_len[v] head slots starting at head_off[v]; head
+ * slots at or past H are zero.  By default heads are padded from H to
+ * Hp = ceil(H/U)*U and every group has Hl = Hp/U slots.
+ *
+ * Layout flags (dit_sp_layout_init_ex):
+ *   DIT_LAYOUT_NOPAD_HEADS  no head padding (cache-dit "Context
+ *     Parallelism", the padding-free variant of Any Head Num): head_len is
+ *     the balanced split of H (the first H mod U groups one more), Hp = H,
+ *     Hl = the largest group.
+ *   DIT_LAYOUT_PAD_LCM64    sequence padding (xLLM "DiT Architecture and
+ *     Capability Matrix": with SP the total length is padded to a multiple
+ *     of lcm(SP, 64) before partitioning): S_pad = S rounded up to a
+ *     multiple of lcm(U*R, 64).  Padding rows travel as zeros, are excluded
+ *     from attention by passing each ring block's real row count, and are
+ *     dropped by the head-to-seq unpack.
  */
+#define DIT_LAYOUT_NOPAD_HEADS 1
+#define DIT_LAYOUT_PAD_LCM64 2
+
 typedef struct {
     int B, S, H, D, U, R;
-    int Hp, Hl;
+    int Hp, Hl;                       /* head slots in total / in the largest group */
     int S_cap;                        /* max ring-block length */
     int ring_len[DIT_MAX_R];          /* rows of ring block r */
     int ring_off[DIT_MAX_R];          /* first global row of ring block r */
     int rank_len[DIT_MAX_RANKS];      /* rows of virtual rank r*U+u */
     int rank_off[DIT_MAX_RANKS];      /* first global row of that rank */
+    int S_pad;                        /* rows split over the ranks (>= S) */
+    int flags;                        /* DIT_LAYOUT_* */
+    int head_len[DIT_MAX_U];          /* head slots of Ulysses rank v */
+    int head_off[DIT_MAX_U];          /* first head slot of Ulysses rank v */
 } dit_sp_layout;
 
 /*
@@ -143,13 +164,19 @@ DIT_API dit_status dit_device_status(int* out_code, int reset);
 DIT_API dit_status dit_sp_layout_init(int B, int S, int H, int D, int U, int R,
                               dit_sp_layout* out);
 
+/* dit_sp_layout_init_ex: as dit_sp_layout_init with DIT_LAYOUT_* flags
+ * (0 gives dit_sp_layout_init); other bits are DIT_ERR_INVALID_ARG. */
+DIT_API dit_status dit_sp_layout_init_ex(int B, int S, int H, int D, int U, int R, int flags,
+                                 dit_sp_layout* out);
+
 /*
  * dit_sp_a2a_counts: the alltoallv argument set of virtual rank `rank` for
  * one exchange carrying `nplanes` planes (3 = packed Q,K,V; 1 = O), in
  * elements, indexed by the peer's Ulysses index within the rank's ring
  * group.  Send blocks are peer-major; the block rank u sends rank v is
- * [nplanes][B][rows][Hl][D] with rows = rank_len of u (seq-to-head) or of
- * v (head-to-seq).  Each output array has room for U entries.  Host only.
+ * [nplanes][B][rows][heads][D] with rows = rank_len of u (seq-to-head) or
+ * of v (head-to-seq) and heads = head_len of v (seq-to-head) or of u
+ * (head-to-seq).  Each output array has room for U entries.  Host only.
  */
 DIT_API dit_status dit_sp_a2a_counts(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
                              int rank, int64_t* send_counts, int64_t* send_displs,
@@ -159,18 +186,22 @@ DIT_API dit_status dit_sp_a2a_counts(const dit_sp_layout* L, dit_a2a_dir dir, in
  * Buffer shapes used by the Ulysses calls (all dense, row-major):
  *   seq layout   [B][S][H][D]              rank (r,u) owns rows
  *                                          [rank_off, rank_off + rank_len)
+ *                                          (the real ones: rows < S)
  *   head layout  [R][B][S_cap][Hp][D]      rank (r,v) owns ring block r,
- *                                          rows [0, ring_len[r]), heads
- *                                          [v*Hl, (v+1)*Hl); rows past
+ *                                          rows [0, ring_len[r]), head
+ *                                          slots [head_off[v], head_off[v]
+ *                                          + head_len[v]); rows past
  *                                          ring_len[r] are never touched
  *   wire         all ranks' send (or receive) buffers end to end in rank-id
- *                order; total nplanes*B*S*Hp*D elements
+ *                order; total nplanes*B*S_pad*Hp*D elements
+ * Sequence-padding rows (>= S) are zero on the wire in both directions and
+ * zero in the head layout after the seq-to-head unpack.
  *
  * dit_ulysses_pack (edge-dit.cpp "Parallel execution": packed QKV send path
  * and head-to-sequence path).
  *   DIT_SEQ_TO_HEAD: src[p] (p < nplanes) are seq-layout planes; every rank
- *     writes, for each destination v in order, its rows of heads
- *     [v*Hl, (v+1)*Hl) of every plane; heads >= H are written as zero.
+ *     writes, for each destination v in order, its rows of head group v of
+ *     every plane; heads >= H are written as zero.
  *   DIT_HEAD_TO_SEQ: src[0] is a head-layout tensor (nplanes must be 1);
  *     rank (r,v) writes, for each destination u, u's rows of its heads;
  *     heads >= H are written as zero.

@@ -75,7 +75,14 @@ class Layout:
             return list(v)[: raw.R]
         if name in ("rank_len", "rank_off"):
             return list(v)[: raw.R * raw.U]
+        if name in ("head_len", "head_off"):
+            return list(v)[: raw.U]
         return v
+
+    def real_rows(self, r: int) -> int:
+        """Rows of ring block r that are not sequence padding."""
+        raw = self.raw
+        return max(0, min(raw.S - raw.ring_off[r], raw.ring_len[r]))
 
     def head_shape(self):
         """Head-layout plane [R, B, S_cap, Hp, D]."""
@@ -88,17 +95,21 @@ class Layout:
 
     def wire_elems(self, nplanes: int) -> int:
         r = self.raw
-        return nplanes * r.B * r.S * r.Hp * r.D
+        return nplanes * r.B * r.S_pad * r.Hp * r.D
 
     def wire_bytes_e4m3(self, nplanes: int) -> int:
         """Bytes of an e4m3 wire: one (D + 16)-byte record per (token, head)."""
         r = self.raw
-        return nplanes * r.B * r.S * r.Hp * (r.D + 16)
+        return nplanes * r.B * r.S_pad * r.Hp * (r.D + 16)
 
 
-def dit_sp_layout_init(B: int, S: int, H: int, D: int, U: int, R: int) -> Layout:
+def dit_sp_layout_init(B: int, S: int, H: int, D: int, U: int, R: int, pad_heads: bool = True,
+                       pad_lcm64: bool = False) -> Layout:
+    """pad_heads=False: the padding-free uneven head split; pad_lcm64: the
+    sequence padded to a multiple of lcm(U*R, 64)."""
     raw = DitSpLayout()
-    check(lib().dit_sp_layout_init(B, S, H, D, U, R, byref(raw)))
+    flags = (0 if pad_heads else _lib.DIT_LAYOUT_NOPAD_HEADS) | (_lib.DIT_LAYOUT_PAD_LCM64 if pad_lcm64 else 0)
+    check(lib().dit_sp_layout_init_ex(B, S, H, D, U, R, flags, byref(raw)))
     return Layout(raw)
 
 

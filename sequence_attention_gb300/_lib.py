@@ -18,11 +18,12 @@ DIT_MAX_RANKS = 64
 
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT, DIT_ERR_RANGE = range(6)
 DIT_F32, DIT_BF16, DIT_F16, DIT_E4M3 = range(4)
+DIT_LAYOUT_NOPAD_HEADS, DIT_LAYOUT_PAD_LCM64 = 1, 2
 DIT_SEQ_TO_HEAD, DIT_HEAD_TO_SEQ = range(2)
 
 #: every function include/ditsp.h declares
 EXPORTS = (
-    "dit_status_string", "dit_last_error", "dit_device_status", "dit_sp_layout_init",
+    "dit_status_string", "dit_last_error", "dit_device_status", "dit_sp_layout_init", "dit_sp_layout_init_ex",
     "dit_sp_a2a_counts", "dit_ulysses_pack", "dit_a2a_sim", "dit_ulysses_unpack",
     "dit_attn_partial", "dit_attn_merge_lse", "dit_attention", "dit_cfg_combine",
     "dit_sp_signal", "dit_a2a_sim_checked", "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint",
@@ -36,6 +37,10 @@ class DitSpLayout(Structure):
         ("ring_off", c_int * DIT_MAX_R),
         ("rank_len", c_int * DIT_MAX_RANKS),
         ("rank_off", c_int * DIT_MAX_RANKS),
+        ("S_pad", c_int),
+        ("flags", c_int),
+        ("head_len", c_int * DIT_MAX_U),
+        ("head_off", c_int * DIT_MAX_U),
     ]
 
 
@@ -74,6 +79,8 @@ def lib() -> ctypes.CDLL:
     L.dit_device_status.argtypes = [POINTER(c_int), c_int]
     L.dit_sp_layout_init.restype = c_int
     L.dit_sp_layout_init.argtypes = [c_int] * 6 + [POINTER(DitSpLayout)]
+    L.dit_sp_layout_init_ex.restype = c_int
+    L.dit_sp_layout_init_ex.argtypes = [c_int] * 7 + [POINTER(DitSpLayout)]
     L.dit_sp_a2a_counts.restype = c_int
     L.dit_sp_a2a_counts.argtypes = [POINTER(DitSpLayout), c_int, c_int, c_int] + [POINTER(c_int64)] * 4
     L.dit_ulysses_pack.restype = c_int

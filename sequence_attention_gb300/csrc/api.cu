@@ -106,8 +106,8 @@ static void split(int S, int n, int* len, int* off, int base) {
     }
 }
 
-extern "C" dit_status dit_sp_layout_init(int B, int S, int H, int D, int U, int R,
-                                         dit_sp_layout* out) {
+extern "C" dit_status dit_sp_layout_init_ex(int B, int S, int H, int D, int U, int R, int flags,
+                                            dit_sp_layout* out) {
     if (!out) return fail(DIT_ERR_INVALID_ARG, "dit_sp_layout_init: out is NULL");
     if (B < 1 || H < 1 || D < 1 || S < 0)
         return fail(DIT_ERR_INVALID_ARG, "dit_sp_layout_init: need B,H,D >= 1 and S >= 0");
@@ -115,17 +115,37 @@ extern "C" dit_status dit_sp_layout_init(int B, int S, int H, int D, int U, int 
         return fail(DIT_ERR_INVALID_ARG,
                     "dit_sp_layout_init: need 1<=U<=%d, 1<=R<=%d, U*R<=%d (got U=%d R=%d)",
                     DIT_MAX_U, DIT_MAX_R, DIT_MAX_RANKS, U, R);
+    if (flags & ~(DIT_LAYOUT_NOPAD_HEADS | DIT_LAYOUT_PAD_LCM64))
+        return fail(DIT_ERR_INVALID_ARG, "dit_sp_layout_init: unknown flags 0x%x", flags);
+    long long S_pad = S;
+    if (flags & DIT_LAYOUT_PAD_LCM64) {
+        long long a = U * R, b = 64;             // lcm(U*R, 64)
+        while (b) { const long long t = a % b; a = b; b = t; }
+        const long long m = (long long)U * R * 64 / a;
+        S_pad = (S + m - 1) / m * m;
+    }
+    const bool nopad = (flags & DIT_LAYOUT_NOPAD_HEADS) != 0;
     const int Hl = (H + U - 1) / U;
-    const long long Hp = (long long)Hl * U;
+    const long long Hp = nopad ? H : (long long)Hl * U;
     // every buffer of the path must be indexable with int64 and its row
     // count with int32
-    const double elems = 3.0 * B * (double)S * (double)Hp * D;
-    if (elems > 4.0e18 || (double)Hp * D > 2.0e9)
+    const double elems = 3.0 * B * (double)S_pad * (double)Hp * D;
+    if (elems > 4.0e18 || (double)Hp * D > 2.0e9 || S_pad > 2000000000LL)
         return fail(DIT_ERR_INVALID_ARG, "dit_sp_layout_init: sizes overflow");
     memset(out, 0, sizeof(*out));
     out->B = B; out->S = S; out->H = H; out->D = D; out->U = U; out->R = R;
     out->Hp = (int)Hp; out->Hl = Hl;
-    split(S, R, out->ring_len, out->ring_off, 0);
+    out->S_pad = (int)S_pad;
+    out->flags = flags;
+    if (nopad) {
+        split(H, U, out->head_len, out->head_off, 0);
+    } else {
+        for (int v = 0; v < U; ++v) {
+            out->head_len[v] = Hl;
+            out->head_off[v] = v * Hl;
+        }
+    }
+    split((int)S_pad, R, out->ring_len, out->ring_off, 0);
     int cap = 0;
     for (int r = 0; r < R; ++r) {
         if (out->ring_len[r] > cap) cap = out->ring_len[r];
@@ -133,6 +153,10 @@ extern "C" dit_status dit_sp_layout_init(int B, int S, int H, int D, int U, int 
     }
     out->S_cap = cap;
     return DIT_OK;
+}
+
+extern "C" dit_status dit_sp_layout_init(int B, int S, int H, int D, int U, int R, dit_sp_layout* out) {
+    return dit_sp_layout_init_ex(B, S, H, D, U, R, 0, out);
 }
 
 extern "C" dit_status dit_sp_a2a_counts(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
@@ -144,13 +168,16 @@ extern "C" dit_status dit_sp_a2a_counts(const dit_sp_layout* L, dit_a2a_dir dir,
         return fail(DIT_ERR_INVALID_ARG, "dit_sp_a2a_counts: bad nplanes or rank");
     if (dir != DIT_SEQ_TO_HEAD && dir != DIT_HEAD_TO_SEQ)
         return fail(DIT_ERR_INVALID_ARG, "dit_sp_a2a_counts: bad direction");
-    const int U = L->U, r = rank / U;
-    const int64_t per_row = (int64_t)nplanes * L->B * L->Hl * L->D;
+    const int U = L->U, r = rank / U, me = rank - r * U;
+    const int64_t row = (int64_t)nplanes * L->B * L->D;     // elements per row and head
     int64_t sacc = 0, racc = 0;
     for (int p = 0; p < U; ++p) {
         const int64_t rows_p = L->rank_len[r * U + p], rows_me = L->rank_len[rank];
-        sc[p] = per_row * (dir == DIT_SEQ_TO_HEAD ? rows_me : rows_p);
-        rc[p] = per_row * (dir == DIT_SEQ_TO_HEAD ? rows_p : rows_me);
+        const int64_t heads_p = L->head_len[p], heads_me = L->head_len[me];
+        // seq->head: I send my rows of p's heads and get p's rows of mine;
+        // head->seq: I send p its rows of my heads and get my rows of p's
+        sc[p] = row * (dir == DIT_SEQ_TO_HEAD ? rows_me * heads_p : rows_p * heads_me);
+        rc[p] = row * (dir == DIT_SEQ_TO_HEAD ? rows_p * heads_me : rows_me * heads_p);
         sd[p] = sacc; sacc += sc[p];
         rd[p] = racc; racc += rc[p];
     }

@@ -52,7 +52,8 @@ struct Fp8Args {
 struct Fp8IO {
     const char* src;
     char* dst;
-    int nreal;        // real heads of the run's group; later heads are padding
+    int nslot;        // head slots (records) of the run
+    int nreal;        // slots holding real heads; later slots (and padding rows) are zero
     int dt;           // the 16/32-bit side's dit_dtype
     int rope_pos;     // joint position whose angles rotate the run, -1 none
 };
@@ -65,31 +66,35 @@ __device__ __forceinline__ Fp8IO fp8_io(const Fp8Args& A, int ri) {
     else if (MODE == Q_PACK_H2S) x = decode_B(L, 1, ri);
     else if (MODE == DQ_UNPACK_S2H) x = decode_H(L, A.np, ri);
     else x = decode_S(L, ri);
-    const long long rec_run = (long long)L.Hl * (L.D + 16);
+    const long long rec = L.D + 16;
+    const bool pad_row = run_row(L, x) >= L.S;
     Fp8IO io;
-    io.nreal = min(max(L.H - x.v * L.Hl, 0), L.Hl);
+    io.nslot = L.head_len[x.v];
+    io.nreal = pad_row ? 0 : real_heads(L, x.v);
     io.rope_pos = -1;
     bool second = false;
     if (MODE == Q_PACK_S2H) {
         io.dt = A.sdt;
         const long long so = io.nreal > 0 ? seq_offset(L, x, A.split, second) : 0;
         io.src = (const char*)(second ? A.src2[x.p] : A.src[x.p]) + so * dtype_bytes(A.sdt);
-        io.dst = (char*)A.dst[0] + ri * rec_run;
+        io.dst = (char*)A.dst[0] + slots_A(L, A.np, x) * rec;
     } else if (MODE == Q_PACK_H2S) {
         io.dt = A.sdt;
         io.src = (const char*)A.src[0] + head_offset(L, x) * dtype_bytes(A.sdt);
-        io.dst = (char*)A.dst[0] + ri * rec_run;
+        io.dst = (char*)A.dst[0] + slots_B(L, 1, x) * rec;
     } else if (MODE == DQ_UNPACK_S2H) {
         io.dt = A.ddt[x.p];
-        io.src = (const char*)A.src[0] + index_B(L, A.np, x) * rec_run;
+        io.src = (const char*)A.src[0] + slots_B(L, A.np, x) * rec;
         io.dst = (char*)A.dst[x.p] + head_offset(L, x) * dtype_bytes(A.ddt[x.p]);
-        if ((A.rope_planes >> x.p) & 1u) io.rope_pos = L.rank_off[x.r * L.U + x.u] + x.i;
+        // the angle tables have S rows: padding rows are not rotated
+        if (((A.rope_planes >> x.p) & 1u) && !pad_row) io.rope_pos = run_row(L, x);
     } else {
         io.dt = A.ddt[0];
-        io.src = (const char*)A.src[0] + index_A(L, 1, x) * rec_run;
+        io.src = (const char*)A.src[0] + slots_A(L, 1, x) * rec;
         const long long doff = io.nreal > 0 ? seq_offset(L, x, A.split, second) : 0;
         io.dst = (char*)(second ? A.dst2[0] : A.dst[0]) + doff * dtype_bytes(A.ddt[0]);
     }
+    (void)ri;
     return io;
 }
 
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 3) fp8_pack_kernel(const __grid_cons
 #pragma unroll
             for (int k = 0; k < EPL; ++k) amax = fmaxf(amax, fabsf(x[k]));
             for (int o = G >> 1; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            if (u < units) {
+            if (u < units && (gh[b] & 0xffff) < ios[g0 + (gh[b] >> 16)].nslot) {
                 const float s = __fdiv_rn(amax, 448.f);
                 const float r = s > 0.f ? __frcp_rn(s) : 0.f;
                 char* rec = ios[g0 + (gh[b] >> 16)].dst + (long long)(gh[b] & 0xffff) * (D + 16);
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 3) fp8_unpack_kernel(const __grid_co
 #pragma unroll
             for (int q = 0; q < NC; ++q) code[b][q] = make_uint4(0, 0, 0, 0);
             scale[b] = 0.f;
-            if (base + b * upw < units) {
+            if (base + b * upw < units && (gh[b] & 0xffff) < ios[g0 + (gh[b] >> 16)].nslot) {
                 const char* rec = ios[g0 + (gh[b] >> 16)].src + (long long)(gh[b] & 0xffff) * (D + 16);
 #pragma unroll
                 for (int q = 0; q < NC; ++q) code[b][q] = reinterpret_cast<const uint4*>(rec + c * EPL)[q];
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 3) fp8_unpack_kernel(const __grid_co
             if (base + b * upw >= units) continue;
             const int h = gh[b] & 0xffff;
             const Fp8IO& io = ios[g0 + (gh[b] >> 16)];
-            if (MODE == DQ_UNPACK_H2S && h >= io.nreal) continue;
+            if (h >= io.nslot || (MODE == DQ_UNPACK_H2S && h >= io.nreal)) continue;
             const dit_dtype t = (dit_dtype)io.dt;
             char* dst = io.dst + ((long long)h * D + c * EPL) * dtype_bytes(t);
             const float* cs = nullptr;
@@ -369,7 +374,7 @@ dit_status fp8_pack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, const 
     a.split = split;
     a.sdt = src_dt;
     a.dst[0] = send;
-    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S_pad;
     const bool wide = dtype_bytes(src_dt) == 4;
     if (L->D == 16) {
         if (dir == DIT_SEQ_TO_HEAD)
@@ -409,7 +414,7 @@ dit_status fp8_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, cons
     a.rope_cos = cos_tab;
     a.rope_sin = sin_tab;
     a.rope_planes = rope_planes;
-    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    a.nruns = (long long)nplanes * L->B * L->U * (dir == DIT_SEQ_TO_HEAD ? L->S_pad : L->S);
     if (L->D == 16) return launch_unpack<16>(a, dir, db == 4, rope_planes != 0, st, who);
     return launch_unpack<32>(a, dir, db == 4, rope_planes != 0, st, who);
 }

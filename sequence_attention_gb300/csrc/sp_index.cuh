@@ -1,15 +1,20 @@
 // Index arithmetic of the Ulysses exchange, shared by the 16/32-bit
 // permutation kernels and the FP8-wire kernels.
 //
-// A "run" is the Hl heads of one rank's head group for one (plane, batch,
-// row): Hl*D contiguous elements on every side of the exchange.  Two wire
-// orders exist:
+// A "run" is the head group of one rank for one (plane, batch, row): the
+// head_len[v] head slots of Ulysses rank v, head_len[v]*D contiguous
+// elements on every side of the exchange.  Two wire orders exist; in units
+// of head slots (Hp = all slots, Hv = head_len[v], ov = head_off[v]):
 //   A (sequence side): rank (r,u)'s buffer = for v: [planes][B][L_u] runs
-//      index  np*B*U*off_u + v*np*B*L_u + (p*B+b)*L_u + i
+//      np*B*Hp*off_u + np*B*L_u*ov + ((p*B+b)*L_u + i)*Hv
 //   B (head side):     rank (r,v)'s buffer = for u: [planes][B][L_u] runs
-//      index  np*B*U*off_r + v*np*B*S_r + np*B*(off_u-off_r) + (p*B+b)*L_u + i
+//      np*B*Hp*off_r + np*B*S_r*ov + np*B*(off_u-off_r)*Hv + ((p*B+b)*L_u + i)*Hv
+// Runs are numbered in either order without regard to their sizes (A: rank,
+// v, plane, batch, row; B: ring block, v, u, plane, batch, row).
 // Seq-to-head: pack writes A, the exchange copies A->B, unpack reads B.
 // Head-to-seq: pack writes B, the exchange copies B->A, unpack reads A.
+// Rows are those of the padded sequence (S_pad); rows at or past S are
+// sequence padding.
 #pragma once
 
 #include "common.cuh"
@@ -78,7 +83,7 @@ __device__ __forceinline__ Run decode_B(const dit_sp_layout& L, int np, int bi) 
 // plane p enumerated as (r, b, row of ring block r, v), so consecutive runs
 // fill one head-layout row.
 __device__ __forceinline__ Run decode_H(const dit_sp_layout& L, int np, int h) {
-    const int per_plane = L.B * L.S * L.U;
+    const int per_plane = L.B * L.S_pad * L.U;
     Run x;
     x.p = h / per_plane;
     const int rem = h - x.p * per_plane;
@@ -96,7 +101,8 @@ __device__ __forceinline__ Run decode_H(const dit_sp_layout& L, int np, int h) {
 }
 
 // Sequence order (destination order of the head->seq unpack, one plane):
-// runs enumerated as (b, token, v), so consecutive runs fill one token row.
+// runs enumerated as (b, token, v) over the S real tokens, so consecutive
+// runs fill one token row.
 __device__ __forceinline__ Run decode_S(const dit_sp_layout& L, int s) {
     Run x;
     x.p = 0;
@@ -111,23 +117,36 @@ __device__ __forceinline__ Run decode_S(const dit_sp_layout& L, int s) {
     return x;
 }
 
-__device__ __forceinline__ long long index_A(const dit_sp_layout& L, int np, const Run& x) {
+// Offset of a run in wire order A / B, in head slots.
+__device__ __forceinline__ long long slots_A(const dit_sp_layout& L, int np, const Run& x) {
     const int rid = x.r * L.U + x.u;
-    const int Lu = L.rank_len[rid];
-    return (long long)np * L.B * L.U * L.rank_off[rid] + (long long)x.v * np * L.B * Lu +
-           ((long long)x.p * L.B + x.b) * Lu + x.i;
+    const long long Lu = L.rank_len[rid];
+    return (long long)np * L.B * L.Hp * L.rank_off[rid] + np * L.B * Lu * L.head_off[x.v] +
+           (((long long)x.p * L.B + x.b) * Lu + x.i) * L.head_len[x.v];
 }
 
-__device__ __forceinline__ long long index_B(const dit_sp_layout& L, int np, const Run& x) {
+__device__ __forceinline__ long long slots_B(const dit_sp_layout& L, int np, const Run& x) {
     const int rid = x.r * L.U + x.u;
     const int offr = L.ring_off[x.r];
-    return (long long)np * L.B * L.U * offr + (long long)x.v * np * L.B * L.ring_len[x.r] +
-           (long long)np * L.B * (L.rank_off[rid] - offr) +
-           ((long long)x.p * L.B + x.b) * L.rank_len[rid] + x.i;
+    const long long Hv = L.head_len[x.v];
+    return (long long)np * L.B * L.Hp * offr + (long long)np * L.B * L.ring_len[x.r] * L.head_off[x.v] +
+           (long long)np * L.B * (L.rank_off[rid] - offr) * Hv +
+           (((long long)x.p * L.B + x.b) * L.rank_len[rid] + x.i) * Hv;
+}
+
+// global (padded-sequence) row of a run
+__device__ __forceinline__ int run_row(const dit_sp_layout& L, const Run& x) {
+    return L.rank_off[x.r * L.U + x.u] + x.i;
+}
+
+// head slots of the run's group that hold real heads (global head < H)
+__device__ __forceinline__ int real_heads(const dit_sp_layout& L, int v) {
+    return min(max(L.H - L.head_off[v], 0), L.head_len[v]);
 }
 
 // element offset of the run's first head in a seq-layout plane [B][S][H][D]
-// (only meaningful when the group has a real head).  With paired streams,
+// (only meaningful when the group has a real head and the row is real).
+// With paired streams,
 // rows at or past `split` are in the second tensor, [B][S - split][H][D];
 // `second` says which.
 __device__ __forceinline__ long long seq_offset(const dit_sp_layout& L, const Run& x, int split, bool& second) {
@@ -138,13 +157,13 @@ __device__ __forceinline__ long long seq_offset(const dit_sp_layout& L, const Ru
         rows = second ? L.S - split : split;
         if (second) row -= split;
     }
-    return (((long long)x.b * rows + row) * L.H + (long long)x.v * L.Hl) * L.D;
+    return (((long long)x.b * rows + row) * L.H + L.head_off[x.v]) * L.D;
 }
 
 // element offset in a head-layout plane [R][B][S_cap][Hp][D]
 __device__ __forceinline__ long long head_offset(const dit_sp_layout& L, const Run& x) {
     const int row = L.rank_off[x.r * L.U + x.u] - L.ring_off[x.r] + x.i;
-    return ((((long long)x.r * L.B + x.b) * L.S_cap + row) * L.Hp + (long long)x.v * L.Hl) * L.D;
+    return ((((long long)x.r * L.B + x.b) * L.S_cap + row) * L.Hp + L.head_off[x.v]) * L.D;
 }
 
 }  // namespace

@@ -106,10 +106,12 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
     else if (MODE == UNPACK_H2S) x = decode_S(L, ri);
     else x = decode_B(L, A.np, ri);
     const int p = x.p;
-    const long long run_elems = (long long)L.Hl * L.D;
-    // real heads of this head group; heads at or past nreal are padding
-    const int nreal = min(max(L.H - x.v * L.Hl, 0), L.Hl);
-    const int full = (L.Hl * L.D) >> 3, real = (nreal * L.D) >> 3;
+    const long long D = L.D;
+    // head slots of this run, and those holding real heads; a row at or past
+    // S is sequence padding and holds none
+    const bool pad_row = run_row(L, x) >= L.S;
+    const int nreal = pad_row ? 0 : real_heads(L, x.v);
+    const int full = (L.head_len[x.v] * L.D) >> 3, real = (nreal * L.D) >> 3;
     RunIO io;
     io.src_lim = io.dst_lim = full;
     io.rope_pos = -1;
@@ -118,31 +120,32 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
     bool second = false;
     if (MODE == PACK_S2H) {
         sdt = A.src_dt[p]; ddt = A.dst_dt[0];
-        so = nreal > 0 ? seq_offset(L, x, A.split, second) : 0; doff = ri * run_elems;
+        so = nreal > 0 ? seq_offset(L, x, A.split, second) : 0; doff = slots_A(L, A.np, x) * D;
         io.src = (const char*)(second ? A.src2[p] : A.src[p]); io.dst = (char*)A.dst[0];
         io.src_lim = real;
     } else if (MODE == UNPACK_H2S) {
         sdt = A.src_dt[0]; ddt = A.dst_dt[0];
-        so = index_A(L, A.np, x) * run_elems; doff = nreal > 0 ? seq_offset(L, x, A.split, second) : 0;
+        so = slots_A(L, A.np, x) * D; doff = nreal > 0 ? seq_offset(L, x, A.split, second) : 0;
         io.src = (const char*)A.src[0]; io.dst = (char*)(second ? A.dst2[0] : A.dst[0]);
         io.dst_lim = real;
     } else if (MODE == PACK_H2S) {
         sdt = A.src_dt[0]; ddt = A.dst_dt[0];
-        so = head_offset(L, x); doff = ri * run_elems;
+        so = head_offset(L, x); doff = slots_B(L, A.np, x) * D;
         io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[0];
         io.src_lim = real;
     } else if (MODE == UNPACK_S2H) {
         sdt = A.src_dt[0]; ddt = A.dst_dt[p];
-        so = index_B(L, A.np, x) * run_elems; doff = head_offset(L, x);
+        so = slots_B(L, A.np, x) * D; doff = head_offset(L, x);
         io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[p];
-        if ((A.rope_planes >> p) & 1u) io.rope_pos = L.rank_off[x.r * L.U + x.u] + x.i;
+        // the angle tables have S rows: padding rows are not rotated
+        if (((A.rope_planes >> p) & 1u) && !pad_row) io.rope_pos = run_row(L, x);
     } else if (MODE == A2A_S2H) {
         sdt = ddt = A.src_dt[0];
-        so = index_A(L, A.np, x) * run_elems; doff = ri * run_elems;
+        so = slots_A(L, A.np, x) * D; doff = slots_B(L, A.np, x) * D;
         io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[0];
     } else {  // A2A_H2S
         sdt = ddt = A.src_dt[0];
-        so = index_B(L, A.np, x) * run_elems; doff = ri * run_elems;
+        so = slots_B(L, A.np, x) * D; doff = slots_A(L, A.np, x) * D;
         io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[0];
     }
     io.src += so * dtype_bytes(sdt);
@@ -151,6 +154,7 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
     io.ddt = ddt;
     // seq->head: rank (r,u) sends to (r,v); head->seq: rank (r,v) sends to (r,u)
     io.sender = x.r * L.U + (MODE == A2A_H2S || MODE == PACK_H2S || MODE == UNPACK_H2S ? x.v : x.u);
+    (void)ri;
     return io;
 }
 
@@ -438,9 +442,11 @@ dit_status record_words(RunArgs* a, const char* who) {
 dit_status check_layout(const dit_sp_layout* L, const char* who) {
     if (!L) return fail(DIT_ERR_INVALID_ARG, "%s: layout is NULL", who);
     dit_sp_layout ref;
-    if (dit_sp_layout_init(L->B, L->S, L->H, L->D, L->U, L->R, &ref) != DIT_OK)
+    if (dit_sp_layout_init_ex(L->B, L->S, L->H, L->D, L->U, L->R, L->flags, &ref) != DIT_OK)
         return fail(DIT_ERR_INVALID_ARG, "%s: layout sizes invalid", who);
-    bool ok = ref.Hp == L->Hp && ref.Hl == L->Hl && ref.S_cap == L->S_cap;
+    bool ok = ref.Hp == L->Hp && ref.Hl == L->Hl && ref.S_cap == L->S_cap && ref.S_pad == L->S_pad;
+    for (int v = 0; ok && v < L->U; ++v)
+        ok = ref.head_len[v] == L->head_len[v] && ref.head_off[v] == L->head_off[v];
     for (int r = 0; ok && r < L->R; ++r)
         ok = ref.ring_len[r] == L->ring_len[r] && ref.ring_off[r] == L->ring_off[r];
     for (int i = 0; ok && i < L->R * L->U; ++i)
@@ -477,7 +483,7 @@ extern "C" dit_status dit_ulysses_pack(const dit_sp_layout* L, dit_a2a_dir dir, 
     }
     a.dst[0] = send;
     a.dst_dt[0] = wire_dt;
-    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S_pad;
     cudaStream_t st = (cudaStream_t)stream;
     if (wire_dt == DIT_E4M3) return fp8_pack(L, dir, nplanes, src, nullptr, 0, src_dt, send, st, who);
     return dir == DIT_SEQ_TO_HEAD ? launch_runs<PACK_S2H>(a, st, who) : launch_runs<PACK_H2S>(a, st, who);
@@ -499,7 +505,7 @@ extern "C" dit_status dit_a2a_sim(const dit_sp_layout* L, dit_a2a_dir dir, int n
     a.np = nplanes;
     a.src[0] = send; a.src_dt[0] = wire_dt;
     a.dst[0] = recv; a.dst_dt[0] = wire_dt;
-    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S_pad;
     if (wire_dt == DIT_E4M3 && (s = record_words(&a, who)) != DIT_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
     return dir == DIT_SEQ_TO_HEAD ? launch_runs<A2A_S2H>(a, st, who) : launch_runs<A2A_H2S>(a, st, who);
@@ -529,7 +535,7 @@ extern "C" dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir
         a.dst_dt[p] = dst_dt[p];
     }
     a.range_flag = d_range_flag;
-    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    a.nruns = (long long)nplanes * L->B * L->U * (dir == DIT_SEQ_TO_HEAD ? L->S_pad : L->S);
     cudaStream_t st = (cudaStream_t)stream;
     if (wire_dt == DIT_E4M3)
         return fp8_unpack(L, dir, nplanes, recv, dst, nullptr, 0, dst_dt, nullptr, nullptr, 0, d_range_flag, st, who);
@@ -573,7 +579,7 @@ extern "C" dit_status dit_a2a_sim_checked(const dit_sp_layout* L, dit_a2a_dir di
     a.np = nplanes;
     a.src[0] = send; a.src_dt[0] = wire_dt;
     a.dst[0] = recv; a.dst_dt[0] = wire_dt;
-    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S_pad;
     a.arrival = d_arrival;
     a.epoch = epoch;
     a.timeout_ns = timeout_ns;
@@ -613,7 +619,7 @@ extern "C" dit_status dit_ulysses_pack_joint(const dit_sp_layout* L, int nplanes
     a.split = has_txt && has_img ? S_txt : 0;
     a.dst[0] = send;
     a.dst_dt[0] = wire_dt;
-    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S_pad;
     if (wire_dt == DIT_E4M3)
         return fp8_pack(L, DIT_SEQ_TO_HEAD, nplanes, a.src, a.src2, a.split, src_dt, send, (cudaStream_t)stream, who);
     return launch_runs<PACK_S2H>(a, (cudaStream_t)stream, who);
@@ -678,7 +684,7 @@ extern "C" dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplane
     a.rope_cos = cos_tab;
     a.rope_sin = sin_tab;
     a.rope_planes = rope_planes;
-    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    a.nruns = (long long)nplanes * L->B * L->U * L->S_pad;
     cudaStream_t st = (cudaStream_t)stream;
     if (wire_dt == DIT_E4M3)
         return fp8_unpack(L, DIT_SEQ_TO_HEAD, nplanes, recv, dst, nullptr, 0, dst_dt, cos_tab, sin_tab, rope_planes,

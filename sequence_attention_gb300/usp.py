@@ -42,12 +42,16 @@ class UspPlan:
                  v_dtype: Optional[torch.dtype] = None,
                  device: str = "cuda", scale: Optional[float] = None,
                  rope: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
-                 fp8_qv: bool = False, fp8_o: bool = False):
+                 fp8_qv: bool = False, fp8_o: bool = False,
+                 pad_heads: bool = True, pad_lcm64: bool = False):
         """rope: optional (cos, sin) float32 [S, D/2] device tables of the
         joint sequence; Q and K are then rotated by the receive preparation.
         fp8_qv / fp8_o: Q and V (one exchange) / the output cross the
-        all-to-all as e4m3 records; K keeps its own 16-bit exchange."""
-        self.L = dit_sp_layout_init(B, S, H, D, U, R)
+        all-to-all as e4m3 records; K keeps its own 16-bit exchange.
+        pad_heads=False: uneven head groups without padding; pad_lcm64: the
+        sequence padded to a multiple of lcm(U*R, 64), padding rows excluded
+        from attention."""
+        self.L = dit_sp_layout_init(B, S, H, D, U, R, pad_heads, pad_lcm64)
         self.B, self.S, self.H, self.D, self.U, self.R = B, S, H, D, U, R
         self.in_dtype = in_dtype
         self.wire_dtype = in_dtype
@@ -93,7 +97,9 @@ class UspPlan:
 
     @property
     def ring_len(self):
-        return self.L.ring_len
+        """Real (non-padding) rows of each ring block: the attention's
+        query and key counts."""
+        return [self.L.real_rows(r) for r in range(self.R)]
 
     def steps(self):
         """Names of the kernels one run() launches, in order."""

@@ -58,6 +58,29 @@ def test_layout_init_matches_oracle(dl, dims):
     assert L.rank_len == list(ref.rank_len) and L.rank_off == list(ref.rank_off)
 
 
+@pytest.mark.parametrize("flags", [(False, False), (True, True), (False, True)])
+@pytest.mark.parametrize("dims", [(1, 4481, 24, 128, 4, 2), (2, 7145, 24, 128, 5, 2), (1, 75600, 40, 128, 8, 4),
+                                  (1, 3, 2, 8, 2, 2), (1, 0, 1, 8, 3, 2), (3, 17, 5, 8, 64, 1)])
+def test_layout_modes_match_oracle(dl, dims, flags):
+    import sequence_attention_gb300 as sa
+    L = sa.dit_sp_layout_init(*dims, pad_heads=flags[0], pad_lcm64=flags[1])
+    ref = olayout.make_layout(*dims, pad_heads=flags[0], pad_lcm64=flags[1])
+    assert (L.Hp, L.Hl, L.S_cap, L.S_pad, L.S) == (ref.Hp, ref.Hl, ref.S_cap, ref.S_pad, ref.S)
+    assert L.head_len == list(ref.head_len) and L.head_off == list(ref.head_off)
+    assert L.ring_len == list(ref.ring_len) and L.ring_off == list(ref.ring_off)
+    assert L.rank_len == list(ref.rank_len) and L.rank_off == list(ref.rank_off)
+    for d, name in ((0, "s2h"), (1, "h2s")):
+        for rank in range(min(dims[4] * dims[5], 9)):
+            got = sa.dit_sp_a2a_counts(L, d, 3 if d == 0 else 1, rank)
+            exp = olayout.a2a_counts(ref, name, 3 if d == 0 else 1, rank)
+            assert [list(x) for x in got] == [list(x) for x in exp]
+
+
+def test_layout_init_rejects_unknown_flags(dl):
+    lay = dl.DitSpLayout()
+    assert dl.lib().dit_sp_layout_init_ex(1, 8, 2, 8, 2, 1, 4, ctypes.byref(lay)) == dl.DIT_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("direction,np_", [(0, 3), (1, 1), (0, 1)])
 def test_a2a_counts_match_oracle(dl, direction, np_):
     import sequence_attention_gb300 as sa
