@@ -100,3 +100,65 @@ def merge(parts: Sequence[Tuple[np.ndarray, np.ndarray]]) -> Tuple[np.ndarray, n
         # weights are per (b, h, i); O is laid out [b, i, h, d]
         o += np.transpose(wr, (0, 2, 1))[..., None] * np.asarray(o_r, dtype=np.float64)
     return o, lse
+
+
+def masked(q: np.ndarray, k: np.ndarray, v: np.ndarray, key_mask: np.ndarray,
+           scale: Optional[float] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Attention where query rows see only the keys their mask allows.
+
+    key_mask: bool [B, Sq, Sk] (True = the key takes part) or [B, Sk] (the
+    same keys for every query).  Source: SGLang Diffusion "Parallelism
+    Overview", Constraints: the masked / tail-padded text path (text tokens
+    padded to a fixed length, the padding excluded as keys); xLLM "DiT
+    Architecture and Capability Matrix": packed data with live/padding
+    boundaries, padding excluded.  A row with no allowed key gives O = 0 and
+    lse = -inf, as an empty chunk does.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, Sq, H, D = q.shape
+    mask = np.asarray(key_mask, dtype=bool)
+    if mask.ndim == 2:
+        mask = np.broadcast_to(mask[:, None, :], (B, Sq, mask.shape[1]))
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = np.zeros((B, Sq, H, v.shape[3]), dtype=np.float64)
+    lse = np.full((B, H, Sq), -np.inf, dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            s = scale * (q[b, :, h, :] @ k[b, :, h, :].T)
+            s = np.where(mask[b], s, -np.inf)
+            m = s.max(axis=1, keepdims=True) if s.shape[1] else np.full((Sq, 1), -np.inf)
+            live = np.isfinite(m[:, 0])
+            msafe = np.where(np.isfinite(m), m, 0.0)
+            e = np.exp(s - msafe)                        # exp(-inf) = 0 for masked keys
+            den = e.sum(axis=1, keepdims=True)
+            with np.errstate(invalid="ignore", divide="ignore"):
+                o[b, :, h, :] = np.where(live[:, None], (e @ v[b, :, h, :]) / den, 0.0)
+                lse[b, h, :] = np.where(live, msafe[:, 0] + np.log(den[:, 0]), -np.inf)
+    return o, lse
+
+
+def varlen(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_q: Sequence[int], cu_k: Sequence[int],
+           scale: Optional[float] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Attention of packed variable-length sequences: q [Tq, H, D], k and v
+    [Tk, H, D]; sequence s has queries [cu_q[s], cu_q[s+1]) and keys
+    [cu_k[s], cu_k[s+1]), and attends only to its own keys.  Returns
+    (O [Tq, H, D], lse [H, Tq]).  Source: SGLang Diffusion "Parallelism
+    Overview", the generic varlen path (several packed segments per row);
+    xLLM, packed TND data with live/padding boundaries.  Query rows outside
+    every sequence are not written (O = 0, lse = -inf here).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    Tq, H, D = q.shape
+    o = np.zeros((Tq, H, np.shape(v)[2]), dtype=np.float64)
+    lse = np.full((H, Tq), -np.inf, dtype=np.float64)
+    for s in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
+        if q1 == q0:
+            continue
+        os_, ls_ = attention(q[None, q0:q1], np.asarray(k)[None, k0:k1], np.asarray(v)[None, k0:k1], scale)
+        o[q0:q1] = os_[0]
+        lse[:, q0:q1] = ls_[0]
+    return o, lse

@@ -174,3 +174,66 @@ def test_merge_rescales_with_the_right_sign():
     o, lse = att.merge([(oa, la), (ob, lb)])
     np.testing.assert_allclose(o, 2.0, atol=1e-15)
     np.testing.assert_allclose(lse, 0.2 + math.log(4.0), atol=1e-15)
+
+
+def test_masked_with_every_key_allowed_is_attention():
+    rng = np.random.default_rng(40)
+    q, k, v = (rng.standard_normal((2, 9, 3, 8)) for _ in range(3))
+    o, l = att.masked(q, k, v, np.ones((2, 9), bool))
+    o2, l2 = att.attention(q, k, v)
+    np.testing.assert_allclose(o, o2, atol=1e-14)
+    np.testing.assert_allclose(l, l2, atol=1e-14)
+
+
+def test_masked_equals_attention_over_the_gathered_keys():
+    # the tail-padded text path: keys [txt_len, S_txt) of each batch are padding
+    rng = np.random.default_rng(41)
+    B, S, H, D, S_txt = 2, 20, 2, 8, 7
+    q, k, v = (rng.standard_normal((B, S, H, D)) for _ in range(3))
+    txt_len = [4, 7]
+    mask = np.ones((B, S), bool)
+    for b in range(B):
+        mask[b, txt_len[b]:S_txt] = False
+    o, l = att.masked(q, k, v, mask)
+    for b in range(B):
+        keep = np.flatnonzero(mask[b])
+        o2, l2 = att.attention(q[b:b + 1], k[b:b + 1, keep], v[b:b + 1, keep])
+        np.testing.assert_allclose(o[b], o2[0], atol=1e-14)
+        np.testing.assert_allclose(l[b], l2[0], atol=1e-14)
+
+
+def test_masked_text_is_the_merge_of_its_two_key_ranges():
+    # the pages fold the masked text portion into the rest with the same merge
+    rng = np.random.default_rng(42)
+    B, S, H, D, S_txt, txt_len = 1, 30, 2, 8, 10, 6
+    q, k, v = (rng.standard_normal((B, S, H, D)) for _ in range(3))
+    mask = np.ones((B, S), bool)
+    mask[:, txt_len:S_txt] = False
+    o, l = att.masked(q, k, v, mask)
+    parts = [att.partial(q, k[:, :S_txt], v[:, :S_txt], txt_len), att.attention(q, k[:, S_txt:], v[:, S_txt:])]
+    o2, l2 = att.merge(parts)
+    np.testing.assert_allclose(o, o2, atol=1e-13)
+    np.testing.assert_allclose(l, l2, atol=1e-13)
+
+
+def test_masked_row_without_keys_is_empty():
+    q = np.ones((1, 2, 1, 4))
+    mask = np.array([[[True, False], [False, False]]])
+    o, l = att.masked(q, q, q, mask)
+    assert np.all(o[0, 1] == 0) and np.isneginf(l[0, 0, 1]) and np.isfinite(l[0, 0, 0])
+
+
+def test_varlen_is_block_diagonal_masked_attention():
+    rng = np.random.default_rng(43)
+    cu_q, cu_k = [0, 3, 3, 10, 16], [0, 5, 9, 9, 20]      # an empty query segment and an empty key one
+    Tq, Tk, H, D = cu_q[-1], cu_k[-1], 2, 8
+    q = rng.standard_normal((Tq, H, D))
+    k, v = rng.standard_normal((Tk, H, D)), rng.standard_normal((Tk, H, D))
+    o, l = att.varlen(q, k, v, cu_q, cu_k)
+    mask = np.zeros((1, Tq, Tk), bool)
+    for s in range(4):
+        mask[0, cu_q[s]:cu_q[s + 1], cu_k[s]:cu_k[s + 1]] = True
+    o2, l2 = att.masked(q[None], k[None], v[None], mask)
+    np.testing.assert_allclose(o, o2[0], atol=1e-14)
+    np.testing.assert_allclose(l, l2[0], atol=1e-14)
+    assert np.all(o[3:10] == 0)                          # the sequence whose keys are empty
