@@ -360,6 +360,28 @@ DIT_API dit_status dit_attn_partial(int B, int H, int D, float scale,
                             dit_lse_view lse, int* d_status, void* stream);
 
 /*
+ * dit_attn_varlen: attention of packed variable-length sequences (SGLang
+ * Diffusion "Parallelism Overview", the generic varlen path with several
+ * packed segments per row; xLLM "DiT Architecture and Capability Matrix",
+ * packed TND data with live/padding boundaries).  Sequence s < nseq has
+ * query rows [cu_q[s], cu_q[s+1]) and key rows [cu_k[s], cu_k[s+1]) and
+ * attends only to its own keys:
+ *   o_i = sum_t softmax_t(scale * <q_i, k_t>) v_t,  lse_i = ln sum_t exp(...)
+ * over its keys t; a sequence with no keys gives o = 0, lse = -inf.  Rows of
+ * q outside every sequence are not written.
+ *   q, o     packed rows [Tq][H][D]: row t at ptr + t*stride_s + h*stride_h
+ *   k, v     packed rows [Tk][H][D]
+ *   lse      [H][Tq] at lse.ptr + h*stride_h + t (may be NULL)
+ *   cu_q, cu_k  host arrays of nseq + 1 non-decreasing row offsets.
+ * Block and batch strides of the views are ignored.  Types, head dims and
+ * alignment as for dit_attn_partial; the library issues one launch per
+ * DIT_MAX_R sequences.
+ */
+DIT_API dit_status dit_attn_varlen(int H, int D, float scale, int nseq, const int* cu_q, const int* cu_k,
+                                   dit_view q, dit_dtype qk_dt, dit_view k, dit_view v, dit_dtype v_dt,
+                                   dit_view o, dit_dtype o_dt, dit_lse_view lse, int* d_status, void* stream);
+
+/*
  * dit_attn_merge_lse: fold n_parts partials of each query block into the
  * exact result (SGLang Diffusion "Parallelism Overview", What happens to the
  * shapes and Constraints: online-softmax merge over ranks holding the same

@@ -34,7 +34,7 @@ __all__ = [
     "dit_sp_layout_init", "dit_sp_a2a_counts", "dit_ulysses_pack", "dit_a2a_sim",
     "dit_ulysses_unpack", "dit_attn_partial", "dit_attn_merge_lse", "dit_attention",
     "dit_cfg_combine", "dit_device_status", "library_path", "dit_sp_signal", "dit_a2a_sim_checked",
-    "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint", "dit_ulysses_unpack_rope",
+    "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint", "dit_ulysses_unpack_rope", "dit_attn_varlen",
 ]
 
 lib()   # load now: fail at import time, not at first call
@@ -212,6 +212,8 @@ def _view(t: torch.Tensor, kind: str) -> DitView:
         v.stride_q, v.stride_kv, v.stride_b, v.stride_s, v.stride_h = st[0], st[1], st[2], st[3], st[4]
     elif kind == "single":
         v.stride_b, v.stride_s, v.stride_h = st[0], st[1], st[2]
+    elif kind == "packed":  # [T, H, D]
+        v.stride_s, v.stride_h = st[0], st[1]
     else:
         raise ValueError(kind)
     return v
@@ -231,6 +233,8 @@ def _lse_view(t: Optional[torch.Tensor], kind: str) -> DitLseView:
         v.stride_q, v.stride_b, v.stride_h = st[0], st[1], st[2]
     elif kind == "single":  # [B, H, S]
         v.stride_b, v.stride_h = st[0], st[1]
+    elif kind == "packed":  # [H, T]
+        v.stride_h = st[0]
     else:
         raise ValueError(kind)
     return v
@@ -278,6 +282,25 @@ def dit_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Te
     check(lib().dit_attention(B, H, D, float(scale), Sq, Sk, _view(q, "single"), _dt(q),
                               _view(k, "single"), _view(v, "single"), _dt(v), _view(o, "single"),
                               _dt(o), _lse_view(lse, "single"), _ptr(status), _stream(stream)))
+
+
+def dit_attn_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                    cu_q: Sequence[int], cu_k: Sequence[int], lse: Optional[torch.Tensor] = None,
+                    scale: Optional[float] = None, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Packed variable-length attention: q, o [Tq, H, D]; k, v [Tk, H, D];
+    sequence s has rows [cu_q[s], cu_q[s+1]) and keys [cu_k[s], cu_k[s+1]);
+    lse [H, Tq] (float32) optional."""
+    _, H, D = q.shape
+    n = len(cu_q) - 1
+    if len(cu_k) != n + 1 or n < 0:
+        raise ValueError("cu_q and cu_k need the same number of sequences")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    cq = (c_int * max(n + 1, 1))(*cu_q)
+    ck = (c_int * max(n + 1, 1))(*cu_k)
+    check(lib().dit_attn_varlen(H, D, float(scale), n, cq, ck, _view(q, "packed"), _dt(q), _view(k, "packed"),
+                                _view(v, "packed"), _dt(v), _view(o, "packed"), _dt(o), _lse_view(lse, "packed"),
+                                _ptr(status), _stream(stream)))
 
 
 def dit_cfg_combine(pred: torch.Tensor, out: torch.Tensor, g: float, stream=None) -> None:

@@ -27,7 +27,7 @@ EXPORTS = (
     "dit_sp_a2a_counts", "dit_ulysses_pack", "dit_a2a_sim", "dit_ulysses_unpack",
     "dit_attn_partial", "dit_attn_merge_lse", "dit_attention", "dit_cfg_combine",
     "dit_sp_signal", "dit_a2a_sim_checked", "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint",
-    "dit_ulysses_unpack_rope",
+    "dit_ulysses_unpack_rope", "dit_attn_varlen",
 )
 
 
@@ -109,6 +109,9 @@ def lib() -> ctypes.CDLL:
     L.dit_attn_partial.argtypes = [c_int, c_int, c_int, c_float, c_int, POINTER(c_int), c_int,
                                    POINTER(c_int), DitView, c_int, DitView, DitView, c_int, DitView,
                                    c_int, DitLseView, c_void_p, c_void_p]
+    L.dit_attn_varlen.restype = c_int
+    L.dit_attn_varlen.argtypes = [c_int, c_int, c_float, c_int, POINTER(c_int), POINTER(c_int), DitView, c_int,
+                                  DitView, DitView, c_int, DitView, c_int, DitLseView, c_void_p, c_void_p]
     L.dit_attn_merge_lse.restype = c_int
     L.dit_attn_merge_lse.argtypes = [c_int, c_int, c_int, c_int, POINTER(c_int), c_int, DitView, c_int,
                                      DitLseView, DitView, c_int, DitLseView, c_void_p]

@@ -90,3 +90,40 @@ extern "C" dit_status dit_attention(int B, int H, int D, float scale, int Sq, in
     a.qk_dt = qk_dt; a.v_dt = v_dt; a.o_dt = o_dt; a.lse = lse; a.status = d_status;
     return validate_and_launch(a, "dit_attention", (cudaStream_t)stream);
 }
+
+extern "C" dit_status dit_attn_varlen(int H, int D, float scale, int nseq, const int* cu_q, const int* cu_k,
+                                      dit_view q, dit_dtype qk_dt, dit_view k, dit_view v, dit_dtype v_dt,
+                                      dit_view o, dit_dtype o_dt, dit_lse_view lse, int* d_status, void* stream) {
+    const char* who = "dit_attn_varlen";
+    if (nseq < 0) return fail(DIT_ERR_INVALID_ARG, "%s: negative sequence count", who);
+    if (nseq == 0) return DIT_OK;
+    if (!cu_q || !cu_k) return fail(DIT_ERR_INVALID_ARG, "%s: NULL offset array", who);
+    if (cu_q[0] < 0 || cu_k[0] < 0) return fail(DIT_ERR_INVALID_ARG, "%s: negative offset", who);
+    for (int s = 0; s < nseq; ++s)
+        if (cu_q[s + 1] < cu_q[s] || cu_k[s + 1] < cu_k[s])
+            return fail(DIT_ERR_INVALID_ARG, "%s: offsets must not decrease", who);
+    // packed rows: no batch or block strides
+    q.stride_q = q.stride_kv = q.stride_b = 0;
+    k.stride_q = k.stride_kv = k.stride_b = 0;
+    v.stride_q = v.stride_kv = v.stride_b = 0;
+    o.stride_q = o.stride_kv = o.stride_b = 0;
+    lse.stride_q = lse.stride_kv = lse.stride_b = 0;
+    // up to DIT_MAX_R sequences per launch, each its own (diagonal) block
+    for (int s0 = 0; s0 < nseq; s0 += DIT_MAX_R) {
+        const int n = nseq - s0 < DIT_MAX_R ? nseq - s0 : DIT_MAX_R;
+        AttnArgs a;
+        memset(&a, 0, sizeof(a));
+        a.B = 1; a.H = H; a.D = D; a.n_q = n; a.n_kv = n; a.scale = scale; a.diag = 1;
+        for (int i = 0; i < n; ++i) {
+            a.q_row0[i] = cu_q[s0 + i];
+            a.kv_row0[i] = cu_k[s0 + i];
+            a.q_len[i] = cu_q[s0 + i + 1] - cu_q[s0 + i];
+            a.kv_len[i] = cu_k[s0 + i + 1] - cu_k[s0 + i];
+        }
+        a.q = q; a.k = k; a.v = v; a.o = o;
+        a.qk_dt = qk_dt; a.v_dt = v_dt; a.o_dt = o_dt; a.lse = lse; a.status = d_status;
+        const dit_status st = validate_and_launch(a, who, (cudaStream_t)stream);
+        if (st != DIT_OK) return st;
+    }
+    return DIT_OK;
+}

@@ -15,6 +15,12 @@ struct AttnArgs {
     dit_dtype qk_dt, v_dt, o_dt;
     dit_lse_view lse;
     int* status;
+    // packed variable-length sequences: block i's rows start at row
+    // q_row0[i] / kv_row0[i] of the views (0 otherwise), and with diag set
+    // query block i attends key block i only (n_q == n_kv)
+    int q_row0[DIT_MAX_R];
+    int kv_row0[DIT_MAX_R];
+    int diag;
 };
 
 dit_status launch_attn_f32(const AttnArgs& a, cudaStream_t st);

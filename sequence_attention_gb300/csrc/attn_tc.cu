@@ -66,7 +66,9 @@ struct TcParams {
     CUtensorMap vmap[DIT_MAX_R];
     int q_len[DIT_MAX_R];
     int kv_len[DIT_MAX_R];
+    int q_row0[DIT_MAX_R];          // first output row of query block r (packed sequences)
     int B, n_q, n_kv;
+    int diag;                       // query block r attends key block r only
     float c;                      // scale * log2(e)
     uint32_t idesc_qk, idesc_pv;
     dit_view o;
@@ -256,8 +258,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int z = blockIdx.z;
     const int b = z % p.B;
-    const int j = (z / p.B) % p.n_kv;
-    const int r = z / (p.B * p.n_kv);
+    const int j = p.diag ? z / p.B : (z / p.B) % p.n_kv;
+    const int r = p.diag ? j : z / (p.B * p.n_kv);
     const int h = blockIdx.y;
     const int qlen = p.q_len[r], kvlen = p.kv_len[j];
     const int row_base = blockIdx.x * (NQT * BM);
@@ -265,10 +267,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     const int ntiles = (kvlen + BN - 1) / BN;
 
     const int eb = dtype_bytes(p.o_dt);
-    char* obase = static_cast<char*>(p.o.ptr) +
-                  (r * p.o.stride_q + j * p.o.stride_kv + b * p.o.stride_b + h * p.o.stride_h) * eb;
+    char* obase = static_cast<char*>(p.o.ptr) + (r * p.o.stride_q + j * p.o.stride_kv + b * p.o.stride_b +
+                                                 h * p.o.stride_h + (long long)p.q_row0[r] * p.o.stride_s) * eb;
     float* lbase = p.lse.ptr ? p.lse.ptr + r * p.lse.stride_q + j * p.lse.stride_kv + b * p.lse.stride_b +
-                                   h * p.lse.stride_h
+                                   h * p.lse.stride_h + p.q_row0[r]
                              : nullptr;
 
     if (ntiles == 0) {   // empty key chunk: O = 0, lse = -inf
@@ -600,14 +602,15 @@ dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
     for (int r = 0; r < a.n_q && s == DIT_OK; ++r) {
         prm->q_len[r] = a.q_len[r];
         if (a.q_len[r] > maxq) maxq = a.q_len[r];
-        const char* base = static_cast<const char*>(a.q.ptr) + r * a.q.stride_q * 2;
+        prm->q_row0[r] = a.q_row0[r];
+        const char* base = static_cast<const char*>(a.q.ptr) + (r * a.q.stride_q + (int64_t)a.q_row0[r] * a.q.stride_s) * 2;
         s = make_map(enc, &prm->qmap[r], base, a.qk_dt, a.D, a.H, a.q_len[r], a.B, a.q.stride_h, a.q.stride_s,
                      a.q.stride_b);
     }
     for (int j = 0; j < a.n_kv && s == DIT_OK; ++j) {
         prm->kv_len[j] = a.kv_len[j];
-        const char* kb = static_cast<const char*>(a.k.ptr) + j * a.k.stride_kv * 2;
-        const char* vb = static_cast<const char*>(a.v.ptr) + j * a.v.stride_kv * 2;
+        const char* kb = static_cast<const char*>(a.k.ptr) + (j * a.k.stride_kv + (int64_t)a.kv_row0[j] * a.k.stride_s) * 2;
+        const char* vb = static_cast<const char*>(a.v.ptr) + (j * a.v.stride_kv + (int64_t)a.kv_row0[j] * a.v.stride_s) * 2;
         s = make_map(enc, &prm->kmap[j], kb, a.qk_dt, a.D, a.H, a.kv_len[j], a.B, a.k.stride_h, a.k.stride_s,
                      a.k.stride_b);
         if (s == DIT_OK)
@@ -615,12 +618,12 @@ dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
                          a.v.stride_b);
     }
     if (s == DIT_OK && maxq > 0) {
-        prm->B = a.B; prm->n_q = a.n_q; prm->n_kv = a.n_kv;
+        prm->B = a.B; prm->n_q = a.n_q; prm->n_kv = a.n_kv; prm->diag = a.diag;
         prm->c = a.scale * 1.4426950408889634f;
         prm->idesc_qk = make_idesc(a.qk_dt == DIT_BF16, false, BN, BM);
         prm->idesc_pv = make_idesc(a.v_dt == DIT_BF16, true, a.D, BM);
         prm->o = a.o; prm->o_dt = a.o_dt; prm->lse = a.lse; prm->status = a.status;
-        dim3 grid((maxq + NQT * BM - 1) / (NQT * BM), a.H, a.n_q * a.n_kv * a.B);
+        dim3 grid((maxq + NQT * BM - 1) / (NQT * BM), a.H, (a.diag ? a.n_q : a.n_q * a.n_kv) * a.B);
         if (grid.y > 65535 || grid.z > 65535) s = fail(DIT_ERR_UNSUPPORTED, "attention: grid too large");
         else if (a.D == 128) s = a.v_dt == DIT_BF16 ? launch_kernel<128, true>(*prm, grid, st) : launch_kernel<128, false>(*prm, grid, st);
         else s = a.v_dt == DIT_BF16 ? launch_kernel<64, true>(*prm, grid, st) : launch_kernel<64, false>(*prm, grid, st);
