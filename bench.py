@@ -528,32 +528,42 @@ def run_sweep(args):
         plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev))
         stream = torch.cuda.current_stream(dev)
         reps = 3 if name == "wan" else 10
-        seg = [[] for _ in range(4)]
+        seg = [[] for _ in range(5)]
         for i in range(reps + 3):
             flush.zero_()
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
             ev[0].record(stream)
             plan.layout_in(q, k, v)
             ev[1].record(stream)
-            plan.attend()
+            plan.partials()
             ev[2].record(stream)
-            plan.layout_out(out)
+            plan.merge()
             ev[3].record(stream)
-            sa.dit_cfg_combine(pred, cfg_out, w.g)
+            plan.layout_out(out)
             ev[4].record(stream)
+            sa.dit_cfg_combine(pred, cfg_out, w.g)
+            ev[5].record(stream)
             torch.cuda.synchronize(dev)
             if i >= 3:
-                for j in range(4):
+                for j in range(5):
                     seg[j].append(ev[j].elapsed_time(ev[j + 1]))
         med = [statistics.median(x) for x in seg]
         fl = w.attn_flops
         tf = fl / (med[1] * 1e-3) / 1e12
+        tfm = fl / ((med[1] + med[2]) * 1e-3) / 1e12
+        L = plan.L
+        # merge bytes: R partials (fp32 O and LSE) of every ring block read, the output written
+        rows = w.B * w.S * w.H
+        merge_bytes = rows * (w.R * (w.D * 4 + 4) + w.D * plan.o_h.element_size()) if w.R > 1 else 0
         res = {"workload": name, "U": U, "R": w.R, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "dtype": w.dtype,
                "step_ms": round(sum(med), 4), "layout_in_ms": round(med[0], 4),
                "attention_ms": round(med[1], 4), "attention_TFLOPs": round(tf, 1),
                "attention_frac_of_measured_peak": round(tf / peaks["bf16_tflops"], 4) if w.dtype != "f32" else None,
-               "layout_out_ms": round(med[2], 4), "cfg_ms": round(med[3], 4),
-               "attention_includes_merge": w.R > 1, "status": int(plan.status.item()),
+               "merge_ms": round(med[2], 4),
+               "merge_GBs": round(merge_bytes / (med[2] * 1e-3) / 1e9, 1) if w.R > 1 else None,
+               "attention_plus_merge_TFLOPs": round(tfm, 1),
+               "layout_out_ms": round(med[3], 4), "cfg_ms": round(med[4], 4),
+               "heads_padded": L.Hp - w.H, "status": int(plan.status.item()),
                "range_flag": int(plan.range_flag.item())}
         print(json.dumps(res), flush=True)
         del q, k, v, pred, out, cfg_out, plan

@@ -149,7 +149,9 @@ class UspPlan:
             dit_ulysses_pack_joint(self.L, txt, img, self.send, stream)
         self._receive(stream)
 
-    def attend(self, stream=None):
+    def partials(self, stream=None):
+        """Every (ring block r, ring block j) partial in one launch; with
+        R = 1 the single partial is the output itself."""
         rl = self.ring_len
         qv, kv, vv = self.heads(self.q_h), self.heads(self.k_h), self.heads(self.v_h)
         if self.R == 1:
@@ -159,8 +161,16 @@ class UspPlan:
             dit_attn_partial(qv, kv, vv, self.heads(self.parts),
                              self.lse_parts[:, :, :, : self.H, :], rl, rl, self.scale,
                              self.status, stream)
+
+    def merge(self, stream=None):
+        """The ring's log-sum-exp merge of the R partials (nothing when R = 1)."""
+        if self.R > 1:
             dit_attn_merge_lse(self.heads(self.parts), self.lse_parts[:, :, :, : self.H, :],
-                               self.heads(self.o_h), None, rl, stream)
+                               self.heads(self.o_h), None, self.ring_len, stream)
+
+    def attend(self, stream=None):
+        self.partials(stream)
+        self.merge(stream)
 
     def layout_out(self, out, stream=None):
         L = self.L
