@@ -188,3 +188,54 @@ def test_status_strings(dl):
     assert L.dit_status_string(0) == b"DIT_OK"
     assert L.dit_status_string(4) == b"DIT_ERR_TIMEOUT"
     assert L.dit_status_string(99) == b"DIT_ERR_UNKNOWN"
+
+
+def test_new_entry_points_validate_before_any_launch(dl):
+    """Argument errors of the receive-preparation, paired-stream, e4m3 and
+    varlen calls are reported before anything touches the CUDA runtime."""
+    L = dl.lib()
+    lay = dl.DitSpLayout()
+    assert L.dit_sp_layout_init(1, 64, 4, 64, 2, 1, ctypes.byref(lay)) == 0
+    p = (ctypes.c_void_p * 3)(1 << 20, 2 << 20, 3 << 20)
+    dts = (ctypes.c_int * 3)(dl.DIT_BF16, dl.DIT_BF16, dl.DIT_F16)
+    buf = ctypes.c_void_p(4 << 20)
+    tab = ctypes.c_void_p(5 << 20)
+    # RoPE on a plane the call does not have
+    assert L.dit_ulysses_unpack_rope(ctypes.byref(lay), 1, buf, dl.DIT_BF16, p, dts, tab, tab, 0b10, None,
+                                     None) == dl.DIT_ERR_INVALID_ARG
+    # RoPE without tables
+    assert L.dit_ulysses_unpack_rope(ctypes.byref(lay), 2, buf, dl.DIT_BF16, p, dts, None, None, 0b1, None,
+                                     None) == dl.DIT_ERR_INVALID_ARG
+    # more text rows than the sequence has
+    assert L.dit_ulysses_pack_joint(ctypes.byref(lay), 3, p, p, 65, dl.DIT_BF16, buf, dl.DIT_BF16,
+                                    None) == dl.DIT_ERR_INVALID_ARG
+    # image stream missing while S_txt < S
+    assert L.dit_ulysses_pack_joint(ctypes.byref(lay), 3, p, None, 10, dl.DIT_BF16, buf, dl.DIT_BF16,
+                                    None) == dl.DIT_ERR_INVALID_ARG
+    # e4m3 is a wire type only, and its head dim must be a power of two in [16, 256]
+    assert L.dit_ulysses_pack(ctypes.byref(lay), 0, 3, p, dl.DIT_E4M3, buf, dl.DIT_BF16,
+                              None) == dl.DIT_ERR_INVALID_ARG
+    lay24 = dl.DitSpLayout()
+    assert L.dit_sp_layout_init(1, 64, 4, 24, 2, 1, ctypes.byref(lay24)) == 0
+    assert L.dit_ulysses_pack(ctypes.byref(lay24), 0, 3, p, dl.DIT_BF16, buf, dl.DIT_E4M3,
+                              None) == dl.DIT_ERR_UNSUPPORTED
+    assert L.dit_a2a_sim(ctypes.byref(lay24), 0, 3, buf, ctypes.c_void_p(6 << 20), dl.DIT_E4M3,
+                         None) == dl.DIT_ERR_UNSUPPORTED
+    # varlen: offsets must not decrease
+    v = dl.DitView()
+    v.ptr = 7 << 20
+    v.stride_s, v.stride_h = 128, 64
+    cu_q = (ctypes.c_int * 3)(0, 5, 4)
+    cu_k = (ctypes.c_int * 3)(0, 5, 10)
+    assert L.dit_attn_varlen(2, 64, 0.125, 2, cu_q, cu_k, v, dl.DIT_BF16, v, v, dl.DIT_F16, v, dl.DIT_BF16,
+                             dl.DitLseView(), None, None) == dl.DIT_ERR_INVALID_ARG
+    assert L.dit_attn_varlen(2, 64, 0.125, 0, None, None, v, dl.DIT_BF16, v, v, dl.DIT_F16, v, dl.DIT_BF16,
+                             dl.DitLseView(), None, None) == dl.DIT_OK          # nothing to do
+
+
+def test_layout_with_lcm_padding_changes_wire_sizes(dl):
+    import sequence_attention_gb300 as sa
+    L = sa.dit_sp_layout_init(1, 4481, 24, 128, 4, 2, pad_lcm64=True)
+    assert L.S_pad == 4544 and L.wire_elems(3) == 3 * 4544 * 24 * 128
+    assert L.wire_bytes_e4m3(2) == 2 * 4544 * 24 * 144
+    assert [L.real_rows(r) for r in range(2)] == [2272, 2209]
