@@ -447,15 +447,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 for (int e = 0; e < BN; ++e)
                     if (e >= valid) x[e] = 0xff800000u;
             }
-            // row max: 8 independent chains of three-input max
+            // row max: 8 independent chains of three-input max over columns
+            // 8 .. BN-9, then the last 8 columns with a two-input max
+            static_assert(BN % 16 == 0, "the max chains take 16 columns per step");
             float m8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(x[e]);
 #pragma unroll
-            for (int e = 8; e < BN; e += 16)
+            for (int e = 8; e + 16 <= BN; e += 16)
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     m8[j] = max3(m8[j], __uint_as_float(x[e + j]), __uint_as_float(x[e + 8 + j]));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m8[j] = fmaxf(m8[j], __uint_as_float(x[BN - 8 + j]));
             const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             const float mxs = mx * c;
             float alpha = 1.f;

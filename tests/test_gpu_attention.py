@@ -166,3 +166,28 @@ def test_merge_kernel_against_oracle_merge():
         fin = np.isfinite(l_ref)
         assert np.array_equal(np.isneginf(got_l), np.isneginf(l_ref))
         assert max_abs(got_l[fin], l_ref[fin]) <= 1e-5
+
+
+@pytest.mark.parametrize("key", [125, 127, 248, 300])
+def test_dominant_key_in_the_last_columns_of_a_tile(key):
+    """The row max must see every column of a key tile: one key whose score
+    exceeds the rest by ~35 (log2 ~51) sits in the last eight columns of its
+    128-key tile; a missed max would overflow P in f16."""
+    import sequence_attention_gb300 as sa
+    B, S, H, D = 1, 384, 2, 128
+    q = synth.normal((B, S, H, D), 90, 0.5, "f32")
+    k = synth.normal((B, S, H, D), 91, 0.5, "f32")
+    v = synth.normal((B, S, H, D), 92, 1.0, "f32")
+    q[..., 0] = 20.0
+    k[:, key, :, :] = 0.0
+    k[:, key, :, 0] = 20.0
+    q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    v = v.to(torch.float16)
+    o = torch.empty((B, S, H, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    sa.dit_attention(q.cuda(), k.cuda(), v.cuda(), o, lse)
+    torch.cuda.synchronize()
+    ref, lref = oatt.attention(f64(q), f64(k), f64(v))
+    assert np.all(np.isfinite(f64(o)))
+    assert max_abs(f64(o), ref) <= 2e-2
+    assert np.max(np.abs(lse.cpu().double().numpy() - lref)) <= 1e-3
