@@ -107,6 +107,15 @@ __device__ __forceinline__ void store8(void* p, dit_dtype t, const Vec8& v) {
     }
 }
 
+// True when a finite x becomes infinite on rounding to nearest even into the
+// 16-bit type t: |x| at or above the midpoint between t's largest finite
+// value and the next power of two (65520 for f16, (2 - 2^-8) * 2^127 for
+// bf16), where the tie goes to the even neighbour, infinity.
+__device__ __forceinline__ bool overflows16(float x, dit_dtype t) {
+    const float lim = t == DIT_F16 ? 65520.f : __uint_as_float(0x7F7F8000u);
+    return fabsf(x) >= lim && !isinf(x);
+}
+
 __device__ __forceinline__ void store8_zero(void* p, dit_dtype t) {
     uint4 z = make_uint4(0, 0, 0, 0);
     uint4* q = reinterpret_cast<uint4*>(p);

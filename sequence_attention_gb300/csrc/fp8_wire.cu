@@ -305,10 +305,8 @@ __global__ void __launch_bounds__(kThreads, 3) fp8_unpack_kernel(const __grid_co
                     uint4 o = make_uint4(pack2(y.f[0], y.f[1], t), pack2(y.f[2], y.f[3], t),
                                          pack2(y.f[4], y.f[5], t), pack2(y.f[6], y.f[7], t));
                     if (check) {
-                        Vec8 back;
-                        load8(&o, t, back);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) overflow |= isinf(back.f[e]) && !isinf(y.f[e]);
+                        for (int e = 0; e < 8; ++e) overflow |= overflows16(y.f[e], t);
                     }
                     reinterpret_cast<uint4*>(dst)[v] = o;
                 }

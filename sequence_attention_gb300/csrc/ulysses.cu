@@ -180,10 +180,8 @@ __device__ __forceinline__ void convert8(const uint4 (&in)[SB / 2], dit_dtype sd
         out[0] = make_uint4(pack2(v.f[0], v.f[1], ddt), pack2(v.f[2], v.f[3], ddt),
                             pack2(v.f[4], v.f[5], ddt), pack2(v.f[6], v.f[7], ddt));
         if (check) {
-            Vec8 back;
-            load8(&out[0], ddt, back);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) overflow |= isinf(back.f[e]) && !isinf(v.f[e]);
+            for (int e = 0; e < 8; ++e) overflow |= overflows16(v.f[e], ddt);
         }
     }
 }
@@ -219,10 +217,8 @@ __device__ __forceinline__ void rope8(const uint4 (&in)[SB / 2], dit_dtype sdt, 
         out[0] = make_uint4(pack2(y.f[0], y.f[1], ddt), pack2(y.f[2], y.f[3], ddt),
                             pack2(y.f[4], y.f[5], ddt), pack2(y.f[6], y.f[7], ddt));
         if (check) {
-            Vec8 back;
-            load8(&out[0], ddt, back);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) overflow |= isinf(back.f[e]) && !isinf(y.f[e]);
+            for (int e = 0; e < 8; ++e) overflow |= overflows16(y.f[e], ddt);
         }
     }
 }

@@ -146,6 +146,36 @@ def test_range_flag_on_f16_overflow():
     assert int(flag.item()) == 5        # DIT_ERR_RANGE
 
 
+@pytest.mark.parametrize("value,dst,flagged", [
+    (65519.99609375, "f16", False),   # the largest float32 below the f16 midpoint: rounds to 65504
+    (65520.0, "f16", True),           # the midpoint: the tie goes to the even neighbour, infinity
+    (-65520.0, "f16", True),
+    (float("inf"), "f16", False),     # already infinite: not a range error
+    (float("nan"), "f16", False),
+    (3.3961775e38, "bf16", True),     # (2 - 2^-8) * 2^127, the bf16 midpoint
+    (3.3961773e38, "bf16", False),    # the float32 just below it
+])
+def test_range_flag_threshold(value, dst, flagged):
+    """The range flag is raised exactly when round-to-nearest-even makes a
+    finite value infinite (float32 wire, 16-bit destination)."""
+    import sequence_attention_gb300 as sa
+    L = sa.dit_sp_layout_init(1, 8, 2, 8, 2, 1)
+    x = torch.ones((1, 8, 2, 8), dtype=torch.float32, device="cuda")
+    x[0, 5, 1, 3] = value
+    send = torch.empty(L.wire_elems(1), dtype=torch.float32, device="cuda")
+    recv = torch.empty_like(send)
+    out = [torch.empty(L.head_shape(), dtype=synth.torch_dtype(dst), device="cuda")]
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sa.dit_ulysses_pack(L, sa.DIT_SEQ_TO_HEAD, [x], send)
+    sa.dit_a2a_sim(L, sa.DIT_SEQ_TO_HEAD, 1, send, recv)
+    sa.dit_ulysses_unpack(L, sa.DIT_SEQ_TO_HEAD, recv, out, flag)
+    torch.cuda.synchronize()
+    assert (int(flag.item()) == 5) == flagged
+    got = out[0][0, 0, 5, 1, 3].float().item()
+    ref = torch.tensor([value], dtype=torch.float32).to(synth.torch_dtype(dst)).float().item()
+    assert (got == ref) or (got != got and ref != ref)
+
+
 @pytest.mark.parametrize("name,U", [("flux1024", 4), ("flux1008", 4), ("qwen1328", 5), ("wan", 8)])
 def test_full_size_layout(name, U):
     """At the workloads' full sizes: S2H gives rank (r, v) exactly its slice of
