@@ -192,6 +192,58 @@ def cpu_oracle_rate(w, budget_s: float, seed: int = 0):
     return flops / dt / 1e12, dt, done, blas_threads()
 
 
+def cpu_oracle_kernels(budget_s: float = 30.0):
+    """The oracle's bandwidth steps timed on the host on the FLUX-like
+    workload (U=4; the merge on FLUX-1008's R=2 partials): GB/s of the same
+    algorithmic bytes the GPU lines count.  Stops once the budget is spent."""
+    import numpy as np
+    import synth
+    from oracle import attention as oatt
+    from oracle import cfg as ocfg
+    from oracle import fp8 as ofp8
+    from oracle import layout as olayout
+    from oracle import rope as orope
+    from oracle import ulysses as ou
+    w = synth.WORKLOADS["flux1024"]
+    L = olayout.make_layout(w.B, w.S, w.H, w.D, 4, 1)
+    planes = [synth.as_bits(t) for t in w.qkv()]
+    eb = 2
+    plane_bytes = w.B * w.S * w.H * w.D * eb
+    res = {}
+    t_all = time.perf_counter()
+
+    def timed(name, nbytes, fn):
+        if time.perf_counter() - t_all > budget_s:
+            return None
+        t0 = time.perf_counter()
+        out = fn()
+        dt = time.perf_counter() - t0
+        res[name + "_GBs"] = round(nbytes / dt / 1e9, 3)
+        return out
+
+    send = timed("s2h_pack", 6 * plane_bytes, lambda: ou.s2h_pack(L, planes, "bf16", "bf16"))
+    recv = None if send is None else timed("a2a", 6 * plane_bytes, lambda: ou.a2a(L, "s2h", 3, send))
+    if recv is not None:
+        timed("s2h_unpack", 6 * plane_bytes, lambda: ou.s2h_unpack(L, recv, "bf16", ("bf16", "bf16", "f16")))
+    w8 = synth.WORKLOADS["flux1008"]
+    L8 = olayout.make_layout(w8.B, w8.S, w8.H, w8.D, 4, w8.R)
+    Sr = L8.ring_len[0]
+    rng = np.random.default_rng(0)
+    parts = [(rng.standard_normal((1, Sr, w8.H, w8.D)), rng.standard_normal((1, w8.H, Sr))) for _ in range(2)]
+    timed("merge", Sr * w8.H * (2 * (w8.D * 4 + 4) + w8.D * 2), lambda: oatt.merge(parts))
+    if recv is not None:
+        cos, sin = (t.double().numpy() for t in synth.rope_tables_joint(w.S_txt, w.S, w.D))
+        timed("receive_prep_rope", 6 * plane_bytes + 4 * w.S * w.D,
+              lambda: orope.receive_prep(L, recv, "bf16", ["bf16", "bf16", "f16"], cos, sin, 0b011))
+    pred = synth.as_bits(w.cfg_pair())
+    n = pred.size // 2
+    timed("cfg", 3 * n * eb, lambda: ocfg.cfg_combine_bits(pred, "bf16", w.g, "bf16"))
+    timed("e4m3_pack_qv", 2 * plane_bytes + 2 * w.B * w.S * L.Hp * (w.D + 16),
+          lambda: ofp8.s2h_pack(L, [planes[0], planes[2]], "bf16"))
+    res["seconds"] = round(time.perf_counter() - t_all, 2)
+    return res
+
+
 def blas_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -340,6 +392,8 @@ def run_ours(args):
                                "sample": f"fp64 numpy oracle attention of {rows} random query rows x "
                                          f"{w.H} heads x B={w.B} against all {w.S} keys "
                                          f"({secs:.1f} s on host cores)"}
+        if not args.no_extra:
+            res["cpu_baseline"]["bandwidth_steps"] = cpu_oracle_kernels()
     if rank == 0:
         print(json.dumps(res), flush=True)
     if ws > 1:
