@@ -4,19 +4,18 @@
 // "Parallelism Overview", The Ulysses transport: an all-to-all is a
 // permutation, so a copy in one memory is bit-identical to any transport).
 //
-// Every buffer in the exchange is a sequence of "runs": Hl*D contiguous
-// elements = the Hl heads of one rank's head group for one (plane, batch,
+// Every buffer in the exchange is a sequence of "runs": the head_len[v]*D
+// contiguous elements of one rank's head group v for one (plane, batch,
 // row).  A run is contiguous on both sides of every step, so each kernel
-// moves whole runs with 16-byte vectors: one warp per run, lanes over
-// 8-element chunks.  Two wire orders exist:
-//   A (sequence side): rank (r,u)'s buffer = for v: [planes][B][L_u] runs
-//      index  np*B*U*off_u + v*np*B*L_u + (p*B+b)*L_u + i
-//   B (head side):     rank (r,v)'s buffer = for u: [planes][B][L_u] runs
-//      index  np*B*U*off_r + v*np*B*S_r + np*B*(off_u-off_r) + (p*B+b)*L_u + i
+// moves whole runs with 16-byte vectors: a warp takes a few runs, lanes over
+// 8-element chunks.  The wire orders A (sequence side) and B (head side) and
+// the offsets of a run in them are written out in sp_index.cuh.
 // Seq-to-head: pack writes A, the exchange copies A->B, unpack reads B.
 // Head-to-seq: pack writes B, the exchange copies B->A, unpack reads A.
 // Each kernel walks the runs in its destination's order (A, B, head-layout
 // or sequence order), so its writes are sequential and its reads gather.
+// Rows of the padded sequence at or past S (lcm(SP, 64) padding) travel as
+// zeros and are never read from or written to the sequence-layout tensors.
 //
 // Two additions of the receive preparation and of the FLUX double-stream
 // blocks (edge-dit.cpp "Parallel execution"):
