@@ -153,3 +153,37 @@ def test_usp_in_every_layout(mode, B, S, H, U, R):
     torch.cuda.synchronize()
     ref, _ = oatt.attention(f64(q), f64(k), f64(v))
     assert_bf16_close(f64(out), ref, f"USP {mode}")
+
+
+@pytest.mark.parametrize("name,U,mode", [("qwen1328", 5, (False, False)), ("wan", 8, (True, True)),
+                                         ("flux1008", 4, (False, True)), ("qwen1328", 5, (False, True))])
+def test_full_size_layout_modes(name, U, mode):
+    """At the workloads' full sizes in the alternate layouts: S2H gives every
+    rank exactly its rows and heads of the global tensors (padding rows and
+    padded heads zero), and H2S after S2H is the identity, bit for bit."""
+    import sequence_attention_gb300 as sa
+    w = synth.WORKLOADS[name]
+    L = sa.dit_sp_layout_init(w.B, w.S, w.H, w.D, U, w.R, pad_heads=mode[0], pad_lcm64=mode[1])
+    q, k, v = w.qkv("cuda")
+    send = torch.empty(L.wire_elems(3), dtype=torch.bfloat16, device="cuda")
+    recv = torch.empty_like(send)
+    heads = [torch.empty(L.head_shape(), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    sa.dit_ulysses_pack(L, sa.DIT_SEQ_TO_HEAD, [q, k, v], send)
+    sa.dit_a2a_sim(L, sa.DIT_SEQ_TO_HEAD, 3, send, recv)
+    sa.dit_ulysses_unpack(L, sa.DIT_SEQ_TO_HEAD, recv, heads)
+    del send, recv
+    for p, x in enumerate((q, k, v)):
+        for r in range(L.R):
+            m = L.real_rows(r)
+            got = heads[p][r, :, :m, : w.H]
+            assert torch.equal(got.view(torch.int16), x[:, L.ring_off[r]:L.ring_off[r] + m].view(torch.int16))
+            assert not heads[p][r, :, m:L.ring_len[r]].any()            # padding rows are zero
+        assert not heads[p][..., w.H:, :].any()                          # padded heads are zero
+    out = torch.empty_like(q)
+    s1 = torch.empty(L.wire_elems(1), dtype=torch.bfloat16, device="cuda")
+    r1 = torch.empty_like(s1)
+    sa.dit_ulysses_pack(L, sa.DIT_HEAD_TO_SEQ, [heads[1]], s1)
+    sa.dit_a2a_sim(L, sa.DIT_HEAD_TO_SEQ, 1, s1, r1)
+    sa.dit_ulysses_unpack(L, sa.DIT_HEAD_TO_SEQ, r1, [out])
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), k.view(torch.int16))
