@@ -346,6 +346,22 @@ def run_ours(args):
     achieved = flops / (attn_ms * 1e-3) / 1e12
     traffic = traffic_per_launch(ATTN_SRC, TRAFFIC_NOTE)
 
+    # the same step replayed from a CUDA graph (one launch of the whole step;
+    # L2 flushed before each replay, median of 20)
+    graph = plan.capture(q, k, v, out, extra=lambda: sa.dit_cfg_combine(pred, cfg_out, w.g))
+    gts = []
+    for i in range(25):
+        flush.zero_()
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record(stream)
+        graph.replay()
+        gb.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= 5:
+            gts.append(ga.elapsed_time(gb))
+    graph_ms = statistics.median(gts)
+    del graph
+
     # end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args)
     extra = {} if args.no_extra else {**bandwidth_at_scale(dev, flush, peaks),
@@ -379,6 +395,8 @@ def run_ours(args):
             "cfg_ms": round(statistics.mean(seg[3]), 4),
             "cfg_GBs": round(cfg_bytes / (statistics.mean(seg[3]) * 1e-3) / 1e9, 1),
             "hbm_peak_GBs": peaks.get("hbm_gbs"),
+            "step_graph_ms": round(graph_ms, 4),
+            "step_graph_TFLOPs": round(flops / (graph_ms * 1e-3) / 1e12, 1),
             **extra,
         },
         "e2e": e2e,

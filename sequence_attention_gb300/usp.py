@@ -190,6 +190,23 @@ class UspPlan:
         self.attend(stream)
         self.layout_out_joint(out_txt, out_img, stream)
 
+    def capture(self, q, k, v, out, extra=None):
+        """A CUDA graph of run(q, k, v, out) (and of extra(), a callable that
+        enqueues more calls, e.g. the CFG combine) for these tensors: replay()
+        launches the whole step at once.  Every call of the step is a
+        stream-ordered kernel launch and nothing is allocated, so the replay
+        gives the same bits as run()."""
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=self.q_h.device)
+        s.wait_stream(torch.cuda.current_stream(self.q_h.device))
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.run(q, k, v, out)
+                if extra is not None:
+                    extra()
+        torch.cuda.current_stream(self.q_h.device).wait_stream(s)
+        return g
+
     def run(self, q, k, v, out, stream=None):
         """q, k, v: [B, S, H, D] seq-sharded inputs; out: [B, S, H, D]."""
         self.layout_in(q, k, v, stream)
