@@ -150,6 +150,95 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
     pdl_trigger();
 }
 
+// Merge, unit-per-lane form: a "unit" is one (row i, head h) of block (r, b).
+// Lane L of a warp computes the log-sum-exp and the NP weights of unit L of
+// the warp's 32 (one set of exponentials per unit, not per output), then the
+// warp streams the units' D outputs, CPU = D/8 lanes per unit, taking each
+// unit's weights from its lane by shuffle.  The partial loads of a step are
+// issued before any arithmetic on them.  Units run i-fastest within a head,
+// so the lanes' LSE loads are contiguous.
+template <int NP>
+__global__ void __launch_bounds__(256) merge_units_kernel(const __grid_constant__ MergeArgs a, int cpu_log2) {
+    const int r = blockIdx.y / a.B, b = blockIdx.y % a.B;
+    const int ql = a.q_len[r];
+    const int units = ql * a.H;               // fits in 32 bits (checked on the host)
+    const int lane = threadIdx.x & 31;
+    const int u0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
+    pdl_wait();
+    if (u0 >= units) {
+        pdl_trigger();
+        return;
+    }
+    // this lane's unit: weights and log-sum-exp
+    float w[NP];
+    float lse = -INFINITY;
+    {
+        const int u = u0 + lane;
+        float lj[NP];
+        float M = -INFINITY;
+        if (u < units) {
+            const int h = u / ql, i = u - h * ql;
+            const float* lp = a.lse_parts.ptr + r * a.lse_parts.stride_q + b * a.lse_parts.stride_b +
+                              h * a.lse_parts.stride_h + i;
+#pragma unroll
+            for (int j = 0; j < NP; ++j) lj[j] = lp[j * a.lse_parts.stride_kv];
+#pragma unroll
+            for (int j = 0; j < NP; ++j) M = fmaxf(M, lj[j]);
+        }
+        if (M != -INFINITY) {
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < NP; ++j) sum += expf(lj[j] - M);
+            lse = M + logf(sum);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) w[j] = expf(lj[j] - lse);
+        } else {
+#pragma unroll
+            for (int j = 0; j < NP; ++j) w[j] = 0.f;
+        }
+        if (u < units && a.lse_out.ptr) {
+            const int h = u / ql, i = u - h * ql;
+            a.lse_out.ptr[r * a.lse_out.stride_q + b * a.lse_out.stride_b + h * a.lse_out.stride_h + i] = lse;
+        }
+    }
+    const int cpu = 1 << cpu_log2;            // lanes per unit (D / 8)
+    const int upi = 32 >> cpu_log2;           // units per step
+    const int c = lane & (cpu - 1);
+    const int eb = dtype_bytes(a.parts_dt), ob = dtype_bytes(a.out_dt);
+    const char* pp = static_cast<const char*>(a.parts.ptr);
+    char* op = static_cast<char*>(a.out.ptr);
+    for (int k0 = 0; k0 < 32; k0 += upi) {
+        const int k = k0 + (lane >> cpu_log2);  // unit of this lane in this step
+        const int u = u0 + k;
+        float wk[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) wk[j] = __shfl_sync(0xffffffffu, w[j], k);
+        if (u >= units) continue;
+        const int h = u / ql, i = u - h * ql;
+        const long long base = r * a.parts.stride_q + b * a.parts.stride_b + (long long)i * a.parts.stride_s +
+                               h * a.parts.stride_h + c * 8;
+        Vec8 o[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) load8(pp + (base + j * a.parts.stride_kv) * eb, a.parts_dt, o[j]);
+        Vec8 acc;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc.f[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NP; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc.f[e] = fmaf(wk[j], o[j].f[e], acc.f[e]);
+        const long long ob_off = r * a.out.stride_q + b * a.out.stride_b + (long long)i * a.out.stride_s +
+                                 h * a.out.stride_h + c * 8;
+        store8(op + ob_off * ob, a.out_dt, acc);
+    }
+    pdl_trigger();
+}
+
+template <int NP>
+cudaError_t launch_merge_units(const MergeArgs& a, dim3 grid, int cpu_log2, cudaStream_t st) {
+    return launch_pdl(merge_units_kernel<NP>, grid, dim3(256), 0, st, a, cpu_log2);
+}
+
 }  // namespace
 }  // namespace ditsp
 
@@ -227,11 +316,33 @@ extern "C" dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int
     if (maxq == 0) return DIT_OK;
     a.parts = parts; a.parts_dt = parts_dt; a.lse_parts = lse_parts;
     a.out = out; a.out_dt = out_dt; a.lse_out = lse_out;
-    const long long work = (long long)maxq * H * (D / 8);
-    const long long bx = (work + 255) / 256;     // one thread per 8 outputs
-    dim3 grid((unsigned)bx, (unsigned)(n_q * B));
-    if (grid.y > 65535) return fail(DIT_ERR_UNSUPPORTED, "%s: n_q * B too large", who);
-    cudaError_t e = launch_pdl(merge_kernel, grid, dim3(256), 0, (cudaStream_t)stream, a);
+    if ((unsigned)(n_q * B) > 65535u) return fail(DIT_ERR_UNSUPPORTED, "%s: n_q * B too large", who);
+    cudaError_t e;
+    const int chunks = D / 8;
+    const bool pow2 = chunks <= 32 && (chunks & (chunks - 1)) == 0;
+    if (pow2 && (long long)maxq * H < (1LL << 31)) {
+        // unit-per-lane form: 256 units (rows x heads) per block of 8 warps
+        int lg = 0;
+        while ((1 << lg) < chunks) ++lg;
+        const long long units = (long long)maxq * H;
+        dim3 grid((unsigned)((units + 255) / 256), (unsigned)(n_q * B));
+        const cudaStream_t st = (cudaStream_t)stream;
+        switch (n_parts) {
+            case 1: e = launch_merge_units<1>(a, grid, lg, st); break;
+            case 2: e = launch_merge_units<2>(a, grid, lg, st); break;
+            case 3: e = launch_merge_units<3>(a, grid, lg, st); break;
+            case 4: e = launch_merge_units<4>(a, grid, lg, st); break;
+            case 5: e = launch_merge_units<5>(a, grid, lg, st); break;
+            case 6: e = launch_merge_units<6>(a, grid, lg, st); break;
+            case 7: e = launch_merge_units<7>(a, grid, lg, st); break;
+            default: e = launch_merge_units<8>(a, grid, lg, st); break;
+        }
+    } else {
+        const long long work = (long long)maxq * H * (D / 8);
+        const long long bx = (work + 255) / 256;     // one thread per 8 outputs
+        dim3 grid((unsigned)bx, (unsigned)(n_q * B));
+        e = launch_pdl(merge_kernel, grid, dim3(256), 0, (cudaStream_t)stream, a);
+    }
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     return check_launch(who);
 }
