@@ -302,9 +302,9 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] or 0) \
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
 
     def timed():
         barrier()
@@ -346,21 +346,25 @@ def run_ours(args):
     achieved = flops / (attn_ms * 1e-3) / 1e12
     traffic = traffic_per_launch(ATTN_SRC, TRAFFIC_NOTE)
 
-    # the same step replayed from a CUDA graph (one launch of the whole step;
-    # L2 flushed before each replay, median of 20)
-    graph = plan.capture(q, k, v, out, extra=lambda: sa.dit_cfg_combine(pred, cfg_out, w.g))
-    gts = []
-    for i in range(25):
-        flush.zero_()
-        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ga.record(stream)
-        graph.replay()
-        gb.record(stream)
-        torch.cuda.synchronize(dev)
-        if i >= 5:
-            gts.append(ga.elapsed_time(gb))
-    graph_ms = statistics.median(gts)
-    del graph
+    # one step alone, launched call by call and replayed from its own CUDA
+    # graph (L2 flushed before each, median of 20): the cost of the launches
+    one = plan.capture(q, k, v, out, extra=lambda: sa.dit_cfg_combine(pred, cfg_out, w.g))
+
+    def one_step(fn):
+        ts = []
+        for i in range(25):
+            flush.zero_()
+            ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ga.record(stream)
+            fn()
+            gb.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 5:
+                ts.append(ga.elapsed_time(gb))
+        return statistics.median(ts)
+    graph_ms = one_step(one.replay)
+    eager_ms = one_step(step)
+    del one
 
     # end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args)
@@ -396,7 +400,7 @@ def run_ours(args):
             "cfg_GBs": round(cfg_bytes / (statistics.mean(seg[3]) * 1e-3) / 1e9, 1),
             "hbm_peak_GBs": peaks.get("hbm_gbs"),
             "step_graph_ms": round(graph_ms, 4),
-            "step_graph_TFLOPs": round(flops / (graph_ms * 1e-3) / 1e12, 1),
+            "step_eager_ms": round(eager_ms, 4),
             **extra,
         },
         "e2e": e2e,
