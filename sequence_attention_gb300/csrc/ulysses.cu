@@ -223,8 +223,8 @@ __device__ __forceinline__ void rope8(const uint4 (&in)[SB / 2], dit_dtype sdt, 
 }
 
 constexpr int kThreads = 256;
-// the rotary path stages 32 runs x 2 x D/2 floats in shared memory: D <= 384
-// keeps that within the 48 KB a block gets without opting in
+// the rotary path stages 64 runs x 2 x D/2 floats in shared memory (96 KB
+// at D = 384, with the opt-in above 48 KB)
 constexpr int kRopeMaxD = 384;
 constexpr int kItems = 8;       // 8-element items per lane in flight
 
@@ -382,15 +382,20 @@ __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __gri
 
 template <int MODE, int SB, int DB, bool ROPE>
 dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
-    // 4 runs per warp keep each block's fixed decode latency small against
-    // its copy time; drop to 2 only when the grid would otherwise have fewer
-    // than two blocks per resident block slot
-    const long long slots = (long long)num_sms() * 3;
-    int rpw = 4;
-    if ((a.nruns + 31) / 32 < 2 * slots) rpw = 2;
+    // 8 runs per warp (64 per block): measured on the FLUX-like step against
+    // 1, 2, 3, 4, 6, 12, 16, 24 and 32, it gives the shortest layout steps
+    // (layout-in 5.8, layout-out 5.7 TB/s) and the fastest Wan-size unpacks;
+    // smaller blocks pay their run decoding too often, larger ones leave the
+    // last wave too uneven.
+    const int rpw = 8;
     const long long blocks = (a.nruns + 8LL * rpw - 1) / (8LL * rpw);
     // rotary tables: two rows of D/2 floats for each of the block's runs
     const size_t smem = ROPE ? (size_t)8 * rpw * a.L.D * sizeof(float) : 0;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(run_kernel<MODE, SB, DB, ROPE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
+    }
     cudaError_t e = launch_pdl(run_kernel<MODE, SB, DB, ROPE>, dim3((unsigned)blocks), dim3(kThreads), smem, st, a, rpw);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     return check_launch(who);
