@@ -382,12 +382,14 @@ __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __gri
 
 template <int MODE, int SB, int DB, bool ROPE>
 dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
-    // 8 runs per warp (64 per block): measured on the FLUX-like step against
-    // 1, 2, 3, 4, 6, 12, 16, 24 and 32, it gives the shortest layout steps
-    // (layout-in 5.8, layout-out 5.7 TB/s) and the fastest Wan-size unpacks;
-    // smaller blocks pay their run decoding too often, larger ones leave the
-    // last wave too uneven.
-    const int rpw = 8;
+    // Up to 8 runs per warp (64 per block): measured on the FLUX-like step
+    // against 1, 2, 3, 4, 6, 12, 16, 24 and 32, 8 gives the shortest layout
+    // steps (layout-in 5.8, layout-out 5.7 TB/s) and the fastest Wan-size
+    // unpacks; smaller blocks pay their run decoding too often, larger ones
+    // leave the last wave uneven.  Small exchanges take fewer runs per warp so
+    // that the grid still has about two blocks per SM.
+    long long fit = a.nruns / (16LL * num_sms());
+    const int rpw = fit < 1 ? 1 : (fit > 8 ? 8 : (int)fit);
     const long long blocks = (a.nruns + 8LL * rpw - 1) / (8LL * rpw);
     // rotary tables: two rows of D/2 floats for each of the block's runs
     const size_t smem = ROPE ? (size_t)8 * rpw * a.L.D * sizeof(float) : 0;
