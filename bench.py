@@ -94,6 +94,7 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.start = 0
 
     def __enter__(self):
         try:
@@ -103,8 +104,15 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            # nvidia-smi takes a while to start: hold the timed region back
+            # until its first sample has come in, so the samples after this
+            # point are the region's own
+            t0 = time.time()
+            while not self.lines and self.proc.poll() is None and time.time() - t0 < 10:
+                time.sleep(0.005)
         except OSError:
             self.proc = None
+        self.start = len(self.lines)
         return self
 
     def _read(self):
@@ -124,7 +132,11 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        inside = self.lines[self.start:]
+        # a region shorter than the sampling interval: the sample taken just
+        # before it started
+        lines = inside if inside else self.lines[max(self.start - 1, 0):self.start]
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -139,7 +151,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_in_region": len(inside)}
 
 
 def traffic_per_launch(kernel_src: str, note: str):
@@ -368,7 +380,7 @@ def run_ours(args):
 
     # end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args)
-    extra = {} if args.no_extra else {**bandwidth_at_scale(dev, flush, peaks),
+    extra = {} if args.no_extra else {**back_to_back(w, U, dev), **bandwidth_at_scale(dev, flush, peaks),
                                       **receive_prep_at_scale(dev, flush),
                                       **fp8_wire_at_scale(dev, flush)}
 
@@ -467,6 +479,76 @@ def bandwidth_at_scale(dev, flush, peaks):
     del pred, cfg
     torch.cuda.empty_cache()
     return res
+
+
+def back_to_back(w, U, dev):
+    """Each bandwidth kernel of the step on its own: 40 launches in a row on
+    one stream (consecutive launches overlap their launch latency through
+    programmatic dependent launch, as inside a model), rotating over enough
+    buffer sets that every launch reads inputs last touched more than three
+    L2 capacities earlier; one event pair around the 40 launches.  The step's
+    own split (events between its phases) includes a launch gap per phase,
+    which weighs most on the short CFG launch."""
+    import torch
+    import sequence_attention_gb300 as sa
+    L = sa.dit_sp_layout_init(w.B, w.S, w.H, w.D, U, w.R)
+    dt = torch.bfloat16 if w.dtype != "f32" else torch.float32
+    eb = 2 if w.dtype != "f32" else 4
+    shp, hs = (w.B, w.S, w.H, w.D), L.head_shape()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    stream = torch.cuda.current_stream(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+
+    def rnd(shape, dtype=dt):
+        return torch.randn(shape, generator=gen, dtype=torch.float32, device=dev).to(dtype)
+
+    def timed(nbytes_in, make, launch, nbytes):
+        nsets = max(2, -(-3 * l2 // max(nbytes_in, 1)))
+        sets = [make() for _ in range(nsets)]
+        for i in range(6):
+            launch(sets[i % nsets])
+        torch.cuda.synchronize(dev)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 40
+        s.record(stream)
+        for i in range(n):
+            launch(sets[i % nsets])
+        e.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = s.elapsed_time(e) / n
+        del sets
+        torch.cuda.empty_cache()
+        return {"us": round(ms * 1e3, 2), "GBs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+
+    plane = w.B * w.S * w.H * w.D * eb
+    wire1 = L.wire_elems(1) * eb
+    wire3 = L.wire_elems(3) * eb
+    S2H, H2S = sa.DIT_SEQ_TO_HEAD, sa.DIT_HEAD_TO_SEQ
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    v_dt = torch.float16 if dt == torch.bfloat16 else dt
+    res = {}
+    res["pack_s2h"] = timed(3 * plane, lambda: ([rnd(shp) for _ in range(3)], torch.empty(L.wire_elems(3), dtype=dt, device=dev)),
+                            lambda x: sa.dit_ulysses_pack(L, S2H, x[0], x[1]), 3 * plane + wire3)
+    res["a2a_s2h"] = timed(wire3, lambda: (rnd(L.wire_elems(3)), torch.empty(L.wire_elems(3), dtype=dt, device=dev)),
+                           lambda x: sa.dit_a2a_sim(L, S2H, 3, x[0], x[1]), 2 * wire3)
+    res["unpack_s2h"] = timed(wire3, lambda: (rnd(L.wire_elems(3)), [torch.empty(hs, dtype=t, device=dev) for t in (dt, dt, v_dt)]),
+                              lambda x: sa.dit_ulysses_unpack(L, S2H, x[0], x[1], flag), 2 * wire3)
+    res["pack_h2s"] = timed(wire1, lambda: (rnd(hs), torch.empty(L.wire_elems(1), dtype=dt, device=dev)),
+                            lambda x: sa.dit_ulysses_pack(L, H2S, [x[0]], x[1]), plane + wire1)
+    res["a2a_h2s"] = timed(wire1, lambda: (rnd(L.wire_elems(1)), torch.empty(L.wire_elems(1), dtype=dt, device=dev)),
+                           lambda x: sa.dit_a2a_sim(L, H2S, 1, x[0], x[1]), 2 * wire1)
+    res["unpack_h2s"] = timed(wire1, lambda: (rnd(L.wire_elems(1)), torch.empty(shp, dtype=dt, device=dev)),
+                              lambda x: sa.dit_ulysses_unpack(L, H2S, x[0], [x[1]]), wire1 + plane)
+    cfg_in = {"f32": torch.float32, "bf16": torch.bfloat16}[w.cfg_in]
+    cfg_out = {"f32": torch.float32, "bf16": torch.bfloat16}[w.cfg_out]
+    n = 1
+    for d in w.cfg_shape[1:]:
+        n *= d
+    ib, ob = (4 if cfg_in == torch.float32 else 2), (4 if cfg_out == torch.float32 else 2)
+    res["cfg"] = timed(2 * n * ib, lambda: (rnd(w.cfg_shape, cfg_in), torch.empty(w.cfg_shape[1:], dtype=cfg_out, device=dev)),
+                       lambda x: sa.dit_cfg_combine(x[0], x[1], w.g), n * (2 * ib + ob))
+    return {"back_to_back": res}
 
 
 def receive_prep_at_scale(dev, flush):
