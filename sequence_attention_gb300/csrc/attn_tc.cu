@@ -31,6 +31,9 @@
 // rounding.  Keys at or past the block's valid length are masked to -inf;
 // TMA zero-fills rows past each block's extent, so padding bytes in the
 // buffers are never read.
+// The epilogue writes O / l into the (by then free) Q and K buffers and
+// stores it with TMA, each warp its 32 rows; the output map has the block's
+// own extents, so no row past the block is written.
 //
 // Every mbarrier wait is bounded (a few seconds of %globaltimer); on expiry
 // the CTA records DIT_ERR_TIMEOUT in the status word, stops issuing work,
@@ -64,6 +67,7 @@ struct TcParams {
     CUtensorMap qmap[DIT_MAX_R];
     CUtensorMap kmap[DIT_MAX_R];
     CUtensorMap vmap[DIT_MAX_R];
+    CUtensorMap omap[DIT_MAX_R];    // output of query block r: (d, h, row, b, key block)
     int q_len[DIT_MAX_R];
     int kv_len[DIT_MAX_R];
     int q_row0[DIT_MAX_R];          // first output row of query block r (packed sequences)
@@ -150,6 +154,22 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
+}
+
+// Shared -> global tile store of one 128-byte-wide box (rows past the map's
+// extent are not written), and the bulk-group completion wait.
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2, int c3,
+                                             int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -241,6 +261,27 @@ __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The CTA's query block r, key block j, batch b, head h and first query row.
+// %ctaid is read with volatile moves, so the epilogue recomputes these rather
+// than keeping them live (in registers the softmax needs) through the
+// key-tile loop.
+struct Cta {
+    int r, j, b, h, row_base;
+};
+__device__ __forceinline__ Cta cta_coords(const TcParams& p) {
+    uint32_t x, y, z;
+    asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(x));
+    asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(y));
+    asm volatile("mov.u32 %0, %%ctaid.z;" : "=r"(z));
+    Cta c;
+    c.b = (int)z % p.B;
+    c.j = p.diag ? (int)z / p.B : ((int)z / p.B) % p.n_kv;
+    c.r = p.diag ? c.j : (int)z / (p.B * p.n_kv);
+    c.h = (int)y;
+    c.row_base = (int)x * (NQT * BM);
+    return c;
+}
+
 // ---- the kernel -------------------------------------------------------------
 template <int D, bool P_BF16>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
@@ -256,24 +297,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int z = blockIdx.z;
-    const int b = z % p.B;
-    const int j = p.diag ? z / p.B : (z / p.B) % p.n_kv;
-    const int r = p.diag ? j : z / (p.B * p.n_kv);
-    const int h = blockIdx.y;
+    const Cta cta = cta_coords(p);
+    const int b = cta.b, j = cta.j, r = cta.r, h = cta.h, row_base = cta.row_base;
     const int qlen = p.q_len[r], kvlen = p.kv_len[j];
-    const int row_base = blockIdx.x * (NQT * BM);
     if (row_base >= qlen) return;
     const int ntiles = (kvlen + BN - 1) / BN;
 
-    const int eb = dtype_bytes(p.o_dt);
-    char* obase = static_cast<char*>(p.o.ptr) + (r * p.o.stride_q + j * p.o.stride_kv + b * p.o.stride_b +
-                                                 h * p.o.stride_h + (long long)p.q_row0[r] * p.o.stride_s) * eb;
-    float* lbase = p.lse.ptr ? p.lse.ptr + r * p.lse.stride_q + j * p.lse.stride_kv + b * p.lse.stride_b +
-                                   h * p.lse.stride_h + p.q_row0[r]
-                             : nullptr;
-
     if (ntiles == 0) {   // empty key chunk: O = 0, lse = -inf
+        const int eb = dtype_bytes(p.o_dt);
+        char* obase = static_cast<char*>(p.o.ptr) + (r * p.o.stride_q + j * p.o.stride_kv + b * p.o.stride_b +
+                                                     h * p.o.stride_h + (long long)p.q_row0[r] * p.o.stride_s) * eb;
+        float* lbase = p.lse.ptr ? p.lse.ptr + r * p.lse.stride_q + j * p.lse.stride_kv + b * p.lse.stride_b +
+                                       h * p.lse.stride_h + p.q_row0[r]
+                                 : nullptr;
         pdl_wait();
         if (threadIdx.x < NQT * BM) {
             const int row = row_base + threadIdx.x;
@@ -431,7 +467,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const uint32_t St = tmem + t * 128 + lane_off;
         const uint32_t Ot = tmem + 256 + t * D + lane_off;
-        const int row = row_base + t * BM + q4 * 32 + lane;
         const float c = p.c;
         float m_used = 0.f, l = 0.f;
         bool ok = true;
@@ -516,20 +551,59 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
-            const bool live = row < qlen;
-            char* orow = obase + (long long)(live ? row : 0) * p.o.stride_s * eb;
-            uint32_t x[D];
-            if constexpr (D == 128) tmem_ld128(Ot, x); else tmem_ld64(Ot, x);
-            if (live) {
+            const Cta e = cta_coords(p);
+            const int eb = dtype_bytes(p.o_dt);
+            // Stage the tile in shared memory (per 128 bytes of d, BM rows of
+            // 128 bytes, 16-byte chunks swizzled by row mod 8) and store it
+            // with TMA, each warp its own 32 rows: every MMA has completed,
+            // so the Q and K buffers are free (tile t takes BM*D*eb bytes
+            // from the start).  Rows past the block's length are clipped by
+            // the output map.
+            const int rt = q4 * 32 + lane;
+            // Shared addresses are recomputed from the array's own address
+            // (the aligned base is at a fixed offset in the shared window)
+            // instead of keeping the generic pointers live through the loop.
+            const uint32_t sbase = (su32(smem_raw) + 1023u) & ~1023u;
+            const uint32_t stage = sbase + (uint32_t)(t * BM * D * eb) + (uint32_t)rt * 128u;
+            auto chunk = [&](int c) { return stage + (uint32_t)((c >> 3) * BM * 128) + (uint32_t)(((c & 7) ^ (rt & 7)) << 4); };
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {     // 32 columns of O at a time
+                uint32_t x[32];
+                tmem_ld32(Ot + cc * 32, x);
+                if (p.o_dt == DIT_F32) {
 #pragma unroll
-                for (int q8 = 0; q8 < D / 8; ++q8) {
-                    Vec8 v;
+                    for (int c = 0; c < 8; ++c)
+                        st_shared16(chunk(cc * 8 + c), __float_as_uint(__uint_as_float(x[4 * c]) * inv),
+                                    __float_as_uint(__uint_as_float(x[4 * c + 1]) * inv),
+                                    __float_as_uint(__uint_as_float(x[4 * c + 2]) * inv),
+                                    __float_as_uint(__uint_as_float(x[4 * c + 3]) * inv));
+                } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v.f[e] = __uint_as_float(x[q8 * 8 + e]) * inv;
-                    store8(orow + q8 * 8 * eb, p.o_dt, v);
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack2(__uint_as_float(x[8 * c + 2 * e]) * inv,
+                                         __uint_as_float(x[8 * c + 2 * e + 1]) * inv, p.o_dt);
+                        st_shared16(chunk(cc * 4 + c), w[0], w[1], w[2], w[3]);
+                    }
                 }
             }
-            if (live && lbase) lbase[row] = (m_used + log2f(l)) * 0.69314718055994531f;
+            // each warp stores its own 32 rows: no wait on the other warps
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            const int row = e.row_base + t * BM + rt;
+            if (p.lse.ptr && row < p.q_len[e.r])
+                p.lse.ptr[e.r * p.lse.stride_q + e.j * p.lse.stride_kv + e.b * p.lse.stride_b + e.h * p.lse.stride_h +
+                          p.q_row0[e.r] + row] = (m_used + log2f(l)) * 0.69314718055994531f;
+            if (lane == 0) {
+                const int nbox = D * eb / 128;
+                for (int bx = 0; bx < nbox; ++bx)
+                    tma_store_5d(&p.omap[e.r], sbase + (uint32_t)(t * BM * D * eb + bx * BM * 128 + q4 * 32 * 128),
+                                 bx * (128 / eb), e.h, e.row_base + t * BM + q4 * 32, e.b, p.diag ? 0 : e.j);
+                bulk_commit();
+                bulk_wait_all();      // the rows are in global memory before the CTA exits
+            }
         }
     }
 
@@ -576,6 +650,42 @@ dit_status make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const
     return DIT_OK;
 }
 
+// 5-D map over the output view of one query block: (d, h, row, b, key
+// block), a box of 128 bytes of d x 1 x 32 rows x 1 x 1 (one warp's rows),
+// 128-byte swizzle.  Its
+// extents are the block's own (rows = the block's query rows), so a store
+// of a ragged last tile writes no row past the block.  Dimensions of extent
+// 1 get the span of the dimensions inside them as stride; a zero stride on
+// a longer dimension would send two rows to one address and is refused.
+dit_status make_omap(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, void* base, dit_dtype dt, int D,
+                     int H, int rows, int B, int nj, int64_t sh, int64_t ss, int64_t sb, int64_t sj) {
+    const int eb = dtype_bytes(dt);
+    if (rows < 1) rows = 1;     // never stored: the kernel skips empty blocks
+    const cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)B, (cuuint64_t)nj};
+    const int64_t st[4] = {sh, ss, sb, sj};
+    cuuint64_t strides[4];
+    uint64_t span = (uint64_t)D * eb;
+    for (int i = 0; i < 4; ++i) {
+        if (dims[i + 1] == 1) {
+            strides[i] = span;
+        } else {
+            if (st[i] == 0) return fail(DIT_ERR_INVALID_ARG, "attention: zero output stride on a dimension longer than 1");
+            strides[i] = (cuuint64_t)st[i] * eb;
+        }
+        span = strides[i] * dims[i + 1];
+    }
+    const cuuint32_t box[5] = {(cuuint32_t)(128 / eb), 1, 32, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUtensorMapDataType ty = dt == DIT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dt == DIT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult res = enc(m, ty, 5, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS)
+        return fail(DIT_ERR_INVALID_ARG, "attention: output tensor map rejected (CUresult %d)", (int)res);
+    return DIT_OK;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with fp32 accumulation.
 uint32_t make_idesc(bool bf16, bool b_mn_major, int N, int M) {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
@@ -598,7 +708,7 @@ dit_status launch_kernel(const TcParams& prm, dim3 grid, cudaStream_t st) {
 dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return fail(DIT_ERR_CUDA, "attention: cuTensorMapEncodeTiled unavailable");
-    TcParams params;                // kernel parameter block (~3.3 KB, on the stack)
+    TcParams params;                // kernel parameter block (~4.4 KB, on the stack)
     memset(&params, 0, sizeof(params));
     TcParams* prm = &params;
     dit_status s = DIT_OK;
@@ -610,6 +720,14 @@ dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
         const char* base = static_cast<const char*>(a.q.ptr) + (r * a.q.stride_q + (int64_t)a.q_row0[r] * a.q.stride_s) * 2;
         s = make_map(enc, &prm->qmap[r], base, a.qk_dt, a.D, a.H, a.q_len[r], a.B, a.q.stride_h, a.q.stride_s,
                      a.q.stride_b);
+        if (s == DIT_OK) {
+            // with diag, query block r writes key block r's partial only
+            char* ob = static_cast<char*>(a.o.ptr) +
+                       (r * a.o.stride_q + (a.diag ? r * a.o.stride_kv : 0) + (int64_t)a.q_row0[r] * a.o.stride_s) *
+                           dtype_bytes(a.o_dt);
+            s = make_omap(enc, &prm->omap[r], ob, a.o_dt, a.D, a.H, a.q_len[r], a.B, a.diag ? 1 : a.n_kv,
+                          a.o.stride_h, a.o.stride_s, a.o.stride_b, a.o.stride_kv);
+        }
     }
     for (int j = 0; j < a.n_kv && s == DIT_OK; ++j) {
         prm->kv_len[j] = a.kv_len[j];
