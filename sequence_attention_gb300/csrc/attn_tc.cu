@@ -61,7 +61,7 @@ constexpr int NTHREADS = 384;
 constexpr int CHUNK = BM * 128;  // bytes of one 64-column (128-byte) swizzle chunk
 constexpr unsigned long long kWaitNs = 4000000000ull;
 
-enum { B_Q = 0, B_KF = 1, B_KE = 3, B_VF = 5, B_VE = 8, B_SF = 11, B_PF = 13, B_OD = 15, NBAR = 16 };
+enum { B_Q = 0, B_KF = 1, B_KE = 3, B_VF = 5, B_VE = 8, B_SF = 11, B_PF = 13, B_OD = 15, NBAR = 17 };
 
 struct TcParams {
     CUtensorMap qmap[DIT_MAX_R];
@@ -167,7 +167,7 @@ __device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t sr
         : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             mbar_init(bar(B_SF + t), 1);
             mbar_init(bar(B_PF + t), 128);
         }
-        mbar_init(bar(B_OD), 1);
+        for (int t = 0; t < NQT; ++t) mbar_init(bar(B_OD + t), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -440,6 +440,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 if (!(ok = wait_phase(bar(B_PF + 0), n & 1, ctl))) break;
                 tc_fence_after();
                 issue_pv(0, s, n > 0);
+                if (!nxt) {
+                    // tile 0 is done: its epilogue overlaps tile 1's last P V
+                    // (every Q K^T, the last reader of the Q and K buffers
+                    // the epilogue stages into, was issued before)
+                    tc_commit(bar(B_OD + 0));
+                }
                 if (nxt) {
                     if (!(ok = wait_phase(bar(B_KF + s1), ph1, ctl))) break;
                     tc_fence_after();
@@ -456,8 +462,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                     tc_commit(bar(B_KE + s1));
                 }
             }
-            tc_commit(bar(B_OD));
-            if (!ok) drain_phase(bar(B_OD), 0);   // every issued MMA has finished
+            // on a normal run tile 0's commit was made in the last key tile;
+            // after an abort its waiters leave on the abort flag, so a second
+            // commit there is harmless
+            if (!ok) tc_commit(bar(B_OD + 0));
+            tc_commit(bar(B_OD + 1));
+            if (!ok) drain_phase(bar(B_OD + 1), 0);   // every issued MMA has finished
         }
         }
     } else {
@@ -547,7 +557,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             mbar_arrive(bar(B_PF + t));
         }
         // epilogue: O / l and lse = ln(2) * (m + log2 l)
-        if (ok) ok = __all_sync(0xffffffffu, wait_phase(bar(B_OD), 0, ctl));
+        // this tile's "O done" barrier; the tile index is re-read from
+        // %tid (volatile) so that nothing derived from it stays live in the
+        // key-tile loop, where the softmax needs every register
+        uint32_t tid_now;
+        asm volatile("mov.u32 %0, %%tid.x;" : "=r"(tid_now));
+        const uint32_t od_bar = ((su32(smem_raw) + 1023u) & ~1023u) +
+                                (uint32_t)((NQT + NSK + NSV) * TILE + (B_OD + (int)(tid_now >> 7)) * 8);
+        if (ok) ok = __all_sync(0xffffffffu, wait_phase(od_bar, 0, ctl));
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
@@ -602,7 +619,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                     tma_store_5d(&p.omap[e.r], sbase + (uint32_t)(t * BM * D * eb + bx * BM * 128 + q4 * 32 * 128),
                                  bx * (128 / eb), e.h, e.row_base + t * BM + q4 * 32, e.b, p.diag ? 0 : e.j);
                 bulk_commit();
-                bulk_wait_all();      // the rows are in global memory before the CTA exits
+                // the shared-memory source must stay until the copy has read
+                // it; the global writes complete with the grid, before any
+                // dependent kernel passes its griddepcontrol.wait
+                bulk_wait_read();
             }
         }
     }
