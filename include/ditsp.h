@@ -351,7 +351,11 @@ DIT_API dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplanes, 
  * F16}, D in {64, 128}, o_dt in {F32, BF16, F16} (tensor-core path: Q K^T
  * in qk_dt with fp32 accumulation; P rounded to v_dt for P V with fp32
  * accumulation).  Strides and pointers must be 16-byte aligned.
- * Head dims other than these return DIT_ERR_UNSUPPORTED.
+ * Head dims other than these return DIT_ERR_UNSUPPORTED.  The output view
+ * must give every result its own address: a zero o stride on a dimension
+ * with more than one index (stride_h with H > 1, stride_s with a block of
+ * more than one row, stride_b with B > 1, stride_q / stride_kv with more
+ * than one block) returns DIT_ERR_INVALID_ARG.
  */
 DIT_API dit_status dit_attn_partial(int B, int H, int D, float scale,
                             int n_q, const int* q_len, int n_kv, const int* kv_len,

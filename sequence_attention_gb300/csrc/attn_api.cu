@@ -47,6 +47,15 @@ dit_status validate_and_launch(AttnArgs& a, const char* who, cudaStream_t st) {
                     stride_ok(a.o.stride_q, ob) && stride_ok(a.o.stride_kv, ob) && stride_ok(a.o.stride_b, ob) &&
                     stride_ok(a.o.stride_s, ob) && stride_ok(a.o.stride_h, ob);
     if (!ok) return fail(DIT_ERR_INVALID_ARG, "%s: strides must be non-negative 16-byte multiples", who);
+    // no two results may share an output address (the tensor-core path
+    // stores whole row tiles with TMA): a zero output stride is allowed only
+    // on a dimension with a single index
+    int maxq = 0;
+    for (int r = 0; r < a.n_q; ++r) maxq = a.q_len[r] > maxq ? a.q_len[r] : maxq;
+    const bool alias = (a.H > 1 && a.o.stride_h == 0) || (maxq > 1 && a.o.stride_s == 0) ||
+                       (a.B > 1 && a.o.stride_b == 0) || (!a.diag && a.n_q > 1 && a.o.stride_q == 0) ||
+                       (!a.diag && a.n_kv > 1 && a.o.stride_kv == 0);
+    if (alias) return fail(DIT_ERR_INVALID_ARG, "%s: output view maps two results to one address", who);
     if (!a.status) a.status = default_status_word();
     if (!a.status) return fail(DIT_ERR_CUDA, "%s: no device status word", who);
     return f32 ? launch_attn_f32(a, st) : launch_attn_tc(a, st);

@@ -183,6 +183,36 @@ def test_attention_argument_checks(dl):
     assert st == dl.DIT_ERR_INVALID_ARG                  # more than 8 query blocks
 
 
+def test_attention_output_aliasing_is_refused(dl):
+    """A zero output stride on a dimension with more than one index would
+    send two results to one address; it is refused before any launch (a
+    zero stride on a dimension of one index is fine)."""
+    from sequence_attention_gb300._lib import DitLseView
+    L = dl.lib()
+    q = _view(1 << 20, 64 * 4 * 128, 4 * 128, 128)
+    lse = DitLseView()
+
+    def attention(o, B=1, Sq=64):
+        return L.dit_attention(B, 4, 128, 0.1, Sq, 64, q, dl.DIT_BF16, q, q, dl.DIT_F16, o, dl.DIT_BF16, lse,
+                               None, None)
+
+    assert attention(_view(1 << 20, 64 * 4 * 128, 0, 128)) == dl.DIT_ERR_INVALID_ARG      # rows alias
+    assert attention(_view(1 << 20, 64 * 4 * 128, 4 * 128, 0)) == dl.DIT_ERR_INVALID_ARG  # heads alias
+    assert attention(_view(1 << 20, 0, 4 * 128, 128), B=2) == dl.DIT_ERR_INVALID_ARG       # batches alias
+    # one query row: a zero row stride is fine, the call goes on to the device
+    assert attention(_view(1 << 20, 64 * 4 * 128, 0, 128), Sq=1) != dl.DIT_ERR_INVALID_ARG
+    lens = (ctypes.c_int * 2)(64, 64)
+    o = _view(1 << 20, 64 * 4 * 128, 4 * 128, 128)
+    o.stride_q, o.stride_kv = 0, 2 * 64 * 4 * 128
+    st = L.dit_attn_partial(1, 4, 128, 0.1, 2, lens, 2, lens, q, dl.DIT_BF16, q, q, dl.DIT_F16, o,
+                            dl.DIT_BF16, lse, None, None)
+    assert st == dl.DIT_ERR_INVALID_ARG                  # query blocks alias
+    o.stride_q, o.stride_kv = 2 * 64 * 4 * 128, 0
+    st = L.dit_attn_partial(1, 4, 128, 0.1, 2, lens, 2, lens, q, dl.DIT_BF16, q, q, dl.DIT_F16, o,
+                            dl.DIT_BF16, lse, None, None)
+    assert st == dl.DIT_ERR_INVALID_ARG                  # key blocks alias
+
+
 def test_status_strings(dl):
     L = dl.lib()
     assert L.dit_status_string(0) == b"DIT_OK"
