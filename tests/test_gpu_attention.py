@@ -58,6 +58,31 @@ def test_tensor_core_attention_matches_oracle(B, Sq, Sk, H, D, v_dtype):
         assert max_abs(f64(lse), lse_ref) <= LSE_ABS
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("o_dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_output_view_is_written_exactly(D, o_dtype):
+    """The output tiles are stored with TMA through a map with the view's own
+    extents. Every row and head of a strided view is written, in f32, bf16
+    and f16. Nothing outside it is written: the rows after the ragged last
+    tile, the padding head and the LSE padding keep their NaN sentinels."""
+    import sequence_attention_gb300 as sa
+    B, Sq, Sk, H, Hp, extra = 2, 300, 200, 3, 4, 40
+    q, k, v = _qkv(B, Sq, Sk, H, D, seed=21)
+    big = torch.full((B, Sq + extra, Hp, D), float("nan"), dtype=o_dtype, device="cuda")
+    lbig = torch.full((B, H + 1, Sq + extra), float("nan"), dtype=torch.float32, device="cuda")
+    o, lse = big[:, :Sq, :H, :], lbig[:, :H, :Sq]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sa.dit_attention(q.cuda(), k.cuda(), v.to(torch.float16).cuda(), o, lse, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o_ref, lse_ref = oatt.attention(f64(q), f64(k), f64(v))
+    assert_bf16_close(f64(o), o_ref, f"O ({o_dtype}, D {D})")
+    assert max_abs(f64(lse), lse_ref) <= LSE_ABS
+    assert torch.isnan(big[:, Sq:]).all() and torch.isnan(big[:, :, H:]).all()
+    assert torch.isnan(lbig[:, :, Sq:]).all() and torch.isnan(lbig[:, H:]).all()
+    assert not torch.isnan(o).any()
+
+
 def test_tensor_core_large_logits():
     """Unit-variance inputs at D = 128 give logits of std ~1 and row maxima
     that grow across key tiles, exercising the O rescale path."""
