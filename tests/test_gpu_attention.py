@@ -131,8 +131,12 @@ def _partials(q, k, v, lens, v_dtype, seed_rows=None):
 
 
 @pytest.mark.parametrize("dt,lens", [("bf16", [200, 200, 133]), ("bf16", [128, 0, 77]),
-                                     ("f32", [100, 100, 56]), ("bf16", [1000] * 4 + [997])])
+                                     ("f32", [100, 100, 56]), ("bf16", [1000] * 4 + [997]),
+                                     ("bf16", [8300, 100])])
 def test_partials_and_merge(dt, lens):
+    """Short key blocks go to the kernel that walks every block of its query
+    rows; a block of more than 64 key tiles (8300 keys) sends the launch to
+    the one-partial-per-CTA kernel."""
     import sequence_attention_gb300 as sa
     B, Sq, H, D = 2, 190, 2, (128 if dt == "bf16" else 64)
     Sk = sum(lens)
@@ -166,6 +170,22 @@ def test_partials_and_merge(dt, lens):
     else:
         assert max_abs(f64(out[0]), o_ref) <= F32_MAX_ABS
     assert max_abs(f64(lse_out[0]), l_ref) <= LSE_ABS
+
+
+def test_walk_with_every_key_block_empty():
+    """Every key block empty: each partial is O = 0 and lse = -inf, and rows
+    past the query blocks' lengths are not written."""
+    import sequence_attention_gb300 as sa
+    B, Sq, H, D = 1, 300, 2, 128
+    q = synth.normal((2, B, Sq, H, D), 60, 0.5, "bf16")
+    k = torch.zeros((3, B, 8, H, D), dtype=torch.bfloat16)
+    o = torch.full((2, 3, B, Sq, H, D), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((2, 3, B, H, Sq), float("nan"), dtype=torch.float32, device="cuda")
+    sa.dit_attn_partial(q.cuda(), k.cuda(), k.to(torch.float16).cuda(), o, lse, [Sq, 120], [0, 0, 0])
+    torch.cuda.synchronize()
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    assert torch.all(o[1, :, :, :120] == 0) and torch.all(torch.isneginf(lse[1, :, :, :, :120]))
+    assert torch.isnan(o[1, :, :, 120:]).all() and torch.isnan(lse[1, :, :, :, 120:]).all()
 
 
 def test_merge_kernel_against_oracle_merge():
