@@ -732,7 +732,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
     pdl_wait();          // barriers and TMEM are set up; tensors from here on
 
     if (warp >= 8) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+        // the walking MMA issuer keeps more loop state: 104 registers here,
+        // 200 for each softmax warpgroup (2*200 + 104 = 3*168)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
         if (warp == 8 || warp == 10) {
         // ------------------------------------------------------------ producers
         // Tiles are numbered across the key blocks (g); stage g % nst.
@@ -862,7 +864,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
         }
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 200;" ::: "memory");
         // ------------------------------------------------------------ softmax
         const int t = warp >> 2, q4 = warp & 3;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
