@@ -42,7 +42,6 @@
 #include <math.h>
 #include <string.h>
 
-#include <algorithm>
 #include <atomic>
 
 #include <cuda.h>
@@ -1183,15 +1182,11 @@ dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
         prm->idesc_qk = make_idesc(a.qk_dt == DIT_BF16, false, BN, BM);
         prm->idesc_pv = make_idesc(a.v_dt == DIT_BF16, true, a.D, BM);
         prm->o = a.o; prm->o_dt = a.o_dt; prm->lse = a.lse; prm->status = a.status;
-        // Several short key blocks per query block: one CTA walks them all,
-        // paying the pipeline fill and drain once instead of once per block
-        // (measured on one GB300: 1121 against 1080 TFLOP/s at 18 key tiles
-        // per block, 1325 against 1308 at 28).  Long blocks amortise those
-        // costs anyway and run faster with the 3-stage V ring of the
-        // one-partial kernel (1463 against 1437 TFLOP/s at 148 tiles).
-        int max_tiles = 0;
-        for (int j = 0; j < a.n_kv; ++j) max_tiles = std::max(max_tiles, (a.kv_len[j] + BN - 1) / BN);
-        const bool walk = !a.diag && a.n_kv > 1 && max_tiles <= 64;
+        // Several key blocks per query block: one CTA walks them all, paying
+        // the pipeline fill and drain once instead of once per block
+        // (measured on one GB300: 1153 against 1080 TFLOP/s at 18 key tiles
+        // per block, 1369 against 1308 at 28, 1448 against 1437 at 148).
+        const bool walk = !a.diag && a.n_kv > 1;
         dim3 grid((maxq + NQT * BM - 1) / (NQT * BM), a.H, (a.diag || walk ? a.n_q : a.n_q * a.n_kv) * a.B);
         const bool pb = a.v_dt == DIT_BF16;
         if (grid.y > 65535 || grid.z > 65535) s = fail(DIT_ERR_UNSUPPORTED, "attention: grid too large");

@@ -134,9 +134,9 @@ def _partials(q, k, v, lens, v_dtype, seed_rows=None):
                                      ("f32", [100, 100, 56]), ("bf16", [1000] * 4 + [997]),
                                      ("bf16", [8300, 100])])
 def test_partials_and_merge(dt, lens):
-    """Short key blocks go to the kernel that walks every block of its query
-    rows; a block of more than 64 key tiles (8300 keys) sends the launch to
-    the one-partial-per-CTA kernel."""
+    """Several key blocks go to the kernel that walks every block of its
+    query rows (empty blocks, a ragged last block and a long 65-tile block
+    included); one block goes to the one-partial-per-CTA kernel."""
     import sequence_attention_gb300 as sa
     B, Sq, H, D = 2, 190, 2, (128 if dt == "bf16" else 64)
     Sk = sum(lens)
