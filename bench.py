@@ -301,12 +301,14 @@ def run_ours(args):
         mark(0)
         plan.layout_in(q, k, v)
         mark(1)
-        plan.attend()
+        plan.partials()
         mark(2)
-        plan.layout_out(out)
+        plan.merge()            # nothing when R = 1
         mark(3)
-        sa.dit_cfg_combine(pred, cfg_out, w.g)
+        plan.layout_out(out)
         mark(4)
+        sa.dit_cfg_combine(pred, cfg_out, w.g)
+        mark(5)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -316,7 +318,7 @@ def run_ours(args):
     K = args.steps
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] or 0) \
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
 
     def timed():
         barrier()
@@ -334,11 +336,12 @@ def run_ours(args):
         clocks = timed()        # rejected once: measure again
         clocks["remeasured"] = True
 
-    seg = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(4)]   # ms per segment
+    # ms per segment: layout-in, attention partials, merge, layout-out, CFG
+    seg = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(5)]
     step_ms = [sum(x) for x in zip(*seg)]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, dev)
-    attn_ms = statistics.mean(seg[1])
+    attn_ms = statistics.mean(seg[1])          # the partial-attention launch alone
     flops = w.attn_flops
     value = ws * flops / (ms_max * 1e-3) / 1e12
 
@@ -356,7 +359,13 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     achieved = flops / (attn_ms * 1e-3) / 1e12
-    traffic = traffic_per_launch(ATTN_SRC, TRAFFIC_NOTE)
+    # the ncu note covers the attention launch of the default FLUX-like workload
+    traffic = traffic_per_launch(ATTN_SRC, TRAFFIC_NOTE) if (w.name == "flux1024" and w.R == 1) else None
+    attn_kernel = (f"attn_f32_kernel<{w.D}>" if w.dtype == "f32" else
+                   f"attn_tc_kernel<{w.D},false>" if w.R == 1 else f"attn_tc_walk_kernel<{w.D},false>")
+    # merge bytes: R fp32 partials and their LSE per real row and head, the
+    # output written once (16-bit)
+    merge_bytes = w.B * w.S * w.H * (w.R * (w.D * 4 + 4) + w.D * 2)
 
     # one step alone, launched call by call and replayed from its own CUDA
     # graph (L2 flushed before each, median of 20): the cost of the launches
@@ -398,7 +407,7 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": traffic, "kernel": "attn_tc_kernel<128,false> (dit_attn_partial)",
+                     "traffic": traffic, "kernel": f"{attn_kernel} (dit_attn_partial)",
                      "peak_source": f"{peak_src} bf16 burst",
                      "frac_of_sustained": round(achieved / peaks.get("bf16_tflops_sustained",
                                                                       peaks["bf16_tflops"]), 4)},
@@ -406,10 +415,12 @@ def run_ours(args):
             "layout_in_ms": round(statistics.mean(seg[0]), 4),
             "layout_in_GBs": round(layout_in_bytes / (statistics.mean(seg[0]) * 1e-3) / 1e9, 1),
             "attention_ms": round(attn_ms, 4), "attention_TFLOPs": round(achieved, 1),
-            "layout_out_ms": round(statistics.mean(seg[2]), 4),
-            "layout_out_GBs": round(layout_out_bytes / (statistics.mean(seg[2]) * 1e-3) / 1e9, 1),
-            "cfg_ms": round(statistics.mean(seg[3]), 4),
-            "cfg_GBs": round(cfg_bytes / (statistics.mean(seg[3]) * 1e-3) / 1e9, 1),
+            **({"merge_ms": round(statistics.mean(seg[2]), 4),
+                "merge_GBs": round(merge_bytes / (statistics.mean(seg[2]) * 1e-3) / 1e9, 1)} if w.R > 1 else {}),
+            "layout_out_ms": round(statistics.mean(seg[3]), 4),
+            "layout_out_GBs": round(layout_out_bytes / (statistics.mean(seg[3]) * 1e-3) / 1e9, 1),
+            "cfg_ms": round(statistics.mean(seg[4]), 4),
+            "cfg_GBs": round(cfg_bytes / (statistics.mean(seg[4]) * 1e-3) / 1e9, 1),
             "hbm_peak_GBs": peaks.get("hbm_gbs"),
             "step_graph_ms": round(graph_ms, 4),
             "step_eager_ms": round(eager_ms, 4),
