@@ -559,6 +559,19 @@ def back_to_back(w, U, dev):
     ib, ob = (4 if cfg_in == torch.float32 else 2), (4 if cfg_out == torch.float32 else 2)
     res["cfg"] = timed(2 * n * ib, lambda: (rnd(w.cfg_shape, cfg_in), torch.empty(w.cfg_shape[1:], dtype=cfg_out, device=dev)),
                        lambda x: sa.dit_cfg_combine(x[0], x[1], w.g), n * (2 * ib + ob))
+    # the ring merge on the FLUX-1008-like partials (R = 2, the step's only
+    # R > 1 bandwidth kernel at this scale): fp32 parts and LSE in, bf16 out
+    import synth
+    wm = synth.WORKLOADS["flux1008"]
+    Lm = sa.dit_sp_layout_init(wm.B, wm.S, wm.H, wm.D, max(wm.U), wm.R)
+    R, cap, rl = wm.R, Lm.S_cap, Lm.ring_len
+    mbytes = sum(rl) * wm.B * wm.H * (R * (wm.D * 4 + 4) + wm.D * 2)
+    res["merge_flux1008"] = timed(
+        R * R * wm.B * cap * wm.H * wm.D * 4,
+        lambda: (torch.randn((R, R, wm.B, cap, wm.H, wm.D), generator=gen, device=dev),
+                 torch.randn((R, R, wm.B, wm.H, cap), generator=gen, device=dev),
+                 torch.empty((R, wm.B, cap, wm.H, wm.D), dtype=torch.bfloat16, device=dev)),
+        lambda x: sa.dit_attn_merge_lse(x[0], x[1], x[2], None, rl), mbytes)
     return {"back_to_back": res}
 
 
