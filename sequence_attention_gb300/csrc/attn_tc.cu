@@ -77,6 +77,7 @@ struct TcParams {
     int q_row0[DIT_MAX_R];          // first output row of query block r (packed sequences)
     int B, n_q, n_kv;
     int diag;                       // query block r attends key block r only
+    int nsm;                        // SMs of the device (CTAs in flight: one per SM)
     float c;                      // scale * log2(e)
     uint32_t idesc_qk, idesc_pv;
     dit_view o;
@@ -289,6 +290,46 @@ __device__ __forceinline__ Cta cta_coords(const TcParams& p) {
 
 // The partial (r, j) of an empty key block: O = 0 and lse = -inf for the
 // CTA's rows, one row per thread of the two softmax warpgroups.
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+// The CTAs of a wave run in step: they all start, and fetch their Q and the
+// first K and V tiles of new heads from DRAM, at once, while in the key loop
+// K and V come from L2 and DRAM idles.  Halfway through its key loop a CTA
+// therefore prefetches into L2 what the first Q K^T and P V of the CTA one
+// SM count further in launch order read (usually one of the next wave):
+// both Q tiles and the first K and V tiles.  A hint only; nothing waits on
+// it.
+template <int D, bool WALK>
+__device__ __forceinline__ void prefetch_next_cta(const TcParams& p) {
+    const unsigned long long gx = gridDim.x, gy = gridDim.y, gz = gridDim.z;
+    const unsigned long long L = blockIdx.x + gx * (blockIdx.y + gy * blockIdx.z) + (unsigned long long)p.nsm;
+    if (L >= gx * gy * gz) return;
+    const int x = (int)(L % gx), h = (int)((L / gx) % gy), z = (int)(L / (gx * gy));
+    const int b = z % p.B;
+    int j, r;
+    if (WALK) {          // the walk starts at its first block with keys
+        r = z / p.B;
+        for (j = 0; j < p.n_kv && p.kv_len[j] == 0; ++j) {
+        }
+        if (j == p.n_kv) return;
+    } else {
+        j = p.diag ? z / p.B : (z / p.B) % p.n_kv;
+        r = p.diag ? j : z / (p.B * p.n_kv);
+    }
+    const int row_base = x * (NQT * BM);
+    if (row_base >= p.q_len[r] || p.kv_len[j] == 0) return;
+    for (int c = 0; c < D / 64; ++c) {
+        for (int t = 0; t < NQT; ++t) tma_prefetch_4d(&p.qmap[r], c * 64, h, row_base + t * BM, b);
+        tma_prefetch_4d(&p.kmap[j], c * 64, h, 0, b);
+        tma_prefetch_4d(&p.vmap[j], c * 64, h, 0, b);
+    }
+}
+
 template <int D>
 __device__ __forceinline__ void write_empty_partial(const TcParams& p, int r, int j, int b, int h, int row_base) {
     if (threadIdx.x >= NQT * BM) return;
@@ -348,7 +389,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     const Ctl ctl{abort_flag, p.status};
     auto bar = [&](int i) { return su32(bars + i); };
 
-    if (threadIdx.x == 0) {
+    // The K producer's thread sets up the barriers and at once issues what the
+    // first Q K^T needs, both Q tiles and K tile 0, so that those loads
+    // overlap the TMEM allocation and the block-wide barrier.  The other K and
+    // V stages wait until Q has landed (see the producers): issued together,
+    // the CTA's first 224 KB of loads kept Q and K tile 0 waiting ~5000
+    // cycles behind tiles needed thousands of cycles later.
+    if (warp == 8 && lane == 0) {
         mbar_init(bar(B_Q), 1);
         for (int s = 0; s < NSK; ++s) {
             mbar_init(bar(B_KF + s), 1);
@@ -366,6 +413,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        pdl_wait();      // the inputs may come from the previous kernel
+        const CUtensorMap* qm = &p.qmap[r];
+        mbar_expect_tx(bar(B_Q), NQT * TILE);
+        for (int t = 0; t < NQT; ++t)
+            for (int c = 0; c < NCH; ++c)
+                tma_load_4d(su32(sQ + t * TILE + c * CHUNK), qm, c * 64, h, row_base + t * BM, b, bar(B_Q));
+        mbar_expect_tx(bar(B_KF), TILE);
+        for (int c = 0; c < NCH; ++c) tma_load_4d(su32(sK + c * CHUNK), &p.kmap[j], c * 64, h, 0, b, bar(B_KF));
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
@@ -389,18 +444,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             const int nst = is_k ? NSK : NSV;
             const int full = is_k ? B_KF : B_VF, empty = is_k ? B_KE : B_VE;
             uint8_t* ring = is_k ? sK : sV;
-            if (is_k) {
-                const CUtensorMap* qm = &p.qmap[r];
-                mbar_expect_tx(bar(B_Q), NQT * TILE);
-                for (int t = 0; t < NQT; ++t)
-                    for (int c = 0; c < NCH; ++c)
-                        tma_load_4d(su32(sQ + t * TILE + c * CHUNK), qm, c * 64, h, row_base + t * BM, b, bar(B_Q));
-            }
-            int issued = 0;
-            bool ok = true;
-            for (int n = 0; n < ntiles; ++n) {
+            // Q and K tile 0 went out before the block barrier
+            int issued = is_k ? 1 : 0;
+            bool ok = wait_phase(bar(B_Q), 0, ctl);
+            for (int n = issued; n < ntiles && ok; ++n) {
                 const int s = n % nst;
                 const uint32_t ph = (n / nst) & 1;
+                if (is_k && n == ntiles / 2) prefetch_next_cta<D, false>(p);
                 if (n >= nst && !(ok = wait_phase(bar(empty + s), ph ^ 1, ctl))) break;
                 mbar_expect_tx(bar(full + s), TILE);
                 for (int c = 0; c < NCH; ++c)
@@ -742,6 +792,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
             const int nst = is_k ? NSK : NSV;
             const int full = is_k ? B_KF : B_VF, empty = is_k ? B_KE : B_VE;
             uint8_t* ring = is_k ? sK : sV;
+            int total = 0;                                  // key tiles over every block
+            for (int jj = 0; jj < nj; ++jj) total += (p.kv_len[j0 + jj] + BN - 1) / BN;
+            // Q and the first K tile go first; the other stages wait until Q
+            // has landed, so they do not compete with what the first Q K^T
+            // needs
             if (is_k) {
                 const CUtensorMap* qm = &p.qmap[r];
                 mbar_expect_tx(bar(B_Q), NQT * TILE);
@@ -758,6 +813,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
                 for (int n = 0; n < nt; ++n, ++g) {
                     const int s = g % nst;
                     const uint32_t ph = (g / nst) & 1;
+                    if (g == (is_k ? 1 : 0) && !(ok = wait_phase(bar(B_Q), 0, ctl))) break;
+                    if (is_k && g == total / 2) prefetch_next_cta<D, true>(p);
                     if (g >= nst && !(ok = wait_phase(bar(empty + s), ph ^ 1, ctl))) break;
                     mbar_expect_tx(bar(full + s), TILE);
                     for (int c = 0; c < NCH; ++c)
@@ -1177,7 +1234,7 @@ dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
                          a.v.stride_b);
     }
     if (s == DIT_OK && maxq > 0) {
-        prm->B = a.B; prm->n_q = a.n_q; prm->n_kv = a.n_kv; prm->diag = a.diag;
+        prm->B = a.B; prm->n_q = a.n_q; prm->n_kv = a.n_kv; prm->diag = a.diag; prm->nsm = num_sms();
         prm->c = a.scale * 1.4426950408889634f;
         prm->idesc_qk = make_idesc(a.qk_dt == DIT_BF16, false, BN, BM);
         prm->idesc_pv = make_idesc(a.v_dt == DIT_BF16, true, a.D, BM);
