@@ -225,6 +225,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&x)[32]) {
         : "r"(taddr)
         : "memory");
 }
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&x)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31]), "=r"(x[32]), "=r"(x[33]), "=r"(x[34]), "=r"(x[35]), "=r"(x[36]), "=r"(x[37]), "=r"(x[38]), "=r"(x[39]), "=r"(x[40]), "=r"(x[41]), "=r"(x[42]), "=r"(x[43]), "=r"(x[44]), "=r"(x[45]), "=r"(x[46]), "=r"(x[47]), "=r"(x[48]), "=r"(x[49]), "=r"(x[50]), "=r"(x[51]), "=r"(x[52]), "=r"(x[53]), "=r"(x[54]), "=r"(x[55]), "=r"(x[56]), "=r"(x[57]), "=r"(x[58]), "=r"(x[59]), "=r"(x[60]), "=r"(x[61]), "=r"(x[62]), "=r"(x[63])
+        : "r"(taddr)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&x)[128]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
@@ -653,50 +661,62 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             // Shared addresses are recomputed from the array's own address
             // (the aligned base is at a fixed offset in the shared window)
             // instead of keeping the generic pointers live through the loop.
+            // The warp's 32 rows of box bx sit at wbase + bx*BM*128.
             const uint32_t sbase = (su32(smem_raw) + 1023u) & ~1023u;
-            const uint32_t stage = sbase + (uint32_t)(t * BM * D * eb) + (uint32_t)rt * 128u;
-            auto chunk = [&](int c) { return stage + (uint32_t)((c >> 3) * BM * 128) + (uint32_t)(((c & 7) ^ (rt & 7)) << 4); };
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {     // 32 columns of O at a time
-                uint32_t x[32];
-                tmem_ld32(Ot + cc * 32, x);
-                if (p.o_dt == DIT_F32) {
+            const uint32_t wbase = sbase + (uint32_t)(t * BM * D * eb + q4 * 32 * 128);
+            const uint32_t myrow = wbase + (uint32_t)lane * 128u;
+            const int grow = e.row_base + t * BM + q4 * 32, gj = p.diag ? 0 : e.j;
+            uint32_t x[D];
+            if constexpr (D == 128) tmem_ld128(Ot, x); else tmem_ld64(Ot, x);   // the whole O row, one round trip
+            // each box goes out as soon as it is staged, so its store overlaps
+            // the staging of the next
+            auto store_box = [&](int bx) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_5d(&p.omap[e.r], wbase + (uint32_t)(bx * BM * 128), bx * (128 / eb), e.h, grow, e.b, gj);
+                    bulk_commit();
+                }
+            };
+            if (p.o_dt == DIT_F32) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        st_shared16(chunk(cc * 8 + c), __float_as_uint(__uint_as_float(x[4 * c]) * inv),
-                                    __float_as_uint(__uint_as_float(x[4 * c + 1]) * inv),
-                                    __float_as_uint(__uint_as_float(x[4 * c + 2]) * inv),
-                                    __float_as_uint(__uint_as_float(x[4 * c + 3]) * inv));
-                } else {
+                for (int bx = 0; bx < D / 32; ++bx) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int k = 0; k < 8; ++k) {
+                        const int i = bx * 32 + 4 * k;
+                        st_shared16(myrow + (uint32_t)(bx * BM * 128) + (uint32_t)((k ^ (lane & 7)) << 4),
+                                    __float_as_uint(__uint_as_float(x[i]) * inv),
+                                    __float_as_uint(__uint_as_float(x[i + 1]) * inv),
+                                    __float_as_uint(__uint_as_float(x[i + 2]) * inv),
+                                    __float_as_uint(__uint_as_float(x[i + 3]) * inv));
+                    }
+                    store_box(bx);
+                }
+            } else {
+#pragma unroll
+                for (int bx = 0; bx < D / 64; ++bx) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int i = bx * 64 + 8 * k;
                         uint32_t w[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = pack2(__uint_as_float(x[8 * c + 2 * e]) * inv,
-                                         __uint_as_float(x[8 * c + 2 * e + 1]) * inv, p.o_dt);
-                        st_shared16(chunk(cc * 4 + c), w[0], w[1], w[2], w[3]);
+                        for (int q = 0; q < 4; ++q)
+                            w[q] = pack2(__uint_as_float(x[i + 2 * q]) * inv, __uint_as_float(x[i + 2 * q + 1]) * inv,
+                                         p.o_dt);
+                        st_shared16(myrow + (uint32_t)(bx * BM * 128) + (uint32_t)((k ^ (lane & 7)) << 4), w[0], w[1],
+                                    w[2], w[3]);
                     }
+                    store_box(bx);
                 }
             }
-            // each warp stores its own 32 rows: no wait on the other warps
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
             const int row = e.row_base + t * BM + rt;
             if (p.lse.ptr && row < p.q_len[e.r])
                 p.lse.ptr[e.r * p.lse.stride_q + e.j * p.lse.stride_kv + e.b * p.lse.stride_b + e.h * p.lse.stride_h +
                           p.q_row0[e.r] + row] = (m_used + log2f(l)) * 0.69314718055994531f;
-            if (lane == 0) {
-                const int nbox = D * eb / 128;
-                for (int bx = 0; bx < nbox; ++bx)
-                    tma_store_5d(&p.omap[e.r], sbase + (uint32_t)(t * BM * D * eb + bx * BM * 128 + q4 * 32 * 128),
-                                 bx * (128 / eb), e.h, e.row_base + t * BM + q4 * 32, e.b, p.diag ? 0 : e.j);
-                bulk_commit();
-                // the shared-memory source must stay until the copy has read
-                // it; the global writes complete with the grid, before any
-                // dependent kernel passes its griddepcontrol.wait
-                bulk_wait_read();
-            }
+            // the shared-memory source must stay until the copies have read
+            // it; the global writes complete with the grid, before any
+            // dependent kernel passes its griddepcontrol.wait
+            if (lane == 0) bulk_wait_read();
         }
     }
 
@@ -1043,54 +1063,56 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
             // The output goes through shared memory (per 128 bytes of d, rows
             // of 128 bytes, 16-byte chunks swizzled by row mod 8) and a TMA
             // store of each warp's 32 rows; rows past the block's length are
-            // clipped by the output map.
-            const int nbox = D * eb / 128;
-            auto put = [&](uint32_t rowaddr, int cbase, const uint32_t* x32, int half) {
-                // chunk k (0..7) of this row's 128-byte box line
-                if (p.o_dt == DIT_F32) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        st_shared16(rowaddr + (uint32_t)(((cbase + k) ^ (rt & 7)) << 4),
-                                    __float_as_uint(__uint_as_float(x32[4 * k]) * inv),
-                                    __float_as_uint(__uint_as_float(x32[4 * k + 1]) * inv),
-                                    __float_as_uint(__uint_as_float(x32[4 * k + 2]) * inv),
-                                    __float_as_uint(__uint_as_float(x32[4 * k + 3]) * inv));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            w[q] = pack2(__uint_as_float(x32[8 * k + 2 * q]) * inv,
-                                         __uint_as_float(x32[8 * k + 2 * q + 1]) * inv, p.o_dt);
-                        st_shared16(rowaddr + (uint32_t)(((cbase + half * 4 + k) ^ (rt & 7)) << 4), w[0], w[1], w[2],
-                                    w[3]);
-                    }
-                }
-            };
-            // each warp's own slot, one 128-byte column box at a time: the
-            // Q, K and V buffers are still in use by the next block
+            // clipped by the output map.  The warp's own slot takes one
+            // 128-byte column box at a time (the Q, K and V buffers are still
+            // in use by the next block); the O row comes from TMEM in one
+            // round trip.
             const uint32_t slot = sbase + (uint32_t)((NQT + NSK + NSV) * TILE + we * kSlot);
-#pragma unroll 1
-            for (int bx = 0; bx < nbox; ++bx) {
+            const uint32_t myrow = slot + (uint32_t)le * 128u;
+            const int grow = e.row_base + te * BM + (rt & ~31);
+            uint32_t x[D];
+            if constexpr (D == 128) tmem_ld128(Ot, x); else tmem_ld64(Ot, x);
+            auto open_slot = [&]() {
                 if (le == 0) bulk_wait_read();     // the slot's last store has read it
                 __syncwarp();
-                uint32_t x[32];
-                if (p.o_dt == DIT_F32) {
-                    tmem_ld32(Ot + bx * 32, x);
-                    put(slot + (uint32_t)le * 128u, 0, x, 0);
-                } else {
-#pragma unroll 1
-                    for (int hf = 0; hf < 2; ++hf) {
-                        tmem_ld32(Ot + bx * 64 + hf * 32, x);
-                        put(slot + (uint32_t)le * 128u, 0, x, hf);
-                    }
-                }
+            };
+            auto store_box = [&](int bx) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (le == 0) {
-                    tma_store_5d(&p.omap[e.r], slot, bx * (128 / eb), e.h, e.row_base + te * BM + (rt & ~31), e.b, j);
+                    tma_store_5d(&p.omap[e.r], slot, bx * (128 / eb), e.h, grow, e.b, j);
                     bulk_commit();
+                }
+            };
+            if (p.o_dt == DIT_F32) {
+#pragma unroll
+                for (int bx = 0; bx < D / 32; ++bx) {
+                    open_slot();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int i = bx * 32 + 4 * k;
+                        st_shared16(myrow + (uint32_t)((k ^ (le & 7)) << 4), __float_as_uint(__uint_as_float(x[i]) * inv),
+                                    __float_as_uint(__uint_as_float(x[i + 1]) * inv),
+                                    __float_as_uint(__uint_as_float(x[i + 2]) * inv),
+                                    __float_as_uint(__uint_as_float(x[i + 3]) * inv));
+                    }
+                    store_box(bx);
+                }
+            } else {
+#pragma unroll
+                for (int bx = 0; bx < D / 64; ++bx) {
+                    open_slot();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int i = bx * 64 + 8 * k;
+                        uint32_t w[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            w[q] = pack2(__uint_as_float(x[i + 2 * q]) * inv, __uint_as_float(x[i + 2 * q + 1]) * inv,
+                                         p.o_dt);
+                        st_shared16(myrow + (uint32_t)((k ^ (le & 7)) << 4), w[0], w[1], w[2], w[3]);
+                    }
+                    store_box(bx);
                 }
             }
         }
