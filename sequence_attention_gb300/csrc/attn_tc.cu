@@ -352,6 +352,85 @@ __device__ __forceinline__ void write_empty_partial(const TcParams& p, int r, in
                   row] = -INFINITY;
 }
 
+// One key tile of the online softmax for the calling thread's query row
+// (its TMEM lane): S (fp32, columns St) becomes P (16-bit, written over the
+// first half of S); the reference max m (log2 domain) and the row sum l are
+// updated, and O (columns Ot) is rescaled when the row max grows by more
+// than 2^8, so P stays <= 256.  Keys at or past `valid` are masked to -inf;
+// `first` marks the first tile of a key block.  Returns once P and any O
+// rescale are in TMEM and ordered before the caller's "P written" arrive.
+template <int D, bool P_BF16>
+__device__ __forceinline__ void softmax_tile(uint32_t St, uint32_t Ot, int valid, bool first, float c, float& m_used,
+                                             float& l) {
+    uint32_t x[BN];
+    tmem_ld128(St, x);                       // the whole score row, one round trip
+    if (valid < BN) {                        // keys past the block: -inf
+#pragma unroll
+        for (int e = 0; e < BN; ++e)
+            if (e >= valid) x[e] = 0xff800000u;
+    }
+    // row max: 8 independent chains of three-input max over columns 8 .. BN-9,
+    // then the last 8 columns with a two-input max
+    static_assert(BN % 16 == 0, "the max chains take 16 columns per step");
+    float m8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(x[e]);
+#pragma unroll
+    for (int e = 8; e + 16 <= BN; e += 16)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m8[q] = max3(m8[q], __uint_as_float(x[e + q]), __uint_as_float(x[e + 8 + q]));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m8[q] = fmaxf(m8[q], __uint_as_float(x[BN - 8 + q]));
+    const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+    const float mxs = mx * c;
+    float alpha = 1.f;
+    bool rescale = false;
+    if (first) {
+        m_used = mxs;
+    } else if (__any_sync(0xffffffffu, mxs > m_used + 8.f)) {
+        // Raise the reference max; O is rescaled below, after P is written
+        // (this tile's P V is not issued before the caller's arrive).
+        const float mnew = fmaxf(m_used, mxs);
+        alpha = ex2(m_used - mnew);
+        m_used = mnew;
+        rescale = true;
+    }
+    // P = 2^(s*c - m) (packed fp32 pairs), row sum in 4 packed chains, P
+    // written over S in two halves
+    const float2 c2 = make_float2(c, c), negm2 = make_float2(-m_used, -m_used);
+    float2 l2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) l2[e] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        // each half's TMEM store runs while the next half is computed
+        uint32_t pk[BN / 4];
+#pragma unroll
+        for (int e = 0; e < BN / 4; ++e) {
+            const int i0 = half * (BN / 2) + 2 * e;
+            const float2 a = __ffma2_rn(make_float2(__uint_as_float(x[i0]), __uint_as_float(x[i0 + 1])), c2, negm2);
+            const float2 pp = make_float2(ex2(a.x), ex2(a.y));
+            l2[e & 3] = __fadd2_rn(l2[e & 3], pp);
+            pk[e] = pack_p<P_BF16>(pp.x, pp.y);
+        }
+        tmem_st32(St + half * (BN / 4), pk);
+    }
+    l = fmaf(l, alpha, ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) + ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y)));
+    if (rescale) {
+        // the previous P V of this tile completed before S became ready
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t y[32];
+            tmem_ld32(Ot + cc * 32, y);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) y[e] = __float_as_uint(__uint_as_float(y[e]) * alpha);
+            tmem_st32(Ot + cc * 32, y);
+        }
+    }
+    tmem_wait_st();
+    tc_fence_before();
+}
+
 // ---- the kernels ------------------------------------------------------------
 // attn_tc_kernel: one partial (r, j) per CTA.
 template <int D, bool P_BF16>
@@ -565,76 +644,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             ok = __all_sync(0xffffffffu, wait_phase(bar(B_SF + t), n & 1, ctl));
             if (!ok) break;
             tc_fence_after();
-            uint32_t x[BN];
-            tmem_ld128(St, x);                       // the whole score row, one round trip
-            const int valid = kvlen - n * BN;
-            if (valid < BN) {                        // keys past the block: -inf
-#pragma unroll
-                for (int e = 0; e < BN; ++e)
-                    if (e >= valid) x[e] = 0xff800000u;
-            }
-            // row max: 8 independent chains of three-input max over columns
-            // 8 .. BN-9, then the last 8 columns with a two-input max
-            static_assert(BN % 16 == 0, "the max chains take 16 columns per step");
-            float m8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(x[e]);
-#pragma unroll
-            for (int e = 8; e + 16 <= BN; e += 16)
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    m8[j] = max3(m8[j], __uint_as_float(x[e + j]), __uint_as_float(x[e + 8 + j]));
-#pragma unroll
-            for (int j = 0; j < 8; ++j) m8[j] = fmaxf(m8[j], __uint_as_float(x[BN - 8 + j]));
-            const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-            const float mxs = mx * c;
-            float alpha = 1.f;
-            bool rescale = false;
-            if (n == 0) {
-                m_used = mxs;
-            } else if (__any_sync(0xffffffffu, mxs > m_used + 8.f)) {
-                // Raise the reference max; O is rescaled below, after P is
-                // written (this tile's P V is not issued before we arrive).
-                const float mnew = fmaxf(m_used, mxs);
-                alpha = ex2(m_used - mnew);
-                m_used = mnew;
-                rescale = true;
-            }
-            // P = 2^(s*c - m) (packed fp32 pairs), row sum in 4 packed
-            // chains, P written over S in two halves
-            const float2 c2 = make_float2(c, c), negm2 = make_float2(-m_used, -m_used);
-            float2 l2[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) l2[e] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                // each half's TMEM store runs while the next half is computed
-                uint32_t pk[BN / 4];
-#pragma unroll
-                for (int e = 0; e < BN / 4; ++e) {
-                    const int i0 = half * (BN / 2) + 2 * e;
-                    const float2 a = __ffma2_rn(make_float2(__uint_as_float(x[i0]), __uint_as_float(x[i0 + 1])),
-                                                c2, negm2);
-                    const float2 pp = make_float2(ex2(a.x), ex2(a.y));
-                    l2[e & 3] = __fadd2_rn(l2[e & 3], pp);
-                    pk[e] = pack_p<P_BF16>(pp.x, pp.y);
-                }
-                tmem_st32(St + half * (BN / 4), pk);
-            }
-            l = fmaf(l, alpha, ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) + ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y)));
-            if (rescale) {
-                // the previous P V of this tile completed before S became ready
-#pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t y[32];
-                    tmem_ld32(Ot + cc * 32, y);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) y[e] = __float_as_uint(__uint_as_float(y[e]) * alpha);
-                    tmem_st32(Ot + cc * 32, y);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
+            softmax_tile<D, P_BF16>(St, Ot, kvlen - n * BN, n == 0, c, m_used, l);
             mbar_arrive(bar(B_PF + t));
         }
         // epilogue: O / l and lse = ln(2) * (m + log2 l)
@@ -963,75 +973,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
                 ok = __all_sync(0xffffffffu, wait_phase(bar(B_SF + t), st & 1, ctl));
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t x[BN];
-                tmem_ld128(St, x);                       // the whole score row, one round trip
-                if (rem < BN) {                          // keys past the block: -inf
-#pragma unroll
-                    for (int e = 0; e < BN; ++e)
-                        if (e >= rem) x[e] = 0xff800000u;
-                }
-                // row max: 8 independent chains of three-input max over columns
-                // 8 .. BN-9, then the last 8 columns with a two-input max
-                static_assert(BN % 16 == 0, "the max chains take 16 columns per step");
-                float m8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(x[e]);
-#pragma unroll
-                for (int e = 8; e + 16 <= BN; e += 16)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        m8[q] = max3(m8[q], __uint_as_float(x[e + q]), __uint_as_float(x[e + 8 + q]));
-#pragma unroll
-                for (int q = 0; q < 8; ++q) m8[q] = fmaxf(m8[q], __uint_as_float(x[BN - 8 + q]));
-                const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-                const float mxs = mx * c;
-                float alpha = 1.f;
-                bool rescale = false;
-                if (n == 0) {
-                    m_used = mxs;
-                } else if (__any_sync(0xffffffffu, mxs > m_used + 8.f)) {
-                    // Raise the reference max; O is rescaled below, after P is
-                    // written (this tile's P V is not issued before we arrive).
-                    const float mnew = fmaxf(m_used, mxs);
-                    alpha = ex2(m_used - mnew);
-                    m_used = mnew;
-                    rescale = true;
-                }
-                // P = 2^(s*c - m) (packed fp32 pairs), row sum in 4 packed
-                // chains, P written over S in two halves
-                const float2 c2 = make_float2(c, c), negm2 = make_float2(-m_used, -m_used);
-                float2 l2[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) l2[e] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    // each half's TMEM store runs while the next half is computed
-                    uint32_t pk[BN / 4];
-#pragma unroll
-                    for (int e = 0; e < BN / 4; ++e) {
-                        const int i0 = half * (BN / 2) + 2 * e;
-                        const float2 a = __ffma2_rn(make_float2(__uint_as_float(x[i0]), __uint_as_float(x[i0 + 1])),
-                                                    c2, negm2);
-                        const float2 pp = make_float2(ex2(a.x), ex2(a.y));
-                        l2[e & 3] = __fadd2_rn(l2[e & 3], pp);
-                        pk[e] = pack_p<P_BF16>(pp.x, pp.y);
-                    }
-                    tmem_st32(St + half * (BN / 4), pk);
-                }
-                l = fmaf(l, alpha, ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) + ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y)));
-                if (rescale) {
-                    // the previous P V of this tile completed before S became ready
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t y[32];
-                        tmem_ld32(Ot + cc * 32, y);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) y[e] = __float_as_uint(__uint_as_float(y[e]) * alpha);
-                        tmem_st32(Ot + cc * 32, y);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
+                softmax_tile<D, P_BF16>(St, Ot, rem, n == 0, c, m_used, l);
                 mbar_arrive(bar(B_PF + t));
                 st ^= 1u;
             }
