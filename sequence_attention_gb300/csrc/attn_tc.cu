@@ -6,17 +6,25 @@
 // ring merge needs each call's softmax LSE; edge-dit.cpp "Parallel
 // execution": exact full-sequence attention per head).
 //
-// CTA = 256 query rows as two 128-row tiles, one (r, j, b, h).  Warp roles:
+// Two kernels share the code below.  attn_tc_kernel computes one partial
+// (r, j) per CTA (single key blocks, packed sequences); attn_tc_walk_kernel
+// lets one CTA walk every key block j of its query rows (several key
+// blocks, the ring's R partials per query block).
+//
+// CTA = 256 query rows as two 128-row tiles.  Warp roles:
 //   warps 0-3  softmax for Q tile 0 (TMEM lanes 0-127, one row per thread)
 //   warps 4-7  softmax for Q tile 1
-//   warp  8    TMA producer of Q (once) and K tiles (2-stage ring)
+//   warp  8    TMA producer of Q (once) and K tiles (2-stage ring); halfway
+//              through, the L2 prefetch of the next wave's first tiles
 //   warp  9    MMA issuer (one thread): S = Q K^T and O += P V
-//   warp  10   TMA producer of V tiles (3-stage ring); K and V loads wait on
-//              their own ring's releases, so neither holds up the other
+//   warp  10   TMA producer of V tiles (3-stage ring, 2 when walking); K and
+//              V loads wait on their own ring's releases, so neither holds up
+//              the other
 //   warp  11   idle (completes the third warpgroup)
 // Registers: launched at 168 per thread; the producer/MMA warpgroup gives
-// back down to 88 and the two softmax warpgroups take 208 each
-// (2*208 + 88 = 3*168), enough to hold a whole 128-column score row.
+// back down to 88 (104 when walking) and the two softmax warpgroups take 208
+// (200) each (2*208 + 88 = 2*200 + 104 = 3*168), enough to hold a whole
+// 128-column score row.
 // TMEM (512 columns x 128 lanes, fp32): S0 [0,128) S1 [128,256)
 // O0 [256,256+D) O1 [256+D,256+2D).  P (16-bit) overwrites the first half
 // of its tile's S columns and feeds the P V MMA straight from TMEM.
@@ -31,9 +39,10 @@
 // rounding.  Keys at or past the block's valid length are masked to -inf;
 // TMA zero-fills rows past each block's extent, so padding bytes in the
 // buffers are never read.
-// The epilogue writes O / l into the (by then free) Q and K buffers and
-// stores it with TMA, each warp its 32 rows; the output map has the block's
-// own extents, so no row past the block is written.
+// The epilogue writes O / l through shared memory (the then free Q and K
+// buffers, or per-warp slots when walking) and TMA stores, each warp its 32
+// rows; the output map has the block's own extents, so no row past the
+// block is written.
 //
 // Every mbarrier wait is bounded (a few seconds of %globaltimer); on expiry
 // the CTA records DIT_ERR_TIMEOUT in the status word, stops issuing work,
