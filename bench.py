@@ -502,6 +502,7 @@ def back_to_back(w, U, dev):
     which weighs most on the short CFG launch."""
     import torch
     import sequence_attention_gb300 as sa
+    import synth
     L = sa.dit_sp_layout_init(w.B, w.S, w.H, w.D, U, w.R)
     dt = torch.bfloat16 if w.dtype != "f32" else torch.float32
     eb = 2 if w.dtype != "f32" else 4
@@ -559,9 +560,29 @@ def back_to_back(w, U, dev):
     ib, ob = (4 if cfg_in == torch.float32 else 2), (4 if cfg_out == torch.float32 else 2)
     res["cfg"] = timed(2 * n * ib, lambda: (rnd(w.cfg_shape, cfg_in), torch.empty(w.cfg_shape[1:], dtype=cfg_out, device=dev)),
                        lambda x: sa.dit_cfg_combine(x[0], x[1], w.g), n * (2 * ib + ob))
+    # the receive preparation with RoPE on Q and K, and the e4m3 wire of Q
+    # and V (records of D + 16 bytes per token and head), on these shapes
+    cos, sin = synth.rope_tables_linear(w.S, w.D)
+    cos, sin = cos.to(dev), sin.to(dev)
+    res["unpack_rope_s2h"] = timed(
+        wire3, lambda: (rnd(L.wire_elems(3)), [torch.empty(hs, dtype=t, device=dev) for t in (dt, dt, v_dt)]),
+        lambda x: sa.dit_ulysses_unpack_rope(L, x[0], x[1], cos, sin, 0b011, flag), 2 * wire3 + 2 * w.S * w.D * 4)
+    rec = 2 * w.B * L.S_pad * L.Hp * (w.D + 16)
+    nrec = L.wire_bytes_e4m3(2)
+    res["pack_e4m3_qv"] = timed(2 * plane, lambda: ([rnd(shp), rnd(shp)], torch.empty(nrec, dtype=torch.uint8, device=dev)),
+                                lambda x: sa.dit_ulysses_pack(L, S2H, x[0], x[1]), 2 * plane + rec)
+    res["a2a_e4m3_qv"] = timed(nrec, lambda: (torch.randint(0, 120, (nrec,), dtype=torch.uint8, device=dev),
+                                              torch.empty(nrec, dtype=torch.uint8, device=dev)),
+                               lambda x: sa.dit_a2a_sim(L, S2H, 2, x[0], x[1]), 2 * rec)
+    def packed_records():
+        src = [rnd(shp), rnd(shp)]
+        buf = torch.empty(nrec, dtype=torch.uint8, device=dev)
+        sa.dit_ulysses_pack(L, S2H, src, buf)
+        return (buf, [torch.empty(hs, dtype=dt, device=dev), torch.empty(hs, dtype=v_dt, device=dev)])
+    res["unpack_e4m3_qv"] = timed(nrec, packed_records, lambda x: sa.dit_ulysses_unpack(L, S2H, x[0], x[1]),
+                                  rec + 2 * (wire3 // 3))
     # the ring merge on the FLUX-1008-like partials (R = 2, the step's only
     # R > 1 bandwidth kernel at this scale): fp32 parts and LSE in, bf16 out
-    import synth
     wm = synth.WORKLOADS["flux1008"]
     Lm = sa.dit_sp_layout_init(wm.B, wm.S, wm.H, wm.D, max(wm.U), wm.R)
     R, cap, rl = wm.R, Lm.S_cap, Lm.ring_len
