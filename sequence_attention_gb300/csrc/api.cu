@@ -81,6 +81,7 @@ extern "C" const char* dit_status_string(dit_status s) {
 extern "C" const char* dit_last_error(void) { return g_msg; }
 
 extern "C" dit_status dit_device_status(int* out_code, int reset) {
+    NvtxRange nvtx_range("dit_device_status");
     if (!out_code) return fail(DIT_ERR_INVALID_ARG, "dit_device_status: out_code is NULL");
     int* p = default_status_word();
     if (!p) return fail(DIT_ERR_CUDA, "dit_device_status: no device status word");
@@ -108,6 +109,7 @@ static void split(int S, int n, int* len, int* off, int base) {
 
 extern "C" dit_status dit_sp_layout_init_ex(int B, int S, int H, int D, int U, int R, int flags,
                                             dit_sp_layout* out) {
+    NvtxRange nvtx_range("dit_sp_layout_init_ex");
     if (!out) return fail(DIT_ERR_INVALID_ARG, "dit_sp_layout_init: out is NULL");
     if (B < 1 || H < 1 || D < 1 || S < 0)
         return fail(DIT_ERR_INVALID_ARG, "dit_sp_layout_init: need B,H,D >= 1 and S >= 0");
@@ -156,12 +158,14 @@ extern "C" dit_status dit_sp_layout_init_ex(int B, int S, int H, int D, int U, i
 }
 
 extern "C" dit_status dit_sp_layout_init(int B, int S, int H, int D, int U, int R, dit_sp_layout* out) {
+    NvtxRange nvtx_range("dit_sp_layout_init");
     return dit_sp_layout_init_ex(B, S, H, D, U, R, 0, out);
 }
 
 extern "C" dit_status dit_sp_a2a_counts(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
                                         int rank, int64_t* sc, int64_t* sd, int64_t* rc,
                                         int64_t* rd) {
+    NvtxRange nvtx_range("dit_sp_a2a_counts");
     if (!L || !sc || !sd || !rc || !rd)
         return fail(DIT_ERR_INVALID_ARG, "dit_sp_a2a_counts: NULL argument");
     if (nplanes < 1 || nplanes > 3 || rank < 0 || rank >= L->U * L->R)

@@ -70,6 +70,7 @@ extern "C" dit_status dit_attn_partial(int B, int H, int D, float scale, int n_q
                                        const int* kv_len, dit_view q, dit_dtype qk_dt, dit_view k, dit_view v,
                                        dit_dtype v_dt, dit_view o, dit_dtype o_dt, dit_lse_view lse,
                                        int* d_status, void* stream) {
+    NvtxRange nvtx_range("dit_attn_partial");
     if (!q_len || !kv_len) return fail(DIT_ERR_INVALID_ARG, "dit_attn_partial: NULL length array");
     if (n_q < 1 || n_q > DIT_MAX_R || n_kv < 1 || n_kv > DIT_MAX_R)
         return fail(DIT_ERR_INVALID_ARG, "dit_attn_partial: need 1 <= n_q, n_kv <= %d", DIT_MAX_R);
@@ -86,6 +87,7 @@ extern "C" dit_status dit_attn_partial(int B, int H, int D, float scale, int n_q
 extern "C" dit_status dit_attention(int B, int H, int D, float scale, int Sq, int Sk, dit_view q, dit_dtype qk_dt,
                                     dit_view k, dit_view v, dit_dtype v_dt, dit_view o, dit_dtype o_dt,
                                     dit_lse_view lse, int* d_status, void* stream) {
+    NvtxRange nvtx_range("dit_attention");
     AttnArgs a;
     memset(&a, 0, sizeof(a));
     a.B = B; a.H = H; a.D = D; a.n_q = 1; a.n_kv = 1; a.scale = scale;
@@ -103,6 +105,7 @@ extern "C" dit_status dit_attention(int B, int H, int D, float scale, int Sq, in
 extern "C" dit_status dit_attn_varlen(int H, int D, float scale, int nseq, const int* cu_q, const int* cu_k,
                                       dit_view q, dit_dtype qk_dt, dit_view k, dit_view v, dit_dtype v_dt,
                                       dit_view o, dit_dtype o_dt, dit_lse_view lse, int* d_status, void* stream) {
+    NvtxRange nvtx_range("dit_attn_varlen");
     const char* who = "dit_attn_varlen";
     if (nseq < 0) return fail(DIT_ERR_INVALID_ARG, "%s: negative sequence count", who);
     if (nseq == 0) return DIT_OK;

@@ -246,6 +246,7 @@ using namespace ditsp;
 
 extern "C" dit_status dit_cfg_combine(const void* pred, dit_dtype in_dt, int64_t N, float g, void* out,
                                       dit_dtype out_dt, void* stream) {
+    NvtxRange nvtx_range("dit_cfg_combine");
     const char* who = "dit_cfg_combine";
     if (!dtype_ok(in_dt) || !dtype_ok(out_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
     if (N < 0) return fail(DIT_ERR_INVALID_ARG, "%s: N < 0", who);
@@ -290,6 +291,7 @@ extern "C" dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int
                                          dit_view parts, dit_dtype parts_dt, dit_lse_view lse_parts,
                                          dit_view out, dit_dtype out_dt, dit_lse_view lse_out,
                                          void* stream) {
+    NvtxRange nvtx_range("dit_attn_merge_lse");
     const char* who = "dit_attn_merge_lse";
     if (B < 1 || H < 1 || D < 8 || D % 8 != 0)
         return fail(DIT_ERR_INVALID_ARG, "%s: need B,H >= 1 and D a positive multiple of 8", who);

@@ -11,7 +11,18 @@
 
 #include "ditsp.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace ditsp {
+
+// NVTX range around one ABI call: names the call on a profiler timeline
+// (Nsight Systems); without a tool attached each push/pop is a no-op.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ---- host-side error reporting (thread-local message) ----------------------
 dit_status fail(dit_status s, const char* fmt, ...);

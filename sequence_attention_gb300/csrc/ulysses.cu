@@ -466,6 +466,7 @@ using namespace ditsp;
 extern "C" dit_status dit_ulysses_pack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
                                        const void* const* src, dit_dtype src_dt, void* send,
                                        dit_dtype wire_dt, void* stream) {
+    NvtxRange nvtx_range("dit_ulysses_pack");
     const char* who = "dit_ulysses_pack";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
@@ -493,6 +494,7 @@ extern "C" dit_status dit_ulysses_pack(const dit_sp_layout* L, dit_a2a_dir dir, 
 
 extern "C" dit_status dit_a2a_sim(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
                                   const void* send, void* recv, dit_dtype wire_dt, void* stream) {
+    NvtxRange nvtx_range("dit_a2a_sim");
     const char* who = "dit_a2a_sim";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
@@ -516,6 +518,7 @@ extern "C" dit_status dit_a2a_sim(const dit_sp_layout* L, dit_a2a_dir dir, int n
 extern "C" dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
                                          const void* recv, dit_dtype wire_dt, void* const* dst,
                                          const dit_dtype* dst_dt, int* d_range_flag, void* stream) {
+    NvtxRange nvtx_range("dit_ulysses_unpack");
     const char* who = "dit_ulysses_unpack";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
@@ -546,6 +549,7 @@ extern "C" dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir
 
 extern "C" dit_status dit_sp_signal(const dit_sp_layout* L, unsigned* d_arrival, const unsigned char* rank_mask,
                                     unsigned epoch, void* stream) {
+    NvtxRange nvtx_range("dit_sp_signal");
     const char* who = "dit_sp_signal";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
@@ -563,6 +567,7 @@ extern "C" dit_status dit_sp_signal(const dit_sp_layout* L, unsigned* d_arrival,
 extern "C" dit_status dit_a2a_sim_checked(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, const void* send,
                                           void* recv, dit_dtype wire_dt, const unsigned* d_arrival, unsigned epoch,
                                           int64_t timeout_ns, int* d_status, void* stream) {
+    NvtxRange nvtx_range("dit_a2a_sim_checked");
     const char* who = "dit_a2a_sim_checked";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
@@ -595,6 +600,7 @@ extern "C" dit_status dit_a2a_sim_checked(const dit_sp_layout* L, dit_a2a_dir di
 extern "C" dit_status dit_ulysses_pack_joint(const dit_sp_layout* L, int nplanes, const void* const* txt,
                                              const void* const* img, int S_txt, dit_dtype src_dt, void* send,
                                              dit_dtype wire_dt, void* stream) {
+    NvtxRange nvtx_range("dit_ulysses_pack_joint");
     const char* who = "dit_ulysses_pack_joint";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
@@ -630,6 +636,7 @@ extern "C" dit_status dit_ulysses_pack_joint(const dit_sp_layout* L, int nplanes
 extern "C" dit_status dit_ulysses_unpack_joint(const dit_sp_layout* L, const void* recv, dit_dtype wire_dt,
                                                void* out_txt, void* out_img, int S_txt, dit_dtype out_dt,
                                                void* stream) {
+    NvtxRange nvtx_range("dit_ulysses_unpack_joint");
     const char* who = "dit_ulysses_unpack_joint";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
@@ -659,6 +666,7 @@ extern "C" dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplane
                                               dit_dtype wire_dt, void* const* dst, const dit_dtype* dst_dt,
                                               const float* cos_tab, const float* sin_tab, unsigned rope_planes,
                                               int* d_range_flag, void* stream) {
+    NvtxRange nvtx_range("dit_ulysses_unpack_rope");
     const char* who = "dit_ulysses_unpack_rope";
     dit_status s = check_layout(L, who);
     if (s != DIT_OK) return s;
