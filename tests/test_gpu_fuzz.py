@@ -23,10 +23,20 @@ def _case(seed):
             int(rng.choice([16, 32, 64])), U, R, bool(rng.integers(0, 2)), bool(rng.integers(0, 2)))
 
 
-@pytest.mark.parametrize("seed", range(40))
+# the largest rank counts the layout takes (DIT_MAX_RANKS = 64 virtual
+# ranks, DIT_MAX_R = 8 ring blocks), with uneven rows and head groups
+MAX_CASES = [(1, 701, 5, 16, 64, 1, True, False), (2, 301, 3, 32, 8, 8, False, True),
+             (1, 517, 70, 16, 64, 1, False, False), (1, 129, 9, 64, 2, 8, True, True)]
+
+
+@pytest.mark.parametrize("seed", list(range(40)) + [f"max{i}" for i in range(len(MAX_CASES))])
 def test_random_layouts_bit_exact(seed):
     import sequence_attention_gb300 as sa
-    B, S, H, D, U, R, ph, pl = _case(seed)
+    if isinstance(seed, str):
+        B, S, H, D, U, R, ph, pl = MAX_CASES[int(seed[3:])]
+        seed = 500 + int(seed[3:])
+    else:
+        B, S, H, D, U, R, ph, pl = _case(seed)
     L = sa.dit_sp_layout_init(B, S, H, D, U, R, pad_heads=ph, pad_lcm64=pl)
     ref = olayout.make_layout(B, S, H, D, U, R, pad_heads=ph, pad_lcm64=pl)
     rng = np.random.default_rng(seed)

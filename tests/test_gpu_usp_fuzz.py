@@ -50,3 +50,19 @@ def test_random_usp_configuration(seed):
     ref, _ = oatt.attention(qr, kr, vr)
     assert_bf16_close(f64(out), ref, f"B{B} S{S} H{H} D{D} U{U} R{R} pad_heads={pad_heads} "
                                      f"lcm64={pad_lcm64} rope={use_rope} e4m3={fp8_qv}")
+
+
+@pytest.mark.parametrize("B,S,H,D,U,R", [(1, 1000, 2, 128, 1, 8), (2, 601, 3, 64, 2, 8), (1, 900, 16, 64, 8, 8)])
+def test_eight_ring_blocks(B, S, H, D, U, R):
+    """The largest ring (8 blocks, 64 (query, key) partials per head walked
+    by the kernel that visits every key block) and 64 virtual ranks, end to
+    end against the oracle."""
+    from sequence_attention_gb300.usp import UspPlan
+    q, k, v = (synth.normal((B, S, H, D), 70 + p, 0.5, "bf16") for p in range(3))
+    plan = UspPlan(B, S, H, D, U, R)
+    out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device="cuda")
+    plan.run(q.cuda(), k.cuda(), v.cuda(), out)
+    torch.cuda.synchronize()
+    assert int(plan.status.item()) == 0
+    ref, _ = oatt.attention(f64(q), f64(k), f64(v))
+    assert_bf16_close(f64(out), ref, f"B{B} S{S} H{H} D{D} U{U} R{R}")
