@@ -374,8 +374,7 @@ def run_ours(args):
     achieved = flops / (attn_ms * 1e-3) / 1e12
     # the ncu note covers the attention launch of the default FLUX-like workload
     traffic = traffic_per_launch(ATTN_SRC, TRAFFIC_NOTE) if (w.name == "flux1024" and w.R == 1) else None
-    attn_kernel = (f"attn_f32_kernel<{w.D}>" if w.dtype == "f32" else
-                   f"attn_tc_kernel<{w.D},false>" if w.R == 1 else f"attn_tc_walk_kernel<{w.D},false>")
+    attn_kernel = f"attn_f32_kernel<{w.D}>" if w.dtype == "f32" else f"attn_tc_kernel<{w.D},false>"
     # merge bytes: R fp32 partials and their LSE per real row and head, the
     # output written once (16-bit)
     merge_bytes = w.B * w.S * w.H * (w.R * (w.D * 4 + 4) + w.D * 2)

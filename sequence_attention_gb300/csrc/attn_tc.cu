@@ -6,25 +6,20 @@
 // ring merge needs each call's softmax LSE; edge-dit.cpp "Parallel
 // execution": exact full-sequence attention per head).
 //
-// Two kernels share the code below.  attn_tc_kernel computes one partial
-// (r, j) per CTA (single key blocks, packed sequences); attn_tc_walk_kernel
-// lets one CTA walk every key block j of its query rows (several key
-// blocks, the ring's R partials per query block).
-//
-// CTA = 256 query rows as two 128-row tiles.  Warp roles:
+// CTA = 256 query rows as two 128-row tiles of one (query block r, batch
+// b, head h); the CTA walks every key block j of r in turn (with diag, block
+// r only) and writes partial (r, j) at the end of block j.  Warp roles:
 //   warps 0-3  softmax for Q tile 0 (TMEM lanes 0-127, one row per thread)
 //   warps 4-7  softmax for Q tile 1
 //   warp  8    TMA producer of Q (once) and K tiles (2-stage ring); halfway
 //              through, the L2 prefetch of the next wave's first tiles
 //   warp  9    MMA issuer (one thread): S = Q K^T and O += P V
-//   warp  10   TMA producer of V tiles (3-stage ring, 2 when walking); K and
-//              V loads wait on their own ring's releases, so neither holds up
-//              the other
+//   warp  10   TMA producer of V tiles (2-stage ring); K and V loads wait on
+//              their own ring's releases, so neither holds up the other
 //   warp  11   idle (completes the third warpgroup)
 // Registers: launched at 168 per thread; the producer/MMA warpgroup gives
-// back down to 88 (104 when walking) and the two softmax warpgroups take 208
-// (200) each (2*208 + 88 = 2*200 + 104 = 3*168), enough to hold a whole
-// 128-column score row.
+// back down to 104 and the two softmax warpgroups take 200 each
+// (2*200 + 104 = 3*168), enough to hold a whole 128-column score row.
 // TMEM (512 columns x 128 lanes, fp32): S0 [0,128) S1 [128,256)
 // O0 [256,256+D) O1 [256+D,256+2D).  P (16-bit) overwrites the first half
 // of its tile's S columns and feeds the P V MMA straight from TMEM.
@@ -39,10 +34,9 @@
 // rounding.  Keys at or past the block's valid length are masked to -inf;
 // TMA zero-fills rows past each block's extent, so padding bytes in the
 // buffers are never read.
-// The epilogue writes O / l through shared memory (the then free Q and K
-// buffers, or per-warp slots when walking) and TMA stores, each warp its 32
-// rows; the output map has the block's own extents, so no row past the
-// block is written.
+// The epilogue writes O / l through a per-warp shared-memory slot and TMA
+// stores, each warp its 32 rows; the output map has the block's own extents,
+// so no row past the block is written.
 //
 // Every mbarrier wait is bounded (a few seconds of %globaltimer); on expiry
 // the CTA records DIT_ERR_TIMEOUT in the status word, stops issuing work,
@@ -65,10 +59,9 @@ constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 128;          // keys per tile (MMA N of Q K^T, K of P V)
 constexpr int NQT = 2;           // query tiles per CTA
 constexpr int NSK = 2;           // K pipeline stages
-// V pipeline stages: 3, or 2 when the CTA walks several key blocks (the
-// freed tile holds the per-warp output staging slots)
-template <bool WALK>
-__host__ __device__ constexpr int nsv() { return WALK ? 2 : 3; }
+// V pipeline stages: 2 (the third tile's worth of shared memory holds the
+// per-warp output staging slots)
+constexpr int kNSV = 2;
 constexpr int kSlot = 32 * 128;  // one warp's staging slot: 32 rows x 128 bytes
 constexpr int NTHREADS = 384;
 constexpr int CHUNK = BM * 128;  // bytes of one 64-column (128-byte) swizzle chunk
@@ -95,14 +88,14 @@ struct TcParams {
     int* status;
 };
 
-// shared memory: Q tiles | K stages | V stages | [staging slots] | barriers
-template <int D, bool WALK>
+// shared memory: Q tiles | K stages | V stages | staging slots | barriers
+template <int D>
 __host__ __device__ constexpr int bars_offset() {
-    return (NQT + NSK + nsv<WALK>()) * BM * D * 2 + (WALK ? 8 * kSlot : 0);
+    return (NQT + NSK + kNSV) * BM * D * 2 + 8 * kSlot;
 }
-template <int D, bool WALK>
+template <int D>
 __host__ __device__ constexpr int smem_bytes() {
-    return bars_offset<D, WALK>() + NBAR * 8 + 16 + 1024;
+    return bars_offset<D>() + NBAR * 8 + 16 + 1024;
 }
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -281,11 +274,12 @@ __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
 // %ctaid is read with volatile moves, so the epilogue recomputes these rather
 // than keeping them live (in registers the softmax needs) through the
 // key-tile loop.
-// With WALK the CTA covers every key block of (r, b) and j is 0.
+// The CTA covers every key block of (r, b), starting at j (0, or r with
+// DIAG, where query block r attends key block r only).
 struct Cta {
     int r, j, b, h, row_base;
 };
-template <bool WALK>
+template <bool DIAG>
 __device__ __forceinline__ Cta cta_coords(const TcParams& p) {
     uint32_t x, y, z;
     asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(x));
@@ -293,13 +287,8 @@ __device__ __forceinline__ Cta cta_coords(const TcParams& p) {
     asm volatile("mov.u32 %0, %%ctaid.z;" : "=r"(z));
     Cta c;
     c.b = (int)z % p.B;
-    if (WALK) {
-        c.j = 0;
-        c.r = (int)z / p.B;
-    } else {
-        c.j = p.diag ? (int)z / p.B : ((int)z / p.B) % p.n_kv;
-        c.r = p.diag ? c.j : (int)z / (p.B * p.n_kv);
-    }
+    c.r = (int)z / p.B;
+    c.j = DIAG ? c.r : 0;
     c.h = (int)y;
     c.row_base = (int)x * (NQT * BM);
     return c;
@@ -321,22 +310,18 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, 
 // SM count further in launch order read (usually one of the next wave):
 // both Q tiles and the first K and V tiles.  A hint only; nothing waits on
 // it.
-template <int D, bool WALK>
+template <int D, bool DIAG>
 __device__ __forceinline__ void prefetch_next_cta(const TcParams& p) {
     const unsigned long long gx = gridDim.x, gy = gridDim.y, gz = gridDim.z;
     const unsigned long long L = blockIdx.x + gx * (blockIdx.y + gy * blockIdx.z) + (unsigned long long)p.nsm;
     if (L >= gx * gy * gz) return;
     const int x = (int)(L % gx), h = (int)((L / gx) % gy), z = (int)(L / (gx * gy));
-    const int b = z % p.B;
-    int j, r;
-    if (WALK) {          // the walk starts at its first block with keys
-        r = z / p.B;
+    const int b = z % p.B, r = z / p.B;
+    int j = r;                       // with DIAG, else the walk's first block with keys
+    if (!DIAG) {
         for (j = 0; j < p.n_kv && p.kv_len[j] == 0; ++j) {
         }
         if (j == p.n_kv) return;
-    } else {
-        j = p.diag ? z / p.B : (z / p.B) % p.n_kv;
-        r = p.diag ? j : z / (p.B * p.n_kv);
     }
     const int row_base = x * (NQT * BM);
     if (row_base >= p.q_len[r] || p.kv_len[j] == 0) return;
@@ -441,327 +426,19 @@ __device__ __forceinline__ void softmax_tile(uint32_t St, uint32_t Ot, int valid
 }
 
 // ---- the kernels ------------------------------------------------------------
-// attn_tc_kernel: one partial (r, j) per CTA.
-template <int D, bool P_BF16>
+// attn_tc_kernel: the CTA walks every key block j of its query rows in turn
+// (with diag, block r only), keeping Q resident, and writes partial (r, j)
+// at the end of block j; the K/V rings, the S/P barriers and the MMA stream
+// run on without a break across the blocks, so the pipeline fills and
+// drains once per CTA instead of once per block.  The V ring has 2 stages;
+// the freed tile holds one output staging slot per softmax warp, since the
+// Q, K and V buffers stay in use until the last block.
+template <int D, bool P_BF16, bool DIAG>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     constexpr int NCH = D / 64;          // 128-byte chunks per row
     constexpr int TILE = BM * D * 2;     // bytes of one Q, K or V tile
-    constexpr int NSV = nsv<false>();
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sK = sQ + NQT * TILE;
-    uint8_t* sV = sK + NSK * TILE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sV + NSV * TILE);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Cta cta = cta_coords<false>(p);
-    const int b = cta.b, j = cta.j, r = cta.r, h = cta.h, row_base = cta.row_base;
-    const int qlen = p.q_len[r], kvlen = p.kv_len[j];
-    if (row_base >= qlen) return;
-    const int ntiles = (kvlen + BN - 1) / BN;
-
-    if (ntiles == 0) {   // empty key chunk: O = 0, lse = -inf
-        const int eb = dtype_bytes(p.o_dt);
-        char* obase = static_cast<char*>(p.o.ptr) + (r * p.o.stride_q + j * p.o.stride_kv + b * p.o.stride_b +
-                                                     h * p.o.stride_h + (long long)p.q_row0[r] * p.o.stride_s) * eb;
-        float* lbase = p.lse.ptr ? p.lse.ptr + r * p.lse.stride_q + j * p.lse.stride_kv + b * p.lse.stride_b +
-                                       h * p.lse.stride_h + p.q_row0[r]
-                                 : nullptr;
-        pdl_wait();
-        if (threadIdx.x < NQT * BM) {
-            const int row = row_base + threadIdx.x;
-            if (row < qlen) {
-                char* orow = obase + (long long)row * p.o.stride_s * eb;
-                for (int d = 0; d < D; d += 8) store8_zero(orow + d * eb, p.o_dt);
-                if (lbase) lbase[row] = -INFINITY;
-            }
-        }
-        return;
-    }
-
-    const Ctl ctl{abort_flag, p.status};
-    auto bar = [&](int i) { return su32(bars + i); };
-
-    // The K producer's thread sets up the barriers and at once issues what the
-    // first Q K^T needs, both Q tiles and K tile 0, so that those loads
-    // overlap the TMEM allocation and the block-wide barrier.  The other K and
-    // V stages wait until Q has landed (see the producers): issued together,
-    // the CTA's first 224 KB of loads kept Q and K tile 0 waiting ~5000
-    // cycles behind tiles needed thousands of cycles later.
-    if (warp == 8 && lane == 0) {
-        mbar_init(bar(B_Q), 1);
-        for (int s = 0; s < NSK; ++s) {
-            mbar_init(bar(B_KF + s), 1);
-            mbar_init(bar(B_KE + s), 1);
-        }
-        for (int s = 0; s < NSV; ++s) {
-            mbar_init(bar(B_VF + s), 1);
-            mbar_init(bar(B_VE + s), 1);
-        }
-        for (int t = 0; t < NQT; ++t) {
-            mbar_init(bar(B_SF + t), 1);
-            mbar_init(bar(B_PF + t), 128);
-        }
-        for (int t = 0; t < NQT; ++t) mbar_init(bar(B_OD + t), 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        pdl_wait();      // the inputs may come from the previous kernel
-        const CUtensorMap* qm = &p.qmap[r];
-        mbar_expect_tx(bar(B_Q), NQT * TILE);
-        for (int t = 0; t < NQT; ++t)
-            for (int c = 0; c < NCH; ++c)
-                tma_load_4d(su32(sQ + t * TILE + c * CHUNK), qm, c * 64, h, row_base + t * BM, b, bar(B_Q));
-        mbar_expect_tx(bar(B_KF), TILE);
-        for (int c = 0; c < NCH; ++c) tma_load_4d(su32(sK + c * CHUNK), &p.kmap[j], c * 64, h, 0, b, bar(B_KF));
-    }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
-                     "r"(512)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    pdl_wait();          // barriers and TMEM are set up; tensors from here on
-
-    if (warp >= 8) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
-        if (warp == 8 || warp == 10) {
-        // ------------------------------------------------------------ producers
-        if (lane == 0) {
-            const bool is_k = (warp == 8);
-            const CUtensorMap* map = is_k ? &p.kmap[j] : &p.vmap[j];
-            const int nst = is_k ? NSK : NSV;
-            const int full = is_k ? B_KF : B_VF, empty = is_k ? B_KE : B_VE;
-            uint8_t* ring = is_k ? sK : sV;
-            // Q and K tile 0 went out before the block barrier
-            int issued = is_k ? 1 : 0;
-            bool ok = wait_phase(bar(B_Q), 0, ctl);
-            for (int n = issued; n < ntiles && ok; ++n) {
-                const int s = n % nst;
-                const uint32_t ph = (n / nst) & 1;
-                if (is_k && n == ntiles / 2) prefetch_next_cta<D, false>(p);
-                if (n >= nst && !(ok = wait_phase(bar(empty + s), ph ^ 1, ctl))) break;
-                mbar_expect_tx(bar(full + s), TILE);
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_4d(su32(ring + s * TILE + c * CHUNK), map, c * 64, h, n * BN, b, bar(full + s));
-                issued = n + 1;
-            }
-            if (!ok || *abort_flag) {
-                // let every copy this thread issued land before smem is released
-                if (is_k) drain_phase(bar(B_Q), 0);
-                for (int n = issued > nst ? issued - nst : 0; n < issued; ++n)
-                    drain_phase(bar(full + n % nst), (n / nst) & 1);
-            }
-        }
-        } else if (warp == 9) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t S[NQT] = {tmem, tmem + 128};
-            const uint32_t O[NQT] = {tmem + 256, tmem + 256 + D};
-            // Descriptors are built once; a k-step only adds an offset (in
-            // 16-byte units) to the start-address field.  Stage buffers are
-            // selected with (s ? x1 : x0), never by indexing an array.
-            static_assert(NQT == 2 && NSK == 2 && NSV == 3, "descriptor selection assumes 2 tiles, 2+3 stages");
-            const uint64_t qd0 = sdesc(su32(sQ), 16, 1024), qd1 = sdesc(su32(sQ + TILE), 16, 1024);
-            const uint64_t kd0 = sdesc(su32(sK), 16, 1024), kd1 = sdesc(su32(sK + TILE), 16, 1024);
-            // V tile rows are keys (K dim), 64-wide d chunks CHUNK apart (N dim)
-            const uint64_t vd0 = sdesc(su32(sV), CHUNK, 1024), vd1 = sdesc(su32(sV + TILE), CHUNK, 1024),
-                           vd2 = sdesc(su32(sV + 2 * TILE), CHUNK, 1024);
-            const uint32_t idesc_qk = p.idesc_qk, idesc_pv = p.idesc_pv;
-            auto issue_qk = [&](int t, int s) {
-                const uint64_t a0 = t ? qd1 : qd0, b0 = s ? kd1 : kd0;
-                const uint32_t d = t ? S[1] : S[0];
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t off = (uint64_t)(((ks & 3) * 32 + (ks >> 2) * CHUNK) >> 4);
-                    mma_ss(d, a0 + off, b0 + off, idesc_qk, ks > 0);
-                }
-            };
-            auto issue_pv = [&](int t, int s, bool acc) {
-                const uint64_t b0 = s == 0 ? vd0 : (s == 1 ? vd1 : vd2);
-                const uint32_t d = t ? O[1] : O[0], a = t ? S[1] : S[0];
-#pragma unroll
-                for (int ks = 0; ks < BN / 16; ++ks)
-                    mma_ts(d, a + ks * 8, b0 + (uint64_t)(ks * 16 * 128 / 16), idesc_pv, (acc || ks > 0) ? 1u : 0u);
-            };
-            bool ok = wait_phase(bar(B_Q), 0, ctl) && wait_phase(bar(B_KF), 0, ctl);
-            if (ok) {
-                tc_fence_after();
-                issue_qk(0, 0);
-                tc_commit(bar(B_SF + 0));
-                issue_qk(1, 0);
-                tc_commit(bar(B_SF + 1));
-                tc_commit(bar(B_KE + 0));
-            }
-            for (int n = 0; n < ntiles && ok; ++n) {
-                const int s = n % NSV;
-                const bool nxt = n + 1 < ntiles;
-                const int s1 = (n + 1) % NSK;
-                const uint32_t ph1 = ((n + 1) / NSK) & 1;
-                if (!(ok = wait_phase(bar(B_VF + s), (n / NSV) & 1, ctl))) break;
-                if (!(ok = wait_phase(bar(B_PF + 0), n & 1, ctl))) break;
-                tc_fence_after();
-                issue_pv(0, s, n > 0);
-                if (!nxt) {
-                    // tile 0 is done: its epilogue overlaps tile 1's last P V
-                    // (every Q K^T, the last reader of the Q and K buffers
-                    // the epilogue stages into, was issued before)
-                    tc_commit(bar(B_OD + 0));
-                }
-                if (nxt) {
-                    if (!(ok = wait_phase(bar(B_KF + s1), ph1, ctl))) break;
-                    tc_fence_after();
-                    issue_qk(0, s1);
-                    tc_commit(bar(B_SF + 0));
-                }
-                if (!(ok = wait_phase(bar(B_PF + 1), n & 1, ctl))) break;
-                tc_fence_after();
-                issue_pv(1, s, n > 0);
-                tc_commit(bar(B_VE + s));
-                if (nxt) {
-                    issue_qk(1, s1);
-                    tc_commit(bar(B_SF + 1));
-                    tc_commit(bar(B_KE + s1));
-                }
-            }
-            // on a normal run tile 0's commit was made in the last key tile;
-            // after an abort its waiters leave on the abort flag, so a second
-            // commit there is harmless
-            if (!ok) tc_commit(bar(B_OD + 0));
-            tc_commit(bar(B_OD + 1));
-            if (!ok) drain_phase(bar(B_OD + 1), 0);   // every issued MMA has finished
-        }
-        }
-    } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
-        // ------------------------------------------------------------ softmax
-        const int t = warp >> 2, q4 = warp & 3;
-        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const uint32_t St = tmem + t * 128 + lane_off;
-        const uint32_t Ot = tmem + 256 + t * D + lane_off;
-        const float c = p.c;
-        float m_used = 0.f, l = 0.f;
-        bool ok = true;
-        for (int n = 0; n < ntiles; ++n) {
-            ok = __all_sync(0xffffffffu, wait_phase(bar(B_SF + t), n & 1, ctl));
-            if (!ok) break;
-            tc_fence_after();
-            softmax_tile<D, P_BF16>(St, Ot, kvlen - n * BN, n == 0, c, m_used, l);
-            mbar_arrive(bar(B_PF + t));
-        }
-        // epilogue: O / l and lse = ln(2) * (m + log2 l)
-        // this tile's "O done" barrier; the tile index is re-read from
-        // %tid (volatile) so that nothing derived from it stays live in the
-        // key-tile loop, where the softmax needs every register
-        uint32_t tid_now;
-        asm volatile("mov.u32 %0, %%tid.x;" : "=r"(tid_now));
-        const uint32_t od_bar = ((su32(smem_raw) + 1023u) & ~1023u) +
-                                (uint32_t)((NQT + NSK + NSV) * TILE + (B_OD + (int)(tid_now >> 7)) * 8);
-        if (ok) ok = __all_sync(0xffffffffu, wait_phase(od_bar, 0, ctl));
-        if (ok) {
-            tc_fence_after();
-            const float inv = 1.f / l;
-            const Cta e = cta_coords<false>(p);
-            const int eb = dtype_bytes(p.o_dt);
-            // Stage the tile in shared memory (per 128 bytes of d, BM rows of
-            // 128 bytes, 16-byte chunks swizzled by row mod 8) and store it
-            // with TMA, each warp its own 32 rows: every MMA has completed,
-            // so the Q and K buffers are free (tile t takes BM*D*eb bytes
-            // from the start).  Rows past the block's length are clipped by
-            // the output map.
-            const int rt = q4 * 32 + lane;
-            // Shared addresses are recomputed from the array's own address
-            // (the aligned base is at a fixed offset in the shared window)
-            // instead of keeping the generic pointers live through the loop.
-            // The warp's 32 rows of box bx sit at wbase + bx*BM*128.
-            const uint32_t sbase = (su32(smem_raw) + 1023u) & ~1023u;
-            const uint32_t wbase = sbase + (uint32_t)(t * BM * D * eb + q4 * 32 * 128);
-            const uint32_t myrow = wbase + (uint32_t)lane * 128u;
-            const int grow = e.row_base + t * BM + q4 * 32, gj = p.diag ? 0 : e.j;
-            uint32_t x[D];
-            if constexpr (D == 128) tmem_ld128(Ot, x); else tmem_ld64(Ot, x);   // the whole O row, one round trip
-            // each box goes out as soon as it is staged, so its store overlaps
-            // the staging of the next
-            auto store_box = [&](int bx) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_5d(&p.omap[e.r], wbase + (uint32_t)(bx * BM * 128), bx * (128 / eb), e.h, grow, e.b, gj);
-                    bulk_commit();
-                }
-            };
-            if (p.o_dt == DIT_F32) {
-#pragma unroll
-                for (int bx = 0; bx < D / 32; ++bx) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int i = bx * 32 + 4 * k;
-                        st_shared16(myrow + (uint32_t)(bx * BM * 128) + (uint32_t)((k ^ (lane & 7)) << 4),
-                                    __float_as_uint(__uint_as_float(x[i]) * inv),
-                                    __float_as_uint(__uint_as_float(x[i + 1]) * inv),
-                                    __float_as_uint(__uint_as_float(x[i + 2]) * inv),
-                                    __float_as_uint(__uint_as_float(x[i + 3]) * inv));
-                    }
-                    store_box(bx);
-                }
-            } else {
-#pragma unroll
-                for (int bx = 0; bx < D / 64; ++bx) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int i = bx * 64 + 8 * k;
-                        uint32_t w[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            w[q] = pack2(__uint_as_float(x[i + 2 * q]) * inv, __uint_as_float(x[i + 2 * q + 1]) * inv,
-                                         p.o_dt);
-                        st_shared16(myrow + (uint32_t)(bx * BM * 128) + (uint32_t)((k ^ (lane & 7)) << 4), w[0], w[1],
-                                    w[2], w[3]);
-                    }
-                    store_box(bx);
-                }
-            }
-            const int row = e.row_base + t * BM + rt;
-            if (p.lse.ptr && row < p.q_len[e.r])
-                p.lse.ptr[e.r * p.lse.stride_q + e.j * p.lse.stride_kv + e.b * p.lse.stride_b + e.h * p.lse.stride_h +
-                          p.q_row0[e.r] + row] = (m_used + log2f(l)) * 0.69314718055994531f;
-            // the shared-memory source must stay until the copies have read
-            // it; the global writes complete with the grid, before any
-            // dependent kernel passes its griddepcontrol.wait
-            if (lane == 0) bulk_wait_read();
-        }
-    }
-
-    pdl_trigger();
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
-    }
-}
-
-// attn_tc_walk_kernel: the CTA walks every key block j of its query rows in
-// turn, keeping Q resident, and writes partial (r, j) at the end of block j;
-// the K/V rings, the S/P barriers and the MMA stream run on without a break
-// across the blocks, so the pipeline fills and drains once per CTA instead
-// of once per block.  The V ring has 2 stages; the freed tile holds one
-// output staging slot per softmax warp, since the Q, K and V buffers stay in
-// use until the last block.
-template <int D, bool P_BF16>
-__global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_constant__ TcParams p) {
-    constexpr bool WALK = true;
-    constexpr int NCH = D / 64;          // 128-byte chunks per row
-    constexpr int TILE = BM * D * 2;     // bytes of one Q, K or V tile
-    constexpr int NSV = nsv<WALK>();
-    constexpr int BARS = bars_offset<D, WALK>();
+    constexpr int NSV = kNSV;
+    constexpr int BARS = bars_offset<D>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
@@ -772,15 +449,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Cta cta = cta_coords<WALK>(p);
+    const Cta cta = cta_coords<DIAG>(p);
     const int b = cta.b, r = cta.r, h = cta.h, row_base = cta.row_base;
-    const int j0 = 0, nj = p.n_kv;                      // every key block
+    // key blocks j0 .. j0 + nj - 1 (j0 = cta.j: 0, or r with DIAG)
+    const int nj = DIAG ? 1 : p.n_kv;
     if (row_base >= p.q_len[r]) return;
     bool any_keys = false;
-    for (int jj = 0; jj < nj; ++jj) any_keys |= p.kv_len[j0 + jj] > 0;
+    for (int jj = 0; jj < nj; ++jj) any_keys |= p.kv_len[cta.j + jj] > 0;
     if (!any_keys) {     // every key block empty: O = 0, lse = -inf
         pdl_wait();
-        for (int jj = 0; jj < nj; ++jj) write_empty_partial<D>(p, r, j0 + jj, b, h, row_base);
+        for (int jj = 0; jj < nj; ++jj) write_empty_partial<D>(p, r, cta.j + jj, b, h, row_base);
         return;
     }
 
@@ -832,6 +510,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
             const int full = is_k ? B_KF : B_VF, empty = is_k ? B_KE : B_VE;
             uint8_t* ring = is_k ? sK : sV;
             int total = 0;                                  // key tiles over every block
+            const int j0 = cta.j;
             for (int jj = 0; jj < nj; ++jj) total += (p.kv_len[j0 + jj] + BN - 1) / BN;
             // Q and the first K tile go first; the other stages wait until Q
             // has landed, so they do not compete with what the first Q K^T
@@ -853,7 +532,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
                     const int s = g % nst;
                     const uint32_t ph = (g / nst) & 1;
                     if (g == (is_k ? 1 : 0) && !(ok = wait_phase(bar(B_Q), 0, ctl))) break;
-                    if (is_k && g == total / 2) prefetch_next_cta<D, true>(p);
+                    if (is_k && g == total / 2) prefetch_next_cta<D, DIAG>(p);
                     if (g >= nst && !(ok = wait_phase(bar(empty + s), ph ^ 1, ctl))) break;
                     mbar_expect_tx(bar(full + s), TILE);
                     for (int c = 0; c < NCH; ++c)
@@ -898,6 +577,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
                 for (int ks = 0; ks < BN / 16; ++ks)
                     mma_ts(d, a + ks * 8, b0 + (uint64_t)(ks * 16 * 128 / 16), idesc_pv, (acc || ks > 0) ? 1u : 0u);
             };
+            const int j0 = cta.j;
             auto tiles_of = [&](int jj) { return (p.kv_len[j0 + jj] + BN - 1) / BN; };
             // positions (key block jj, key tile n), empty blocks skipped;
             // gk / gv count K / V tiles, gs positions
@@ -971,9 +651,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
         // bit 1 the O-done phase (per block), bits 8.. the key block
         uint32_t st = 0;
         for (; (int)(st >> 8) < nj && ok; st += 256u) {
-            int rem = p.kv_len[j0 + (int)(st >> 8)];     // keys of the block not yet seen
+            int rem = p.kv_len[(DIAG ? cta_coords<DIAG>(p).j : 0) + (int)(st >> 8)];   // keys not yet seen
             if (rem == 0) {
-                const Cta e = cta_coords<WALK>(p);
+                const Cta e = cta_coords<DIAG>(p);
                 write_empty_partial<D>(p, e.r, e.j + (int)(st >> 8), e.b, e.h, e.row_base);
                 continue;
             }
@@ -1003,8 +683,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
             if (!ok) break;
             tc_fence_after();
             const float inv = 1.f / l;
-            const Cta e = cta_coords<WALK>(p);
+            const Cta e = cta_coords<DIAG>(p);
             const int j = e.j + (int)(st >> 8);
+            const int jc = DIAG ? 0 : j;                // the output map's key-block coordinate
             const int eb = dtype_bytes(p.o_dt);
             const int rt = (int)(tid_now & 127);      // row within the tile
             const int row = e.row_base + te * BM + rt;
@@ -1031,7 +712,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_walk_kernel(const __grid_
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (le == 0) {
-                    tma_store_5d(&p.omap[e.r], slot, bx * (128 / eb), e.h, grow, e.b, j);
+                    tma_store_5d(&p.omap[e.r], slot, bx * (128 / eb), e.h, grow, e.b, jc);
                     bulk_commit();
                 }
             };
@@ -1158,11 +839,11 @@ uint32_t make_idesc(bool bf16, bool b_mn_major, int N, int M) {
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-template <int D, bool PB, bool WALK>
+template <int D, bool PB>
 dit_status launch_kernel(const TcParams& prm, dim3 grid, cudaStream_t st) {
-    int smem = smem_bytes<D, WALK>();
+    int smem = smem_bytes<D>();
     if (smem < 116 * 1024) smem = 116 * 1024;   // one CTA per SM: it owns all 512 TMEM columns
-    auto kernel = WALK ? attn_tc_walk_kernel<D, PB> : attn_tc_kernel<D, PB>;
+    auto kernel = prm.diag ? attn_tc_kernel<D, PB, true> : attn_tc_kernel<D, PB, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "attention: %s", cudaGetErrorString(e));
     e = launch_pdl(kernel, grid, dim3(NTHREADS), (size_t)smem, st, prm);
@@ -1208,24 +889,23 @@ dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
     }
     if (s == DIT_OK && maxq > 0) {
         prm->B = a.B; prm->n_q = a.n_q; prm->n_kv = a.n_kv; prm->diag = a.diag; prm->nsm = num_sms();
+
         prm->c = a.scale * 1.4426950408889634f;
         prm->idesc_qk = make_idesc(a.qk_dt == DIT_BF16, false, BN, BM);
         prm->idesc_pv = make_idesc(a.v_dt == DIT_BF16, true, a.D, BM);
         prm->o = a.o; prm->o_dt = a.o_dt; prm->lse = a.lse; prm->status = a.status;
-        // Several key blocks per query block: one CTA walks them all, paying
-        // the pipeline fill and drain once instead of once per block
-        // (measured on one GB300: 1153 against 1080 TFLOP/s at 18 key tiles
-        // per block, 1369 against 1308 at 28, 1448 against 1437 at 148).
-        const bool walk = !a.diag && a.n_kv > 1;
-        dim3 grid((maxq + NQT * BM - 1) / (NQT * BM), a.H, (a.diag || walk ? a.n_q : a.n_q * a.n_kv) * a.B);
+        // One CTA per (256 query rows, head, query block, batch) walks every
+        // key block (with diag, its own block): measured on one GB300 against
+        // one CTA per (query block, key block), 1153 against 1080 TFLOP/s at
+        // 18 key tiles per block, 1369 against 1308 at 28, 1448 against 1437
+        // at 148, and the same 1296 with a single key block.
+        dim3 grid((maxq + NQT * BM - 1) / (NQT * BM), a.H, a.n_q * a.B);
         const bool pb = a.v_dt == DIT_BF16;
         if (grid.y > 65535 || grid.z > 65535) s = fail(DIT_ERR_UNSUPPORTED, "attention: grid too large");
         else if (a.D == 128)
-            s = walk ? (pb ? launch_kernel<128, true, true>(*prm, grid, st) : launch_kernel<128, false, true>(*prm, grid, st))
-                     : (pb ? launch_kernel<128, true, false>(*prm, grid, st) : launch_kernel<128, false, false>(*prm, grid, st));
+            s = pb ? launch_kernel<128, true>(*prm, grid, st) : launch_kernel<128, false>(*prm, grid, st);
         else
-            s = walk ? (pb ? launch_kernel<64, true, true>(*prm, grid, st) : launch_kernel<64, false, true>(*prm, grid, st))
-                     : (pb ? launch_kernel<64, true, false>(*prm, grid, st) : launch_kernel<64, false, false>(*prm, grid, st));
+            s = pb ? launch_kernel<64, true>(*prm, grid, st) : launch_kernel<64, false>(*prm, grid, st);
     }
     return s;
 }
