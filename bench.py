@@ -13,7 +13,9 @@ Prints one JSON line (rank 0).  `value` is attention TFLOP/s over the whole
 step (algorithmic 4*B*H*S^2*D flops / step time, summed over ranks);
 `e2e` is the same through the public API with pinned host buffers and the
 host<->device copies inside the timed region.  L2 is flushed (a 256 MiB
-write) before every timed step; only the step itself is inside the events.
+write) before every timed step; only the step itself is inside the events
+(one at its start, one at its end); a second pass with events between the
+phases gives the per-phase split in `kernels`.
 """
 from __future__ import annotations
 
@@ -307,9 +309,11 @@ def run_ours(args):
     names = plan.steps() + ["cfg"]
     n_cfg_kernels = 1 if (pred.numel() // 2) % 8 == 0 else 2
 
-    def step(ev=None):
+    def step(ev=None, phases=True):
+        # ev: 6 events to record (phases=True: between every two phases;
+        # False: at the step's start and end only, events 0 and 5)
         def mark(i):
-            if ev is not None:
+            if ev is not None and (phases or i in (0, 5)):
                 ev[i].record(stream)
         mark(0)
         plan.layout_in(q, k, v)
@@ -333,27 +337,32 @@ def run_ours(args):
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
 
-    def timed():
+    def timed(phases):
         barrier()
         torch.cuda.synchronize(dev)
         with ClockSampler(gpu_index) as cs:
             for i in range(K):
                 flush.zero_()
-                step(evs[i])
+                step(evs[i], phases)
             torch.cuda.synchronize(dev)
         barrier()
         return cs.summary()
 
-    clocks = timed()
+    # The timed steps: events at each step's start and end only (an event
+    # between two phases breaks their launch overlap); L2 flushed between
+    # steps, outside the events.
+    clocks = timed(False)
     if any(r in clocks["reasons"] for r in BAD_REASONS):
-        clocks = timed()        # rejected once: measure again
+        clocks = timed(False)   # rejected once: measure again
         clocks["remeasured"] = True
-
-    # ms per segment: layout-in, attention partials, merge, layout-out, CFG
-    seg = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(5)]
-    step_ms = [sum(x) for x in zip(*seg)]
+    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, dev)
+    # A second pass with events between the phases gives the split below:
+    # ms per segment: layout-in, attention partials, merge, layout-out, CFG
+    timed(True)
+    seg = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(5)]
+    split_ms = statistics.mean([sum(x) for x in zip(*seg)])
     attn_ms = statistics.mean(seg[1])          # the partial-attention launch alone
     flops = w.attn_flops
     value = ws * flops / (ms_max * 1e-3) / 1e12
@@ -436,6 +445,7 @@ def run_ours(args):
             "hbm_peak_GBs": peaks.get("hbm_gbs"),
             "step_graph_ms": round(graph_ms, 4),
             "step_eager_ms": round(eager_ms, 4),
+            "step_split_ms": round(split_ms, 4),     # the same steps with events between phases
             **extra,
         },
         "e2e": e2e,
