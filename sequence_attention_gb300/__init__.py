@@ -58,8 +58,16 @@ def _stream(stream) -> c_void_p:
     return c_void_p(s.cuda_stream)
 
 
+def _addr(t: torch.Tensor) -> int:
+    """The device address of t: every buffer the kernels touch must live on a
+    CUDA device (a host pointer would fault the GPU, so it is refused here)."""
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    return t.data_ptr()
+
+
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else c_void_p(t.data_ptr())
+    return None if t is None else c_void_p(_addr(t))
 
 
 class Layout:
@@ -122,7 +130,7 @@ def dit_sp_a2a_counts(L: Layout, direction: int, nplanes: int, rank: int):
 
 def dit_ulysses_pack(L: Layout, direction: int, srcs: Sequence[torch.Tensor], send: torch.Tensor,
                      stream=None) -> None:
-    arr = (c_void_p * 3)(*[s.data_ptr() for s in srcs])
+    arr = (c_void_p * 3)(*[_addr(s) for s in srcs])
     check(lib().dit_ulysses_pack(byref(L.raw), direction, len(srcs), arr, _dt(srcs[0]),
                                  _ptr(send), _dt(send), _stream(stream)))
 
@@ -152,14 +160,14 @@ def dit_a2a_sim_checked(L: Layout, direction: int, nplanes: int, send: torch.Ten
 
 def dit_ulysses_unpack(L: Layout, direction: int, recv: torch.Tensor, dsts: Sequence[torch.Tensor],
                        range_flag: Optional[torch.Tensor] = None, stream=None) -> None:
-    ptrs = (c_void_p * 3)(*[d.data_ptr() for d in dsts])
+    ptrs = (c_void_p * 3)(*[_addr(d) for d in dsts])
     dts = (c_int * 3)(*[_dt(d) for d in dsts])
     check(lib().dit_ulysses_unpack(byref(L.raw), direction, len(dsts), _ptr(recv), _dt(recv), ptrs,
                                    dts, _ptr(range_flag), _stream(stream)))
 
 
 def _ptrs(ts: Optional[Sequence[torch.Tensor]], n: int):
-    return None if ts is None else (c_void_p * n)(*[t.data_ptr() for t in ts])
+    return None if ts is None else (c_void_p * n)(*[_addr(t) for t in ts])
 
 
 def dit_ulysses_pack_joint(L: Layout, txt: Optional[Sequence[torch.Tensor]], img: Optional[Sequence[torch.Tensor]],
@@ -190,7 +198,7 @@ def dit_ulysses_unpack_rope(L: Layout, recv: torch.Tensor, dsts: Sequence[torch.
     for t in (cos, sin):
         if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (L.raw.S, L.raw.D // 2):
             raise ValueError("rotary tables must be contiguous float32 [S, D/2]")
-    ptrs = (c_void_p * 3)(*[d.data_ptr() for d in dsts])
+    ptrs = (c_void_p * 3)(*[_addr(d) for d in dsts])
     dts = (c_int * 3)(*[_dt(d) for d in dsts])
     check(lib().dit_ulysses_unpack_rope(byref(L.raw), len(dsts), _ptr(recv), _dt(recv), ptrs, dts, _ptr(cos),
                                         _ptr(sin), rope_planes, _ptr(range_flag), _stream(stream)))
@@ -203,7 +211,7 @@ def _view(t: torch.Tensor, kind: str) -> DitView:
     if st[-1] != 1:
         raise ValueError("the head dim must be contiguous")
     v = DitView()
-    v.ptr = t.data_ptr()
+    v.ptr = _addr(t)
     if kind in ("q", "out"):
         v.stride_q, v.stride_b, v.stride_s, v.stride_h = st[0], st[1], st[2], st[3]
     elif kind == "kv":
@@ -226,7 +234,7 @@ def _lse_view(t: Optional[torch.Tensor], kind: str) -> DitLseView:
     if t.dtype != torch.float32 or t.stride(-1) != 1:
         raise ValueError("lse must be float32 with contiguous rows")
     st = t.stride()
-    v.ptr = t.data_ptr()
+    v.ptr = _addr(t)
     if kind == "o":        # [n_q, n_kv, B, H, S]
         v.stride_q, v.stride_kv, v.stride_b, v.stride_h = st[0], st[1], st[2], st[3]
     elif kind == "out":    # [n_q, B, H, S]

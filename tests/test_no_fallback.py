@@ -39,3 +39,20 @@ def test_package_never_imports_the_oracle_or_numpy():
         for name in _imports(f):
             root = name.split(".")[0]
             assert root not in ("oracle", "numpy", "scipy", "synth"), f"{f} imports {name}"
+
+
+def test_host_tensors_are_refused_before_any_launch():
+    """A CPU tensor handed to a call would put a host pointer in a kernel;
+    the binding refuses it instead (no GPU needed to check)."""
+    import torch
+    import sequence_attention_gb300 as sa
+    L = sa.dit_sp_layout_init(1, 64, 4, 64, 2, 1)
+    q = torch.zeros((1, 64, 4, 64), dtype=torch.bfloat16)
+    send = torch.zeros(L.wire_elems(3), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        sa.dit_ulysses_pack(L, sa.DIT_SEQ_TO_HEAD, [q, q, q], send)
+    o = torch.zeros_like(q)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        sa.dit_attention(q, q, q, o)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        sa.dit_cfg_combine(torch.zeros((2, 8)), torch.zeros(8), 1.0)
