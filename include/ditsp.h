@@ -46,6 +46,12 @@
  *    to nearest even; widening is exact.
  *  - Pointers passed to kernels must be 16-byte aligned and every tensor's
  *    innermost (head-dim) extent in bytes a multiple of 16.
+ *  - Empty work: a call with nothing to read or write (a layout with S = 0,
+ *    attention or a merge with no query rows, a CFG combine with N = 0)
+ *    checks its other arguments, launches nothing and returns DIT_OK; its
+ *    buffer pointers may then be NULL, as an allocator gives for zero bytes.
+ *    Attention whose every key block is empty writes O = 0 and lse = -inf
+ *    and may take NULL K and V.
  */
 #ifndef DITSP_H
 #define DITSP_H

@@ -22,12 +22,6 @@ dit_status validate_and_launch(AttnArgs& a, const char* who, cudaStream_t st) {
         if (a.kv_len[r] < 0) return fail(DIT_ERR_INVALID_ARG, "%s: negative key length", who);
     if (!dtype_ok(a.qk_dt) || !dtype_ok(a.v_dt) || !dtype_ok(a.o_dt))
         return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
-    if (!a.q.ptr || !a.k.ptr || !a.v.ptr || !a.o.ptr)
-        return fail(DIT_ERR_INVALID_ARG, "%s: NULL tensor pointer", who);
-    if (!aligned16(a.q.ptr) || !aligned16(a.k.ptr) || !aligned16(a.v.ptr) || !aligned16(a.o.ptr))
-        return fail(DIT_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", who);
-    if (a.lse.ptr && (reinterpret_cast<uintptr_t>(a.lse.ptr) & 3))
-        return fail(DIT_ERR_INVALID_ARG, "%s: lse pointer misaligned", who);
     const bool f32 = a.qk_dt == DIT_F32;
     if (f32) {
         if (a.v_dt != DIT_F32 || a.o_dt != DIT_F32)
@@ -56,6 +50,26 @@ dit_status validate_and_launch(AttnArgs& a, const char* who, cudaStream_t st) {
                        (a.B > 1 && a.o.stride_b == 0) || (!a.diag && a.n_q > 1 && a.o.stride_q == 0) ||
                        (!a.diag && a.n_kv > 1 && a.o.stride_kv == 0);
     if (alias) return fail(DIT_ERR_INVALID_ARG, "%s: output view maps two results to one address", who);
+    // No query rows: nothing is read or written, so the (empty) buffers may
+    // be NULL, as an allocator gives for zero bytes.
+    if (maxq == 0) return DIT_OK;
+    if (!a.q.ptr || !a.o.ptr) return fail(DIT_ERR_INVALID_ARG, "%s: NULL tensor pointer", who);
+    if (!aligned16(a.q.ptr) || !aligned16(a.o.ptr))
+        return fail(DIT_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", who);
+    if (a.lse.ptr && (reinterpret_cast<uintptr_t>(a.lse.ptr) & 3))
+        return fail(DIT_ERR_INVALID_ARG, "%s: lse pointer misaligned", who);
+    bool any_keys = false;
+    for (int j = 0; j < a.n_kv; ++j) any_keys |= a.kv_len[j] > 0;
+    if (!any_keys && (!a.k.ptr || !a.v.ptr)) {
+        // Every key block is empty (O = 0, lse = -inf): K and V are never
+        // read, and may be NULL.  The kernels still take descriptors of
+        // them, so they get Q's view, which is valid and never used.
+        a.k = a.q;
+        a.v = a.q;
+    }
+    if (!a.k.ptr || !a.v.ptr) return fail(DIT_ERR_INVALID_ARG, "%s: NULL tensor pointer", who);
+    if (!aligned16(a.k.ptr) || !aligned16(a.v.ptr))
+        return fail(DIT_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", who);
     if (!a.status) a.status = default_status_word();
     if (!a.status) return fail(DIT_ERR_CUDA, "%s: no device status word", who);
     return f32 ? launch_attn_f32(a, st) : launch_attn_tc(a, st);

@@ -298,8 +298,6 @@ extern "C" dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int
     if (n_q < 1 || n_q > DIT_MAX_R || !q_len || n_parts < 1 || n_parts > DIT_MAX_R)
         return fail(DIT_ERR_INVALID_ARG, "%s: need 1 <= n_q, n_parts <= %d", who, DIT_MAX_R);
     if (!dtype_ok(parts_dt) || !dtype_ok(out_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
-    if (!parts.ptr || !out.ptr || !lse_parts.ptr || !aligned16(parts.ptr) || !aligned16(out.ptr))
-        return fail(DIT_ERR_INVALID_ARG, "%s: NULL or misaligned pointer", who);
     const int64_t pstr[] = {parts.stride_q, parts.stride_kv, parts.stride_b, parts.stride_s, parts.stride_h};
     const int64_t ostr[] = {out.stride_q, out.stride_b, out.stride_s, out.stride_h};
     for (int64_t s : pstr)
@@ -315,7 +313,10 @@ extern "C" dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int
         a.q_len[r] = q_len[r];
         if (q_len[r] > maxq) maxq = q_len[r];
     }
+    // no rows: nothing is read or written, and the (empty) buffers may be NULL
     if (maxq == 0) return DIT_OK;
+    if (!parts.ptr || !out.ptr || !lse_parts.ptr || !aligned16(parts.ptr) || !aligned16(out.ptr))
+        return fail(DIT_ERR_INVALID_ARG, "%s: NULL or misaligned pointer", who);
     a.parts = parts; a.parts_dt = parts_dt; a.lse_parts = lse_parts;
     a.out = out; a.out_dt = out_dt; a.lse_out = lse_out;
     if ((unsigned)(n_q * B) > 65535u) return fail(DIT_ERR_UNSUPPORTED, "%s: n_q * B too large", who);

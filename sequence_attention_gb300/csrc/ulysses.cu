@@ -430,10 +430,24 @@ dit_status launch_runs(const RunArgs& a, cudaStream_t st, const char* who) {
 
 // The e4m3 wire's exchange: a record of D + 16 bytes is (D + 16) / 2 16-bit
 // words, so the exchange is the 16-bit permutation of runs of that width.
-dit_status record_words(RunArgs* a, const char* who) {
-    const int D = a->L.D;
+static dit_status check_e4m3_dim(int D, const char* who) {
     if (D < 16 || D > 256 || (D & (D - 1)))
         return fail(DIT_ERR_UNSUPPORTED, "%s: the e4m3 wire needs D in {16, 32, 64, 128, 256}", who);
+    return DIT_OK;
+}
+
+// A layout with S = 0 has no rows on either side of the exchange: the call
+// moves nothing, launches nothing and does not look at its buffer pointers
+// (an allocator may give NULL for zero bytes).  The e4m3 wire's head-dim
+// rule is still checked, so the answer does not depend on S.
+static dit_status empty_exchange(const dit_sp_layout* L, dit_dtype wire_dt, const char* who) {
+    return wire_dt == DIT_E4M3 ? check_e4m3_dim(L->D, who) : DIT_OK;
+}
+
+dit_status record_words(RunArgs* a, const char* who) {
+    const int D = a->L.D;
+    const dit_status s = check_e4m3_dim(D, who);
+    if (s != DIT_OK) return s;
     a->L.D = (D + 16) / 2;
     a->src_dt[0] = a->dst_dt[0] = DIT_BF16;
     return DIT_OK;
@@ -474,6 +488,7 @@ extern "C" dit_status dit_ulysses_pack(const dit_sp_layout* L, dit_a2a_dir dir, 
     if (dir != DIT_SEQ_TO_HEAD && dir != DIT_HEAD_TO_SEQ) return fail(DIT_ERR_INVALID_ARG, "%s: bad direction", who);
     if (nplanes < 1 || nplanes > 3 || (dir == DIT_HEAD_TO_SEQ && nplanes != 1))
         return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3 (1 for head-to-seq)", who);
+    if (L->S == 0) return empty_exchange(L, wire_dt, who);
     if (!src || !send || !aligned16(send)) return fail(DIT_ERR_INVALID_ARG, "%s: send NULL or misaligned", who);
     RunArgs a;
     memset(&a, 0, sizeof(a));
@@ -501,6 +516,7 @@ extern "C" dit_status dit_a2a_sim(const dit_sp_layout* L, dit_a2a_dir dir, int n
     if (!wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
     if (dir != DIT_SEQ_TO_HEAD && dir != DIT_HEAD_TO_SEQ) return fail(DIT_ERR_INVALID_ARG, "%s: bad direction", who);
     if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
+    if (L->S == 0) return empty_exchange(L, wire_dt, who);
     if (!send || !recv || !aligned16(send) || !aligned16(recv) || send == recv)
         return fail(DIT_ERR_INVALID_ARG, "%s: send/recv NULL, misaligned or identical", who);
     RunArgs a;
@@ -526,7 +542,11 @@ extern "C" dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir
     if (dir != DIT_SEQ_TO_HEAD && dir != DIT_HEAD_TO_SEQ) return fail(DIT_ERR_INVALID_ARG, "%s: bad direction", who);
     if (nplanes < 1 || nplanes > 3 || (dir == DIT_HEAD_TO_SEQ && nplanes != 1))
         return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3 (1 for head-to-seq)", who);
-    if (!recv || !aligned16(recv) || !dst || !dst_dt)
+    if (!dst_dt) return fail(DIT_ERR_INVALID_ARG, "%s: dst_dt NULL", who);
+    for (int p = 0; p < nplanes; ++p)
+        if (!dtype_ok(dst_dt[p])) return fail(DIT_ERR_INVALID_ARG, "%s: bad dst dtype", who);
+    if (L->S == 0) return empty_exchange(L, wire_dt, who);
+    if (!recv || !aligned16(recv) || !dst)
         return fail(DIT_ERR_INVALID_ARG, "%s: recv/dst NULL or misaligned", who);
     RunArgs a;
     memset(&a, 0, sizeof(a));
@@ -535,7 +555,6 @@ extern "C" dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir
     a.src[0] = recv; a.src_dt[0] = wire_dt;
     for (int p = 0; p < nplanes; ++p) {
         if (!dst[p] || !aligned16(dst[p])) return fail(DIT_ERR_INVALID_ARG, "%s: dst[%d] NULL or misaligned", who, p);
-        if (!dtype_ok(dst_dt[p])) return fail(DIT_ERR_INVALID_ARG, "%s: bad dst dtype", who);
         a.dst[p] = dst[p];
         a.dst_dt[p] = dst_dt[p];
     }
@@ -574,12 +593,14 @@ extern "C" dit_status dit_a2a_sim_checked(const dit_sp_layout* L, dit_a2a_dir di
     if (!wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
     if (dir != DIT_SEQ_TO_HEAD && dir != DIT_HEAD_TO_SEQ) return fail(DIT_ERR_INVALID_ARG, "%s: bad direction", who);
     if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
-    if (!send || !recv || !aligned16(send) || !aligned16(recv) || send == recv)
-        return fail(DIT_ERR_INVALID_ARG, "%s: send/recv NULL, misaligned or identical", who);
     if (!d_arrival || (reinterpret_cast<uintptr_t>(d_arrival) & 3))
         return fail(DIT_ERR_INVALID_ARG, "%s: arrival counters NULL or misaligned", who);
     if (timeout_ns <= 0 || timeout_ns > 10000000000LL)
         return fail(DIT_ERR_INVALID_ARG, "%s: timeout must be in (0, 10 s]", who);
+    // nothing is read, so nothing waits for the senders
+    if (L->S == 0) return empty_exchange(L, wire_dt, who);
+    if (!send || !recv || !aligned16(send) || !aligned16(recv) || send == recv)
+        return fail(DIT_ERR_INVALID_ARG, "%s: send/recv NULL, misaligned or identical", who);
     RunArgs a;
     memset(&a, 0, sizeof(a));
     a.L = *L;
@@ -607,6 +628,7 @@ extern "C" dit_status dit_ulysses_pack_joint(const dit_sp_layout* L, int nplanes
     if (!dtype_ok(src_dt) || !wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
     if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
     if (S_txt < 0 || S_txt > L->S) return fail(DIT_ERR_INVALID_ARG, "%s: S_txt out of [0, S]", who);
+    if (L->S == 0) return empty_exchange(L, wire_dt, who);
     if (!send || !aligned16(send)) return fail(DIT_ERR_INVALID_ARG, "%s: send NULL or misaligned", who);
     const bool has_txt = S_txt > 0, has_img = S_txt < L->S;
     if ((has_txt && !txt) || (has_img && !img)) return fail(DIT_ERR_INVALID_ARG, "%s: stream array NULL", who);
@@ -642,6 +664,7 @@ extern "C" dit_status dit_ulysses_unpack_joint(const dit_sp_layout* L, const voi
     if (s != DIT_OK) return s;
     if (!wire_ok(wire_dt) || !dtype_ok(out_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad dtype", who);
     if (S_txt < 0 || S_txt > L->S) return fail(DIT_ERR_INVALID_ARG, "%s: S_txt out of [0, S]", who);
+    if (L->S == 0) return empty_exchange(L, wire_dt, who);
     if (!recv || !aligned16(recv)) return fail(DIT_ERR_INVALID_ARG, "%s: recv NULL or misaligned", who);
     const bool has_txt = S_txt > 0, has_img = S_txt < L->S;
     if ((has_txt && (!out_txt || !aligned16(out_txt))) || (has_img && (!out_img || !aligned16(out_img))))
@@ -673,11 +696,15 @@ extern "C" dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplane
     if (!wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad wire dtype", who);
     if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
     if (rope_planes >> nplanes) return fail(DIT_ERR_INVALID_ARG, "%s: rope_planes names a missing plane", who);
-    if (rope_planes && (!cos_tab || !sin_tab || !aligned16(cos_tab) || !aligned16(sin_tab)))
-        return fail(DIT_ERR_INVALID_ARG, "%s: rotary tables NULL or misaligned", who);
     if (rope_planes && L->D > kRopeMaxD && wire_dt != DIT_E4M3)
         return fail(DIT_ERR_UNSUPPORTED, "%s: rotary path supports D <= %d", who, kRopeMaxD);
-    if (!recv || !aligned16(recv) || !dst || !dst_dt)
+    if (!dst_dt) return fail(DIT_ERR_INVALID_ARG, "%s: dst_dt NULL", who);
+    for (int p = 0; p < nplanes; ++p)
+        if (!dtype_ok(dst_dt[p])) return fail(DIT_ERR_INVALID_ARG, "%s: bad dst dtype", who);
+    if (L->S == 0) return empty_exchange(L, wire_dt, who);
+    if (rope_planes && (!cos_tab || !sin_tab || !aligned16(cos_tab) || !aligned16(sin_tab)))
+        return fail(DIT_ERR_INVALID_ARG, "%s: rotary tables NULL or misaligned", who);
+    if (!recv || !aligned16(recv) || !dst)
         return fail(DIT_ERR_INVALID_ARG, "%s: recv/dst NULL or misaligned", who);
     RunArgs a;
     memset(&a, 0, sizeof(a));
@@ -686,7 +713,6 @@ extern "C" dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplane
     a.src[0] = recv; a.src_dt[0] = wire_dt;
     for (int p = 0; p < nplanes; ++p) {
         if (!dst[p] || !aligned16(dst[p])) return fail(DIT_ERR_INVALID_ARG, "%s: dst[%d] NULL or misaligned", who, p);
-        if (!dtype_ok(dst_dt[p])) return fail(DIT_ERR_INVALID_ARG, "%s: bad dst dtype", who);
         a.dst[p] = dst[p];
         a.dst_dt[p] = dst_dt[p];
     }

@@ -269,3 +269,72 @@ def test_layout_with_lcm_padding_changes_wire_sizes(dl):
     assert L.S_pad == 4544 and L.wire_elems(3) == 3 * 4544 * 24 * 128
     assert L.wire_bytes_e4m3(2) == 2 * 4544 * 24 * 144
     assert [L.real_rows(r) for r in range(2)] == [2272, 2209]
+
+
+@pytest.mark.parametrize("pad_lcm64", [False, True])
+def test_empty_layout_moves_nothing(dl, pad_lcm64):
+    """S = 0: every buffer of the exchange is empty (an allocator gives NULL
+    for zero bytes), so each call checks its other arguments and returns
+    DIT_OK without a launch; the answer to a bad argument does not change."""
+    L = dl.lib()
+    lay = dl.DitSpLayout()
+    flags = dl.DIT_LAYOUT_PAD_LCM64 if pad_lcm64 else 0
+    assert L.dit_sp_layout_init_ex(3, 0, 9, 32, 1, 4, flags, ctypes.byref(lay)) == 0
+    assert lay.S_pad == 0
+    null3 = (ctypes.c_void_p * 3)(None, None, None)
+    dts = (ctypes.c_int * 3)(dl.DIT_BF16, dl.DIT_BF16, dl.DIT_F16)
+    ok = dl.DIT_OK
+    for wire in (dl.DIT_BF16, dl.DIT_E4M3):
+        assert L.dit_ulysses_pack(ctypes.byref(lay), 0, 3, null3, dl.DIT_BF16, None, wire, None) == ok
+        assert L.dit_ulysses_pack(ctypes.byref(lay), 1, 1, null3, dl.DIT_BF16, None, wire, None) == ok
+        assert L.dit_a2a_sim(ctypes.byref(lay), 0, 3, None, None, wire, None) == ok
+        assert L.dit_ulysses_unpack(ctypes.byref(lay), 0, 3, None, wire, null3, dts, None, None) == ok
+        assert L.dit_ulysses_unpack(ctypes.byref(lay), 1, 1, None, wire, null3, dts, None, None) == ok
+        assert L.dit_ulysses_unpack_rope(ctypes.byref(lay), 3, None, wire, null3, dts, None, None, 0b011, None,
+                                         None) == ok
+        assert L.dit_ulysses_pack_joint(ctypes.byref(lay), 3, None, None, 0, dl.DIT_BF16, None, wire, None) == ok
+        assert L.dit_ulysses_unpack_joint(ctypes.byref(lay), None, wire, None, None, 0, dl.DIT_BF16, None) == ok
+        assert L.dit_a2a_sim_checked(ctypes.byref(lay), 0, 3, None, None, wire, ctypes.c_void_p(1 << 20), 1,
+                                     1000, None, None) == ok
+    # the other arguments are still checked
+    assert L.dit_ulysses_pack(ctypes.byref(lay), 1, 3, null3, dl.DIT_BF16, None, dl.DIT_BF16, None) \
+        == dl.DIT_ERR_INVALID_ARG                            # head-to-seq with 3 planes
+    assert L.dit_ulysses_unpack(ctypes.byref(lay), 0, 3, None, dl.DIT_BF16, null3, None, None, None) \
+        == dl.DIT_ERR_INVALID_ARG                            # no destination types
+    assert L.dit_a2a_sim_checked(ctypes.byref(lay), 0, 3, None, None, dl.DIT_BF16, None, 1, 1000, None, None) \
+        == dl.DIT_ERR_INVALID_ARG                            # counters required
+    lay24 = dl.DitSpLayout()
+    assert L.dit_sp_layout_init(1, 0, 4, 24, 2, 1, ctypes.byref(lay24)) == 0
+    assert L.dit_ulysses_pack(ctypes.byref(lay24), 0, 3, null3, dl.DIT_BF16, None, dl.DIT_E4M3, None) \
+        == dl.DIT_ERR_UNSUPPORTED                            # e4m3 head dim, as with S > 0
+
+
+def test_attention_without_rows_touches_nothing(dl):
+    """No query rows: attention and the merge check their sizes, types and
+    strides, then return DIT_OK without a launch, with NULL buffers."""
+    from sequence_attention_gb300._lib import DitLseView
+    L = dl.lib()
+    null, lse = _view(0, 0, 4 * 128, 128), DitLseView()
+    assert L.dit_attention(1, 4, 128, 0.1, 0, 64, null, dl.DIT_BF16, null, null, dl.DIT_F16, null,
+                           dl.DIT_BF16, lse, None, None) == dl.DIT_OK
+    assert L.dit_attention(1, 4, 96, 0.1, 0, 64, null, dl.DIT_BF16, null, null, dl.DIT_F16, null,
+                           dl.DIT_BF16, lse, None, None) == dl.DIT_ERR_UNSUPPORTED    # D still checked
+    zeros = (ctypes.c_int * 2)(0, 0)
+    lens = (ctypes.c_int * 2)(5, 0)
+    o = _view(0, 0, 4 * 128, 128)
+    o.stride_q, o.stride_kv = 2 * 8 * 4 * 128, 8 * 4 * 128   # blocks of the (empty) output stay apart
+    assert L.dit_attn_partial(1, 4, 128, 0.1, 2, zeros, 2, lens, null, dl.DIT_BF16, null, null, dl.DIT_F16,
+                              o, dl.DIT_F32, lse, None, None) == dl.DIT_OK
+    assert L.dit_attn_merge_lse(1, 4, 128, 2, zeros, 2, null, dl.DIT_F32, lse, null, dl.DIT_BF16, lse,
+                                None) == dl.DIT_OK
+    assert L.dit_attn_merge_lse(1, 4, 128, 2, lens, 2, null, dl.DIT_F32, lse, null, dl.DIT_BF16, lse,
+                                None) == dl.DIT_ERR_INVALID_ARG                      # rows need buffers
+    cu = (ctypes.c_int * 3)(0, 0, 0)
+    assert L.dit_attn_varlen(4, 128, 0.1, 2, cu, cu, null, dl.DIT_BF16, null, null, dl.DIT_F16, null,
+                             dl.DIT_BF16, lse, None, None) == dl.DIT_OK
+    # rows but NULL Q is still an error; NULL K and V with keys too
+    assert L.dit_attention(1, 4, 128, 0.1, 8, 0, null, dl.DIT_BF16, null, null, dl.DIT_F16, null,
+                           dl.DIT_BF16, lse, None, None) == dl.DIT_ERR_INVALID_ARG
+    q = _view(1 << 20, 64 * 4 * 128, 4 * 128, 128)
+    assert L.dit_attention(1, 4, 128, 0.1, 8, 8, q, dl.DIT_BF16, null, null, dl.DIT_F16, q,
+                           dl.DIT_BF16, lse, None, None) == dl.DIT_ERR_INVALID_ARG

@@ -188,6 +188,35 @@ def test_walk_with_every_key_block_empty():
     assert torch.isnan(o[1, :, :, 120:]).all() and torch.isnan(lse[1, :, :, :, 120:]).all()
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_empty_tensors(dt):
+    """Zero-size tensors (a NULL pointer from the allocator): with no keys
+    the output is the empty chunk's O = 0, lse = -inf; with no query rows
+    nothing is launched and nothing is written."""
+    import sequence_attention_gb300 as sa
+    tdt = {"bf16": torch.bfloat16, "f32": torch.float32}[dt]
+    vdt = torch.float16 if dt == "bf16" else torch.float32
+    B, Sq, H, D = 2, 200, 3, 128
+    q = synth.normal((B, Sq, H, D), 61, 0.5, dt).cuda()
+    k = torch.empty((B, 0, H, D), dtype=tdt, device="cuda")
+    v = torch.empty((B, 0, H, D), dtype=vdt, device="cuda")
+    assert k.data_ptr() == 0 and v.data_ptr() == 0
+    o = torch.full((B, Sq, H, D), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((B, H, Sq), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sa.dit_attention(q, k, v, o, lse, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+    # no query rows: keys present or not, the call is a no-op
+    kk = synth.normal((B, 64, H, D), 62, 0.5, dt).cuda()
+    q0 = torch.empty((B, 0, H, D), dtype=tdt, device="cuda")
+    o0 = torch.empty((B, 0, H, D), dtype=torch.float32, device="cuda")
+    sa.dit_attention(q0, kk, kk.to(vdt), o0)
+    sa.dit_attention(q0, k, v, o0)
+    torch.cuda.synchronize()
+
+
 def test_merge_kernel_against_oracle_merge():
     """Merge alone on random partials (fp32 parts, bf16 out), with an all-empty row."""
     import sequence_attention_gb300 as sa

@@ -27,14 +27,21 @@ def _case(seed):
 # ranks, DIT_MAX_R = 8 ring blocks), with uneven rows and head groups
 MAX_CASES = [(1, 701, 5, 16, 64, 1, True, False), (2, 301, 3, 32, 8, 8, False, True),
              (1, 517, 70, 16, 64, 1, False, False), (1, 129, 9, 64, 2, 8, True, True)]
+# an empty sequence (every buffer has zero bytes, so its pointer is NULL),
+# with and without the lcm(U*R, 64) padding; the first is the draw of seed 432
+EMPTY_CASES = [(3, 0, 9, 32, 1, 4, True, True), (1, 0, 5, 64, 4, 2, False, False)]
 
 
-@pytest.mark.parametrize("seed", list(range(40)) + [f"max{i}" for i in range(len(MAX_CASES))])
+@pytest.mark.parametrize("seed", list(range(40)) + [f"max{i}" for i in range(len(MAX_CASES))]
+                         + [f"empty{i}" for i in range(len(EMPTY_CASES))])
 def test_random_layouts_bit_exact(seed):
     import sequence_attention_gb300 as sa
-    if isinstance(seed, str):
+    if isinstance(seed, str) and seed.startswith("max"):
         B, S, H, D, U, R, ph, pl = MAX_CASES[int(seed[3:])]
         seed = 500 + int(seed[3:])
+    elif isinstance(seed, str):
+        B, S, H, D, U, R, ph, pl = EMPTY_CASES[int(seed[5:])]
+        seed = 600 + int(seed[5:])
     else:
         B, S, H, D, U, R, ph, pl = _case(seed)
     L = sa.dit_sp_layout_init(B, S, H, D, U, R, pad_heads=ph, pad_lcm64=pl)

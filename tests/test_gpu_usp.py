@@ -164,3 +164,17 @@ def test_double_stream_block_with_rope(B, S, H, U, R, S_txt):
     got = np.concatenate([f64(out_t), f64(out_i)], axis=1)
     assert_bf16_close(got, ref, "double-stream attention")
     assert int(plan.range_flag.item()) == 0
+
+
+@pytest.mark.parametrize("U,R", [(2, 2), (1, 3)])
+def test_empty_sequence(U, R):
+    """S = 0: every call of the step sees zero-size buffers (NULL pointers)
+    and launches nothing; the step completes with a clean status."""
+    from sequence_attention_gb300.usp import UspPlan
+    B, H, D = 1, 3, 64
+    q, k, v = (torch.empty((B, 0, H, D), dtype=torch.bfloat16, device="cuda") for _ in range(3))
+    out = torch.empty((B, 0, H, D), dtype=torch.bfloat16, device="cuda")
+    plan = UspPlan(B, 0, H, D, U, R)
+    plan.run(q, k, v, out)
+    torch.cuda.synchronize()
+    assert int(plan.status.item()) == 0 and int(plan.range_flag.item()) == 0
