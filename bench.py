@@ -384,9 +384,10 @@ def run_ours(args):
     # the ncu note covers the attention launch of the default FLUX-like workload
     traffic = traffic_per_launch(ATTN_SRC, TRAFFIC_NOTE) if (w.name == "flux1024" and w.R == 1) else None
     attn_kernel = f"attn_f32_kernel<{w.D}>" if w.dtype == "f32" else f"attn_tc_kernel<{w.D},false>"
-    # merge bytes: R fp32 partials and their LSE per real row and head, the
-    # output written once (16-bit)
-    merge_bytes = w.B * w.S * w.H * (w.R * (w.D * 4 + 4) + w.D * 2)
+    # merge bytes: R partials (in the plan's partial type) and their LSE per
+    # real row and head, the output written once (16-bit)
+    pb = plan.parts.element_size() if w.R > 1 else 4
+    merge_bytes = w.B * w.S * w.H * (w.R * (w.D * pb + 4) + w.D * 2)
 
     # one step alone, launched call by call and replayed from its own CUDA
     # graph (L2 flushed before each, median of 20): the cost of the launches
@@ -777,9 +778,11 @@ def run_sweep(args):
         tf = fl / (med[1] * 1e-3) / 1e12
         tfm = fl / ((med[1] + med[2]) * 1e-3) / 1e12
         L = plan.L
-        # merge bytes: R partials (fp32 O and LSE) of every ring block read, the output written
+        # merge bytes: R partials (O in the plan's partial type, and LSE) of
+        # every ring block read, the output written
         rows = w.B * w.S * w.H
-        merge_bytes = rows * (w.R * (w.D * 4 + 4) + w.D * plan.o_h.element_size()) if w.R > 1 else 0
+        pb = plan.parts.element_size() if w.R > 1 else 0
+        merge_bytes = rows * (w.R * (w.D * pb + 4) + w.D * plan.o_h.element_size()) if w.R > 1 else 0
         res = {"workload": name, "U": U, "R": w.R, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "dtype": w.dtype,
                "step_ms": round(sum(med), 4), "layout_in_ms": round(med[0], 4),
                "attention_ms": round(med[1], 4), "attention_TFLOPs": round(tf, 1),

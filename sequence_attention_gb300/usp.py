@@ -43,14 +43,21 @@ class UspPlan:
                  device: str = "cuda", scale: Optional[float] = None,
                  rope: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
                  fp8_qv: bool = False, fp8_o: bool = False,
-                 pad_heads: bool = True, pad_lcm64: bool = False):
+                 pad_heads: bool = True, pad_lcm64: bool = False,
+                 parts_dtype: Optional[torch.dtype] = None):
         """rope: optional (cos, sin) float32 [S, D/2] device tables of the
         joint sequence; Q and K are then rotated by the receive preparation.
         fp8_qv / fp8_o: Q and V (one exchange) / the output cross the
         all-to-all as e4m3 records; K keeps its own 16-bit exchange.
         pad_heads=False: uneven head groups without padding; pad_lcm64: the
         sequence padded to a multiple of lcm(U*R, 64), padding rows excluded
-        from attention."""
+        from attention.
+        parts_dtype: type of the R x R ring partials (R > 1).  By default f16
+        when V is f16 and the output 16-bit: a partial is a convex
+        combination of V rows, so it stays within V's range, and f16 keeps
+        11 significant bits against the output's 8 (bf16), at half the
+        bytes of f32 for the attention's stores and the merge's loads.
+        Otherwise f32."""
         self.L = dit_sp_layout_init(B, S, H, D, U, R, pad_heads, pad_lcm64)
         self.B, self.S, self.H, self.D, self.U, self.R = B, S, H, D, U, R
         self.in_dtype = in_dtype
@@ -77,8 +84,14 @@ class UspPlan:
         self.k_h = torch.empty(hs, dtype=in_dtype, device=dev)
         self.v_h = torch.empty(hs, dtype=v_dtype, device=dev)
         self.o_h = torch.empty(hs, dtype=self.out_dtype, device=dev)
+        if parts_dtype is None:
+            half_ok = v_dtype == torch.float16 and self.out_dtype in (torch.bfloat16, torch.float16)
+            parts_dtype = torch.float16 if half_ok else torch.float32
+        if parts_dtype == torch.float16 and v_dtype != torch.float16:
+            raise ValueError("f16 partials need f16 V (a partial lies within V's range)")
+        self.parts_dtype = parts_dtype
         if R > 1:
-            self.parts = torch.empty((R, R) + tuple(hs[1:]), dtype=torch.float32, device=dev)
+            self.parts = torch.empty((R, R) + tuple(hs[1:]), dtype=parts_dtype, device=dev)
             self.lse_parts = torch.empty((R, R, B, L.Hp, L.S_cap), dtype=torch.float32, device=dev)
         else:
             self.parts = self.lse_parts = None

@@ -338,3 +338,17 @@ def test_attention_without_rows_touches_nothing(dl):
     q = _view(1 << 20, 64 * 4 * 128, 4 * 128, 128)
     assert L.dit_attention(1, 4, 128, 0.1, 8, 8, q, dl.DIT_BF16, null, null, dl.DIT_F16, q,
                            dl.DIT_BF16, lse, None, None) == dl.DIT_ERR_INVALID_ARG
+
+
+def test_plan_partial_type(dl):
+    """Ring partials are f16 when V is f16 and the output 16-bit (a partial
+    lies within V's range), f32 otherwise; f16 partials without f16 V are
+    refused.  Plans are built on the host here: nothing is launched."""
+    import torch
+    from sequence_attention_gb300.usp import UspPlan
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu").parts.dtype == torch.float16
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", out_dtype=torch.float32).parts.dtype == torch.float32
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", v_dtype=torch.bfloat16).parts.dtype == torch.float32
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", parts_dtype=torch.float32).parts.dtype == torch.float32
+    with pytest.raises(ValueError):
+        UspPlan(1, 64, 2, 64, 2, 2, device="cpu", v_dtype=torch.bfloat16, parts_dtype=torch.float16)

@@ -178,3 +178,22 @@ def test_empty_sequence(U, R):
     plan.run(q, k, v, out)
     torch.cuda.synchronize()
     assert int(plan.status.item()) == 0 and int(plan.range_flag.item()) == 0
+
+
+def test_half_partials_against_float_partials():
+    """The step's default f16 ring partials against f32 ones (both with f32
+    output), FLUX-1008-like (R = 2): within the merge bar of 1e-3 rel-RMS.
+    (The default step's output against the oracle is covered above.)"""
+    from sequence_attention_gb300.usp import UspPlan
+    from tests.helpers import MERGE_REL_RMS, rel_rms
+    w = synth.WORKLOADS["flux1008"]
+    q, k, v = (t.cuda() for t in w.qkv())
+    outs = {}
+    for pdt in (torch.float16, torch.float32):
+        plan = UspPlan(w.B, w.S, w.H, w.D, 4, w.R, out_dtype=torch.float32, parts_dtype=pdt)
+        assert plan.parts.dtype == pdt
+        outs[pdt] = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.float32, device="cuda")
+        plan.run(q, k, v, outs[pdt])
+        torch.cuda.synchronize()
+        assert int(plan.status.item()) == 0
+    assert rel_rms(f64(outs[torch.float16]), f64(outs[torch.float32])) <= MERGE_REL_RMS
