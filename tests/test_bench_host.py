@@ -54,3 +54,27 @@ def test_malformed_lines_are_skipped_and_missing_tool_gives_nulls(monkeypatch):
         pass
     s = cs2.summary()
     assert s["sm_mhz"] is None and s["samples"] == 0
+
+
+def test_reference_arm_line(capsys, monkeypatch):
+    """The reference arm (the fp64 oracle on the host cores) prints one JSON
+    line with the contract's keys; under a launcher only rank 0 prints."""
+    import json
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    bench.main(["--impl", "reference", "--steps", "2", "--warmup", "0", "--workload", "tiny",
+                "--cpu-budget", "0.01"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 2
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0", "--workload", "tiny",
+                "--cpu-budget", "0.01"])
+    assert capsys.readouterr().out.strip() == ""
