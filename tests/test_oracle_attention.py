@@ -149,6 +149,22 @@ def test_merge_of_any_partition_equals_single_shot(cuts):
     np.testing.assert_allclose(lse2, lse, atol=1e-14)
 
 
+def test_partial_lies_between_the_values_it_averages():
+    """A chunk-normalised partial is a convex combination of the chunk's V
+    rows: every element lies between that column's smallest and largest
+    value (so it cannot leave V's range, whatever its storage type).  A
+    missing or wrong normalisation fails this."""
+    q = _rand((2, 9, 3, 8), 80) * 4.0
+    k = _rand((2, 40, 3, 8), 81) * 4.0
+    v = _rand((2, 40, 3, 8), 82) * 3.0e4
+    for a, b in ((0, 40), (5, 6), (7, 33)):
+        o, _ = att.partial(q, k[:, a:b], v[:, a:b])
+        lo = v[:, a:b].min(axis=1, keepdims=True)
+        hi = v[:, a:b].max(axis=1, keepdims=True)
+        slack = 1e-12 * np.abs(v).max()
+        assert np.all(o >= lo - slack) and np.all(o <= hi + slack)
+
+
 def test_merge_of_one_part_is_identity():
     q, k, v = _rand((1, 4, 2, 8), 33), _rand((1, 9, 2, 8), 34), _rand((1, 9, 2, 8), 35)
     p = att.attention(q, k, v)
