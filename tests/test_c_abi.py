@@ -1,7 +1,7 @@
 """The boundary is a plain C ABI: a C99 program that includes only
 include/ditsp.h compiles with gcc, links against libditsp.so and runs the
 host-side calls (layout, all-to-all counts, argument validation, error
-strings) without Python, torch or a GPU; and the last-error string is kept
+strings, the empty exchange) without Python, torch or a GPU; and the last-error string is kept
 per calling thread."""
 import ctypes
 import os
@@ -33,6 +33,12 @@ int main(void) {
     printf("S_pad=%d Hp=%d head_len0=%d\n", L.S_pad, L.Hp, L.head_len[0]);
     s = dit_sp_layout_init(0, 8, 1, 8, 1, 1, &L);        /* B = 0 is refused */
     printf("bad=%s msg=%s\n", dit_status_string(s), strlen(dit_last_error()) > 0 ? "yes" : "no");
+    /* an empty sequence: the exchange moves nothing and takes NULL buffers */
+    s = dit_sp_layout_init(1, 0, 4, 64, 2, 2, &L);
+    const void* none[3] = {NULL, NULL, NULL};
+    dit_status e1 = dit_ulysses_pack(&L, DIT_SEQ_TO_HEAD, 3, none, DIT_BF16, NULL, DIT_BF16, NULL);
+    dit_status e2 = dit_a2a_sim(&L, DIT_SEQ_TO_HEAD, 3, NULL, NULL, DIT_BF16, NULL);
+    printf("empty=%s,%s,%s\n", dit_status_string(s), dit_status_string(e1), dit_status_string(e2));
     return 0;
 }
 """
@@ -60,6 +66,7 @@ def test_plain_c_program_uses_the_library(built, tmp_path):
     assert out[1] == f"send0={3 * 2 * 715 * 5 * 128} recv4={3 * 2 * 714 * 5 * 128}"
     assert out[2] == "S_pad=4544 Hp=24 head_len0=6"
     assert out[3] == "bad=DIT_ERR_INVALID_ARG msg=yes"
+    assert out[4] == "empty=DIT_OK,DIT_OK,DIT_OK"
 
 
 def test_last_error_is_per_thread():
