@@ -298,8 +298,11 @@ def run_ours(args):
     from sequence_attention_gb300.usp import UspPlan
 
     w, U = workload_config(args.workload, args.U)
-    q, k, v = (t.to(dev) for t in w.qkv())
-    pred = w.cfg_pair().to(dev)
+    host_qkv, host_pred = w.qkv(), w.cfg_pair()
+    inputs_sha = synth.digest(*host_qkv, host_pred)
+    q, k, v = (t.to(dev) for t in host_qkv)
+    pred = host_pred.to(dev)
+    del host_qkv, host_pred
     out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev)
     cfg_out = torch.empty(w.cfg_shape[1:], dtype=synth.torch_dtype(w.cfg_out), device=dev)
     plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev))
@@ -425,7 +428,8 @@ def run_ours(args):
                                f"{w.cfg_in}->{w.cfg_out} g={w.g}",
                    "B": w.B, "S": w.S, "H": w.H, "D": w.D, "U": U, "R": w.R,
                    "parallelism": f"virtual ranks U{U}xR{w.R} on one GPU; replicas across GPUs",
-                   "l2": "flushed before every timed step (256 MiB write, outside the events)"},
+                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "inputs_sha256": inputs_sha},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["bf16_tflops"], 4),

@@ -68,6 +68,16 @@ def as_bits(t: torch.Tensor) -> np.ndarray:
     raise ValueError("unsupported element size")
 
 
+def digest(*tensors: torch.Tensor) -> str:
+    """First 16 hex digits of the SHA-256 of the tensors' raw bytes, in
+    order: a record of exactly which inputs a run used."""
+    import hashlib
+    h = hashlib.sha256()
+    for t in tensors:
+        h.update(as_bits(t).tobytes())
+    return h.hexdigest()[:16]
+
+
 def _tables(angles: np.ndarray):
     """float32 cos/sin tables of float64 angles [S, D/2] (RNE to float32)."""
     return (torch.from_numpy(np.cos(angles).astype(np.float32)),
