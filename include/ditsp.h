@@ -352,11 +352,13 @@ DIT_API dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplanes, 
  *            lse.ptr may be NULL (not written)
  *   q_len, kv_len: host arrays; n_q, n_kv <= DIT_MAX_R.
  *
- * Supported: (qk_dt, v_dt) = (F32, F32) with o_dt F32 and D a multiple of 4
- * up to 128 (fp32 CUDA-core path); or qk_dt in {BF16, F16}, v_dt in {BF16,
+ * Supported: (qk_dt, v_dt) = (F32, F32) with o_dt F32 and D in {16, 32,
+ * 64, 128} (fp32 CUDA-core path); or qk_dt in {BF16, F16}, v_dt in {BF16,
  * F16}, D in {64, 128}, o_dt in {F32, BF16, F16} (tensor-core path: Q K^T
  * in qk_dt with fp32 accumulation; P rounded to v_dt for P V with fp32
- * accumulation).  Strides and pointers must be 16-byte aligned.
+ * accumulation).  Strides and pointers must be 16-byte aligned.  Each o row
+ * is a convex combination of V rows, so o_dt = F16 cannot overflow when
+ * v_dt is F16.
  * Head dims other than these return DIT_ERR_UNSUPPORTED.  The output view
  * must give every result its own address: a zero o stride on a dimension
  * with more than one index (stride_h with H > 1, stride_s with a block of
