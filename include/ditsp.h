@@ -225,8 +225,9 @@ DIT_API dit_status dit_sp_a2a_counts(const dit_sp_layout* L, dit_a2a_dir dir, in
  *   DIT_HEAD_TO_SEQ: dst[0] is a seq-layout tensor [B][S][H][D] in dst_dt[0];
  *     padded heads are dropped.
  *
- * The three calls require D*sizeof(type) to be a multiple of 16 bytes for
- * every type involved and 16-byte aligned pointers.  send/recv must not
+ * The three calls require D to be a multiple of 8 (so that a head row is a
+ * multiple of 16 bytes in every type; else DIT_ERR_UNSUPPORTED) and 16-byte
+ * aligned pointers.  send/recv must not
  * overlap any other buffer of the same call.
  *
  * wire_dt = DIT_E4M3 (cache-dit "Context Parallelism", Async FP8 Ulysses
