@@ -324,7 +324,9 @@ DIT_API dit_status dit_ulysses_unpack_joint(const dit_sp_layout* L, const void* 
  *   rope_planes       bit mask over the nplanes planes (0x3 = Q and K);
  *                     0 gives dit_ulysses_unpack exactly.
  * Padded heads stay zero.  d_range_flag as for dit_ulysses_unpack (a 16-bit
- * destination value that becomes infinite sets it).
+ * destination value that becomes infinite sets it).  On a 16- or 32-bit wire
+ * the rotation needs D <= 384 (else DIT_ERR_UNSUPPORTED); the e4m3 wire takes
+ * its own D set.
  */
 DIT_API dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplanes, const void* recv,
                                            dit_dtype wire_dt, void* const* dst, const dit_dtype* dst_dt,
