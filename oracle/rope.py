@@ -47,16 +47,23 @@ def receive_prep(L, recv: np.ndarray, wire_dt: str, dst_dts, cos: np.ndarray, si
     a rotated plane as float64 (the exact rotation of the received values,
     before the rounding to its destination type); any other plane as the
     storage bits of dst_dts[p], as ``ulysses.s2h_unpack`` gives them.  Row s
-    of ring block r is the token at joint position ring_off[r] + s.
+    of ring block r is the token at joint position ring_off[r] + s; rows of
+    an lcm(SP, 64)-padded layout at or past S are padding, never rotated
+    (xLLM "DiT Architecture and Capability Matrix": the padding is not part
+    of the sequence).
     """
     from . import numeric, ulysses
 
     kinds = [wire_dt if (rope_planes >> p) & 1 else dt for p, dt in enumerate(dst_dts)]
     ranks = ulysses.s2h_unpack(L, recv, wire_dt, kinds)
     for (r, _v), planes in ranks.items():
-        rows = slice(L.ring_off[r], L.ring_off[r] + L.ring_len[r])
+        # the tables hold the S real tokens: rows of a padded layout at or
+        # past S (sequence padding) are not rotated and stay zero
+        n = L.real_rows(r)
+        rows = slice(L.ring_off[r], L.ring_off[r] + n)
         for p in range(len(planes)):
             if (rope_planes >> p) & 1:
                 x = numeric.to_f64(planes[p], wire_dt)
-                planes[p] = rope(x, np.asarray(cos)[rows], np.asarray(sin)[rows])
+                x[:, :n] = rope(x[:, :n], np.asarray(cos)[rows], np.asarray(sin)[rows])
+                planes[p] = x
     return ranks

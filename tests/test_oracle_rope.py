@@ -1,5 +1,6 @@
 """Pins for the oracle's rotary embedding: the properties that define it."""
 import numpy as np
+import pytest
 
 from oracle import rope as orope
 
@@ -73,13 +74,15 @@ def _global_planes(B, S, H, D, n, dt, seed):
     return [bits(t) for t in ts]
 
 
-def test_receive_prep_matches_direct_indexing():
+@pytest.mark.parametrize("pad_lcm64", [False, True])
+def test_receive_prep_matches_direct_indexing(pad_lcm64):
     # brute force: every head-layout element of every rank, read straight
-    # from the rotated global planes (no send/receive bookkeeping)
+    # from the rotated global planes (no send/receive bookkeeping); rows of
+    # the padded layout at or past S are zero and unrotated
     import synth
     from oracle import layout as olayout, numeric, ulysses
     B, S, H, D, U, R = 2, 23, 5, 8, 3, 2
-    L = olayout.make_layout(B, S, H, D, U, R)
+    L = olayout.make_layout(B, S, H, D, U, R, pad_lcm64=pad_lcm64)
     planes = _global_planes(B, S, H, D, 3, "bf16", 40)
     cos, sin = (t.numpy().astype(np.float64) for t in synth.rope_tables_linear(S, D))
     recv = ulysses.a2a(L, "s2h", 3, ulysses.s2h_pack(L, planes, "bf16", "bf16"))
@@ -90,12 +93,14 @@ def test_receive_prep_matches_direct_indexing():
             t = L.ring_off[r] + s
             for hl in range(L.Hl):
                 h = v * L.Hl + hl
+                real = h < H and t < S
                 for p in range(2):
-                    want = rotated[p][:, t, h] if h < H else np.zeros((B, D))
+                    want = rotated[p][:, t, h] if real else np.zeros((B, D))
                     np.testing.assert_array_equal(pl[p][:, s, hl], want)
-                want_v = (numeric.convert_bits(planes[2][:, t, h], "bf16", "f16") if h < H
+                want_v = (numeric.convert_bits(planes[2][:, t, h], "bf16", "f16") if real
                           else np.zeros((B, D), np.uint16))
                 np.testing.assert_array_equal(pl[2][:, s, hl], want_v)
+    assert (L.S_pad > S) == pad_lcm64
 
 
 def test_receive_prep_with_zero_angles_is_the_plain_unpack():
