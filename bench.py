@@ -1,10 +1,13 @@
 """Benchmark of the sequence-parallel DiT attention hot path on GB300.
 
 One step = one pass of the whole path over one batch of synthetic input
-already resident in HBM: Ulysses pack -> simulated all-to-all -> unpack ->
-attention partials -> merge (when R > 1) -> inverse pack / all-to-all /
-unpack -> CFG combine.  The default workload is the FLUX-1024-like one
-(B=1, S=4608, H=24, D=128, U=4, R=1; CFG on [2,4608,3072] bf16, g=3.5).
+already resident in HBM: Ulysses seq->head layout -> attention partials ->
+merge (when R > 1) -> head->seq layout -> CFG combine.  The layout steps run
+as one pass each (--exchange direct, the default: on one memory the
+all-to-all aliases receive and send blocks) or as pack -> simulated
+all-to-all -> unpack (--exchange a2a, the calls a multi-GPU build keeps).
+The default workload is the FLUX-1024-like one (B=1, S=4608, H=24, D=128,
+U=4, R=1; CFG on [2,4608,3072] bf16, g=3.5).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--U U]
     python bench.py --impl reference ...     # the fp64 CPU oracle, timed
@@ -15,7 +18,10 @@ step (algorithmic 4*B*H*S^2*D flops / step time, summed over ranks);
 host<->device copies inside the timed region.  L2 is flushed (a 256 MiB
 write) before every timed step; only the step itself is inside the events
 (one at its start, one at its end); a second pass with events between the
-phases gives the per-phase split in `kernels`.
+phases gives the per-phase split in `kernels`.  The block of K timed steps
+is repeated back to back until it has run for at least half a second, so
+that the clock sampler (nvidia-smi, 20 ms period) takes its samples inside
+the timed region; `value` is the mean over every timed step.
 """
 from __future__ import annotations
 
@@ -172,6 +178,15 @@ def traffic_per_launch(kernel_src: str, note: str):
 
 
 # ---------------------------------------------------------------- workload
+def bench_config(w, U: int):
+    """The workload part of the JSON line's config, the same for both arms."""
+    return {"workload": f"{w.name}-like: B={w.B} S={w.S} H={w.H} D={w.D}, Ulysses U={U}, "
+                        f"ring R={w.R}; CFG [2,{','.join(map(str, w.cfg_shape[1:]))}] "
+                        f"{w.cfg_in}->{w.cfg_out} g={w.g}",
+            "B": w.B, "S": w.S, "H": w.H, "D": w.D, "U": U, "R": w.R,
+            "parallelism": f"virtual ranks U{U}xR{w.R} on one GPU; replicas across GPUs"}
+
+
 def workload_config(name: str, U: int):
     import synth
     w = synth.WORKLOADS[name]
@@ -180,43 +195,77 @@ def workload_config(name: str, U: int):
     return w, U
 
 
-_ORACLE_INPUTS = {}
+class OracleStep:
+    """The oracle's work on a workload, for the CPU baselines.
 
+    full():      the whole step as the oracle composes it (USP layout as an
+                 index permutation, attention partials of every rank, the
+                 log-sum-exp merge, the inverse layout) and the CFG combine.
+    attention(): plain fp64 attention of the given query rows (all heads)
+                 against every key, the oracle's definition of the result.
+    cfg():       the CFG combine of a leading fraction of the elements."""
 
-def _oracle_inputs(w):
-    """The workload's Q (bf16) and fp64 K, V per batch, made once per process
-    (generating them is not part of the timed oracle work)."""
-    import torch
-    if w.name not in _ORACLE_INPUTS:
+    def __init__(self, w, U: int):
+        import synth
+        from oracle import layout as olayout
+        self.w, self.U = w, U
+        self.L = olayout.make_layout(w.B, w.S, w.H, w.D, U, w.R)
         q, k, v = w.qkv()
-        _ORACLE_INPUTS[w.name] = (q, [k[b].to(torch.float64).numpy() for b in range(w.B)],
-                                  [v[b].to(torch.float64).numpy() for b in range(w.B)])
-    return _ORACLE_INPUTS[w.name]
+        self.qkv = [synth.as_f64(t) for t in (q, k, v)]
+        self.pred = synth.as_bits(w.cfg_pair()).reshape(2, -1)
 
+    def full(self):
+        from oracle import cfg as ocfg
+        from oracle import usp as ousp
+        o, _ = ousp.usp_attention(self.L, *self.qkv)
+        c = ocfg.cfg_combine_bits(self.pred, self.w.cfg_in, self.w.g, self.w.cfg_out)
+        return o, c
 
-def cpu_oracle_rate(w, budget_s: float, seed: int = 0):
-    """Time the fp64 oracle's attention on a bounded sample of query rows
-    (all heads, full key sequence): chunks of 256 rows until budget_s has
-    passed (at least one); returns (TFLOP/s, seconds, rows, cores)."""
-    import numpy as np
-    import torch
-    from oracle import attention as oatt
-    q, kf, vf = _oracle_inputs(w)
-    rng = np.random.default_rng(seed)
-    rows = rng.permutation(w.S)
-    chunk = max(16, min(256, w.S))
-    done = 0
-    flops = 0.0
-    t0 = time.perf_counter()
-    while done < w.S and (done == 0 or (time.perf_counter() - t0) < budget_s):
-        sel = np.sort(rows[done:done + chunk])
+    def rows(self, n: int, seed: int):
+        import numpy as np
+        return np.sort(np.random.default_rng(seed).choice(self.w.S, size=min(n, self.w.S), replace=False))
+
+    def attention(self, rows) -> float:
+        from oracle import attention as oatt
+        w = self.w
+        q, k, v = self.qkv
         for b in range(w.B):
-            qb = q[b, torch.from_numpy(sel)].to(torch.float64).numpy()
-            oatt.attention(qb[None], kf[b][None], vf[b][None])
-        flops += 4.0 * w.B * w.H * len(sel) * w.S * w.D
-        done += len(sel)
+            oatt.attention(q[b:b + 1, rows], k[b:b + 1], v[b:b + 1])
+        return 4.0 * w.B * w.H * len(rows) * w.S * w.D
+
+    def cfg(self, frac: float):
+        from oracle import cfg as ocfg
+        n = max(1, int(self.pred.shape[1] * frac))
+        ocfg.cfg_combine_bits(self.pred[:, :n], self.w.cfg_in, self.w.g, self.w.cfg_out)
+
+
+def oracle_baseline(w, U: int, budget_s: float):
+    """The oracle's attention timed on the host cores: every query row when
+    that fits budget_s (estimated from 64 rows), else a seeded sample of rows
+    sized to the budget, with the full time extrapolated from the sampled
+    rate and labelled as such."""
+    st = OracleStep(w, U)
+    t0 = time.perf_counter()
+    st.attention(st.rows(64, 5))
+    est = (time.perf_counter() - t0) * w.S / min(64, w.S)
+    cores = blas_threads()
+    full = est <= budget_s
+    rows = st.rows(w.S if full else max(16, int(w.S * budget_s / est)), 6)
+    t0 = time.perf_counter()
+    fl = st.attention(rows)
     dt = time.perf_counter() - t0
-    return flops / dt / 1e12, dt, done, blas_threads()
+    rate = fl / dt / 1e12
+    res = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle"}
+    if full:
+        res["sample"] = (f"full fp64 oracle attention: all {w.S} query rows x {w.H} heads x B={w.B} against all "
+                         f"{w.S} keys, {dt:.2f} s on the host cores")
+        res["full_s"] = round(dt, 3)
+    else:
+        res["sample"] = (f"fp64 oracle attention of {len(rows)} seeded query rows x {w.H} heads x B={w.B} against "
+                         f"all {w.S} keys, {dt:.1f} s on the host cores")
+        res["per_row_ms"] = round(dt / len(rows) * 1e3, 3)
+        res["extrapolated_full_s"] = round(w.attn_flops / (rate * 1e12), 1)
+    return res
 
 
 def cpu_oracle_kernels(budget_s: float = 30.0):
@@ -305,7 +354,8 @@ def run_ours(args):
     del host_qkv, host_pred
     out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev)
     cfg_out = torch.empty(w.cfg_shape[1:], dtype=synth.torch_dtype(w.cfg_out), device=dev)
-    plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev))
+    plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev),
+                   exchange=args.exchange)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -340,45 +390,66 @@ def run_ours(args):
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
 
-    def timed(phases):
+    def block(phases):
         barrier()
         torch.cuda.synchronize(dev)
-        with ClockSampler(gpu_index) as cs:
-            for i in range(K):
-                flush.zero_()
-                step(evs[i], phases)
-            torch.cuda.synchronize(dev)
+        for i in range(K):
+            flush.zero_()
+            step(evs[i], phases)
+        torch.cuda.synchronize(dev)
         barrier()
-        return cs.summary()
+
+    # repeats of the K-step block: enough for >= 0.5 s of wall time, so that
+    # the clock samples fall inside the timed region (the same count on
+    # every rank)
+    t0 = time.perf_counter()
+    block(False)
+    block_s = max(time.perf_counter() - t0, 1e-4)
+    reps = int(max_over_ranks(float(max(1, math.ceil(args.min_timed_s / block_s))), dev))
+
+    def timed(phases, nrep):
+        ms = []
+        with ClockSampler(gpu_index) as cs:
+            for _ in range(nrep):
+                block(phases)
+                if phases:
+                    ms.append([[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(5)])
+                else:
+                    ms.extend(e[0].elapsed_time(e[5]) for e in evs)
+        return cs.summary(), ms
 
     # The timed steps: events at each step's start and end only (an event
     # between two phases breaks their launch overlap); L2 flushed between
     # steps, outside the events.
-    clocks = timed(False)
+    clocks, step_ms = timed(False, reps)
     if any(r in clocks["reasons"] for r in BAD_REASONS):
-        clocks = timed(False)   # rejected once: measure again
+        clocks, step_ms = timed(False, reps)   # rejected once: measure again
         clocks["remeasured"] = True
-    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, dev)
     # A second pass with events between the phases gives the split below:
     # ms per segment: layout-in, attention partials, merge, layout-out, CFG
-    timed(True)
-    seg = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(5)]
+    _, split_blocks = timed(True, 1)
+    seg = split_blocks[0]
     split_ms = statistics.mean([sum(x) for x in zip(*seg)])
     attn_ms = statistics.mean(seg[1])          # the partial-attention launch alone
     flops = w.attn_flops
     value = ws * flops / (ms_max * 1e-3) / 1e12
 
-    # bytes of the bandwidth steps (real elements read + written)
+    # bytes of the bandwidth steps (real elements read + written; the head
+    # layout's padded heads are written, so they count)
     L = plan.L
     eb = 2 if w.dtype != "f32" else 4
     qkv_bytes = 3 * w.B * w.S * w.H * w.D * eb
     wire3 = 3 * w.B * w.S * L.Hp * w.D * eb
-    layout_in_bytes = (qkv_bytes + wire3) + 2 * wire3 + (wire3 + wire3)
     o_bytes = w.B * w.S * w.H * w.D * 2
     wire1 = w.B * w.S * L.Hp * w.D * 2
-    layout_out_bytes = (o_bytes + wire1) + 2 * wire1 + (wire1 + o_bytes)
+    if plan.exchange == "direct":
+        layout_in_bytes = qkv_bytes + wire3          # sequence planes in, head layout out
+        layout_out_bytes = o_bytes + o_bytes         # real heads of the head layout in, output out
+    else:
+        layout_in_bytes = (qkv_bytes + wire3) + 2 * wire3 + (wire3 + wire3)
+        layout_out_bytes = (o_bytes + wire1) + 2 * wire1 + (wire1 + o_bytes)
     cfg_n = pred.numel() // 2
     cfg_bytes = cfg_n * (2 * pred.element_size() + cfg_out.element_size())
 
@@ -421,14 +492,15 @@ def run_ours(args):
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
         "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_max, 4),
+        "repeats": reps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V, N(0,1) CFG branches)",
-        "config": {"workload": f"{w.name}-like: B={w.B} S={w.S} H={w.H} D={w.D}, Ulysses U={U}, "
-                               f"ring R={w.R}; CFG [2,{','.join(map(str, w.cfg_shape[1:]))}] "
-                               f"{w.cfg_in}->{w.cfg_out} g={w.g}",
-                   "B": w.B, "S": w.S, "H": w.H, "D": w.D, "U": U, "R": w.R,
-                   "parallelism": f"virtual ranks U{U}xR{w.R} on one GPU; replicas across GPUs",
+        "config": {**bench_config(w, U),
+                   "exchange": plan.exchange,
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "timing": f"CUDA events around each step; the block of {K} steps repeated {reps} times "
+                             f"back to back (>= {args.min_timed_s} s, so the clock samples fall inside); "
+                             f"value = mean over all {K * reps} timed steps",
                    "inputs_sha256": inputs_sha},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
@@ -454,16 +526,11 @@ def run_ours(args):
             **extra,
         },
         "e2e": e2e,
-        "gpu_launches": K * (len(names) - 1 + n_cfg_kernels),
+        "gpu_launches": K * reps * (len(names) - 1 + n_cfg_kernels),
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, secs, rows, cores = cpu_oracle_rate(w, args.cpu_budget)
-        res["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": cores,
-                               "kind": "oracle",
-                               "sample": f"fp64 numpy oracle attention of {rows} random query rows x "
-                                         f"{w.H} heads x B={w.B} against all {w.S} keys "
-                                         f"({secs:.1f} s on host cores)"}
+        res["cpu_baseline"] = oracle_baseline(w, U, args.cpu_budget)
         if not args.no_extra:
             res["cpu_baseline"]["bandwidth_steps"] = cpu_oracle_kernels()
     if rank == 0:
@@ -579,6 +646,12 @@ def back_to_back(w, U, dev):
                            lambda x: sa.dit_a2a_sim(L, H2S, 1, x[0], x[1]), 2 * wire1)
     res["unpack_h2s"] = timed(wire1, lambda: (rnd(L.wire_elems(1)), torch.empty(shp, dtype=dt, device=dev)),
                               lambda x: sa.dit_ulysses_unpack(L, H2S, x[0], [x[1]]), wire1 + plane)
+    # the one-pass layout steps of the default step (no wire buffers)
+    res["seq_to_head"] = timed(3 * plane, lambda: ([rnd(shp) for _ in range(3)],
+                                                   [torch.empty(hs, dtype=t, device=dev) for t in (dt, dt, v_dt)]),
+                               lambda x: sa.dit_ulysses_seq_to_head(L, x[0], x[1], flag), 3 * plane + wire3)
+    res["head_to_seq"] = timed(wire1, lambda: (rnd(hs), torch.empty(shp, dtype=dt, device=dev)),
+                               lambda x: sa.dit_ulysses_head_to_seq(L, x[0], x[1]), 2 * plane)
     cfg_in = {"f32": torch.float32, "bf16": torch.bfloat16}[w.cfg_in]
     cfg_out = {"f32": torch.float32, "bf16": torch.bfloat16}[w.cfg_out]
     n = 1
@@ -591,6 +664,9 @@ def back_to_back(w, U, dev):
     # and V (records of D + 16 bytes per token and head), on these shapes
     cos, sin = synth.rope_tables_linear(w.S, w.D)
     cos, sin = cos.to(dev), sin.to(dev)
+    res["seq_to_head_rope"] = timed(
+        3 * plane, lambda: ([rnd(shp) for _ in range(3)], [torch.empty(hs, dtype=t, device=dev) for t in (dt, dt, v_dt)]),
+        lambda x: sa.dit_ulysses_seq_to_head(L, x[0], x[1], flag, rope=(cos, sin)), 3 * plane + wire3 + 2 * w.S * w.D * 4)
     res["unpack_rope_s2h"] = timed(
         wire3, lambda: (rnd(L.wire_elems(3)), [torch.empty(hs, dtype=t, device=dev) for t in (dt, dt, v_dt)]),
         lambda x: sa.dit_ulysses_unpack_rope(L, x[0], x[1], cos, sin, 0b011, flag), 2 * wire3 + 2 * w.S * w.D * 4)
@@ -620,6 +696,14 @@ def back_to_back(w, U, dev):
                  torch.randn((R, R, wm.B, wm.H, cap), generator=gen, device=dev),
                  torch.empty((R, wm.B, cap, wm.H, wm.D), dtype=torch.bfloat16, device=dev)),
         lambda x: sa.dit_attn_merge_lse(x[0], x[1], x[2], None, rl), mbytes)
+    # ... and with the step's own f16 partials
+    mbytes16 = sum(rl) * wm.B * wm.H * (R * (wm.D * 2 + 4) + wm.D * 2)
+    res["merge_flux1008_f16"] = timed(
+        R * R * wm.B * cap * wm.H * wm.D * 2,
+        lambda: (torch.randn((R, R, wm.B, cap, wm.H, wm.D), generator=gen, device=dev).half(),
+                 torch.randn((R, R, wm.B, wm.H, cap), generator=gen, device=dev),
+                 torch.empty((R, wm.B, cap, wm.H, wm.D), dtype=torch.bfloat16, device=dev)),
+        lambda x: sa.dit_attn_merge_lse(x[0], x[1], x[2], None, rl), mbytes16)
     return {"back_to_back": res}
 
 
@@ -715,7 +799,8 @@ def fp8_wire_at_scale(dev, flush):
         w = synth.WORKLOADS[name]
         tag = "flux" if name == "flux1024" else name
         q, k, v = (torch.randn((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev) for _ in range(3))
-        plan16 = UspPlan(w.B, w.S, w.H, w.D, U, w.R, device=str(dev))
+        plan16 = UspPlan(w.B, w.S, w.H, w.D, U, w.R, device=str(dev), exchange="a2a")
+        plan1 = UspPlan(w.B, w.S, w.H, w.D, U, w.R, device=str(dev), exchange="direct")
         plan8 = UspPlan(w.B, w.S, w.H, w.D, U, w.R, device=str(dev), fp8_qv=True)
         L = plan8.L
         rec = 2 * w.B * w.S * L.Hp * (w.D + 16)
@@ -729,9 +814,10 @@ def fp8_wire_at_scale(dev, flush):
         res[f"unpack_e4m3_{tag}_GBs"] = round((rec + heads) / (ms * 1e-3) / 1e9, 1)
         res[f"layout_in_bf16_{tag}_ms"] = round(timed(lambda: plan16.layout_in(q, k, v)), 4)
         res[f"layout_in_e4m3_qv_{tag}_ms"] = round(timed(lambda: plan8.layout_in(q, k, v)), 4)
+        res[f"layout_in_direct_{tag}_ms"] = round(timed(lambda: plan1.layout_in(q, k, v)), 4)
         res[f"wire_bytes_ratio_{tag}"] = round((rec + w.B * w.S * L.Hp * w.D * 2) /
                                                (3 * w.B * w.S * L.Hp * w.D * 2), 4)
-        del q, k, v, plan16, plan8
+        del q, k, v, plan16, plan8, plan1
         torch.cuda.empty_cache()
     return res
 
@@ -755,7 +841,8 @@ def run_sweep(args):
         pred = w.cfg_pair().to(dev)
         out = torch.empty((w.B, w.S, w.H, w.D), dtype=q.dtype, device=dev)
         cfg_out = torch.empty(w.cfg_shape[1:], dtype=synth.torch_dtype(w.cfg_out), device=dev)
-        plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev))
+        plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev),
+                       exchange=args.exchange)
         stream = torch.cuda.current_stream(dev)
         reps = 3 if name == "wan" else 10
         seg = [[] for _ in range(5)]
@@ -796,7 +883,9 @@ def run_sweep(args):
                "attention_plus_merge_TFLOPs": round(tfm, 1),
                "layout_out_ms": round(med[3], 4), "cfg_ms": round(med[4], 4),
                "heads_padded": L.Hp - w.H, "status": int(plan.status.item()),
-               "range_flag": int(plan.range_flag.item())}
+               "range_flag": int(plan.range_flag.item()), "exchange": plan.exchange}
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = oracle_baseline(w, U, args.cpu_budget)
         print(json.dumps(res), flush=True)
         del q, k, v, pred, out, cfg_out, plan
         torch.cuda.empty_cache()
@@ -874,33 +963,52 @@ def run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args):
 
 # ---------------------------------------------------------------- reference arm
 def run_reference(args):
+    """The oracle as it stands, timed on the host cores on this arm's
+    workload.  Each step is one measured slice of the workload: fp64
+    attention of a seeded sample of query rows (all heads, every key) and
+    the CFG combine of the same fraction of the prediction tensors, the
+    sample sized so that the W + K steps take about --ref-budget seconds (a
+    whole oracle step, with its layout permutations, takes longer than the
+    run may: about half a minute at the FLUX-like size).  ms_per_step and
+    value are the timed steps' own wall time and work; nothing is
+    extrapolated."""
     rank, _, ws = dist_env()
     if rank != 0:
         return
     w, U = workload_config(args.workload, args.U)
-    # up to 1 s of oracle work per step, and the whole run near cpu_budget * 10
-    # s at most however many steps are asked for (each step computes at least
-    # one 256-row chunk)
-    per_step = min(1.0, max(0.1, 10 * args.cpu_budget / max(args.steps + args.warmup, 1)))
-    for _ in range(max(args.warmup, 3) if args.warmup else 0):
-        cpu_oracle_rate(w, per_step / 4, seed=1)
-    rates, secs, rows_tot, cores = [], 0.0, 0, 1
+    st = OracleStep(w, U)
+    W = max(args.warmup, 3)
+    per_step = args.ref_budget / (args.steps + W)
+    n = min(64, w.S)
+    # warm-up steps, each resizing the sample from the last one's cost
+    for i in range(W):
+        t0 = time.perf_counter()
+        st.attention(st.rows(n, 10 + i))
+        st.cfg(n / w.S)
+        dt = max(time.perf_counter() - t0, 1e-6)
+        # the cost grows faster than the row count (numpy temporaries), so
+        # the resize is damped and bounded
+        n = max(16, min(w.S, 4 * n, max(n // 4, int(n * (per_step / dt) ** 0.7))))
+    frac = n / w.S
+    times, flops = [], 0.0
     for i in range(args.steps):
-        r, s, rows, cores = cpu_oracle_rate(w, per_step, seed=100 + i)
-        rates.append(r)
-        secs += s
-        rows_tot += rows
-    value = statistics.mean(rates)
-    ms = 4.0 * w.B * w.H * w.S * w.S * w.D / (value * 1e12) * 1e3
-    sample = (f"each step: fp64 numpy oracle attention of ~{rows_tot // max(args.steps, 1)} random "
-              f"query rows x {w.H} heads x B={w.B} against all {w.S} keys, about {per_step:.1f} s")
+        rows = st.rows(n, 100 + i)
+        t0 = time.perf_counter()
+        flops += st.attention(rows)
+        st.cfg(frac)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = flops / total / 1e12
+    ms = total / max(args.steps, 1) * 1e3
+    cores = blas_threads()
+    sample = (f"each step: fp64 oracle attention of {n} seeded query rows ({100 * frac:.1f} % of {w.S}) x {w.H} "
+              f"heads x B={w.B} against all {w.S} keys, and the oracle CFG combine of the same fraction of "
+              f"[2,{','.join(map(str, w.cfg_shape[1:]))}]; value = the timed steps' attention flops / their wall time")
     res = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
-           "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 3),
+           "steps": args.steps, "warmup": W, "ms_per_step": round(ms, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "impl": "reference",
-           "config": {"workload": f"{w.name}-like: B={w.B} S={w.S} H={w.H} D={w.D}, Ulysses U={U}, "
-                                  f"ring R={w.R}", "B": w.B, "S": w.S, "H": w.H, "D": w.D,
-                      "U": U, "R": w.R},
+           "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V, N(0,1) CFG branches)", "impl": "reference",
+           "config": bench_config(w, U),
            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -916,10 +1024,17 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="flux1024")
     ap.add_argument("--U", type=int, default=None)
-    ap.add_argument("--cpu-budget", type=float, default=12.0, dest="cpu_budget")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, dest="cpu_budget",
+                    help="seconds of oracle work for the cpu_baseline (a whole step when it fits)")
+    ap.add_argument("--ref-budget", type=float, default=120.0, dest="ref_budget",
+                    help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the Wan-size merge/CFG timings")
     ap.add_argument("--sweep", action="store_true", help="one line per workload instead of the bench line")
+    ap.add_argument("--exchange", choices=("direct", "a2a"), default="direct",
+                    help="layout steps in one pass (direct) or as pack / exchange / unpack (a2a)")
+    ap.add_argument("--min-timed-s", type=float, default=0.5, dest="min_timed_s",
+                    help="repeat the K-step block until the timed region lasts this long")
     args = ap.parse_args(argv)
     if args.sweep:
         run_sweep(args)

@@ -11,6 +11,9 @@
  *                                            the same for paired text/image
  *                                            streams (joint sequence)
  *   dit_ulysses_unpack_rope                  receive preparation with RoPE
+ *   dit_ulysses_seq_to_head / dit_ulysses_head_to_seq
+ *                                            pack, exchange and unpack in one
+ *                                            pass (ranks sharing one memory)
  *   dit_sp_signal / dit_a2a_sim_checked      the exchange with arrival counters
  *                                            and a bounded wait
  *   dit_attn_partial                         attention of query blocks against
@@ -131,6 +134,9 @@ typedef struct {
     int flags;                        /* DIT_LAYOUT_* */
     int head_len[DIT_MAX_U];          /* head slots of Ulysses rank v */
     int head_off[DIT_MAX_U];          /* first head slot of Ulysses rank v */
+    int ring_real[DIT_MAX_R];         /* rows of ring block r that are real
+                                         (< S): its attention query and key
+                                         counts */
 } dit_sp_layout;
 
 /*
@@ -266,7 +272,14 @@ DIT_API dit_status dit_a2a_sim(const dit_sp_layout* L, dit_a2a_dir dir, int npla
  *   *d_status = DIT_ERR_TIMEOUT (the library's word if d_status is NULL) and
  *   the rest of the exchange is abandoned: runs whose senders timed out are
  *   not written, and the receive buffer must be treated as invalid.  The
- *   kernel always returns; the device stays usable.
+ *   kernel always returns; the device stays usable.  The status word must
+ *   not hold DIT_ERR_TIMEOUT when the call starts: the kernel reads it to
+ *   abandon the exchange at once, so a stale value from an earlier call makes
+ *   every wait give up immediately (clear it, e.g. dit_device_status with
+ *   reset = 1 for the library's word).  The signalling side publishes with
+ *   a release (a fence before the counter store) and the waiting side
+ *   fences after observing the counter, so a sender that is not stream
+ *   ordered with the exchange is read in full.
  */
 DIT_API dit_status dit_sp_signal(const dit_sp_layout* L, unsigned* d_arrival, const unsigned char* rank_mask,
                                  unsigned epoch, void* stream);
@@ -323,7 +336,8 @@ DIT_API dit_status dit_ulysses_unpack_joint(const dit_sp_layout* L, const void* 
  *                     caller-owned (the model's angles: the pages give none).
  *   rope_planes       bit mask over the nplanes planes (0x3 = Q and K);
  *                     0 gives dit_ulysses_unpack exactly.
- * Padded heads stay zero.  d_range_flag as for dit_ulysses_unpack (a 16-bit
+ * Padded heads are not rotated and stay +0.  d_range_flag as for
+ * dit_ulysses_unpack (a 16-bit
  * destination value that becomes infinite sets it).  On a 16- or 32-bit wire
  * the rotation needs D <= 384 (else DIT_ERR_UNSUPPORTED); the e4m3 wire takes
  * its own D set.
@@ -332,6 +346,50 @@ DIT_API dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplanes, 
                                            dit_dtype wire_dt, void* const* dst, const dit_dtype* dst_dt,
                                            const float* cos_tab, const float* sin_tab, unsigned rope_planes,
                                            int* d_range_flag, void* stream);
+
+/*
+ * One-pass permutation (edge-dit.cpp "Parallel execution": packed QKV send
+ * path, receive preparation and head-to-sequence path; SGLang Diffusion
+ * "Parallelism Overview", The Ulysses transport).  When every virtual rank
+ * lives in one memory, rank v's receive block from u is rank u's send block
+ * to v, so the exchange may alias the two (recv[v][u] == send[u][v]) and
+ * pack, exchange and unpack compose into one pass that reads each element
+ * once and writes it once, with no send or receive buffer.  The results are
+ * bit-identical to the three calls with the wire in the source type.
+ *
+ * Sequence-side tensors come in one piece or as a pair split at row
+ * `split` (the paired text/image streams of a double-stream block): rows
+ * t < split in src[p] ([B][split][H][D]) and rows t >= split in src2[p]
+ * ([B][S - split][H][D]) at row t - split.  split = 0 (or S): src[p] holds
+ * all S rows ([B][S][H][D]) and src2 is not read (may be NULL).
+ *
+ * dit_ulysses_seq_to_head: head-layout planes dst[p] ([R][B][S_cap][Hp][D],
+ *   dst_dt[p]) from the sequence-layout planes: row i of ring block r, batch
+ *   b = sequence row ring_off[r] + i, its H heads converted src_dt ->
+ *   dst_dt[p] (one rounding) and Hp - H zero heads; sequence-padding rows
+ *   are zero; rows past ring_len[r] are not touched.  Planes with bit p of
+ *   rope_planes set are rotated as by dit_ulysses_unpack_rope (cos_tab,
+ *   sin_tab float32 [S][D/2], 16-byte aligned; NULL when rope_planes = 0).
+ *   d_range_flag as for dit_ulysses_unpack.  Equal to dit_ulysses_pack (or
+ *   _pack_joint) + dit_a2a_sim + dit_ulysses_unpack (or _unpack_rope) with
+ *   wire_dt = src_dt.
+ * dit_ulysses_head_to_seq: the sequence-layout output (dst / dst2 split as
+ *   above, [B][S][H][D] in dst_dt) from a head-layout tensor src (src_dt):
+ *   row t < S = the first H heads of head-layout row (r, b, t - ring_off[r]).
+ *   Equal to dit_ulysses_pack + dit_a2a_sim + dit_ulysses_unpack (or
+ *   _unpack_joint) with wire_dt = src_dt.
+ * Both: D a multiple of 8, pointers 16-byte aligned, destination types of
+ * one size per call; a layout with S = 0 moves nothing.  Source and
+ * destination must not overlap.
+ */
+DIT_API dit_status dit_ulysses_seq_to_head(const dit_sp_layout* L, int nplanes, const void* const* src,
+                                           const void* const* src2, int split, dit_dtype src_dt,
+                                           void* const* dst, const dit_dtype* dst_dt, const float* cos_tab,
+                                           const float* sin_tab, unsigned rope_planes, int* d_range_flag,
+                                           void* stream);
+
+DIT_API dit_status dit_ulysses_head_to_seq(const dit_sp_layout* L, const void* src, dit_dtype src_dt, void* dst,
+                                           void* dst2, int split, dit_dtype dst_dt, void* stream);
 
 /*
  * dit_attn_partial: for every query block r < n_q and key/value block

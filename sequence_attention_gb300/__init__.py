@@ -35,6 +35,7 @@ __all__ = [
     "dit_ulysses_unpack", "dit_attn_partial", "dit_attn_merge_lse", "dit_attention",
     "dit_cfg_combine", "dit_device_status", "library_path", "dit_sp_signal", "dit_a2a_sim_checked",
     "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint", "dit_ulysses_unpack_rope", "dit_attn_varlen",
+    "dit_ulysses_seq_to_head", "dit_ulysses_head_to_seq",
 ]
 
 lib()   # load now: fail at import time, not at first call
@@ -79,7 +80,7 @@ class Layout:
     def __getattr__(self, name):
         raw = self.__dict__["raw"]
         v = getattr(raw, name)
-        if name in ("ring_len", "ring_off"):
+        if name in ("ring_len", "ring_off", "ring_real"):
             return list(v)[: raw.R]
         if name in ("rank_len", "rank_off"):
             return list(v)[: raw.R * raw.U]
@@ -88,9 +89,9 @@ class Layout:
         return v
 
     def real_rows(self, r: int) -> int:
-        """Rows of ring block r that are not sequence padding."""
-        raw = self.raw
-        return max(0, min(raw.S - raw.ring_off[r], raw.ring_len[r]))
+        """Rows of ring block r that are not sequence padding (the layout's
+        ring_real, filled by dit_sp_layout_init)."""
+        return self.raw.ring_real[r]
 
     def head_shape(self):
         """Head-layout plane [R, B, S_cap, Hp, D]."""
@@ -202,6 +203,43 @@ def dit_ulysses_unpack_rope(L: Layout, recv: torch.Tensor, dsts: Sequence[torch.
     dts = (c_int * 3)(*[_dt(d) for d in dsts])
     check(lib().dit_ulysses_unpack_rope(byref(L.raw), len(dsts), _ptr(recv), _dt(recv), ptrs, dts, _ptr(cos),
                                         _ptr(sin), rope_planes, _ptr(range_flag), _stream(stream)))
+
+
+def dit_ulysses_seq_to_head(L: Layout, srcs: Sequence[torch.Tensor], dsts: Sequence[torch.Tensor],
+                            range_flag: Optional[torch.Tensor] = None, rope=None, rope_planes: int = 0x3,
+                            src2: Optional[Sequence[torch.Tensor]] = None, stream=None) -> None:
+    """Sequence layout -> head layout in one pass (pack, exchange and unpack
+    composed): srcs[p] [B,S,H,D] -> dsts[p] [R,B,S_cap,Hp,D].  With src2,
+    srcs[p] holds the first rows of the joint sequence ([B,split,H,D], e.g.
+    the text stream) and src2[p] the rest ([B,S-split,H,D]).  rope: optional
+    (cos, sin) float32 [S, D/2] tables; the planes in rope_planes are then
+    rotated."""
+    n = len(dsts)
+    if len(srcs) != n or (src2 is not None and len(src2) != n):
+        raise ValueError("one source (pair) per destination plane")
+    split = srcs[0].shape[1] if src2 is not None else 0
+    cos = sin = None
+    planes = 0
+    if rope is not None:
+        cos, sin = rope
+        for t in (cos, sin):
+            if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (L.raw.S, L.raw.D // 2):
+                raise ValueError("rotary tables must be contiguous float32 [S, D/2]")
+        planes = rope_planes
+    dts = (c_int * 3)(*[_dt(d) for d in dsts])
+    check(lib().dit_ulysses_seq_to_head(byref(L.raw), n, _ptrs(srcs, n), _ptrs(src2, n), split, _dt(srcs[0]),
+                                        _ptrs(dsts, n), dts, _ptr(cos), _ptr(sin), planes, _ptr(range_flag),
+                                        _stream(stream)))
+
+
+def dit_ulysses_head_to_seq(L: Layout, src: torch.Tensor, dst: torch.Tensor, dst2: Optional[torch.Tensor] = None,
+                            stream=None) -> None:
+    """Head layout [R,B,S_cap,Hp,D] -> sequence layout [B,S,H,D] in one pass.
+    With dst2, dst takes the first rows of the joint sequence ([B,split,H,D])
+    and dst2 the rest ([B,S-split,H,D])."""
+    split = dst.shape[1] if dst2 is not None else 0
+    check(lib().dit_ulysses_head_to_seq(byref(L.raw), _ptr(src), _dt(src), _ptr(dst), _ptr(dst2), split, _dt(dst),
+                                        _stream(stream)))
 
 
 def _view(t: torch.Tensor, kind: str) -> DitView:

@@ -27,7 +27,7 @@ EXPORTS = (
     "dit_sp_a2a_counts", "dit_ulysses_pack", "dit_a2a_sim", "dit_ulysses_unpack",
     "dit_attn_partial", "dit_attn_merge_lse", "dit_attention", "dit_cfg_combine",
     "dit_sp_signal", "dit_a2a_sim_checked", "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint",
-    "dit_ulysses_unpack_rope", "dit_attn_varlen",
+    "dit_ulysses_unpack_rope", "dit_attn_varlen", "dit_ulysses_seq_to_head", "dit_ulysses_head_to_seq",
 )
 
 
@@ -41,6 +41,7 @@ class DitSpLayout(Structure):
         ("flags", c_int),
         ("head_len", c_int * DIT_MAX_U),
         ("head_off", c_int * DIT_MAX_U),
+        ("ring_real", c_int * DIT_MAX_R),
     ]
 
 
@@ -105,6 +106,13 @@ def lib() -> ctypes.CDLL:
     L.dit_ulysses_unpack_rope.restype = c_int
     L.dit_ulysses_unpack_rope.argtypes = [POINTER(DitSpLayout), c_int, c_void_p, c_int, POINTER(c_void_p),
                                           POINTER(c_int), c_void_p, c_void_p, c_uint, c_void_p, c_void_p]
+    L.dit_ulysses_seq_to_head.restype = c_int
+    L.dit_ulysses_seq_to_head.argtypes = [POINTER(DitSpLayout), c_int, POINTER(c_void_p), POINTER(c_void_p), c_int,
+                                          c_int, POINTER(c_void_p), POINTER(c_int), c_void_p, c_void_p, c_uint,
+                                          c_void_p, c_void_p]
+    L.dit_ulysses_head_to_seq.restype = c_int
+    L.dit_ulysses_head_to_seq.argtypes = [POINTER(DitSpLayout), c_void_p, c_int, c_void_p, c_void_p, c_int, c_int,
+                                          c_void_p]
     L.dit_attn_partial.restype = c_int
     L.dit_attn_partial.argtypes = [c_int, c_int, c_int, c_float, c_int, POINTER(c_int), c_int,
                                    POINTER(c_int), DitView, c_int, DitView, DitView, c_int, DitView,

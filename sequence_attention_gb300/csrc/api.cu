@@ -154,6 +154,10 @@ extern "C" dit_status dit_sp_layout_init_ex(int B, int S, int H, int D, int U, i
         split(out->ring_len[r], U, out->rank_len + r * U, out->rank_off + r * U, out->ring_off[r]);
     }
     out->S_cap = cap;
+    for (int r = 0; r < R; ++r) {
+        const int real = S - out->ring_off[r];
+        out->ring_real[r] = real < 0 ? 0 : (real > out->ring_len[r] ? out->ring_len[r] : real);
+    }
     return DIT_OK;
 }
 

@@ -88,11 +88,11 @@ __global__ void cfg_scalar_kernel(const char* __restrict__ pred, dit_dtype in_dt
 }
 
 // ---------------------------------------------------------------------------
-// Merge: one thread per 8 consecutive d of one (r, b, i, h) row, no
-// grid-stride loop.  Grid y is (r, b); x covers rows * heads * D/8 of the
+// Merge arguments: grid y is (r, b); x covers rows * heads * D/8 chunks of the
 // longest block.
 struct MergeArgs {
     int B, H, D, n_parts;
+    int n_q_b;                  // n_q * B (grid y)
     int q_len[DIT_MAX_R];
     dit_view parts;
     dit_dtype parts_dt;
@@ -102,141 +102,117 @@ struct MergeArgs {
     dit_lse_view lse_out;
 };
 
-__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ MergeArgs a) {
+// Merge, chunk-per-thread form: thread t of block (x, r*B + b) takes the
+// 8-element chunk c of unit u = (row i, head h), and SLOTS such chunks
+// spaced one block apart.  Every load of a thread -- the NP log-sum-exp
+// values and the NP partial chunks of each of its slots -- is issued before
+// any arithmetic, so one memory round trip covers all of them (the lanes of
+// one unit read the same log-sum-exp words, served by one transaction).
+// Each thread then forms the unit's weights itself: a few exponentials per
+// 8 outputs, far below what the bandwidth leaves free.  SLOTS * NP is about
+// four, so a thread keeps 64 (16-bit parts) or 128 bytes of partials in
+// flight.  Units run h-fastest within a row and chunks c-fastest within a
+// head, so the block's loads and stores cover whole contiguous rows.
+template <int NP, int SLOTS, int PB>
+__global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant__ MergeArgs a) {
     const int r = blockIdx.y / a.B, b = blockIdx.y % a.B;
     const int chunks = a.D >> 3;
     const long long per_row = (long long)a.H * chunks;
     const long long total = (long long)a.q_len[r] * per_row;
-    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    pdl_wait();
-    if (t < total) {
-        const int i = (int)(t / per_row);
-        const int rem = (int)(t - (long long)i * per_row);
-        const int h = rem / chunks, c = rem - h * chunks;
-        const float* lp = a.lse_parts.ptr + r * a.lse_parts.stride_q + b * a.lse_parts.stride_b +
-                          h * a.lse_parts.stride_h + i;
-        float lj[DIT_MAX_R];
-        float M = -INFINITY;
-        for (int j = 0; j < a.n_parts; ++j) {
-            lj[j] = lp[j * a.lse_parts.stride_kv];
-            M = fmaxf(M, lj[j]);
+    const long long t0 = (long long)blockIdx.x * blockDim.x * SLOTS + threadIdx.x;
+    const char* pp = static_cast<const char*>(a.parts.ptr);
+    const dit_dtype pdt = a.parts_dt;
+    long long base[SLOTS];
+    int lrow[SLOTS];           // row i of the slot's unit (-1: no chunk)
+    int lh[SLOTS], lc[SLOTS];
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) {
+        const long long t = t0 + (long long)k * blockDim.x;
+        lrow[k] = -1;
+        if (t < total) {
+            const int i = (int)(t / per_row);
+            const int rem = (int)(t - (long long)i * per_row);
+            const int h = rem / chunks;
+            lrow[k] = i;
+            lh[k] = h;
+            lc[k] = rem - h * chunks;
+            base[k] = r * a.parts.stride_q + b * a.parts.stride_b + (long long)i * a.parts.stride_s +
+                      h * a.parts.stride_h + lc[k] * 8;
         }
+    }
+    pdl_wait();
+    float lj[SLOTS][NP];
+    uint4 raw[SLOTS][NP][PB / 2];
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) {
+        if (lrow[k] < 0) continue;
+        const float* lp = a.lse_parts.ptr + r * a.lse_parts.stride_q + b * a.lse_parts.stride_b +
+                          lh[k] * a.lse_parts.stride_h + lrow[k];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) lj[k][j] = lp[j * a.lse_parts.stride_kv];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const uint4* q = reinterpret_cast<const uint4*>(pp + (base[k] + j * a.parts.stride_kv) * PB);
+#pragma unroll
+            for (int h = 0; h < PB / 2; ++h) raw[k][j][h] = q[h];
+        }
+    }
+    char* op = static_cast<char*>(a.out.ptr);
+    const int ob = dtype_bytes(a.out_dt);
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) {
+        if (lrow[k] < 0) continue;
+        float M = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) M = fmaxf(M, lj[k][j]);
         Vec8 acc;
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc.f[e] = 0.f;
         float lse = -INFINITY;
         if (M != -INFINITY) {
-            float s = 0.f;
-            for (int j = 0; j < a.n_parts; ++j) s += expf(lj[j] - M);
-            lse = M + logf(s);
-            const long long base = r * a.parts.stride_q + b * a.parts.stride_b + i * a.parts.stride_s +
-                                   h * a.parts.stride_h + c * 8;
-            const char* pp = static_cast<const char*>(a.parts.ptr);
-            const int eb = dtype_bytes(a.parts_dt);
-            for (int j = 0; j < a.n_parts; ++j) {
-                const float w = expf(lj[j] - lse);
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < NP; ++j) sum += expf(lj[k][j] - M);
+            lse = M + logf(sum);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const float w = expf(lj[k][j] - lse);
                 Vec8 o;
-                load8(pp + (base + j * a.parts.stride_kv) * eb, a.parts_dt, o);
+                load8(&raw[k][j][0], pdt, o);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc.f[e] = fmaf(w, o.f[e], acc.f[e]);
             }
         }
-        const long long ob = r * a.out.stride_q + b * a.out.stride_b + i * a.out.stride_s +
-                             h * a.out.stride_h + c * 8;
-        store8(static_cast<char*>(a.out.ptr) + ob * dtype_bytes(a.out_dt), a.out_dt, acc);
-        if (a.lse_out.ptr && c == 0)
-            a.lse_out.ptr[r * a.lse_out.stride_q + b * a.lse_out.stride_b + h * a.lse_out.stride_h + i] = lse;
+        const long long off = r * a.out.stride_q + b * a.out.stride_b + (long long)lrow[k] * a.out.stride_s +
+                              lh[k] * a.out.stride_h + lc[k] * 8;
+        store8(op + off * ob, a.out_dt, acc);
+        if (a.lse_out.ptr && lc[k] == 0)
+            a.lse_out.ptr[r * a.lse_out.stride_q + b * a.lse_out.stride_b + lh[k] * a.lse_out.stride_h + lrow[k]] =
+                lse;
     }
     pdl_trigger();
 }
 
-// Merge, unit-per-lane form: a "unit" is one (row i, head h) of block (r, b).
-// Lane L of a warp computes the log-sum-exp and the NP weights of unit L of
-// the warp's 32 (one set of exponentials per unit, not per output), then the
-// warp streams the units' D outputs, CPU = D/8 lanes per unit, taking each
-// unit's weights from its lane by shuffle.  The partial loads of a step are
-// issued before any arithmetic on them.  Units run i-fastest within a head,
-// so the lanes' LSE loads are contiguous.
-template <int NP>
-__global__ void __launch_bounds__(256) merge_units_kernel(const __grid_constant__ MergeArgs a, int cpu_log2) {
-    const int r = blockIdx.y / a.B, b = blockIdx.y % a.B;
-    const int ql = a.q_len[r];
-    const int units = ql * a.H;               // fits in 32 bits (checked on the host)
-    const int lane = threadIdx.x & 31;
-    const int u0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
-    pdl_wait();
-    if (u0 >= units) {
-        pdl_trigger();
-        return;
-    }
-    // this lane's unit: weights and log-sum-exp
-    float w[NP];
-    float lse = -INFINITY;
-    {
-        const int u = u0 + lane;
-        float lj[NP];
-        float M = -INFINITY;
-        if (u < units) {
-            const int h = u / ql, i = u - h * ql;
-            const float* lp = a.lse_parts.ptr + r * a.lse_parts.stride_q + b * a.lse_parts.stride_b +
-                              h * a.lse_parts.stride_h + i;
-#pragma unroll
-            for (int j = 0; j < NP; ++j) lj[j] = lp[j * a.lse_parts.stride_kv];
-#pragma unroll
-            for (int j = 0; j < NP; ++j) M = fmaxf(M, lj[j]);
-        }
-        if (M != -INFINITY) {
-            float sum = 0.f;
-#pragma unroll
-            for (int j = 0; j < NP; ++j) sum += expf(lj[j] - M);
-            lse = M + logf(sum);
-#pragma unroll
-            for (int j = 0; j < NP; ++j) w[j] = expf(lj[j] - lse);
-        } else {
-#pragma unroll
-            for (int j = 0; j < NP; ++j) w[j] = 0.f;
-        }
-        if (u < units && a.lse_out.ptr) {
-            const int h = u / ql, i = u - h * ql;
-            a.lse_out.ptr[r * a.lse_out.stride_q + b * a.lse_out.stride_b + h * a.lse_out.stride_h + i] = lse;
-        }
-    }
-    const int cpu = 1 << cpu_log2;            // lanes per unit (D / 8)
-    const int upi = 32 >> cpu_log2;           // units per step
-    const int c = lane & (cpu - 1);
-    const int eb = dtype_bytes(a.parts_dt), ob = dtype_bytes(a.out_dt);
-    const char* pp = static_cast<const char*>(a.parts.ptr);
-    char* op = static_cast<char*>(a.out.ptr);
-    for (int k0 = 0; k0 < 32; k0 += upi) {
-        const int k = k0 + (lane >> cpu_log2);  // unit of this lane in this step
-        const int u = u0 + k;
-        float wk[NP];
-#pragma unroll
-        for (int j = 0; j < NP; ++j) wk[j] = __shfl_sync(0xffffffffu, w[j], k);
-        if (u >= units) continue;
-        const int h = u / ql, i = u - h * ql;
-        const long long base = r * a.parts.stride_q + b * a.parts.stride_b + (long long)i * a.parts.stride_s +
-                               h * a.parts.stride_h + c * 8;
-        Vec8 o[NP];
-#pragma unroll
-        for (int j = 0; j < NP; ++j) load8(pp + (base + j * a.parts.stride_kv) * eb, a.parts_dt, o[j]);
-        Vec8 acc;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc.f[e] = 0.f;
-#pragma unroll
-        for (int j = 0; j < NP; ++j)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc.f[e] = fmaf(wk[j], o[j].f[e], acc.f[e]);
-        const long long ob_off = r * a.out.stride_q + b * a.out.stride_b + (long long)i * a.out.stride_s +
-                                 h * a.out.stride_h + c * 8;
-        store8(op + ob_off * ob, a.out_dt, acc);
-    }
-    pdl_trigger();
+template <int NP, int PB>
+cudaError_t launch_merge_chunks(const MergeArgs& a, long long work, cudaStream_t st) {
+    constexpr int SLOTS = NP >= 4 ? 1 : 4 / NP;
+    const long long per_block = 256LL * SLOTS;
+    const dim3 grid((unsigned)((work + per_block - 1) / per_block), (unsigned)a.n_q_b);
+    return launch_pdl(merge_chunks_kernel<NP, SLOTS, PB>, grid, dim3(256), 0, st, a);
 }
 
-template <int NP>
-cudaError_t launch_merge_units(const MergeArgs& a, dim3 grid, int cpu_log2, cudaStream_t st) {
-    return launch_pdl(merge_units_kernel<NP>, grid, dim3(256), 0, st, a, cpu_log2);
+template <int PB>
+cudaError_t launch_merge(const MergeArgs& a, long long work, cudaStream_t st) {
+    switch (a.n_parts) {
+        case 1: return launch_merge_chunks<1, PB>(a, work, st);
+        case 2: return launch_merge_chunks<2, PB>(a, work, st);
+        case 3: return launch_merge_chunks<3, PB>(a, work, st);
+        case 4: return launch_merge_chunks<4, PB>(a, work, st);
+        case 5: return launch_merge_chunks<5, PB>(a, work, st);
+        case 6: return launch_merge_chunks<6, PB>(a, work, st);
+        case 7: return launch_merge_chunks<7, PB>(a, work, st);
+        default: return launch_merge_chunks<8, PB>(a, work, st);
+    }
 }
 
 }  // namespace
@@ -319,33 +295,12 @@ extern "C" dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int
         return fail(DIT_ERR_INVALID_ARG, "%s: NULL or misaligned pointer", who);
     a.parts = parts; a.parts_dt = parts_dt; a.lse_parts = lse_parts;
     a.out = out; a.out_dt = out_dt; a.lse_out = lse_out;
-    if ((unsigned)(n_q * B) > 65535u) return fail(DIT_ERR_UNSUPPORTED, "%s: n_q * B too large", who);
-    cudaError_t e;
-    const int chunks = D / 8;
-    const bool pow2 = chunks <= 32 && (chunks & (chunks - 1)) == 0;
-    if (pow2 && (long long)maxq * H < (1LL << 31)) {
-        // unit-per-lane form: 256 units (rows x heads) per block of 8 warps
-        int lg = 0;
-        while ((1 << lg) < chunks) ++lg;
-        const long long units = (long long)maxq * H;
-        dim3 grid((unsigned)((units + 255) / 256), (unsigned)(n_q * B));
-        const cudaStream_t st = (cudaStream_t)stream;
-        switch (n_parts) {
-            case 1: e = launch_merge_units<1>(a, grid, lg, st); break;
-            case 2: e = launch_merge_units<2>(a, grid, lg, st); break;
-            case 3: e = launch_merge_units<3>(a, grid, lg, st); break;
-            case 4: e = launch_merge_units<4>(a, grid, lg, st); break;
-            case 5: e = launch_merge_units<5>(a, grid, lg, st); break;
-            case 6: e = launch_merge_units<6>(a, grid, lg, st); break;
-            case 7: e = launch_merge_units<7>(a, grid, lg, st); break;
-            default: e = launch_merge_units<8>(a, grid, lg, st); break;
-        }
-    } else {
-        const long long work = (long long)maxq * H * (D / 8);
-        const long long bx = (work + 255) / 256;     // one thread per 8 outputs
-        dim3 grid((unsigned)bx, (unsigned)(n_q * B));
-        e = launch_pdl(merge_kernel, grid, dim3(256), 0, (cudaStream_t)stream, a);
-    }
+    if ((long long)n_q * B > 65535) return fail(DIT_ERR_UNSUPPORTED, "%s: n_q * B too large", who);
+    a.n_q_b = n_q * B;
+    const long long work = (long long)maxq * H * (D / 8);      // chunks of the longest block
+    if (work / 256 >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 2^39 chunks per block", who);
+    const cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e = parts_dt == DIT_F32 ? launch_merge<4>(a, work, st) : launch_merge<2>(a, work, st);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     return check_launch(who);
 }

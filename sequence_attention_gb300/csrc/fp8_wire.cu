@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 3) fp8_unpack_kernel(const __grid_co
             char* dst = io.dst + ((long long)h * D + c * EPL) * dtype_bytes(t);
             const float* cs = nullptr;
             const float* sn = nullptr;
-            if (ROPE && io.rope_pos >= 0) {
+            if (ROPE && io.rope_pos >= 0 && h < io.nreal) {     // padded heads stay +0
                 cs = A.rope_cos + (long long)io.rope_pos * (D >> 1) + c * (EPL / 2);
                 sn = A.rope_sin + (long long)io.rope_pos * (D >> 1) + c * (EPL / 2);
             }

@@ -29,6 +29,7 @@
 //    cos[t][i], sin[t][i]:  (x0, x1) -> (x0 c - x1 s, x0 s + x1 c), in fp32.
 #include <string.h>
 
+#include "convert.cuh"
 #include "sp_index.cuh"
 
 namespace ditsp {
@@ -79,10 +80,6 @@ __global__ void signal_kernel(unsigned* arrival, int nranks, unsigned long long 
     pdl_trigger();
 }
 
-__device__ __forceinline__ bool narrowing(dit_dtype s, dit_dtype d) {
-    return (s == DIT_F32 && d != DIT_F32) || (s == DIT_BF16 && d == DIT_F16);
-}
-
 // Where one run comes from and goes to (chunk = 8 elements).
 struct RunIO {
     const char* src;
@@ -92,6 +89,7 @@ struct RunIO {
     int sdt, ddt;     // dit_dtype of source and destination
     int sender;       // virtual rank that sent this run (exchange kernels)
     int rope_pos;     // joint-sequence position whose angles rotate the run; -1: none
+    int rot_lim;      // chunks of the run that are rotated (real heads; padded heads stay +0)
 };
 
 template <int MODE>
@@ -114,6 +112,7 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
     RunIO io;
     io.src_lim = io.dst_lim = full;
     io.rope_pos = -1;
+    io.rot_lim = real;
     long long so = 0, doff = 0;
     dit_dtype sdt, ddt;
     bool second = false;
@@ -157,70 +156,12 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
     return io;
 }
 
-// Convert 8 elements held in registers (SB bytes each) to the destination
-// encoding (DB bytes each); narrowing rounds to nearest even.  With `check`,
-// a finite value that becomes infinite sets `overflow`.
-template <int SB, int DB>
-__device__ __forceinline__ void convert8(const uint4 (&in)[SB / 2], dit_dtype sdt, dit_dtype ddt, bool check,
-                                         uint4 (&out)[DB / 2], bool& overflow) {
-    if (sdt == ddt) {
-#pragma unroll
-        for (int h = 0; h < DB / 2; ++h) out[h] = in[h < SB / 2 ? h : 0];
-        return;
-    }
-    Vec8 v;
-    load8(&in[0], sdt, v);
-    if constexpr (DB == 4) {
-        out[0] = make_uint4(__float_as_uint(v.f[0]), __float_as_uint(v.f[1]), __float_as_uint(v.f[2]),
-                            __float_as_uint(v.f[3]));
-        out[1] = make_uint4(__float_as_uint(v.f[4]), __float_as_uint(v.f[5]), __float_as_uint(v.f[6]),
-                            __float_as_uint(v.f[7]));
-    } else {
-        out[0] = make_uint4(pack2(v.f[0], v.f[1], ddt), pack2(v.f[2], v.f[3], ddt),
-                            pack2(v.f[4], v.f[5], ddt), pack2(v.f[6], v.f[7], ddt));
-        if (check) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) overflow |= overflows16(v.f[e], ddt);
-        }
-    }
-}
-
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// Rotate the four interleaved pairs held in 8 elements by the angles with
-// cosines c and sines s, in fp32, then convert to the destination type.
-template <int SB, int DB>
-__device__ __forceinline__ void rope8(const uint4 (&in)[SB / 2], dit_dtype sdt, dit_dtype ddt, float4 c, float4 s,
-                                      bool check, uint4 (&out)[DB / 2], bool& overflow) {
-    Vec8 v;
-    load8(&in[0], sdt, v);
-    const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {s.x, s.y, s.z, s.w};
-    Vec8 y;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float x0 = v.f[2 * k], x1 = v.f[2 * k + 1];
-        y.f[2 * k] = fmaf(x0, cc[k], -(x1 * ss[k]));
-        y.f[2 * k + 1] = fmaf(x0, ss[k], x1 * cc[k]);
-    }
-    if constexpr (DB == 4) {
-        out[0] = make_uint4(__float_as_uint(y.f[0]), __float_as_uint(y.f[1]), __float_as_uint(y.f[2]),
-                            __float_as_uint(y.f[3]));
-        out[1] = make_uint4(__float_as_uint(y.f[4]), __float_as_uint(y.f[5]), __float_as_uint(y.f[6]),
-                            __float_as_uint(y.f[7]));
-    } else {
-        out[0] = make_uint4(pack2(y.f[0], y.f[1], ddt), pack2(y.f[2], y.f[3], ddt),
-                            pack2(y.f[4], y.f[5], ddt), pack2(y.f[6], y.f[7], ddt));
-        if (check) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) overflow |= overflows16(y.f[e], ddt);
-        }
-    }
-}
 
 constexpr int kThreads = 256;
 // the rotary path stages 64 runs x 2 x D/2 floats in shared memory (96 KB
@@ -270,6 +211,9 @@ __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __gri
             }
         }
         if (!arrived) io.src_lim = io.dst_lim = 0;
+        // the counter was read relaxed: order this thread's observation of
+        // the sender's release before the block's loads of the send buffer
+        else __threadfence();
     }
     __syncthreads();
     const int dch = A.L.D >> 3;          // chunks per head = float4s per table row
@@ -343,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __gri
                 if (ci < io.dst_lim) {
                     const dit_dtype sdt = (dit_dtype)io.sdt, ddt = (dit_dtype)io.ddt;
                     uint4 o[DB / 2];
-                    if (ROPE && io.rope_pos >= 0) {
+                    if (ROPE && io.rope_pos >= 0 && ci < io.rot_lim) {
                         const int sl = slot[ROPE ? g0 + gi : 0], cc = ci % dch;
                         rope8<SB, DB>(raw[t], sdt, ddt, rope_sm[(2 * sl) * dch + cc],
                                       rope_sm[(2 * sl + 1) * dch + cc], want_check && ddt != DIT_F32, o,
@@ -464,7 +408,8 @@ dit_status check_layout(const dit_sp_layout* L, const char* who) {
     for (int v = 0; ok && v < L->U; ++v)
         ok = ref.head_len[v] == L->head_len[v] && ref.head_off[v] == L->head_off[v];
     for (int r = 0; ok && r < L->R; ++r)
-        ok = ref.ring_len[r] == L->ring_len[r] && ref.ring_off[r] == L->ring_off[r];
+        ok = ref.ring_len[r] == L->ring_len[r] && ref.ring_off[r] == L->ring_off[r] &&
+             ref.ring_real[r] == L->ring_real[r];
     for (int i = 0; ok && i < L->R * L->U; ++i)
         ok = ref.rank_len[i] == L->rank_len[i] && ref.rank_off[i] == L->rank_off[i];
     if (!ok) return fail(DIT_ERR_INVALID_ARG, "%s: layout tables are inconsistent", who);

@@ -6,19 +6,24 @@ Parallelism", USP: Ulysses all-to-all, then ring attention on the
 redistributed data, then the inverse all-to-all; SGLang Diffusion
 "Parallelism Overview", What happens to the shapes):
 
-  dit_ulysses_pack(S2H)   seq-sharded Q,K,V -> peer-major send buffer
-  dit_a2a_sim(S2H)        send -> receive buffers (the all-to-all)
-  dit_ulysses_unpack(S2H) receive -> head layout [R,B,S_cap,Hp,D] (V as f16)
+  layout in    seq-sharded Q,K,V -> head layout [R,B,S_cap,Hp,D] (V as f16)
   dit_attn_partial        every (ring block r, ring block j) partial, one launch
   dit_attn_merge_lse      R partials -> exact output (skipped when R = 1)
-  dit_ulysses_pack(H2S), dit_a2a_sim(H2S), dit_ulysses_unpack(H2S)
-                          head layout -> seq-sharded output [B,S,H,D]
+  layout out   head layout -> seq-sharded output [B,S,H,D]
 
-With rotary tables, the seq-to-head unpack is the receive preparation that
-rotates Q and K as it writes them (dit_ulysses_unpack_rope); run_joint()
-takes the paired text and image streams of a double-stream block and
-returns the output in the same two streams (dit_ulysses_pack_joint,
-dit_ulysses_unpack_joint), so the joint sequence is never concatenated.
+The layout steps run one of two ways (``exchange``):
+  "direct"  dit_ulysses_seq_to_head / dit_ulysses_head_to_seq: on one memory
+            the exchange aliases receive and send blocks, so pack, exchange
+            and unpack are one pass (each element read and written once);
+  "a2a"     dit_ulysses_pack -> dit_a2a_sim -> dit_ulysses_unpack, the three
+            calls a multi-GPU build keeps (the exchange becomes an alltoallv
+            with the counts of dit_sp_a2a_counts); the e4m3 wire needs it.
+Both give the same bits.
+
+With rotary tables, the seq-to-head step is the receive preparation that
+rotates Q and K as it writes them; run_joint() takes the paired text and
+image streams of a double-stream block and returns the output in the same
+two streams, so the joint sequence is never concatenated.
 
 All buffers are allocated once, when the plan is built; run() allocates
 nothing and only enqueues kernels on the current (or given) stream.
@@ -30,9 +35,10 @@ from typing import Optional, Sequence, Tuple
 
 import torch
 
-from . import (DIT_HEAD_TO_SEQ, DIT_SEQ_TO_HEAD, dit_a2a_sim, dit_attn_merge_lse, dit_attn_partial,
-               dit_sp_layout_init, dit_ulysses_pack, dit_ulysses_pack_joint, dit_ulysses_unpack,
-               dit_ulysses_unpack_joint, dit_ulysses_unpack_rope)
+from . import (DIT_HEAD_TO_SEQ, DIT_SEQ_TO_HEAD, DitError, dit_a2a_sim, dit_attn_merge_lse, dit_attn_partial,
+               dit_sp_layout_init, dit_ulysses_head_to_seq, dit_ulysses_pack, dit_ulysses_pack_joint,
+               dit_ulysses_seq_to_head, dit_ulysses_unpack, dit_ulysses_unpack_joint, dit_ulysses_unpack_rope)
+from ._lib import DIT_ERR_RANGE, DIT_ERR_TIMEOUT
 
 
 class UspPlan:
@@ -44,7 +50,7 @@ class UspPlan:
                  rope: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
                  fp8_qv: bool = False, fp8_o: bool = False,
                  pad_heads: bool = True, pad_lcm64: bool = False,
-                 parts_dtype: Optional[torch.dtype] = None):
+                 parts_dtype: Optional[torch.dtype] = None, exchange: Optional[str] = None):
         """rope: optional (cos, sin) float32 [S, D/2] device tables of the
         joint sequence; Q and K are then rotated by the receive preparation.
         fp8_qv / fp8_o: Q and V (one exchange) / the output cross the
@@ -57,7 +63,14 @@ class UspPlan:
         combination of V rows, so it stays within V's range, and f16 keeps
         11 significant bits against the output's 8 (bf16), at half the
         bytes of f32 for the attention's stores and the merge's loads.
-        Otherwise f32."""
+        Otherwise f32.
+        exchange: "direct" (one pass per layout step) or "a2a" (pack,
+        exchange, unpack); default "direct", or "a2a" with an e4m3 wire.
+        v_dtype: by default f16 for bf16 inputs (P V runs with P in V's type,
+        and f16 keeps P to 11 significant bits).  f16 holds |v| < 65520: a
+        larger V value becomes infinite and makes the output inf/NaN.  The
+        layout step then sets the plan's range flag; check() reports it.  Pass
+        v_dtype=torch.bfloat16 for inputs that may exceed that range."""
         self.L = dit_sp_layout_init(B, S, H, D, U, R, pad_heads, pad_lcm64)
         self.B, self.S, self.H, self.D, self.U, self.R = B, S, H, D, U, R
         self.in_dtype = in_dtype
@@ -73,13 +86,25 @@ class UspPlan:
         hs = L.head_shape()
         dev = torch.device(device)
         self.fp8_qv, self.fp8_o = fp8_qv, fp8_o
-        if fp8_qv:
+        if exchange is None:
+            exchange = "a2a" if (fp8_qv or fp8_o) else "direct"
+        if exchange not in ("direct", "a2a"):
+            raise ValueError(f"exchange must be 'direct' or 'a2a', got {exchange!r}")
+        if exchange == "direct" and (fp8_qv or fp8_o):
+            raise ValueError("the e4m3 wire needs exchange='a2a' (the direct path has no wire)")
+        self.exchange = exchange
+        direct = exchange == "direct"
+        self.send = self.recv = self.send_qv = self.recv_qv = self.send_o = self.recv_o = None
+        if direct:
+            pass
+        elif fp8_qv:
             self.send_qv = torch.empty(L.wire_bytes_e4m3(2), dtype=torch.uint8, device=dev)
             self.recv_qv = torch.empty_like(self.send_qv)
             self.send = torch.empty(L.wire_elems(1), dtype=in_dtype, device=dev)     # K
         else:
             self.send = torch.empty(L.wire_elems(3), dtype=in_dtype, device=dev)
-        self.recv = torch.empty_like(self.send)
+        if not direct:
+            self.recv = torch.empty_like(self.send)
         self.q_h = torch.empty(hs, dtype=in_dtype, device=dev)
         self.k_h = torch.empty(hs, dtype=in_dtype, device=dev)
         self.v_h = torch.empty(hs, dtype=v_dtype, device=dev)
@@ -95,14 +120,21 @@ class UspPlan:
             self.lse_parts = torch.empty((R, R, B, L.Hp, L.S_cap), dtype=torch.float32, device=dev)
         else:
             self.parts = self.lse_parts = None
-        if fp8_o:
+        if direct:
+            pass
+        elif fp8_o:
             self.send_o = torch.empty(L.wire_bytes_e4m3(1), dtype=torch.uint8, device=dev)
         else:
             self.send_o = torch.empty(L.wire_elems(1), dtype=self.out_dtype, device=dev)
-        self.recv_o = torch.empty_like(self.send_o)
+        if not direct:
+            self.recv_o = torch.empty_like(self.send_o)
         self.rope = rope
-        self.range_flag = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # device words the kernels set and never clear: [0] the range flag of
+        # the layout step (a value that overflowed its 16-bit destination),
+        # [1] the attention's status (a bounded wait that ran out)
+        self.flags = torch.zeros(2, dtype=torch.int32, device=dev)
+        self.range_flag = self.flags[0:1]
+        self.status = self.flags[1:2]
 
     # ---- views of the real (unpadded) heads --------------------------------
     def heads(self, t: torch.Tensor) -> torch.Tensor:
@@ -111,18 +143,38 @@ class UspPlan:
     @property
     def ring_len(self):
         """Real (non-padding) rows of each ring block: the attention's
-        query and key counts."""
-        return [self.L.real_rows(r) for r in range(self.R)]
+        query and key counts (the layout's ring_real)."""
+        return self.L.ring_real
+
+    def check(self, reset: bool = True) -> None:
+        """Wait for the stream, then raise DitError if a kernel of an earlier
+        run set the range flag (a value overflowed its 16-bit destination,
+        e.g. |V| >= 65520 converted to f16) or the status word (a bounded wait
+        ran out).  The words are sticky: they keep a set value across runs
+        until this call (reset=True) clears them."""
+        torch.cuda.current_stream(self.flags.device).synchronize()
+        rng, st = (int(x) for x in self.flags.tolist())
+        if reset and (rng or st):
+            self.flags.zero_()
+        if st:
+            raise DitError(DIT_ERR_TIMEOUT if st == DIT_ERR_TIMEOUT else st,
+                           "a bounded device-side wait ran out in the attention")
+        if rng:
+            raise DitError(DIT_ERR_RANGE, "a value overflowed its 16-bit destination type "
+                                          "(f16 holds |x| < 65520; use v_dtype=torch.bfloat16)")
 
     def steps(self):
         """Names of the kernels one run() launches, in order."""
-        s = ["pack_s2h", "a2a_s2h", "unpack_s2h"]
-        if self.fp8_qv:
+        if self.exchange == "direct":
+            s = ["seq_to_head"]
+        elif self.fp8_qv:
             s = ["pack_s2h_k", "pack_s2h_qv", "a2a_s2h_k", "a2a_s2h_qv", "unpack_s2h_k", "unpack_s2h_qv"]
+        else:
+            s = ["pack_s2h", "a2a_s2h", "unpack_s2h"]
         s = s + ["attn_partial"]
         if self.R > 1:
             s.append("merge")
-        return s + ["pack_h2s", "a2a_h2s", "unpack_h2s"]
+        return s + (["head_to_seq"] if self.exchange == "direct" else ["pack_h2s", "a2a_h2s", "unpack_h2s"])
 
     def _unpack(self, recv, heads, rope_mask, stream):
         if self.rope is not None:
@@ -143,6 +195,10 @@ class UspPlan:
             self._unpack(self.recv, [self.q_h, self.k_h, self.v_h], 0b011, stream)
 
     def layout_in(self, q, k, v, stream=None):
+        if self.exchange == "direct":
+            dit_ulysses_seq_to_head(self.L, [q, k, v], [self.q_h, self.k_h, self.v_h], self.range_flag,
+                                    rope=self.rope, rope_planes=0b011, stream=stream)
+            return
         if self.fp8_qv:
             dit_ulysses_pack(self.L, DIT_SEQ_TO_HEAD, [k], self.send, stream)
             dit_ulysses_pack(self.L, DIT_SEQ_TO_HEAD, [q, v], self.send_qv, stream)
@@ -154,6 +210,12 @@ class UspPlan:
                         stream=None):
         """txt / img: (q, k, v) of the text [B,S_txt,H,D] and image
         [B,S-S_txt,H,D] streams (None for a stream without rows)."""
+        if self.exchange == "direct":
+            first, second = (txt, img) if txt is not None else (img, None)
+            dit_ulysses_seq_to_head(self.L, list(first), [self.q_h, self.k_h, self.v_h], self.range_flag,
+                                    rope=self.rope, rope_planes=0b011,
+                                    src2=None if second is None else list(second), stream=stream)
+            return
         if self.fp8_qv:
             sel = lambda t, idx: None if t is None else [t[i] for i in idx]   # noqa: E731
             dit_ulysses_pack_joint(self.L, sel(txt, [1]), sel(img, [1]), self.send, stream)
@@ -187,12 +249,19 @@ class UspPlan:
 
     def layout_out(self, out, stream=None):
         L = self.L
+        if self.exchange == "direct":
+            dit_ulysses_head_to_seq(L, self.o_h, out, stream=stream)
+            return
         dit_ulysses_pack(L, DIT_HEAD_TO_SEQ, [self.o_h], self.send_o, stream)
         dit_a2a_sim(L, DIT_HEAD_TO_SEQ, 1, self.send_o, self.recv_o, stream)
         dit_ulysses_unpack(L, DIT_HEAD_TO_SEQ, self.recv_o, [out], None, stream)
 
     def layout_out_joint(self, out_txt, out_img, stream=None):
         L = self.L
+        if self.exchange == "direct":
+            first, second = (out_txt, out_img) if out_txt is not None else (out_img, None)
+            dit_ulysses_head_to_seq(L, self.o_h, first, second, stream=stream)
+            return
         dit_ulysses_pack(L, DIT_HEAD_TO_SEQ, [self.o_h], self.send_o, stream)
         dit_a2a_sim(L, DIT_HEAD_TO_SEQ, 1, self.send_o, self.recv_o, stream)
         dit_ulysses_unpack_joint(L, self.recv_o, out_txt, out_img, stream)
@@ -220,9 +289,12 @@ class UspPlan:
         torch.cuda.current_stream(self.q_h.device).wait_stream(s)
         return g
 
-    def run(self, q, k, v, out, stream=None):
-        """q, k, v: [B, S, H, D] seq-sharded inputs; out: [B, S, H, D]."""
+    def run(self, q, k, v, out, stream=None, check: bool = False):
+        """q, k, v: [B, S, H, D] seq-sharded inputs; out: [B, S, H, D].
+        check=True waits for the step and raises as check() does."""
         self.layout_in(q, k, v, stream)
         self.attend(stream)
         self.layout_out(out, stream)
+        if check:
+            self.check()
         return out

@@ -56,6 +56,7 @@ def test_layout_init_matches_oracle(dl, dims):
     assert (L.Hp, L.Hl, L.S_cap) == (ref.Hp, ref.Hl, ref.S_cap)
     assert L.ring_len == list(ref.ring_len) and L.ring_off == list(ref.ring_off)
     assert L.rank_len == list(ref.rank_len) and L.rank_off == list(ref.rank_off)
+    assert L.ring_real == [ref.real_rows(r) for r in range(ref.R)]
 
 
 @pytest.mark.parametrize("flags", [(False, False), (True, True), (False, True)])
@@ -69,6 +70,7 @@ def test_layout_modes_match_oracle(dl, dims, flags):
     assert L.head_len == list(ref.head_len) and L.head_off == list(ref.head_off)
     assert L.ring_len == list(ref.ring_len) and L.ring_off == list(ref.ring_off)
     assert L.rank_len == list(ref.rank_len) and L.rank_off == list(ref.rank_off)
+    assert L.ring_real == [ref.real_rows(r) for r in range(ref.R)]
     for d, name in ((0, "s2h"), (1, "h2s")):
         for rank in range(min(dims[4] * dims[5], 9)):
             got = sa.dit_sp_a2a_counts(L, d, 3 if d == 0 else 1, rank)
@@ -261,6 +263,54 @@ def test_new_entry_points_validate_before_any_launch(dl):
                              dl.DitLseView(), None, None) == dl.DIT_ERR_INVALID_ARG
     assert L.dit_attn_varlen(2, 64, 0.125, 0, None, None, v, dl.DIT_BF16, v, v, dl.DIT_F16, v, dl.DIT_BF16,
                              dl.DitLseView(), None, None) == dl.DIT_OK          # nothing to do
+
+
+def test_one_pass_permutation_validates_before_any_launch(dl):
+    """dit_ulysses_seq_to_head / dit_ulysses_head_to_seq refuse bad arguments
+    on the host: no launch, no CUDA call."""
+    L = dl.lib()
+    lay = dl.DitSpLayout()
+    assert L.dit_sp_layout_init(1, 64, 4, 64, 2, 1, ctypes.byref(lay)) == 0
+    p = (ctypes.c_void_p * 3)(1 << 20, 2 << 20, 3 << 20)
+    mis = (ctypes.c_void_p * 3)((1 << 20) + 8, 2 << 20, 3 << 20)
+    dts = (ctypes.c_int * 3)(dl.DIT_BF16, dl.DIT_BF16, dl.DIT_F16)
+    bad_dts = (ctypes.c_int * 3)(dl.DIT_BF16, dl.DIT_E4M3, dl.DIT_F16)
+    tab = ctypes.c_void_p(5 << 20)
+    lp = ctypes.byref(lay)
+    E = dl.DIT_ERR_INVALID_ARG
+    s2h, h2s = L.dit_ulysses_seq_to_head, L.dit_ulysses_head_to_seq
+    assert s2h(lp, 0, p, None, 0, dl.DIT_BF16, p, dts, None, None, 0, None, None) == E        # no planes
+    assert s2h(lp, 4, p, None, 0, dl.DIT_BF16, p, dts, None, None, 0, None, None) == E        # too many
+    assert s2h(lp, 3, p, None, 0, dl.DIT_E4M3, p, dts, None, None, 0, None, None) == E        # no e4m3 source
+    assert s2h(lp, 3, p, None, 0, dl.DIT_BF16, p, bad_dts, None, None, 0, None, None) == E    # nor destination
+    assert s2h(lp, 3, p, None, 65, dl.DIT_BF16, p, dts, None, None, 0, None, None) == E       # split > S
+    assert s2h(lp, 3, p, None, 10, dl.DIT_BF16, p, dts, None, None, 0, None, None) == E       # second stream
+    assert s2h(lp, 3, mis, None, 0, dl.DIT_BF16, p, dts, None, None, 0, None, None) == E      # misaligned
+    assert s2h(lp, 3, p, None, 0, dl.DIT_BF16, mis, dts, None, None, 0, None, None) == E
+    assert s2h(lp, 2, p, None, 0, dl.DIT_BF16, p, dts, None, None, 0b100, None, None) == E    # missing plane
+    assert s2h(lp, 3, p, None, 0, dl.DIT_BF16, p, dts, None, None, 0b011, None, None) == E    # no tables
+    assert s2h(lp, 3, p, None, 0, dl.DIT_BF16, p, dts, tab, None, 0b011, None, None) == E
+    assert s2h(None, 3, p, None, 0, dl.DIT_BF16, p, dts, None, None, 0, None, None) == E      # no layout
+    buf = ctypes.c_void_p(4 << 20)
+    assert h2s(lp, None, dl.DIT_BF16, buf, None, 0, dl.DIT_BF16, None) == E
+    assert h2s(lp, buf, dl.DIT_BF16, None, None, 0, dl.DIT_BF16, None) == E
+    assert h2s(lp, buf, dl.DIT_BF16, buf, None, 10, dl.DIT_BF16, None) == E                   # second stream
+    assert h2s(lp, buf, dl.DIT_E4M3, buf, None, 0, dl.DIT_BF16, None) == E
+    assert h2s(lp, buf, dl.DIT_BF16, buf, None, -1, dl.DIT_BF16, None) == E
+    lay24 = dl.DitSpLayout()
+    assert L.dit_sp_layout_init(1, 64, 4, 12, 2, 1, ctypes.byref(lay24)) == 0
+    assert s2h(ctypes.byref(lay24), 3, p, None, 0, dl.DIT_BF16, p, dts, None, None, 0, None,
+               None) == dl.DIT_ERR_UNSUPPORTED                                                 # D % 8 != 0
+    # a corrupted layout table is refused
+    bad = dl.DitSpLayout.from_buffer_copy(lay)
+    bad.ring_real[0] = 3
+    assert h2s(ctypes.byref(bad), buf, dl.DIT_BF16, buf, None, 0, dl.DIT_BF16, None) == E
+    # S = 0 moves nothing, whatever the pointers
+    lay0 = dl.DitSpLayout()
+    assert L.dit_sp_layout_init(2, 0, 4, 64, 2, 2, ctypes.byref(lay0)) == 0
+    null3 = (ctypes.c_void_p * 3)(None, None, None)
+    assert s2h(ctypes.byref(lay0), 3, null3, None, 0, dl.DIT_BF16, null3, dts, None, None, 0, None, None) == 0
+    assert h2s(ctypes.byref(lay0), None, dl.DIT_BF16, None, None, 0, dl.DIT_BF16, None) == 0
 
 
 def test_layout_with_lcm_padding_changes_wire_sizes(dl):

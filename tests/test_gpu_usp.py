@@ -56,8 +56,9 @@ def test_tiny_fp32_full(U, R):
     assert max_abs(o2, ref) <= 1e-12
 
 
+@pytest.mark.parametrize("exchange", ["direct", "a2a"])
 @pytest.mark.parametrize("B,S,H,U,R", [(1, 1000, 5, 3, 2), (2, 700, 4, 2, 3), (1, 333, 3, 4, 1)])
-def test_medium_bf16_full(B, S, H, U, R):
+def test_medium_bf16_full(B, S, H, U, R, exchange):
     """Sizes the oracle finishes in seconds, spanning several tiles and ragged
     tails, with padded heads and uneven ranks: compared in full."""
     D = 128
@@ -65,24 +66,23 @@ def test_medium_bf16_full(B, S, H, U, R):
     k = synth.normal((B, S, H, D), 21, 0.5, "bf16")
     v = synth.normal((B, S, H, D), 22, 0.5, "bf16")
     from sequence_attention_gb300.usp import UspPlan
-    plan = UspPlan(B, S, H, D, U, R)
+    plan = UspPlan(B, S, H, D, U, R, exchange=exchange)
     out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device="cuda")
-    plan.run(q.cuda(), k.cuda(), v.cuda(), out)
-    torch.cuda.synchronize()
+    plan.run(q.cuda(), k.cuda(), v.cuda(), out, check=True)
     ref, _ = oatt.attention(f64(q), f64(k), f64(v))
     assert_bf16_close(f64(out), ref, "usp")
-    assert int(plan.status.item()) == 0 and int(plan.range_flag.item()) == 0
 
 
-FULL = [("flux1024", 2), ("flux1024", 4), ("flux1008", 4), ("flux1008_4480", 4),
-        ("qwen1328", 5), ("wan", 8)]
+# FLUX-1024 and FLUX-1008 are compared on every row in test_gpu_fullsize.py;
+# the two larger workloads on their seams plus seeded random rows.
+FULL = [("qwen1328", 5, "direct"), ("qwen1328", 5, "a2a"), ("wan", 8, "direct")]
 
 
-@pytest.mark.parametrize("name,U", FULL)
-def test_full_size_sampled(name, U):
+@pytest.mark.parametrize("name,U,exchange", FULL)
+def test_full_size_sampled(name, U, exchange):
     w = synth.WORKLOADS[name]
     q, k, v = w.qkv()
-    plan = _plan(w, U)
+    plan = _plan(w, U, exchange=exchange)
     out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device="cuda")
     plan.run(q.cuda(), k.cuda(), v.cuda(), out)
     torch.cuda.synchronize()
@@ -197,3 +197,27 @@ def test_half_partials_against_float_partials():
         torch.cuda.synchronize()
         assert int(plan.status.item()) == 0
     assert rel_rms(f64(outs[torch.float16]), f64(outs[torch.float32])) <= MERGE_REL_RMS
+
+
+@pytest.mark.parametrize("exchange", ["direct", "a2a"])
+def test_plan_check_reports_f16_overflow_and_clears(exchange):
+    """A V value past f16's range makes the default plan's output non-finite;
+    check() raises DIT_ERR_RANGE for it, clears the sticky word, and a plan
+    with bf16 V runs the same inputs cleanly."""
+    import sequence_attention_gb300 as sa
+    from sequence_attention_gb300.usp import UspPlan
+    B, S, H, D, U, R = 1, 300, 4, 64, 2, 2
+    q = synth.normal((B, S, H, D), 30, 0.5, "bf16").cuda()
+    k = synth.normal((B, S, H, D), 31, 0.5, "bf16").cuda()
+    v = synth.normal((B, S, H, D), 32, 0.5, "bf16").cuda()
+    v[0, 17, 2, 5] = 1.0e6
+    out = torch.empty_like(q)
+    plan = UspPlan(B, S, H, D, U, R, exchange=exchange)
+    plan.run(q, k, v, out)
+    with pytest.raises(sa.DitError) as ei:
+        plan.check()
+    assert ei.value.status == 5
+    plan.check()                                  # cleared: no error now
+    plan_bf = UspPlan(B, S, H, D, U, R, exchange=exchange, v_dtype=torch.bfloat16)
+    plan_bf.run(q, k, v, out, check=True)
+    assert torch.isfinite(out.float()).all()
