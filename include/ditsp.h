@@ -369,7 +369,8 @@ DIT_API dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplanes, 
  *   dst_dt[p] (one rounding) and Hp - H zero heads; sequence-padding rows
  *   are zero; rows past ring_len[r] are not touched.  Planes with bit p of
  *   rope_planes set are rotated as by dit_ulysses_unpack_rope (cos_tab,
- *   sin_tab float32 [S][D/2], 16-byte aligned; NULL when rope_planes = 0).
+ *   sin_tab float32 [S][D/2], 16-byte aligned; NULL when rope_planes = 0;
+ *   D <= 384 when rope_planes != 0, else DIT_ERR_UNSUPPORTED).
  *   d_range_flag as for dit_ulysses_unpack.  Equal to dit_ulysses_pack (or
  *   _pack_joint) + dit_a2a_sim + dit_ulysses_unpack (or _unpack_rope) with
  *   wire_dt = src_dt.

@@ -9,7 +9,8 @@
 //   otherwise move it when the two differ by many binades).
 // Merge (SGLang Diffusion "Parallelism Overview", What happens to the shapes /
 // Constraints: the ring's online-softmax merge over same-head, different-row
-// partials):  lse = M + ln sum_j exp(lse_j - M),  O = sum_j exp(lse_j - lse) O_j.
+// partials):  lse = M + ln sum_j exp(lse_j - M),  O = sum_j exp(lse_j - lse) O_j
+// (evaluated as sum_j (e_j / sum e) O_j with e_j = exp(lse_j - M)).
 #include <math.h>
 #include <string.h>
 
@@ -102,24 +103,47 @@ struct MergeArgs {
     dit_lse_view lse_out;
 };
 
+// Unsigned division by a divisor fixed at launch, as a multiply-high and a
+// shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): with s = ceil(log2 d) and m = floor(2^32 (2^s - d)
+// / d) + 1, n / d = (mulhi(n, m) + n) >> s for every n < 2^31.
+struct FastDiv {
+    uint32_t d, m, s;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.s = 0;
+    while ((1ull << f.s) < d) ++f.s;
+    f.m = (uint32_t)(((1ull << 32) * ((1ull << f.s) - d)) / d + 1);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+    return (uint32_t)(((unsigned long long)__umulhi(n, f.m) + n) >> f.s);
+}
+
 // Merge, chunk-per-thread form: thread t of block (x, r*B + b) takes the
 // 8-element chunk c of unit u = (row i, head h), and SLOTS such chunks
 // spaced one block apart.  Every load of a thread -- the NP log-sum-exp
 // values and the NP partial chunks of each of its slots -- is issued before
 // any arithmetic, so one memory round trip covers all of them (the lanes of
 // one unit read the same log-sum-exp words, served by one transaction).
-// Each thread then forms the unit's weights itself: a few exponentials per
-// 8 outputs, far below what the bandwidth leaves free.  SLOTS * NP is about
-// four, so a thread keeps 64 (16-bit parts) or 128 bytes of partials in
-// flight.  Units run h-fastest within a row and chunks c-fastest within a
-// head, so the block's loads and stores cover whole contiguous rows.
+// Each thread forms its unit's weights itself as w_j = e_j / sum_j e_j with
+// e_j = 2^((lse_j - M) log2 e): NP exponentials and one reciprocal per 8
+// outputs, and the merged log-sum-exp (a logarithm) only when it is asked
+// for.  Index decoding is 32-bit, with divisions by the launch's fixed row
+// and head sizes done as multiply-shifts.  SLOTS * NP is about four, so a
+// thread keeps 64 (16-bit parts) or 128 bytes of partials in flight.  Units
+// run h-fastest within a row and chunks c-fastest within a head, so the
+// block's loads and stores cover whole contiguous rows.
 template <int NP, int SLOTS, int PB>
-__global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant__ MergeArgs a) {
+__global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant__ MergeArgs a, FastDiv per_row,
+                                                           FastDiv chunks) {
     const int r = blockIdx.y / a.B, b = blockIdx.y % a.B;
-    const int chunks = a.D >> 3;
-    const long long per_row = (long long)a.H * chunks;
-    const long long total = (long long)a.q_len[r] * per_row;
-    const long long t0 = (long long)blockIdx.x * blockDim.x * SLOTS + threadIdx.x;
+    const uint32_t total = (uint32_t)a.q_len[r] * per_row.d;
+    const uint32_t t0 = blockIdx.x * (blockDim.x * SLOTS) + threadIdx.x;
     const char* pp = static_cast<const char*>(a.parts.ptr);
     const dit_dtype pdt = a.parts_dt;
     long long base[SLOTS];
@@ -127,17 +151,17 @@ __global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant
     int lh[SLOTS], lc[SLOTS];
 #pragma unroll
     for (int k = 0; k < SLOTS; ++k) {
-        const long long t = t0 + (long long)k * blockDim.x;
+        const uint32_t t = t0 + (uint32_t)k * blockDim.x;
         lrow[k] = -1;
         if (t < total) {
-            const int i = (int)(t / per_row);
-            const int rem = (int)(t - (long long)i * per_row);
-            const int h = rem / chunks;
-            lrow[k] = i;
-            lh[k] = h;
-            lc[k] = rem - h * chunks;
+            const uint32_t i = fdiv(t, per_row);
+            const uint32_t rem = t - i * per_row.d;
+            const uint32_t h = fdiv(rem, chunks);
+            lrow[k] = (int)i;
+            lh[k] = (int)h;
+            lc[k] = (int)(rem - h * chunks.d);
             base[k] = r * a.parts.stride_q + b * a.parts.stride_b + (long long)i * a.parts.stride_s +
-                      h * a.parts.stride_h + lc[k] * 8;
+                      (long long)h * a.parts.stride_h + lc[k] * 8;
         }
     }
     pdl_wait();
@@ -159,6 +183,7 @@ __global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant
     }
     char* op = static_cast<char*>(a.out.ptr);
     const int ob = dtype_bytes(a.out_dt);
+    constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll
     for (int k = 0; k < SLOTS; ++k) {
         if (lrow[k] < 0) continue;
@@ -170,13 +195,19 @@ __global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant
         for (int e = 0; e < 8; ++e) acc.f[e] = 0.f;
         float lse = -INFINITY;
         if (M != -INFINITY) {
+            float ej[NP];
             float sum = 0.f;
-#pragma unroll
-            for (int j = 0; j < NP; ++j) sum += expf(lj[k][j] - M);
-            lse = M + logf(sum);
+            const float mb = M * kLog2e;
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
-                const float w = expf(lj[k][j] - lse);
+                ej[j] = exp2f(fmaf(lj[k][j], kLog2e, -mb));      // 2^((lse_j - M) log2 e); -inf -> 0
+                sum += ej[j];
+            }
+            const float inv = 1.0f / sum;                         // sum >= 1 (the largest part gives 1)
+            if (a.lse_out.ptr && lc[k] == 0) lse = M + logf(sum);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const float w = ej[j] * inv;
                 Vec8 o;
                 load8(&raw[k][j][0], pdt, o);
 #pragma unroll
@@ -198,7 +229,8 @@ cudaError_t launch_merge_chunks(const MergeArgs& a, long long work, cudaStream_t
     constexpr int SLOTS = NP >= 4 ? 1 : 4 / NP;
     const long long per_block = 256LL * SLOTS;
     const dim3 grid((unsigned)((work + per_block - 1) / per_block), (unsigned)a.n_q_b);
-    return launch_pdl(merge_chunks_kernel<NP, SLOTS, PB>, grid, dim3(256), 0, st, a);
+    const FastDiv per_row = make_fastdiv((uint32_t)(a.H * (a.D / 8))), chunks = make_fastdiv((uint32_t)(a.D / 8));
+    return launch_pdl(merge_chunks_kernel<NP, SLOTS, PB>, grid, dim3(256), 0, st, a, per_row, chunks);
 }
 
 template <int PB>
@@ -298,7 +330,9 @@ extern "C" dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int
     if ((long long)n_q * B > 65535) return fail(DIT_ERR_UNSUPPORTED, "%s: n_q * B too large", who);
     a.n_q_b = n_q * B;
     const long long work = (long long)maxq * H * (D / 8);      // chunks of the longest block
-    if (work / 256 >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 2^39 chunks per block", who);
+    // 32-bit index decoding in the kernel: every block's chunk count, and the
+    // grid's last chunk index, below 2^31
+    if (work + 256LL * 4 >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: 2^31 or more chunks per block", who);
     const cudaStream_t st = (cudaStream_t)stream;
     const cudaError_t e = parts_dt == DIT_F32 ? launch_merge<4>(a, work, st) : launch_merge<2>(a, work, st);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));

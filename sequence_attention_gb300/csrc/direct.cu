@@ -17,13 +17,13 @@
 //   head -> seq:  sequence row (b, t < S) = the first H heads of head-layout
 //                 row (r, b, t - ring_off[r]).
 //
-// Work division: the destination is a flat sequence of 8-element chunks, rows
-// of cpr chunks each.  Every warp takes one contiguous equal share of the
-// chunks (rounded to whole 32-chunk steps), so all warps of the grid finish
-// together; lanes walk the share 32 chunks apart.  Per batch of kItems
-// chunks a lane issues every 16-byte load first, then converts and stores.
-// The grid holds as many blocks as fit on the SMs at once (or fewer for
-// small copies): one wave, no tail.
+// Work division: the destination is a sequence of rows of cpr 8-element
+// chunks, one row per warp; a row's source and destination addresses are the
+// same for every lane (no per-chunk index arithmetic), and lanes take its
+// chunks 32 apart.  Per batch of kDirItems chunks a lane issues every 16-byte
+// load first, then converts and stores.  A rotated row's angle rows are
+// staged in shared memory once per warp, so each chunk reads its cosines and
+// sines from there.
 #include <string.h>
 
 #include "convert.cuh"
@@ -34,6 +34,7 @@ namespace {
 
 constexpr int kDirThreads = 256;
 constexpr int kDirItems = 8;     // chunks per lane in flight
+constexpr int kDirMaxRopeD = 384;   // largest head dim of the rotary path
 
 struct DirectArgs {
     dit_sp_layout L;
@@ -53,7 +54,7 @@ struct DirectArgs {
     long long nrows;             // destination rows
     int cpr;                     // chunks per destination row
     int creal;                   // chunks of a row that carry real heads (H * D / 8)
-    long long share;             // chunks per warp
+    long long share;             // destination rows per warp
 };
 
 // Byte address of the first element of sequence row t of batch b.
@@ -80,100 +81,101 @@ __device__ __forceinline__ long long head_row_elems(const dit_sp_layout& L, int 
     return (((long long)r * L.B + b) * L.S_cap + i) * L.Hp * L.D;
 }
 
-template <bool S2H, int SB, int DB, bool ROPE>
-__global__ void __launch_bounds__(kDirThreads) direct_kernel(const __grid_constant__ DirectArgs A) {
+// Where destination row `row` reads from and writes to.  src is NULL for a
+// sequence-padding row (seq -> head), which is written as zeros.
+struct RowIO {
+    const char* src;
+    char* dst;
+    int p, t;
+};
+
+template <bool S2H, int SB, int DB>
+__device__ __forceinline__ RowIO row_io(const DirectArgs& A, long long row) {
     const dit_sp_layout& L = A.L;
-    const int lane = threadIdx.x & 31;
-    const long long warp = (long long)blockIdx.x * (kDirThreads / 32) + (threadIdx.x >> 5);
-    const long long q0 = warp * A.share;
-    const long long q1 = min(A.nrows * A.cpr, q0 + A.share);
-    pdl_wait();
-    if (q0 >= q1) {
-        pdl_trigger();
-        return;
+    RowIO io;
+    if (S2H) {
+        const long long per_plane = (long long)L.B * L.S_pad;
+        io.p = (int)(row / per_plane);
+        const long long rem = row - io.p * per_plane;
+        const int b = (int)(rem / L.S_pad);
+        io.t = (int)(rem - (long long)b * L.S_pad);
+        io.dst = A.head[io.p] + head_row_elems(L, b, io.t) * DB;
+        io.src = io.t < L.S ? seq_row(A, A.seq, A.seq2, io.p, b, io.t, SB) : nullptr;
+    } else {
+        const int b = (int)(row / L.S);
+        io.p = 0;
+        io.t = (int)(row - (long long)b * L.S);
+        io.src = A.head[0] + head_row_elems(L, b, io.t) * SB;
+        io.dst = seq_row(A, A.seq, A.seq2, 0, b, io.t, DB);
     }
+    return io;
+}
+
+template <bool S2H, int SB, int DB, bool ROPE>
+__global__ void __launch_bounds__(kDirThreads, ROPE ? 3 : 1) direct_kernel(const __grid_constant__ DirectArgs A) {
+    // rotary path: the token's cosine row then sine row (D/2 floats each),
+    // staged per warp while the row's first data loads are in flight
+    __shared__ float4 tab_sm[ROPE ? kDirThreads / 32 : 1][ROPE ? kDirMaxRopeD / 4 : 1];
+    const dit_sp_layout& L = A.L;
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const long long warp = (long long)blockIdx.x * (kDirThreads / 32) + wib;
+    const long long row0 = warp * A.share;
+    const long long row1 = min(A.nrows, row0 + A.share);
+    pdl_wait();
     const bool want_check = S2H && A.range_flag != nullptr;
     bool overflow = false;
-    // the lane's next chunk: destination row `row`, chunk `c` of it
-    long long q = q0 + lane;
-    long long row = q / A.cpr;
-    int c = (int)(q - row * A.cpr);
-    // decoded row (refreshed when `row` changes)
-    long long cur = -1;
-    const char* srow = nullptr;
-    char* drow = nullptr;
-    int rp = 0, rt = 0;
-    bool rreal = false;
-    auto decode = [&]() {
-        cur = row;
-        if (S2H) {
-            const long long per_plane = (long long)L.B * L.S_pad;
-            rp = (int)(row / per_plane);
-            const long long rem = row - rp * per_plane;
-            const int b = (int)(rem / L.S_pad);
-            rt = (int)(rem - (long long)b * L.S_pad);
-            rreal = rt < L.S;
-            drow = A.head[rp] + head_row_elems(L, b, rt) * DB;
-            srow = rreal ? seq_row(A, A.seq, A.seq2, rp, b, rt, SB) : nullptr;
-        } else {
-            const int b = (int)(row / L.S);
-            rt = (int)(row - (long long)b * L.S);
-            rp = 0;
-            rreal = true;
-            srow = A.head[0] + head_row_elems(L, b, rt) * SB;
-            drow = seq_row(A, A.seq, A.seq2, 0, b, rt, DB);
-        }
-    };
     constexpr int NI = kDirItems;
-    uint4 raw[NI][SB / 2];
-    char* dptr[NI];
-    int meta[NI];      // plane, | 4 when rotated; -1: no chunk
-    long long tab[NI]; // rotary table offset (floats) of the chunk's first pair
-    for (long long qb = q0; qb < q1; qb += 32 * NI) {
+    const int q4 = L.D >> 3;                 // float4s per table row
+    for (long long row = row0; row < row1; ++row) {
+        // the row's place on both sides (the same for every lane of the warp)
+        const RowIO io = row_io<S2H, SB, DB>(A, row);
+        const int rp = io.p;
+        const bool rreal = io.src != nullptr;
+        const dit_dtype sdt = A.src_dt[rp], ddt = A.dst_dt[rp];
+        const bool rot = ROPE && rreal && ((A.rope_planes >> rp) & 1u);
+        const int lim = rreal ? A.creal : 0;     // chunks read from the source; the rest are zero
+        if (ROPE && rot) {
+            const float4* ct = reinterpret_cast<const float4*>(A.cos_tab + (long long)io.t * (L.D >> 1));
+            const float4* sn = reinterpret_cast<const float4*>(A.sin_tab + (long long)io.t * (L.D >> 1));
+            for (int j = lane; j < 2 * q4; j += 32) cp_async16(&tab_sm[wib][j], j < q4 ? ct + j : sn + (j - q4));
+            cp_async_commit();
+        }
+        // every lane runs the same batches (the table staging has a warp barrier)
+        for (int c0 = 0; c0 < A.cpr; c0 += 32 * NI) {
+            uint4 raw[NI][SB / 2];
 #pragma unroll
-        for (int k = 0; k < NI; ++k) {
-            meta[k] = -1;
+            for (int k = 0; k < NI; ++k) {
+                const int c = c0 + lane + 32 * k;
 #pragma unroll
-            for (int h = 0; h < SB / 2; ++h) raw[k][h] = make_uint4(0, 0, 0, 0);
-            if (q < q1) {
-                if (row != cur) decode();
-                dptr[k] = drow + (long long)c * 8 * DB;
-                int m = rp;
-                if (rreal && c < A.creal) {
-                    const uint4* s = reinterpret_cast<const uint4*>(srow + (long long)c * 8 * SB);
+                for (int h = 0; h < SB / 2; ++h) raw[k][h] = make_uint4(0, 0, 0, 0);
+                if (c < lim) {
+                    const uint4* src = reinterpret_cast<const uint4*>(io.src + (long long)c * 8 * SB);
 #pragma unroll
-                    for (int h = 0; h < SB / 2; ++h) raw[k][h] = s[h];
-                    if (ROPE && ((A.rope_planes >> rp) & 1u)) {
-                        m |= 4;
-                        tab[k] = (long long)rt * (L.D >> 1) + (((c * 8) % L.D) >> 1);
-                    }
+                    for (int h = 0; h < SB / 2; ++h) raw[k][h] = src[h];
                 }
-                meta[k] = m;
             }
-            q += 32;
-            c += 32;
-            while (c >= A.cpr) {
-                c -= A.cpr;
-                ++row;
+            if (ROPE && rot && c0 == 0) {
+                cp_async_wait_all();
+                __syncwarp();
+            }
+#pragma unroll
+            for (int k = 0; k < NI; ++k) {
+                const int c = c0 + lane + 32 * k;
+                if (c >= A.cpr) break;
+                uint4 o[DB / 2];
+                if (ROPE && rot && c < lim) {
+                    const int i4 = (((c * 8) % L.D) >> 3);
+                    rope8<SB, DB>(raw[k], sdt, ddt, tab_sm[wib][i4], tab_sm[wib][q4 + i4], want_check && ddt != DIT_F32,
+                                  o, overflow);
+                } else {
+                    convert8<SB, DB>(raw[k], sdt, ddt, want_check && narrowing(sdt, ddt), o, overflow);
+                }
+                uint4* d = reinterpret_cast<uint4*>(io.dst + (long long)c * 8 * DB);
+#pragma unroll
+                for (int h = 0; h < DB / 2; ++h) d[h] = o[h];
             }
         }
-#pragma unroll
-        for (int k = 0; k < NI; ++k) {
-            if (meta[k] < 0) continue;
-            const int p = meta[k] & 3;
-            const dit_dtype sdt = A.src_dt[p], ddt = A.dst_dt[p];
-            uint4 o[DB / 2];
-            if (ROPE && (meta[k] & 4)) {
-                const float4 cs = __ldg(reinterpret_cast<const float4*>(A.cos_tab + tab[k]));
-                const float4 sn = __ldg(reinterpret_cast<const float4*>(A.sin_tab + tab[k]));
-                rope8<SB, DB>(raw[k], sdt, ddt, cs, sn, want_check && ddt != DIT_F32, o, overflow);
-            } else {
-                convert8<SB, DB>(raw[k], sdt, ddt, want_check && narrowing(sdt, ddt), o, overflow);
-            }
-            uint4* d = reinterpret_cast<uint4*>(dptr[k]);
-#pragma unroll
-            for (int h = 0; h < DB / 2; ++h) d[h] = o[h];
-        }
+        if (ROPE && rot) __syncwarp();      // the next row's staging overwrites the tables
     }
     if (overflow) *A.range_flag = (int)DIT_ERR_RANGE;
     pdl_trigger();
@@ -181,23 +183,15 @@ __global__ void __launch_bounds__(kDirThreads) direct_kernel(const __grid_consta
 
 template <bool S2H, int SB, int DB, bool ROPE>
 dit_status launch_direct_sized(DirectArgs& a, cudaStream_t st, const char* who) {
-    auto kern = direct_kernel<S2H, SB, DB, ROPE>;
-    // blocks resident per SM, looked up once per instantiation
-    static const int occ = [&] {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDirThreads, 0) != cudaSuccess || n <= 0) n = 2;
-        return n;
-    }();
-    const long long total = a.nrows * a.cpr;
-    const long long per_block = (long long)kDirThreads * kDirItems;
-    long long blocks = (total + per_block - 1) / per_block;
-    const long long resident = (long long)num_sms() * occ;
-    if (blocks > resident) blocks = resident;
-    const long long warps = blocks * (kDirThreads / 32);
-    long long share = (total + warps - 1) / warps;
-    share = (share + 31) / 32 * 32;
-    a.share = share;
-    cudaError_t e = launch_pdl(kern, dim3((unsigned)blocks), dim3(kDirThreads), 0, st, a);
+    // one destination row per warp, as many blocks as that takes: the block
+    // scheduler streams them through memory in order (measured against one
+    // wave of resident warps with equal shares of rows and against a staged
+    // form with bulk copies into shared memory: both slower, 5.3-5.9 TB/s
+    // against 6.0 at the FLUX-like and 7.1 TB/s at the Wan-like size)
+    a.share = 1;
+    const long long blocks = (a.nrows + kDirThreads / 32 - 1) / (kDirThreads / 32);
+    if (blocks >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: too many rows", who);
+    cudaError_t e = launch_pdl(direct_kernel<S2H, SB, DB, ROPE>, dim3((unsigned)blocks), dim3(kDirThreads), 0, st, a);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     return check_launch(who);
 }
@@ -244,6 +238,8 @@ extern "C" dit_status dit_ulysses_seq_to_head(const dit_sp_layout* L, int nplane
         if (!dtype_ok(dst_dt[p])) return fail(DIT_ERR_INVALID_ARG, "%s: bad destination dtype", who);
     if (split < 0 || split > L->S) return fail(DIT_ERR_INVALID_ARG, "%s: split out of [0, S]", who);
     if (rope_planes >> nplanes) return fail(DIT_ERR_INVALID_ARG, "%s: rope_planes names a missing plane", who);
+    if (rope_planes && L->D > kDirMaxRopeD)
+        return fail(DIT_ERR_UNSUPPORTED, "%s: the rotary path supports D <= %d", who, kDirMaxRopeD);
     if (L->S == 0) return DIT_OK;
     if (rope_planes && (!cos_tab || !sin_tab || !aligned16(cos_tab) || !aligned16(sin_tab)))
         return fail(DIT_ERR_INVALID_ARG, "%s: rotary tables NULL or misaligned", who);

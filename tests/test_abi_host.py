@@ -301,6 +301,10 @@ def test_one_pass_permutation_validates_before_any_launch(dl):
     assert L.dit_sp_layout_init(1, 64, 4, 12, 2, 1, ctypes.byref(lay24)) == 0
     assert s2h(ctypes.byref(lay24), 3, p, None, 0, dl.DIT_BF16, p, dts, None, None, 0, None,
                None) == dl.DIT_ERR_UNSUPPORTED                                                 # D % 8 != 0
+    lay512 = dl.DitSpLayout()
+    assert L.dit_sp_layout_init(1, 64, 2, 512, 2, 1, ctypes.byref(lay512)) == 0
+    assert s2h(ctypes.byref(lay512), 3, p, None, 0, dl.DIT_BF16, p, dts, tab, tab, 0b011, None,
+               None) == dl.DIT_ERR_UNSUPPORTED                                                 # rotary D > 384
     # a corrupted layout table is refused
     bad = dl.DitSpLayout.from_buffer_copy(lay)
     bad.ring_real[0] = 3
