@@ -322,10 +322,11 @@ dit_status launch_fp8(K kernel, const Fp8Args& a, cudaStream_t st, const char* w
     if (a.nruns == 0) return DIT_OK;
     if (a.nruns >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 2^31 runs", who);
     // 16 runs per warp (128 per block): measured against 1, 2, 4 and 8 on the
-    // FLUX- and Wan-like shapes, the fastest or equal except the FLUX-size
-    // unpack (4 runs per warp: 13 % faster back to back, 4 % with L2 flushed).
-    // Fewer runs per block pay the per-block decode of run offsets more often.
-    const int rpw = 16;
+    // FLUX- and Wan-like shapes, the fastest at the Wan size (fewer runs per
+    // block pay the per-block decode of run offsets more often).  When 16
+    // would leave fewer than 3 blocks per SM (the FLUX-like exchange), 8
+    // runs per warp: pack 4.61 against 4.45 TB/s, unpack 4.03 against 3.85.
+    const int rpw = (a.nruns + 127) / 128 < 3LL * num_sms() ? 8 : 16;
     const long long blocks = (a.nruns + 8LL * rpw - 1) / (8LL * rpw);
     cudaError_t e = launch_pdl(kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, a, rpw);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
