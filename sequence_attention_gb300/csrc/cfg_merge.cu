@@ -124,6 +124,19 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
     return (uint32_t)(((unsigned long long)__umulhi(n, f.m) + n) >> f.s);
 }
 
+// The SFU's base-2 exponential and reciprocal (relative errors about 2^-22
+// and 2^-23): ex2(-inf) = 0, so an empty partial gets weight 0.
+__device__ __forceinline__ float sfu_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float sfu_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Merge, chunk-per-thread form: thread t of block (x, r*B + b) takes the
 // 8-element chunk c of unit u = (row i, head h), and SLOTS such chunks
 // spaced one block apart.  Every load of a thread -- the NP log-sum-exp
@@ -131,9 +144,10 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
 // any arithmetic, so one memory round trip covers all of them (the lanes of
 // one unit read the same log-sum-exp words, served by one transaction).
 // Each thread forms its unit's weights itself as w_j = e_j / sum_j e_j with
-// e_j = 2^((lse_j - M) log2 e): NP exponentials and one reciprocal per 8
-// outputs, and the merged log-sum-exp (a logarithm) only when it is asked
-// for.  Index decoding is 32-bit, with divisions by the launch's fixed row
+// e_j = 2^((lse_j - M) log2 e): NP SFU exponentials and one SFU reciprocal
+// per 8 outputs (relative error of a weight below 1e-6, far inside the
+// merge's fp32 bound), and the merged log-sum-exp (an accurate logarithm)
+// only when it is asked for.  Index decoding is 32-bit, with divisions by the launch's fixed row
 // and head sizes done as multiply-shifts.  SLOTS * NP is about four, so a
 // thread keeps 64 (16-bit parts) or 128 bytes of partials in flight.  Units
 // run h-fastest within a row and chunks c-fastest within a head, so the
@@ -200,10 +214,10 @@ __global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant
             const float mb = M * kLog2e;
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
-                ej[j] = exp2f(fmaf(lj[k][j], kLog2e, -mb));      // 2^((lse_j - M) log2 e); -inf -> 0
+                ej[j] = sfu_ex2(fmaf(lj[k][j], kLog2e, -mb));    // 2^((lse_j - M) log2 e); -inf -> 0
                 sum += ej[j];
             }
-            const float inv = 1.0f / sum;                         // sum >= 1 (the largest part gives 1)
+            const float inv = sfu_rcp(sum);                       // sum >= 1 (the largest part gives ~1)
             if (a.lse_out.ptr && lc[k] == 0) lse = M + logf(sum);
 #pragma unroll
             for (int j = 0; j < NP; ++j) {

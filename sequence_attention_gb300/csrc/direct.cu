@@ -23,7 +23,9 @@
 // chunks 32 apart.  Per batch of kDirItems chunks a lane issues every 16-byte
 // load first, then converts and stores.  A rotated row's angle rows are
 // staged in shared memory once per warp, so each chunk reads its cosines and
-// sines from there.
+// sines from there.  The 16-bit-source and rotated forms are held to three
+// blocks per SM (80 registers; 8 to 32 bytes of spill): ncu showed the
+// two-block form with a fifth of the warps active and long-scoreboard stalls.
 #include <string.h>
 
 #include "convert.cuh"
@@ -112,7 +114,7 @@ __device__ __forceinline__ RowIO row_io(const DirectArgs& A, long long row) {
 }
 
 template <bool S2H, int SB, int DB, bool ROPE>
-__global__ void __launch_bounds__(kDirThreads, ROPE ? 3 : 1) direct_kernel(const __grid_constant__ DirectArgs A) {
+__global__ void __launch_bounds__(kDirThreads, (ROPE || SB == 2) ? 3 : 1) direct_kernel(const __grid_constant__ DirectArgs A) {
     // rotary path: the token's cosine row then sine row (D/2 floats each),
     // staged per warp while the row's first data loads are in flight
     __shared__ float4 tab_sm[ROPE ? kDirThreads / 32 : 1][ROPE ? kDirMaxRopeD / 4 : 1];
