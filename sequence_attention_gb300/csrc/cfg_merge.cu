@@ -137,32 +137,36 @@ __device__ __forceinline__ float sfu_rcp(float x) {
     return y;
 }
 
-// Merge, chunk-per-thread form: thread t of block (x, r*B + b) takes the
-// 8-element chunk c of unit u = (row i, head h), and SLOTS such chunks
-// spaced one block apart.  Every load of a thread -- the NP log-sum-exp
-// values and the NP partial chunks of each of its slots -- is issued before
-// any arithmetic, so one memory round trip covers all of them (the lanes of
-// one unit read the same log-sum-exp words, served by one transaction).
-// Each thread forms its unit's weights itself as w_j = e_j / sum_j e_j with
-// e_j = 2^((lse_j - M) log2 e): NP SFU exponentials and one SFU reciprocal
-// per 8 outputs (relative error of a weight below 1e-6, far inside the
-// merge's fp32 bound), and the merged log-sum-exp (an accurate logarithm)
-// only when it is asked for.  Index decoding is 32-bit, with divisions by the launch's fixed row
-// and head sizes done as multiply-shifts.  SLOTS * NP is about four, so a
-// thread keeps 64 (16-bit parts) or 128 bytes of partials in flight.  Units
-// run h-fastest within a row and chunks c-fastest within a head, so the
-// block's loads and stores cover whole contiguous rows.
-template <int NP, int SLOTS, int PB>
+// Merge, chunk-per-thread form: thread t of block (x, r*B + b) takes CPT
+// 8-element chunks of unit u = (row i, head h), D / 8 / CPT chunks apart (so
+// each load instruction of a warp still covers whole 128-byte segments) --
+// the same weights for all of them -- and SLOTS such groups spaced one
+// block apart.
+// Every load of a thread -- the NP log-sum-exp values and the NP partial
+// chunks of each of its slots -- is issued before any arithmetic, so one
+// memory round trip covers all of them (the lanes of one unit read the same
+// log-sum-exp words, served by one transaction).  Each thread forms its
+// unit's weights itself as w_j = e_j / sum_j e_j with e_j = 2^((lse_j - M)
+// log2 e): NP SFU exponentials and one SFU reciprocal per 8 * CPT outputs
+// (relative error of a weight below 1e-6, far inside the merge's fp32
+// bound), and the merged log-sum-exp (an accurate logarithm) only when it is
+// asked for.  Index decoding is 32-bit, with divisions by the launch's fixed
+// row and head sizes done as multiply-shifts.  A thread keeps 64 (16-bit
+// parts) or 128 bytes of partials in flight.  Units run h-fastest within a
+// row and chunks c-fastest within a head, so the block's loads and stores
+// cover whole contiguous rows.
+template <int NP, int SLOTS, int PB, int CPT>
 __global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant__ MergeArgs a, FastDiv per_row,
-                                                           FastDiv chunks) {
+                                                           FastDiv groups) {
     const int r = blockIdx.y / a.B, b = blockIdx.y % a.B;
     const uint32_t total = (uint32_t)a.q_len[r] * per_row.d;
     const uint32_t t0 = blockIdx.x * (blockDim.x * SLOTS) + threadIdx.x;
     const char* pp = static_cast<const char*>(a.parts.ptr);
     const dit_dtype pdt = a.parts_dt;
+    const int cstride = (int)groups.d;   // chunks between a thread's CPT chunks (D / 8 / CPT)
     long long base[SLOTS];
-    int lrow[SLOTS];           // row i of the slot's unit (-1: no chunk)
-    int lh[SLOTS], lc[SLOTS];
+    int lrow[SLOTS];           // row i of the slot's unit (-1: none)
+    int lh[SLOTS], lc[SLOTS];  // head, first chunk (lc == 0: the thread writes the merged lse)
 #pragma unroll
     for (int k = 0; k < SLOTS; ++k) {
         const uint32_t t = t0 + (uint32_t)k * blockDim.x;
@@ -170,17 +174,17 @@ __global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant
         if (t < total) {
             const uint32_t i = fdiv(t, per_row);
             const uint32_t rem = t - i * per_row.d;
-            const uint32_t h = fdiv(rem, chunks);
+            const uint32_t h = fdiv(rem, groups);
             lrow[k] = (int)i;
             lh[k] = (int)h;
-            lc[k] = (int)(rem - h * chunks.d);
+            lc[k] = (int)(rem - h * groups.d);          // chunks lc, lc + chunks/CPT, ...
             base[k] = r * a.parts.stride_q + b * a.parts.stride_b + (long long)i * a.parts.stride_s +
                       (long long)h * a.parts.stride_h + lc[k] * 8;
         }
     }
     pdl_wait();
     float lj[SLOTS][NP];
-    uint4 raw[SLOTS][NP][PB / 2];
+    uint4 raw[SLOTS][NP][CPT][PB / 2];
 #pragma unroll
     for (int k = 0; k < SLOTS; ++k) {
         if (lrow[k] < 0) continue;
@@ -192,7 +196,9 @@ __global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant
         for (int j = 0; j < NP; ++j) {
             const uint4* q = reinterpret_cast<const uint4*>(pp + (base[k] + j * a.parts.stride_kv) * PB);
 #pragma unroll
-            for (int h = 0; h < PB / 2; ++h) raw[k][j][h] = q[h];
+            for (int c = 0; c < CPT; ++c)
+#pragma unroll
+                for (int h = 0; h < PB / 2; ++h) raw[k][j][c][h] = q[c * cstride * (PB / 2) + h];
         }
     }
     char* op = static_cast<char*>(a.out.ptr);
@@ -204,9 +210,11 @@ __global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant
         float M = -INFINITY;
 #pragma unroll
         for (int j = 0; j < NP; ++j) M = fmaxf(M, lj[k][j]);
-        Vec8 acc;
+        Vec8 acc[CPT];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc.f[e] = 0.f;
+        for (int c = 0; c < CPT; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[c].f[e] = 0.f;
         float lse = -INFINITY;
         if (M != -INFINITY) {
             float ej[NP];
@@ -222,15 +230,19 @@ __global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
                 const float w = ej[j] * inv;
-                Vec8 o;
-                load8(&raw[k][j][0], pdt, o);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc.f[e] = fmaf(w, o.f[e], acc.f[e]);
+                for (int c = 0; c < CPT; ++c) {
+                    Vec8 o;
+                    load8(&raw[k][j][c][0], pdt, o);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[c].f[e] = fmaf(w, o.f[e], acc[c].f[e]);
+                }
             }
         }
         const long long off = r * a.out.stride_q + b * a.out.stride_b + (long long)lrow[k] * a.out.stride_s +
                               lh[k] * a.out.stride_h + lc[k] * 8;
-        store8(op + off * ob, a.out_dt, acc);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) store8(op + (off + (long long)c * cstride * 8) * ob, a.out_dt, acc[c]);
         if (a.lse_out.ptr && lc[k] == 0)
             a.lse_out.ptr[r * a.lse_out.stride_q + b * a.lse_out.stride_b + lh[k] * a.lse_out.stride_h + lrow[k]] =
                 lse;
@@ -240,11 +252,27 @@ __global__ void __launch_bounds__(256) merge_chunks_kernel(const __grid_constant
 
 template <int NP, int PB>
 cudaError_t launch_merge_chunks(const MergeArgs& a, long long work, cudaStream_t st) {
+    const int chunks = a.D / 8;
+    // two chunks per thread (one set of weights for 16 outputs) for three or
+    // four 16-bit parts, when the head's chunk count is even: Wan-like R = 4
+    // on f16 partials 540 against 627 us.  With two parts the weights cost
+    // less than the second slot's independent loads gain (FLUX-1008 15.0
+    // against 16.1 us, Qwen 40.2 against 42.1), and fp32 parts need the
+    // registers.
+    constexpr bool two = NP >= 3 && NP * PB <= 8;
+    if (two && chunks % 2 == 0) {
+        constexpr int CPT = two ? 2 : 1;
+        constexpr int SLOTS = NP * CPT >= 4 ? 1 : 4 / (NP * CPT);
+        const long long per_block = 256LL * SLOTS * CPT;
+        const dim3 grid((unsigned)((work + per_block - 1) / per_block), (unsigned)a.n_q_b);
+        const FastDiv per_row = make_fastdiv((uint32_t)(a.H * (chunks / CPT))), groups = make_fastdiv((uint32_t)(chunks / CPT));
+        return launch_pdl(merge_chunks_kernel<NP, SLOTS, PB, CPT>, grid, dim3(256), 0, st, a, per_row, groups);
+    }
     constexpr int SLOTS = NP >= 4 ? 1 : 4 / NP;
     const long long per_block = 256LL * SLOTS;
     const dim3 grid((unsigned)((work + per_block - 1) / per_block), (unsigned)a.n_q_b);
-    const FastDiv per_row = make_fastdiv((uint32_t)(a.H * (a.D / 8))), chunks = make_fastdiv((uint32_t)(a.D / 8));
-    return launch_pdl(merge_chunks_kernel<NP, SLOTS, PB>, grid, dim3(256), 0, st, a, per_row, chunks);
+    const FastDiv per_row = make_fastdiv((uint32_t)(a.H * chunks)), groups = make_fastdiv((uint32_t)chunks);
+    return launch_pdl(merge_chunks_kernel<NP, SLOTS, PB, 1>, grid, dim3(256), 0, st, a, per_row, groups);
 }
 
 template <int PB>
