@@ -355,7 +355,7 @@ def run_ours(args):
     out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev)
     cfg_out = torch.empty(w.cfg_shape[1:], dtype=synth.torch_dtype(w.cfg_out), device=dev)
     plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev),
-                   exchange=args.exchange)
+                   exchange=args.exchange, ring_merge=args.ring_merge)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -460,7 +460,7 @@ def run_ours(args):
     attn_kernel = f"attn_f32_kernel<{w.D}>" if w.dtype == "f32" else f"attn_tc_kernel<{w.D},false>"
     # merge bytes: R partials (in the plan's partial type) and their LSE per
     # real row and head, the output written once (16-bit)
-    pb = plan.parts.element_size() if w.R > 1 else 4
+    pb = plan.parts.element_size() if plan.parts is not None else 4
     merge_bytes = w.B * w.S * w.H * (w.R * (w.D * pb + 4) + w.D * 2)
 
     # one step alone, launched call by call and replayed from its own CUDA
@@ -482,6 +482,19 @@ def run_ours(args):
     graph_ms = one_step(one.replay)
     eager_ms = one_step(lambda: step(None, False))
     del one
+    other = {}
+    if w.R > 1:
+        # the other form of the ring merge, one step alone (same launches)
+        alt = "partials" if plan.ring_merge == "fold" else "fold"
+        plan2 = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev),
+                        exchange=args.exchange, ring_merge=alt)
+
+        def step2():
+            plan2.run(q, k, v, out)
+            sa.dit_cfg_combine(pred, cfg_out, w.g)
+        step2()
+        other[f"step_{alt}_ms"] = round(one_step(step2), 4)
+        del plan2
 
     # end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(plan, w, q, k, v, pred, out, cfg_out, dev, args)
@@ -489,6 +502,11 @@ def run_ours(args):
                                       **receive_prep_at_scale(dev, flush),
                                       **fp8_wire_at_scale(dev, flush)}
 
+    if "merge_step_f16" in extra.get("back_to_back", {}):
+        # the merge launch alone (40 in a row, inputs out of L2): the step's
+        # split above adds the launch latency its events expose
+        extra["merge_kernel_us"] = extra["back_to_back"]["merge_step_f16"]["us"]
+        extra["merge_kernel_GBs"] = extra["back_to_back"]["merge_step_f16"]["GBs"]
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
         "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_max, 4),
@@ -497,6 +515,7 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V, N(0,1) CFG branches)",
         "config": {**bench_config(w, U),
                    "exchange": plan.exchange,
+                   **({"ring_merge": plan.ring_merge} if w.R > 1 else {}),
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "timing": f"CUDA events around each step; the block of {K} steps repeated {reps} times "
                              f"back to back (>= {args.min_timed_s} s, so the clock samples fall inside); "
@@ -514,7 +533,8 @@ def run_ours(args):
             "layout_in_GBs": round(layout_in_bytes / (statistics.mean(seg[0]) * 1e-3) / 1e9, 1),
             "attention_ms": round(attn_ms, 4), "attention_TFLOPs": round(achieved, 1),
             **({"merge_ms": round(statistics.mean(seg[2]), 4),
-                "merge_GBs": round(merge_bytes / (statistics.mean(seg[2]) * 1e-3) / 1e9, 1)} if w.R > 1 else {}),
+                "merge_GBs": round(merge_bytes / (statistics.mean(seg[2]) * 1e-3) / 1e9, 1)}
+               if plan.parts is not None else {}),
             "layout_out_ms": round(statistics.mean(seg[3]), 4),
             "layout_out_GBs": round(layout_out_bytes / (statistics.mean(seg[3]) * 1e-3) / 1e9, 1),
             "cfg_ms": round(statistics.mean(seg[4]), 4),
@@ -523,6 +543,7 @@ def run_ours(args):
             "step_graph_ms": round(graph_ms, 4),
             "step_eager_ms": round(eager_ms, 4),
             "step_split_ms": round(split_ms, 4),     # the same steps with events between phases
+            **other,
             **extra,
         },
         "e2e": e2e,
@@ -696,6 +717,17 @@ def back_to_back(w, U, dev):
                  torch.randn((R, R, wm.B, wm.H, cap), generator=gen, device=dev),
                  torch.empty((R, wm.B, cap, wm.H, wm.D), dtype=torch.bfloat16, device=dev)),
         lambda x: sa.dit_attn_merge_lse(x[0], x[1], x[2], None, rl), mbytes)
+    # the merge of this workload's own step (f16 partials, bf16 out) when it has one
+    if w.R > 1:
+        Lw = sa.dit_sp_layout_init(w.B, w.S, w.H, w.D, U, w.R)
+        Rw, capw, rlw = w.R, Lw.S_cap, Lw.ring_real
+        res["merge_step_f16"] = timed(
+            Rw * Rw * w.B * capw * w.H * w.D * 2,
+            lambda: (torch.randn((Rw, Rw, w.B, capw, w.H, w.D), generator=gen, device=dev).half(),
+                     torch.randn((Rw, Rw, w.B, w.H, capw), generator=gen, device=dev),
+                     torch.empty((Rw, w.B, capw, w.H, w.D), dtype=torch.bfloat16, device=dev)),
+            lambda x: sa.dit_attn_merge_lse(x[0], x[1], x[2], None, rlw),
+            sum(rlw) * w.B * w.H * (Rw * (w.D * 2 + 4) + w.D * 2))
     # ... and with the step's own f16 partials
     mbytes16 = sum(rl) * wm.B * wm.H * (R * (wm.D * 2 + 4) + wm.D * 2)
     res["merge_flux1008_f16"] = timed(
@@ -842,7 +874,7 @@ def run_sweep(args):
         out = torch.empty((w.B, w.S, w.H, w.D), dtype=q.dtype, device=dev)
         cfg_out = torch.empty(w.cfg_shape[1:], dtype=synth.torch_dtype(w.cfg_out), device=dev)
         plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, in_dtype=synth.torch_dtype(w.dtype), device=str(dev),
-                       exchange=args.exchange)
+                       exchange=args.exchange, ring_merge=args.ring_merge)
         stream = torch.cuda.current_stream(dev)
         reps = 3 if name == "wan" else 10
         seg = [[] for _ in range(5)]
@@ -872,14 +904,15 @@ def run_sweep(args):
         # merge bytes: R partials (O in the plan's partial type, and LSE) of
         # every ring block read, the output written
         rows = w.B * w.S * w.H
-        pb = plan.parts.element_size() if w.R > 1 else 0
-        merge_bytes = rows * (w.R * (w.D * pb + 4) + w.D * plan.o_h.element_size()) if w.R > 1 else 0
+        pb = plan.parts.element_size() if plan.parts is not None else 0
+        merge_bytes = rows * (w.R * (w.D * pb + 4) + w.D * plan.o_h.element_size()) if plan.parts is not None else 0
         res = {"workload": name, "U": U, "R": w.R, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "dtype": w.dtype,
                "step_ms": round(sum(med), 4), "layout_in_ms": round(med[0], 4),
                "attention_ms": round(med[1], 4), "attention_TFLOPs": round(tf, 1),
                "attention_frac_of_measured_peak": round(tf / peaks["bf16_tflops"], 4) if w.dtype != "f32" else None,
                "merge_ms": round(med[2], 4),
-               "merge_GBs": round(merge_bytes / (med[2] * 1e-3) / 1e9, 1) if w.R > 1 else None,
+               "merge_GBs": round(merge_bytes / (med[2] * 1e-3) / 1e9, 1) if plan.parts is not None else None,
+               "ring_merge": plan.ring_merge,
                "attention_plus_merge_TFLOPs": round(tfm, 1),
                "layout_out_ms": round(med[3], 4), "cfg_ms": round(med[4], 4),
                "heads_padded": L.Hp - w.H, "status": int(plan.status.item()),
@@ -1033,6 +1066,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="one line per workload instead of the bench line")
     ap.add_argument("--exchange", choices=("direct", "a2a"), default="direct",
                     help="layout steps in one pass (direct) or as pack / exchange / unpack (a2a)")
+    ap.add_argument("--ring-merge", choices=("fold", "partials"), default="fold", dest="ring_merge",
+                    help="R > 1: key blocks folded in the attention kernel, or partials then the merge kernel")
     ap.add_argument("--min-timed-s", type=float, default=0.5, dest="min_timed_s",
                     help="repeat the K-step block until the timed region lasts this long")
     args = ap.parse_args(argv)

@@ -19,6 +19,8 @@
  *   dit_attn_partial                         attention of query blocks against
  *                                            key/value chunks, with log-sum-exp
  *   dit_attn_merge_lse                       exact merge of the partials
+ *   dit_attn_ring                            the partials of every key block
+ *                                            folded in as the CTA walks them
  *   dit_attention                            single-shot attention
  *   dit_cfg_combine                          classifier-free guidance combine
  *
@@ -432,6 +434,33 @@ DIT_API dit_status dit_attn_partial(int B, int H, int D, float scale,
                             dit_view q, dit_dtype qk_dt, dit_view k, dit_view v,
                             dit_dtype v_dt, dit_view o, dit_dtype o_dt,
                             dit_lse_view lse, int* d_status, void* stream);
+
+/*
+ * dit_attn_ring: ring attention of every query block r < n_q against all its
+ * key/value blocks j < n_kv, folded into one exact result per query block
+ * (SGLang Diffusion "Parallelism Overview", What happens to the shapes and
+ * Constraints: Q stays in place while the K/V chunks of the ring group visit,
+ * and each hop is folded in with the online softmax).  For each batch b,
+ * head h and row i < q_len[r], over every key t < kv_len[j] of every block j:
+ *   o_i   = sum_t softmax_t(scale * <q_i, k_t>) v_t
+ *   lse_i = ln sum_t exp(scale * <q_i, k_t>)
+ * which equals dit_attn_partial followed by dit_attn_merge_lse up to
+ * rounding.  The kernel walks the blocks in order with one running row max,
+ * sum and O accumulator (in TMEM on the tensor-core path), so no partial is
+ * written.  Blocks with kv_len[j] == 0 are skipped; a query block whose every
+ * key block is empty gets o = 0, lse = -inf.
+ *   q, k, v   as for dit_attn_partial
+ *   o         query block r at o.ptr + r*o.stride_q, [B][q_len[r]][H][D]
+ *             (o.stride_kv is ignored)
+ *   lse       row i of (r, b, h) at r*stride_q + b*stride_b + h*stride_h + i
+ *             (stride_kv ignored); lse.ptr may be NULL
+ * Types, head dims, alignment and the output-aliasing rule as for
+ * dit_attn_partial.
+ */
+DIT_API dit_status dit_attn_ring(int B, int H, int D, float scale, int n_q, const int* q_len, int n_kv,
+                                 const int* kv_len, dit_view q, dit_dtype qk_dt, dit_view k, dit_view v,
+                                 dit_dtype v_dt, dit_view o, dit_dtype o_dt, dit_lse_view lse, int* d_status,
+                                 void* stream);
 
 /*
  * dit_attn_varlen: attention of packed variable-length sequences (SGLang

@@ -35,7 +35,7 @@ __all__ = [
     "dit_ulysses_unpack", "dit_attn_partial", "dit_attn_merge_lse", "dit_attention",
     "dit_cfg_combine", "dit_device_status", "library_path", "dit_sp_signal", "dit_a2a_sim_checked",
     "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint", "dit_ulysses_unpack_rope", "dit_attn_varlen",
-    "dit_ulysses_seq_to_head", "dit_ulysses_head_to_seq",
+    "dit_ulysses_seq_to_head", "dit_ulysses_head_to_seq", "dit_attn_ring",
 ]
 
 lib()   # load now: fail at import time, not at first call
@@ -306,6 +306,23 @@ def dit_attn_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch
                                  _lens(kv_len, n_kv, k.shape[2]), _view(q, "q"), _dt(q),
                                  _view(k, "kv"), _view(v, "kv"), _dt(v), _view(o, "o"), _dt(o),
                                  _lse_view(lse, "o"), _ptr(status), _stream(stream)))
+
+
+def dit_attn_ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                  lse: Optional[torch.Tensor] = None, q_len: Optional[Sequence[int]] = None,
+                  kv_len: Optional[Sequence[int]] = None, scale: Optional[float] = None,
+                  status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Every query block against all key/value blocks, folded into one
+    result per query block: q [n_q,B,S,H,D], k/v [n_kv,B,S,H,D],
+    o [n_q,B,S,H,D], lse [n_q,B,H,S] (float32, optional)."""
+    n_q, B, Sq, H, D = q.shape
+    n_kv = k.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    check(lib().dit_attn_ring(B, H, D, float(scale), n_q, _lens(q_len, n_q, Sq), n_kv,
+                              _lens(kv_len, n_kv, k.shape[2]), _view(q, "q"), _dt(q),
+                              _view(k, "kv"), _view(v, "kv"), _dt(v), _view(o, "out"), _dt(o),
+                              _lse_view(lse, "out"), _ptr(status), _stream(stream)))
 
 
 def dit_attn_merge_lse(parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor,

@@ -48,7 +48,7 @@ dit_status validate_and_launch(AttnArgs& a, const char* who, cudaStream_t st) {
     for (int r = 0; r < a.n_q; ++r) maxq = a.q_len[r] > maxq ? a.q_len[r] : maxq;
     const bool alias = (a.H > 1 && a.o.stride_h == 0) || (maxq > 1 && a.o.stride_s == 0) ||
                        (a.B > 1 && a.o.stride_b == 0) || (!a.diag && a.n_q > 1 && a.o.stride_q == 0) ||
-                       (!a.diag && a.n_kv > 1 && a.o.stride_kv == 0);
+                       (!a.diag && !a.fold && a.n_kv > 1 && a.o.stride_kv == 0);
     if (alias) return fail(DIT_ERR_INVALID_ARG, "%s: output view maps two results to one address", who);
     // No query rows: nothing is read or written, so the (empty) buffers may
     // be NULL, as an allocator gives for zero bytes.
@@ -96,6 +96,26 @@ extern "C" dit_status dit_attn_partial(int B, int H, int D, float scale, int n_q
     a.q = q; a.k = k; a.v = v; a.o = o;
     a.qk_dt = qk_dt; a.v_dt = v_dt; a.o_dt = o_dt; a.lse = lse; a.status = d_status;
     return validate_and_launch(a, "dit_attn_partial", (cudaStream_t)stream);
+}
+
+extern "C" dit_status dit_attn_ring(int B, int H, int D, float scale, int n_q, const int* q_len, int n_kv,
+                                    const int* kv_len, dit_view q, dit_dtype qk_dt, dit_view k, dit_view v,
+                                    dit_dtype v_dt, dit_view o, dit_dtype o_dt, dit_lse_view lse, int* d_status,
+                                    void* stream) {
+    NvtxRange nvtx_range("dit_attn_ring");
+    if (!q_len || !kv_len) return fail(DIT_ERR_INVALID_ARG, "dit_attn_ring: NULL length array");
+    if (n_q < 1 || n_q > DIT_MAX_R || n_kv < 1 || n_kv > DIT_MAX_R)
+        return fail(DIT_ERR_INVALID_ARG, "dit_attn_ring: need 1 <= n_q, n_kv <= %d", DIT_MAX_R);
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.B = B; a.H = H; a.D = D; a.n_q = n_q; a.n_kv = n_kv; a.scale = scale; a.fold = 1;
+    for (int r = 0; r < n_q; ++r) a.q_len[r] = q_len[r];
+    for (int r = 0; r < n_kv; ++r) a.kv_len[r] = kv_len[r];
+    o.stride_kv = 0;                  // one result per query block
+    lse.stride_kv = 0;
+    a.q = q; a.k = k; a.v = v; a.o = o;
+    a.qk_dt = qk_dt; a.v_dt = v_dt; a.o_dt = o_dt; a.lse = lse; a.status = d_status;
+    return validate_and_launch(a, "dit_attn_ring", (cudaStream_t)stream);
 }
 
 extern "C" dit_status dit_attention(int B, int H, int D, float scale, int Sq, int Sk, dit_view q, dit_dtype qk_dt,

@@ -21,6 +21,10 @@ struct AttnArgs {
     int q_row0[DIT_MAX_R];
     int kv_row0[DIT_MAX_R];
     int diag;
+    // with fold set, every query block walks all key blocks and folds them
+    // into one result with the online softmax (the ring's per-hop merge): o
+    // and lse have no key-block dimension (their stride_kv is ignored)
+    int fold;
 };
 
 dit_status launch_attn_f32(const AttnArgs& a, cudaStream_t st);

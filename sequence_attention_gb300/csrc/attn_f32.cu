@@ -27,11 +27,13 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const __grid_constant__ A
 
     const int z = blockIdx.z;
     const int b = z % a.B;
-    const int j = a.diag ? z / a.B : (z / a.B) % a.n_kv;
-    const int r = a.diag ? j : z / (a.B * a.n_kv);
+    // folding: z = (r, b) and the CTA walks every key block j in turn with
+    // one running (m, l, acc) -- the ring's per-hop online-softmax merge
+    const int j = a.fold ? 0 : (a.diag ? z / a.B : (z / a.B) % a.n_kv);
+    const int r = a.fold ? z / a.B : (a.diag ? j : z / (a.B * a.n_kv));
     const int h = blockIdx.y;
     const int row0 = blockIdx.x * ROWS;
-    const int qlen = a.q_len[r], kvlen = a.kv_len[j];
+    const int qlen = a.q_len[r];
     if (row0 >= qlen) return;
 
     pdl_wait();
@@ -50,10 +52,13 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const __grid_constant__ A
     }
     float m = -INFINITY, l = 0.f;
 
-    const float* kb = static_cast<const float*>(a.k.ptr) + j * a.k.stride_kv + b * a.k.stride_b + h * a.k.stride_h +
-                      (long long)a.kv_row0[j] * a.k.stride_s;
-    const float* vb = static_cast<const float*>(a.v.ptr) + j * a.v.stride_kv + b * a.v.stride_b + h * a.v.stride_h +
-                      (long long)a.kv_row0[j] * a.v.stride_s;
+    const int j_end = a.fold ? a.n_kv : j + 1;
+    for (int jb = j; jb < j_end; ++jb) {
+    const int kvlen = a.kv_len[jb];
+    const float* kb = static_cast<const float*>(a.k.ptr) + jb * a.k.stride_kv + b * a.k.stride_b + h * a.k.stride_h +
+                      (long long)a.kv_row0[jb] * a.k.stride_s;
+    const float* vb = static_cast<const float*>(a.v.ptr) + jb * a.v.stride_kv + b * a.v.stride_b + h * a.v.stride_h +
+                      (long long)a.kv_row0[jb] * a.v.stride_s;
 
     for (int kt = 0; kt < kvlen; kt += KT) {
         __syncthreads();
@@ -94,11 +99,12 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const __grid_constant__ A
         }
         m = mnew;
     }
+    }
     if (!valid) {
         pdl_trigger();
         return;
     }
-    const float inv = kvlen > 0 ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? 1.f / l : 0.f;          // l >= 1 once any key was seen
     float* op = static_cast<float*>(a.o.ptr) + r * a.o.stride_q + j * a.o.stride_kv + b * a.o.stride_b +
                 ((long long)a.q_row0[r] + i) * a.o.stride_s + h * a.o.stride_h + part * DT;
 #pragma unroll
@@ -106,7 +112,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const __grid_constant__ A
         *reinterpret_cast<float4*>(op + d) = make_float4(acc[d] * inv, acc[d + 1] * inv, acc[d + 2] * inv, acc[d + 3] * inv);
     if (a.lse.ptr && part == 0)
         a.lse.ptr[r * a.lse.stride_q + j * a.lse.stride_kv + b * a.lse.stride_b + h * a.lse.stride_h + a.q_row0[r] + i] =
-            kvlen > 0 ? m + logf(l) : -INFINITY;
+            l > 0.f ? m + logf(l) : -INFINITY;
     pdl_trigger();
 }
 
@@ -117,7 +123,7 @@ dit_status launch_attn_f32(const AttnArgs& a, cudaStream_t st) {
     for (int r = 0; r < a.n_q; ++r) maxq = a.q_len[r] > maxq ? a.q_len[r] : maxq;
     if (maxq == 0) return DIT_OK;
     const int rows = a.D == 128 ? 64 : 128;
-    dim3 grid((maxq + rows - 1) / rows, a.H, (a.diag ? a.n_q : a.n_q * a.n_kv) * a.B);
+    dim3 grid((maxq + rows - 1) / rows, a.H, ((a.diag || a.fold) ? a.n_q : a.n_q * a.n_kv) * a.B);
     if (grid.y > 65535 || grid.z > 65535) return fail(DIT_ERR_UNSUPPORTED, "attention: grid too large");
     cudaError_t e;
     switch (a.D) {

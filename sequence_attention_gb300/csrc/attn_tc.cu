@@ -79,6 +79,7 @@ struct TcParams {
     int q_row0[DIT_MAX_R];          // first output row of query block r (packed sequences)
     int B, n_q, n_kv;
     int diag;                       // query block r attends key block r only
+    int fold;                       // one output per query block: the key blocks folded by the online softmax
     int nsm;                        // SMs of the device (CTAs in flight: one per SM)
     float c;                      // scale * log2(e)
     uint32_t idesc_qk, idesc_pv;
@@ -433,8 +434,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t St, uint32_t Ot, int valid
 // drains once per CTA instead of once per block.  The V ring has 2 stages;
 // the freed tile holds one output staging slot per softmax warp, since the
 // Q, K and V buffers stay in use until the last block.
-template <int D, bool P_BF16, bool DIAG>
+template <int D, bool P_BF16, bool DIAG, bool FOLD>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
+    static_assert(!(DIAG && FOLD), "folding walks every key block");
     constexpr int NCH = D / 64;          // 128-byte chunks per row
     constexpr int TILE = BM * D * 2;     // bytes of one Q, K or V tile
     constexpr int NSV = kNSV;
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
     for (int jj = 0; jj < nj; ++jj) any_keys |= p.kv_len[cta.j + jj] > 0;
     if (!any_keys) {     // every key block empty: O = 0, lse = -inf
         pdl_wait();
-        for (int jj = 0; jj < nj; ++jj) write_empty_partial<D>(p, r, cta.j + jj, b, h, row_base);
+        for (int jj = 0; jj < (FOLD ? 1 : nj); ++jj) write_empty_partial<D>(p, r, cta.j + jj, b, h, row_base);
         return;
     }
 
@@ -600,17 +602,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 if (!(ok = wait_phase(bar(B_VF + sv), (gv / NSV) & 1, ctl))) break;
                 if (!(ok = wait_phase(bar(B_PF + 0), gs & 1, ctl))) break;
                 tc_fence_after();
-                issue_pv(0, sv, n > 0);
+                // folding, P V accumulates across the key blocks: only the
+                // very first position starts O afresh
+                issue_pv(0, sv, FOLD ? gs > 0 : n > 0);
                 const bool last = n + 1 == nt;
-                // block done for tile 0: its epilogue overlaps tile 1's last
-                // P V (and, walking, the next block's first Q K^T)
-                if (last) tc_commit(bar(B_OD + 0));
                 int jn = jj, nn = n + 1;
                 if (last) {
                     nn = 0;
                     do ++jn; while (jn < nj && tiles_of(jn) == 0);
                 }
                 const bool more = jn < nj;
+                // output done for tile 0 (the block's partial; folding, the
+                // whole walk): its epilogue overlaps tile 1's last P V (and,
+                // walking, the next block's first Q K^T)
+                const bool done = last && (!FOLD || !more);
+                if (done) tc_commit(bar(B_OD + 0));
                 const int sk = (int)(gk % NSK);
                 if (more) {
                     if (!(ok = wait_phase(bar(B_KF + sk), (gk / NSK) & 1, ctl))) break;
@@ -620,10 +626,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 }
                 if (!(ok = wait_phase(bar(B_PF + 1), gs & 1, ctl))) break;
                 tc_fence_after();
-                issue_pv(1, sv, n > 0);
+                issue_pv(1, sv, FOLD ? gs > 0 : n > 0);
                 tc_commit(bar(B_VE + sv));
                 ++gv;
-                if (last) tc_commit(bar(B_OD + 1));
+                if (done) tc_commit(bar(B_OD + 1));
                 ++gs;
                 if (!more) break;
                 issue_qk(1, sk);
@@ -648,25 +654,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         const float c = p.c;
         bool ok = true;
         // one register of loop state: bit 0 the S/P phase (per key tile),
-        // bit 1 the O-done phase (per block), bits 8.. the key block
+        // bit 1 the O-done phase (per block), bit 2 a key tile seen (folding),
+        // bits 8.. the key block
         uint32_t st = 0;
+        float m_used = 0.f, l = 0.f;          // folding: carried across the key blocks
         for (; (int)(st >> 8) < nj && ok; st += 256u) {
             int rem = p.kv_len[(DIAG ? cta_coords<DIAG>(p).j : 0) + (int)(st >> 8)];   // keys not yet seen
             if (rem == 0) {
-                const Cta e = cta_coords<DIAG>(p);
-                write_empty_partial<D>(p, e.r, e.j + (int)(st >> 8), e.b, e.h, e.row_base);
+                if (!FOLD) {
+                    const Cta e = cta_coords<DIAG>(p);
+                    write_empty_partial<D>(p, e.r, e.j + (int)(st >> 8), e.b, e.h, e.row_base);
+                }
                 continue;
             }
-            float m_used = 0.f, l = 0.f;
+            if (!FOLD) m_used = l = 0.f;
             for (int n = 0; rem > 0; ++n, rem -= BN) {
                 ok = __all_sync(0xffffffffu, wait_phase(bar(B_SF + t), st & 1, ctl));
                 if (!ok) break;
                 tc_fence_after();
-                softmax_tile<D, P_BF16>(St, Ot, rem, n == 0, c, m_used, l);
+                softmax_tile<D, P_BF16>(St, Ot, rem, FOLD ? !(st & 4u) : n == 0, c, m_used, l);
                 mbar_arrive(bar(B_PF + t));
                 st ^= 1u;
+                st |= 4u;
             }
             if (!ok) break;
+            if (FOLD) {
+                // the walk goes on into a later block with keys: no output yet
+                bool later = false;
+                for (int jj = (int)(st >> 8) + 1; jj < nj; ++jj) later |= p.kv_len[jj] > 0;
+                if (later) continue;
+            }
             // epilogue of block j: O / l and lse = ln(2) * (m + log2 l).  This
             // tile's "O done" barrier; the tile index is re-read from %tid
             // (volatile) and the address recomputed from the array's own
@@ -685,7 +702,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             const float inv = 1.f / l;
             const Cta e = cta_coords<DIAG>(p);
             const int j = e.j + (int)(st >> 8);
-            const int jc = DIAG ? 0 : j;                // the output map's key-block coordinate
+            const int jc = (DIAG || FOLD) ? 0 : j;     // the output map's key-block coordinate
             const int eb = dtype_bytes(p.o_dt);
             const int rt = (int)(tid_now & 127);      // row within the tile
             const int row = e.row_base + te * BM + rt;
@@ -843,7 +860,8 @@ template <int D, bool PB>
 dit_status launch_kernel(const TcParams& prm, dim3 grid, cudaStream_t st) {
     int smem = smem_bytes<D>();
     if (smem < 116 * 1024) smem = 116 * 1024;   // one CTA per SM: it owns all 512 TMEM columns
-    auto kernel = prm.diag ? attn_tc_kernel<D, PB, true> : attn_tc_kernel<D, PB, false>;
+    auto kernel = prm.diag ? attn_tc_kernel<D, PB, true, false>
+                           : (prm.fold ? attn_tc_kernel<D, PB, false, true> : attn_tc_kernel<D, PB, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "attention: %s", cudaGetErrorString(e));
     e = launch_pdl(kernel, grid, dim3(NTHREADS), (size_t)smem, st, prm);
@@ -873,7 +891,7 @@ dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
             char* ob = static_cast<char*>(a.o.ptr) +
                        (r * a.o.stride_q + (a.diag ? r * a.o.stride_kv : 0) + (int64_t)a.q_row0[r] * a.o.stride_s) *
                            dtype_bytes(a.o_dt);
-            s = make_omap(enc, &prm->omap[r], ob, a.o_dt, a.D, a.H, a.q_len[r], a.B, a.diag ? 1 : a.n_kv,
+            s = make_omap(enc, &prm->omap[r], ob, a.o_dt, a.D, a.H, a.q_len[r], a.B, (a.diag || a.fold) ? 1 : a.n_kv,
                           a.o.stride_h, a.o.stride_s, a.o.stride_b, a.o.stride_kv);
         }
     }
@@ -888,7 +906,7 @@ dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
                          a.v.stride_b);
     }
     if (s == DIT_OK && maxq > 0) {
-        prm->B = a.B; prm->n_q = a.n_q; prm->n_kv = a.n_kv; prm->diag = a.diag; prm->nsm = num_sms();
+        prm->B = a.B; prm->n_q = a.n_q; prm->n_kv = a.n_kv; prm->diag = a.diag; prm->fold = a.fold; prm->nsm = num_sms();
 
         prm->c = a.scale * 1.4426950408889634f;
         prm->idesc_qk = make_idesc(a.qk_dt == DIT_BF16, false, BN, BM);

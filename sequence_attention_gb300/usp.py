@@ -7,8 +7,12 @@ redistributed data, then the inverse all-to-all; SGLang Diffusion
 "Parallelism Overview", What happens to the shapes):
 
   layout in    seq-sharded Q,K,V -> head layout [R,B,S_cap,Hp,D] (V as f16)
-  dit_attn_partial        every (ring block r, ring block j) partial, one launch
-  dit_attn_merge_lse      R partials -> exact output (skipped when R = 1)
+  attention    every ring block r against every ring block j, one launch:
+               ring_merge="fold" (default) dit_attn_ring, each hop folded in
+               by the online softmax as the kernel walks the K/V blocks;
+               ring_merge="partials" dit_attn_partial (every (r, j)
+               partial) then dit_attn_merge_lse (the R-way log-sum-exp
+               merge), the form whose partials could come from other GPUs
   layout out   head layout -> seq-sharded output [B,S,H,D]
 
 The layout steps run one of two ways (``exchange``):
@@ -36,6 +40,7 @@ from typing import Optional, Sequence, Tuple
 import torch
 
 from . import (DIT_HEAD_TO_SEQ, DIT_SEQ_TO_HEAD, DitError, dit_a2a_sim, dit_attn_merge_lse, dit_attn_partial,
+               dit_attn_ring,
                dit_sp_layout_init, dit_ulysses_head_to_seq, dit_ulysses_pack, dit_ulysses_pack_joint,
                dit_ulysses_seq_to_head, dit_ulysses_unpack, dit_ulysses_unpack_joint, dit_ulysses_unpack_rope)
 from ._lib import DIT_ERR_RANGE, DIT_ERR_TIMEOUT
@@ -50,7 +55,8 @@ class UspPlan:
                  rope: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
                  fp8_qv: bool = False, fp8_o: bool = False,
                  pad_heads: bool = True, pad_lcm64: bool = False,
-                 parts_dtype: Optional[torch.dtype] = None, exchange: Optional[str] = None):
+                 parts_dtype: Optional[torch.dtype] = None, exchange: Optional[str] = None,
+                 ring_merge: str = "fold"):
         """rope: optional (cos, sin) float32 [S, D/2] device tables of the
         joint sequence; Q and K are then rotated by the receive preparation.
         fp8_qv / fp8_o: Q and V (one exchange) / the output cross the
@@ -64,6 +70,9 @@ class UspPlan:
         11 significant bits against the output's 8 (bf16), at half the
         bytes of f32 for the attention's stores and the merge's loads.
         Otherwise f32.
+        ring_merge: "fold" (the K/V blocks folded into one result as the
+        kernel walks them) or "partials" (every partial written, then the
+        R-way merge kernel); the same result up to rounding.
         exchange: "direct" (one pass per layout step) or "a2a" (pack,
         exchange, unpack); default "direct", or "a2a" with an e4m3 wire.
         v_dtype: by default f16 for bf16 inputs (P V runs with P in V's type,
@@ -115,7 +124,10 @@ class UspPlan:
         if parts_dtype == torch.float16 and v_dtype != torch.float16:
             raise ValueError("f16 partials need f16 V (a partial lies within V's range)")
         self.parts_dtype = parts_dtype
-        if R > 1:
+        if ring_merge not in ("fold", "partials"):
+            raise ValueError(f"ring_merge must be 'fold' or 'partials', got {ring_merge!r}")
+        self.ring_merge = ring_merge
+        if R > 1 and ring_merge == "partials":
             self.parts = torch.empty((R, R) + tuple(hs[1:]), dtype=parts_dtype, device=dev)
             self.lse_parts = torch.empty((R, R, B, L.Hp, L.S_cap), dtype=torch.float32, device=dev)
         else:
@@ -171,9 +183,12 @@ class UspPlan:
             s = ["pack_s2h_k", "pack_s2h_qv", "a2a_s2h_k", "a2a_s2h_qv", "unpack_s2h_k", "unpack_s2h_qv"]
         else:
             s = ["pack_s2h", "a2a_s2h", "unpack_s2h"]
-        s = s + ["attn_partial"]
-        if self.R > 1:
-            s.append("merge")
+        if self.R > 1 and self.ring_merge == "fold":
+            s = s + ["attn_ring"]
+        else:
+            s = s + ["attn_partial"]
+            if self.R > 1:
+                s.append("merge")
         return s + (["head_to_seq"] if self.exchange == "direct" else ["pack_h2s", "a2a_h2s", "unpack_h2s"])
 
     def _unpack(self, recv, heads, rope_mask, stream):
@@ -225,21 +240,26 @@ class UspPlan:
         self._receive(stream)
 
     def partials(self, stream=None):
-        """Every (ring block r, ring block j) partial in one launch; with
-        R = 1 the single partial is the output itself."""
+        """The attention of every ring block against every ring block in one
+        launch: folded into the output (ring_merge="fold"), or every (r, j)
+        partial written for merge(); with R = 1 the single partial is the
+        output itself."""
         rl = self.ring_len
         qv, kv, vv = self.heads(self.q_h), self.heads(self.k_h), self.heads(self.v_h)
         if self.R == 1:
             o = self.heads(self.o_h).unsqueeze(1)        # [1, 1, B, S, H, D]
             dit_attn_partial(qv, kv, vv, o, None, rl, rl, self.scale, self.status, stream)
+        elif self.ring_merge == "fold":
+            dit_attn_ring(qv, kv, vv, self.heads(self.o_h), None, rl, rl, self.scale, self.status, stream)
         else:
             dit_attn_partial(qv, kv, vv, self.heads(self.parts),
                              self.lse_parts[:, :, :, : self.H, :], rl, rl, self.scale,
                              self.status, stream)
 
     def merge(self, stream=None):
-        """The ring's log-sum-exp merge of the R partials (nothing when R = 1)."""
-        if self.R > 1:
+        """The ring's log-sum-exp merge of the R partials (nothing when R = 1
+        or when the attention folded the blocks itself)."""
+        if self.R > 1 and self.ring_merge == "partials":
             dit_attn_merge_lse(self.heads(self.parts), self.lse_parts[:, :, :, : self.H, :],
                                self.heads(self.o_h), None, self.ring_len, stream)
 

@@ -400,9 +400,18 @@ def test_plan_partial_type(dl):
     refused.  Plans are built on the host here: nothing is launched."""
     import torch
     from sequence_attention_gb300.usp import UspPlan
-    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu").parts.dtype == torch.float16
-    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", out_dtype=torch.float32).parts.dtype == torch.float32
-    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", v_dtype=torch.bfloat16).parts.dtype == torch.float32
-    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", parts_dtype=torch.float32).parts.dtype == torch.float32
+    rm = {"ring_merge": "partials"}
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", **rm).parts.dtype == torch.float16
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", out_dtype=torch.float32, **rm).parts.dtype == torch.float32
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", v_dtype=torch.bfloat16, **rm).parts.dtype == torch.float32
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", parts_dtype=torch.float32, **rm).parts.dtype == torch.float32
     with pytest.raises(ValueError):
         UspPlan(1, 64, 2, 64, 2, 2, device="cpu", v_dtype=torch.bfloat16, parts_dtype=torch.float16)
+    # folding the ring blocks in the attention needs no partial buffers
+    fold = UspPlan(1, 64, 2, 64, 2, 2, device="cpu")
+    assert fold.ring_merge == "fold" and fold.parts is None and fold.lse_parts is None
+    assert fold.steps() == ["seq_to_head", "attn_ring", "head_to_seq"]
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", **rm).steps() == ["seq_to_head", "attn_partial", "merge",
+                                                                        "head_to_seq"]
+    with pytest.raises(ValueError):
+        UspPlan(1, 64, 2, 64, 2, 2, device="cpu", ring_merge="tree")

@@ -1,0 +1,150 @@
+"""GPU parity of the folded ring attention (dit_attn_ring) against the oracle.
+
+Each query block attends every key/value block of the ring in turn and the
+kernel folds each block into one running result with the online softmax
+(SGLang Diffusion "Parallelism Overview", What happens to the shapes and
+Constraints: Q stays while the K/V chunks visit, each hop merged by the
+online softmax).  The result must be the oracle's attention over the
+concatenated valid keys of all blocks: the tensor-core path at the bf16 bars
+(max-abs 2e-2, rel-RMS 5e-3; log-sum-exp within 1e-4), the fp32 path within
+1e-5, and against the device's own partials + R-way merge within the merge
+bar (1e-3 rel-RMS, fp32 outputs).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import attention as oatt
+from tests.helpers import F32_MAX_ABS, LSE_ABS, MERGE_REL_RMS, assert_bf16_close, f64, max_abs, rel_rms
+
+pytestmark = pytest.mark.gpu
+
+
+def _blocks(x, lens, cap):
+    """[B, sum(lens), H, D] -> [n, B, cap, H, D] blocks, NaN past each length."""
+    B, _, H, D = x.shape
+    out = torch.full((len(lens), B, cap, H, D), float("nan"), dtype=x.dtype)
+    off = 0
+    for j, L in enumerate(lens):
+        out[j, :, :L] = x[:, off:off + L]
+        off += L
+    return out
+
+
+def _ring(q, k, v, q_lens, kv_lens, v_dt, o_dt, Hs, with_lse=True):
+    """Run dit_attn_ring on padded block tensors with Hs >= H storage heads;
+    returns (o [n_q, B, cap, Hs, D] on the host, lse or None)."""
+    import sequence_attention_gb300 as sa
+    B, _, H, D = q.shape
+    cq, ck = max(max(q_lens), 1), max(max(kv_lens), 1)
+    qb, kb, vb = _blocks(q, q_lens, cq), _blocks(k, kv_lens, ck), _blocks(v.to(v_dt), kv_lens, ck)
+    def store(x):
+        full = torch.zeros(x.shape[:3] + (Hs, D), dtype=x.dtype)
+        full[..., :H, :] = x
+        return full.cuda()
+    qd, kd, vd = store(qb), store(kb), store(vb)
+    o = torch.full((len(q_lens), B, cq, Hs, D), float("nan"), dtype=o_dt, device="cuda")
+    lse = torch.full((len(q_lens), B, Hs, cq), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sa.dit_attn_ring(qd[..., :H, :], kd[..., :H, :], vd[..., :H, :], o[..., :H, :],
+                     None if lse is None else lse[:, :, :H, :], q_lens, kv_lens, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return o.cpu(), (None if lse is None else lse.cpu())
+
+
+CASES = [
+    # B, H, D, q block lengths, key block lengths
+    (1, 2, 128, [300], [200, 133]),
+    (2, 3, 128, [190, 190], [128, 0, 77]),              # an empty middle block
+    (1, 1, 128, [2241, 2240], [2241, 2240]),            # FLUX-1008's ring blocks, one head
+    (1, 2, 64, [640, 5], [1000, 1000, 1000, 997]),      # D = 64, four blocks, a 5-row query block
+    (1, 1, 128, [129], [1, 0, 0, 127]),                  # one-key block, empty blocks
+    (2, 2, 128, [257], [8300, 100]),                     # a long 65-tile block
+    (1, 2, 128, [100], [0, 0]),                          # every key block empty
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("v_dt,o_dt", [(torch.float16, torch.bfloat16), (torch.float16, torch.float32),
+                                       (torch.bfloat16, torch.float16)])
+def test_ring_matches_oracle(case, v_dt, o_dt):
+    B, H, D, q_lens, kv_lens = case
+    Sq, Sk = sum(q_lens), sum(kv_lens)
+    q = synth.normal((B, Sq, H, D), 90, 0.5, "bf16")
+    k = synth.normal((B, max(Sk, 1), H, D), 91, 0.5, "bf16")[:, :Sk]
+    v = synth.normal((B, max(Sk, 1), H, D), 92, 0.5, "bf16")[:, :Sk]
+    Hs = H + 1                                           # one padded head the kernel must not touch
+    o, lse = _ring(q, k, v, q_lens, kv_lens, v_dt, o_dt, Hs)
+    vq = v.to(v_dt)
+    o_ref, l_ref = oatt.attention(f64(q), f64(k), f64(vq))
+    off = 0
+    for r, L in enumerate(q_lens):
+        got = f64(o[r, :, :L, :H])
+        if Sk == 0:
+            assert np.all(got == 0) and np.all(np.isneginf(f64(lse[r, :, :H, :L])))
+        else:
+            assert_bf16_close(got, o_ref[:, off:off + L], f"query block {r}")
+            assert max_abs(f64(lse[r, :, :H, :L]), l_ref[:, :, off:off + L]) <= LSE_ABS
+        # rows past the block and the padded head are never written
+        assert torch.isnan(o[r, :, L:].float()).all() and torch.isnan(o[r, ..., H:, :].float()).all()
+        assert torch.isnan(lse[r, :, H:]).all() and torch.isnan(lse[r, :, :, L:]).all()
+        off += L
+
+
+@pytest.mark.parametrize("case", CASES[:4])
+def test_ring_fp32_path(case):
+    B, H, D, q_lens, kv_lens = case
+    D = 64 if D == 128 else D
+    Sq, Sk = sum(q_lens), sum(kv_lens)
+    q = synth.normal((B, Sq, H, D), 93, 1.0, "f32")
+    k = synth.normal((B, Sk, H, D), 94, 1.0, "f32")
+    v = synth.normal((B, Sk, H, D), 95, 1.0, "f32")
+    o, lse = _ring(q, k, v, q_lens, kv_lens, torch.float32, torch.float32, H)
+    o_ref, l_ref = oatt.attention(f64(q), f64(k), f64(v))
+    off = 0
+    for r, L in enumerate(q_lens):
+        assert max_abs(f64(o[r, :, :L]), o_ref[:, off:off + L]) <= F32_MAX_ABS
+        assert max_abs(f64(lse[r, :, :, :L]), l_ref[:, :, off:off + L]) <= F32_MAX_ABS
+        off += L
+
+
+def test_ring_equals_partials_and_merge_on_device():
+    """Folding in the kernel and merging written partials agree within the
+    merge bar (FLUX-1008-like R = 2 ring blocks, all 24 heads, fp32 outputs)."""
+    import sequence_attention_gb300 as sa
+    w = synth.WORKLOADS["flux1008"]
+    L = sa.dit_sp_layout_init(w.B, w.S, w.H, w.D, 1, w.R)
+    q, k, v = w.qkv()
+    rl, cap = L.ring_real, L.S_cap
+    qb = _blocks(q, rl, cap).cuda()
+    kb = _blocks(k, rl, cap).cuda()
+    vb = _blocks(v.to(torch.float16), rl, cap).cuda()
+    ring = torch.empty((w.R, w.B, cap, w.H, w.D), dtype=torch.float32, device="cuda")
+    sa.dit_attn_ring(qb, kb, vb, ring, None, rl, rl)
+    parts = torch.empty((w.R, w.R, w.B, cap, w.H, w.D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((w.R, w.R, w.B, w.H, cap), dtype=torch.float32, device="cuda")
+    sa.dit_attn_partial(qb, kb, vb, parts, lse, rl, rl)
+    merged = torch.empty_like(ring)
+    sa.dit_attn_merge_lse(parts, lse, merged, None, rl)
+    torch.cuda.synchronize()
+    for r in range(w.R):
+        n = rl[r]
+        assert rel_rms(f64(ring[r, :, :n]), f64(merged[r, :, :n])) <= MERGE_REL_RMS
+
+
+def test_ring_argument_checks():
+    import sequence_attention_gb300 as sa
+    q = torch.zeros((2, 1, 64, 2, 128), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros((2, 1, 64, 2, 128), dtype=torch.float16, device="cuda")
+    o = torch.zeros((2, 1, 64, 2, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sa.DitError):
+        sa.dit_attn_ring(q, q, v, o, None, [64, 64], [64, 64], scale=-1.0)       # scale must be positive
+    with pytest.raises(sa.DitError):
+        sa.dit_attn_ring(q, q, v, o, None, [64, -1], [64, 64])                   # negative length
+    with pytest.raises(sa.DitError):
+        sa.dit_attn_ring(q, q, v, o.expand(2, 1, 64, 2, 128).as_strided(o.shape, (0,) + o.stride()[1:]), None,
+                         [64, 64], [64, 64])                                       # two blocks on one address
