@@ -672,12 +672,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 ok = __all_sync(0xffffffffu, wait_phase(bar(B_SF + t), st & 1, ctl));
                 if (!ok) break;
                 tc_fence_after();
-                softmax_tile<D, P_BF16>(St, Ot, rem, FOLD ? !(st & 4u) : n == 0, c, m_used, l);
+                softmax_tile<D, P_BF16>(St, Ot, rem, n == 0 && !(st & 4u), c, m_used, l);
                 mbar_arrive(bar(B_PF + t));
                 st ^= 1u;
-                st |= 4u;
             }
             if (!ok) break;
+            if (FOLD) st |= 4u;           // later blocks continue the running max and sum
             if (FOLD) {
                 // the walk goes on into a later block with keys: no output yet
                 bool later = false;

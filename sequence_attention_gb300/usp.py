@@ -8,7 +8,7 @@ redistributed data, then the inverse all-to-all; SGLang Diffusion
 
   layout in    seq-sharded Q,K,V -> head layout [R,B,S_cap,Hp,D] (V as f16)
   attention    every ring block r against every ring block j, one launch:
-               ring_merge="fold" (default) dit_attn_ring, each hop folded in
+               ring_merge="fold" (default up to R = 2) dit_attn_ring, each hop folded in
                by the online softmax as the kernel walks the K/V blocks;
                ring_merge="partials" dit_attn_partial (every (r, j)
                partial) then dit_attn_merge_lse (the R-way log-sum-exp
@@ -56,7 +56,7 @@ class UspPlan:
                  fp8_qv: bool = False, fp8_o: bool = False,
                  pad_heads: bool = True, pad_lcm64: bool = False,
                  parts_dtype: Optional[torch.dtype] = None, exchange: Optional[str] = None,
-                 ring_merge: str = "fold"):
+                 ring_merge: Optional[str] = None):
         """rope: optional (cos, sin) float32 [S, D/2] device tables of the
         joint sequence; Q and K are then rotated by the receive preparation.
         fp8_qv / fp8_o: Q and V (one exchange) / the output cross the
@@ -72,7 +72,12 @@ class UspPlan:
         Otherwise f32.
         ring_merge: "fold" (the K/V blocks folded into one result as the
         kernel walks them) or "partials" (every partial written, then the
-        R-way merge kernel); the same result up to rounding.
+        R-way merge kernel); the same result up to rounding.  By default
+        "fold" for R <= 2 and "partials" above: measured on one GB300, the
+        fold saves the merge pass (FLUX-1008-like R = 2: 0.256 against 0.270
+        ms per step; Qwen-like 1.06 against 1.09), but its walk over many long
+        blocks ran ~1.7 % slower than the partial kernel's (Wan-like R = 4:
+        80.3 against 78.9 ms of attention), more than the 0.55 ms merge.
         exchange: "direct" (one pass per layout step) or "a2a" (pack,
         exchange, unpack); default "direct", or "a2a" with an e4m3 wire.
         v_dtype: by default f16 for bf16 inputs (P V runs with P in V's type,
@@ -124,6 +129,8 @@ class UspPlan:
         if parts_dtype == torch.float16 and v_dtype != torch.float16:
             raise ValueError("f16 partials need f16 V (a partial lies within V's range)")
         self.parts_dtype = parts_dtype
+        if ring_merge is None:
+            ring_merge = "fold" if R <= 2 else "partials"
         if ring_merge not in ("fold", "partials"):
             raise ValueError(f"ring_merge must be 'fold' or 'partials', got {ring_merge!r}")
         self.ring_merge = ring_merge

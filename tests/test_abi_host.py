@@ -415,3 +415,5 @@ def test_plan_partial_type(dl):
                                                                         "head_to_seq"]
     with pytest.raises(ValueError):
         UspPlan(1, 64, 2, 64, 2, 2, device="cpu", ring_merge="tree")
+    # the default: fold up to two ring blocks, partials and the merge beyond
+    assert UspPlan(1, 64, 2, 64, 2, 4, device="cpu").ring_merge == "partials"

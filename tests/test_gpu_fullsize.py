@@ -50,13 +50,13 @@ def _oracle_attention(name):
     return _ORACLE[name]
 
 
-@pytest.mark.parametrize("exchange", ["direct", "a2a"])
+@pytest.mark.parametrize("exchange,ring_merge", [("direct", "fold"), ("a2a", "partials")])
 @pytest.mark.parametrize("name,U", [("flux1024", 2), ("flux1024", 4), ("flux1008", 4), ("flux1008_4480", 4)])
-def test_every_row_against_the_full_oracle(name, U, exchange):
+def test_every_row_against_the_full_oracle(name, U, exchange, ring_merge):
     from sequence_attention_gb300.usp import UspPlan
     w = synth.WORKLOADS[name]
     q, k, v = w.qkv()
-    plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, exchange=exchange)
+    plan = UspPlan(w.B, w.S, w.H, w.D, U, w.R, exchange=exchange, ring_merge=ring_merge)
     out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device="cuda")
     plan.run(q.cuda(), k.cuda(), v.cuda(), out, check=True)
     assert_bf16_close(f64(out), _oracle_attention(name), f"{name} U={U} {exchange}")

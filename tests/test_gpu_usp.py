@@ -75,14 +75,15 @@ def test_medium_bf16_full(B, S, H, U, R, exchange):
 
 # FLUX-1024 and FLUX-1008 are compared on every row in test_gpu_fullsize.py;
 # the two larger workloads on their seams plus seeded random rows.
-FULL = [("qwen1328", 5, "direct"), ("qwen1328", 5, "a2a"), ("wan", 8, "direct")]
+FULL = [("qwen1328", 5, "direct", "fold"), ("qwen1328", 5, "a2a", "partials"), ("wan", 8, "direct", "partials"),
+        ("wan", 8, "direct", "fold")]
 
 
-@pytest.mark.parametrize("name,U,exchange", FULL)
-def test_full_size_sampled(name, U, exchange):
+@pytest.mark.parametrize("name,U,exchange,ring_merge", FULL)
+def test_full_size_sampled(name, U, exchange, ring_merge):
     w = synth.WORKLOADS[name]
     q, k, v = w.qkv()
-    plan = _plan(w, U, exchange=exchange)
+    plan = _plan(w, U, exchange=exchange, ring_merge=ring_merge)
     out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device="cuda")
     plan.run(q.cuda(), k.cuda(), v.cuda(), out)
     torch.cuda.synchronize()
