@@ -73,7 +73,8 @@ class UspPlan:
         ring_merge: "fold" (the K/V blocks folded into one result as the
         kernel walks them) or "partials" (every partial written, then the
         R-way merge kernel); the same result up to rounding.  By default
-        "fold" for R <= 2 and "partials" above: measured on one GB300, the
+        "fold" for R <= 2 on 16-bit inputs and "partials" otherwise:
+        measured on one GB300, the
         fold saves the merge pass (FLUX-1008-like R = 2: 0.256 against 0.270
         ms per step; Qwen-like 1.06 against 1.09), but its walk over many long
         blocks ran ~1.7 % slower than the partial kernel's (Wan-like R = 4:
@@ -130,7 +131,10 @@ class UspPlan:
             raise ValueError("f16 partials need f16 V (a partial lies within V's range)")
         self.parts_dtype = parts_dtype
         if ring_merge is None:
-            ring_merge = "fold" if R <= 2 else "partials"
+            # the fp32 CUDA-core kernel folds with one CTA per query block
+            # and row tile, half the CTAs of its partials (tiny: 0.116
+            # against 0.106 ms per step)
+            ring_merge = "fold" if R <= 2 and in_dtype != torch.float32 else "partials"
         if ring_merge not in ("fold", "partials"):
             raise ValueError(f"ring_merge must be 'fold' or 'partials', got {ring_merge!r}")
         self.ring_merge = ring_merge

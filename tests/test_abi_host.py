@@ -417,3 +417,4 @@ def test_plan_partial_type(dl):
         UspPlan(1, 64, 2, 64, 2, 2, device="cpu", ring_merge="tree")
     # the default: fold up to two ring blocks, partials and the merge beyond
     assert UspPlan(1, 64, 2, 64, 2, 4, device="cpu").ring_merge == "partials"
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", in_dtype=torch.float32).ring_merge == "partials"
