@@ -1068,7 +1068,7 @@ def main(argv=None):
                     help="layout steps in one pass (direct) or as pack / exchange / unpack (a2a)")
     ap.add_argument("--ring-merge", choices=("fold", "partials"), default=None, dest="ring_merge",
                     help="R > 1: key blocks folded in the attention kernel, or partials then the merge kernel "
-                         "(default: the plan's choice, fold up to R = 2)")
+                         "(default: the plan's choice, fold on 16-bit inputs)")
     ap.add_argument("--min-timed-s", type=float, default=0.5, dest="min_timed_s",
                     help="repeat the K-step block until the timed region lasts this long")
     args = ap.parse_args(argv)

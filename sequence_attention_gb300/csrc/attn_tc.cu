@@ -67,7 +67,11 @@ constexpr int NTHREADS = 384;
 constexpr int CHUNK = BM * 128;  // bytes of one 64-column (128-byte) swizzle chunk
 constexpr unsigned long long kWaitNs = 4000000000ull;
 
-enum { B_Q = 0, B_KF = 1, B_KE = 3, B_VF = 5, B_VE = 8, B_SF = 11, B_PF = 13, B_OD = 15, B_END = 17, NBAR = 18 };
+// Barriers.  Position g of the walk (key tile g over every block) consumes
+// the pair (K tile g+1, V tile g) -- what P V(g) and Q K^T(g+1) read -- and
+// the pair lands on one full barrier B_F + g % 2 and is released by one
+// commit on B_E + g % 2; K tile 0 lands with Q on B_Q.
+enum { B_Q = 0, B_F = 1, B_E = 3, B_SF = 5, B_PF = 7, B_OD = 9, B_END = 11, NBAR = 12 };
 
 struct TcParams {
     CUtensorMap qmap[DIT_MAX_R];
@@ -129,10 +133,20 @@ __device__ __forceinline__ unsigned long long gtimer() {
     return t;
 }
 
+// The CTA's abort flag (a shared-memory word, by its 32-bit shared address)
+// and the caller's status word.
 struct Ctl {
-    volatile int* abort;
+    uint32_t abort;
     int* status;
 };
+__device__ __forceinline__ int ld_flag(uint32_t a) {
+    int v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_flag(uint32_t a, int v) {
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
 
 // Wait for the phase of `parity` to complete.  Returns false if the CTA has
 // aborted or this wait ran out of time (then the CTA is marked aborted).
@@ -142,9 +156,9 @@ __device__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl& ctl) {
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 63) == 0) {
-            if (*ctl.abort) return false;
+            if (ld_flag(ctl.abort)) return false;
             if (gtimer() - t0 > kWaitNs) {
-                *ctl.abort = 1;
+                st_flag(ctl.abort, 1);
                 atomicExch(ctl.status, (int)DIT_ERR_TIMEOUT);
                 return false;
             }
@@ -431,15 +445,18 @@ __device__ __forceinline__ void softmax_tile(uint32_t St, uint32_t Ot, int valid
 // (with diag, block r only), keeping Q resident, and writes partial (r, j)
 // at the end of block j; the K/V rings, the S/P barriers and the MMA stream
 // run on without a break across the blocks, so the pipeline fills and
-// drains once per CTA instead of once per block.  The V ring has 2 stages;
-// the freed tile holds one output staging slot per softmax warp, since the
-// Q, K and V buffers stay in use until the last block.
+// drains once per CTA instead of once per block.  Warp roles: 0-7 softmax
+// (two warpgroups, one query tile each), 8 the TMA producer, 9 the MMA
+// issuer.  K and V have 2 stages each; the third tile's worth of shared
+// memory holds one output staging slot per softmax warp, since the Q, K and
+// V buffers stay in use until the last block.
 template <int D, bool P_BF16, bool DIAG, bool FOLD>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     static_assert(!(DIAG && FOLD), "folding walks every key block");
     constexpr int NCH = D / 64;          // 128-byte chunks per row
     constexpr int TILE = BM * D * 2;     // bytes of one Q, K or V tile
     constexpr int NSV = kNSV;
+    static_assert(NSV == 2 && NSK == 2, "pairs (K g+1, V g) use stage g % 2 of both rings");
     constexpr int BARS = bars_offset<D>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -464,18 +481,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         return;
     }
 
-    const Ctl ctl{abort_flag, p.status};
+    const Ctl ctl{su32(const_cast<int*>(abort_flag)), p.status};
     auto bar = [&](int i) { return su32(bars + i); };
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q), 1);
-        for (int s = 0; s < NSK; ++s) {
-            mbar_init(bar(B_KF + s), 1);
-            mbar_init(bar(B_KE + s), 1);
-        }
-        for (int s = 0; s < NSV; ++s) {
-            mbar_init(bar(B_VF + s), 1);
-            mbar_init(bar(B_VE + s), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(B_F + s), 1);
+            mbar_init(bar(B_E + s), 1);
         }
         for (int t = 0; t < NQT; ++t) {
             mbar_init(bar(B_SF + t), 1);
@@ -503,65 +516,82 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
         // the walking MMA issuer keeps more loop state: 104 registers here,
         // 200 for each softmax warpgroup (2*200 + 104 = 3*168)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
-        if (warp == 8 || warp == 10) {
-        // ------------------------------------------------------------ producers
-        // Tiles are numbered across the key blocks (g); stage g % nst.
+        if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        // Key tiles are numbered across the key blocks (g); K tile g sits in
+        // K stage g % 2, V tile g in V stage g % 2.  Pair g = (K g+1, V g)
+        // waits until pair g-2's buffers are released (pair -1 is K tile 0,
+        // released after the first Q K^T of both query tiles).
         if (lane == 0) {
-            const bool is_k = (warp == 8);
-            const int nst = is_k ? NSK : NSV;
-            const int full = is_k ? B_KF : B_VF, empty = is_k ? B_KE : B_VE;
-            uint8_t* ring = is_k ? sK : sV;
-            int total = 0;                                  // key tiles over every block
             const int j0 = cta.j;
+            int total = 0;                                  // key tiles over every block
             for (int jj = 0; jj < nj; ++jj) total += (p.kv_len[j0 + jj] + BN - 1) / BN;
-            // Q and the first K tile go first; the other stages wait until Q
-            // has landed, so they do not compete with what the first Q K^T
-            // needs
-            if (is_k) {
-                const CUtensorMap* qm = &p.qmap[r];
-                mbar_expect_tx(bar(B_Q), NQT * TILE);
-                for (int t = 0; t < NQT; ++t)
-                    for (int c = 0; c < NCH; ++c)
-                        tma_load_4d(su32(sQ + t * TILE + c * CHUNK), qm, c * 64, h, row_base + t * BM, b, bar(B_Q));
-            }
+            // cursor over the walk's key tiles: block jj, tile n (empty blocks skipped)
+            struct Cur { int jj, n; };
+            auto first = [&]() {
+                Cur c{0, 0};
+                while (p.kv_len[j0 + c.jj] == 0) ++c.jj;   // some block has keys
+                return c;
+            };
+            auto next = [&](Cur c) {
+                if (++c.n * BN >= p.kv_len[j0 + c.jj]) {
+                    c.n = 0;
+                    do ++c.jj; while (c.jj < nj && p.kv_len[j0 + c.jj] == 0);
+                }
+                return c;
+            };
+            auto load = [&](const CUtensorMap* maps, Cur c, uint8_t* dst, uint32_t full) {
+                for (int ch = 0; ch < NCH; ++ch)
+                    tma_load_4d(su32(dst + ch * CHUNK), &maps[j0 + c.jj], ch * 64, h, c.n * BN, b, full);
+            };
+            Cur vc = first(), kc = vc;
+            // Q and K tile 0 first
+            mbar_expect_tx(bar(B_Q), (NQT + 1) * TILE);
+            for (int t = 0; t < NQT; ++t)
+                for (int ch = 0; ch < NCH; ++ch)
+                    tma_load_4d(su32(sQ + t * TILE + ch * CHUNK), &p.qmap[r], ch * 64, h, row_base + t * BM, b, bar(B_Q));
+            load(p.kmap, kc, sK, bar(B_Q));
+            kc = next(kc);
             int g = 0;
             bool ok = true;
-            for (int jj = 0; jj < nj && ok; ++jj) {
-                const int j = j0 + jj;
-                const CUtensorMap* map = is_k ? &p.kmap[j] : &p.vmap[j];
-                const int nt = (p.kv_len[j] + BN - 1) / BN;
-                for (int n = 0; n < nt; ++n, ++g) {
-                    const int s = g % nst;
-                    const uint32_t ph = (g / nst) & 1;
-                    if (g == (is_k ? 1 : 0) && !(ok = wait_phase(bar(B_Q), 0, ctl))) break;
-                    if (is_k && g == total / 2) prefetch_next_cta<D, DIAG>(p);
-                    if (g >= nst && !(ok = wait_phase(bar(empty + s), ph ^ 1, ctl))) break;
-                    mbar_expect_tx(bar(full + s), TILE);
-                    for (int c = 0; c < NCH; ++c)
-                        tma_load_4d(su32(ring + s * TILE + c * CHUNK), map, c * 64, h, n * BN, b, bar(full + s));
+            for (; g < total; ++g) {
+                const int x = g & 1;
+                if (g >= 1 && !(ok = wait_phase(bar(B_E + x), ((g - 1) >> 1) & 1, ctl))) break;
+                if (g == total / 2) prefetch_next_cta<D, DIAG>(p);
+                const bool has_k = g + 1 < total;
+                mbar_expect_tx(bar(B_F + x), (has_k ? 2 : 1) * TILE);
+                if (has_k) {
+                    load(p.kmap, kc, sK + ((g + 1) & 1) * TILE, bar(B_F + x));
+                    kc = next(kc);
                 }
+                load(p.vmap, vc, sV + x * TILE, bar(B_F + x));
+                vc = next(vc);
             }
             if (!ok || *abort_flag) {
                 // let every copy this thread issued land before smem is released
-                if (is_k) drain_phase(bar(B_Q), 0);
-                for (int k = g > nst ? g - nst : 0; k < g; ++k) drain_phase(bar(full + k % nst), (k / nst) & 1);
+                drain_phase(bar(B_Q), 0);
+                for (int k = g > 2 ? g - 2 : 0; k < g; ++k) drain_phase(bar(B_F + (k & 1)), (k >> 1) & 1);
             }
         }
         } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
+        // The issuing thread stays inside tcgen05.mma until the tensor core
+        // takes the instruction, and each commit or barrier wait after a
+        // group of MMAs waits for that group to drain, so the waits and
+        // commits are gathered into two gaps per position, where P must be
+        // waited for in any case: P V(0, g) and Q K^T(0, g+1) go back to
+        // back, so do P V(1, g) and Q K^T(1, g+1).
         if (lane == 0) {
             const uint32_t S[NQT] = {tmem, tmem + 128};
             const uint32_t O[NQT] = {tmem + 256, tmem + 256 + D};
             // Descriptors are built once; a k-step only adds an offset (in
             // 16-byte units) to the start-address field.  Stage buffers are
             // selected with (s ? x1 : x0), never by indexing an array.
-            static_assert(NQT == 2 && NSK == 2 && (NSV == 2 || NSV == 3),
-                          "descriptor selection assumes 2 tiles, 2 K stages, 2 or 3 V stages");
+            static_assert(NQT == 2 && NSK == 2 && kNSV == 2, "descriptor selection assumes 2 tiles and 2 stages");
             const uint64_t qd0 = sdesc(su32(sQ), 16, 1024), qd1 = sdesc(su32(sQ + TILE), 16, 1024);
             const uint64_t kd0 = sdesc(su32(sK), 16, 1024), kd1 = sdesc(su32(sK + TILE), 16, 1024);
             // V tile rows are keys (K dim), 64-wide d chunks CHUNK apart (N dim)
-            const uint64_t vd0 = sdesc(su32(sV), CHUNK, 1024), vd1 = sdesc(su32(sV + TILE), CHUNK, 1024),
-                           vd2 = sdesc(su32(sV + (NSV - 1) * TILE), CHUNK, 1024);
+            const uint64_t vd0 = sdesc(su32(sV), CHUNK, 1024), vd1 = sdesc(su32(sV + TILE), CHUNK, 1024);
             const uint32_t idesc_qk = p.idesc_qk, idesc_pv = p.idesc_pv;
             auto issue_qk = [&](int t, int s) {
                 const uint64_t a0 = t ? qd1 : qd0, b0 = s ? kd1 : kd0;
@@ -573,7 +603,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                 }
             };
             auto issue_pv = [&](int t, int s, bool acc) {
-                const uint64_t b0 = s == 0 ? vd0 : (s == 1 ? vd1 : vd2);
+                const uint64_t b0 = s ? vd1 : vd0;
                 const uint32_t d = t ? O[1] : O[0], a = t ? S[1] : S[0];
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks)
@@ -581,30 +611,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
             };
             const int j0 = cta.j;
             auto tiles_of = [&](int jj) { return (p.kv_len[j0 + jj] + BN - 1) / BN; };
-            // positions (key block jj, key tile n), empty blocks skipped;
-            // gk / gv count K / V tiles, gs positions
+            // positions (key block jj, key tile n), empty blocks skipped; g
+            // counts positions over the whole walk
             int jj = 0;
             while (tiles_of(jj) == 0) ++jj;       // some block has keys
             int nt = tiles_of(jj), n = 0;
-            uint32_t gk = 0, gv = 0, gs = 0;
-            bool ok = wait_phase(bar(B_Q), 0, ctl) && wait_phase(bar(B_KF), 0, ctl);
+            uint32_t g = 0;
+            bool ok = wait_phase(bar(B_Q), 0, ctl);
             if (ok) {
                 tc_fence_after();
                 issue_qk(0, 0);
                 tc_commit(bar(B_SF + 0));
                 issue_qk(1, 0);
                 tc_commit(bar(B_SF + 1));
-                tc_commit(bar(B_KE + 0));
-                gk = 1;
+                tc_commit(bar(B_E + 1));           // K tile 0 read (pair -1)
             }
             while (ok) {
-                const int sv = (int)(gv % NSV);
-                if (!(ok = wait_phase(bar(B_VF + sv), (gv / NSV) & 1, ctl))) break;
-                if (!(ok = wait_phase(bar(B_PF + 0), gs & 1, ctl))) break;
+                const int x = (int)(g & 1);
+                // pair g: K tile g+1 (when there is one) and V tile g
+                if (!(ok = wait_phase(bar(B_F + x), (g >> 1) & 1, ctl))) break;
+                if (!(ok = wait_phase(bar(B_PF + 0), g & 1, ctl))) break;
                 tc_fence_after();
-                // folding, P V accumulates across the key blocks: only the
-                // very first position starts O afresh
-                issue_pv(0, sv, FOLD ? gs > 0 : n > 0);
                 const bool last = n + 1 == nt;
                 int jn = jj, nn = n + 1;
                 if (last) {
@@ -612,30 +639,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_tc_kernel(const __grid_const
                     do ++jn; while (jn < nj && tiles_of(jn) == 0);
                 }
                 const bool more = jn < nj;
-                // output done for tile 0 (the block's partial; folding, the
-                // whole walk): its epilogue overlaps tile 1's last P V (and,
-                // walking, the next block's first Q K^T)
+                // output done for a tile (the block's partial; folding, the
+                // whole walk): its epilogue overlaps the next block's Q K^T
                 const bool done = last && (!FOLD || !more);
+                // folding, P V accumulates across the key blocks: only the
+                // very first position starts O afresh
+                const bool acc = FOLD ? g > 0 : n > 0;
+                issue_pv(0, x, acc);
                 if (done) tc_commit(bar(B_OD + 0));
-                const int sk = (int)(gk % NSK);
                 if (more) {
-                    if (!(ok = wait_phase(bar(B_KF + sk), (gk / NSK) & 1, ctl))) break;
-                    tc_fence_after();
-                    issue_qk(0, sk);
+                    issue_qk(0, x ^ 1);
                     tc_commit(bar(B_SF + 0));
                 }
-                if (!(ok = wait_phase(bar(B_PF + 1), gs & 1, ctl))) break;
+                if (!(ok = wait_phase(bar(B_PF + 1), g & 1, ctl))) break;
                 tc_fence_after();
-                issue_pv(1, sv, FOLD ? gs > 0 : n > 0);
-                tc_commit(bar(B_VE + sv));
-                ++gv;
+                issue_pv(1, x, acc);
                 if (done) tc_commit(bar(B_OD + 1));
-                ++gs;
+                if (more) {
+                    issue_qk(1, x ^ 1);
+                    tc_commit(bar(B_SF + 1));
+                }
+                tc_commit(bar(B_E + x));           // K tile g+1 and V tile g read
+                ++g;
                 if (!more) break;
-                issue_qk(1, sk);
-                tc_commit(bar(B_SF + 1));
-                tc_commit(bar(B_KE + sk));
-                ++gk;
                 if (last) nt = tiles_of(jn);
                 jj = jn;
                 n = nn;

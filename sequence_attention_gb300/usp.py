@@ -8,7 +8,7 @@ redistributed data, then the inverse all-to-all; SGLang Diffusion
 
   layout in    seq-sharded Q,K,V -> head layout [R,B,S_cap,Hp,D] (V as f16)
   attention    every ring block r against every ring block j, one launch:
-               ring_merge="fold" (default up to R = 2) dit_attn_ring, each hop folded in
+               ring_merge="fold" (default on 16-bit inputs) dit_attn_ring, each hop folded in
                by the online softmax as the kernel walks the K/V blocks;
                ring_merge="partials" dit_attn_partial (every (r, j)
                partial) then dit_attn_merge_lse (the R-way log-sum-exp
@@ -73,12 +73,11 @@ class UspPlan:
         ring_merge: "fold" (the K/V blocks folded into one result as the
         kernel walks them) or "partials" (every partial written, then the
         R-way merge kernel); the same result up to rounding.  By default
-        "fold" for R <= 2 on 16-bit inputs and "partials" otherwise:
-        measured on one GB300, the
-        fold saves the merge pass (FLUX-1008-like R = 2: 0.256 against 0.270
-        ms per step; Qwen-like 1.06 against 1.09), but its walk over many long
-        blocks ran ~1.7 % slower than the partial kernel's (Wan-like R = 4:
-        80.3 against 78.9 ms of attention), more than the 0.55 ms merge.
+        "fold" on 16-bit inputs and "partials" on the fp32 path: measured
+        on one GB300, the fold saves the merge pass and the partials' writes
+        (FLUX-1008-like R = 2: 0.246 against 0.266 ms per step; Wan-like
+        R = 4: 79.1 against 80.8 ms), while the fp32 CUDA-core kernel folds
+        with half the CTAs of its partials (tiny: 0.116 against 0.106 ms).
         exchange: "direct" (one pass per layout step) or "a2a" (pack,
         exchange, unpack); default "direct", or "a2a" with an e4m3 wire.
         v_dtype: by default f16 for bf16 inputs (P V runs with P in V's type,
@@ -131,10 +130,7 @@ class UspPlan:
             raise ValueError("f16 partials need f16 V (a partial lies within V's range)")
         self.parts_dtype = parts_dtype
         if ring_merge is None:
-            # the fp32 CUDA-core kernel folds with one CTA per query block
-            # and row tile, half the CTAs of its partials (tiny: 0.116
-            # against 0.106 ms per step)
-            ring_merge = "fold" if R <= 2 and in_dtype != torch.float32 else "partials"
+            ring_merge = "fold" if in_dtype != torch.float32 else "partials"
         if ring_merge not in ("fold", "partials"):
             raise ValueError(f"ring_merge must be 'fold' or 'partials', got {ring_merge!r}")
         self.ring_merge = ring_merge

@@ -415,6 +415,7 @@ def test_plan_partial_type(dl):
                                                                         "head_to_seq"]
     with pytest.raises(ValueError):
         UspPlan(1, 64, 2, 64, 2, 2, device="cpu", ring_merge="tree")
-    # the default: fold up to two ring blocks, partials and the merge beyond
-    assert UspPlan(1, 64, 2, 64, 2, 4, device="cpu").ring_merge == "partials"
+    # the default: fold on 16-bit inputs at any ring degree, partials and
+    # the merge on the fp32 path
+    assert UspPlan(1, 64, 2, 64, 2, 4, device="cpu").ring_merge == "fold"
     assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", in_dtype=torch.float32).ring_merge == "partials"
