@@ -371,7 +371,7 @@ def run_ours(args):
         mark(0)
         plan.layout_in(q, k, v)
         mark(1)
-        plan.partials()
+        plan.partials(out=out)  # writes out itself when the plan can (no layout-out pass then)
         mark(2)
         plan.merge()            # nothing when R = 1
         mark(3)
@@ -444,9 +444,10 @@ def run_ours(args):
     wire3 = 3 * w.B * w.S * L.Hp * w.D * eb
     o_bytes = w.B * w.S * w.H * w.D * 2
     wire1 = w.B * w.S * L.Hp * w.D * 2
+    out_in_place = plan.direct_out(out)              # the attention writes out: no layout-out pass
     if plan.exchange == "direct":
         layout_in_bytes = qkv_bytes + wire3          # sequence planes in, head layout out
-        layout_out_bytes = o_bytes + o_bytes         # real heads of the head layout in, output out
+        layout_out_bytes = 0 if out_in_place else o_bytes + o_bytes   # real heads in, output out
     else:
         layout_in_bytes = (qkv_bytes + wire3) + 2 * wire3 + (wire3 + wire3)
         layout_out_bytes = (o_bytes + wire1) + 2 * wire1 + (wire1 + o_bytes)
@@ -536,7 +537,9 @@ def run_ours(args):
                 "merge_GBs": round(merge_bytes / (statistics.mean(seg[2]) * 1e-3) / 1e9, 1)}
                if plan.parts is not None else {}),
             "layout_out_ms": round(statistics.mean(seg[3]), 4),
-            "layout_out_GBs": round(layout_out_bytes / (statistics.mean(seg[3]) * 1e-3) / 1e9, 1),
+            "layout_out_GBs": (round(layout_out_bytes / (statistics.mean(seg[3]) * 1e-3) / 1e9, 1)
+                               if layout_out_bytes else None),
+            "layout_out": "in the attention's output view" if out_in_place else "a pass of its own",
             "cfg_ms": round(statistics.mean(seg[4]), 4),
             "cfg_GBs": round(cfg_bytes / (statistics.mean(seg[4]) * 1e-3) / 1e9, 1),
             "hbm_peak_GBs": peaks.get("hbm_gbs"),
@@ -884,7 +887,7 @@ def run_sweep(args):
             ev[0].record(stream)
             plan.layout_in(q, k, v)
             ev[1].record(stream)
-            plan.partials()
+            plan.partials(out=out)
             ev[2].record(stream)
             plan.merge()
             ev[3].record(stream)
@@ -915,6 +918,7 @@ def run_sweep(args):
                "ring_merge": plan.ring_merge,
                "attention_plus_merge_TFLOPs": round(tfm, 1),
                "layout_out_ms": round(med[3], 4), "cfg_ms": round(med[4], 4),
+               "layout_out": "in the attention's output view" if plan.direct_out(out) else "a pass of its own",
                "heads_padded": L.Hp - w.H, "status": int(plan.status.item()),
                "range_flag": int(plan.range_flag.item()), "exchange": plan.exchange}
         if not args.no_cpu_baseline:

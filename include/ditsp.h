@@ -21,6 +21,8 @@
  *   dit_attn_merge_lse                       exact merge of the partials
  *   dit_attn_ring                            the partials of every key block
  *                                            folded in as the CTA walks them
+ *   dit_attn_ring_rows                       the same, each query block's
+ *                                            output placed at its own row
  *   dit_attention                            single-shot attention
  *   dit_cfg_combine                          classifier-free guidance combine
  *
@@ -461,6 +463,26 @@ DIT_API dit_status dit_attn_ring(int B, int H, int D, float scale, int n_q, cons
                                  const int* kv_len, dit_view q, dit_dtype qk_dt, dit_view k, dit_view v,
                                  dit_dtype v_dt, dit_view o, dit_dtype o_dt, dit_lse_view lse, int* d_status,
                                  void* stream);
+
+/*
+ * dit_attn_ring_rows: dit_attn_ring with each query block's output moved
+ * o_row0[r] rows further into o:
+ *   o         query block r at o.ptr + r*o.stride_q + o_row0[r]*o.stride_s,
+ *             [B][q_len[r]][H][D]
+ * When every rank lives in one memory, the head-to-sequence exchange of the
+ * output (edge-dit.cpp "Parallel execution", head-to-sequence path) only
+ * moves ring block r's rows to rows ring_off[r] + i of the sequence layout
+ * and drops the padded heads; with o.stride_q = 0, o_row0[r] = ring_off[r]
+ * and the sequence layout's strides, the attention writes each result at
+ * that place and no layout pass follows.  The lse rows are not moved.
+ * o_row0 is a host array of n_q entries >= 0.  With o.stride_q == 0 the
+ * blocks' output rows [o_row0[r], o_row0[r] + q_len[r]) must not overlap
+ * (DIT_ERR_INVALID_ARG otherwise).  Everything else as for dit_attn_ring.
+ */
+DIT_API dit_status dit_attn_ring_rows(int B, int H, int D, float scale, int n_q, const int* q_len,
+                                      const int* o_row0, int n_kv, const int* kv_len, dit_view q,
+                                      dit_dtype qk_dt, dit_view k, dit_view v, dit_dtype v_dt, dit_view o,
+                                      dit_dtype o_dt, dit_lse_view lse, int* d_status, void* stream);
 
 /*
  * dit_attn_varlen: attention of packed variable-length sequences (SGLang

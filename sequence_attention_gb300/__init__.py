@@ -35,7 +35,7 @@ __all__ = [
     "dit_ulysses_unpack", "dit_attn_partial", "dit_attn_merge_lse", "dit_attention",
     "dit_cfg_combine", "dit_device_status", "library_path", "dit_sp_signal", "dit_a2a_sim_checked",
     "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint", "dit_ulysses_unpack_rope", "dit_attn_varlen",
-    "dit_ulysses_seq_to_head", "dit_ulysses_head_to_seq", "dit_attn_ring",
+    "dit_ulysses_seq_to_head", "dit_ulysses_head_to_seq", "dit_attn_ring", "dit_attn_ring_rows",
 ]
 
 lib()   # load now: fail at import time, not at first call
@@ -323,6 +323,24 @@ def dit_attn_ring(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Te
                               _lens(kv_len, n_kv, k.shape[2]), _view(q, "q"), _dt(q),
                               _view(k, "kv"), _view(v, "kv"), _dt(v), _view(o, "out"), _dt(o),
                               _lse_view(lse, "out"), _ptr(status), _stream(stream)))
+
+
+def dit_attn_ring_rows(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                       o_row0: Sequence[int], lse: Optional[torch.Tensor] = None,
+                       q_len: Optional[Sequence[int]] = None, kv_len: Optional[Sequence[int]] = None,
+                       scale: Optional[float] = None, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """dit_attn_ring with every query block's output in one tensor o
+    [B,S,H,D]: query block r's rows start at row o_row0[r]."""
+    n_q, B, Sq, H, D = q.shape
+    n_kv = k.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if len(o_row0) != n_q:
+        raise ValueError("o_row0 needs one entry per query block")
+    check(lib().dit_attn_ring_rows(B, H, D, float(scale), n_q, _lens(q_len, n_q, Sq), (c_int * n_q)(*o_row0), n_kv,
+                                   _lens(kv_len, n_kv, k.shape[2]), _view(q, "q"), _dt(q),
+                                   _view(k, "kv"), _view(v, "kv"), _dt(v), _view(o, "single"), _dt(o),
+                                   _lse_view(lse, "out"), _ptr(status), _stream(stream)))
 
 
 def dit_attn_merge_lse(parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor,

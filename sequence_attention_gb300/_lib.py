@@ -29,6 +29,7 @@ EXPORTS = (
     "dit_sp_signal", "dit_a2a_sim_checked", "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint",
     "dit_ulysses_unpack_rope", "dit_attn_varlen", "dit_ulysses_seq_to_head", "dit_ulysses_head_to_seq",
     "dit_attn_ring",
+    "dit_attn_ring_rows",
 )
 
 
@@ -122,6 +123,10 @@ def lib() -> ctypes.CDLL:
     L.dit_attn_ring.argtypes = [c_int, c_int, c_int, c_float, c_int, POINTER(c_int), c_int,
                                 POINTER(c_int), DitView, c_int, DitView, DitView, c_int, DitView,
                                 c_int, DitLseView, c_void_p, c_void_p]
+    L.dit_attn_ring_rows.restype = c_int
+    L.dit_attn_ring_rows.argtypes = [c_int, c_int, c_int, c_float, c_int, POINTER(c_int), POINTER(c_int), c_int,
+                                     POINTER(c_int), DitView, c_int, DitView, DitView, c_int, DitView,
+                                     c_int, DitLseView, c_void_p, c_void_p]
     L.dit_attn_varlen.restype = c_int
     L.dit_attn_varlen.argtypes = [c_int, c_int, c_float, c_int, POINTER(c_int), POINTER(c_int), DitView, c_int,
                                   DitView, DitView, c_int, DitView, c_int, DitLseView, c_void_p, c_void_p]

@@ -10,6 +10,18 @@ namespace {
 
 bool stride_ok(int64_t s, int elem_bytes) { return s >= 0 && ((s * elem_bytes) % 16) == 0; }
 
+// With one output base for every query block (o.stride_q == 0), the blocks'
+// output rows [q_row0 + o_row0, + q_len) must not overlap.
+bool block_rows_disjoint(const AttnArgs& a) {
+    for (int r = 0; r < a.n_q; ++r)
+        for (int s = r + 1; s < a.n_q; ++s) {
+            if (a.q_len[r] == 0 || a.q_len[s] == 0) continue;
+            const long long r0 = (long long)a.q_row0[r] + a.o_row0[r], s0 = (long long)a.q_row0[s] + a.o_row0[s];
+            if (r0 < s0 + a.q_len[s] && s0 < r0 + a.q_len[r]) return false;
+        }
+    return true;
+}
+
 dit_status validate_and_launch(AttnArgs& a, const char* who, cudaStream_t st) {
     if (a.B < 1 || a.H < 1 || a.D < 1) return fail(DIT_ERR_INVALID_ARG, "%s: need B, H, D >= 1", who);
     if (!(a.scale > 0.f) || !isfinite(a.scale))
@@ -47,7 +59,8 @@ dit_status validate_and_launch(AttnArgs& a, const char* who, cudaStream_t st) {
     int maxq = 0;
     for (int r = 0; r < a.n_q; ++r) maxq = a.q_len[r] > maxq ? a.q_len[r] : maxq;
     const bool alias = (a.H > 1 && a.o.stride_h == 0) || (maxq > 1 && a.o.stride_s == 0) ||
-                       (a.B > 1 && a.o.stride_b == 0) || (!a.diag && a.n_q > 1 && a.o.stride_q == 0) ||
+                       (a.B > 1 && a.o.stride_b == 0) ||
+                       (!a.diag && a.n_q > 1 && a.o.stride_q == 0 && !block_rows_disjoint(a)) ||
                        (!a.diag && !a.fold && a.n_kv > 1 && a.o.stride_kv == 0);
     if (alias) return fail(DIT_ERR_INVALID_ARG, "%s: output view maps two results to one address", who);
     // No query rows: nothing is read or written, so the (empty) buffers may
@@ -116,6 +129,31 @@ extern "C" dit_status dit_attn_ring(int B, int H, int D, float scale, int n_q, c
     a.q = q; a.k = k; a.v = v; a.o = o;
     a.qk_dt = qk_dt; a.v_dt = v_dt; a.o_dt = o_dt; a.lse = lse; a.status = d_status;
     return validate_and_launch(a, "dit_attn_ring", (cudaStream_t)stream);
+}
+
+extern "C" dit_status dit_attn_ring_rows(int B, int H, int D, float scale, int n_q, const int* q_len,
+                                         const int* o_row0, int n_kv, const int* kv_len, dit_view q, dit_dtype qk_dt,
+                                         dit_view k, dit_view v, dit_dtype v_dt, dit_view o, dit_dtype o_dt,
+                                         dit_lse_view lse, int* d_status, void* stream) {
+    NvtxRange nvtx_range("dit_attn_ring_rows");
+    const char* who = "dit_attn_ring_rows";
+    if (!q_len || !kv_len || !o_row0) return fail(DIT_ERR_INVALID_ARG, "%s: NULL length or row array", who);
+    if (n_q < 1 || n_q > DIT_MAX_R || n_kv < 1 || n_kv > DIT_MAX_R)
+        return fail(DIT_ERR_INVALID_ARG, "%s: need 1 <= n_q, n_kv <= %d", who, DIT_MAX_R);
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.B = B; a.H = H; a.D = D; a.n_q = n_q; a.n_kv = n_kv; a.scale = scale; a.fold = 1;
+    for (int r = 0; r < n_q; ++r) {
+        if (o_row0[r] < 0) return fail(DIT_ERR_INVALID_ARG, "%s: negative output row", who);
+        a.q_len[r] = q_len[r];
+        a.o_row0[r] = o_row0[r];
+    }
+    for (int r = 0; r < n_kv; ++r) a.kv_len[r] = kv_len[r];
+    o.stride_kv = 0;                  // one result per query block
+    lse.stride_kv = 0;
+    a.q = q; a.k = k; a.v = v; a.o = o;
+    a.qk_dt = qk_dt; a.v_dt = v_dt; a.o_dt = o_dt; a.lse = lse; a.status = d_status;
+    return validate_and_launch(a, who, (cudaStream_t)stream);
 }
 
 extern "C" dit_status dit_attention(int B, int H, int D, float scale, int Sq, int Sk, dit_view q, dit_dtype qk_dt,

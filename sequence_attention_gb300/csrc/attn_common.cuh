@@ -20,6 +20,9 @@ struct AttnArgs {
     // query block i attends key block i only (n_q == n_kv)
     int q_row0[DIT_MAX_R];
     int kv_row0[DIT_MAX_R];
+    // query block i's output rows start o_row0[i] rows further into o (after
+    // q_row0[i]); the lse rows are not moved (0 unless the caller asks)
+    int o_row0[DIT_MAX_R];
     int diag;
     // with fold set, every query block walks all key blocks and folds them
     // into one result with the online softmax (the ring's per-hop merge): o

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const __grid_constant__ A
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;          // l >= 1 once any key was seen
     float* op = static_cast<float*>(a.o.ptr) + r * a.o.stride_q + j * a.o.stride_kv + b * a.o.stride_b +
-                ((long long)a.q_row0[r] + i) * a.o.stride_s + h * a.o.stride_h + part * DT;
+                ((long long)a.q_row0[r] + a.o_row0[r] + i) * a.o.stride_s + h * a.o.stride_h + part * DT;
 #pragma unroll
     for (int d = 0; d < DT; d += 4)
         *reinterpret_cast<float4*>(op + d) = make_float4(acc[d] * inv, acc[d + 1] * inv, acc[d + 2] * inv, acc[d + 3] * inv);

@@ -81,6 +81,7 @@ struct TcParams {
     int q_len[DIT_MAX_R];
     int kv_len[DIT_MAX_R];
     int q_row0[DIT_MAX_R];          // first output row of query block r (packed sequences)
+    int o_row0[DIT_MAX_R];          // further rows into o of query block r's output
     int B, n_q, n_kv;
     int diag;                       // query block r attends key block r only
     int fold;                       // one output per query block: the key blocks folded by the online softmax
@@ -354,7 +355,8 @@ __device__ __forceinline__ void write_empty_partial(const TcParams& p, int r, in
     if (row >= p.q_len[r]) return;
     const int eb = dtype_bytes(p.o_dt);
     char* orow = static_cast<char*>(p.o.ptr) + (r * p.o.stride_q + j * p.o.stride_kv + b * p.o.stride_b +
-                                                h * p.o.stride_h + ((long long)p.q_row0[r] + row) * p.o.stride_s) * eb;
+                                                h * p.o.stride_h +
+                                                ((long long)p.q_row0[r] + p.o_row0[r] + row) * p.o.stride_s) * eb;
     for (int d = 0; d < D; d += 8) store8_zero(orow + d * eb, p.o_dt);
     if (p.lse.ptr)
         p.lse.ptr[r * p.lse.stride_q + j * p.lse.stride_kv + b * p.lse.stride_b + h * p.lse.stride_h + p.q_row0[r] +
@@ -909,13 +911,15 @@ dit_status launch_attn_tc(const AttnArgs& a, cudaStream_t st) {
         prm->q_len[r] = a.q_len[r];
         if (a.q_len[r] > maxq) maxq = a.q_len[r];
         prm->q_row0[r] = a.q_row0[r];
+        prm->o_row0[r] = a.o_row0[r];
         const char* base = static_cast<const char*>(a.q.ptr) + (r * a.q.stride_q + (int64_t)a.q_row0[r] * a.q.stride_s) * 2;
         s = make_map(enc, &prm->qmap[r], base, a.qk_dt, a.D, a.H, a.q_len[r], a.B, a.q.stride_h, a.q.stride_s,
                      a.q.stride_b);
         if (s == DIT_OK) {
             // with diag, query block r writes key block r's partial only
             char* ob = static_cast<char*>(a.o.ptr) +
-                       (r * a.o.stride_q + (a.diag ? r * a.o.stride_kv : 0) + (int64_t)a.q_row0[r] * a.o.stride_s) *
+                       (r * a.o.stride_q + (a.diag ? r * a.o.stride_kv : 0) +
+                        ((int64_t)a.q_row0[r] + a.o_row0[r]) * a.o.stride_s) *
                            dtype_bytes(a.o_dt);
             s = make_omap(enc, &prm->omap[r], ob, a.o_dt, a.D, a.H, a.q_len[r], a.B, (a.diag || a.fold) ? 1 : a.n_kv,
                           a.o.stride_h, a.o.stride_s, a.o.stride_b, a.o.stride_kv);

@@ -13,7 +13,11 @@ redistributed data, then the inverse all-to-all; SGLang Diffusion
                ring_merge="partials" dit_attn_partial (every (r, j)
                partial) then dit_attn_merge_lse (the R-way log-sum-exp
                merge), the form whose partials could come from other GPUs
-  layout out   head layout -> seq-sharded output [B,S,H,D]
+  layout out   head layout -> seq-sharded output [B,S,H,D]; with the
+               one-pass exchange and one result per query block (R = 1 or
+               the fold) the attention writes each block's rows straight to
+               their sequence positions (dit_attn_ring_rows) and this pass
+               is skipped
 
 The layout steps run one of two ways (``exchange``):
   "direct"  dit_ulysses_seq_to_head / dit_ulysses_head_to_seq: on one memory
@@ -40,7 +44,7 @@ from typing import Optional, Sequence, Tuple
 import torch
 
 from . import (DIT_HEAD_TO_SEQ, DIT_SEQ_TO_HEAD, DitError, dit_a2a_sim, dit_attn_merge_lse, dit_attn_partial,
-               dit_attn_ring,
+               dit_attn_ring, dit_attn_ring_rows,
                dit_sp_layout_init, dit_ulysses_head_to_seq, dit_ulysses_pack, dit_ulysses_pack_joint,
                dit_ulysses_seq_to_head, dit_ulysses_unpack, dit_ulysses_unpack_joint, dit_ulysses_unpack_rope)
 from ._lib import DIT_ERR_RANGE, DIT_ERR_TIMEOUT
@@ -182,8 +186,22 @@ class UspPlan:
             raise DitError(DIT_ERR_RANGE, "a value overflowed its 16-bit destination type "
                                           "(f16 holds |x| < 65520; use v_dtype=torch.bfloat16)")
 
+    def direct_out(self, out: torch.Tensor) -> bool:
+        """Whether the attention can write `out` [B,S,H,D] in place of the
+        layout-out pass: on one memory the head-to-sequence permutation only
+        moves ring block r's rows to rows ring_off[r] + i and drops padded
+        heads, so the attention's output view can do it, when it gives one
+        result per query block (R = 1 or the fold) and out has the plan's
+        shape in a type the attention writes."""
+        if self.exchange != "direct" or not (self.R == 1 or self.ring_merge == "fold"):
+            return False
+        if tuple(out.shape) != (self.B, self.S, self.H, self.D) or out.stride(-1) != 1:
+            return False
+        return self.in_dtype != torch.float32 or out.dtype == torch.float32
+
     def steps(self):
-        """Names of the kernels one run() launches, in order."""
+        """Names of the kernels one run() launches, in order (run() with an
+        output the attention can write in place)."""
         if self.exchange == "direct":
             s = ["seq_to_head"]
         elif self.fp8_qv:
@@ -196,7 +214,9 @@ class UspPlan:
             s = s + ["attn_partial"]
             if self.R > 1:
                 s.append("merge")
-        return s + (["head_to_seq"] if self.exchange == "direct" else ["pack_h2s", "a2a_h2s", "unpack_h2s"])
+        if self.exchange != "direct":
+            return s + ["pack_h2s", "a2a_h2s", "unpack_h2s"]
+        return s if (self.R == 1 or self.ring_merge == "fold") else s + ["head_to_seq"]
 
     def _unpack(self, recv, heads, rope_mask, stream):
         if self.rope is not None:
@@ -246,16 +266,22 @@ class UspPlan:
             dit_ulysses_pack_joint(self.L, txt, img, self.send, stream)
         self._receive(stream)
 
-    def partials(self, stream=None):
+    def partials(self, stream=None, out: Optional[torch.Tensor] = None):
         """The attention of every ring block against every ring block in one
         launch: folded into the output (ring_merge="fold"), or every (r, j)
         partial written for merge(); with R = 1 the single partial is the
-        output itself."""
+        output itself.  Given out (the step's [B,S,H,D] output) and
+        direct_out(out), the result goes straight to out and layout_out(out)
+        has nothing left to do."""
         rl = self.ring_len
         qv, kv, vv = self.heads(self.q_h), self.heads(self.k_h), self.heads(self.v_h)
+        direct = out is not None and self.direct_out(out)
+        self._o_at = out if direct else None
         if self.R == 1:
-            o = self.heads(self.o_h).unsqueeze(1)        # [1, 1, B, S, H, D]
+            o = (out if direct else self.heads(self.o_h)[0]).unsqueeze(0).unsqueeze(0)   # [1, 1, B, S, H, D]
             dit_attn_partial(qv, kv, vv, o, None, rl, rl, self.scale, self.status, stream)
+        elif self.ring_merge == "fold" and direct:
+            dit_attn_ring_rows(qv, kv, vv, out, self.L.ring_off, None, rl, rl, self.scale, self.status, stream)
         elif self.ring_merge == "fold":
             dit_attn_ring(qv, kv, vv, self.heads(self.o_h), None, rl, rl, self.scale, self.status, stream)
         else:
@@ -270,12 +296,14 @@ class UspPlan:
             dit_attn_merge_lse(self.heads(self.parts), self.lse_parts[:, :, :, : self.H, :],
                                self.heads(self.o_h), None, self.ring_len, stream)
 
-    def attend(self, stream=None):
-        self.partials(stream)
+    def attend(self, stream=None, out: Optional[torch.Tensor] = None):
+        self.partials(stream, out)
         self.merge(stream)
 
     def layout_out(self, out, stream=None):
         L = self.L
+        if getattr(self, "_o_at", None) is out:
+            return                      # the attention wrote out in place
         if self.exchange == "direct":
             dit_ulysses_head_to_seq(L, self.o_h, out, stream=stream)
             return
@@ -320,7 +348,7 @@ class UspPlan:
         """q, k, v: [B, S, H, D] seq-sharded inputs; out: [B, S, H, D].
         check=True waits for the step and raises as check() does."""
         self.layout_in(q, k, v, stream)
-        self.attend(stream)
+        self.attend(stream, out)
         self.layout_out(out, stream)
         if check:
             self.check()

@@ -410,7 +410,12 @@ def test_plan_partial_type(dl):
     # folding the ring blocks in the attention needs no partial buffers
     fold = UspPlan(1, 64, 2, 64, 2, 2, device="cpu")
     assert fold.ring_merge == "fold" and fold.parts is None and fold.lse_parts is None
-    assert fold.steps() == ["seq_to_head", "attn_ring", "head_to_seq"]
+    # with the one-pass exchange the folded attention writes the output in place
+    assert fold.steps() == ["seq_to_head", "attn_ring"]
+    out = torch.empty((1, 64, 2, 64), dtype=torch.bfloat16)
+    assert fold.direct_out(out) and not fold.direct_out(out[:, :32])
+    assert not UspPlan(1, 64, 2, 64, 2, 2, device="cpu", exchange="a2a").direct_out(out)
+    assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", exchange="a2a").steps()[-1] == "unpack_h2s"
     assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", **rm).steps() == ["seq_to_head", "attn_partial", "merge",
                                                                         "head_to_seq"]
     with pytest.raises(ValueError):

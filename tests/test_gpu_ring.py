@@ -18,7 +18,7 @@ import torch
 
 import synth
 from oracle import attention as oatt
-from tests.helpers import F32_MAX_ABS, LSE_ABS, MERGE_REL_RMS, assert_bf16_close, f64, max_abs, rel_rms
+from tests.helpers import F32_MAX_ABS, LSE_ABS, MERGE_REL_RMS, assert_bf16_close, bits, f64, max_abs, rel_rms
 
 pytestmark = pytest.mark.gpu
 
@@ -148,3 +148,51 @@ def test_ring_argument_checks():
     with pytest.raises(sa.DitError):
         sa.dit_attn_ring(q, q, v, o.expand(2, 1, 64, 2, 128).as_strided(o.shape, (0,) + o.stride()[1:]), None,
                          [64, 64], [64, 64])                                       # two blocks on one address
+
+
+@pytest.mark.parametrize("v_dt,o_dt", [(torch.float16, torch.bfloat16), (torch.float32, torch.float32)])
+def test_ring_rows_into_one_sequence_tensor(v_dt, o_dt):
+    """dit_attn_ring_rows places query block r at rows o_row0[r] of one
+    [B,S,H,D] tensor: bit for bit what dit_attn_ring writes per block, every
+    row written once, nothing else touched (an empty block in the middle)."""
+    import sequence_attention_gb300 as sa
+    B, H, D = 2, 3, 64
+    q_lens, kv_lens = [130, 0, 77, 201], [130, 64, 77, 201]
+    f32 = v_dt == torch.float32
+    kind = "f32" if f32 else "bf16"
+    Sq, Sk = sum(q_lens), sum(kv_lens)
+    q = synth.normal((B, Sq, H, D), 96, 0.5, kind)
+    k = synth.normal((B, Sk, H, D), 97, 0.5, kind)
+    v = synth.normal((B, Sk, H, D), 98, 0.5, kind)
+    cq, ck = max(q_lens), max(kv_lens)
+    qd, kd, vd = (_blocks(x, l, c).cuda() for x, l, c in ((q, q_lens, cq), (k, kv_lens, ck), (v.to(v_dt), kv_lens, ck)))
+    # per-block outputs, then the same into one tensor with a spare row at the end
+    ref = torch.full((len(q_lens), B, cq, H, D), float("nan"), dtype=o_dt, device="cuda")
+    sa.dit_attn_ring(qd, kd, vd, ref, None, q_lens, kv_lens)
+    out = torch.full((B, Sq + 1, H, D), float("nan"), dtype=o_dt, device="cuda")
+    row0 = [sum(q_lens[:r]) for r in range(len(q_lens))]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sa.dit_attn_ring_rows(qd, kd, vd, out, row0, None, q_lens, kv_lens, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for r, L in enumerate(q_lens):
+        np.testing.assert_array_equal(bits(out[:, row0[r]:row0[r] + L]), bits(ref[r, :, :L]))
+    assert torch.isnan(out[:, Sq:].float()).all()                    # the spare row is untouched
+    assert not torch.isnan(out[:, :Sq].float()).any()
+    if not f32:
+        o_ref, _ = oatt.attention(f64(q), f64(k), f64(v.to(v_dt)))
+        # every query row attends every key of every block: the full attention
+        assert_bf16_close(f64(out[:, :Sq]), o_ref, "ring rows")
+
+
+def test_ring_rows_argument_checks():
+    import sequence_attention_gb300 as sa
+    q = torch.zeros((2, 1, 64, 2, 128), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros((2, 1, 64, 2, 128), dtype=torch.float16, device="cuda")
+    out = torch.zeros((1, 128, 2, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sa.DitError):
+        sa.dit_attn_ring_rows(q, q, v, out, [0, 32], None, [64, 64], [64, 64])    # blocks' rows overlap
+    with pytest.raises(sa.DitError):
+        sa.dit_attn_ring_rows(q, q, v, out, [0, -1], None, [64, 64], [64, 64])    # negative row
+    sa.dit_attn_ring_rows(q, q, v, out, [64, 0], None, [64, 64], [64, 64])        # any order of disjoint rows
+    torch.cuda.synchronize()
