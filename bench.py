@@ -484,6 +484,17 @@ def run_ours(args):
     eager_ms = one_step(lambda: step(None, False))
     del one
     other = {}
+    if out_in_place:
+        # the same step with the output exchange as a pass of its own: the
+        # attention writes the head layout, the one-pass head->seq follows
+        def step_pass():
+            plan.layout_in(q, k, v)
+            plan.partials()
+            plan.merge()
+            plan.layout_out(out)
+            sa.dit_cfg_combine(pred, cfg_out, w.g)
+        step_pass()
+        other["step_layout_out_pass_ms"] = round(one_step(step_pass), 4)
     if w.R > 1:
         # the other form of the ring merge, one step alone (same launches)
         alt = "partials" if plan.ring_merge == "fold" else "fold"
