@@ -196,3 +196,39 @@ def test_ring_rows_argument_checks():
         sa.dit_attn_ring_rows(q, q, v, out, [0, -1], None, [64, 64], [64, 64])    # negative row
     sa.dit_attn_ring_rows(q, q, v, out, [64, 0], None, [64, 64], [64, 64])        # any order of disjoint rows
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_ring_rows_fuzz(seed):
+    """Random block counts and lengths (empty blocks included), output rows
+    placed with random gaps between the blocks in one tensor: every block's
+    rows are what dit_attn_ring writes for it, and the gaps stay untouched."""
+    import sequence_attention_gb300 as sa
+    rng = np.random.default_rng(1000 + seed)
+    B, H = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+    D = int(rng.choice([64, 128]))
+    n_q, n_kv = int(rng.integers(1, 5)), int(rng.integers(1, 5))
+    q_lens = [int(x) for x in rng.integers(0, 300, size=n_q)]
+    kv_lens = [int(x) for x in rng.integers(0, 400, size=n_kv)]
+    if sum(q_lens) == 0:
+        q_lens[0] = 1
+    gaps = [int(x) for x in rng.integers(0, 5, size=n_q + 1)]
+    row0, at = [], gaps[0]
+    for r in range(n_q):
+        row0.append(at)
+        at += q_lens[r] + gaps[r + 1]
+    cq, ck = max(max(q_lens), 1), max(max(kv_lens), 1)
+    q = synth.normal((n_q, B, cq, H, D), 2000 + seed, 0.5, "bf16").cuda()
+    k = synth.normal((n_kv, B, ck, H, D), 3000 + seed, 0.5, "bf16").cuda()
+    v = synth.normal((n_kv, B, ck, H, D), 4000 + seed, 0.5, "f16").cuda()
+    ref = torch.full((n_q, B, cq, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sa.dit_attn_ring(q, k, v, ref, None, q_lens, kv_lens)
+    out = torch.full((B, at, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sa.dit_attn_ring_rows(q, k, v, out, row0, None, q_lens, kv_lens)
+    torch.cuda.synchronize()
+    written = torch.zeros(at, dtype=torch.bool)
+    for r in range(n_q):
+        L = q_lens[r]
+        np.testing.assert_array_equal(bits(out[:, row0[r]:row0[r] + L]), bits(ref[r, :, :L]))
+        written[row0[r]:row0[r] + L] = True
+    assert torch.isnan(out[:, ~written.cuda()].float()).all()
