@@ -142,4 +142,25 @@ __device__ __forceinline__ void copy8(void* dst, const void* src, dit_dtype t) {
     if (t == DIT_F32) d[1] = s[1];
 }
 
+// Unsigned division by a divisor fixed at launch, as a multiply-high and a
+// shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): with s = ceil(log2 d) and m = floor(2^32 (2^s - d)
+// / d) + 1, n / d = (mulhi(n, m) + n) >> s for every n < 2^31.
+struct FastDiv {
+    uint32_t d, m, s;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.s = 0;
+    while ((1ull << f.s) < d) ++f.s;
+    f.m = (uint32_t)(((1ull << 32) * ((1ull << f.s) - d)) / d + 1);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+    return (uint32_t)(((unsigned long long)__umulhi(n, f.m) + n) >> f.s);
+}
+
 }  // namespace ditsp

@@ -210,6 +210,153 @@ dit_status launch_direct(DirectArgs& a, cudaStream_t st, const char* who) {
     return launch_direct_sized<S2H, 2, 4, ROPE>(a, st, who);
 }
 
+// ---- the three-call path's seq -> head unpack, one head-layout row per warp
+// Head-layout row (plane p, ring block r, batch b, row t - ring_off[r]) holds
+// Hp heads that arrive as U runs of the receive wire (order B): run v is
+// head_len[v] heads of D elements at slot slots_B(p, b, t, v).  With U <= 32
+// lane v keeps run v's start, less head_off[v]*D, so chunk c (8 elements,
+// c*8 into the row) reads wire element base(v(c)) + c*8, with v(c) the group
+// of head c*8/D (a multiply-shift division when every group has Hl heads);
+// with more ranks each chunk computes its run's start itself.  Chunks of real
+// heads of real rows are rotated when the plane is; the rest are copied
+// (zeros on the wire).  Same arithmetic as the run-walking unpack, so the
+// same bits.
+struct WireArgs {
+    dit_sp_layout L;
+    int np;
+    const char* wire;
+    char* head[3];
+    dit_dtype src_dt, dst_dt[3];
+    int* range_flag;
+    const float* cos_tab;
+    const float* sin_tab;
+    unsigned rope_planes;
+    long long nrows;             // np * B * S_pad
+    int cpr;                     // chunks per head-layout row (Hp * D / 8)
+    int creal;                   // chunks of real heads (H * D / 8)
+    FastDiv head_of;             // chunk -> head (D / 8 chunks a head)
+    FastDiv group_of;            // head -> group when every group has Hl heads
+    int even;
+};
+
+template <int SB, int DB, bool ROPE>
+__global__ void __launch_bounds__(kDirThreads, SB == 2 ? 3 : 1) wire_unpack_kernel(const __grid_constant__ WireArgs A) {
+    __shared__ float4 tab_sm[ROPE ? kDirThreads / 32 : 1][ROPE ? kDirMaxRopeD / 4 : 1];
+    const dit_sp_layout& L = A.L;
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const long long row = (long long)blockIdx.x * (kDirThreads / 32) + wib;
+    pdl_wait();
+    if (row >= A.nrows) {      // no block barrier below: a warp may leave
+        pdl_trigger();
+        return;
+    }
+    const long long per_plane = (long long)L.B * L.S_pad;
+    const int p = (int)(row / per_plane);
+    const long long rem = row - p * per_plane;
+    const int b = (int)(rem / L.S_pad), t = (int)(rem - (long long)b * L.S_pad);
+    Run x;
+    const int rid = rank_of_row(L, t);
+    x.r = rid / L.U;
+    x.u = rid - x.r * L.U;
+    x.p = p;
+    x.b = b;
+    x.i = t - L.rank_off[rid];
+    char* dst = A.head[p] + ((((long long)x.r * L.B + b) * L.S_cap + (t - L.ring_off[x.r])) * L.Hp) * L.D * DB;
+    long long base = 0;        // lane v: run v's first wire element, less head_off[v] * D
+    if (lane < L.U && lane < 32) {
+        x.v = lane;
+        base = slots_B(L, A.np, x) * L.D - (long long)L.head_off[lane] * L.D;
+    }
+    const dit_dtype sdt = A.src_dt, ddt = A.dst_dt[p];
+    const bool rot = ROPE && t < L.S && ((A.rope_planes >> p) & 1u);
+    const int rlim = rot ? A.creal : 0;          // chunks rotated
+    const bool want_check = A.range_flag != nullptr && narrowing(sdt, ddt);
+    const bool want_check_rot = A.range_flag != nullptr && ddt != DIT_F32;
+    bool overflow = false;
+    const int q4 = L.D >> 3;
+    if (ROPE && rot) {
+        const float4* ct = reinterpret_cast<const float4*>(A.cos_tab + (long long)t * (L.D >> 1));
+        const float4* sn = reinterpret_cast<const float4*>(A.sin_tab + (long long)t * (L.D >> 1));
+        for (int j = lane; j < 2 * q4; j += 32) cp_async16(&tab_sm[wib][j], j < q4 ? ct + j : sn + (j - q4));
+        cp_async_commit();
+    }
+    constexpr int NI = kDirItems;
+    for (int c0 = 0; c0 < A.cpr; c0 += 32 * NI) {        // every lane runs the same batches
+        uint4 raw[NI][SB / 2];
+#pragma unroll
+        for (int k = 0; k < NI; ++k) {
+            const int c = c0 + lane + 32 * k;
+            const int h = (int)fdiv((uint32_t)min(c, A.cpr - 1), A.head_of);
+            int v;
+            if (A.even) {
+                v = (int)fdiv((uint32_t)h, A.group_of);
+            } else {
+                int lo = 0, hi = L.U - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (L.head_off[mid] <= h) lo = mid; else hi = mid - 1;
+                }
+                v = lo;
+            }
+            long long src;
+            if (L.U <= 32) {                                 // warp-uniform
+                src = __shfl_sync(0xffffffffu, base, v);
+            } else {
+                Run y = x;
+                y.v = v;
+                src = slots_B(L, A.np, y) * L.D - (long long)L.head_off[v] * L.D;
+            }
+#pragma unroll
+            for (int e = 0; e < SB / 2; ++e) raw[k][e] = make_uint4(0, 0, 0, 0);
+            if (c < A.cpr) {
+                const uint4* g = reinterpret_cast<const uint4*>(A.wire + (src + (long long)c * 8) * SB);
+#pragma unroll
+                for (int e = 0; e < SB / 2; ++e) raw[k][e] = g[e];
+            }
+        }
+        if (ROPE && rot && c0 == 0) {
+            cp_async_wait_all();
+            __syncwarp();
+        }
+#pragma unroll
+        for (int k = 0; k < NI; ++k) {
+            const int c = c0 + lane + 32 * k;
+            if (c >= A.cpr) break;
+            uint4 o[DB / 2];
+            if (ROPE && c < rlim) {
+                const int i4 = c - (int)fdiv((uint32_t)c, A.head_of) * q4;
+                rope8<SB, DB>(raw[k], sdt, ddt, tab_sm[wib][i4], tab_sm[wib][q4 + i4], want_check_rot, o, overflow);
+            } else {
+                convert8<SB, DB>(raw[k], sdt, ddt, want_check, o, overflow);
+            }
+            uint4* d = reinterpret_cast<uint4*>(dst + (long long)c * 8 * DB);
+#pragma unroll
+            for (int e = 0; e < DB / 2; ++e) d[e] = o[e];
+        }
+    }
+    if (ROPE && rot) __syncwarp();
+    if (overflow) *A.range_flag = (int)DIT_ERR_RANGE;
+    pdl_trigger();
+}
+
+template <int SB, int DB, bool ROPE>
+dit_status launch_wire(const WireArgs& a, cudaStream_t st, const char* who) {
+    const long long blocks = (a.nrows + kDirThreads / 32 - 1) / (kDirThreads / 32);
+    if (blocks >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: too many rows", who);
+    cudaError_t e = launch_pdl(wire_unpack_kernel<SB, DB, ROPE>, dim3((unsigned)blocks), dim3(kDirThreads), 0, st, a);
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
+    return check_launch(who);
+}
+
+template <bool ROPE>
+dit_status launch_wire_typed(const WireArgs& a, cudaStream_t st, const char* who) {
+    const int sb = dtype_bytes(a.src_dt), db = dtype_bytes(a.dst_dt[0]);
+    if (sb == 2 && db == 2) return launch_wire<2, 2, ROPE>(a, st, who);
+    if (sb == 4 && db == 4) return launch_wire<4, 4, ROPE>(a, st, who);
+    if (sb == 4 && db == 2) return launch_wire<4, 2, ROPE>(a, st, who);
+    return launch_wire<2, 4, ROPE>(a, st, who);
+}
+
 // Checks shared by both directions: the sequence-side pointer pair of
 // plane p given split (0: one tensor).
 dit_status seq_pair_ok(const void* s, const void* s2, int split, int S, const char* who, int p) {
@@ -220,6 +367,44 @@ dit_status seq_pair_ok(const void* s, const void* s2, int split, int S, const ch
 }
 
 }  // namespace
+
+// The three-call seq -> head unpack (16/32-bit wire), optional RoPE: see
+// wire_unpack_kernel.  Arguments are validated by the callers.
+dit_status wire_unpack_s2h(const dit_sp_layout* L, int nplanes, const void* recv, dit_dtype wire_dt,
+                           void* const* dst, const dit_dtype* dst_dt, const float* cos_tab, const float* sin_tab,
+                           unsigned rope_planes, int* range_flag, cudaStream_t st, const char* who) {
+    const int db = dtype_bytes(dst_dt[0]);
+    for (int p = 1; p < nplanes; ++p)
+        if (dtype_bytes(dst_dt[p]) != db)
+            return fail(DIT_ERR_UNSUPPORTED, "%s: planes of one call need destination types of one size", who);
+    if (rope_planes && L->D > kDirMaxRopeD)
+        return fail(DIT_ERR_UNSUPPORTED, "%s: the rotary path supports D <= %d", who, kDirMaxRopeD);
+    if (L->U > 64) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 64 Ulysses ranks", who);
+    WireArgs a;
+    memset(&a, 0, sizeof(a));
+    a.L = *L;
+    a.np = nplanes;
+    a.wire = static_cast<const char*>(recv);
+    for (int p = 0; p < nplanes; ++p) {
+        a.head[p] = static_cast<char*>(dst[p]);
+        a.dst_dt[p] = dst_dt[p];
+    }
+    a.src_dt = wire_dt;
+    a.range_flag = range_flag;
+    a.cos_tab = cos_tab;
+    a.sin_tab = sin_tab;
+    a.rope_planes = rope_planes;
+    a.nrows = (long long)nplanes * L->B * L->S_pad;
+    a.cpr = (int)(((long long)L->Hp * L->D) >> 3);
+    a.creal = (int)(((long long)L->H * L->D) >> 3);
+    a.head_of = make_fastdiv((uint32_t)(L->D >> 3));
+    a.even = 1;
+    for (int v = 0; v < L->U; ++v) a.even &= L->head_len[v] == L->Hl && L->head_off[v] == v * L->Hl;
+    a.group_of = make_fastdiv((uint32_t)(L->Hl > 0 ? L->Hl : 1));
+    if (a.nrows == 0) return DIT_OK;
+    return rope_planes ? launch_wire_typed<true>(a, st, who) : launch_wire_typed<false>(a, st, who);
+}
+
 }  // namespace ditsp
 
 using namespace ditsp;

@@ -180,6 +180,13 @@ dit_status check_layout(const dit_sp_layout* L, const char* who);
 dit_status fp8_pack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, const void* const* src,
                     const void* const* src2, int split, dit_dtype src_dt, void* send, cudaStream_t st,
                     const char* who);
+// The three-call seq -> head unpack of a 16/32-bit wire into head-layout
+// planes, one head-layout row per warp, optional RoPE on rope_planes
+// (direct.cu).  Arguments are validated by the callers except the plane
+// types' sizes and the rotary head dim.
+dit_status wire_unpack_s2h(const dit_sp_layout* L, int nplanes, const void* recv, dit_dtype wire_dt,
+                           void* const* dst, const dit_dtype* dst_dt, const float* cos_tab, const float* sin_tab,
+                           unsigned rope_planes, int* range_flag, cudaStream_t st, const char* who);
 dit_status fp8_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, const void* recv, void* const* dst,
                       void* const* dst2, int split, const dit_dtype* dst_dt, const float* cos_tab,
                       const float* sin_tab, unsigned rope_planes, int* range_flag, cudaStream_t st,

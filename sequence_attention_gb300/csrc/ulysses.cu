@@ -35,7 +35,8 @@
 namespace ditsp {
 namespace {
 
-enum Mode { PACK_S2H = 0, UNPACK_H2S, PACK_H2S, UNPACK_S2H, A2A_S2H, A2A_H2S };
+// The seq -> head unpack is the row-per-warp wire_unpack_s2h (direct.cu).
+enum Mode { PACK_S2H = 0, UNPACK_H2S, PACK_H2S, A2A_S2H, A2A_H2S };
 
 struct RunArgs {
     dit_sp_layout L;
@@ -56,11 +57,6 @@ struct RunArgs {
     const void* src2[3];
     void* dst2[3];
     int split;
-    // rotary embedding of the seq->head unpack: tables [S][D/2] (fp32),
-    // applied to plane p when bit p of rope_planes is set
-    const float* rope_cos;
-    const float* rope_sin;
-    unsigned rope_planes;
 };
 
 __device__ __forceinline__ unsigned long long gtimer_ns() {
@@ -88,8 +84,6 @@ struct RunIO {
     int dst_lim;      // chunks of the destination written; later chunks skipped
     int sdt, ddt;     // dit_dtype of source and destination
     int sender;       // virtual rank that sent this run (exchange kernels)
-    int rope_pos;     // joint-sequence position whose angles rotate the run; -1: none
-    int rot_lim;      // chunks of the run that are rotated (real heads; padded heads stay +0)
 };
 
 template <int MODE>
@@ -99,7 +93,6 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
     // consecutive runs write consecutive memory.
     Run x;
     if (MODE == PACK_S2H || MODE == A2A_H2S) x = decode_A(L, A.np, ri);
-    else if (MODE == UNPACK_S2H) x = decode_H(L, A.np, ri);
     else if (MODE == UNPACK_H2S) x = decode_S(L, ri);
     else x = decode_B(L, A.np, ri);
     const int p = x.p;
@@ -111,8 +104,6 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
     const int full = (L.head_len[x.v] * L.D) >> 3, real = (nreal * L.D) >> 3;
     RunIO io;
     io.src_lim = io.dst_lim = full;
-    io.rope_pos = -1;
-    io.rot_lim = real;
     long long so = 0, doff = 0;
     dit_dtype sdt, ddt;
     bool second = false;
@@ -131,12 +122,6 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
         so = head_offset(L, x); doff = slots_B(L, A.np, x) * D;
         io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[0];
         io.src_lim = real;
-    } else if (MODE == UNPACK_S2H) {
-        sdt = A.src_dt[0]; ddt = A.dst_dt[p];
-        so = slots_B(L, A.np, x) * D; doff = head_offset(L, x);
-        io.src = (const char*)A.src[0]; io.dst = (char*)A.dst[p];
-        // the angle tables have S rows: padding rows are not rotated
-        if (((A.rope_planes >> p) & 1u) && !pad_row) io.rope_pos = run_row(L, x);
     } else if (MODE == A2A_S2H) {
         sdt = ddt = A.src_dt[0];
         so = slots_A(L, A.np, x) * D; doff = slots_B(L, A.np, x) * D;
@@ -158,9 +143,6 @@ __device__ __forceinline__ RunIO run_io(const RunArgs& A, int ri) {
 
 
 constexpr int kThreads = 256;
-// the rotary path stages 64 runs x 2 x D/2 floats in shared memory (96 KB
-// at D = 384, with the opt-in above 48 KB)
-constexpr int kRopeMaxD = 384;
 constexpr int kItems = 8;       // 8-element items per lane in flight
 
 // Each block takes 8 * rpw consecutive runs (rpw = runs per warp, 4, or 2
@@ -168,17 +150,9 @@ constexpr int kItems = 8;       // 8-element items per lane in flight
 // one run each into shared memory, then each warp streams its rpw runs,
 // lanes over their 8-element chunks.  Per group of kItems items a lane
 // issues every load first, converts in registers, then stores.
-// The rotary variant is held to three blocks per SM (80 registers, 8 bytes
-// of spill for 16-bit types): on the Wan-like shape it moves 4.2 TB/s that
-// way against 2.9 TB/s at two blocks per SM without the cap.
-template <int MODE, int SB, int DB, bool ROPE>
-__global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __grid_constant__ RunArgs A, int rpw) {
+template <int MODE, int SB, int DB>
+__global__ void __launch_bounds__(kThreads, 1) run_kernel(const __grid_constant__ RunArgs A, int rpw) {
     __shared__ RunIO ios[kThreads];
-    // rotary path: each run's table rows (cos, then sin; D/8 float4 each),
-    // loaded once per distinct token of the block; slot[] = the run whose
-    // rows a run uses
-    extern __shared__ float4 rope_sm[];
-    __shared__ short slot[ROPE ? kThreads : 1];
     const int rpb = rpw * (kThreads / 32);
     const long long r0 = (long long)blockIdx.x * rpb;
     const int nrun = (int)min((long long)rpb, A.nruns - r0);
@@ -210,40 +184,15 @@ __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __gri
         else __threadfence();
     }
     __syncthreads();
-    const int dch = A.L.D >> 3;          // chunks per head = float4s per table row
-    if constexpr (ROPE) {
-        // Runs of one token are adjacent (head groups innermost): the first
-        // run of each token copies its table rows into shared memory with
-        // asynchronous copies, which land while the first data loads below
-        // are in flight.
-        const int t = threadIdx.x;
-        if (t < nrun) {
-            const int pos = ios[t].rope_pos;
-            int l = t;
-            while (l > 0 && ios[l - 1].rope_pos == pos) --l;
-            slot[t] = (short)l;
-            if (pos >= 0 && l == t) {
-                const float* cs = A.rope_cos + (long long)pos * (A.L.D >> 1);
-                const float* sn = A.rope_sin + (long long)pos * (A.L.D >> 1);
-                for (int c = 0; c < dch; ++c) {
-                    cp_async16(&rope_sm[(2 * t) * dch + c], cs + 4 * c);
-                    cp_async16(&rope_sm[(2 * t + 1) * dch + c], sn + 4 * c);
-                }
-            }
-        }
-        cp_async_commit();
-    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g0 = warp * rpw;
     const int gn = min(rpw, nrun - g0);
-    if (!ROPE && gn <= 0) {   // the rotary variant's warps all reach its barrier
+    if (gn <= 0) {
         pdl_trigger();
         return;
     }
     const int nch = (A.L.Hl * A.L.D) >> 3;
     const int items = gn > 0 ? gn * nch : 0;
-    const bool want_check = (MODE == UNPACK_S2H) && A.range_flag != nullptr;
-    bool overflow = false;
     constexpr int NI = kItems;
     int g = lane / nch, c = lane - (lane / nch) * nch;   // item k0 = lane
     uint4 raw[NI][SB / 2];
@@ -281,14 +230,8 @@ __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __gri
                 if (ci < io.dst_lim) {
                     const dit_dtype sdt = (dit_dtype)io.sdt, ddt = (dit_dtype)io.ddt;
                     uint4 o[DB / 2];
-                    if (ROPE && io.rope_pos >= 0 && ci < io.rot_lim) {
-                        const int sl = slot[ROPE ? g0 + gi : 0], cc = ci % dch;
-                        rope8<SB, DB>(raw[t], sdt, ddt, rope_sm[(2 * sl) * dch + cc],
-                                      rope_sm[(2 * sl + 1) * dch + cc], want_check && ddt != DIT_F32, o,
-                                      overflow);
-                    } else {
-                        convert8<SB, DB>(raw[t], sdt, ddt, want_check && narrowing(sdt, ddt), o, overflow);
-                    }
+                    bool unused = false;     // no narrowing to check off the seq -> head unpack
+                    convert8<SB, DB>(raw[t], sdt, ddt, false, o, unused);
                     uint4* q = reinterpret_cast<uint4*>(io.dst + (long long)ci * 8 * DB);
 #pragma unroll
                     for (int h = 0; h < DB / 2; ++h) q[h] = o[h];
@@ -296,29 +239,14 @@ __global__ void __launch_bounds__(kThreads, ROPE ? 3 : 1) run_kernel(const __gri
             }
         }
     };
-    if constexpr (ROPE) {
-        // the first batch of data loads is issued before the barrier that
-        // publishes the table rows
-        int k0 = lane;
+    for (int k0 = lane; k0 < items; k0 += 32 * NI) {
         load_batch(k0);
-        cp_async_wait_all();
-        __syncthreads();
-        while (k0 < items) {
-            store_batch(k0);
-            k0 += 32 * NI;
-            if (k0 < items) load_batch(k0);
-        }
-    } else {
-        for (int k0 = lane; k0 < items; k0 += 32 * NI) {
-            load_batch(k0);
-            store_batch(k0);
-        }
+        store_batch(k0);
     }
-    if (overflow) *A.range_flag = (int)DIT_ERR_RANGE;
     pdl_trigger();
 }
 
-template <int MODE, int SB, int DB, bool ROPE>
+template <int MODE, int SB, int DB>
 dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
     // Up to 8 runs per warp (64 per block): measured on the FLUX-like step
     // against 1, 2, 3, 4, 6, 12, 16, 24 and 32, 8 gives the shortest layout
@@ -329,14 +257,7 @@ dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
     long long fit = a.nruns / (16LL * num_sms());
     const int rpw = fit < 1 ? 1 : (fit > 8 ? 8 : (int)fit);
     const long long blocks = (a.nruns + 8LL * rpw - 1) / (8LL * rpw);
-    // rotary tables: two rows of D/2 floats for each of the block's runs
-    const size_t smem = ROPE ? (size_t)8 * rpw * a.L.D * sizeof(float) : 0;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(run_kernel<MODE, SB, DB, ROPE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: %s", who, cudaGetErrorString(e));
-    }
-    cudaError_t e = launch_pdl(run_kernel<MODE, SB, DB, ROPE>, dim3((unsigned)blocks), dim3(kThreads), smem, st, a, rpw);
+    cudaError_t e = launch_pdl(run_kernel<MODE, SB, DB>, dim3((unsigned)blocks), dim3(kThreads), 0, st, a, rpw);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     return check_launch(who);
 }
@@ -344,7 +265,7 @@ dit_status launch_sized(const RunArgs& a, cudaStream_t st, const char* who) {
 // Element sizes are template parameters so that 16-bit paths hold 16-byte
 // items; every plane of one call must use source (and destination) types
 // of one size.
-template <int MODE, bool ROPE = false>
+template <int MODE>
 dit_status launch_runs(const RunArgs& a, cudaStream_t st, const char* who) {
     if (a.nruns == 0) return DIT_OK;
     if (a.nruns >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 2^31 runs", who);
@@ -358,10 +279,10 @@ dit_status launch_runs(const RunArgs& a, cudaStream_t st, const char* who) {
         if (a.dst[p] && dtype_bytes(a.dst_dt[p]) != db)
             return fail(DIT_ERR_UNSUPPORTED, "%s: planes of one call need destination types of one size", who);
     }
-    if (sb == 2 && db == 2) return launch_sized<MODE, 2, 2, ROPE>(a, st, who);
-    if (sb == 4 && db == 4) return launch_sized<MODE, 4, 4, ROPE>(a, st, who);
-    if (sb == 4 && db == 2) return launch_sized<MODE, 4, 2, ROPE>(a, st, who);
-    return launch_sized<MODE, 2, 4, ROPE>(a, st, who);
+    if (sb == 2 && db == 2) return launch_sized<MODE, 2, 2>(a, st, who);
+    if (sb == 4 && db == 4) return launch_sized<MODE, 4, 4>(a, st, who);
+    if (sb == 4 && db == 2) return launch_sized<MODE, 4, 2>(a, st, who);
+    return launch_sized<MODE, 2, 4>(a, st, who);
 }
 
 }  // namespace
@@ -502,7 +423,9 @@ extern "C" dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir
     cudaStream_t st = (cudaStream_t)stream;
     if (wire_dt == DIT_E4M3)
         return fp8_unpack(L, dir, nplanes, recv, dst, nullptr, 0, dst_dt, nullptr, nullptr, 0, d_range_flag, st, who);
-    return dir == DIT_SEQ_TO_HEAD ? launch_runs<UNPACK_S2H>(a, st, who) : launch_runs<UNPACK_H2S>(a, st, who);
+    if (dir == DIT_SEQ_TO_HEAD)
+        return wire_unpack_s2h(L, nplanes, recv, wire_dt, dst, dst_dt, nullptr, nullptr, 0, d_range_flag, st, who);
+    return launch_runs<UNPACK_H2S>(a, st, who);
 }
 
 extern "C" dit_status dit_sp_signal(const dit_sp_layout* L, unsigned* d_arrival, const unsigned char* rank_mask,
@@ -635,8 +558,6 @@ extern "C" dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplane
     if (!wire_ok(wire_dt)) return fail(DIT_ERR_INVALID_ARG, "%s: bad wire dtype", who);
     if (nplanes < 1 || nplanes > 3) return fail(DIT_ERR_INVALID_ARG, "%s: nplanes must be 1..3", who);
     if (rope_planes >> nplanes) return fail(DIT_ERR_INVALID_ARG, "%s: rope_planes names a missing plane", who);
-    if (rope_planes && L->D > kRopeMaxD && wire_dt != DIT_E4M3)
-        return fail(DIT_ERR_UNSUPPORTED, "%s: rotary path supports D <= %d", who, kRopeMaxD);
     if (!dst_dt) return fail(DIT_ERR_INVALID_ARG, "%s: dst_dt NULL", who);
     for (int p = 0; p < nplanes; ++p)
         if (!dtype_ok(dst_dt[p])) return fail(DIT_ERR_INVALID_ARG, "%s: bad dst dtype", who);
@@ -645,24 +566,12 @@ extern "C" dit_status dit_ulysses_unpack_rope(const dit_sp_layout* L, int nplane
         return fail(DIT_ERR_INVALID_ARG, "%s: rotary tables NULL or misaligned", who);
     if (!recv || !aligned16(recv) || !dst)
         return fail(DIT_ERR_INVALID_ARG, "%s: recv/dst NULL or misaligned", who);
-    RunArgs a;
-    memset(&a, 0, sizeof(a));
-    a.L = *L;
-    a.np = nplanes;
-    a.src[0] = recv; a.src_dt[0] = wire_dt;
-    for (int p = 0; p < nplanes; ++p) {
+    for (int p = 0; p < nplanes; ++p)
         if (!dst[p] || !aligned16(dst[p])) return fail(DIT_ERR_INVALID_ARG, "%s: dst[%d] NULL or misaligned", who, p);
-        a.dst[p] = dst[p];
-        a.dst_dt[p] = dst_dt[p];
-    }
-    a.range_flag = d_range_flag;
-    a.rope_cos = cos_tab;
-    a.rope_sin = sin_tab;
-    a.rope_planes = rope_planes;
-    a.nruns = (long long)nplanes * L->B * L->U * L->S_pad;
     cudaStream_t st = (cudaStream_t)stream;
     if (wire_dt == DIT_E4M3)
         return fp8_unpack(L, DIT_SEQ_TO_HEAD, nplanes, recv, dst, nullptr, 0, dst_dt, cos_tab, sin_tab, rope_planes,
                           d_range_flag, st, who);
-    return rope_planes ? launch_runs<UNPACK_S2H, true>(a, st, who) : launch_runs<UNPACK_S2H>(a, st, who);
+    return wire_unpack_s2h(L, nplanes, recv, wire_dt, dst, dst_dt, cos_tab, sin_tab, rope_planes, d_range_flag, st,
+                           who);
 }
