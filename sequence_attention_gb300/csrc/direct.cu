@@ -357,6 +357,105 @@ dit_status launch_wire_typed(const WireArgs& a, cudaStream_t st, const char* who
     return launch_wire<2, 4, ROPE>(a, st, who);
 }
 
+// ---- the three-call path's seq -> head exchange, one sequence row per warp
+// Row (plane p, batch b, padded-sequence row t) of the send wire (order A)
+// holds U runs, run v at slots_A(p, b, t, v); the exchange copies each to
+// slots_B(p, b, t, v) of the receive wire (order B).  Lane v keeps both
+// starts less head_off[v]*D, so chunk c of the row (8 elements) moves from
+// src(v(c)) + c*8 to dst(v(c)) + c*8, v(c) found as in wire_unpack_kernel.
+// A raw copy (e4m3 records travel as (D + 16) / 2 16-bit words).
+struct CopyArgs {
+    dit_sp_layout L;             // D = elements (or 16-bit words) a head slot
+    int np;
+    const char* src;
+    char* dst;
+    long long nrows;             // np * B * S_pad
+    int cpr;                     // chunks per row (Hp * D / 8)
+    FastDiv head_of;
+    FastDiv group_of;
+    int even;
+};
+
+template <int EB>
+__global__ void __launch_bounds__(kDirThreads, EB == 2 ? 3 : 1) wire_a2a_kernel(const __grid_constant__ CopyArgs A) {
+    const dit_sp_layout& L = A.L;
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * (kDirThreads / 32) + (threadIdx.x >> 5);
+    pdl_wait();
+    if (row >= A.nrows) {
+        pdl_trigger();
+        return;
+    }
+    const long long per_plane = (long long)L.B * L.S_pad;
+    const int p = (int)(row / per_plane);
+    const long long rem = row - p * per_plane;
+    const int b = (int)(rem / L.S_pad), t = (int)(rem - (long long)b * L.S_pad);
+    Run x;
+    const int rid = rank_of_row(L, t);
+    x.r = rid / L.U;
+    x.u = rid - x.r * L.U;
+    x.p = p;
+    x.b = b;
+    x.i = t - L.rank_off[rid];
+    long long sa = 0, sb = 0;  // lane v: run v's starts on both wires, less head_off[v] * D
+    if (lane < L.U && lane < 32) {
+        x.v = lane;
+        const long long back = (long long)L.head_off[lane] * L.D;
+        sa = slots_A(L, A.np, x) * L.D - back;
+        sb = slots_B(L, A.np, x) * L.D - back;
+    }
+    constexpr int NI = kDirItems;
+    for (int c0 = 0; c0 < A.cpr; c0 += 32 * NI) {
+        uint4 raw[NI][EB / 2];
+        long long to[NI];
+#pragma unroll
+        for (int k = 0; k < NI; ++k) {
+            const int c = c0 + lane + 32 * k;
+            const int h = (int)fdiv((uint32_t)min(c, A.cpr - 1), A.head_of);
+            int v;
+            if (A.even) {
+                v = (int)fdiv((uint32_t)h, A.group_of);
+            } else {
+                int lo = 0, hi = L.U - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (L.head_off[mid] <= h) lo = mid; else hi = mid - 1;
+                }
+                v = lo;
+            }
+            long long from;
+            if (L.U <= 32) {                                 // warp-uniform
+                from = __shfl_sync(0xffffffffu, sa, v);
+                to[k] = __shfl_sync(0xffffffffu, sb, v);
+            } else {
+                Run y = x;
+                y.v = v;
+                const long long back = (long long)L.head_off[v] * L.D;
+                from = slots_A(L, A.np, y) * L.D - back;
+                to[k] = slots_B(L, A.np, y) * L.D - back;
+            }
+            from += (long long)c * 8;
+            to[k] += (long long)c * 8;
+#pragma unroll
+            for (int e = 0; e < EB / 2; ++e) raw[k][e] = make_uint4(0, 0, 0, 0);
+            if (c < A.cpr) {
+                const uint4* g = reinterpret_cast<const uint4*>(A.src + from * EB);
+#pragma unroll
+                for (int e = 0; e < EB / 2; ++e) raw[k][e] = g[e];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NI; ++k) {
+            const int c = c0 + lane + 32 * k;
+            if (c >= A.cpr) break;
+            uint4* d = reinterpret_cast<uint4*>(A.dst + to[k] * EB);
+#pragma unroll
+            for (int e = 0; e < EB / 2; ++e) d[e] = raw[k][e];
+        }
+    }
+    pdl_trigger();
+}
+
 // Checks shared by both directions: the sequence-side pointer pair of
 // plane p given split (0: one tensor).
 dit_status seq_pair_ok(const void* s, const void* s2, int split, int S, const char* who, int p) {
@@ -367,6 +466,32 @@ dit_status seq_pair_ok(const void* s, const void* s2, int split, int S, const ch
 }
 
 }  // namespace
+
+// The three-call seq -> head exchange: see wire_a2a_kernel.  Lw is the
+// layout with D = the head slot's width in units of eb bytes (2 or 4).
+dit_status wire_a2a_s2h(const dit_sp_layout* Lw, int nplanes, const void* send, void* recv, int eb,
+                        cudaStream_t st, const char* who) {
+    if (Lw->U > 64) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 64 Ulysses ranks", who);
+    CopyArgs a;
+    memset(&a, 0, sizeof(a));
+    a.L = *Lw;
+    a.np = nplanes;
+    a.src = static_cast<const char*>(send);
+    a.dst = static_cast<char*>(recv);
+    a.nrows = (long long)nplanes * Lw->B * Lw->S_pad;
+    a.cpr = (int)(((long long)Lw->Hp * Lw->D) >> 3);
+    a.head_of = make_fastdiv((uint32_t)(Lw->D >> 3));
+    a.even = 1;
+    for (int v = 0; v < Lw->U; ++v) a.even &= Lw->head_len[v] == Lw->Hl && Lw->head_off[v] == v * Lw->Hl;
+    a.group_of = make_fastdiv((uint32_t)(Lw->Hl > 0 ? Lw->Hl : 1));
+    if (a.nrows == 0) return DIT_OK;
+    const long long blocks = (a.nrows + kDirThreads / 32 - 1) / (kDirThreads / 32);
+    if (blocks >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: too many rows", who);
+    cudaError_t e = eb == 4 ? launch_pdl(wire_a2a_kernel<4>, dim3((unsigned)blocks), dim3(kDirThreads), 0, st, a)
+                            : launch_pdl(wire_a2a_kernel<2>, dim3((unsigned)blocks), dim3(kDirThreads), 0, st, a);
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
+    return check_launch(who);
+}
 
 // The three-call seq -> head unpack (16/32-bit wire), optional RoPE: see
 // wire_unpack_kernel.  Arguments are validated by the callers.

@@ -180,6 +180,11 @@ dit_status check_layout(const dit_sp_layout* L, const char* who);
 dit_status fp8_pack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, const void* const* src,
                     const void* const* src2, int split, dit_dtype src_dt, void* send, cudaStream_t st,
                     const char* who);
+// The three-call seq -> head exchange as a copy of each sequence row's U runs
+// from send order A to receive order B (direct.cu); Lw->D is the head slot's
+// width in units of eb (2 or 4) bytes.
+dit_status wire_a2a_s2h(const dit_sp_layout* Lw, int nplanes, const void* send, void* recv, int eb,
+                        cudaStream_t st, const char* who);
 // The three-call seq -> head unpack of a 16/32-bit wire into head-layout
 // planes, one head-layout row per warp, optional RoPE on rope_planes
 // (direct.cu).  Arguments are validated by the callers except the plane

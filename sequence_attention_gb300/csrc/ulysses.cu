@@ -388,7 +388,8 @@ extern "C" dit_status dit_a2a_sim(const dit_sp_layout* L, dit_a2a_dir dir, int n
     a.nruns = (long long)nplanes * L->B * L->U * L->S_pad;
     if (wire_dt == DIT_E4M3 && (s = record_words(&a, who)) != DIT_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
-    return dir == DIT_SEQ_TO_HEAD ? launch_runs<A2A_S2H>(a, st, who) : launch_runs<A2A_H2S>(a, st, who);
+    if (dir == DIT_SEQ_TO_HEAD) return wire_a2a_s2h(&a.L, nplanes, send, recv, dtype_bytes(a.src_dt[0]), st, who);
+    return launch_runs<A2A_H2S>(a, st, who);
 }
 
 extern "C" dit_status dit_ulysses_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes,
