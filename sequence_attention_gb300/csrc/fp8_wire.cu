@@ -11,23 +11,26 @@
 // destination type (and, in the receive preparation, the RoPE rotation of the
 // float32 values before that rounding).
 //
-// Kernels walk the same runs (Hl heads of one (plane, batch, row)) in the
-// same destination orders as the 16-bit permutation kernels; a block decodes
-// 32 runs into shared memory, each warp then covers its runs' heads with
-// D/32 lanes per head, so the head's amax is a shuffle
-// reduction inside an aligned group of lanes (32 values per lane; 16 when
-// D = 16).  The exchange between the
-// pack and the unpack is the 16-bit permutation kernel on records seen as
-// (D + 16) / 2 words.
+// The packs and the head -> seq unpack walk the same runs (Hl heads of one
+// (plane, batch, row)) in the same destination orders as the 16-bit
+// permutation kernels; a block decodes its runs into shared memory, each warp
+// then covers its runs' heads with D/32 lanes per head, so the head's amax is
+// a shuffle reduction inside an aligned group of lanes (32 values per lane;
+// 16 when D = 16).  The seq -> head unpack takes one head-layout row per
+// warp, a lane 8 values of one head at a time (fp8_unpack_rows_kernel).  The
+// exchange between the pack and the unpack is the 16-bit exchange on records
+// seen as (D + 16) / 2 words.
 #include <cuda_fp8.h>
 #include <string.h>
 
+#include "convert.cuh"
 #include "sp_index.cuh"
 
 namespace ditsp {
 namespace {
 
-enum Fp8Mode { Q_PACK_S2H = 0, Q_PACK_H2S, DQ_UNPACK_S2H, DQ_UNPACK_H2S };
+// The seq -> head decoding unpack is fp8_unpack_rows_kernel (below).
+enum Fp8Mode { Q_PACK_S2H = 0, Q_PACK_H2S, DQ_UNPACK_H2S };
 
 constexpr int kThreads = 256;
 
@@ -43,9 +46,6 @@ struct Fp8Args {
     dit_dtype sdt;                 // 16/32-bit type of the pack's source
     dit_dtype ddt[3];              // 16/32-bit types of the unpack's destinations
     int* range_flag;
-    const float* rope_cos;
-    const float* rope_sin;
-    unsigned rope_planes;
     long long nruns;
 };
 
@@ -55,7 +55,6 @@ struct Fp8IO {
     int nslot;        // head slots (records) of the run
     int nreal;        // slots holding real heads; later slots (and padding rows) are zero
     int dt;           // the 16/32-bit side's dit_dtype
-    int rope_pos;     // joint position whose angles rotate the run, -1 none
 };
 
 template <int MODE>
@@ -64,14 +63,12 @@ __device__ __forceinline__ Fp8IO fp8_io(const Fp8Args& A, int ri) {
     Run x;
     if (MODE == Q_PACK_S2H) x = decode_A(L, A.np, ri);
     else if (MODE == Q_PACK_H2S) x = decode_B(L, 1, ri);
-    else if (MODE == DQ_UNPACK_S2H) x = decode_H(L, A.np, ri);
     else x = decode_S(L, ri);
     const long long rec = L.D + 16;
     const bool pad_row = run_row(L, x) >= L.S;
     Fp8IO io;
     io.nslot = L.head_len[x.v];
     io.nreal = pad_row ? 0 : real_heads(L, x.v);
-    io.rope_pos = -1;
     bool second = false;
     if (MODE == Q_PACK_S2H) {
         io.dt = A.sdt;
@@ -82,12 +79,6 @@ __device__ __forceinline__ Fp8IO fp8_io(const Fp8Args& A, int ri) {
         io.dt = A.sdt;
         io.src = (const char*)A.src[0] + head_offset(L, x) * dtype_bytes(A.sdt);
         io.dst = (char*)A.dst[0] + slots_B(L, 1, x) * rec;
-    } else if (MODE == DQ_UNPACK_S2H) {
-        io.dt = A.ddt[x.p];
-        io.src = (const char*)A.src[0] + slots_B(L, A.np, x) * rec;
-        io.dst = (char*)A.dst[x.p] + head_offset(L, x) * dtype_bytes(A.ddt[x.p]);
-        // the angle tables have S rows: padding rows are not rotated
-        if (((A.rope_planes >> x.p) & 1u) && !pad_row) io.rope_pos = run_row(L, x);
     } else {
         io.dt = A.ddt[0];
         io.src = (const char*)A.src[0] + slots_A(L, 1, x) * rec;
@@ -212,9 +203,9 @@ __global__ void __launch_bounds__(kThreads, 3) fp8_pack_kernel(const __grid_cons
     pdl_trigger();
 }
 
-// Dequantizing unpack: records -> destination heads (16/32-bit), with the
-// optional RoPE rotation of the receive preparation.
-template <int MODE, int EB, bool ROPE, int EPL>
+// Dequantizing unpack, head -> seq: records -> sequence-layout heads
+// (16/32-bit, real heads only).
+template <int MODE, int EB, int EPL>
 __global__ void __launch_bounds__(kThreads, 3) fp8_unpack_kernel(const __grid_constant__ Fp8Args A, int rpw) {
     constexpr int NC = EPL / 16;             // 16-byte code vectors per lane and head
     constexpr int NU = 4;                    // heads in flight per lane
@@ -270,12 +261,6 @@ __global__ void __launch_bounds__(kThreads, 3) fp8_unpack_kernel(const __grid_co
             if (h >= io.nslot || (MODE == DQ_UNPACK_H2S && h >= io.nreal)) continue;
             const dit_dtype t = (dit_dtype)io.dt;
             char* dst = io.dst + ((long long)h * D + c * EPL) * dtype_bytes(t);
-            const float* cs = nullptr;
-            const float* sn = nullptr;
-            if (ROPE && io.rope_pos >= 0 && h < io.nreal) {     // padded heads stay +0
-                cs = A.rope_cos + (long long)io.rope_pos * (D >> 1) + c * (EPL / 2);
-                sn = A.rope_sin + (long long)io.rope_pos * (D >> 1) + c * (EPL / 2);
-            }
 #pragma unroll
             for (int v = 0; v < EPL / 8; ++v) {          // 8 values at a time
                 const uint32_t w0 = (&code[b][v >> 1].x)[(v & 1) * 2];
@@ -287,17 +272,6 @@ __global__ void __launch_bounds__(kThreads, 3) fp8_unpack_kernel(const __grid_co
                     const float2 f = from_e4m3x2((uint16_t)(w[k >> 1] >> (16 * (k & 1))));
                     y.f[2 * k] = __fmul_rn(f.x, scale[b]);
                     y.f[2 * k + 1] = __fmul_rn(f.y, scale[b]);
-                }
-                if (ROPE && cs != nullptr) {
-                    const float4 cc = reinterpret_cast<const float4*>(cs)[v];
-                    const float4 ss = reinterpret_cast<const float4*>(sn)[v];
-                    const float ca[4] = {cc.x, cc.y, cc.z, cc.w}, sa[4] = {ss.x, ss.y, ss.z, ss.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float x0 = y.f[2 * k], x1 = y.f[2 * k + 1];
-                        y.f[2 * k] = fmaf(x0, ca[k], -(x1 * sa[k]));
-                        y.f[2 * k + 1] = fmaf(x0, sa[k], x1 * ca[k]);
-                    }
                 }
                 if (EB == 4) {
                     store8(dst + v * 32, DIT_F32, y);
@@ -315,6 +289,164 @@ __global__ void __launch_bounds__(kThreads, 3) fp8_unpack_kernel(const __grid_co
     }
     if (overflow) *A.range_flag = (int)DIT_ERR_RANGE;
     pdl_trigger();
+}
+
+// ---- seq -> head decoding unpack, one head-layout row per warp -----------
+// As the three-call 16-bit unpack (direct.cu): lane v holds the record index
+// of run v's first slot less head_off[v], so head h of the row is record
+// rec(v(h)) + h; a lane takes 8 values of one head at a time (8 code bytes and
+// the record's scale), decodes, rotates when asked (angle rows staged per
+// warp) and stores them.  Same arithmetic as fp8_unpack_kernel.
+constexpr int kRowThreads = 256;
+constexpr int kRowItems = 8;
+constexpr int kRowMaxRopeD = 256;
+
+struct Fp8RowArgs {
+    dit_sp_layout L;
+    int np;
+    const char* wire;
+    char* head[3];
+    dit_dtype ddt[3];
+    int* range_flag;
+    const float* rope_cos;
+    const float* rope_sin;
+    unsigned rope_planes;
+    long long nrows;              // np * B * S_pad
+    int cpr;                      // 8-value chunks per head-layout row (Hp * D / 8)
+    int creal;                    // chunks of real heads (H * D / 8)
+    FastDiv head_of;              // chunk -> head (D / 8 chunks a head)
+    FastDiv group_of;             // head -> group when every group has Hl heads
+    int even;
+};
+
+template <int DB, bool ROPE>
+__global__ void __launch_bounds__(kRowThreads, 3) fp8_unpack_rows_kernel(const __grid_constant__ Fp8RowArgs A) {
+    __shared__ float4 tab_sm[ROPE ? kRowThreads / 32 : 1][ROPE ? kRowMaxRopeD / 4 : 1];
+    const dit_sp_layout& L = A.L;
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const long long row = (long long)blockIdx.x * (kRowThreads / 32) + wib;
+    pdl_wait();
+    if (row >= A.nrows) {
+        pdl_trigger();
+        return;
+    }
+    const long long per_plane = (long long)L.B * L.S_pad;
+    const int p = (int)(row / per_plane);
+    const long long rem = row - p * per_plane;
+    const int b = (int)(rem / L.S_pad), t = (int)(rem - (long long)b * L.S_pad);
+    Run x;
+    const int rid = rank_of_row(L, t);
+    x.r = rid / L.U;
+    x.u = rid - x.r * L.U;
+    x.p = p;
+    x.b = b;
+    x.i = t - L.rank_off[rid];
+    const long long rec = L.D + 16;
+    char* dst = A.head[p] + ((((long long)x.r * L.B + b) * L.S_cap + (t - L.ring_off[x.r])) * L.Hp) * L.D * DB;
+    long long base = 0;        // lane v: run v's first record, less head_off[v]
+    if (lane < L.U && lane < 32) {
+        x.v = lane;
+        base = slots_B(L, A.np, x) - L.head_off[lane];
+    }
+    const dit_dtype dt = A.ddt[p];
+    const bool rot = ROPE && t < L.S && ((A.rope_planes >> p) & 1u);
+    const int rlim = rot ? A.creal : 0;
+    const bool check = A.range_flag != nullptr;
+    bool overflow = false;
+    const int q4 = L.D >> 3;
+    if (ROPE && rot) {
+        const float4* ct = reinterpret_cast<const float4*>(A.rope_cos + (long long)t * (L.D >> 1));
+        const float4* sn = reinterpret_cast<const float4*>(A.rope_sin + (long long)t * (L.D >> 1));
+        for (int j = lane; j < 2 * q4; j += 32) cp_async16(&tab_sm[wib][j], j < q4 ? ct + j : sn + (j - q4));
+        cp_async_commit();
+    }
+    constexpr int NI = kRowItems;
+    for (int c0 = 0; c0 < A.cpr; c0 += 32 * NI) {
+        uint2 code[NI];
+        float scale[NI];
+#pragma unroll
+        for (int k = 0; k < NI; ++k) {
+            const int c = c0 + lane + 32 * k;
+            const int h = (int)fdiv((uint32_t)min(c, A.cpr - 1), A.head_of);
+            int v;
+            if (A.even) {
+                v = (int)fdiv((uint32_t)h, A.group_of);
+            } else {
+                int lo = 0, hi = L.U - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (L.head_off[mid] <= h) lo = mid; else hi = mid - 1;
+                }
+                v = lo;
+            }
+            long long r0;
+            if (L.U <= 32) {                                 // warp-uniform
+                r0 = __shfl_sync(0xffffffffu, base, v);
+            } else {
+                Run y = x;
+                y.v = v;
+                r0 = slots_B(L, A.np, y) - L.head_off[v];
+            }
+            code[k] = make_uint2(0, 0);
+            scale[k] = 0.f;
+            if (c < A.cpr) {
+                const char* r = A.wire + (r0 + h) * rec;
+                code[k] = *reinterpret_cast<const uint2*>(r + (c - h * q4) * 8);
+                scale[k] = *reinterpret_cast<const float*>(r + L.D);
+            }
+        }
+        if (ROPE && rot && c0 == 0) {
+            cp_async_wait_all();
+            __syncwarp();
+        }
+#pragma unroll
+        for (int k = 0; k < NI; ++k) {
+            const int c = c0 + lane + 32 * k;
+            if (c >= A.cpr) break;
+            const uint32_t w[2] = {code[k].x, code[k].y};
+            Vec8 y;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = from_e4m3x2((uint16_t)(w[e >> 1] >> (16 * (e & 1))));
+                y.f[2 * e] = __fmul_rn(f.x, scale[k]);
+                y.f[2 * e + 1] = __fmul_rn(f.y, scale[k]);
+            }
+            if (ROPE && c < rlim) {
+                const int i4 = c - (int)fdiv((uint32_t)c, A.head_of) * q4;
+                const float4 cc = tab_sm[wib][i4], ss = tab_sm[wib][q4 + i4];
+                const float ca[4] = {cc.x, cc.y, cc.z, cc.w}, sa[4] = {ss.x, ss.y, ss.z, ss.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = y.f[2 * e], x1 = y.f[2 * e + 1];
+                    y.f[2 * e] = fmaf(x0, ca[e], -(x1 * sa[e]));
+                    y.f[2 * e + 1] = fmaf(x0, sa[e], x1 * ca[e]);
+                }
+            }
+            char* d = dst + (long long)c * 8 * DB;
+            if (DB == 4) {
+                store8(d, DIT_F32, y);
+            } else {
+                if (check) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) overflow |= overflows16(y.f[e], dt);
+                }
+                *reinterpret_cast<uint4*>(d) = make_uint4(pack2(y.f[0], y.f[1], dt), pack2(y.f[2], y.f[3], dt),
+                                                          pack2(y.f[4], y.f[5], dt), pack2(y.f[6], y.f[7], dt));
+            }
+        }
+    }
+    if (ROPE && rot) __syncwarp();
+    if (overflow) *A.range_flag = (int)DIT_ERR_RANGE;
+    pdl_trigger();
+}
+
+template <int DB, bool ROPE>
+dit_status launch_rows(const Fp8RowArgs& a, cudaStream_t st, const char* who) {
+    const long long blocks = (a.nrows + kRowThreads / 32 - 1) / (kRowThreads / 32);
+    if (blocks >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: too many rows", who);
+    cudaError_t e = launch_pdl(fp8_unpack_rows_kernel<DB, ROPE>, dim3((unsigned)blocks), dim3(kRowThreads), 0, st, a);
+    if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
+    return check_launch(who);
 }
 
 template <typename K>
@@ -346,15 +478,9 @@ dit_status check_fp8_shape(const dit_sp_layout* L, const char* who, int* lg) {
 }
 
 template <int EPL>
-dit_status launch_unpack(const Fp8Args& a, dit_a2a_dir dir, bool wide, bool rope, cudaStream_t st, const char* who) {
-    if (dir == DIT_HEAD_TO_SEQ)
-        return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_H2S, 4, false, EPL>, a, st, who)
-                    : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_H2S, 2, false, EPL>, a, st, who);
-    if (rope)
-        return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 4, true, EPL>, a, st, who)
-                    : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 2, true, EPL>, a, st, who);
-    return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 4, false, EPL>, a, st, who)
-                : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_S2H, 2, false, EPL>, a, st, who);
+dit_status launch_unpack(const Fp8Args& a, bool wide, cudaStream_t st, const char* who) {
+    return wide ? launch_fp8(fp8_unpack_kernel<DQ_UNPACK_H2S, 4, EPL>, a, st, who)
+                : launch_fp8(fp8_unpack_kernel<DQ_UNPACK_H2S, 2, EPL>, a, st, who);
 }
 
 }  // namespace
@@ -395,6 +521,39 @@ dit_status fp8_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, cons
                       void* const* dst2, int split, const dit_dtype* dst_dt, const float* cos_tab,
                       const float* sin_tab, unsigned rope_planes, int* range_flag, cudaStream_t st,
                       const char* who) {
+    const int db = dtype_bytes(dst_dt[0]);
+    if (dir == DIT_SEQ_TO_HEAD) {
+        int lg;
+        dit_status s = check_fp8_shape(L, who, &lg);
+        if (s != DIT_OK) return s;
+        for (int p = 1; p < nplanes; ++p)
+            if (dtype_bytes(dst_dt[p]) != db)
+                return fail(DIT_ERR_UNSUPPORTED, "%s: planes of one call need destination types of one size", who);
+        if (L->U > 64) return fail(DIT_ERR_UNSUPPORTED, "%s: more than 64 Ulysses ranks", who);
+        Fp8RowArgs a;
+        memset(&a, 0, sizeof(a));
+        a.L = *L;
+        a.np = nplanes;
+        a.wire = static_cast<const char*>(recv);
+        for (int p = 0; p < nplanes; ++p) {
+            a.head[p] = static_cast<char*>(dst[p]);
+            a.ddt[p] = dst_dt[p];
+        }
+        a.range_flag = range_flag;
+        a.rope_cos = cos_tab;
+        a.rope_sin = sin_tab;
+        a.rope_planes = rope_planes;
+        a.nrows = (long long)nplanes * L->B * L->S_pad;
+        a.cpr = (int)(((long long)L->Hp * L->D) >> 3);
+        a.creal = (int)(((long long)L->H * L->D) >> 3);
+        a.head_of = make_fastdiv((uint32_t)(L->D >> 3));
+        a.even = 1;
+        for (int v = 0; v < L->U; ++v) a.even &= L->head_len[v] == L->Hl && L->head_off[v] == v * L->Hl;
+        a.group_of = make_fastdiv((uint32_t)(L->Hl > 0 ? L->Hl : 1));
+        if (a.nrows == 0) return DIT_OK;
+        if (rope_planes) return db == 4 ? launch_rows<4, true>(a, st, who) : launch_rows<2, true>(a, st, who);
+        return db == 4 ? launch_rows<4, false>(a, st, who) : launch_rows<2, false>(a, st, who);
+    }
     Fp8Args a;
     memset(&a, 0, sizeof(a));
     dit_status s = check_fp8_shape(L, who, &a.lg);
@@ -402,7 +561,6 @@ dit_status fp8_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, cons
     a.L = *L;
     a.np = nplanes;
     a.src[0] = recv;
-    const int db = dtype_bytes(dst_dt[0]);
     for (int p = 0; p < nplanes; ++p) {
         a.dst[p] = dst[p];
         a.dst2[p] = dst2 ? dst2[p] : nullptr;
@@ -412,12 +570,9 @@ dit_status fp8_unpack(const dit_sp_layout* L, dit_a2a_dir dir, int nplanes, cons
     }
     a.split = split;
     a.range_flag = range_flag;
-    a.rope_cos = cos_tab;
-    a.rope_sin = sin_tab;
-    a.rope_planes = rope_planes;
-    a.nruns = (long long)nplanes * L->B * L->U * (dir == DIT_SEQ_TO_HEAD ? L->S_pad : L->S);
-    if (L->D == 16) return launch_unpack<16>(a, dir, db == 4, rope_planes != 0, st, who);
-    return launch_unpack<32>(a, dir, db == 4, rope_planes != 0, st, who);
+    a.nruns = (long long)nplanes * L->B * L->U * L->S;
+    if (L->D == 16) return launch_unpack<16>(a, db == 4, st, who);
+    return launch_unpack<32>(a, db == 4, st, who);
 }
 
 }  // namespace ditsp
