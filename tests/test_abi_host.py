@@ -424,3 +424,27 @@ def test_plan_partial_type(dl):
     # the merge on the fp32 path
     assert UspPlan(1, 64, 2, 64, 2, 4, device="cpu").ring_merge == "fold"
     assert UspPlan(1, 64, 2, 64, 2, 2, device="cpu", in_dtype=torch.float32).ring_merge == "partials"
+
+
+def test_ring_rows_argument_checks(dl):
+    """dit_attn_ring_rows refuses, before any launch: a NULL row array, a
+    negative output row, and blocks whose output rows overlap in one tensor
+    (o.stride_q == 0).  (Disjoint rows are run on the GPU, in test_gpu_ring.)"""
+    from sequence_attention_gb300._lib import DitLseView, DitView
+    L = dl.lib()
+    H, D = 2, 128
+    q = DitView()
+    q.ptr, q.stride_q, q.stride_b, q.stride_s, q.stride_h = 1 << 20, 64 * H * D, 64 * H * D, H * D, D
+    o = DitView()                        # one [1, 256, H, D] tensor for both blocks
+    o.ptr, o.stride_b, o.stride_s, o.stride_h = 1 << 20, 256 * H * D, H * D, D
+    lse = DitLseView()
+    lens = (ctypes.c_int * 2)(64, 64)
+
+    def call(rows):
+        r = None if rows is None else (ctypes.c_int * 2)(*rows)
+        return L.dit_attn_ring_rows(1, H, D, 0.1, 2, lens, r, 2, lens, q, dl.DIT_BF16, q, q, dl.DIT_F16, o,
+                                    dl.DIT_BF16, lse, None, None)
+
+    assert call(None) == dl.DIT_ERR_INVALID_ARG
+    assert call([0, -1]) == dl.DIT_ERR_INVALID_ARG
+    assert call([0, 32]) == dl.DIT_ERR_INVALID_ARG       # rows 32..63 written by both blocks
