@@ -23,6 +23,9 @@
  *                                            folded in as the CTA walks them
  *   dit_attn_ring_rows                       the same, each query block's
  *                                            output placed at its own row
+ *   dit_attn_ring_merge_static               partials + merge with the
+ *                                            partials in the library's own
+ *                                            fixed device array
  *   dit_attention                            single-shot attention
  *   dit_cfg_combine                          classifier-free guidance combine
  *
@@ -97,6 +100,8 @@ typedef enum { DIT_SEQ_TO_HEAD = 0, DIT_HEAD_TO_SEQ = 1 } dit_a2a_dir;
 #define DIT_MAX_U 64
 #define DIT_MAX_R 8
 #define DIT_MAX_RANKS 64
+/* bytes of the fixed scratch array of dit_attn_ring_merge_static */
+#define DIT_RING_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
 /*
  * Rank partition of one sequence-parallel attention (edge-dit.cpp
@@ -523,6 +528,47 @@ DIT_API dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int* q
                               int n_parts, dit_view parts, dit_dtype parts_dt,
                               dit_lse_view lse_parts, dit_view out, dit_dtype out_dt,
                               dit_lse_view lse_out, void* stream);
+
+/*
+ * dit_attn_ring_merge_static: dit_attn_partial followed by
+ * dit_attn_merge_lse, with the partials (fp32) and their log-sum-exp rows
+ * held in a fixed device array of the library instead of caller memory.
+ * The pages have no counterpart of this call: it exists for callers that
+ * cannot allocate device memory, e.g. code running inside an engine or
+ * framework whose memory pool owns the whole device (a stray cudaMalloc
+ * would fail there or break the pool's accounting), or code on a
+ * latency-critical path where cudaMalloc/cudaFree would stall on an
+ * implicit device synchronisation.
+ *
+ * Arguments, types, head dims and results are those of dit_attn_ring (the
+ * same o and lse layout: query block r at o.ptr + r*o.stride_q, stride_kv
+ * ignored); the result equals the caller-buffer pair dit_attn_partial ->
+ * dit_attn_merge_lse on fp32 partials, and dit_attn_ring up to rounding.
+ *
+ * The scratch array:
+ *  - size DIT_RING_STATIC_SCRATCH_BYTES (64 MiB), aligned to 256 bytes;
+ *    every device on which the library's code is loaded holds it until the
+ *    process exits.  One call needs
+ *      P = n_q*n_kv*B*H*max_r(q_len[r])*D*4 bytes of partials, rounded up
+ *          to a multiple of 256, plus n_q*n_kv*B*H*max_r(q_len[r])*4 bytes
+ *          of log-sum-exp rows;
+ *    a call that needs more returns DIT_ERR_INVALID_ARG before touching the
+ *    device.
+ *  - the first call on a device looks up the array's device address on the
+ *    current device (cudaGetSymbolAddress) and caches it; make that first
+ *    call outside any stream capture.
+ *  - every call on a device shares the one array, and it keeps the last
+ *    call's contents.  Nothing in it needs clearing: the partial step writes
+ *    every value the merge step reads.  Calls that overlap on the GPU (on
+ *    different streams, or from several host threads without ordering)
+ *    race on it and give wrong results; order them on one stream.
+ * The call allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library routine.
+ */
+DIT_API dit_status dit_attn_ring_merge_static(int B, int H, int D, float scale, int n_q, const int* q_len,
+                                              int n_kv, const int* kv_len, dit_view q, dit_dtype qk_dt,
+                                              dit_view k, dit_view v, dit_dtype v_dt, dit_view o,
+                                              dit_dtype o_dt, dit_lse_view lse, int* d_status, void* stream);
 
 /*
  * dit_attention: single-shot attention O = softmax(scale * Q K^T) V over

@@ -36,6 +36,7 @@ __all__ = [
     "dit_cfg_combine", "dit_device_status", "library_path", "dit_sp_signal", "dit_a2a_sim_checked",
     "dit_ulysses_pack_joint", "dit_ulysses_unpack_joint", "dit_ulysses_unpack_rope", "dit_attn_varlen",
     "dit_ulysses_seq_to_head", "dit_ulysses_head_to_seq", "dit_attn_ring", "dit_attn_ring_rows",
+    "dit_attn_ring_merge_static",
 ]
 
 lib()   # load now: fail at import time, not at first call
@@ -341,6 +342,25 @@ def dit_attn_ring_rows(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
                                    _lens(kv_len, n_kv, k.shape[2]), _view(q, "q"), _dt(q),
                                    _view(k, "kv"), _view(v, "kv"), _dt(v), _view(o, "single"), _dt(o),
                                    _lse_view(lse, "out"), _ptr(status), _stream(stream)))
+
+
+def dit_attn_ring_merge_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                               lse: Optional[torch.Tensor] = None, q_len: Optional[Sequence[int]] = None,
+                               kv_len: Optional[Sequence[int]] = None, scale: Optional[float] = None,
+                               status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """dit_attn_ring's arguments and result, computed as fp32 partials and
+    their merge in the library's fixed device scratch array: the call
+    allocates no memory, for callers that cannot.  Calls that overlap on the
+    GPU share that array and race; the partials must fit
+    DIT_RING_STATIC_SCRATCH_BYTES."""
+    n_q, B, Sq, H, D = q.shape
+    n_kv = k.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    check(lib().dit_attn_ring_merge_static(B, H, D, float(scale), n_q, _lens(q_len, n_q, Sq), n_kv,
+                                           _lens(kv_len, n_kv, k.shape[2]), _view(q, "q"), _dt(q),
+                                           _view(k, "kv"), _view(v, "kv"), _dt(v), _view(o, "out"), _dt(o),
+                                           _lse_view(lse, "out"), _ptr(status), _stream(stream)))
 
 
 def dit_attn_merge_lse(parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor,

@@ -15,6 +15,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libditsp.so
 DIT_MAX_U = 64
 DIT_MAX_R = 8
 DIT_MAX_RANKS = 64
+#: bytes of the fixed device scratch array of dit_attn_ring_merge_static
+DIT_RING_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT, DIT_ERR_RANGE = range(6)
 DIT_F32, DIT_BF16, DIT_F16, DIT_E4M3 = range(4)
@@ -30,6 +32,7 @@ EXPORTS = (
     "dit_ulysses_unpack_rope", "dit_attn_varlen", "dit_ulysses_seq_to_head", "dit_ulysses_head_to_seq",
     "dit_attn_ring",
     "dit_attn_ring_rows",
+    "dit_attn_ring_merge_static",
 )
 
 
@@ -127,6 +130,10 @@ def lib() -> ctypes.CDLL:
     L.dit_attn_ring_rows.argtypes = [c_int, c_int, c_int, c_float, c_int, POINTER(c_int), POINTER(c_int), c_int,
                                      POINTER(c_int), DitView, c_int, DitView, DitView, c_int, DitView,
                                      c_int, DitLseView, c_void_p, c_void_p]
+    L.dit_attn_ring_merge_static.restype = c_int
+    L.dit_attn_ring_merge_static.argtypes = [c_int, c_int, c_int, c_float, c_int, POINTER(c_int), c_int,
+                                             POINTER(c_int), DitView, c_int, DitView, DitView, c_int, DitView,
+                                             c_int, DitLseView, c_void_p, c_void_p]
     L.dit_attn_varlen.restype = c_int
     L.dit_attn_varlen.argtypes = [c_int, c_int, c_float, c_int, POINTER(c_int), POINTER(c_int), DitView, c_int,
                                   DitView, DitView, c_int, DitView, c_int, DitLseView, c_void_p, c_void_p]
