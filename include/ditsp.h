@@ -37,7 +37,9 @@
  *
  * Conventions shared by every call
  *  - Ownership: the caller allocates and owns every buffer.  The library
- *    allocates no device or host memory in any call.
+ *    allocates no device or host memory in any call.  Its one piece of
+ *    device memory is the fixed scratch array of dit_attn_ring_merge_static,
+ *    part of its device code (DIT_RING_STATIC_SCRATCH_BYTES per device).
  *  - Asynchrony: every call that takes `stream` (a cudaStream_t passed as
  *    void*, NULL = legacy default stream) validates its arguments on the
  *    host, enqueues its kernels on that stream and returns without waiting.
