@@ -60,18 +60,31 @@ extern "C" dit_status dit_attn_ring_merge_static(int B, int H, int D, float scal
         if (q_len[r] < 0) return fail(DIT_ERR_INVALID_ARG, "%s: negative query length", who);
         maxq = q_len[r] > maxq ? q_len[r] : maxq;
     }
+    // No query rows: dit_attn_ring checks the other arguments and launches
+    // nothing (its buffers may be NULL).
+    if (maxq == 0)
+        return dit_attn_ring(B, H, D, scale, n_q, q_len, n_kv, kv_len, q, qk_dt, k, v, v_dt, o, o_dt, lse, d_status,
+                             stream);
     // fp32 partials [n_q][n_kv][B][maxq][H][D], then fp32 lse rows
-    // [n_q][n_kv][B][H][maxq] from the next 256-byte boundary
-    const unsigned long long rows = (unsigned long long)n_q * n_kv * B * H * (unsigned long long)maxq;
-    const unsigned long long part_bytes = rows * (unsigned long long)D * 4ull;
+    // [n_q][n_kv][B][H][maxq] from the next 256-byte boundary.  The size is
+    // built factor by factor against the limit, so no product can wrap.
+    const unsigned long long cap = DIT_RING_STATIC_SCRATCH_BYTES;
+    const unsigned long long factors[6] = {(unsigned long long)n_q, (unsigned long long)n_kv, (unsigned long long)B,
+                                           (unsigned long long)H, (unsigned long long)maxq, 4ull * (unsigned long long)D};
+    unsigned long long part_bytes = 1;
+    bool fits = true;
+    for (int f = 0; f < 6 && fits; ++f) {
+        fits = part_bytes <= cap / factors[f];
+        part_bytes *= fits ? factors[f] : 1ull;
+    }
+    const unsigned long long rows = fits ? part_bytes / factors[5] : 0;
     const unsigned long long lse_off = (part_bytes + 255ull) & ~255ull;
-    const unsigned long long need = lse_off + rows * 4ull;
-    if (need > (unsigned long long)DIT_RING_STATIC_SCRATCH_BYTES)
+    if (!fits || lse_off + rows * 4ull > cap)
         return fail(DIT_ERR_INVALID_ARG,
-                    "%s: the partials need %llu bytes of scratch; the library's fixed scratch holds %llu "
-                    "(use dit_attn_partial + dit_attn_merge_lse with caller buffers, or dit_attn_ring)",
-                    who, need, (unsigned long long)DIT_RING_STATIC_SCRATCH_BYTES);
-    if (maxq == 0) return DIT_OK;
+                    "%s: the partials of %d x %d blocks, B=%d, H=%d, %d rows, D=%d do not fit the library's fixed "
+                    "scratch of %llu bytes (use dit_attn_partial + dit_attn_merge_lse with caller buffers, or "
+                    "dit_attn_ring)",
+                    who, n_q, n_kv, B, H, maxq, D, cap);
 
     unsigned char* base = nullptr;
     dit_status s = scratch_address(&base, who);

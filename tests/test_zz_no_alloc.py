@@ -84,19 +84,41 @@ def test_static_scratch_matches_caller_buffers_twice():
         _check(out, fold, lse, lse_fold, q_lens, f"folded ring, B={B} H={H} D={D}")
 
 
-def test_static_scratch_rejects_a_request_beyond_its_size():
-    """FLUX-sized blocks (2 x 4608 rows, 24 heads, D = 128) need about 218 MiB
-    of partials: refused with DIT_ERR_INVALID_ARG before any device work (no
-    GPU needed)."""
+def _call_host_only(B, H, D, q_lens, kv_lens):
+    """Call the entry point with NULL tensors; only host-side checks run."""
     from ctypes import c_int
 
     from sequence_attention_gb300 import _lib
     L = _lib.lib()
-    need = 2 * 2 * 24 * 4608 * (128 * 4 + 4)
-    assert need > _lib.DIT_RING_STATIC_SCRATCH_BYTES
-    lens = (c_int * 2)(4608, 4608)
+    ql, kl = (c_int * len(q_lens))(*q_lens), (c_int * len(kv_lens))(*kv_lens)
     view, lse = _lib.DitView(), _lib.DitLseView()
-    st = L.dit_attn_ring_merge_static(1, 24, 128, 0.088, 2, lens, 2, lens, view, _lib.DIT_BF16, view, view,
-                                      _lib.DIT_F16, view, _lib.DIT_BF16, lse, None, None)
+    view.stride_s, view.stride_h = H * D, D                # [blocks][B][rows][H][D] rows of empty tensors
+    st = L.dit_attn_ring_merge_static(B, H, D, 0.088, len(q_lens), ql, len(kv_lens), kl, view, _lib.DIT_BF16,
+                                      view, view, _lib.DIT_F16, view, _lib.DIT_BF16, lse, None, None)
+    return st, L.dit_last_error()
+
+
+@pytest.mark.parametrize("B,H,D,q_lens", [
+    (1, 24, 128, [4608, 4608]),              # FLUX-sized blocks: about 218 MiB of partials
+    (1 << 30, 1 << 30, 128, [1 << 30] * 8),  # a size whose byte count would wrap 64 bits
+    (1, 1, 1 << 30, [1 << 30]),
+])
+def test_static_scratch_rejects_a_request_beyond_its_size(B, H, D, q_lens):
+    """Refused with DIT_ERR_INVALID_ARG before any device work (no GPU
+    needed)."""
+    from sequence_attention_gb300 import _lib
+    rows = len(q_lens) * len(q_lens) * B * H * max(q_lens)
+    assert rows * (4 * D + 4) > _lib.DIT_RING_STATIC_SCRATCH_BYTES
+    st, msg = _call_host_only(B, H, D, q_lens, q_lens)
     assert st == _lib.DIT_ERR_INVALID_ARG
-    assert b"scratch" in L.dit_last_error()
+    assert b"fixed scratch" in msg
+
+
+def test_static_scratch_no_query_rows_is_a_no_op():
+    """No query rows: the other arguments are checked, nothing is launched,
+    and the NULL buffers of zero-size tensors are accepted."""
+    from sequence_attention_gb300 import _lib
+    st, _ = _call_host_only(1, 24, 128, [0, 0], [4608, 4608])
+    assert st == _lib.DIT_OK
+    st, msg = _call_host_only(1, 24, 96, [0, 0], [4608, 4608])     # an unsupported head dim is still refused
+    assert st == _lib.DIT_ERR_UNSUPPORTED, msg
