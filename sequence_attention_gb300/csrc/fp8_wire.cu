@@ -456,9 +456,17 @@ dit_status launch_fp8(K kernel, const Fp8Args& a, cudaStream_t st, const char* w
     // 16 runs per warp (128 per block): measured against 1, 2, 4 and 8 on the
     // FLUX- and Wan-like shapes, the fastest at the Wan size (fewer runs per
     // block pay the per-block decode of run offsets more often).  When 16
-    // would leave fewer than 3 blocks per SM (the FLUX-like exchange), 8
-    // runs per warp: pack 4.61 against 4.45 TB/s, unpack 4.03 against 3.85.
-    const int rpw = (a.nruns + 127) / 128 < 3LL * num_sms() ? 8 : 16;
+    // would leave less than one wave of blocks (3 per SM), the fewest runs
+    // per warp from 8 up whose grid fills at most 90 % of one wave: a grid
+    // just over one wave leaves a tail of blocks that waits for the first
+    // wave to drain.  FLUX-like Q and V pack (36,864 runs, 456 resident
+    // blocks): 12 runs per warp, 384 blocks, 17.9 us; 8 (576 blocks) 19.2,
+    // 10 (461) 22.3, 11 (419) 18.2, 16 (288) 19.9.
+    const long long cap = 3LL * num_sms();
+    int rpw = 16;
+    if ((a.nruns + 127) / 128 < cap)
+        for (rpw = 8; rpw < 16 && (a.nruns + 8LL * rpw - 1) / (8LL * rpw) > cap * 9 / 10; ++rpw) {
+        }
     const long long blocks = (a.nruns + 8LL * rpw - 1) / (8LL * rpw);
     cudaError_t e = launch_pdl(kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, a, rpw);
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
