@@ -113,8 +113,11 @@ __device__ __forceinline__ RowIO row_io(const DirectArgs& A, long long row) {
     return io;
 }
 
-template <bool S2H, int SB, int DB, bool ROPE>
-__global__ void __launch_bounds__(kDirThreads, (ROPE || SB == 2) ? 3 : 1) direct_kernel(const __grid_constant__ DirectArgs A) {
+// OCC4: a 64-register build (4 blocks per SM) of the 16-bit head -> seq
+// pass, for grids between one wave of 3 and one wave of 4 blocks per SM.
+template <bool S2H, int SB, int DB, bool ROPE, bool OCC4 = false>
+__global__ void __launch_bounds__(kDirThreads, OCC4 ? 4 : ((ROPE || SB == 2) ? 3 : 1))
+    direct_kernel(const __grid_constant__ DirectArgs A) {
     // rotary path: the token's cosine row then sine row (D/2 floats each),
     // staged per warp while the row's first data loads are in flight
     __shared__ float4 tab_sm[ROPE ? kDirThreads / 32 : 1][ROPE ? kDirMaxRopeD / 4 : 1];
@@ -193,7 +196,20 @@ dit_status launch_direct_sized(DirectArgs& a, cudaStream_t st, const char* who) 
     a.share = 1;
     const long long blocks = (a.nrows + kDirThreads / 32 - 1) / (kDirThreads / 32);
     if (blocks >= (1LL << 31)) return fail(DIT_ERR_UNSUPPORTED, "%s: too many rows", who);
-    cudaError_t e = launch_pdl(direct_kernel<S2H, SB, DB, ROPE>, dim3((unsigned)blocks), dim3(kDirThreads), 0, st, a);
+    cudaError_t e;
+    // A 16-bit head -> seq grid just over one wave of 3 blocks per SM runs
+    // in one wave of the 4-blocks-per-SM build (FLUX-like output, 576
+    // blocks: 10.57 against 10.86 us back to back, same bits); over many
+    // waves the 3-block build is faster (Wan-like: 223.4 against 226.2 us).
+    if constexpr (!S2H && SB == 2 && !ROPE) {
+        const long long nsm = num_sms();
+        if (blocks > 3 * nsm && blocks <= 4 * nsm)
+            e = launch_pdl(direct_kernel<S2H, SB, DB, ROPE, true>, dim3((unsigned)blocks), dim3(kDirThreads), 0, st, a);
+        else
+            e = launch_pdl(direct_kernel<S2H, SB, DB, ROPE>, dim3((unsigned)blocks), dim3(kDirThreads), 0, st, a);
+    } else {
+        e = launch_pdl(direct_kernel<S2H, SB, DB, ROPE>, dim3((unsigned)blocks), dim3(kDirThreads), 0, st, a);
+    }
     if (e != cudaSuccess) return fail(DIT_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
     return check_launch(who);
 }
