@@ -560,7 +560,7 @@ DIT_API dit_status dit_attn_merge_lse(int B, int H, int D, int n_q, const int* q
  *    current device (cudaGetSymbolAddress) and caches it for the life of the
  *    process (like the library's status word); make that first call outside
  *    any stream capture, and make no call after a cudaDeviceReset of that
- *    device, whose new context places the array elsewhere.
+ *    device, whose new context may place the array elsewhere.
  *  - every call on a device shares the one array, and it keeps the last
  *    call's contents.  Nothing in it needs clearing: the partial step writes
  *    every value the merge step reads.  Calls that overlap on the GPU (on
