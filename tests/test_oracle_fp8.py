@@ -117,3 +117,31 @@ def test_exchange_in_the_unpadded_and_lcm_padded_layouts():
             h0, h1 = L.head_off[v], min(L.head_off[v] + L.head_len[v], H)
             np.testing.assert_array_equal(got[:, :m, :h1 - h0], want[:, L.ring_off[r]:L.ring_off[r] + m, h0:h1])
             assert np.all(got[:, m:] == 0) and np.all(got[:, :, h1 - h0:] == 0)
+
+
+def test_float32_step_order_agrees_with_the_exact_scale():
+    """The pages fix no e4m3 format; the oracle reads it as float32 steps
+    (amax, s = amax / 448, r = 1 / s, y = x * r, then the code).  Against the
+    exact scale (y = x * 448 / amax in float64, then the same rounding) the
+    codes agree, except where the exact y lies within a few float32 ulps of a
+    midpoint between two codes; there they differ by one step."""
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal((1024, 8, 128)) * np.exp2(rng.integers(-12, 12, (1024, 8, 1)))).astype(np.float32)
+    codes, _ = fp8.quantize_heads(x)
+    amax = np.abs(x.astype(np.float64)).max(axis=-1, keepdims=True)
+    y = x.astype(np.float64) * (448.0 / amax)
+    exact = fp8.e4m3_encode(y)
+    diff = codes != exact
+    assert diff.mean() <= 1e-4
+    if diff.any():
+        a, b = codes[diff], exact[diff]
+        assert np.all((a >> 7) == (b >> 7))                      # same sign
+        assert np.all(np.abs((a & 0x7F).astype(int) - (b & 0x7F).astype(int)) == 1)
+        lo = np.minimum(fp8.e4m3_value(a & 0x7F), fp8.e4m3_value(b & 0x7F))
+        hi = np.maximum(fp8.e4m3_value(a & 0x7F), fp8.e4m3_value(b & 0x7F))
+        mid = (lo + hi) / 2
+        assert np.all(np.abs(np.abs(y[diff]) - mid) <= 4 * 2.0 ** -23 * mid)
+    # each non-zero head's largest magnitude is exactly 448 on both sides
+    k = np.argmax(np.abs(x), axis=-1)[..., None]
+    assert np.all((np.take_along_axis(codes, k, -1) & 0x7F) == 0x7E)
+    assert np.all((np.take_along_axis(exact, k, -1) & 0x7F) == 0x7E)
